@@ -1,0 +1,436 @@
+#!/usr/bin/env python
+"""Decode benchmark: Qwen3-8B-shaped q4_0 model, batch 1, 2048-token context, greedy steps.
+
+One "step" is one whole decode step (embed, 36 layers of RMSNorm / q4_0 qkv GEMV / qk-norm +
+RoPE + paged KV append / split-K paged GQA attention / o GEMV + residual / RMSNorm / gate|up
+GEMV + SiLU*up / down GEMV + residual, final RMSNorm, lm_head GEMV + greedy argmax, position
+advance) for every sequence of the batch, replayed as one CUDA graph.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ql|reference] [--config e1|e32]
+
+Prints one JSON line. ``--impl reference`` times the f64 CPU oracle on the host cores on a
+bounded sample of the same workload. Under torchrun each rank runs an independent replica
+(the decode step does not shard) and rank 0 reports the aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import ql_inputs  # noqa: E402
+
+METRIC = "decode tokens/s at 1 GB300; q4_0 GEMV + paged attn achieved HBM GB/s vs peak"
+CTX = 2048
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ----------------------------------------------------------------------------- distributed
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value: float, world: int) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.path = tempfile.mktemp(suffix=".csv")
+        self.proc = None
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def device_tensor_fn(cfg, seed: int):
+    """Seeded device-side weight draws with the pages' distributions (N(0,0.02) matrices,
+    1 + N(0,0.1) norm weights, N(0,0.02) f32 embedding)."""
+    import torch
+
+    names = ("attn_norm", "ffn_norm", "q_norm", "k_norm", "wqkv", "wo", "wgu", "wd")
+    shapes = {"attn_norm": (cfg.hidden,), "ffn_norm": (cfg.hidden,), "q_norm": (cfg.head_dim,),
+              "k_norm": (cfg.head_dim,), "wqkv": (cfg.qkv_rows, cfg.hidden),
+              "wo": (cfg.hidden, cfg.n_heads * cfg.head_dim), "wgu": (2 * cfg.intermediate, cfg.hidden),
+              "wd": (cfg.hidden, cfg.intermediate), "embed": (cfg.vocab, cfg.hidden),
+              "final_norm": (cfg.hidden,), "lm_head": (cfg.vocab, cfg.hidden)}
+
+    def fn(layer, name):
+        key = (seed * 1000003 + (0 if layer is None else layer + 1) * 101 + (names.index(name) if name in names else 50 + len(name))) & 0x7FFFFFFF
+        g = torch.Generator(device="cuda")
+        g.manual_seed(key)
+        t = torch.randn(shapes[name], generator=g, device="cuda", dtype=torch.float32)
+        if name.endswith("norm"):
+            return t.mul_(0.1).add_(1.0)
+        return t.mul_(0.02)
+    return fn
+
+
+def gpu_arm(args, rank, world, local_rank):
+    import torch
+
+    from quantized_transformer_decode_ql_gb300 import build as qbuild
+    if rank == 0 or world == 1:
+        qbuild.build()
+    barrier(world)
+    import quantized_transformer_decode_ql_gb300 as ql
+    from quantized_transformer_decode_ql_gb300.model import DeviceModel
+
+    torch.cuda.set_device(local_rank)
+    cfg = ql_inputs.QWEN3_8B
+    B = 1 if args.config == "e1" else 32
+    steps, warmup = args.steps, args.warmup
+    max_ctx = CTX + warmup + steps + 2
+    maxb = (max_ctx + 15) // 16
+    num_blocks = B * maxb + 8
+    t_setup = time.time()
+    gm = DeviceModel.from_layer_fn(cfg, device_tensor_fn(cfg, seed=0), num_blocks=num_blocks,
+                                   max_batch=B, max_blocks_per_seq=maxb)
+    # fragmented block tables; pre-filled synthetic context of CTX positions N(0,1) f16 per slot
+    perm = torch.from_numpy(ql_inputs.fragmented_block_ids(num_blocks, seed=5)).cuda()
+    bt = perm[: B * maxb].reshape(B, maxb).contiguous()
+    g = torch.Generator(device="cuda")
+    g.manual_seed(4)
+    nctx_blocks = CTX // 16
+    for b in range(B):
+        ids = bt[b, :nctx_blocks].long()
+        gm.k_pool[:, ids] = torch.randn((cfg.n_layers, nctx_blocks, cfg.n_kv_heads, 16, cfg.head_dim),
+                                        generator=g, device="cuda").half()
+        gm.v_pool[:, ids] = torch.randn((cfg.n_layers, nctx_blocks, cfg.n_kv_heads, 16, cfg.head_dim),
+                                        generator=g, device="cuda").half()
+    first = torch.from_numpy(ql_inputs.prompt_tokens(B, cfg.vocab, seed=1)).cuda()
+    tokens = first.clone()
+    positions = torch.full((B,), CTX, dtype=torch.int32, device="cuda")
+    out_tokens = torch.full((B, max_ctx + 1), -1, dtype=torch.int32, device="cuda")
+    sargs = gm.step_args(tokens, positions, bt, tokens, out_tokens=out_tokens)
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    gm.ql_decode_graph_capture(sargs, s)
+    setup_s = time.time() - t_setup
+
+    def reset():
+        tokens.copy_(first)
+        positions.fill_(CTX)
+
+    # warm-up (untimed), then reset to the same starting state
+    with torch.cuda.stream(s):
+        reset()
+        gm.ql_decode_graph_replay(B, warmup, s)
+        reset()
+    s.synchronize()
+    gm.ql_check_device_error()
+
+    # ---- timed region: K graph replays, device-timed with events on the launching stream
+    clock = ClockSampler(local_rank)
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        e0.record(s)
+        gm.ql_decode_graph_replay(B, steps, s)
+        e1.record(s)
+    s.synchronize()
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = clock.stop()
+    ms = e0.elapsed_time(e1)
+    ms_max = max_over_ranks(ms, world)
+    gm.ql_check_device_error()
+    toks = out_tokens.cpu().numpy()
+
+    # ---- algorithmic bytes per step (weights + KV read/write + embedding row + logits)
+    wbytes = gm.weight_bytes()
+    kv_tok = cfg.n_layers * 2 * cfg.n_kv_heads * cfg.head_dim * 2
+    ctx_avg = CTX + 1 + (steps - 1) / 2.0
+    step_bytes = wbytes + B * (kv_tok * ctx_avg + kv_tok + cfg.hidden * 4 + cfg.vocab * 4)
+
+    # ---- dominant kernel: the gate|up q4_0 GEMV (SiLU*up epilogue), over the 36 layers'
+    # own matrices in turn (every launch streams a fresh 56.6 MB matrix: no L2 reuse)
+    x16 = torch.randn((B, cfg.hidden), generator=g, device="cuda").half()
+    act = torch.empty((B, cfg.intermediate), dtype=torch.float16, device="cuda")
+    reps = 3
+
+    def gu_all():
+        for L in gm.layers:
+            W = L["wgu"]
+            ql.ql_gemv_q4_0(W.scales, W.quants, W.rows, W.cols, x16, B, act, ql.QL_DTYPE_F16,
+                            ql.QL_EPI_SILU_MUL, None, s)
+    with torch.cuda.stream(s):
+        gu_all()
+        k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        k0.record(s)
+        for _ in range(reps):
+            gu_all()
+        k1.record(s)
+    s.synchronize()
+    gu_launches = reps * cfg.n_layers
+    gu_ms = k0.elapsed_time(k1) / gu_launches
+    W = gm.layers[0]["wgu"]
+    gu_bytes = W.nbytes() + B * cfg.hidden * 2 + B * cfg.intermediate * 2
+
+    # ---- attention alone at this workload (context CTX + steps/2), 36 layers' pools in turn
+    at_ctx = torch.full((B,), int(ctx_avg), dtype=torch.int32, device="cuda")
+    qa = torch.randn((B, cfg.n_heads, cfg.head_dim), generator=g, device="cuda").half()
+    oa = torch.empty((B, cfg.n_heads * cfg.head_dim), dtype=torch.float16, device="cuda")
+    wsb = ql.ql_paged_attn_workspace_bytes(B, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim, 16, maxb)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
+
+    def attn_all():
+        for li in range(cfg.n_layers):
+            ql.ql_paged_attn_decode(qa, gm.k_pool[li], gm.v_pool[li], bt, at_ctx, B, cfg.n_heads,
+                                    cfg.n_kv_heads, cfg.head_dim, 16, maxb, num_blocks,
+                                    1.0 / math.sqrt(cfg.head_dim), oa, ws, s)
+    with torch.cuda.stream(s):
+        attn_all()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(s)
+        for _ in range(reps):
+            attn_all()
+        a1.record(s)
+    s.synchronize()
+    at_ms = a0.elapsed_time(a1) / (reps * cfg.n_layers)
+    L = int(ctx_avg)
+    at_bytes = B * (2 * L * cfg.n_kv_heads * cfg.head_dim * 2 + 4 * ((L + 15) // 16)) + B * cfg.n_heads * cfg.head_dim * 4
+
+    # ---- end to end through the public API with host buffers: per step, H2D of the step's
+    # token ids from pinned memory, one graph replay, D2H of the next tokens, host sync
+    h_tok = torch.empty((B,), dtype=torch.int32, pin_memory=True)
+    h_out = torch.empty((B,), dtype=torch.int32, pin_memory=True)
+    h_tok.copy_(first.cpu())
+    with torch.cuda.stream(s):
+        positions.fill_(CTX)
+    s.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        with torch.cuda.stream(s):
+            tokens.copy_(h_tok, non_blocking=True)
+            gm.ql_decode_graph_replay(B, 1, s)
+            h_out.copy_(tokens, non_blocking=True)
+        s.synchronize()
+        h_tok.copy_(h_out)
+    e2e_s = time.perf_counter() - t0
+    e2e_s = max_over_ranks(e2e_s, world)
+
+    peak, peak_src = load_peaks()
+    tok_total = sum_over_ranks(float(B * steps), world)
+    value = tok_total / (ms_max / 1e3)
+    per_kernel = {
+        "gemv_gate_up": {"achieved_gbs": gu_bytes / (gu_ms / 1e3) / 1e9, "us_per_launch": gu_ms * 1e3,
+                         "bytes_per_launch": gu_bytes, "launches": gu_launches},
+        "paged_attention": {"achieved_gbs": at_bytes / (at_ms / 1e3) / 1e9, "us_per_launch": at_ms * 1e3,
+                            "bytes_per_launch": at_bytes, "context": L},
+    }
+    gu_gbs = per_kernel["gemv_gate_up"]["achieved_gbs"]
+    step_gbs = step_bytes * steps / (ms_max / 1e3) / 1e9
+    kernels_per_step = 2 + 6 * cfg.n_layers + 2
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world,
+        "steps": steps, "warmup": warmup, "ms_per_step": round(ms_max / steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "q4_0 weights, f16 act/KV, f32 accum",
+        "data": "synthetic (seeded random-init weights, N(0,1) f16 KV context, random prompt token)",
+        "config": {"workload": f"qwen3-8b-shaped q4_0 decode, batch {B}, {CTX}-token context, {steps} greedy steps",
+                   "hidden": cfg.hidden, "layers": cfg.n_layers, "heads": f"{cfg.n_heads}/{cfg.n_kv_heads}",
+                   "head_dim": cfg.head_dim, "intermediate": cfg.intermediate, "vocab": cfg.vocab,
+                   "batch": B, "context": CTX, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (%.2f GB of q4_0 weights streamed per step)" % (wbytes / 1e9)},
+        "roofline": {"bound": "hbm", "kernel": "q4_0 GEMV (gate|up, SiLU*up epilogue, batch %d)" % B,
+                     "achieved": round(gu_gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(gu_gbs / peak, 4), "traffic": None, "peak_source": peak_src},
+        "step_roofline": {"bytes_per_step": int(step_bytes), "achieved_gbs": round(step_gbs, 1),
+                          "frac": round(step_gbs / peak, 4),
+                          "roofline_tokens_s": round(B * peak * 1e9 / step_bytes, 1)},
+        "kernels": per_kernel,
+        "clocks": clocks,
+        "e2e": {"value": round(tok_total / e2e_s, 2), "unit": "tokens/s", "h2d_bytes_per_step": 4 * B,
+                "d2h_bytes_per_step": 4 * B},
+        "gpu_launches": kernels_per_step * steps,
+        "setup_s": round(setup_s, 1),
+        "tokens_head": toks[0, CTX + 1: CTX + 9].tolist(),
+    }
+    return line
+
+
+# ----------------------------------------------------------------------------- CPU oracle arm
+def oracle_sample(budget_s: float = 20.0):
+    """Time the f64 oracle on a bounded sample of the batch-1 8B-shaped decode: one full decode
+    step of layer 0 (attention over a 2048-position f16 context) and the lm_head on a slice of
+    rows, then scale to one token (36 layers + the whole vocabulary). Returns (tokens/s, info)."""
+    from oracle import decode, ops
+
+    cfg = ql_inputs.QWEN3_8B
+    lm_rows = 8192
+    one = ql_inputs.Config(**{**cfg.as_dict(), "n_layers": 1, "vocab": lm_rows})
+    w = {"embed": ql_inputs._normal(ql_inputs.sub_rng(0, 0, 0), (lm_rows, cfg.hidden), 0.02),
+         "final_norm": ql_inputs.layer_tensor(cfg, 0, 0, "attn_norm"),
+         "lm_head": ql_inputs.gemv_weight(lm_rows, cfg.hidden, seed=2),
+         "layers": [{n: ql_inputs.layer_tensor(cfg, 0, 0, n) for n in
+                     ("attn_norm", "ffn_norm", "q_norm", "k_norm", "wqkv", "wo", "wgu", "wd")}]}
+    model = decode.Q4Model(one, w)
+    k, v = ql_inputs.kv_context(1, cfg.n_kv_heads, cfg.head_dim, CTX, seed=4)
+    cache = decode.KVCache(one, 1, CTX + 64)
+    cache.preload(0, k, v)
+    hf = np.random.default_rng(0).standard_normal((1, cfg.hidden))
+    t_layer, t_lm, n = [], [], 0
+    t_start = time.perf_counter()
+    while True:
+        t0 = time.perf_counter()
+        decode.decode_step(model, cache, [1], [CTX + n])          # layer 0 + lm_head slice
+        t1 = time.perf_counter()
+        ops.gemv(model.dense(model.lm_head), hf)                   # the lm_head slice alone
+        t2 = time.perf_counter()
+        t_layer.append((t1 - t0) - (t2 - t1))
+        t_lm.append(t2 - t1)
+        n += 1
+        if time.perf_counter() - t_start > budget_s or n >= 8:
+            break
+    tl, tm = statistics.median(t_layer), statistics.median(t_lm)
+    t_token = cfg.n_layers * tl + tm * (cfg.vocab / lm_rows)
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    info = {"kind": "oracle", "cores": cores,
+            "sample": (f"{n} oracle decode steps of layer 0 (2048-position f16 context) + lm_head on "
+                       f"{lm_rows} of {cfg.vocab} rows, scaled to 36 layers + full vocab; "
+                       f"{tl:.2f} s/layer, {tm:.2f} s per lm_head slice"),
+            "s_per_token": t_token}
+    return 1.0 / t_token, info
+
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return None
+    budget = max(10.0, min(120.0, 6.0 * (args.steps + args.warmup)))
+    tps, info = oracle_sample(budget_s=budget)
+    cpu = {"value": round(tps, 6), "unit": "tokens/s", "cores": info["cores"], "kind": "oracle",
+           "sample": info["sample"]}
+    return {
+        "metric": METRIC, "value": round(tps, 6), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 / tps, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": f"qwen3-8b-shaped q4_0 decode, batch 1, {CTX}-token context, {args.steps} greedy steps"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(tps, 6), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=256)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ql", choices=["ql", "reference"])
+    ap.add_argument("--config", default="e1", choices=["e1"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        if args.impl == "reference":
+            if rank != 0:
+                return
+        else:
+            torch.cuda.set_device(local_rank)
+            dist.init_process_group("nccl")
+    if args.impl == "reference":
+        line = reference_arm(args, rank, 1 if rank == 0 else world)
+        if line is not None:
+            line["n_gpus"] = args.gpus
+            print(json.dumps(line), flush=True)
+        return
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+    line = gpu_arm(args, rank, world, local_rank)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            tps, info = oracle_sample(budget_s=20.0)
+            line["cpu_baseline"] = {"value": round(tps, 6), "unit": "tokens/s", "cores": info["cores"],
+                                    "kind": "oracle", "sample": info["sample"]}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,237 @@
+/*
+ * libql - single-token decode of a dense Qwen3-style transformer with q4_0 weights and a
+ * paged f16 KV cache, on one NVIDIA GB300 (sm_103a).
+ *
+ * C ABI. Every entry point returns an int status (QL_OK = 0 or a negative QL_E* code) and
+ * never throws. On failure ql_last_error() returns a thread-local message.
+ *
+ * Memory: every pointer named d_* is a DEVICE pointer owned by the caller; h_* / plain
+ * pointers in the codec are HOST pointers. The library never frees caller memory. A model
+ * handle owns only its own workspace (activation scratch, RoPE tables, attention partials,
+ * captured graphs) and frees it in ql_model_destroy. Caller buffers must stay alive while any
+ * call, handle or captured graph that references them may still run.
+ *
+ * Streams: kernel entry points are asynchronous on the given stream (a cudaStream_t passed as
+ * void*, NULL = the legacy default stream). A returned QL_OK means the arguments validated and
+ * the kernels were enqueued. Out-of-range indices found ON THE DEVICE (a block id outside the
+ * pool, a position past the block table, a token outside the vocabulary) do not fault: the
+ * kernel skips the access and records the first such event in a per-device error record that
+ * ql_check_device_error() reads (it synchronizes the device).
+ *
+ * The first call on a device allocates that device's error record with cudaMalloc; make it
+ * outside any stream capture (ql_model_create does it).
+ *
+ * Sources (public web pages; cited by page and item):
+ *   [IL]  inferencelayer, src/cuda_llm.rs        - Q4Dev, CudaQwen3::{gemv, rms_add, step,
+ *                                                   capture, run_graph}, rope_inv_freq
+ *   [FK]  ferrum-kernels, backend/cuda/cuda_decode.rs - launch_paged_decode_attention,
+ *                                                   attention_paged, alloc_block,
+ *                                                   decode_step, batch_decode_step
+ *   [ME]  memra-engine, qwen4exp_gpu.rs          - host_rms_norm, host_rope_at
+ */
+#ifndef QL_H
+#define QL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------- status codes */
+enum {
+    QL_OK = 0,
+    QL_EINVAL = -1,  /* bad argument (null pointer, bad shape, unsupported size)            */
+    QL_ENOMEM = -2,  /* the library could not allocate its own workspace                     */
+    QL_ECUDA = -3,   /* a CUDA launch or runtime call failed (message in ql_last_error)     */
+    QL_EPOOL = -4,   /* KV block pool exhausted ([FK] alloc_block)                           */
+    QL_ERANGE = -5,  /* an index is out of range (host-side check)                           */
+    QL_EDEVICE = -6, /* a kernel recorded an out-of-range index (see ql_check_device_error) */
+    QL_ESTATE = -7   /* call out of order, e.g. a graph replay before its capture            */
+};
+
+enum { QL_DTYPE_F32 = 0, QL_DTYPE_F16 = 1 };
+
+/* GEMV epilogues */
+enum {
+    QL_EPI_NONE = 0,         /* y = W x                                                      */
+    QL_EPI_ADD_RESIDUAL = 1, /* y = residual + W x (f32; y may be the residual buffer itself) */
+    QL_EPI_SILU_MUL = 2      /* W = [gate | up] rows; y[b][i] = silu(g_i) * u_i, i < rows/2   */
+};
+
+const char* ql_status_str(int status);
+const char* ql_last_error(void);
+int ql_version(void);
+
+/* --------------------------------------------------------------- q4_0 codec (host)
+ * [IL] Q4Dev: a [rows, cols] matrix in 32-weight blocks; one f16 scale d and 16 bytes of
+ * 4-bit codes q per block; weight = (q - 8) * d. Scales and codes are separate arrays,
+ * row-major: scales [rows][cols/32] (f16 bit patterns), quants [rows][cols/32][16].
+ * Byte j of a block holds element j in its low nibble and element j+16 in its high nibble.
+ * Quantiser (the page does not print one; this is the rule the library fixes):
+ *   d = nearest f16 (ties to even) of max|x|/7, computed in f64;
+ *   q = clamp(round_half_even(x/d), -7, 7) + 8 in f64; a block with d == 0 gets q = 8.
+ * For blocks with a normal f16 scale this gives |x - (q-8) d| <= d/2 for every weight.
+ * Returns QL_EINVAL if cols % 32 != 0, a pointer is NULL, a weight is not finite or a block
+ * scale overflows f16. Deterministic; uses several host threads for large matrices.      */
+int ql_q4_0_pack(const float* w, int64_t rows, int64_t cols, uint16_t* scales,
+                 uint8_t* quants);
+/* w[r][32j+e] = (q - 8) * d, exactly (f32 holds every such product). */
+int ql_q4_0_unpack(const uint16_t* scales, const uint8_t* quants, int64_t rows,
+                   int64_t cols, float* w);
+/* The same quantiser on the GPU (bit-identical to ql_q4_0_pack): d_w f32 [rows][cols] ->
+ * d_scales, d_quants. A non-finite weight or an f16 overflow of a scale is recorded in the
+ * device error record (that block is written as d = 0, q = 8). Asynchronous on stream.   */
+int ql_q4_0_pack_device(const float* d_w, int64_t rows, int64_t cols, void* d_scales,
+                        void* d_quants, void* stream);
+
+/* --------------------------------------------------------------- q4_0 GEMV
+ * [IL] CudaQwen3::gemv: y[b][r] = sum_k dq(W)[r][k] * x[b][k].
+ * d_scales / d_quants: the q4_0 matrix above (device). d_x: f16 [batch][cols].
+ * d_y: [batch][rows] (QL_EPI_SILU_MUL: [batch][rows/2]) in y_dtype (f32 or f16;
+ * QL_EPI_ADD_RESIDUAL requires f32). d_residual: f32 [batch][rows] for QL_EPI_ADD_RESIDUAL,
+ * else ignored; it may equal d_y. cols % 32 == 0; rows even for QL_EPI_SILU_MUL;
+ * 1 <= batch <= 64. Accumulation is f32 across blocks. Picks the CUDA-core GEMV for small
+ * batches and the tensor-core skinny GEMM for larger ones.                               */
+int ql_gemv_q4_0(const void* d_scales, const void* d_quants, int64_t rows, int64_t cols,
+                 const void* d_x, int64_t batch, void* d_y, int y_dtype, int epilogue,
+                 const float* d_residual, void* stream);
+
+/* --------------------------------------------------------------- paged decode attention
+ * [FK] launch_paged_decode_attention / attention_paged, split-K over the context:
+ *   out[b][h][:] = sum_{t < context_lens[b]} softmax_t(q[b][h] . K_t * scale) V_t
+ * with K_t, V_t of kv head g = h / (n_heads / n_kv_heads), stored at physical block
+ * block_tables[b][t / block_size], slot t % block_size.
+ * d_q: f16 [batch][n_heads][head_dim]. d_k_pool, d_v_pool: f16
+ * [num_blocks][n_kv_heads][block_size][head_dim] (one layer). d_block_tables: int32
+ * [batch][max_blocks_per_seq]. d_context_lens: int32 [batch], each in
+ * [1, max_blocks_per_seq * block_size] (0 is allowed and marks an idle slot: its output is
+ * left untouched). d_out: f16 [batch][n_heads * head_dim].
+ * head_dim in {64, 128}; block_size 16; n_heads % n_kv_heads == 0, group <= 8.
+ * d_workspace: ql_paged_attn_workspace_bytes(...) bytes, ZERO-FILLED before its first use
+ * (the kernels leave it zero-filled again for the next call); one workspace per stream.  */
+size_t ql_paged_attn_workspace_bytes(int64_t batch, int n_heads, int n_kv_heads,
+                                     int head_dim, int block_size,
+                                     int64_t max_blocks_per_seq);
+int ql_paged_attn_decode(const void* d_q, const void* d_k_pool, const void* d_v_pool,
+                         const int32_t* d_block_tables, const int32_t* d_context_lens,
+                         int64_t batch, int n_heads, int n_kv_heads, int head_dim,
+                         int block_size, int64_t max_blocks_per_seq, int64_t num_blocks,
+                         float scale, void* d_out, void* d_workspace,
+                         size_t workspace_bytes, void* stream);
+
+/* --------------------------------------------------------------- qk-norm + RoPE + KV append
+ * [IL] CudaQwen3::step (qk_norm_rope kernel), [FK] decode_step / attention_paged:
+ * for slot b at position p = d_positions[b]:
+ *   q_h = rope(rms(q_h) * q_norm, p), k_g = rope(rms(k_g) * k_norm, p)  (RMS over head_dim,
+ *   [ME] host_rms_norm), V unchanged; rope is the NeoX split-half rotation of pairs
+ *   (i, i + head_dim/2) by angle p * theta^(-2i/head_dim) ([ME] host_rope_at,
+ *   [IL] rope_inv_freq), taken from the tables d_cos/d_sin [max_position][head_dim/2].
+ * d_qkv: f32 [batch][(n_heads + 2 n_kv_heads) * head_dim] (rows q | k | v).
+ * Writes q as f16 [batch][n_heads][head_dim] to d_q_out and K, V (f16) to pool slot
+ * (block_tables[b][p / block_size], p % block_size) of kv head g.
+ * d_active: int32 [batch] or NULL; a slot with active == 0 is skipped.                    */
+int ql_fused_norm_rope(const float* d_qkv, const float* d_q_norm_w, const float* d_k_norm_w,
+                       const float* d_cos, const float* d_sin, const int32_t* d_positions,
+                       const int32_t* d_active, float eps, int64_t batch, int n_heads,
+                       int n_kv_heads, int head_dim, void* d_q_out, void* d_k_pool,
+                       void* d_v_pool, const int32_t* d_block_tables,
+                       int64_t max_blocks_per_seq, int block_size, int64_t num_blocks,
+                       int64_t max_position, void* stream);
+/* Host: cos/sin tables [max_position][head_dim/2] (f32, computed in f64) for theta. */
+int ql_rope_tables(float* h_cos, float* h_sin, int64_t max_position, int head_dim,
+                   double theta);
+
+/* --------------------------------------------------------------- model + decode step */
+typedef struct {
+    const void* scales; /* f16 [rows][cols/32] (device) */
+    const void* quants; /* u8  [rows][cols/32][16] (device) */
+    int64_t rows, cols;
+} ql_q4_0_matrix;
+
+typedef struct {
+    const float* attn_norm; /* [hidden] */
+    const float* ffn_norm;  /* [hidden] */
+    const float* q_norm;    /* [head_dim] */
+    const float* k_norm;    /* [head_dim] */
+    ql_q4_0_matrix qkv;     /* [(n_heads + 2 n_kv) * head_dim, hidden], rows q | k | v */
+    ql_q4_0_matrix o;       /* [hidden, n_heads * head_dim] */
+    ql_q4_0_matrix gate_up; /* [2 * intermediate, hidden], rows gate | up */
+    ql_q4_0_matrix down;    /* [hidden, intermediate] */
+} ql_layer_desc;
+
+typedef struct {
+    int64_t hidden, n_layers, n_heads, n_kv_heads, head_dim, intermediate, vocab;
+    float eps;                  /* RMSNorm epsilon */
+    double rope_theta;
+    const float* embed;         /* f32 [vocab][hidden] (device) */
+    const float* final_norm;    /* [hidden] */
+    ql_q4_0_matrix lm_head;     /* [vocab, hidden] (untied) */
+    const ql_layer_desc* layers;/* HOST array [n_layers] of device pointers; copied */
+    void* k_pool;               /* f16 [n_layers][num_blocks][n_kv][block_size][head_dim] */
+    void* v_pool;               /* same */
+    int64_t num_blocks;
+    int block_size;             /* 16 */
+    int64_t max_batch;          /* largest batch any step will use */
+    int64_t max_blocks_per_seq; /* block-table row length; max context = this * block_size */
+} ql_model_desc;
+
+typedef struct ql_model ql_model;
+
+/* Validates dims and allocates the handle's workspace on the current device. */
+int ql_model_create(const ql_model_desc* desc, ql_model** out);
+int ql_model_destroy(ql_model* m);
+
+/* One decode step for `batch` slots ([IL] CudaQwen3::step, [FK] batch_decode_step).
+ * Every per-step input lives in device memory so the step can be captured and replayed:
+ *   tokens      int32 [batch]  this step's token per slot (read)
+ *   positions   int32 [batch]  position of tokens[b]; its K/V is appended there and the
+ *                              attention covers positions 0..positions[b]; advanced by one
+ *                              for every active slot at the end of the step
+ *   block_tables int32 [batch][max_blocks_per_seq] of the model; blocks for position
+ *                              positions[b] must be assigned before the step
+ *   active      int32 [batch] or NULL (all active); inactive slots append nothing, keep
+ *                              their position and their next token
+ *   logits      f32 [batch][vocab] or NULL (then kept in the workspace)
+ *   next_tokens int32 [batch]  greedy argmax of the logits, lowest index on ties; may be
+ *                              the tokens buffer itself (feeds the next replay)
+ *   out_tokens  int32 [batch][out_stride] or NULL: next token also written at index
+ *                              positions[b] + 1 (if < out_stride)                          */
+typedef struct {
+    int64_t batch;
+    const int32_t* tokens;
+    int32_t* positions;
+    const int32_t* block_tables;
+    const int32_t* active;
+    float* logits;
+    int32_t* next_tokens;
+    int32_t* out_tokens;
+    int64_t out_stride;
+} ql_step_args;
+
+int ql_decode_step(ql_model* m, const ql_step_args* args, void* stream);
+/* Capture one ql_decode_step with these arguments as a CUDA graph keyed by args->batch
+ * ([IL] CudaQwen3::capture). Replaces an earlier graph of the same batch.               */
+int ql_decode_graph_capture(ql_model* m, const ql_step_args* args, void* stream);
+/* Replay the graph of this batch n_steps times back to back ([IL] run_graph).
+ * QL_ESTATE if no graph of that batch was captured.                                    */
+int ql_decode_graph_replay(ql_model* m, int64_t batch, int n_steps, void* stream);
+/* Synchronizes the device and reads (and clears) its error record: QL_OK, or QL_EDEVICE
+ * with the first recorded event described in ql_last_error(). m may be NULL.            */
+int ql_check_device_error(ql_model* m);
+
+/* --------------------------------------------------------------- KV block allocator (host)
+ * [FK] alloc_block / release_kv_cache: take the most recently freed block first, else the
+ * next never-used id; QL_EPOOL when the pool is exhausted.                               */
+typedef struct ql_block_pool ql_block_pool;
+int ql_block_pool_create(int64_t num_blocks, ql_block_pool** out);
+int ql_block_pool_destroy(ql_block_pool* p);
+int ql_block_pool_alloc(ql_block_pool* p, int32_t* out_id);
+int ql_block_pool_free(ql_block_pool* p, const int32_t* ids, int64_t n);
+int64_t ql_block_pool_in_use(const ql_block_pool* p);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QL_H */

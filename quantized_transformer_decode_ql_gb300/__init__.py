@@ -1,0 +1,111 @@
+"""libql Python binding: q4_0 dense-transformer decode on one GB300.
+
+Thin wrappers with the names of the C entry points (``include/ql.h``). Device buffers are
+``torch`` CUDA tensors (PyTorch provides memory and streams only); every computation runs in
+the CUDA library ``_build/libql.so``. Each wrapper raises :class:`QLError` on a non-zero
+status.
+"""
+from __future__ import annotations
+
+import ctypes
+
+from ._lib import (QLError, QL_OK, QL_EINVAL, QL_ENOMEM, QL_ECUDA, QL_EPOOL, QL_ERANGE,
+                   QL_EDEVICE, QL_ESTATE, QL_DTYPE_F32, QL_DTYPE_F16, QL_EPI_NONE,
+                   QL_EPI_ADD_RESIDUAL, QL_EPI_SILU_MUL, Q4Matrix, LayerDesc, ModelDesc,
+                   StepArgs, SIGNATURES, LIB_PATH, lib, check, ptr, stream_ptr)
+
+__all__ = [
+    "QLError", "lib", "ql_q4_0_pack", "ql_q4_0_unpack", "ql_q4_0_pack_device", "ql_gemv_q4_0",
+    "ql_paged_attn_workspace_bytes", "ql_paged_attn_decode", "ql_fused_norm_rope",
+    "ql_rope_tables", "ql_check_device_error", "BlockPool", "SIGNATURES",
+]
+
+
+def ql_q4_0_pack(w, scales, quants):
+    """Host codec: ``w`` f32 [rows, cols] numpy -> ``scales`` u16 [rows, cols/32], ``quants`` u8."""
+    rows, cols = w.shape
+    check(lib().ql_q4_0_pack(w.ctypes.data, rows, cols, scales.ctypes.data, quants.ctypes.data))
+
+
+def ql_q4_0_unpack(scales, quants, w):
+    rows, cols = w.shape
+    check(lib().ql_q4_0_unpack(scales.ctypes.data, quants.ctypes.data, rows, cols, w.ctypes.data))
+
+
+def ql_q4_0_pack_device(w, scales, quants, stream=None):
+    rows, cols = w.shape
+    check(lib().ql_q4_0_pack_device(ptr(w), rows, cols, ptr(scales), ptr(quants), stream_ptr(stream)))
+
+
+def ql_gemv_q4_0(scales, quants, rows, cols, x, batch, y, y_dtype=QL_DTYPE_F32,
+                 epilogue=QL_EPI_NONE, residual=None, stream=None):
+    check(lib().ql_gemv_q4_0(ptr(scales), ptr(quants), rows, cols, ptr(x), batch, ptr(y), y_dtype,
+                             epilogue, ptr(residual), stream_ptr(stream)))
+
+
+def ql_paged_attn_workspace_bytes(batch, n_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq):
+    return int(lib().ql_paged_attn_workspace_bytes(batch, n_heads, n_kv_heads, head_dim, block_size,
+                                                   max_blocks_per_seq))
+
+
+def ql_paged_attn_decode(q, k_pool, v_pool, block_tables, context_lens, batch, n_heads, n_kv_heads,
+                         head_dim, block_size, max_blocks_per_seq, num_blocks, scale, out,
+                         workspace, stream=None):
+    check(lib().ql_paged_attn_decode(ptr(q), ptr(k_pool), ptr(v_pool), ptr(block_tables),
+                                     ptr(context_lens), batch, n_heads, n_kv_heads, head_dim,
+                                     block_size, max_blocks_per_seq, num_blocks, scale, ptr(out),
+                                     ptr(workspace), workspace.numel() * workspace.element_size(),
+                                     stream_ptr(stream)))
+
+
+def ql_fused_norm_rope(qkv, q_norm, k_norm, cos_t, sin_t, positions, active, eps, batch, n_heads,
+                       n_kv_heads, head_dim, q_out, k_pool, v_pool, block_tables,
+                       max_blocks_per_seq, block_size, num_blocks, max_position, stream=None):
+    check(lib().ql_fused_norm_rope(ptr(qkv), ptr(q_norm), ptr(k_norm), ptr(cos_t), ptr(sin_t),
+                                   ptr(positions), ptr(active), eps, batch, n_heads, n_kv_heads,
+                                   head_dim, ptr(q_out), ptr(k_pool), ptr(v_pool), ptr(block_tables),
+                                   max_blocks_per_seq, block_size, num_blocks, max_position,
+                                   stream_ptr(stream)))
+
+
+def ql_rope_tables(cos_t, sin_t, theta):
+    """Host: fill numpy f32 ``cos_t``, ``sin_t`` [max_position, head_dim/2]."""
+    n, half = cos_t.shape
+    check(lib().ql_rope_tables(cos_t.ctypes.data, sin_t.ctypes.data, n, 2 * half, theta))
+
+
+def ql_check_device_error(model=None):
+    h = model.handle if model is not None else None
+    check(lib().ql_check_device_error(h))
+
+
+class BlockPool:
+    """Host KV block allocator (free list first, then bump; QL_EPOOL when exhausted)."""
+
+    def __init__(self, num_blocks: int):
+        h = ctypes.c_void_p()
+        check(lib().ql_block_pool_create(num_blocks, ctypes.byref(h)))
+        self.handle = h.value
+
+    def alloc(self) -> int:
+        out = ctypes.c_int32()
+        check(lib().ql_block_pool_alloc(self.handle, ctypes.byref(out)))
+        return int(out.value)
+
+    def free(self, ids):
+        arr = (ctypes.c_int32 * len(ids))(*[int(i) for i in ids])
+        check(lib().ql_block_pool_free(self.handle, arr, len(ids)))
+
+    def in_use(self) -> int:
+        return int(lib().ql_block_pool_in_use(self.handle))
+
+    def close(self):
+        if self.handle:
+            lib().ql_block_pool_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,158 @@
+// Internal declarations shared by the libql translation units (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include <string>
+
+#include "../../include/ql.h"
+
+namespace ql {
+
+// ---------------------------------------------------------------- errors (host)
+int set_error(int status, const std::string& msg);
+int cuda_error(cudaError_t e, const char* what);
+
+#define QL_TRY_CUDA(call)                                                    \
+    do {                                                                     \
+        cudaError_t e_ = (call);                                             \
+        if (e_ != cudaSuccess) return ::ql::cuda_error(e_, #call);           \
+    } while (0)
+
+#define QL_REQUIRE(cond, msg)                                                \
+    do {                                                                     \
+        if (!(cond)) return ::ql::set_error(QL_EINVAL, msg);                 \
+    } while (0)
+
+// ---------------------------------------------------------------- device error record
+// First out-of-range event seen by any kernel on a device. Kernels record with
+// record_device_error() and skip the access; the host reads it in ql_check_device_error.
+struct DevError {
+    int code;      // nonzero once something was recorded
+    int where;     // which kernel (DevErrWhere)
+    long long index;
+    long long value;
+};
+enum DevErrWhere {
+    kErrEmbedToken = 1,
+    kErrRopePosition = 2,
+    kErrRopeBlock = 3,
+    kErrAttnBlock = 4,
+    kErrAttnLength = 5,
+    kErrPackNonFinite = 6,
+    kErrPackOverflow = 7,
+};
+// The current device's record (allocated on first use, zero-filled).
+DevError* device_error_record();
+
+#ifdef __CUDACC__
+__device__ __forceinline__ void record_device_error(DevError* e, int where, long long index,
+                                                    long long value) {
+    if (e != nullptr && atomicCAS(&e->code, 0, 1) == 0) {
+        e->where = where;
+        e->index = index;
+        e->value = value;
+    }
+}
+#endif
+
+// ---------------------------------------------------------------- launch helpers
+int num_sms();   // SM count of the current device (cached per device)
+
+// Programmatic dependent launch (PDL): a kernel launched with this attribute may start while
+// its predecessor in the stream is still running; it must call pdl_wait() before touching
+// anything the predecessor writes. Kernels call pdl_trigger() once their own early work is
+// issued so that the successor can start.
+#ifdef __CUDACC__
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+#endif
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                   cudaStream_t s, bool pdl, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// ---------------------------------------------------------------- GEMV (internal form)
+enum GemvPrologue { kProX16 = 0, kProRmsF32 = 1 };
+enum { kEpiArgmax = 3 };   // internal epilogue: logits (optional) + packed argmax keys
+
+struct GemvArgs {
+    const __half* scales;
+    const uint8_t* quants;
+    int64_t rows, cols;
+    int batch;
+    // input: kProX16 -> x16 [batch][cols] f16; kProRmsF32 -> xf [batch][cols] f32, normed
+    // with norm_w and eps inside the kernel (RMSNorm prologue)
+    int prologue;
+    const __half* x16;
+    const float* xf;
+    const float* norm_w;
+    float eps;
+    int epilogue;               // QL_EPI_* or kEpiArgmax
+    int y_dtype;                // QL_DTYPE_*
+    void* y;
+    const float* residual;
+    unsigned long long* argmax_keys;   // [batch], kEpiArgmax
+    const int32_t* active;      // optional, kEpiArgmax: inactive columns skip the argmax
+};
+int gemv_launch(const GemvArgs& a, cudaStream_t s, bool pdl);
+
+// ---------------------------------------------------------------- attention (internal)
+struct AttnArgs {
+    const __half* q;
+    const __half* k_pool;
+    const __half* v_pool;
+    const int32_t* block_tables;
+    const int32_t* context_lens;   // if null: positions[b] + 1 (decode step form)
+    const int32_t* positions;
+    const int32_t* active;
+    int batch, n_heads, n_kv_heads, head_dim, block_size;
+    int64_t max_blocks_per_seq, num_blocks;
+    float scale;
+    __half* out;
+    void* workspace;
+    size_t workspace_bytes;
+};
+size_t attn_workspace_bytes(int64_t batch, int n_heads, int n_kv_heads, int head_dim,
+                            int block_size, int64_t max_blocks_per_seq);
+int attn_launch(const AttnArgs& a, cudaStream_t s, bool pdl);
+
+// ---------------------------------------------------------------- norm + rope (internal)
+struct RopeArgs {
+    const float* qkv;
+    const float* q_norm;
+    const float* k_norm;
+    const float* cos_t;
+    const float* sin_t;
+    const int32_t* positions;
+    const int32_t* active;
+    float eps;
+    int batch, n_heads, n_kv_heads, head_dim;
+    __half* q_out;
+    __half* k_pool;
+    __half* v_pool;
+    const int32_t* block_tables;
+    int64_t max_blocks_per_seq;
+    int block_size;
+    int64_t num_blocks;
+    int64_t max_position;
+};
+int rope_launch(const RopeArgs& a, cudaStream_t s, bool pdl);
+
+}  // namespace ql

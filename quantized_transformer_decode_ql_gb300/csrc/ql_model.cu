@@ -1,0 +1,379 @@
+// Model handle and the whole decode step.
+//
+// [IL] inferencelayer cuda_llm.rs CudaQwen3::step / seed / capture / run_graph: a step takes
+// no host arguments (token, position and KV offset live in device memory), allocates
+// nothing, and is captured once as a CUDA graph that every later step replays; greedy argmax
+// and the position advance stay on the device. [FK] ferrum-kernels cuda_decode.rs
+// batch_decode_step: several sequences per step over a paged KV pool.
+//
+// Kernel sequence of one step (batch B), all launched with programmatic dependent launch so
+// that each GEMV starts streaming its weights into L2 while its predecessor drains:
+//   embed                      x[b] = E[token[b]]                          (f32 residual)
+//   per layer:
+//     gemv  rms(x)*attn_norm -> W_qkv                                       -> qkv f32
+//     norm_rope                q/k RMSNorm + RoPE, K/V -> paged pool        -> q f16
+//     attention                split-K paged GQA over positions 0..p       -> o f16
+//     gemv  o -> W_o, x += .                                                (residual epilogue)
+//     gemv  rms(x)*ffn_norm -> W_gate|up, silu(g)*u                         -> act f16
+//     gemv  act -> W_down, x += .                                           (residual epilogue)
+//   gemv  rms(x)*final_norm -> W_lm, logits + packed argmax keys
+//   finalize                   next token, position += 1, keys re-armed
+#include <cuda_fp16.h>
+
+#include <map>
+#include <vector>
+
+#include "ql_internal.h"
+
+struct ql_model {
+    ql_model_desc d;
+    std::vector<ql_layer_desc> layers;
+    int device = 0;
+    // workspace (owned)
+    float* x = nullptr;          // [maxB][hidden]
+    float* qkv = nullptr;        // [maxB][qkv_rows]
+    __half* q16 = nullptr;       // [maxB][nh*hd]
+    __half* attn = nullptr;      // [maxB][nh*hd]
+    __half* act = nullptr;       // [maxB][inter]
+    float* logits = nullptr;     // [maxB][vocab]
+    unsigned long long* keys = nullptr;   // [maxB]
+    float* cos_t = nullptr;      // [max_pos][hd/2]
+    float* sin_t = nullptr;
+    void* attn_ws = nullptr;
+    size_t attn_ws_bytes = 0;
+    std::vector<void*> owned;
+    std::map<int64_t, cudaGraphExec_t> graphs;
+};
+
+namespace ql {
+namespace {
+
+__global__ void embed_kernel(const float* __restrict__ E, const int32_t* __restrict__ tokens,
+                             const int32_t* __restrict__ active, float* __restrict__ x, int hidden,
+                             int vocab, DevError* err) {
+    const int b = blockIdx.x;
+    pdl_wait();
+    pdl_trigger();
+    int tok = tokens[b];
+    const bool act = active == nullptr || active[b] != 0;
+    if (tok < 0 || tok >= vocab) {
+        if (act && threadIdx.x == 0) record_device_error(err, kErrEmbedToken, b, tok);
+        tok = 0;
+    }
+    const float4* src = reinterpret_cast<const float4*>(E + (size_t)tok * hidden);
+    float4* dst = reinterpret_cast<float4*>(x + (size_t)b * hidden);
+    for (int i = threadIdx.x; i < hidden / 4; i += blockDim.x) dst[i] = src[i];
+}
+
+__global__ void finalize_kernel(unsigned long long* keys, const int32_t* active, int32_t* positions,
+                                int32_t* next_tokens, int32_t* out_tokens, long long out_stride,
+                                float* logits_dummy, int batch) {
+    (void)logits_dummy;
+    pdl_wait();
+    pdl_trigger();
+    for (int b = threadIdx.x; b < batch; b += blockDim.x) {
+        const unsigned long long k = keys[b];
+        keys[b] = 0ull;
+        if (active && active[b] == 0) continue;
+        const int tok = (int)(0xFFFFFFFFu - (uint32_t)(k & 0xFFFFFFFFull));
+        const int pos = positions[b];
+        next_tokens[b] = tok;
+        if (out_tokens && pos + 1 >= 0 && pos + 1 < out_stride)
+            out_tokens[(size_t)b * out_stride + pos + 1] = tok;
+        positions[b] = pos + 1;
+    }
+}
+
+bool check_matrix(const ql_q4_0_matrix& m, int64_t rows, int64_t cols) {
+    return m.scales && m.quants && m.rows == rows && m.cols == cols;
+}
+
+int alloc(ql_model* m, void** p, size_t bytes) {
+    cudaError_t e = cudaMalloc(p, bytes);
+    if (e != cudaSuccess) return set_error(QL_ENOMEM, std::string("ql_model_create: cudaMalloc failed: ") + cudaGetErrorString(e));
+    m->owned.push_back(*p);
+    return QL_OK;
+}
+
+int run_step(ql_model* m, const ql_step_args* a, cudaStream_t s) {
+    const ql_model_desc& d = m->d;
+    const int B = (int)a->batch;
+    const bool pdl = true;
+    const int hd = (int)d.head_dim, nh = (int)d.n_heads, nkv = (int)d.n_kv_heads;
+    const size_t layer_pool = (size_t)d.num_blocks * nkv * d.block_size * hd;
+    int rc;
+
+    cudaError_t e = launch(embed_kernel, dim3(B), dim3(256), 0, s, pdl, d.embed, a->tokens, a->active,
+                           m->x, (int)d.hidden, (int)d.vocab, device_error_record());
+    if (e != cudaSuccess) return cuda_error(e, "embed launch");
+
+    for (int li = 0; li < d.n_layers; ++li) {
+        const ql_layer_desc& L = m->layers[li];
+        GemvArgs g = {};
+        g.batch = B;
+        // qkv projection with the attention RMSNorm as prologue
+        g.scales = static_cast<const __half*>(L.qkv.scales);
+        g.quants = static_cast<const uint8_t*>(L.qkv.quants);
+        g.rows = L.qkv.rows;
+        g.cols = L.qkv.cols;
+        g.prologue = kProRmsF32;
+        g.xf = m->x;
+        g.norm_w = L.attn_norm;
+        g.eps = d.eps;
+        g.epilogue = QL_EPI_NONE;
+        g.y_dtype = QL_DTYPE_F32;
+        g.y = m->qkv;
+        if ((rc = gemv_launch(g, s, pdl)) != QL_OK) return rc;
+
+        RopeArgs r = {};
+        r.qkv = m->qkv;
+        r.q_norm = L.q_norm;
+        r.k_norm = L.k_norm;
+        r.cos_t = m->cos_t;
+        r.sin_t = m->sin_t;
+        r.positions = a->positions;
+        r.active = a->active;
+        r.eps = d.eps;
+        r.batch = B;
+        r.n_heads = nh;
+        r.n_kv_heads = nkv;
+        r.head_dim = hd;
+        r.q_out = m->q16;
+        r.k_pool = static_cast<__half*>(d.k_pool) + layer_pool * li;
+        r.v_pool = static_cast<__half*>(d.v_pool) + layer_pool * li;
+        r.block_tables = a->block_tables;
+        r.max_blocks_per_seq = d.max_blocks_per_seq;
+        r.block_size = d.block_size;
+        r.num_blocks = d.num_blocks;
+        r.max_position = d.max_blocks_per_seq * d.block_size;
+        if ((rc = rope_launch(r, s, pdl)) != QL_OK) return rc;
+
+        AttnArgs at = {};
+        at.q = m->q16;
+        at.k_pool = r.k_pool;
+        at.v_pool = r.v_pool;
+        at.block_tables = a->block_tables;
+        at.context_lens = nullptr;
+        at.positions = a->positions;
+        at.active = a->active;
+        at.batch = B;
+        at.n_heads = nh;
+        at.n_kv_heads = nkv;
+        at.head_dim = hd;
+        at.block_size = d.block_size;
+        at.max_blocks_per_seq = d.max_blocks_per_seq;
+        at.num_blocks = d.num_blocks;
+        at.scale = 1.0f / sqrtf((float)hd);
+        at.out = m->attn;
+        at.workspace = m->attn_ws;
+        at.workspace_bytes = m->attn_ws_bytes;
+        if ((rc = attn_launch(at, s, pdl)) != QL_OK) return rc;
+
+        GemvArgs go = {};
+        go.batch = B;
+        go.scales = static_cast<const __half*>(L.o.scales);
+        go.quants = static_cast<const uint8_t*>(L.o.quants);
+        go.rows = L.o.rows;
+        go.cols = L.o.cols;
+        go.prologue = kProX16;
+        go.x16 = m->attn;
+        go.epilogue = QL_EPI_ADD_RESIDUAL;
+        go.y_dtype = QL_DTYPE_F32;
+        go.y = m->x;
+        go.residual = m->x;
+        if ((rc = gemv_launch(go, s, pdl)) != QL_OK) return rc;
+
+        GemvArgs gu = {};
+        gu.batch = B;
+        gu.scales = static_cast<const __half*>(L.gate_up.scales);
+        gu.quants = static_cast<const uint8_t*>(L.gate_up.quants);
+        gu.rows = L.gate_up.rows;
+        gu.cols = L.gate_up.cols;
+        gu.prologue = kProRmsF32;
+        gu.xf = m->x;
+        gu.norm_w = L.ffn_norm;
+        gu.eps = d.eps;
+        gu.epilogue = QL_EPI_SILU_MUL;
+        gu.y_dtype = QL_DTYPE_F16;
+        gu.y = m->act;
+        if ((rc = gemv_launch(gu, s, pdl)) != QL_OK) return rc;
+
+        GemvArgs gd = {};
+        gd.batch = B;
+        gd.scales = static_cast<const __half*>(L.down.scales);
+        gd.quants = static_cast<const uint8_t*>(L.down.quants);
+        gd.rows = L.down.rows;
+        gd.cols = L.down.cols;
+        gd.prologue = kProX16;
+        gd.x16 = m->act;
+        gd.epilogue = QL_EPI_ADD_RESIDUAL;
+        gd.y_dtype = QL_DTYPE_F32;
+        gd.y = m->x;
+        gd.residual = m->x;
+        if ((rc = gemv_launch(gd, s, pdl)) != QL_OK) return rc;
+    }
+
+    GemvArgs gl = {};
+    gl.batch = B;
+    gl.scales = static_cast<const __half*>(d.lm_head.scales);
+    gl.quants = static_cast<const uint8_t*>(d.lm_head.quants);
+    gl.rows = d.lm_head.rows;
+    gl.cols = d.lm_head.cols;
+    gl.prologue = kProRmsF32;
+    gl.xf = m->x;
+    gl.norm_w = d.final_norm;
+    gl.eps = d.eps;
+    gl.epilogue = kEpiArgmax;
+    gl.y_dtype = QL_DTYPE_F32;
+    gl.y = a->logits ? a->logits : m->logits;
+    gl.argmax_keys = m->keys;
+    gl.active = a->active;
+    if ((rc = gemv_launch(gl, s, pdl)) != QL_OK) return rc;
+
+    e = launch(finalize_kernel, dim3(1), dim3(64), 0, s, pdl, m->keys, a->active, a->positions,
+               a->next_tokens, a->out_tokens, (long long)a->out_stride, (float*)nullptr, B);
+    if (e != cudaSuccess) return cuda_error(e, "finalize launch");
+    return QL_OK;
+}
+
+int check_step_args(ql_model* m, const ql_step_args* a) {
+    if (!m || !a) return set_error(QL_EINVAL, "decode step: null model or args");
+    if (a->batch < 1 || a->batch > m->d.max_batch)
+        return set_error(QL_EINVAL, "decode step: batch must be in [1, max_batch]");
+    if (!a->tokens || !a->positions || !a->block_tables || !a->next_tokens)
+        return set_error(QL_EINVAL, "decode step: tokens, positions, block_tables and next_tokens are required");
+    if (a->out_tokens && a->out_stride <= 0)
+        return set_error(QL_EINVAL, "decode step: out_stride must be positive with out_tokens");
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev != m->device) return set_error(QL_EINVAL, "decode step: current device differs from the model's");
+    return QL_OK;
+}
+
+}  // namespace
+}  // namespace ql
+
+using namespace ql;
+
+extern "C" int ql_model_create(const ql_model_desc* desc, ql_model** out) {
+    if (!desc || !out) return set_error(QL_EINVAL, "ql_model_create: null pointer");
+    *out = nullptr;
+    const ql_model_desc& d = *desc;
+    QL_REQUIRE(d.hidden > 0 && d.hidden % 32 == 0, "ql_model_create: hidden must be a positive multiple of 32");
+    QL_REQUIRE(d.n_layers > 0 && d.layers, "ql_model_create: need layers");
+    QL_REQUIRE(d.head_dim == 64 || d.head_dim == 128, "ql_model_create: head_dim must be 64 or 128");
+    QL_REQUIRE(d.n_kv_heads > 0 && d.n_heads % d.n_kv_heads == 0, "ql_model_create: bad head counts");
+    const int64_t G = d.n_heads / d.n_kv_heads;
+    QL_REQUIRE(G == 1 || G == 2 || G == 4 || G == 8, "ql_model_create: GQA group must be 1, 2, 4 or 8");
+    QL_REQUIRE(d.intermediate > 0 && d.intermediate % 32 == 0, "ql_model_create: intermediate must be a multiple of 32");
+    QL_REQUIRE((d.n_heads * d.head_dim) % 32 == 0, "ql_model_create: n_heads*head_dim must be a multiple of 32");
+    QL_REQUIRE(d.vocab > 0 && d.embed && d.final_norm, "ql_model_create: need vocab, embed, final_norm");
+    QL_REQUIRE(d.block_size == 16, "ql_model_create: block_size must be 16");
+    QL_REQUIRE(d.k_pool && d.v_pool && d.num_blocks > 0, "ql_model_create: need KV pools");
+    QL_REQUIRE(d.max_batch >= 1 && d.max_batch <= 4096, "ql_model_create: max_batch out of range");
+    QL_REQUIRE(d.max_blocks_per_seq >= 1, "ql_model_create: bad max_blocks_per_seq");
+    QL_REQUIRE(d.eps > 0.f && d.rope_theta > 0.0, "ql_model_create: eps and rope_theta must be positive");
+    QL_REQUIRE(check_matrix(d.lm_head, d.vocab, d.hidden), "ql_model_create: lm_head must be [vocab, hidden]");
+    const int64_t qkv_rows = (d.n_heads + 2 * d.n_kv_heads) * d.head_dim;
+    for (int64_t i = 0; i < d.n_layers; ++i) {
+        const ql_layer_desc& L = d.layers[i];
+        const std::string li = " (layer " + std::to_string(i) + ")";
+        QL_REQUIRE(L.attn_norm && L.ffn_norm && L.q_norm && L.k_norm, "ql_model_create: missing norm weights" + li);
+        QL_REQUIRE(check_matrix(L.qkv, qkv_rows, d.hidden), "ql_model_create: qkv must be [(nh+2nkv)*hd, hidden]" + li);
+        QL_REQUIRE(check_matrix(L.o, d.hidden, d.n_heads * d.head_dim), "ql_model_create: o must be [hidden, nh*hd]" + li);
+        QL_REQUIRE(check_matrix(L.gate_up, 2 * d.intermediate, d.hidden), "ql_model_create: gate_up must be [2*inter, hidden]" + li);
+        QL_REQUIRE(check_matrix(L.down, d.hidden, d.intermediate), "ql_model_create: down must be [hidden, inter]" + li);
+    }
+    if (!device_error_record()) return set_error(QL_ECUDA, "ql_model_create: cannot allocate the device error record");
+
+    ql_model* m = new (std::nothrow) ql_model();
+    if (!m) return set_error(QL_ENOMEM, "ql_model_create: out of host memory");
+    m->d = d;
+    m->layers.assign(d.layers, d.layers + d.n_layers);
+    m->d.layers = m->layers.data();
+    cudaGetDevice(&m->device);
+    const int64_t B = d.max_batch;
+    const int64_t max_pos = d.max_blocks_per_seq * d.block_size;
+    int rc = QL_OK;
+    auto A = [&](void** p, size_t bytes) { if (rc == QL_OK) rc = alloc(m, p, bytes); };
+    A((void**)&m->x, B * d.hidden * 4);
+    A((void**)&m->qkv, B * qkv_rows * 4);
+    A((void**)&m->q16, B * d.n_heads * d.head_dim * 2);
+    A((void**)&m->attn, B * d.n_heads * d.head_dim * 2);
+    A((void**)&m->act, B * d.intermediate * 2);
+    A((void**)&m->logits, B * d.vocab * 4);
+    A((void**)&m->keys, B * 8);
+    A((void**)&m->cos_t, max_pos * (d.head_dim / 2) * 4);
+    A((void**)&m->sin_t, max_pos * (d.head_dim / 2) * 4);
+    m->attn_ws_bytes = attn_workspace_bytes(B, (int)d.n_heads, (int)d.n_kv_heads, (int)d.head_dim,
+                                            d.block_size, d.max_blocks_per_seq);
+    A(&m->attn_ws, m->attn_ws_bytes);
+    if (rc == QL_OK) {
+        std::vector<float> hc(max_pos * (d.head_dim / 2)), hs(hc.size());
+        rc = ql_rope_tables(hc.data(), hs.data(), max_pos, (int)d.head_dim, d.rope_theta);
+        cudaError_t e = cudaSuccess;
+        if (rc == QL_OK) e = cudaMemcpy(m->cos_t, hc.data(), hc.size() * 4, cudaMemcpyHostToDevice);
+        if (rc == QL_OK && e == cudaSuccess) e = cudaMemcpy(m->sin_t, hs.data(), hs.size() * 4, cudaMemcpyHostToDevice);
+        if (rc == QL_OK && e == cudaSuccess) e = cudaMemset(m->keys, 0, B * 8);
+        if (rc == QL_OK && e == cudaSuccess) e = cudaMemset(m->attn_ws, 0, m->attn_ws_bytes);
+        if (rc == QL_OK && e == cudaSuccess) e = cudaMemset(m->x, 0, B * d.hidden * 4);
+        if (rc == QL_OK && e == cudaSuccess) e = cudaDeviceSynchronize();
+        if (rc == QL_OK && e != cudaSuccess) rc = cuda_error(e, "ql_model_create: workspace init");
+    }
+    if (rc != QL_OK) {
+        std::string msg = ql_last_error();
+        ql_model_destroy(m);
+        return set_error(rc, msg);
+    }
+    *out = m;
+    return QL_OK;
+}
+
+extern "C" int ql_model_destroy(ql_model* m) {
+    if (!m) return QL_OK;
+    for (auto& kv : m->graphs) cudaGraphExecDestroy(kv.second);
+    for (void* p : m->owned) cudaFree(p);
+    delete m;
+    return QL_OK;
+}
+
+extern "C" int ql_decode_step(ql_model* m, const ql_step_args* args, void* stream) {
+    int rc = check_step_args(m, args);
+    if (rc != QL_OK) return rc;
+    return run_step(m, args, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int ql_decode_graph_capture(ql_model* m, const ql_step_args* args, void* stream) {
+    int rc = check_step_args(m, args);
+    if (rc != QL_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (!s) return set_error(QL_EINVAL, "ql_decode_graph_capture: needs a non-default stream");
+    QL_TRY_CUDA(cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal));
+    rc = run_step(m, args, s);
+    cudaGraph_t g = nullptr;
+    cudaError_t e = cudaStreamEndCapture(s, &g);
+    if (rc != QL_OK) {
+        if (g) cudaGraphDestroy(g);
+        return rc;
+    }
+    if (e != cudaSuccess) return cuda_error(e, "cudaStreamEndCapture");
+    cudaGraphExec_t ex = nullptr;
+    e = cudaGraphInstantiate(&ex, g, 0);
+    cudaGraphDestroy(g);
+    if (e != cudaSuccess) return cuda_error(e, "cudaGraphInstantiate");
+    auto it = m->graphs.find(args->batch);
+    if (it != m->graphs.end()) cudaGraphExecDestroy(it->second);
+    m->graphs[args->batch] = ex;
+    return QL_OK;
+}
+
+extern "C" int ql_decode_graph_replay(ql_model* m, int64_t batch, int n_steps, void* stream) {
+    if (!m) return set_error(QL_EINVAL, "ql_decode_graph_replay: null model");
+    if (n_steps < 0) return set_error(QL_EINVAL, "ql_decode_graph_replay: n_steps < 0");
+    auto it = m->graphs.find(batch);
+    if (it == m->graphs.end())
+        return set_error(QL_ESTATE, "ql_decode_graph_replay: no graph captured for batch " + std::to_string(batch));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    for (int i = 0; i < n_steps; ++i) QL_TRY_CUDA(cudaGraphLaunch(it->second, s));
+    return QL_OK;
+}

@@ -1,0 +1,174 @@
+"""Device-resident model built on the libql C ABI (memory via PyTorch, compute in libql).
+
+``DeviceModel`` owns the torch tensors that hold a model's q4_0 weights, norms, embedding and
+paged KV pools, fills the ``ql_model_desc`` and drives ``ql_decode_step`` /
+``ql_decode_graph_capture`` / ``ql_decode_graph_replay``. Weights arrive as f32 (host numpy
+arrays or device tensors) and are quantised on the device by ``ql_q4_0_pack_device``.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from ._lib import (LayerDesc, ModelDesc, Q4Matrix, StepArgs, check, lib, ptr, stream_ptr)
+
+BLOCK = 16
+
+
+class Q4Tensor:
+    """A q4_0 matrix on the device: ``scales`` int16 [rows, cols/32] (f16 bits), ``quants`` u8."""
+
+    def __init__(self, rows: int, cols: int, device="cuda"):
+        self.rows, self.cols = rows, cols
+        self.scales = torch.empty((rows, cols // 32), dtype=torch.int16, device=device)
+        self.quants = torch.empty((rows, cols // 32, 16), dtype=torch.uint8, device=device)
+
+    @classmethod
+    def pack(cls, w: torch.Tensor, stream=None) -> "Q4Tensor":
+        """Quantise an f32 device matrix (``ql_q4_0_pack_device``)."""
+        assert w.dtype == torch.float32 and w.is_cuda and w.is_contiguous()
+        t = cls(w.shape[0], w.shape[1], w.device)
+        check(lib().ql_q4_0_pack_device(ptr(w), t.rows, t.cols, ptr(t.scales), ptr(t.quants),
+                                        stream_ptr(stream)))
+        return t
+
+    def desc(self) -> Q4Matrix:
+        return Q4Matrix(ptr(self.scales), ptr(self.quants), self.rows, self.cols)
+
+    def nbytes(self) -> int:
+        return self.scales.numel() * 2 + self.quants.numel()
+
+
+def _dev(a, device="cuda") -> torch.Tensor:
+    if isinstance(a, torch.Tensor):
+        return a.to(device=device, dtype=torch.float32).contiguous()
+    return torch.from_numpy(a).to(device=device, dtype=torch.float32).contiguous()
+
+
+class DeviceModel:
+    """A dense Qwen3-style model resident on one GPU, plus its paged KV pools."""
+
+    def __init__(self, cfg, weights: dict, num_blocks: int, max_batch: int,
+                 max_blocks_per_seq: int, device="cuda"):
+        self.cfg = cfg
+        self.device = device
+        self.num_blocks = num_blocks
+        self.max_batch = max_batch
+        self.max_blocks_per_seq = max_blocks_per_seq
+        torch.cuda.synchronize()
+        self.embed = _dev(weights["embed"], device)
+        self.final_norm = _dev(weights["final_norm"], device)
+        self.lm_head = Q4Tensor.pack(_dev(weights["lm_head"], device))
+        self.layers = []
+        for lw in weights["layers"]:
+            L = {n: _dev(lw[n], device) for n in ("attn_norm", "ffn_norm", "q_norm", "k_norm")}
+            for n in ("wqkv", "wo", "wgu", "wd"):
+                L[n] = Q4Tensor.pack(_dev(lw[n], device))
+            self.layers.append(L)
+        torch.cuda.synchronize()
+        check(lib().ql_check_device_error(None))
+        shape = (cfg.n_layers, num_blocks, cfg.n_kv_heads, BLOCK, cfg.head_dim)
+        self.k_pool = torch.zeros(shape, dtype=torch.float16, device=device)
+        self.v_pool = torch.zeros(shape, dtype=torch.float16, device=device)
+        self._create()
+
+    @classmethod
+    def from_layer_fn(cls, cfg, tensor_fn, num_blocks, max_batch, max_blocks_per_seq, device="cuda"):
+        """Build from ``tensor_fn(layer or None, name) -> f32 device tensor``, one tensor at a
+        time (for models too large to hold as f32 anywhere)."""
+        self = cls.__new__(cls)
+        self.cfg, self.device = cfg, device
+        self.num_blocks, self.max_batch, self.max_blocks_per_seq = num_blocks, max_batch, max_blocks_per_seq
+        self.embed = tensor_fn(None, "embed")
+        self.final_norm = tensor_fn(None, "final_norm")
+        self.lm_head = Q4Tensor.pack(tensor_fn(None, "lm_head"))
+        self.layers = []
+        for li in range(cfg.n_layers):
+            L = {n: tensor_fn(li, n) for n in ("attn_norm", "ffn_norm", "q_norm", "k_norm")}
+            for n in ("wqkv", "wo", "wgu", "wd"):
+                w = tensor_fn(li, n)
+                L[n] = Q4Tensor.pack(w)
+                del w
+            self.layers.append(L)
+        torch.cuda.synchronize()
+        check(lib().ql_check_device_error(None))
+        shape = (cfg.n_layers, num_blocks, cfg.n_kv_heads, BLOCK, cfg.head_dim)
+        self.k_pool = torch.zeros(shape, dtype=torch.float16, device=device)
+        self.v_pool = torch.zeros(shape, dtype=torch.float16, device=device)
+        self._create()
+        return self
+
+    def _create(self):
+        cfg = self.cfg
+        self._layer_descs = (LayerDesc * cfg.n_layers)()
+        for i, L in enumerate(self.layers):
+            self._layer_descs[i] = LayerDesc(ptr(L["attn_norm"]), ptr(L["ffn_norm"]), ptr(L["q_norm"]),
+                                             ptr(L["k_norm"]), L["wqkv"].desc(), L["wo"].desc(),
+                                             L["wgu"].desc(), L["wd"].desc())
+        d = ModelDesc()
+        d.hidden, d.n_layers, d.n_heads = cfg.hidden, cfg.n_layers, cfg.n_heads
+        d.n_kv_heads, d.head_dim, d.intermediate, d.vocab = cfg.n_kv_heads, cfg.head_dim, cfg.intermediate, cfg.vocab
+        d.eps, d.rope_theta = cfg.eps, cfg.rope_theta
+        d.embed, d.final_norm, d.lm_head = ptr(self.embed), ptr(self.final_norm), self.lm_head.desc()
+        d.layers = self._layer_descs
+        d.k_pool, d.v_pool = ptr(self.k_pool), ptr(self.v_pool)
+        d.num_blocks, d.block_size = self.num_blocks, BLOCK
+        d.max_batch, d.max_blocks_per_seq = self.max_batch, self.max_blocks_per_seq
+        self._desc = d
+        h = ctypes.c_void_p()
+        check(lib().ql_model_create(ctypes.byref(d), ctypes.byref(h)))
+        self.handle = h.value
+
+    def weight_bytes(self) -> int:
+        n = self.lm_head.nbytes()
+        for L in self.layers:
+            n += sum(L[k].nbytes() for k in ("wqkv", "wo", "wgu", "wd"))
+        return n
+
+    @staticmethod
+    def step_args(tokens, positions, block_tables, next_tokens, active=None, logits=None,
+                  out_tokens=None) -> StepArgs:
+        a = StepArgs()
+        a.batch = tokens.numel()
+        a.tokens, a.positions, a.block_tables = ptr(tokens), ptr(positions), ptr(block_tables)
+        a.active, a.logits, a.next_tokens = ptr(active), ptr(logits), ptr(next_tokens)
+        a.out_tokens = ptr(out_tokens)
+        a.out_stride = out_tokens.shape[1] if out_tokens is not None else 0
+        return a
+
+    def ql_decode_step(self, args: StepArgs, stream=None):
+        check(lib().ql_decode_step(self.handle, ctypes.byref(args), stream_ptr(stream)))
+
+    def ql_decode_graph_capture(self, args: StepArgs, stream):
+        check(lib().ql_decode_graph_capture(self.handle, ctypes.byref(args), stream_ptr(stream)))
+
+    def ql_decode_graph_replay(self, batch: int, n_steps: int, stream=None):
+        check(lib().ql_decode_graph_replay(self.handle, batch, n_steps, stream_ptr(stream)))
+
+    def ql_check_device_error(self):
+        check(lib().ql_check_device_error(self.handle))
+
+    def write_context(self, slot_blocks, k_ctx, v_ctx):
+        """Place a pre-filled context ``[n_layers, n_kv, n_pos, hd]`` (f16) into the pools
+        through a slot's block list (a host-side copy that stands in for prefill)."""
+        n = k_ctx.shape[2]
+        kc = torch.as_tensor(k_ctx, dtype=torch.float16, device=self.device)
+        vc = torch.as_tensor(v_ctx, dtype=torch.float16, device=self.device)
+        for i, blk in enumerate(slot_blocks):
+            lo, hi = i * BLOCK, min(n, (i + 1) * BLOCK)
+            if lo >= n:
+                break
+            self.k_pool[:, blk, :, : hi - lo] = kc[:, :, lo:hi]
+            self.v_pool[:, blk, :, : hi - lo] = vc[:, :, lo:hi]
+
+    def close(self):
+        if getattr(self, "handle", None):
+            lib().ql_model_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,160 @@
+"""Whole decode step on the GPU (ql_decode_step / graphs) against the oracle.
+
+Tiny config (hidden 256, 2 layers, 4/2 heads, hd 64, SwiGLU 768, vocab 1024): 16 prompt tokens
+fed as sequential decode, then 16 greedy steps, teacher-forced with the oracle's tokens (a
+legitimate near-tie flip cannot derail later steps). Bar: logits within 2e-2 + 1e-2 |ref|, and
+the greedy token equal to the oracle's wherever the top-2 margin exceeds that tolerance.
+"""
+import numpy as np
+import pytest
+import torch
+
+import ql_inputs
+from oracle import decode
+
+from gpu_util import lib, dev
+
+pytestmark = pytest.mark.gpu
+
+CFG = ql_inputs.TINY
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    lib()
+    from quantized_transformer_decode_ql_gb300.model import DeviceModel
+    w = ql_inputs.weights(CFG, seed=0)
+    gm = DeviceModel(CFG, w, num_blocks=64, max_batch=8, max_blocks_per_seq=4)
+    om = decode.Q4Model(CFG, w)
+    yield gm, om
+    gm.close()
+
+
+def slot_tables(B, maxb, seed=5, num_blocks=64):
+    ids = ql_inputs.fragmented_block_ids(num_blocks, seed=seed)
+    return ids[: B * maxb].reshape(B, maxb).copy()
+
+
+def test_tiny_teacher_forced_32_steps(tiny):
+    gm, om = tiny
+    prompt = ql_inputs.prompt_tokens(16, CFG.vocab, seed=1)
+    cache = decode.KVCache(CFG, 1, 32)
+    bt = dev(slot_tables(1, 4))
+    tokens = torch.zeros(1, dtype=torch.int32, device="cuda")
+    positions = torch.zeros(1, dtype=torch.int32, device="cuda")
+    nxt = torch.zeros(1, dtype=torch.int32, device="cuda")
+    logits = torch.zeros((1, CFG.vocab), dtype=torch.float32, device="cuda")
+    args = gm.step_args(tokens, positions, bt, nxt, logits=logits)
+    tok = int(prompt[0])
+    agreed = 0
+    for step in range(32):
+        want = decode.decode_step(om, cache, [tok], [step])[0]
+        tokens.fill_(tok)
+        gm.ql_decode_step(args)
+        torch.cuda.synchronize()
+        got = logits.cpu().numpy()[0].astype(np.float64)
+        ok = decode.logits_close(got, want)
+        assert ok.all(), f"step {step}: {np.sum(~ok)} logits off, max err {np.abs(got - want).max():.3e}"
+        assert int(positions.item()) == step + 1
+        g_tok = int(nxt.item())
+        o_tok = int(decode.greedy(want))
+        if decode.greedy_must_agree(want):
+            assert g_tok == o_tok, f"step {step}"
+            agreed += 1
+        tok = int(prompt[step + 1]) if step + 1 < 16 else o_tok
+    gm.ql_check_device_error()
+    assert agreed >= 24
+
+
+def test_graph_replay_equals_eager(tiny):
+    gm, _ = tiny
+    B = 3
+    start = ql_inputs.prompt_tokens(B, CFG.vocab, seed=9)
+    runs = []
+    for mode in ("eager", "graph"):
+        tokens = dev(start.astype(np.int32))
+        positions = torch.zeros(B, dtype=torch.int32, device="cuda")
+        out = torch.full((B, 64), -1, dtype=torch.int32, device="cuda")
+        bt = dev(slot_tables(B, 4, seed=21))
+        logits = torch.zeros((B, CFG.vocab), dtype=torch.float32, device="cuda")
+        args = gm.step_args(tokens, positions, bt, tokens, logits=logits, out_tokens=out)
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            if mode == "eager":
+                for _ in range(12):
+                    gm.ql_decode_step(args, s)
+            else:
+                gm.ql_decode_graph_capture(args, s)   # captured, not executed
+                gm.ql_decode_graph_replay(B, 12, s)
+        s.synchronize()
+        runs.append((out.cpu().numpy(), logits.cpu().numpy(), positions.cpu().numpy()))
+    assert np.array_equal(runs[0][0], runs[1][0])
+    assert np.array_equal(runs[0][1], runs[1][1])
+    assert np.all(runs[0][2] == 12)
+    assert np.all(runs[0][0][:, 1:13] >= 0)
+
+
+def test_identical_slots_equal_batch_one(tiny):
+    gm, om = tiny
+    tok0 = int(ql_inputs.prompt_tokens(1, CFG.vocab, seed=3)[0])
+    res = {}
+    for B in (1, 4):
+        tokens = torch.full((B,), tok0, dtype=torch.int32, device="cuda")
+        positions = torch.zeros(B, dtype=torch.int32, device="cuda")
+        bt = dev(slot_tables(B, 4, seed=31))
+        logits = torch.zeros((B, CFG.vocab), dtype=torch.float32, device="cuda")
+        args = gm.step_args(tokens, positions, bt, tokens, logits=logits)
+        for _ in range(5):
+            gm.ql_decode_step(args)
+        torch.cuda.synchronize()
+        res[B] = logits.cpu().numpy()
+    for b in range(4):
+        assert np.array_equal(res[4][b], res[4][0])
+    np.testing.assert_allclose(res[4][0], res[1][0], rtol=1e-5, atol=1e-5)
+
+
+def test_inactive_slot_is_frozen(tiny):
+    gm, _ = tiny
+    B = 2
+    tokens = dev(np.array([5, 7], np.int32))
+    positions = dev(np.array([0, 3], np.int32))
+    active = dev(np.array([1, 0], np.int32))
+    bt_np = slot_tables(B, 4, seed=41)
+    bt = dev(bt_np)
+    before = gm.k_pool[:, bt_np[1]].clone()
+    args = gm.step_args(tokens, positions, bt, tokens, active=active)
+    gm.ql_decode_step(args)
+    torch.cuda.synchronize()
+    assert positions.cpu().tolist() == [1, 3]
+    assert int(tokens[1].item()) == 7
+    assert torch.equal(gm.k_pool[:, bt_np[1]], before)
+
+
+def test_device_error_on_bad_token_and_block(tiny):
+    ql = lib()
+    gm, _ = tiny
+    tokens = dev(np.array([CFG.vocab + 5], np.int32))
+    positions = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bt = dev(np.array([[0, 1, 2, 3]], np.int32))
+    args = gm.step_args(tokens, positions, bt, torch.zeros(1, dtype=torch.int32, device="cuda"))
+    gm.ql_decode_step(args)
+    with pytest.raises(ql.QLError) as e:
+        gm.ql_check_device_error()
+    assert e.value.status == ql.QL_EDEVICE and "vocabulary" in str(e.value)
+    gm.ql_check_device_error()          # the record is cleared once read
+    tokens.fill_(1)
+    bad_bt = dev(np.array([[9999, 1, 2, 3]], np.int32))
+    positions.fill_(0)
+    args = gm.step_args(tokens, positions, bad_bt, torch.zeros(1, dtype=torch.int32, device="cuda"))
+    gm.ql_decode_step(args)
+    with pytest.raises(ql.QLError) as e:
+        gm.ql_check_device_error()
+    assert "block id" in str(e.value)
+
+
+def test_replay_before_capture_is_an_error(tiny):
+    ql = lib()
+    gm, _ = tiny
+    with pytest.raises(ql.QLError) as e:
+        gm.ql_decode_graph_replay(7, 1)
+    assert e.value.status == ql.QL_ESTATE
