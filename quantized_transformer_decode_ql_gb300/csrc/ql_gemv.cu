@@ -25,6 +25,9 @@
 // (gate | up rows), and greedy argmax over the rows (lm_head).
 #include <cuda_fp16.h>
 
+#include <mutex>
+#include <set>
+
 #include "ql_internal.h"
 
 namespace ql {
@@ -176,7 +179,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q4_0_kernel(KParams p, DevEr
         const size_t row_bytes = (size_t)p.nblk * 16;
         const int nr = silu_mul ? (t1 - t0) * (R / 2) : (t1 - t0) * R;
         const int r0 = silu_mul ? t0 * (R / 2) : t0 * R;
-        size_t bytes = row_bytes * (size_t)min(nr, p.rows - r0);
+        const int limit = silu_mul ? half_rows : p.rows;   // rows of one range
+        size_t bytes = row_bytes * (size_t)min(nr, limit - r0);
         bytes = bytes > 65536 ? 65536 : bytes;
         const uint8_t* a0 = p.quants + (size_t)r0 * row_bytes;
         asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a0), "r"((uint32_t)bytes)
@@ -364,18 +368,36 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q4_0_kernel(KParams p, DevEr
 
 template <int NB, int R>
 cudaError_t launch_nb(const KParams& p0, int grid, size_t smem, cudaStream_t s, bool pdl) {
-    auto* k = gemv_q4_0_kernel<NB, R>;
-    static bool configured = false;   // per-instantiation; attribute is per function
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kMaxStageBytes);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
-    return launch(k, dim3(grid), dim3(kThreads), smem, s, pdl, p0, device_error_record());
+    return launch(gemv_q4_0_kernel<NB, R>, dim3(grid), dim3(kThreads), smem, s, pdl, p0,
+                  device_error_record());
+}
+
+template <int NB, int R>
+cudaError_t allow_smem() {
+    return cudaFuncSetAttribute(gemv_q4_0_kernel<NB, R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kMaxStageBytes);
 }
 
 }  // namespace
+
+// Kernel attributes are set once per device, outside any stream capture.
+int gemv_prepare() {
+    static std::mutex mu;
+    static std::set<int> done;
+    int dev = 0;
+    QL_TRY_CUDA(cudaGetDevice(&dev));
+    std::lock_guard<std::mutex> lk(mu);
+    if (done.count(dev)) return QL_OK;
+    cudaError_t e = allow_smem<1, 4>();
+    if (e == cudaSuccess) e = allow_smem<2, 4>();
+    if (e == cudaSuccess) e = allow_smem<1, 2>();
+    if (e == cudaSuccess) e = allow_smem<2, 2>();
+    if (e == cudaSuccess) e = allow_smem<4, 2>();
+    if (e == cudaSuccess) e = allow_smem<8, 2>();
+    if (e != cudaSuccess) return cuda_error(e, "gemv: cudaFuncSetAttribute");
+    done.insert(dev);
+    return QL_OK;
+}
 
 int gemv_launch(const GemvArgs& a, cudaStream_t s, bool pdl) {
     QL_REQUIRE(a.scales && a.quants && a.y, "gemv: null pointer");
@@ -390,6 +412,7 @@ int gemv_launch(const GemvArgs& a, cudaStream_t s, bool pdl) {
     QL_REQUIRE(a.y_dtype == QL_DTYPE_F32 || a.y_dtype == QL_DTYPE_F16, "gemv: bad y dtype");
     QL_REQUIRE(a.epilogue != kEpiArgmax || a.y_dtype == QL_DTYPE_F32, "gemv: argmax logits are f32");
     if (!device_error_record()) return set_error(QL_ECUDA, "gemv: no device error record");
+    if (int rc = gemv_prepare()) return rc;
 
     const int nblk = (int)(a.cols / 32);
     const size_t col_bytes = (size_t)nblk * 64;

@@ -112,6 +112,7 @@ struct GemvArgs {
     const int32_t* active;      // optional, kEpiArgmax: inactive columns skip the argmax
 };
 int gemv_launch(const GemvArgs& a, cudaStream_t s, bool pdl);
+int gemv_prepare();   // per-device kernel attributes; call outside stream capture
 
 // ---------------------------------------------------------------- attention (internal)
 struct AttnArgs {

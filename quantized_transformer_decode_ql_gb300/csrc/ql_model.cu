@@ -285,6 +285,7 @@ extern "C" int ql_model_create(const ql_model_desc* desc, ql_model** out) {
         QL_REQUIRE(check_matrix(L.down, d.hidden, d.intermediate), "ql_model_create: down must be [hidden, inter]" + li);
     }
     if (!device_error_record()) return set_error(QL_ECUDA, "ql_model_create: cannot allocate the device error record");
+    if (int rc0 = gemv_prepare()) return rc0;
 
     ql_model* m = new (std::nothrow) ql_model();
     if (!m) return set_error(QL_ENOMEM, "ql_model_create: out of host memory");
@@ -305,8 +306,12 @@ extern "C" int ql_model_create(const ql_model_desc* desc, ql_model** out) {
     A((void**)&m->keys, B * 8);
     A((void**)&m->cos_t, max_pos * (d.head_dim / 2) * 4);
     A((void**)&m->sin_t, max_pos * (d.head_dim / 2) * 4);
-    m->attn_ws_bytes = attn_workspace_bytes(B, (int)d.n_heads, (int)d.n_kv_heads, (int)d.head_dim,
-                                            d.block_size, d.max_blocks_per_seq);
+    // the split layout depends on the step's batch: size for the largest over 1..max_batch
+    for (int64_t b = 1; b <= B; ++b) {
+        const size_t need = attn_workspace_bytes(b, (int)d.n_heads, (int)d.n_kv_heads, (int)d.head_dim,
+                                                 d.block_size, d.max_blocks_per_seq);
+        if (need > m->attn_ws_bytes) m->attn_ws_bytes = need;
+    }
     A(&m->attn_ws, m->attn_ws_bytes);
     if (rc == QL_OK) {
         std::vector<float> hc(max_pos * (d.head_dim / 2)), hs(hc.size());
