@@ -394,6 +394,107 @@ def reference_arm(args, rank, world):
     }
 
 
+# ----------------------------------------------------------------------------- kernel microbenchmarks
+def micro_gemv(shapes, batches, iters):
+    """q4_0 GEMV alone on the projection shapes; rotates weight copies totalling > 3x L2."""
+    import torch
+    from quantized_transformer_decode_ql_gb300 import build as qbuild
+    qbuild.build()
+    import quantized_transformer_decode_ql_gb300 as ql
+    from quantized_transformer_decode_ql_gb300.model import Q4Tensor
+    peak, src = load_peaks()
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    s = torch.cuda.Stream()
+    g = torch.Generator(device="cuda")
+    g.manual_seed(2)
+    out = []
+    for rows, cols in shapes:
+        one = rows * cols * 18 // 32
+        copies = max(1, min(64, -(-3 * l2 // one)))
+        Ws = []
+        for c in range(copies):
+            w = torch.randn((rows, cols), generator=g, device="cuda").mul_(0.02)
+            Ws.append(Q4Tensor.pack(w))
+            del w
+        for B in batches:
+            x = torch.randn((B, cols), generator=g, device="cuda").half()
+            y = torch.empty((B, rows), dtype=torch.float32, device="cuda")
+
+            def run(n):
+                for i in range(n):
+                    W = Ws[i % copies]
+                    ql.ql_gemv_q4_0(W.scales, W.quants, rows, cols, x, B, y, 0, 0, None, s)
+            with torch.cuda.stream(s):
+                run(max(copies, 8))
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                n = max(iters, copies)
+                e0.record(s)
+                run(n)
+                e1.record(s)
+            s.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / n
+            nbytes = one + B * cols * 2 + B * rows * 4
+            gbs = nbytes / (us * 1e-6) / 1e9
+            out.append({"kernel": "ql_gemv_q4_0", "rows": rows, "cols": cols, "batch": B,
+                        "us": round(us, 2), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
+                        "peak": peak, "peak_source": src, "copies": copies})
+            print(json.dumps(out[-1]), flush=True)
+        del Ws
+    return out
+
+
+def micro_attn(batches, iters):
+    """Paged GQA decode attention alone: 32/8 heads, hd 128, lengths uniform in [512, 32768]."""
+    import torch
+    from quantized_transformer_decode_ql_gb300 import build as qbuild
+    qbuild.build()
+    import quantized_transformer_decode_ql_gb300 as ql
+    peak, src = load_peaks()
+    nh, nkv, hd = 32, 8, 128
+    s = torch.cuda.Stream()
+    g = torch.Generator(device="cuda")
+    g.manual_seed(4)
+    for B in batches:
+        lens = ql_inputs.batched_lengths(B, 512, 32768, seed=6)
+        nblk = [(int(L) + 15) // 16 for L in lens]
+        maxb = max(nblk)
+        num_blocks = sum(nblk)
+        perm = torch.from_numpy(ql_inputs.fragmented_block_ids(num_blocks, seed=5)).cuda()
+        bt = torch.full((B, maxb), -1, dtype=torch.int32, device="cuda")
+        off = 0
+        for b, n in enumerate(nblk):
+            bt[b, :n] = perm[off:off + n]
+            off += n
+        kp = torch.randn((num_blocks, nkv, 16, hd), generator=g, device="cuda").half()
+        vp = torch.randn((num_blocks, nkv, 16, hd), generator=g, device="cuda").half()
+        q = torch.randn((B, nh, hd), generator=g, device="cuda").half()
+        o = torch.empty((B, nh * hd), dtype=torch.float16, device="cuda")
+        cl = torch.from_numpy(lens).cuda()
+        ws = torch.zeros(ql.ql_paged_attn_workspace_bytes(B, nh, nkv, hd, 16, maxb), dtype=torch.uint8, device="cuda")
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+
+        def run():
+            ql.ql_paged_attn_decode(q, kp, vp, bt, cl, B, nh, nkv, hd, 16, maxb, num_blocks,
+                                    1 / math.sqrt(hd), o, ws, s)
+        times = []
+        with torch.cuda.stream(s):
+            run()
+            for _ in range(iters):
+                flush.fill_(1)          # evict the KV from L2 between launches
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(s)
+                run()
+                e1.record(s)
+                times.append((e0, e1))
+        s.synchronize()
+        us = statistics.median(a.elapsed_time(b) for a, b in times) * 1e3
+        nbytes = sum(2 * int(L) * nkv * hd * 2 + 4 * ((int(L) + 15) // 16) for L in lens) + B * nh * hd * 4
+        gbs = nbytes / (us * 1e-6) / 1e9
+        print(json.dumps({"kernel": "ql_paged_attn_decode", "batch": B, "sum_len": int(lens.sum()),
+                          "us": round(us, 2), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
+                          "peak": peak, "peak_source": src}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -402,7 +503,20 @@ def main():
     ap.add_argument("--impl", default="ql", choices=["ql", "reference"])
     ap.add_argument("--config", default="e1", choices=["e1"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--micro", choices=["gemv", "attn"], help="time one kernel family alone")
+    ap.add_argument("--shape", default=None, help="micro gemv: ROWSxCOLS (default: all shapes)")
+    ap.add_argument("--batch", default=None, help="micro: comma-separated batch sizes")
+    ap.add_argument("--iters", type=int, default=50)
     args = ap.parse_args()
+    if args.micro == "gemv":
+        shapes = [tuple(int(v) for v in args.shape.split("x"))] if args.shape else ql_inputs.GEMV_SHAPES
+        batches = [int(b) for b in args.batch.split(",")] if args.batch else [1, 4, 16, 64]
+        micro_gemv(shapes, batches, args.iters)
+        return
+    if args.micro == "attn":
+        batches = [int(b) for b in args.batch.split(",")] if args.batch else [1, 2, 4, 8, 16, 32, 64]
+        micro_attn(batches, args.iters)
+        return
     rank, world, local_rank = dist_env()
     if world > 1:
         import torch

@@ -30,6 +30,7 @@ namespace {
 constexpr int kAttnWarps = 4;
 constexpr int kAttnThreads = kAttnWarps * 32;
 constexpr int kBS = 16;   // tokens per KV block
+constexpr int kMaxSplit = 256;   // splits per (sequence, kv head), bounded by the host
 
 struct AParams {
     const __half* q;
@@ -48,6 +49,7 @@ struct AParams {
     float* pl;
     float* pacc;        // [batch][n_heads][nsplit][HD]
     int nsplit, spb;
+    int prefetch;       // warm L2 with this CTA's K/V tiles before waiting on the predecessor
 };
 
 __device__ __forceinline__ float2 h2f(uint32_t u) {
@@ -68,6 +70,21 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AParams p, Dev
 
     const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (p.prefetch && (p.active == nullptr || p.active[b] != 0)) {
+        // In the decode step the context length comes from the position, which is final before
+        // this kernel starts; only the newest slot is still being written (prefetch is a hint).
+        const int Lp = p.positions[b] + 1;
+        const int b0 = s * p.spb, b1 = min((Lp + kBS - 1) / kBS, b0 + p.spb);
+        if (Lp <= p.maxb * kBS && (int)threadIdx.x < 2 * (b1 - b0) && b0 < b1) {
+            const int blk = b0 + (threadIdx.x >> 1);
+            const int phys = p.block_tables[(size_t)b * p.maxb + blk];
+            if (phys >= 0 && phys < p.num_blocks) {
+                const __half* base = (threadIdx.x & 1) ? p.v_pool : p.k_pool;
+                const __half* t = base + ((size_t)phys * p.n_kv + g) * kBS * HD;
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(t), "r"((uint32_t)(kBS * HD * 2)) : "memory");
+            }
+        }
+    }
     pdl_wait();
     pdl_trigger();
     if (p.active && p.active[b] == 0) return;
@@ -238,19 +255,54 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AParams p, Dev
     __syncthreads();
     if (!last_flag) return;
     __threadfence();
-    for (int i = threadIdx.x; i < G * HD; i += kAttnThreads) {
-        const int h = i / HD, d = i - h * HD;
-        const int hg = g * G + h;
-        const size_t base = ((size_t)b * n_heads + hg) * p.nsplit;
+    // merge: per-split weights exp2(m_k - M) / L into shared memory (one warp per head), then
+    // every thread sums float4 chunks of the partial outputs with independent loads
+    __shared__ float sw[G][kMaxSplit];
+    for (int h = warp; h < G; h += kAttnWarps) {
+        const size_t base = ((size_t)b * n_heads + g * G + h) * p.nsplit;
         float M = -INFINITY;
-        for (int k = 0; k < n_active; ++k) M = fmaxf(M, __ldcg(p.pm + base + k));
-        float Ls = 0.f, A = 0.f;
-        for (int k = 0; k < n_active; ++k) {
+        for (int k = lane; k < n_active; k += 32) M = fmaxf(M, __ldcg(p.pm + base + k));
+#pragma unroll
+        for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float Ls = 0.f;
+        for (int k = lane; k < n_active; k += 32) {
             const float f = exp2f(__ldcg(p.pm + base + k) - M);
-            Ls += __ldcg(p.pl + base + k) * f;
-            A += __ldcg(p.pacc + (base + k) * HD + d) * f;
+            sw[h][k] = f;
+            Ls += f * __ldcg(p.pl + base + k);
         }
-        p.out[((size_t)b * n_heads + hg) * HD + d] = __float2half_rn(A / Ls);
+#pragma unroll
+        for (int o = 16; o; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
+        const float inv = 1.0f / Ls;
+        __syncwarp();
+        for (int k = lane; k < n_active; k += 32) sw[h][k] *= inv;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < G * HD / 4; i += kAttnThreads) {
+        const int h = i / (HD / 4), d4 = i - h * (HD / 4);
+        const size_t base = ((size_t)b * n_heads + g * G + h) * p.nsplit;
+        const float4* src = reinterpret_cast<const float4*>(p.pacc) + base * (HD / 4) + d4;
+        float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+        int k = 0;
+        for (; k + 8 <= n_active; k += 8) {
+            float4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = __ldcg(src + (size_t)(k + u) * (HD / 4));
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const float w = sw[h][k + u];
+                A.x = fmaf(w, v[u].x, A.x); A.y = fmaf(w, v[u].y, A.y);
+                A.z = fmaf(w, v[u].z, A.z); A.w = fmaf(w, v[u].w, A.w);
+            }
+        }
+        for (; k < n_active; ++k) {
+            const float4 v = __ldcg(src + (size_t)k * (HD / 4));
+            const float w = sw[h][k];
+            A.x = fmaf(w, v.x, A.x); A.y = fmaf(w, v.y, A.y);
+            A.z = fmaf(w, v.z, A.z); A.w = fmaf(w, v.w, A.w);
+        }
+        __half* o = p.out + ((size_t)b * n_heads + g * G + h) * HD + d4 * 4;
+        *reinterpret_cast<__half2*>(o) = __floats2half2_rn(A.x, A.y);
+        *reinterpret_cast<__half2*>(o + 2) = __floats2half2_rn(A.z, A.w);
     }
     if (threadIdx.x == 0) p.tickets[b * p.n_kv + g] = 0;   // re-arm for the next call
 }
@@ -269,6 +321,7 @@ Layout layout(int64_t batch, int n_heads, int n_kv, int head_dim, int64_t maxb, 
     if (spb < 4) spb = 4;
     if (spb > maxb) spb = maxb;
     if (spb < 1) spb = 1;
+    if ((maxb + spb - 1) / spb > kMaxSplit) spb = (maxb + kMaxSplit - 1) / kMaxSplit;
     lo.spb = (int)spb;
     lo.nsplit = (int)((maxb + spb - 1) / spb);
     auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
@@ -351,6 +404,7 @@ int attn_launch(const AttnArgs& a, cudaStream_t s, bool pdl) {
     p.pacc = reinterpret_cast<float*>(ws + lo.pacc_off);
     p.nsplit = lo.nsplit;
     p.spb = lo.spb;
+    p.prefetch = a.context_lens == nullptr ? 1 : 0;
     cudaError_t e = a.head_dim == 128 ? launch_h<128>(p, G, a.batch, s, pdl)
                                       : launch_h<64>(p, G, a.batch, s, pdl);
     if (e != cudaSuccess) return cuda_error(e, "attention launch");

@@ -161,6 +161,75 @@ __device__ void stage_x(const KParams& p, uint4* xs, float* red) {
     }
 }
 
+// Reduce a task's per-lane partial sums over the warp and apply the epilogue.
+template <int NB, int R>
+__device__ __forceinline__ void epilogue_task(const KParams& p, int t, float (&acc)[R][NB], int lane,
+                                              bool silu_mul, int half_rows,
+                                              unsigned long long (&best)[NB]) {
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int b = 0; b < NB; ++b)
+#pragma unroll
+            for (int o = 16; o; o >>= 1) acc[r][b] += __shfl_xor_sync(0xffffffffu, acc[r][b], o);
+    int row[R];
+    bool ok[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        if (silu_mul) {
+            const int i = t * (R / 2) + (r % (R / 2));
+            ok[r] = i < half_rows;
+            row[r] = (r < R / 2) ? i : half_rows + i;
+        } else {
+            row[r] = t * R + r;
+            ok[r] = row[r] < p.rows;
+        }
+    }
+    // lane l writes output number l (R * NB <= 32)
+    if (silu_mul) {
+#pragma unroll
+        for (int r = 0; r < R / 2; ++r)
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                if (lane == r * NB + b && ok[r] && b < p.batch) {
+                    const float v = silu(acc[r][b]) * acc[r + R / 2][b];
+                    const size_t o = (size_t)b * p.y_ld + row[r];
+                    if (p.y_dtype == QL_DTYPE_F16)
+                        reinterpret_cast<__half*>(p.y)[o] = __float2half_rn(v);
+                    else
+                        reinterpret_cast<float*>(p.y)[o] = v;
+                }
+            }
+    } else if (p.epilogue == kEpiArgmax) {
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                if (ok[r] && b < p.batch) {
+                    const unsigned long long k = argmax_key(acc[r][b], row[r]);
+                    best[b] = k > best[b] ? k : best[b];
+                    if (p.y && lane == r * NB + b)
+                        reinterpret_cast<float*>(p.y)[(size_t)b * p.y_ld + row[r]] = acc[r][b];
+                }
+            }
+    } else {
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                if (lane == r * NB + b && ok[r] && b < p.batch) {
+                    const size_t o = (size_t)b * p.y_ld + row[r];
+                    float v = acc[r][b];
+                    if (p.epilogue == QL_EPI_ADD_RESIDUAL) v += p.residual[o];
+                    if (p.y_dtype == QL_DTYPE_F16)
+                        reinterpret_cast<__half*>(p.y)[o] = __float2half_rn(v);
+                    else
+                        reinterpret_cast<float*>(p.y)[o] = v;
+                }
+            }
+    }
+}
+
 template <int NB, int R>
 __global__ void __launch_bounds__(kThreads, 2) gemv_q4_0_kernel(KParams p, DevError* err) {
     extern __shared__ uint4 xs[];
@@ -204,148 +273,110 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q4_0_kernel(KParams p, DevEr
 #pragma unroll
     for (int b = 0; b < NB; ++b) best[b] = 0ull;
 
-    for (int t = t0 + warp; t < t1; t += kWarps) {
-        int row[R];
-        bool ok[R];
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            if (silu_mul) {
-                const int i = t * (R / 2) + (r % (R / 2));
-                row[r] = (r < R / 2) ? i : half_rows + i;
-                ok[r] = i < half_rows;
-            } else {
-                row[r] = t * R + r;
-                ok[r] = row[r] < p.rows;
-            }
-            if (!ok[r]) row[r] = 0;
-        }
-        float acc[R][NB];
-#pragma unroll
-        for (int r = 0; r < R; ++r)
-#pragma unroll
-            for (int b = 0; b < NB; ++b) acc[r][b] = 0.f;
+    // Each warp walks a flat sequence of (task, 32-block step) iterations. The loads of the
+    // next D iterations are always in flight, across task boundaries, so every lane keeps
+    // D * R * 16 bytes of weight codes outstanding.
+    constexpr int D = NB >= 4 ? 2 : (NB == 2 && R == 4) ? 3 : 4;
+    const int njit = (p.nblk + 31) >> 5;
+    const int my_tasks = (t1 - t0 > warp) ? (t1 - t0 - warp + kWarps - 1) / kWarps : 0;
+    const int total = my_tasks * njit;
 
-        const uint4* qrow[R];
-        const __half* srow[R];
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            qrow[r] = reinterpret_cast<const uint4*>(p.quants) + (size_t)row[r] * p.nblk;
-            srow[r] = p.scales + (size_t)row[r] * p.nblk;
-        }
-        uint4 qc[R];
-        __half sc[R];
-        int j = lane;
-        if (j < p.nblk) {
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                qc[r] = ok[r] ? __ldg(qrow[r] + j) : make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
-                sc[r] = ok[r] ? srow[r][j] : __float2half(0.f);
-            }
-        }
-        for (; j < p.nblk; j += 32) {
-            uint4 qn[R];
-            __half sn[R];
-            const int jn = j + 32;
-            if (jn < p.nblk) {
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    qn[r] = ok[r] ? __ldg(qrow[r] + jn) : make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
-                    sn[r] = ok[r] ? srow[r][jn] : __float2half(0.f);
-                }
-            }
-            __half2 a[R][NB];
-#pragma unroll
-            for (int r = 0; r < R; ++r)
-#pragma unroll
-                for (int b = 0; b < NB; ++b) a[r][b] = __float2half2_rn(0.f);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                uint4 X[NB];
-#pragma unroll
-                for (int b = 0; b < NB; ++b) X[b] = xs[b * nchunk + xslot(j, i)];
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    const uint32_t w = (i == 0) ? qc[r].x : (i == 1) ? qc[r].y : (i == 2) ? qc[r].z : qc[r].w;
-                    const uint32_t s8 = w >> 8;
-                    const __half2 lo0 = __hsub2(h2((w & 0x000F000Fu) | 0x64006400u), k1032);
-                    const __half2 hi0 = __hsub2(h2((w & 0x00F000F0u) | 0x64006400u), k1152);
-                    const __half2 lo1 = __hsub2(h2((s8 & 0x000F000Fu) | 0x64006400u), k1032);
-                    const __half2 hi1 = __hsub2(h2((s8 & 0x00F000F0u) | 0x64006400u), k1152);
-#pragma unroll
-                    for (int b = 0; b < NB; ++b) {
-                        a[r][b] = __hfma2(lo0, h2(X[b].x), a[r][b]);
-                        a[r][b] = __hfma2(lo1, h2(X[b].y), a[r][b]);
-                        a[r][b] = __hfma2(hi0, h2(X[b].z), a[r][b]);
-                        a[r][b] = __hfma2(hi1, h2(X[b].w), a[r][b]);
-                    }
-                }
-            }
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const float d = __half2float(sc[r]);
-#pragma unroll
-                for (int b = 0; b < NB; ++b) {
-                    const float2 f = __half22float2(a[r][b]);
-                    acc[r][b] = fmaf(d, f.x + f.y, acc[r][b]);
-                }
-            }
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                qc[r] = qn[r];
-                sc[r] = sn[r];
-            }
-        }
-        // reduce over the 32 lanes (every lane ends with every sum)
-#pragma unroll
-        for (int r = 0; r < R; ++r)
-#pragma unroll
-            for (int b = 0; b < NB; ++b)
-#pragma unroll
-                for (int o = 16; o; o >>= 1)
-                    acc[r][b] += __shfl_xor_sync(0xffffffffu, acc[r][b], o);
-
-        // epilogue: lane l writes output number l (R * NB <= 32)
+    auto row_of = [&](int t, int r, bool& ok) -> int {
         if (silu_mul) {
+            const int i = t * (R / 2) + (r % (R / 2));
+            ok = i < half_rows;
+            return ok ? ((r < R / 2) ? i : half_rows + i) : 0;
+        }
+        const int rr = t * R + r;
+        ok = rr < p.rows;
+        return ok ? rr : 0;
+    };
+    auto load = [&](int it, uint4 (&qv)[R], __half (&sv)[R]) {
+        const int t = t0 + warp + (it / njit) * kWarps;
+        const int j = (it % njit) * 32 + lane;
 #pragma unroll
-            for (int r = 0; r < R / 2; ++r)
+        for (int r = 0; r < R; ++r) {
+            bool ok;
+            const int row = row_of(t, r, ok);
+            if (ok && j < p.nblk) {
+                const size_t o = (size_t)row * p.nblk + j;
+                qv[r] = __ldg(reinterpret_cast<const uint4*>(p.quants) + o);
+                sv[r] = p.scales[o];
+            } else {
+                qv[r] = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
+                sv[r] = __float2half(0.f);
+            }
+        }
+    };
+
+    uint4 ring[D][R];
+    __half sring[D][R];
 #pragma unroll
-                for (int b = 0; b < NB; ++b) {
-                    if (lane == r * NB + b && ok[r] && b < p.batch) {
-                        const float v = silu(acc[r][b]) * acc[r + R / 2][b];
-                        const size_t o = (size_t)b * p.y_ld + row[r];
-                        if (p.y_dtype == QL_DTYPE_F16)
-                            reinterpret_cast<__half*>(p.y)[o] = __float2half_rn(v);
-                        else
-                            reinterpret_cast<float*>(p.y)[o] = v;
+    for (int u = 0; u < D; ++u)
+        if (u < total) load(u, ring[u], sring[u]);
+
+    float acc[R][NB];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int b = 0; b < NB; ++b) acc[r][b] = 0.f;
+
+    for (int it0 = 0; it0 < total; it0 += D) {
+#pragma unroll
+        for (int u = 0; u < D; ++u) {
+            const int it = it0 + u;
+            if (it < total) {
+                const int jstep = it % njit;
+                const int j = jstep * 32 + lane;
+                if (j < p.nblk) {
+                    __half2 a[R][NB];
+#pragma unroll
+                    for (int r = 0; r < R; ++r)
+#pragma unroll
+                        for (int b = 0; b < NB; ++b) a[r][b] = __float2half2_rn(0.f);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint4 X[NB];
+#pragma unroll
+                        for (int b = 0; b < NB; ++b) X[b] = xs[b * nchunk + xslot(j, i)];
+#pragma unroll
+                        for (int r = 0; r < R; ++r) {
+                            const uint4 qv = ring[u][r];
+                            const uint32_t w = (i == 0) ? qv.x : (i == 1) ? qv.y : (i == 2) ? qv.z : qv.w;
+                            const uint32_t s8 = w >> 8;
+                            const __half2 lo0 = __hsub2(h2((w & 0x000F000Fu) | 0x64006400u), k1032);
+                            const __half2 hi0 = __hsub2(h2((w & 0x00F000F0u) | 0x64006400u), k1152);
+                            const __half2 lo1 = __hsub2(h2((s8 & 0x000F000Fu) | 0x64006400u), k1032);
+                            const __half2 hi1 = __hsub2(h2((s8 & 0x00F000F0u) | 0x64006400u), k1152);
+#pragma unroll
+                            for (int b = 0; b < NB; ++b) {
+                                a[r][b] = __hfma2(lo0, h2(X[b].x), a[r][b]);
+                                a[r][b] = __hfma2(lo1, h2(X[b].y), a[r][b]);
+                                a[r][b] = __hfma2(hi0, h2(X[b].z), a[r][b]);
+                                a[r][b] = __hfma2(hi1, h2(X[b].w), a[r][b]);
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        const float d = __half2float(sring[u][r]);
+#pragma unroll
+                        for (int b = 0; b < NB; ++b) {
+                            const float2 f = __half22float2(a[r][b]);
+                            acc[r][b] = fmaf(d, f.x + f.y, acc[r][b]);
+                        }
                     }
                 }
-        } else if (p.epilogue == kEpiArgmax) {
+                if (it + D < total) load(it + D, ring[u], sring[u]);
+                if (jstep == njit - 1) {
+                    const int t = t0 + warp + (it / njit) * kWarps;
+                    epilogue_task<NB, R>(p, t, acc, lane, silu_mul, half_rows, best);
 #pragma unroll
-            for (int r = 0; r < R; ++r)
+                    for (int r = 0; r < R; ++r)
 #pragma unroll
-                for (int b = 0; b < NB; ++b) {
-                    if (ok[r] && b < p.batch) {
-                        const unsigned long long k = argmax_key(acc[r][b], row[r]);
-                        best[b] = k > best[b] ? k : best[b];
-                        if (p.y && lane == r * NB + b)
-                            reinterpret_cast<float*>(p.y)[(size_t)b * p.y_ld + row[r]] = acc[r][b];
-                    }
+                        for (int b = 0; b < NB; ++b) acc[r][b] = 0.f;
                 }
-        } else {
-#pragma unroll
-            for (int r = 0; r < R; ++r)
-#pragma unroll
-                for (int b = 0; b < NB; ++b) {
-                    if (lane == r * NB + b && ok[r] && b < p.batch) {
-                        const size_t o = (size_t)b * p.y_ld + row[r];
-                        float v = acc[r][b];
-                        if (p.epilogue == QL_EPI_ADD_RESIDUAL) v += p.residual[o];
-                        if (p.y_dtype == QL_DTYPE_F16)
-                            reinterpret_cast<__half*>(p.y)[o] = __float2half_rn(v);
-                        else
-                            reinterpret_cast<float*>(p.y)[o] = v;
-                    }
-                }
+            }
         }
     }
     if (p.epilogue == kEpiArgmax) {
