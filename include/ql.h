@@ -121,6 +121,26 @@ int ql_paged_attn_decode(const void* d_q, const void* d_k_pool, const void* d_v_
                          float scale, void* d_out, void* d_workspace,
                          size_t workspace_bytes, void* stream);
 
+/* The same attention without a caller-supplied workspace, for callers that cannot allocate
+ * device memory: for example a plugin inside a host application whose own pool owns all
+ * device memory, or a latency-critical loop that cannot afford cudaMalloc/cudaFree (they can
+ * synchronise the device). The pages have no counterpart; this is a library convenience.
+ * Arguments mean what they mean for ql_paged_attn_decode. The split-K scratch comes from a
+ * fixed 8 MiB array compiled into the library (held by every GPU that loads the library until
+ * the process exits); a shape whose scratch, as ql_paged_attn_workspace_bytes reports it,
+ * exceeds 8 MiB is rejected with QL_EINVAL. Nothing is allocated: the first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress) with that device current, so
+ * make that first call before any stream capture. Every call clears the part of the array
+ * that must start at zero, then shares the rest with every other call: calls whose kernels
+ * overlap on the GPU (two streams, or two host threads) race on it and must be serialised by
+ * the caller. Out-of-range block ids or lengths are skipped; they are recorded for
+ * ql_check_device_error only if another libql call already created this device's record.  */
+int ql_paged_attn_decode_noalloc(const void* d_q, const void* d_k_pool, const void* d_v_pool,
+                                 const int32_t* d_block_tables, const int32_t* d_context_lens,
+                                 int64_t batch, int n_heads, int n_kv_heads, int head_dim,
+                                 int block_size, int64_t max_blocks_per_seq, int64_t num_blocks,
+                                 float scale, void* d_out, void* stream);
+
 /* --------------------------------------------------------------- qk-norm + RoPE + KV append
  * [IL] CudaQwen3::step (qk_norm_rope kernel), [FK] decode_step / attention_paged:
  * for slot b at position p = d_positions[b]:

@@ -16,7 +16,8 @@ from ._lib import (QLError, QL_OK, QL_EINVAL, QL_ENOMEM, QL_ECUDA, QL_EPOOL, QL_
 
 __all__ = [
     "QLError", "lib", "ql_q4_0_pack", "ql_q4_0_unpack", "ql_q4_0_pack_device", "ql_gemv_q4_0",
-    "ql_paged_attn_workspace_bytes", "ql_paged_attn_decode", "ql_fused_norm_rope",
+    "ql_paged_attn_workspace_bytes", "ql_paged_attn_decode", "ql_paged_attn_decode_noalloc",
+    "ql_fused_norm_rope",
     "ql_rope_tables", "ql_check_device_error", "BlockPool", "SIGNATURES",
 ]
 
@@ -56,6 +57,17 @@ def ql_paged_attn_decode(q, k_pool, v_pool, block_tables, context_lens, batch, n
                                      block_size, max_blocks_per_seq, num_blocks, scale, ptr(out),
                                      ptr(workspace), workspace.numel() * workspace.element_size(),
                                      stream_ptr(stream)))
+
+
+def ql_paged_attn_decode_noalloc(q, k_pool, v_pool, block_tables, context_lens, batch, n_heads,
+                                 n_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks,
+                                 scale, out, stream=None):
+    """Attention whose split-K scratch is the library's fixed 8 MiB device array (no workspace
+    argument, no device allocation); see include/ql.h for its limits."""
+    check(lib().ql_paged_attn_decode_noalloc(ptr(q), ptr(k_pool), ptr(v_pool), ptr(block_tables),
+                                             ptr(context_lens), batch, n_heads, n_kv_heads,
+                                             head_dim, block_size, max_blocks_per_seq, num_blocks,
+                                             scale, ptr(out), stream_ptr(stream)))
 
 
 def ql_fused_norm_rope(qkv, q_norm, k_norm, cos_t, sin_t, positions, active, eps, batch, n_heads,

@@ -64,6 +64,9 @@ SIGNATURES = {
     "ql_paged_attn_decode": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int64,
                                      c_int, c_int, c_int, c_int, c_int64, c_int64, c_float,
                                      c_void_p, c_void_p, c_size_t, c_void_p]),
+    "ql_paged_attn_decode_noalloc": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                             c_int64, c_int, c_int, c_int, c_int, c_int64, c_int64,
+                                             c_float, c_void_p, c_void_p]),
     "ql_fused_norm_rope": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                    c_void_p, c_float, c_int64, c_int, c_int, c_int, c_void_p,
                                    c_void_p, c_void_p, c_void_p, c_int64, c_int, c_int64, c_int64,

@@ -448,3 +448,123 @@ extern "C" int ql_paged_attn_decode(const void* d_q, const void* d_k_pool, const
     if (batch < 1 || batch > 65535) return set_error(QL_EINVAL, "ql_paged_attn_decode: batch out of range");
     return attn_launch(a, static_cast<cudaStream_t>(stream), true);
 }
+
+// ------------------------------------------------------------------ no-allocation variant
+// Some callers cannot allocate device memory for the split-K workspace: a plugin running
+// inside a host application that owns every byte of device memory through its own pool (a raw
+// cudaMalloc would bypass that pool's accounting or exceed its budget), or a latency-critical
+// loop that must not pay for cudaMalloc / cudaFree, which can synchronise the whole device.
+// ql_paged_attn_decode_noalloc serves them from a fixed scratch array that lives in the
+// library image itself; every GPU that loads the library holds it until the process exits.
+#include <map>
+#include <mutex>
+
+namespace ql {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = (size_t)8 << 20;   // 8 MiB per device
+static __device__ __align__(256) unsigned char g_attn_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+std::map<int, void*> g_noalloc_addr;
+
+// Device address of the scratch array on the current device. In host code the array's name is
+// only a host-side stand-in, so the address is looked up once per device, with that device
+// current, and cached.
+int noalloc_scratch_address(void** out) {
+    int dev = 0;
+    QL_TRY_CUDA(cudaGetDevice(&dev));
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    auto it = g_noalloc_addr.find(dev);
+    if (it == g_noalloc_addr.end()) {
+        void* p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_attn_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_error(e, "ql_paged_attn_decode_noalloc: cudaGetSymbolAddress");
+        it = g_noalloc_addr.emplace(dev, p).first;
+    }
+    *out = it->second;
+    return QL_OK;
+}
+
+template <int HD, int G>
+cudaError_t launch_hg_err(const AParams& p, int batch, cudaStream_t s, DevError* err) {
+    dim3 grid(p.nsplit, p.n_kv, batch);
+    return launch(attn_split_kernel<HD, G>, grid, dim3(kAttnThreads), 0, s, true, p, err);
+}
+
+template <int HD>
+cudaError_t launch_h_err(const AParams& p, int G, int batch, cudaStream_t s, DevError* err) {
+    switch (G) {
+        case 1: return launch_hg_err<HD, 1>(p, batch, s, err);
+        case 2: return launch_hg_err<HD, 2>(p, batch, s, err);
+        case 4: return launch_hg_err<HD, 4>(p, batch, s, err);
+        case 8: return launch_hg_err<HD, 8>(p, batch, s, err);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+}  // namespace ql
+
+extern "C" int ql_paged_attn_decode_noalloc(const void* d_q, const void* d_k_pool, const void* d_v_pool,
+                                            const int32_t* d_block_tables,
+                                            const int32_t* d_context_lens, int64_t batch,
+                                            int n_heads, int n_kv_heads, int head_dim,
+                                            int block_size, int64_t max_blocks_per_seq,
+                                            int64_t num_blocks, float scale, void* d_out,
+                                            void* stream) {
+    using namespace ql;
+    QL_REQUIRE(d_q && d_k_pool && d_v_pool && d_block_tables && d_context_lens && d_out,
+               "ql_paged_attn_decode_noalloc: null pointer");
+    QL_REQUIRE(head_dim == 64 || head_dim == 128, "ql_paged_attn_decode_noalloc: head_dim must be 64 or 128");
+    QL_REQUIRE(block_size == kBS, "ql_paged_attn_decode_noalloc: block_size must be 16");
+    QL_REQUIRE(n_kv_heads > 0 && n_heads > 0 && n_heads % n_kv_heads == 0,
+               "ql_paged_attn_decode_noalloc: n_heads % n_kv_heads != 0");
+    const int G = n_heads / n_kv_heads;
+    QL_REQUIRE(G == 1 || G == 2 || G == 4 || G == 8, "ql_paged_attn_decode_noalloc: GQA group must be 1, 2, 4 or 8");
+    QL_REQUIRE(batch >= 1 && batch <= 65535, "ql_paged_attn_decode_noalloc: batch out of range");
+    QL_REQUIRE(max_blocks_per_seq >= 1 && max_blocks_per_seq * kBS < (1ll << 31),
+               "ql_paged_attn_decode_noalloc: bad max_blocks_per_seq");
+    QL_REQUIRE(num_blocks >= 1, "ql_paged_attn_decode_noalloc: bad num_blocks");
+    const Layout lo = layout(batch, n_heads, n_kv_heads, head_dim, max_blocks_per_seq, num_sms());
+    if (lo.total > kNoAllocScratchBytes)
+        return set_error(QL_EINVAL, "ql_paged_attn_decode_noalloc: this shape needs " +
+                                        std::to_string(lo.total) + " bytes of split-K scratch, more than the " +
+                                        std::to_string(kNoAllocScratchBytes) +
+                                        " bytes built into the library; use ql_paged_attn_decode with a workspace");
+    void* scratch = nullptr;
+    if (int rc = noalloc_scratch_address(&scratch)) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the split tickets must start at zero; the array keeps whatever the last call left
+    QL_TRY_CUDA(cudaMemsetAsync(static_cast<char*>(scratch) + lo.tickets_off, 0,
+                                (size_t)batch * n_kv_heads * sizeof(int), s));
+    AParams p = {};
+    p.q = static_cast<const __half*>(d_q);
+    p.k_pool = static_cast<const __half*>(d_k_pool);
+    p.v_pool = static_cast<const __half*>(d_v_pool);
+    p.block_tables = d_block_tables;
+    p.context_lens = d_context_lens;
+    p.positions = nullptr;
+    p.active = nullptr;
+    p.n_heads = n_heads;
+    p.n_kv = n_kv_heads;
+    p.maxb = (int)max_blocks_per_seq;
+    p.num_blocks = num_blocks;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.out = static_cast<__half*>(d_out);
+    char* ws = static_cast<char*>(scratch);
+    p.tickets = reinterpret_cast<int*>(ws + lo.tickets_off);
+    p.pm = reinterpret_cast<float*>(ws + lo.pm_off);
+    p.pl = reinterpret_cast<float*>(ws + lo.pl_off);
+    p.pacc = reinterpret_cast<float*>(ws + lo.pacc_off);
+    p.nsplit = lo.nsplit;
+    p.spb = lo.spb;
+    p.prefetch = 0;
+    // out-of-range indices are skipped; they are recorded only if this device already has an
+    // error record (this path never creates one, since that would allocate)
+    DevError* err = device_error_record_existing();
+    const cudaError_t e = head_dim == 128 ? launch_h_err<128>(p, G, (int)batch, s, err)
+                                          : launch_h_err<64>(p, G, (int)batch, s, err);
+    if (e != cudaSuccess) return cuda_error(e, "ql_paged_attn_decode_noalloc launch");
+    return QL_OK;
+}

@@ -48,6 +48,14 @@ DevError* device_error_record() {
     return p;
 }
 
+DevError* device_error_record_existing() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    auto it = g_dev_err.find(dev);
+    return it == g_dev_err.end() ? nullptr : it->second;
+}
+
 int num_sms() {
     int dev = 0;
     cudaGetDevice(&dev);

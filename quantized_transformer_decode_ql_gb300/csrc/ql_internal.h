@@ -46,6 +46,8 @@ enum DevErrWhere {
 };
 // The current device's record (allocated on first use, zero-filled).
 DevError* device_error_record();
+// The current device's record if one was already created, else nullptr (never allocates).
+DevError* device_error_record_existing();
 
 #ifdef __CUDACC__
 __device__ __forceinline__ void record_device_error(DevError* e, int where, long long index,
