@@ -416,6 +416,7 @@ def micro_gemv(shapes, batches, iters):
             w = torch.randn((rows, cols), generator=g, device="cuda").mul_(0.02)
             Ws.append(Q4Tensor.pack(w))
             del w
+        torch.cuda.synchronize()      # packing runs on the default stream; time nothing before it ends
         for B in batches:
             x = torch.randn((B, cols), generator=g, device="cuda").half()
             y = torch.empty((B, rows), dtype=torch.float32, device="cuda")
@@ -472,6 +473,7 @@ def micro_attn(batches, iters):
         cl = torch.from_numpy(lens).cuda()
         ws = torch.zeros(ql.ql_paged_attn_workspace_bytes(B, nh, nkv, hd, 16, maxb), dtype=torch.uint8, device="cuda")
         flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        torch.cuda.synchronize()
 
         def run():
             ql.ql_paged_attn_decode(q, kp, vp, bt, cl, B, nh, nkv, hd, 16, maxb, num_blocks,

@@ -291,21 +291,39 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q4_0_kernel(KParams p, DevEr
         ok = rr < p.rows;
         return ok ? rr : 0;
     };
-    auto load = [&](int it, uint4 (&qv)[R], __half (&sv)[R]) {
-        const int t = t0 + warp + (it / njit) * kWarps;
-        const int j = (it % njit) * 32 + lane;
+    // Load cursor: runs D iterations ahead of the compute cursor; row pointers are set once per
+    // task and advanced by 32 blocks per iteration (no per-iteration index arithmetic).
+    const uint4* q4 = reinterpret_cast<const uint4*>(p.quants);
+    int ltask = t0 + warp, ljs = 0;
+    int loff[R];     // element index row * nblk + j of the next load, per row (< 2^31)
+    bool lok[R];
+    auto set_rows = [&](int t) {
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             bool ok;
             const int row = row_of(t, r, ok);
-            if (ok && j < p.nblk) {
-                const size_t o = (size_t)row * p.nblk + j;
-                qv[r] = __ldg(reinterpret_cast<const uint4*>(p.quants) + o);
-                sv[r] = p.scales[o];
+            lok[r] = ok;
+            loff[r] = row * p.nblk + lane;
+        }
+    };
+    set_rows(ltask);
+    auto issue = [&](uint4 (&qv)[R], __half (&sv)[R]) {
+        const bool jok = (ljs << 5) + lane < p.nblk;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            if (lok[r] && jok) {
+                qv[r] = __ldg(q4 + loff[r]);
+                sv[r] = p.scales[loff[r]];
             } else {
                 qv[r] = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
                 sv[r] = __float2half(0.f);
             }
+            loff[r] += 32;
+        }
+        if (++ljs == njit) {
+            ljs = 0;
+            ltask += kWarps;
+            set_rows(ltask);
         }
     };
 
@@ -313,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q4_0_kernel(KParams p, DevEr
     __half sring[D][R];
 #pragma unroll
     for (int u = 0; u < D; ++u)
-        if (u < total) load(u, ring[u], sring[u]);
+        if (u < total) issue(ring[u], sring[u]);
 
     float acc[R][NB];
 #pragma unroll
@@ -321,14 +339,15 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q4_0_kernel(KParams p, DevEr
 #pragma unroll
         for (int b = 0; b < NB; ++b) acc[r][b] = 0.f;
 
+    int cjs = 0, ctask = t0 + warp;
     for (int it0 = 0; it0 < total; it0 += D) {
 #pragma unroll
         for (int u = 0; u < D; ++u) {
             const int it = it0 + u;
             if (it < total) {
-                const int jstep = it % njit;
-                const int j = jstep * 32 + lane;
+                const int j = (cjs << 5) + lane;
                 if (j < p.nblk) {
+                    const int xb = j << 2, sw = (j >> 1) & 3;
                     __half2 a[R][NB];
 #pragma unroll
                     for (int r = 0; r < R; ++r)
@@ -338,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q4_0_kernel(KParams p, DevEr
                     for (int i = 0; i < 4; ++i) {
                         uint4 X[NB];
 #pragma unroll
-                        for (int b = 0; b < NB; ++b) X[b] = xs[b * nchunk + xslot(j, i)];
+                        for (int b = 0; b < NB; ++b) X[b] = xs[b * nchunk + xb + (i ^ sw)];
 #pragma unroll
                         for (int r = 0; r < R; ++r) {
                             const uint4 qv = ring[u][r];
@@ -367,14 +386,15 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q4_0_kernel(KParams p, DevEr
                         }
                     }
                 }
-                if (it + D < total) load(it + D, ring[u], sring[u]);
-                if (jstep == njit - 1) {
-                    const int t = t0 + warp + (it / njit) * kWarps;
-                    epilogue_task<NB, R>(p, t, acc, lane, silu_mul, half_rows, best);
+                if (it + D < total) issue(ring[u], sring[u]);
+                if (++cjs == njit) {
+                    epilogue_task<NB, R>(p, ctask, acc, lane, silu_mul, half_rows, best);
 #pragma unroll
                     for (int r = 0; r < R; ++r)
 #pragma unroll
                         for (int b = 0; b < NB; ++b) acc[r][b] = 0.f;
+                    cjs = 0;
+                    ctask += kWarps;
                 }
             }
         }
@@ -433,7 +453,8 @@ int gemv_prepare() {
 int gemv_launch(const GemvArgs& a, cudaStream_t s, bool pdl) {
     QL_REQUIRE(a.scales && a.quants && a.y, "gemv: null pointer");
     QL_REQUIRE(a.rows > 0 && a.cols > 0 && a.cols % 32 == 0, "gemv: need rows > 0, cols % 32 == 0");
-    QL_REQUIRE(a.rows < (1ll << 31) && a.cols < (1ll << 24), "gemv: matrix too large");
+    QL_REQUIRE(a.rows < (1ll << 31) && a.cols < (1ll << 24) && a.rows * (a.cols / 32) < (1ll << 31),
+               "gemv: matrix too large");
     QL_REQUIRE(a.batch >= 1 && a.batch <= 64, "gemv: batch must be in [1, 64]");
     QL_REQUIRE(a.prologue == kProX16 ? a.x16 != nullptr : (a.xf && a.norm_w), "gemv: null input");
     QL_REQUIRE(a.epilogue != QL_EPI_SILU_MUL || a.rows % 2 == 0, "gemv: silu_mul needs even rows");
