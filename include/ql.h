@@ -92,8 +92,10 @@ int ql_q4_0_pack_device(const float* d_w, int64_t rows, int64_t cols, void* d_sc
  * d_y: [batch][rows] (QL_EPI_SILU_MUL: [batch][rows/2]) in y_dtype (f32 or f16;
  * QL_EPI_ADD_RESIDUAL requires f32). d_residual: f32 [batch][rows] for QL_EPI_ADD_RESIDUAL,
  * else ignored; it may equal d_y. cols % 32 == 0; rows even for QL_EPI_SILU_MUL;
- * 1 <= batch <= 64. Accumulation is f32 across blocks. Picks the CUDA-core GEMV for small
- * batches and the tensor-core skinny GEMM for larger ones.                               */
+ * 1 <= batch <= 64. d_quants and d_x must be 16-byte aligned, d_scales, d_y and d_residual
+ * 4-byte aligned (QL_EINVAL otherwise). Products and sums are f32: codes 1024 + q are exact
+ * f16 operands of the tensor-core MMA, the -8 offset is folded into the accumulator, and each
+ * 32-weight block is scaled in f32. Batches above 8 run in passes of at most 8 columns.    */
 int ql_gemv_q4_0(const void* d_scales, const void* d_quants, int64_t rows, int64_t cols,
                  const void* d_x, int64_t batch, void* d_y, int y_dtype, int epilogue,
                  const float* d_residual, void* stream);

@@ -382,6 +382,9 @@ int attn_launch(const AttnArgs& a, cudaStream_t s, bool pdl) {
     const Layout lo = layout(a.batch, a.n_heads, a.n_kv_heads, a.head_dim, a.max_blocks_per_seq, num_sms());
     if (a.workspace_bytes < lo.total)
         return set_error(QL_EINVAL, "attention: workspace too small (need " + std::to_string(lo.total) + " bytes)");
+    QL_REQUIRE(((reinterpret_cast<uintptr_t>(a.k_pool) | reinterpret_cast<uintptr_t>(a.v_pool)) & 15) == 0 &&
+                   (reinterpret_cast<uintptr_t>(a.out) & 3) == 0 && (reinterpret_cast<uintptr_t>(a.q) & 1) == 0,
+               "attention: K/V pools must be 16-byte aligned, the output 4-byte aligned");
     if (!device_error_record()) return set_error(QL_ECUDA, "attention: no device error record");
     AParams p = {};
     p.q = a.q;

@@ -1,28 +1,33 @@
-// q4_0 GEMV on the CUDA cores: y[b][r] = sum_k (q[r][k] - 8) * d[r][k/32] * x[b][k].
+// q4_0 GEMV for batch <= 8 per pass: y[b][r] = sum_k (q[r][k] - 8) * d[r][k/32] * x[b][k].
 //
 // [IL] inferencelayer cuda_llm.rs, CudaQwen3::gemv / Q4Dev (the q4_0 format and the
 // one-GEMV-per-projection dataflow, fused q|k|v and gate|up rows).
 //
-// Design (GB300): the step is HBM-bound weight streaming, so the kernel is built around the
-// instruction budget per weight rather than around the tensor cores:
-//  * each lane streams whole 32-weight blocks (16 code bytes, one 16-byte load per row) of R
-//    rows at once; a warp covers 32 consecutive blocks of a row, so every load instruction
-//    of a warp reads 512 contiguous bytes per row;
-//  * the activation vector is staged once per CTA in shared memory as f16, permuted so that
-//    one 16-byte shared load yields exactly the four f16 pairs that match the four code pairs
-//    a 32-bit code word expands to, and swizzled so that the 8 lanes of a quarter-warp hit 8
-//    different bank groups; each staged chunk is reused by the R rows of a task;
-//  * a 32-bit code word expands to four f16x2 values with one shift and four LOP3s: a nibble
-//    OR'ed into the mantissa of 1024.0h gives 1024 + q exactly; the high nibbles land 4 bits
-//    up (1024 + 16 q) and their activations are staged pre-divided by 16 (exact);
-//    subtracting 1032 (resp. 1152) gives (q - 8) (resp. 16 (q - 8)) exactly;
-//  * the 32 products of a block accumulate in f16x2 (16 terms per half), and each block's sum
-//    is scaled by d and accumulated in f32;
-//  * the CTA's rows are contiguous, so its first bytes are prefetched into L2 before the
-//    kernel waits on its predecessor (programmatic dependent launch).
-// Fused prologue: RMSNorm of an f32 residual stream (x / sqrt(mean(x^2) + eps) * w, [ME]
-// host_rms_norm) into the staged f16 activations. Fused epilogues: residual add, SiLU * up
-// (gate | up rows), and greedy argmax over the rows (lm_head).
+// Design (GB300). The step is HBM-bound weight streaming, and at 18 bytes per 32 weights the
+// GPU must retire ~1.2e13 weights/s: the instruction mix per weight decides whether the HBM
+// bound is reachable. Measured with ncu on an f16x2 CUDA-core variant of this kernel, the f16
+// FMA/add pipe (64 lanes/clk/SM on this part, half the f32 rate) and the integer pipe were the
+// limit at ~45% of HBM. This kernel therefore feeds the dot products to mma.sync (m16n8k16,
+// f16 in, f32 accumulate) and keeps the CUDA cores for the nibble expansion only:
+//  * a warp owns a 16-row tile (SiLU*up: 8 gate rows + the matching 8 up rows) and walks the
+//    32-weight blocks of one K segment; lane (g, t) = (lane / 4, lane % 4) loads 32-bit code
+//    word t of block j for rows g and g + 8, so the 4 lanes of a row read the block's 16 bytes;
+//    code loads run kD blocks ahead (a register ring);
+//  * one shift and four LOP3 turn a code word into four f16 pairs 1024 + q (low nibbles) and
+//    1024 + 16 q (high nibbles), exactly; each pair lands in the A-fragment slots of the k
+//    values it holds (any k permutation is allowed as long as B uses the same one);
+//  * the activation columns are staged once per CTA in shared memory, permuted so that one
+//    16-byte load gives the B fragments of both MMAs of a block, high-nibble activations
+//    pre-divided by 16 (exact);
+//  * the offsets are folded into the accumulator: the MMA computes sum (1024 + q) x, and the
+//    accumulator starts at -(1032 sum_lo x + 1152 sum_hi x/16) per (block, column), computed
+//    once per CTA from the staged values, so no f16 subtraction is executed per weight;
+//  * per block, the f32 result is scaled by the row's f16 scale with one FFMA per output.
+// Small matrices split K over up to 8 warps of a CTA and reduce in shared memory, so that every
+// shape fills the GPU. The CTA's first codes are prefetched into L2 before the kernel waits on
+// its predecessor (programmatic dependent launch).
+// Fused prologue: RMSNorm of an f32 residual stream ([ME] host_rms_norm) into the staged f16
+// activations. Fused epilogues: residual add, SiLU * up, greedy argmax over the rows (lm_head).
 #include <cuda_fp16.h>
 
 #include <mutex>
@@ -35,9 +40,8 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
-constexpr size_t kMaxStageBytes = 100 * 1024;   // staged activations per CTA
-
-__device__ __forceinline__ int xslot(int j, int i) { return (j << 2) + (i ^ ((j >> 1) & 3)); }
+constexpr int kD = 8;                            // blocks of code loads in flight per lane
+constexpr size_t kMaxStageBytes = 100 * 1024;    // dynamic shared memory per CTA
 
 __device__ __forceinline__ __half2 h2(uint32_t u) {
     __half2 h;
@@ -55,12 +59,21 @@ __device__ __forceinline__ unsigned long long argmax_key(float v, int row) {
     return ((unsigned long long)b << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)row);
 }
 
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 struct KParams {
     const __half* scales;
     const uint8_t* quants;
     int rows;          // weight rows
     int nblk;          // cols / 32
-    int batch;         // columns handled by this launch (<= NB)
+    int batch;         // columns of this launch (<= 8)
     int prologue;
     const __half* x16; // [batch][cols]
     const float* xf;   // [batch][cols]
@@ -73,360 +86,295 @@ struct KParams {
     const float* residual;
     unsigned long long* keys;
     const int32_t* active;
-    int ntasks;
-    int tasks_per_cta;
+    int ntile;         // 16-row tiles (SiLU*up: 8 gate + 8 up rows)
+    int S;             // K segments per tile (1, 2, 4 or 8 warps)
+    int seg_blocks;    // blocks per K segment
+    int cstride;       // uint4 units between staged columns
 };
 
-// Stage the activation columns into shared memory in the permuted, swizzled chunk layout.
-template <int NB>
-__device__ void stage_x(const KParams& p, uint4* xs, float* red) {
+// Stage the activations: per column, per block j, 4 chunks of 16 bytes (chunk t serves lane
+// t of the MMA), plus the accumulator start value of each (block, column).
+__device__ void stage_x(const KParams& p, uint4* xs, float* bias, float* red) {
     const int cols = p.nblk * 32;
     const int tid = threadIdx.x;
-    float rs[NB];
+    float rs[8];
 #pragma unroll
-    for (int b = 0; b < NB; ++b) rs[b] = 1.0f;
+    for (int b = 0; b < 8; ++b) rs[b] = 1.0f;
     if (p.prologue == kProRmsF32) {
-        float ss[NB];
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {
-            ss[b] = 0.f;
-            if (b < p.batch) {
-                const float4* xb = reinterpret_cast<const float4*>(p.xf + (size_t)b * cols);
-                for (int k = tid; k < cols / 4; k += kThreads) {
-                    const float4 v = xb[k];
-                    ss[b] += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-                }
+        const int warp = tid >> 5, lane = tid & 31;
+        for (int b = 0; b < p.batch; ++b) {
+            float ss = 0.f;
+            const float4* xb = reinterpret_cast<const float4*>(p.xf + (size_t)b * cols);
+            for (int k = tid; k < cols / 4; k += kThreads) {
+                const float4 v = xb[k];
+                ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
             }
 #pragma unroll
-            for (int o = 16; o; o >>= 1) ss[b] += __shfl_xor_sync(0xffffffffu, ss[b], o);
-        }
-        const int warp = tid >> 5, lane = tid & 31;
-        if (lane == 0) {
-#pragma unroll
-            for (int b = 0; b < NB; ++b) red[warp * NB + b] = ss[b];
+            for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+            if (lane == 0) red[warp * 8 + b] = ss;
         }
         __syncthreads();
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {
+        for (int b = 0; b < p.batch; ++b) {
             float t = 0.f;
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) t += red[w * NB + b];
-            rs[b] = 1.0f / sqrtf(t / (float)cols + p.eps);
-        }
-    }
-    const int nchunk = p.nblk * 4;
-    for (int c = tid; c < NB * nchunk; c += kThreads) {
-        const int b = c / nchunk;
-        const int rem = c - b * nchunk;
-        const int j = rem >> 2, i = rem & 3;
-        float lo[4], hi[4];   // x[32j + 4i + 0..3], x[32j + 16 + 4i + 0..3]
-        if (b < p.batch) {
-            const size_t base = (size_t)b * cols + 32 * j + 4 * i;
-            if (p.prologue == kProRmsF32) {
-                const float4 a = *reinterpret_cast<const float4*>(p.xf + base);
-                const float4 h = *reinterpret_cast<const float4*>(p.xf + base + 16);
-                const float4 wa = *reinterpret_cast<const float4*>(p.norm_w + 32 * j + 4 * i);
-                const float4 wh = *reinterpret_cast<const float4*>(p.norm_w + 32 * j + 16 + 4 * i);
-                float rr = rs[0];
+            for (int w = 0; w < kWarps; ++w) t += red[w * 8 + b];
+            const float r = 1.0f / sqrtf(t / (float)cols + p.eps);
 #pragma unroll
-                for (int bb = 0; bb < NB; ++bb)
-                    if (bb == b) rr = rs[bb];
-                // RMSNorm output rounded to f16 (the GEMV's activation precision)
-                lo[0] = __half2float(__float2half_rn(a.x * rr * wa.x));
-                lo[1] = __half2float(__float2half_rn(a.y * rr * wa.y));
-                lo[2] = __half2float(__float2half_rn(a.z * rr * wa.z));
-                lo[3] = __half2float(__float2half_rn(a.w * rr * wa.w));
-                hi[0] = __half2float(__float2half_rn(h.x * rr * wh.x));
-                hi[1] = __half2float(__float2half_rn(h.y * rr * wh.y));
-                hi[2] = __half2float(__float2half_rn(h.z * rr * wh.z));
-                hi[3] = __half2float(__float2half_rn(h.w * rr * wh.w));
-            } else {
-                const uint2 a = *reinterpret_cast<const uint2*>(p.x16 + base);
-                const uint2 h = *reinterpret_cast<const uint2*>(p.x16 + base + 16);
-                const float2 a0 = __half22float2(h2(a.x)), a1 = __half22float2(h2(a.y));
-                const float2 h0 = __half22float2(h2(h.x)), h1 = __half22float2(h2(h.y));
-                lo[0] = a0.x; lo[1] = a0.y; lo[2] = a1.x; lo[3] = a1.y;
-                hi[0] = h0.x; hi[1] = h0.y; hi[2] = h1.x; hi[3] = h1.y;
+            for (int bb = 0; bb < 8; ++bb)
+                if (bb == b) rs[bb] = r;
+        }
+        __syncthreads();   // red is reused later
+    }
+    for (int item = tid; item < 8 * p.nblk; item += kThreads) {
+        const int b = item / p.nblk, j = item - b * p.nblk;
+        if (b >= p.batch) {
+            bias[j * 8 + b] = 0.f;
+            continue;
+        }
+        float v[32];
+        const size_t base = (size_t)b * cols + 32 * j;
+        if (p.prologue == kProRmsF32) {
+            float rr = rs[0];
+#pragma unroll
+            for (int bb = 1; bb < 8; ++bb)
+                if (bb == b) rr = rs[bb];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const float4 a = *reinterpret_cast<const float4*>(p.xf + base + 4 * c);
+                const float4 w = *reinterpret_cast<const float4*>(p.norm_w + 32 * j + 4 * c);
+                v[4 * c + 0] = __half2float(__float2half_rn(a.x * rr * w.x));
+                v[4 * c + 1] = __half2float(__float2half_rn(a.y * rr * w.y));
+                v[4 * c + 2] = __half2float(__float2half_rn(a.z * rr * w.z));
+                v[4 * c + 3] = __half2float(__float2half_rn(a.w * rr * w.w));
             }
         } else {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) lo[e] = hi[e] = 0.f;
+            for (int c = 0; c < 4; ++c) {
+                const uint4 u = *reinterpret_cast<const uint4*>(p.x16 + base + 8 * c);
+                const float2 f0 = __half22float2(h2(u.x)), f1 = __half22float2(h2(u.y));
+                const float2 f2 = __half22float2(h2(u.z)), f3 = __half22float2(h2(u.w));
+                v[8 * c + 0] = f0.x; v[8 * c + 1] = f0.y; v[8 * c + 2] = f1.x; v[8 * c + 3] = f1.y;
+                v[8 * c + 4] = f2.x; v[8 * c + 5] = f2.y; v[8 * c + 6] = f3.x; v[8 * c + 7] = f3.y;
+            }
         }
-        uint4 v;
-        v.x = u32(__floats2half2_rn(lo[0], lo[2]));
-        v.y = u32(__floats2half2_rn(lo[1], lo[3]));
-        v.z = u32(__floats2half2_rn(hi[0] * 0.0625f, hi[2] * 0.0625f));
-        v.w = u32(__floats2half2_rn(hi[1] * 0.0625f, hi[3] * 0.0625f));
-        xs[b * nchunk + xslot(j, i)] = v;
+        float lo = 0.f, hi = 0.f;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const __half2 p0 = __floats2half2_rn(v[4 * t], v[4 * t + 2]);
+            const __half2 p1 = __floats2half2_rn(v[4 * t + 1], v[4 * t + 3]);
+            const __half2 p2 = __floats2half2_rn(v[16 + 4 * t] * 0.0625f, v[18 + 4 * t] * 0.0625f);
+            const __half2 p3 = __floats2half2_rn(v[17 + 4 * t] * 0.0625f, v[19 + 4 * t] * 0.0625f);
+            const float2 f0 = __half22float2(p0), f1 = __half22float2(p1);
+            const float2 f2 = __half22float2(p2), f3 = __half22float2(p3);
+            lo += (f0.x + f0.y) + (f1.x + f1.y);
+            hi += (f2.x + f2.y) + (f3.x + f3.y);
+            xs[b * p.cstride + 4 * j + t] = make_uint4(u32(p0), u32(p1), u32(p2), u32(p3));
+        }
+        // sum (1024 + q) x_lo + (1024 + 16 q) x_hi/16 = sum (q - 8) x + 1032 sum x_lo + 1152 sum x_hi/16
+        bias[j * 8 + b] = -(1032.0f * lo + 1152.0f * hi);
     }
 }
 
-// Reduce a task's per-lane partial sums over the warp and apply the epilogue.
-template <int NB, int R>
-__device__ __forceinline__ void epilogue_task(const KParams& p, int t, float (&acc)[R][NB], int lane,
-                                              bool silu_mul, int half_rows,
-                                              unsigned long long (&best)[NB]) {
-#pragma unroll
-    for (int r = 0; r < R; ++r)
-#pragma unroll
-        for (int b = 0; b < NB; ++b)
-#pragma unroll
-            for (int o = 16; o; o >>= 1) acc[r][b] += __shfl_xor_sync(0xffffffffu, acc[r][b], o);
-    int row[R];
-    bool ok[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-        if (silu_mul) {
-            const int i = t * (R / 2) + (r % (R / 2));
-            ok[r] = i < half_rows;
-            row[r] = (r < R / 2) ? i : half_rows + i;
-        } else {
-            row[r] = t * R + r;
-            ok[r] = row[r] < p.rows;
-        }
-    }
-    // lane l writes output number l (R * NB <= 32)
-    if (silu_mul) {
-#pragma unroll
-        for (int r = 0; r < R / 2; ++r)
-#pragma unroll
-            for (int b = 0; b < NB; ++b) {
-                if (lane == r * NB + b && ok[r] && b < p.batch) {
-                    const float v = silu(acc[r][b]) * acc[r + R / 2][b];
-                    const size_t o = (size_t)b * p.y_ld + row[r];
-                    if (p.y_dtype == QL_DTYPE_F16)
-                        reinterpret_cast<__half*>(p.y)[o] = __float2half_rn(v);
-                    else
-                        reinterpret_cast<float*>(p.y)[o] = v;
-                }
-            }
-    } else if (p.epilogue == kEpiArgmax) {
-#pragma unroll
-        for (int r = 0; r < R; ++r)
-#pragma unroll
-            for (int b = 0; b < NB; ++b) {
-                if (ok[r] && b < p.batch) {
-                    const unsigned long long k = argmax_key(acc[r][b], row[r]);
-                    best[b] = k > best[b] ? k : best[b];
-                    if (p.y && lane == r * NB + b)
-                        reinterpret_cast<float*>(p.y)[(size_t)b * p.y_ld + row[r]] = acc[r][b];
-                }
-            }
-    } else {
-#pragma unroll
-        for (int r = 0; r < R; ++r)
-#pragma unroll
-            for (int b = 0; b < NB; ++b) {
-                if (lane == r * NB + b && ok[r] && b < p.batch) {
-                    const size_t o = (size_t)b * p.y_ld + row[r];
-                    float v = acc[r][b];
-                    if (p.epilogue == QL_EPI_ADD_RESIDUAL) v += p.residual[o];
-                    if (p.y_dtype == QL_DTYPE_F16)
-                        reinterpret_cast<__half*>(p.y)[o] = __float2half_rn(v);
-                    else
-                        reinterpret_cast<float*>(p.y)[o] = v;
-                }
-            }
-    }
+__device__ __forceinline__ void store_out(const KParams& p, int n, int row, float v) {
+    const size_t o = (size_t)n * p.y_ld + row;
+    if (p.epilogue == QL_EPI_ADD_RESIDUAL) v += p.residual[o];
+    if (p.y_dtype == QL_DTYPE_F16)
+        reinterpret_cast<__half*>(p.y)[o] = __float2half_rn(v);
+    else
+        reinterpret_cast<float*>(p.y)[o] = v;
 }
 
-template <int NB, int R>
-__global__ void __launch_bounds__(kThreads, 2) gemv_q4_0_kernel(KParams p, DevError* err) {
-    extern __shared__ uint4 xs[];
-    __shared__ float red[kWarps * 8];
-    __shared__ unsigned long long kred[kWarps * 8];
+__global__ void __launch_bounds__(kThreads, 3) gemv_q4_0_mma_kernel(KParams p, DevError* err) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    uint4* xs = reinterpret_cast<uint4*>(smem);
+    float* bias = reinterpret_cast<float*>(xs + (size_t)p.batch * p.cstride);
+    float* red = bias + (size_t)p.nblk * 8;           // [kWarps][32][4]
+    __shared__ unsigned long long kred[kWarps][8];
     (void)err;
+
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 2, t = lane & 3;
     const bool silu_mul = (p.epilogue == QL_EPI_SILU_MUL);
     const int half_rows = p.rows >> 1;
-    const int t0 = blockIdx.x * p.tasks_per_cta;
-    const int t1 = min(p.ntasks, t0 + p.tasks_per_cta);
+    const int tiles_per_cta = kWarps / p.S;
+    const int tile = blockIdx.x * tiles_per_cta + warp / p.S;
+    const int seg = warp % p.S;
 
-    // Weights do not depend on the previous kernel: warm L2 with the start of this CTA's rows
-    // while the predecessor finishes.
-    if (threadIdx.x == 0 && t0 < t1) {
+    // The weights do not depend on the previous kernel: warm L2 with this CTA's first codes
+    // while the predecessor drains.
+    if (threadIdx.x == 0) {
         const size_t row_bytes = (size_t)p.nblk * 16;
-        const int nr = silu_mul ? (t1 - t0) * (R / 2) : (t1 - t0) * R;
-        const int r0 = silu_mul ? t0 * (R / 2) : t0 * R;
-        const int limit = silu_mul ? half_rows : p.rows;   // rows of one range
-        size_t bytes = row_bytes * (size_t)min(nr, limit - r0);
-        bytes = bytes > 65536 ? 65536 : bytes;
-        const uint8_t* a0 = p.quants + (size_t)r0 * row_bytes;
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a0), "r"((uint32_t)bytes)
-                     : "memory");
-        if (silu_mul) {
-            const uint8_t* a1 = p.quants + (size_t)(half_rows + r0) * row_bytes;
-            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a1),
-                         "r"((uint32_t)bytes)
-                         : "memory");
+        const int t0 = blockIdx.x * tiles_per_cta;
+        const int nt = min(tiles_per_cta, p.ntile - t0);
+        if (nt > 0) {
+            const int rows_per_tile = silu_mul ? 8 : 16;
+            const int limit = silu_mul ? half_rows : p.rows;
+            const int r0 = t0 * rows_per_tile;
+            size_t bytes = row_bytes * (size_t)min(nt * rows_per_tile, limit - r0);
+            bytes = bytes > 49152 ? 49152 : bytes;
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.quants + (size_t)r0 * row_bytes),
+                         "r"((uint32_t)bytes) : "memory");
+            if (silu_mul)
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                             ::"l"(p.quants + (size_t)(half_rows + r0) * row_bytes), "r"((uint32_t)bytes)
+                             : "memory");
         }
     }
     pdl_wait();
-    stage_x<NB>(p, xs, red);
+    stage_x(p, xs, bias, red);
     __syncthreads();
     pdl_trigger();
 
-    const int nchunk = p.nblk * 4;
-    const __half2 k1032 = __float2half2_rn(1032.0f);
-    const __half2 k1152 = __float2half2_rn(1152.0f);
-    unsigned long long best[NB];
+    // rows of this lane: ra (fragment row g) and rb (row g + 8)
+    int ra, rb;
+    bool oka, okb;
+    if (silu_mul) {
+        const int i = tile * 8 + g;
+        oka = okb = (tile < p.ntile) && i < half_rows;
+        ra = oka ? i : 0;
+        rb = okb ? half_rows + i : 0;
+    } else {
+        ra = tile * 16 + g;
+        rb = ra + 8;
+        oka = (tile < p.ntile) && ra < p.rows;
+        okb = (tile < p.ntile) && rb < p.rows;
+        ra = oka ? ra : 0;
+        rb = okb ? rb : 0;
+    }
+    const int j0 = seg * p.seg_blocks;
+    const int j1 = (tile < p.ntile) ? min(p.nblk, j0 + p.seg_blocks) : j0;
+    const int nit = j1 > j0 ? j1 - j0 : 0;
+    const uint32_t* qa = reinterpret_cast<const uint32_t*>(p.quants) + ((size_t)ra * p.nblk + j0) * 4 + t;
+    const uint32_t* qb = reinterpret_cast<const uint32_t*>(p.quants) + ((size_t)rb * p.nblk + j0) * 4 + t;
+    const unsigned short* sa = reinterpret_cast<const unsigned short*>(p.scales) + (size_t)ra * p.nblk + j0;
+    const unsigned short* sb = reinterpret_cast<const unsigned short*>(p.scales) + (size_t)rb * p.nblk + j0;
+    const float mask_a = oka ? 1.f : 0.f, mask_b = okb ? 1.f : 0.f;
+    const bool has_col = g < p.batch;
+    const uint4* xcol = xs + (size_t)(has_col ? g : 0) * p.cstride;
+
+    uint32_t rwa[kD], rwb[kD], rsc[kD];
 #pragma unroll
-    for (int b = 0; b < NB; ++b) best[b] = 0ull;
-
-    // Each warp walks a flat sequence of (task, 32-block step) iterations. The loads of the
-    // next D iterations are always in flight, across task boundaries, so every lane keeps
-    // D * R * 16 bytes of weight codes outstanding.
-    constexpr int D = NB >= 4 ? 2 : (NB == 2 && R == 4) ? 3 : 4;
-    const int njit = (p.nblk + 31) >> 5;
-    const int my_tasks = (t1 - t0 > warp) ? (t1 - t0 - warp + kWarps - 1) / kWarps : 0;
-    const int total = my_tasks * njit;
-
-    auto row_of = [&](int t, int r, bool& ok) -> int {
-        if (silu_mul) {
-            const int i = t * (R / 2) + (r % (R / 2));
-            ok = i < half_rows;
-            return ok ? ((r < R / 2) ? i : half_rows + i) : 0;
+    for (int u = 0; u < kD; ++u) {
+        if (u < nit) {
+            rwa[u] = __ldg(qa + 4 * u);
+            rwb[u] = __ldg(qb + 4 * u);
+            rsc[u] = (uint32_t)__ldg(sa + u) | ((uint32_t)__ldg(sb + u) << 16);
         }
-        const int rr = t * R + r;
-        ok = rr < p.rows;
-        return ok ? rr : 0;
-    };
-    // Load cursor: runs D iterations ahead of the compute cursor; row pointers are set once per
-    // task and advanced by 32 blocks per iteration (no per-iteration index arithmetic).
-    const uint4* q4 = reinterpret_cast<const uint4*>(p.quants);
-    int ltask = t0 + warp, ljs = 0;
-    int loff[R];     // element index row * nblk + j of the next load, per row (< 2^31)
-    bool lok[R];
-    auto set_rows = [&](int t) {
+    }
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int it0 = 0; it0 < nit; it0 += kD) {
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-            bool ok;
-            const int row = row_of(t, r, ok);
-            lok[r] = ok;
-            loff[r] = row * p.nblk + lane;
-        }
-    };
-    set_rows(ltask);
-    auto issue = [&](uint4 (&qv)[R], __half (&sv)[R]) {
-        const bool jok = (ljs << 5) + lane < p.nblk;
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            if (lok[r] && jok) {
-                qv[r] = __ldg(q4 + loff[r]);
-                sv[r] = p.scales[loff[r]];
-            } else {
-                qv[r] = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
-                sv[r] = __float2half(0.f);
-            }
-            loff[r] += 32;
-        }
-        if (++ljs == njit) {
-            ljs = 0;
-            ltask += kWarps;
-            set_rows(ltask);
-        }
-    };
-
-    uint4 ring[D][R];
-    __half sring[D][R];
-#pragma unroll
-    for (int u = 0; u < D; ++u)
-        if (u < total) issue(ring[u], sring[u]);
-
-    float acc[R][NB];
-#pragma unroll
-    for (int r = 0; r < R; ++r)
-#pragma unroll
-        for (int b = 0; b < NB; ++b) acc[r][b] = 0.f;
-
-    int cjs = 0, ctask = t0 + warp;
-    for (int it0 = 0; it0 < total; it0 += D) {
-#pragma unroll
-        for (int u = 0; u < D; ++u) {
+        for (int u = 0; u < kD; ++u) {
             const int it = it0 + u;
-            if (it < total) {
-                const int j = (cjs << 5) + lane;
-                if (j < p.nblk) {
-                    const int xb = j << 2, sw = (j >> 1) & 3;
-                    __half2 a[R][NB];
-#pragma unroll
-                    for (int r = 0; r < R; ++r)
-#pragma unroll
-                        for (int b = 0; b < NB; ++b) a[r][b] = __float2half2_rn(0.f);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        uint4 X[NB];
-#pragma unroll
-                        for (int b = 0; b < NB; ++b) X[b] = xs[b * nchunk + xb + (i ^ sw)];
-#pragma unroll
-                        for (int r = 0; r < R; ++r) {
-                            const uint4 qv = ring[u][r];
-                            const uint32_t w = (i == 0) ? qv.x : (i == 1) ? qv.y : (i == 2) ? qv.z : qv.w;
-                            const uint32_t s8 = w >> 8;
-                            const __half2 lo0 = __hsub2(h2((w & 0x000F000Fu) | 0x64006400u), k1032);
-                            const __half2 hi0 = __hsub2(h2((w & 0x00F000F0u) | 0x64006400u), k1152);
-                            const __half2 lo1 = __hsub2(h2((s8 & 0x000F000Fu) | 0x64006400u), k1032);
-                            const __half2 hi1 = __hsub2(h2((s8 & 0x00F000F0u) | 0x64006400u), k1152);
-#pragma unroll
-                            for (int b = 0; b < NB; ++b) {
-                                a[r][b] = __hfma2(lo0, h2(X[b].x), a[r][b]);
-                                a[r][b] = __hfma2(lo1, h2(X[b].y), a[r][b]);
-                                a[r][b] = __hfma2(hi0, h2(X[b].z), a[r][b]);
-                                a[r][b] = __hfma2(hi1, h2(X[b].w), a[r][b]);
-                            }
-                        }
-                    }
-#pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        const float d = __half2float(sring[u][r]);
-#pragma unroll
-                        for (int b = 0; b < NB; ++b) {
-                            const float2 f = __half22float2(a[r][b]);
-                            acc[r][b] = fmaf(d, f.x + f.y, acc[r][b]);
-                        }
-                    }
+            if (it < nit) {
+                const int j = j0 + it;
+                const uint32_t wa = rwa[u], wb = rwb[u];
+                const __half2 sc = h2(rsc[u]);
+                const int nx = it + kD;
+                if (nx < nit) {
+                    rwa[u] = __ldg(qa + 4 * nx);
+                    rwb[u] = __ldg(qb + 4 * nx);
+                    rsc[u] = (uint32_t)__ldg(sa + nx) | ((uint32_t)__ldg(sb + nx) << 16);
                 }
-                if (it + D < total) issue(ring[u], sring[u]);
-                if (++cjs == njit) {
-                    epilogue_task<NB, R>(p, ctask, acc, lane, silu_mul, half_rows, best);
-#pragma unroll
-                    for (int r = 0; r < R; ++r)
-#pragma unroll
-                        for (int b = 0; b < NB; ++b) acc[r][b] = 0.f;
-                    cjs = 0;
-                    ctask += kWarps;
+                uint4 X = has_col ? xcol[4 * j + t] : make_uint4(0u, 0u, 0u, 0u);
+                const float2 bz = *reinterpret_cast<const float2*>(bias + j * 8 + 2 * t);
+                float c[4] = {bz.x, bz.y, bz.x, bz.y};
+                const uint32_t sa8 = wa >> 8, sb8 = wb >> 8;
+                mma16816(c, (wa & 0x000F000Fu) | 0x64006400u, (wb & 0x000F000Fu) | 0x64006400u,
+                         (sa8 & 0x000F000Fu) | 0x64006400u, (sb8 & 0x000F000Fu) | 0x64006400u, X.x, X.y);
+                mma16816(c, (wa & 0x00F000F0u) | 0x64006400u, (wb & 0x00F000F0u) | 0x64006400u,
+                         (sa8 & 0x00F000F0u) | 0x64006400u, (sb8 & 0x00F000F0u) | 0x64006400u, X.z, X.w);
+                const float2 d = __half22float2(sc);
+                acc[0] = fmaf(d.x, c[0], acc[0]);
+                acc[1] = fmaf(d.x, c[1], acc[1]);
+                acc[2] = fmaf(d.y, c[2], acc[2]);
+                acc[3] = fmaf(d.y, c[3], acc[3]);
+            }
+        }
+    }
+    acc[0] *= mask_a; acc[1] *= mask_a; acc[2] *= mask_b; acc[3] *= mask_b;
+
+    // combine the K segments of a tile
+    if (p.S > 1) {
+        float4* r4 = reinterpret_cast<float4*>(red);
+        r4[warp * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        __syncthreads();
+        if (seg == 0) {
+            for (int s2 = 1; s2 < p.S; ++s2) {
+                const float4 o = r4[(warp + s2) * 32 + lane];
+                acc[0] += o.x; acc[1] += o.y; acc[2] += o.z; acc[3] += o.w;
+            }
+        }
+    }
+
+    unsigned long long best0 = 0ull, best1 = 0ull;   // argmax keys of columns 2t, 2t+1
+    const int n0 = 2 * t, n1 = 2 * t + 1;
+    if (seg == 0 && tile < p.ntile) {
+        if (silu_mul) {
+            const int i = tile * 8 + g;
+            if (oka) {
+                if (n0 < p.batch) store_out(p, n0, i, silu(acc[0]) * acc[2]);
+                if (n1 < p.batch) store_out(p, n1, i, silu(acc[1]) * acc[3]);
+            }
+        } else if (p.epilogue == kEpiArgmax) {
+            const int rga = tile * 16 + g, rgb = rga + 8;
+            if (oka) {
+                if (n0 < p.batch) {
+                    best0 = argmax_key(acc[0], rga);
+                    if (p.y) reinterpret_cast<float*>(p.y)[(size_t)n0 * p.y_ld + rga] = acc[0];
                 }
+                if (n1 < p.batch) {
+                    best1 = argmax_key(acc[1], rga);
+                    if (p.y) reinterpret_cast<float*>(p.y)[(size_t)n1 * p.y_ld + rga] = acc[1];
+                }
+            }
+            if (okb) {
+                if (n0 < p.batch) {
+                    const unsigned long long k = argmax_key(acc[2], rgb);
+                    best0 = k > best0 ? k : best0;
+                    if (p.y) reinterpret_cast<float*>(p.y)[(size_t)n0 * p.y_ld + rgb] = acc[2];
+                }
+                if (n1 < p.batch) {
+                    const unsigned long long k = argmax_key(acc[3], rgb);
+                    best1 = k > best1 ? k : best1;
+                    if (p.y) reinterpret_cast<float*>(p.y)[(size_t)n1 * p.y_ld + rgb] = acc[3];
+                }
+            }
+        } else {
+            const int rga = tile * 16 + g, rgb = rga + 8;
+            if (oka) {
+                if (n0 < p.batch) store_out(p, n0, rga, acc[0]);
+                if (n1 < p.batch) store_out(p, n1, rga, acc[1]);
+            }
+            if (okb) {
+                if (n0 < p.batch) store_out(p, n0, rgb, acc[2]);
+                if (n1 < p.batch) store_out(p, n1, rgb, acc[3]);
             }
         }
     }
     if (p.epilogue == kEpiArgmax) {
-        // every lane holds the same per-warp maxima; reduce across the CTA, one atomic each
-        if (lane == 0) {
+        // lanes with the same t hold the same two columns: reduce over g, then over warps
 #pragma unroll
-            for (int b = 0; b < NB; ++b) kred[warp * NB + b] = best[b];
+        for (int o = 4; o < 32; o <<= 1) {
+            const unsigned long long k0 = __shfl_xor_sync(0xffffffffu, best0, o);
+            const unsigned long long k1 = __shfl_xor_sync(0xffffffffu, best1, o);
+            best0 = k0 > best0 ? k0 : best0;
+            best1 = k1 > best1 ? k1 : best1;
+        }
+        if (lane < 4) {
+            kred[warp][2 * lane] = best0;
+            kred[warp][2 * lane + 1] = best1;
         }
         __syncthreads();
-        if (threadIdx.x < NB && (int)threadIdx.x < p.batch) {
+        if (threadIdx.x < 8 && (int)threadIdx.x < p.batch) {
             const int b = threadIdx.x;
             unsigned long long m = 0ull;
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) m = kred[w * NB + b] > m ? kred[w * NB + b] : m;
+            for (int w = 0; w < kWarps; ++w) m = kred[w][b] > m ? kred[w][b] : m;
             const bool act = p.active == nullptr || p.active[b] != 0;
             if (m && act) atomicMax(p.keys + b, m);
         }
     }
-}
-
-template <int NB, int R>
-cudaError_t launch_nb(const KParams& p0, int grid, size_t smem, cudaStream_t s, bool pdl) {
-    return launch(gemv_q4_0_kernel<NB, R>, dim3(grid), dim3(kThreads), smem, s, pdl, p0,
-                  device_error_record());
-}
-
-template <int NB, int R>
-cudaError_t allow_smem() {
-    return cudaFuncSetAttribute(gemv_q4_0_kernel<NB, R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)kMaxStageBytes);
 }
 
 }  // namespace
@@ -439,12 +387,8 @@ int gemv_prepare() {
     QL_TRY_CUDA(cudaGetDevice(&dev));
     std::lock_guard<std::mutex> lk(mu);
     if (done.count(dev)) return QL_OK;
-    cudaError_t e = allow_smem<1, 4>();
-    if (e == cudaSuccess) e = allow_smem<2, 4>();
-    if (e == cudaSuccess) e = allow_smem<1, 2>();
-    if (e == cudaSuccess) e = allow_smem<2, 2>();
-    if (e == cudaSuccess) e = allow_smem<4, 2>();
-    if (e == cudaSuccess) e = allow_smem<8, 2>();
+    const cudaError_t e = cudaFuncSetAttribute(gemv_q4_0_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)kMaxStageBytes);
     if (e != cudaSuccess) return cuda_error(e, "gemv: cudaFuncSetAttribute");
     done.insert(dev);
     return QL_OK;
@@ -453,7 +397,7 @@ int gemv_prepare() {
 int gemv_launch(const GemvArgs& a, cudaStream_t s, bool pdl) {
     QL_REQUIRE(a.scales && a.quants && a.y, "gemv: null pointer");
     QL_REQUIRE(a.rows > 0 && a.cols > 0 && a.cols % 32 == 0, "gemv: need rows > 0, cols % 32 == 0");
-    QL_REQUIRE(a.rows < (1ll << 31) && a.cols < (1ll << 24) && a.rows * (a.cols / 32) < (1ll << 31),
+    QL_REQUIRE(a.rows < (1ll << 31) && a.cols < (1ll << 24) && a.rows * (a.cols / 32) < (1ll << 29),
                "gemv: matrix too large");
     QL_REQUIRE(a.batch >= 1 && a.batch <= 64, "gemv: batch must be in [1, 64]");
     QL_REQUIRE(a.prologue == kProX16 ? a.x16 != nullptr : (a.xf && a.norm_w), "gemv: null input");
@@ -463,20 +407,25 @@ int gemv_launch(const GemvArgs& a, cudaStream_t s, bool pdl) {
     QL_REQUIRE(a.epilogue != kEpiArgmax || a.argmax_keys, "gemv: argmax needs key buffer");
     QL_REQUIRE(a.y_dtype == QL_DTYPE_F32 || a.y_dtype == QL_DTYPE_F16, "gemv: bad y dtype");
     QL_REQUIRE(a.epilogue != kEpiArgmax || a.y_dtype == QL_DTYPE_F32, "gemv: argmax logits are f32");
+    auto al = [](const void* q, uintptr_t n) { return (reinterpret_cast<uintptr_t>(q) & (n - 1)) == 0; };
+    QL_REQUIRE(al(a.quants, 16) && al(a.scales, 4) && al(a.x16, 16) && al(a.xf, 16) && al(a.norm_w, 16) &&
+                   al(a.y, 4) && al(a.residual, 4),
+               "gemv: codes, activations and norm weights must be 16-byte aligned, scales and outputs 4-byte");
     if (!device_error_record()) return set_error(QL_ECUDA, "gemv: no device error record");
     if (int rc = gemv_prepare()) return rc;
 
     const int nblk = (int)(a.cols / 32);
-    const size_t col_bytes = (size_t)nblk * 64;
-    int nb_max = (int)(kMaxStageBytes / col_bytes);
-    QL_REQUIRE(nb_max >= 1, "gemv: cols too large for the staged activation");
-    nb_max = nb_max >= 8 ? 8 : nb_max >= 4 ? 4 : nb_max >= 2 ? 2 : 1;
-    const int out_ld = (int)(a.epilogue == QL_EPI_SILU_MUL ? a.rows / 2 : a.rows);
+    const int cstride = nblk * 4 + 4;                              // +64 B: no bank aliasing
+    const size_t fixed = (size_t)nblk * 8 * 4 + kWarps * 32 * 16;  // bias + segment reduction
+    QL_REQUIRE(fixed + (size_t)cstride * 16 <= kMaxStageBytes, "gemv: cols too large for the staged activation");
+    int nb_max = (int)((kMaxStageBytes - fixed) / ((size_t)cstride * 16));
+    if (nb_max > 8) nb_max = 8;
+    const bool silu = a.epilogue == QL_EPI_SILU_MUL;
+    const int out_ld = (int)(silu ? a.rows / 2 : a.rows);
     const int sms = num_sms();
 
     for (int b0 = 0; b0 < a.batch; b0 += nb_max) {
         const int nb = a.batch - b0 < nb_max ? a.batch - b0 : nb_max;
-        const int NB = nb <= 1 ? 1 : nb <= 2 ? 2 : nb <= 4 ? 4 : 8;
         KParams p = {};
         p.scales = a.scales;
         p.quants = a.quants;
@@ -496,29 +445,18 @@ int gemv_launch(const GemvArgs& a, cudaStream_t s, bool pdl) {
         p.residual = a.residual ? a.residual + (size_t)b0 * out_ld : nullptr;
         p.keys = a.argmax_keys ? a.argmax_keys + b0 : nullptr;
         p.active = a.active ? a.active + b0 : nullptr;
-        // rows per warp task: 4 when there is enough work to fill the GPU, else 2
-        const int eff_rows = (int)(a.epilogue == QL_EPI_SILU_MUL ? a.rows / 2 : a.rows);
-        const int per_task_4 = a.epilogue == QL_EPI_SILU_MUL ? 2 : 4;
-        const bool use4 = NB <= 2 && (eff_rows + per_task_4 - 1) / per_task_4 >= 2 * kWarps * sms;
-        const int R = use4 ? 4 : 2;
-        const int per_task = a.epilogue == QL_EPI_SILU_MUL ? R / 2 : R;
-        p.ntasks = (eff_rows + per_task - 1) / per_task;
-        int grid = (p.ntasks + kWarps - 1) / kWarps;
-        if (grid > 2 * sms) grid = 2 * sms;
-        p.tasks_per_cta = (p.ntasks + grid - 1) / grid;
-        grid = (p.ntasks + p.tasks_per_cta - 1) / p.tasks_per_cta;
-        const size_t smem = (size_t)NB * col_bytes;
-        cudaError_t e;
-        if (R == 4) {
-            e = NB == 1 ? launch_nb<1, 4>(p, grid, smem, s, pdl) : launch_nb<2, 4>(p, grid, smem, s, pdl);
-        } else {
-            switch (NB) {
-                case 1: e = launch_nb<1, 2>(p, grid, smem, s, pdl); break;
-                case 2: e = launch_nb<2, 2>(p, grid, smem, s, pdl); break;
-                case 4: e = launch_nb<4, 2>(p, grid, smem, s, pdl); break;
-                default: e = launch_nb<8, 2>(p, grid, smem, s, pdl); break;
-            }
-        }
+        p.ntile = silu ? (int)((a.rows / 2 + 7) / 8) : (int)((a.rows + 15) / 16);
+        // split K over the warps of a CTA until the grid holds ~3 warps per SM sub-partition
+        int S = 1;
+        while (S < kWarps && (long long)p.ntile * S < 12ll * sms && nblk / (2 * S) >= 8) S *= 2;
+        p.S = S;
+        p.seg_blocks = (nblk + S - 1) / S;
+        p.cstride = cstride;
+        const int tiles_per_cta = kWarps / S;
+        const int grid = (p.ntile + tiles_per_cta - 1) / tiles_per_cta;
+        const size_t smem = fixed + (size_t)nb * cstride * 16;
+        const cudaError_t e = launch(gemv_q4_0_mma_kernel, dim3(grid), dim3(kThreads), smem, s, pdl, p,
+                                     device_error_record());
         if (e != cudaSuccess) return cuda_error(e, "gemv launch");
     }
     return QL_OK;
