@@ -123,6 +123,29 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def graph_ms(fn, stream, reps: int, warm: int = 1) -> float:
+    """Capture ``fn`` (a sequence of library launches on ``stream``) into a CUDA graph and time
+    ``reps`` replays with CUDA events on that stream; returns ms per replay. Replaying a graph
+    keeps host launch overhead out of the kernel timings."""
+    import torch
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        fn()
+    for _ in range(warm):
+        graph.replay()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        e1.record(stream)
+    stream.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    del graph
+    return ms
+
+
 # ----------------------------------------------------------------------------- GPU arm
 def device_tensor_fn(cfg, seed: int):
     """Seeded device-side weight draws with the pages' distributions (N(0,0.02) matrices,
@@ -237,16 +260,9 @@ def gpu_arm(args, rank, world, local_rank):
             W = L["wgu"]
             ql.ql_gemv_q4_0(W.scales, W.quants, W.rows, W.cols, x16, B, act, ql.QL_DTYPE_F16,
                             ql.QL_EPI_SILU_MUL, None, s)
-    with torch.cuda.stream(s):
-        gu_all()
-        k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        k0.record(s)
-        for _ in range(reps):
-            gu_all()
-        k1.record(s)
-    s.synchronize()
+    gu_ms_rep = graph_ms(gu_all, s, reps)
     gu_launches = reps * cfg.n_layers
-    gu_ms = k0.elapsed_time(k1) / gu_launches
+    gu_ms = gu_ms_rep / cfg.n_layers
     W = gm.layers[0]["wgu"]
     gu_bytes = W.nbytes() + B * cfg.hidden * 2 + B * cfg.intermediate * 2
 
@@ -262,15 +278,8 @@ def gpu_arm(args, rank, world, local_rank):
             ql.ql_paged_attn_decode(qa, gm.k_pool[li], gm.v_pool[li], bt, at_ctx, B, cfg.n_heads,
                                     cfg.n_kv_heads, cfg.head_dim, 16, maxb, num_blocks,
                                     1.0 / math.sqrt(cfg.head_dim), oa, ws, s)
-    with torch.cuda.stream(s):
-        attn_all()
-        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a0.record(s)
-        for _ in range(reps):
-            attn_all()
-        a1.record(s)
-    s.synchronize()
-    at_ms = a0.elapsed_time(a1) / (reps * cfg.n_layers)
+    at_ms_rep = graph_ms(attn_all, s, reps)
+    at_ms = at_ms_rep / cfg.n_layers
     L = int(ctx_avg)
     at_bytes = B * (2 * L * cfg.n_kv_heads * cfg.head_dim * 2 + 4 * ((L + 15) // 16)) + B * cfg.n_heads * cfg.head_dim * 4
 
@@ -425,15 +434,11 @@ def micro_gemv(shapes, batches, iters):
                 for i in range(n):
                     W = Ws[i % copies]
                     ql.ql_gemv_q4_0(W.scales, W.quants, rows, cols, x, B, y, 0, 0, None, s)
+            n = max(iters, copies)
             with torch.cuda.stream(s):
-                run(max(copies, 8))
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                n = max(iters, copies)
-                e0.record(s)
-                run(n)
-                e1.record(s)
+                run(1)                  # first call outside capture (per-device set-up)
             s.synchronize()
-            us = e0.elapsed_time(e1) * 1e3 / n
+            us = graph_ms(lambda: run(n), s, 3) * 1e3 / n
             nbytes = one + B * cols * 2 + B * rows * 4
             gbs = nbytes / (us * 1e-6) / 1e9
             out.append({"kernel": "ql_gemv_q4_0", "rows": rows, "cols": cols, "batch": B,
@@ -478,18 +483,19 @@ def micro_attn(batches, iters):
         def run():
             ql.ql_paged_attn_decode(q, kp, vp, bt, cl, B, nh, nkv, hd, 16, maxb, num_blocks,
                                     1 / math.sqrt(hd), o, ws, s)
-        times = []
         with torch.cuda.stream(s):
-            run()
+            run()                       # first call outside capture (per-device set-up)
+        s.synchronize()
+
+        def flush_then_run():
             for _ in range(iters):
                 flush.fill_(1)          # evict the KV from L2 between launches
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(s)
                 run()
-                e1.record(s)
-                times.append((e0, e1))
-        s.synchronize()
-        us = statistics.median(a.elapsed_time(b) for a, b in times) * 1e3
+
+        def flush_only():
+            for _ in range(iters):
+                flush.fill_(1)
+        us = (graph_ms(flush_then_run, s, 3) - graph_ms(flush_only, s, 3)) * 1e3 / iters
         nbytes = sum(2 * int(L) * nkv * hd * 2 + 4 * ((int(L) + 15) // 16) for L in lens) + B * nh * hd * 4
         gbs = nbytes / (us * 1e-6) / 1e9
         print(json.dumps({"kernel": "ql_paged_attn_decode", "batch": B, "sum_len": int(lens.sum()),

@@ -184,115 +184,15 @@ __device__ __forceinline__ void store_out(const KParams& p, int n, int row, floa
         reinterpret_cast<float*>(p.y)[o] = v;
 }
 
-__global__ void __launch_bounds__(kThreads, 3) gemv_q4_0_mma_kernel(KParams p, DevError* err) {
-    extern __shared__ __align__(16) unsigned char smem[];
-    uint4* xs = reinterpret_cast<uint4*>(smem);
-    float* bias = reinterpret_cast<float*>(xs + (size_t)p.batch * p.cstride);
-    float* red = bias + (size_t)p.nblk * 8;           // [kWarps][32][4]
-    __shared__ unsigned long long kred[kWarps][8];
-    (void)err;
-
+// Combine the K segments of a tile, apply the epilogue and (argmax) reduce the keys.
+// Every thread of the CTA calls this (it contains CTA barriers).
+__device__ __forceinline__ void finish_tile(const KParams& p, float* red, unsigned long long (*kred)[8],
+                                            int tile, int seg, float (&acc)[4], bool oka, bool okb) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, t = lane & 3;
     const bool silu_mul = (p.epilogue == QL_EPI_SILU_MUL);
-    const int half_rows = p.rows >> 1;
-    const int tiles_per_cta = kWarps / p.S;
-    const int tile = blockIdx.x * tiles_per_cta + warp / p.S;
-    const int seg = warp % p.S;
-
-    // The weights do not depend on the previous kernel: warm L2 with this CTA's first codes
-    // while the predecessor drains.
-    if (threadIdx.x == 0) {
-        const size_t row_bytes = (size_t)p.nblk * 16;
-        const int t0 = blockIdx.x * tiles_per_cta;
-        const int nt = min(tiles_per_cta, p.ntile - t0);
-        if (nt > 0) {
-            const int rows_per_tile = silu_mul ? 8 : 16;
-            const int limit = silu_mul ? half_rows : p.rows;
-            const int r0 = t0 * rows_per_tile;
-            size_t bytes = row_bytes * (size_t)min(nt * rows_per_tile, limit - r0);
-            bytes = bytes > 49152 ? 49152 : bytes;
-            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.quants + (size_t)r0 * row_bytes),
-                         "r"((uint32_t)bytes) : "memory");
-            if (silu_mul)
-                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
-                             ::"l"(p.quants + (size_t)(half_rows + r0) * row_bytes), "r"((uint32_t)bytes)
-                             : "memory");
-        }
-    }
-    pdl_wait();
-    stage_x(p, xs, bias, red);
-    __syncthreads();
-    pdl_trigger();
-
-    // rows of this lane: ra (fragment row g) and rb (row g + 8)
-    int ra, rb;
-    bool oka, okb;
-    if (silu_mul) {
-        const int i = tile * 8 + g;
-        oka = okb = (tile < p.ntile) && i < half_rows;
-        ra = oka ? i : 0;
-        rb = okb ? half_rows + i : 0;
-    } else {
-        ra = tile * 16 + g;
-        rb = ra + 8;
-        oka = (tile < p.ntile) && ra < p.rows;
-        okb = (tile < p.ntile) && rb < p.rows;
-        ra = oka ? ra : 0;
-        rb = okb ? rb : 0;
-    }
-    const int j0 = seg * p.seg_blocks;
-    const int j1 = (tile < p.ntile) ? min(p.nblk, j0 + p.seg_blocks) : j0;
-    const int nit = j1 > j0 ? j1 - j0 : 0;
-    const uint32_t* qa = reinterpret_cast<const uint32_t*>(p.quants) + ((size_t)ra * p.nblk + j0) * 4 + t;
-    const uint32_t* qb = reinterpret_cast<const uint32_t*>(p.quants) + ((size_t)rb * p.nblk + j0) * 4 + t;
-    const unsigned short* sa = reinterpret_cast<const unsigned short*>(p.scales) + (size_t)ra * p.nblk + j0;
-    const unsigned short* sb = reinterpret_cast<const unsigned short*>(p.scales) + (size_t)rb * p.nblk + j0;
-    const float mask_a = oka ? 1.f : 0.f, mask_b = okb ? 1.f : 0.f;
-    const bool has_col = g < p.batch;
-    const uint4* xcol = xs + (size_t)(has_col ? g : 0) * p.cstride;
-
-    uint32_t rwa[kD], rwb[kD], rsc[kD];
-#pragma unroll
-    for (int u = 0; u < kD; ++u) {
-        if (u < nit) {
-            rwa[u] = __ldg(qa + 4 * u);
-            rwb[u] = __ldg(qb + 4 * u);
-            rsc[u] = (uint32_t)__ldg(sa + u) | ((uint32_t)__ldg(sb + u) << 16);
-        }
-    }
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int it0 = 0; it0 < nit; it0 += kD) {
-#pragma unroll
-        for (int u = 0; u < kD; ++u) {
-            const int it = it0 + u;
-            if (it < nit) {
-                const int j = j0 + it;
-                const uint32_t wa = rwa[u], wb = rwb[u];
-                const __half2 sc = h2(rsc[u]);
-                const int nx = it + kD;
-                if (nx < nit) {
-                    rwa[u] = __ldg(qa + 4 * nx);
-                    rwb[u] = __ldg(qb + 4 * nx);
-                    rsc[u] = (uint32_t)__ldg(sa + nx) | ((uint32_t)__ldg(sb + nx) << 16);
-                }
-                uint4 X = has_col ? xcol[4 * j + t] : make_uint4(0u, 0u, 0u, 0u);
-                const float2 bz = *reinterpret_cast<const float2*>(bias + j * 8 + 2 * t);
-                float c[4] = {bz.x, bz.y, bz.x, bz.y};
-                const uint32_t sa8 = wa >> 8, sb8 = wb >> 8;
-                mma16816(c, (wa & 0x000F000Fu) | 0x64006400u, (wb & 0x000F000Fu) | 0x64006400u,
-                         (sa8 & 0x000F000Fu) | 0x64006400u, (sb8 & 0x000F000Fu) | 0x64006400u, X.x, X.y);
-                mma16816(c, (wa & 0x00F000F0u) | 0x64006400u, (wb & 0x00F000F0u) | 0x64006400u,
-                         (sa8 & 0x00F000F0u) | 0x64006400u, (sb8 & 0x00F000F0u) | 0x64006400u, X.z, X.w);
-                const float2 d = __half22float2(sc);
-                acc[0] = fmaf(d.x, c[0], acc[0]);
-                acc[1] = fmaf(d.x, c[1], acc[1]);
-                acc[2] = fmaf(d.y, c[2], acc[2]);
-                acc[3] = fmaf(d.y, c[3], acc[3]);
-            }
-        }
-    }
-    acc[0] *= mask_a; acc[1] *= mask_a; acc[2] *= mask_b; acc[3] *= mask_b;
+    if (!oka) acc[0] = acc[1] = 0.f;
+    if (!okb) acc[2] = acc[3] = 0.f;
 
     // combine the K segments of a tile
     if (p.S > 1) {
@@ -377,6 +277,277 @@ __global__ void __launch_bounds__(kThreads, 3) gemv_q4_0_mma_kernel(KParams p, D
     }
 }
 
+__global__ void __launch_bounds__(kThreads, 3) gemv_q4_0_mma_kernel(KParams p, DevError* err) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    uint4* xs = reinterpret_cast<uint4*>(smem);
+    float* bias = reinterpret_cast<float*>(xs + (size_t)p.batch * p.cstride);
+    float* red = bias + (size_t)p.nblk * 8;           // [kWarps][32][4]
+    __shared__ unsigned long long kred[kWarps][8];
+    (void)err;
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const bool silu_mul = (p.epilogue == QL_EPI_SILU_MUL);
+    const int half_rows = p.rows >> 1;
+    const int tiles_per_cta = kWarps / p.S;
+    const int tile = blockIdx.x * tiles_per_cta + warp / p.S;
+    const int seg = warp % p.S;
+
+    // The weights do not depend on the previous kernel: warm L2 with this CTA's first codes
+    // while the predecessor drains.
+    if (threadIdx.x == 0) {
+        const size_t row_bytes = (size_t)p.nblk * 16;
+        const int t0 = blockIdx.x * tiles_per_cta;
+        const int nt = min(tiles_per_cta, p.ntile - t0);
+        if (nt > 0) {
+            const int rows_per_tile = silu_mul ? 8 : 16;
+            const int limit = silu_mul ? half_rows : p.rows;
+            const int r0 = t0 * rows_per_tile;
+            size_t bytes = row_bytes * (size_t)min(nt * rows_per_tile, limit - r0);
+            bytes = bytes > 49152 ? 49152 : bytes;
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.quants + (size_t)r0 * row_bytes),
+                         "r"((uint32_t)bytes) : "memory");
+            if (silu_mul)
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                             ::"l"(p.quants + (size_t)(half_rows + r0) * row_bytes), "r"((uint32_t)bytes)
+                             : "memory");
+        }
+    }
+    pdl_wait();
+    stage_x(p, xs, bias, red);
+    __syncthreads();
+    pdl_trigger();
+
+    // rows of this lane: ra (fragment row g) and rb (row g + 8)
+    int ra, rb;
+    bool oka, okb;
+    if (silu_mul) {
+        const int i = tile * 8 + g;
+        oka = okb = (tile < p.ntile) && i < half_rows;
+        ra = oka ? i : 0;
+        rb = okb ? half_rows + i : 0;
+    } else {
+        ra = tile * 16 + g;
+        rb = ra + 8;
+        oka = (tile < p.ntile) && ra < p.rows;
+        okb = (tile < p.ntile) && rb < p.rows;
+        ra = oka ? ra : 0;
+        rb = okb ? rb : 0;
+    }
+    const int j0 = seg * p.seg_blocks;
+    const int j1 = (tile < p.ntile) ? min(p.nblk, j0 + p.seg_blocks) : j0;
+    const int nit = j1 > j0 ? j1 - j0 : 0;
+    const uint32_t* qa = reinterpret_cast<const uint32_t*>(p.quants) + ((size_t)ra * p.nblk + j0) * 4 + t;
+    const uint32_t* qb = reinterpret_cast<const uint32_t*>(p.quants) + ((size_t)rb * p.nblk + j0) * 4 + t;
+    const unsigned short* sa = reinterpret_cast<const unsigned short*>(p.scales) + (size_t)ra * p.nblk + j0;
+    const unsigned short* sb = reinterpret_cast<const unsigned short*>(p.scales) + (size_t)rb * p.nblk + j0;
+    const bool has_col = g < p.batch;
+    const uint4* xcol = xs + (size_t)(has_col ? g : 0) * p.cstride;
+
+    uint32_t rwa[kD], rwb[kD], rsc[kD];
+#pragma unroll
+    for (int u = 0; u < kD; ++u) {
+        if (u < nit) {
+            rwa[u] = __ldg(qa + 4 * u);
+            rwb[u] = __ldg(qb + 4 * u);
+            rsc[u] = (uint32_t)__ldg(sa + u) | ((uint32_t)__ldg(sb + u) << 16);
+        }
+    }
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int it0 = 0; it0 < nit; it0 += kD) {
+#pragma unroll
+        for (int u = 0; u < kD; ++u) {
+            const int it = it0 + u;
+            if (it < nit) {
+                const int j = j0 + it;
+                const uint32_t wa = rwa[u], wb = rwb[u];
+                const __half2 sc = h2(rsc[u]);
+                const int nx = it + kD;
+                if (nx < nit) {
+                    rwa[u] = __ldg(qa + 4 * nx);
+                    rwb[u] = __ldg(qb + 4 * nx);
+                    rsc[u] = (uint32_t)__ldg(sa + nx) | ((uint32_t)__ldg(sb + nx) << 16);
+                }
+                uint4 X = has_col ? xcol[4 * j + t] : make_uint4(0u, 0u, 0u, 0u);
+                const float2 bz = *reinterpret_cast<const float2*>(bias + j * 8 + 2 * t);
+                float c[4] = {bz.x, bz.y, bz.x, bz.y};
+                const uint32_t sa8 = wa >> 8, sb8 = wb >> 8;
+                mma16816(c, (wa & 0x000F000Fu) | 0x64006400u, (wb & 0x000F000Fu) | 0x64006400u,
+                         (sa8 & 0x000F000Fu) | 0x64006400u, (sb8 & 0x000F000Fu) | 0x64006400u, X.x, X.y);
+                mma16816(c, (wa & 0x00F000F0u) | 0x64006400u, (wb & 0x00F000F0u) | 0x64006400u,
+                         (sa8 & 0x00F000F0u) | 0x64006400u, (sb8 & 0x00F000F0u) | 0x64006400u, X.z, X.w);
+                const float2 d = __half22float2(sc);
+                acc[0] = fmaf(d.x, c[0], acc[0]);
+                acc[1] = fmaf(d.x, c[1], acc[1]);
+                acc[2] = fmaf(d.y, c[2], acc[2]);
+                acc[3] = fmaf(d.y, c[3], acc[3]);
+            }
+        }
+    }
+    finish_tile(p, red, kred, tile, seg, acc, oka, okb);
+}
+
+
+// ---------------------------------------------------------------------------------------------
+// The same GEMV with the codes streamed into shared memory by the bulk-copy engine. Each warp
+// owns a ring of NS stages; a stage holds 8 blocks (256 k) of its 16 rows: 128 code bytes per
+// row (rows padded to 144 B so the 8 row-lanes of a load hit distinct banks) and 16 scale bytes
+// per row. Lanes 0..15 each issue the two copies of one row; completion is tracked by one
+// mbarrier per stage (expect-tx bytes). The first NS stages are issued before the kernel waits
+// on its predecessor, so the weight stream starts while the previous kernel drains.
+constexpr int kStageBlocks = 8;
+constexpr int kRowPitch = 144;
+constexpr int kStageBytes = 16 * kRowPitch + 16 * 16;   // codes + scales of 16 rows
+constexpr long long kSpinLimit = 1ll << 26;             // bounded mbarrier waits
+
+__device__ __forceinline__ uint32_t smem_u32(const void* ptr) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(ptr));
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    for (long long i = 0; i < kSpinLimit; ++i) {
+        uint32_t ok;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+            " selp.u32 %0, 1, 0, p;\n}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (ok) return true;
+    }
+    return false;
+}
+
+// Issue the copies of one stage: lane r < 16 copies row r's 128 code bytes and 16 scale bytes.
+__device__ __forceinline__ void issue_stage(const KParams& p, uint32_t ring, uint32_t bar, int lane,
+                                            int row_r, bool ok_r, int jblk, uint32_t bytes) {
+    if (lane == 0)
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+    __syncwarp();
+    if (lane < 16 && ok_r) {
+        const uint8_t* src = p.quants + ((size_t)row_r * p.nblk + jblk) * 16;
+        const __half* ssrc = p.scales + (size_t)row_r * p.nblk + jblk;
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], 128, [%2];"
+            ::"r"(ring + lane * kRowPitch), "l"(src), "r"(bar) : "memory");
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], 16, [%2];"
+            ::"r"(ring + 16 * kRowPitch + lane * 16), "l"(ssrc), "r"(bar) : "memory");
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 2) gemv_q4_0_bulk_kernel(KParams p, int NS, DevError* err) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    // layout: rings | mbarriers | xs | bias | red
+    unsigned char* rings = smem;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(rings + (size_t)kWarps * NS * kStageBytes);
+    uint4* xs = reinterpret_cast<uint4*>(bars + kWarps * NS);
+    float* bias = reinterpret_cast<float*>(xs + (size_t)p.batch * p.cstride);
+    float* red = bias + (size_t)p.nblk * 8;
+    __shared__ unsigned long long kred[kWarps][8];
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const bool silu_mul = (p.epilogue == QL_EPI_SILU_MUL);
+    const int half_rows = p.rows >> 1;
+    const int tiles_per_cta = kWarps / p.S;
+    const int tile = blockIdx.x * tiles_per_cta + warp / p.S;
+    const int seg = warp % p.S;
+    const bool live = tile < p.ntile;
+
+    // the weight row each lane copies (lanes 0..15 -> tile rows 0..15)
+    const int rr = lane & 15;
+    int row_r;
+    bool ok_r;
+    if (silu_mul) {
+        const int i = tile * 8 + (rr & 7);
+        ok_r = live && i < half_rows;
+        row_r = rr < 8 ? i : half_rows + i;
+    } else {
+        row_r = tile * 16 + rr;
+        ok_r = live && row_r < p.rows;
+    }
+    // bytes one stage delivers: 144 per valid row
+    uint32_t valid = __ballot_sync(0xffffffffu, lane < 16 && ok_r);
+    const uint32_t stage_bytes = (uint32_t)__popc(valid) * (128u + 16u);
+
+    const uint32_t ring0 = smem_u32(rings + (size_t)warp * NS * kStageBytes);
+    const uint32_t bar0 = smem_u32(bars + warp * NS);
+    if (lane == 0) {
+        for (int s2 = 0; s2 < NS; ++s2)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar0 + 8 * s2) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
+    const int j0 = seg * p.seg_blocks;
+    const int nst = live ? p.seg_blocks / kStageBlocks : 0;
+    // weights do not depend on the previous kernel: start streaming before the PDL wait
+    for (int s2 = 0; s2 < NS && s2 < nst; ++s2)
+        issue_stage(p, ring0 + s2 * kStageBytes, bar0 + 8 * s2, lane, row_r, ok_r, j0 + s2 * kStageBlocks,
+                    stage_bytes);
+
+    pdl_wait();
+    stage_x(p, xs, bias, red);
+    __syncthreads();
+    pdl_trigger();
+
+    const bool has_col = g < p.batch;
+    const uint4* xcol = xs + (size_t)(has_col ? g : 0) * p.cstride;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    bool failed = false;
+    for (int st = 0; st < nst; ++st) {
+        const int slot = st % NS;
+        const uint32_t ring = ring0 + slot * kStageBytes, bar = bar0 + 8 * slot;
+        // every lane observes the phase (visibility of the copied bytes); the decision is uniform
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(bar, (uint32_t)((st / NS) & 1)));
+        if (!ok) {
+            failed = true;
+            break;
+        }
+        const unsigned char* rs = rings + (size_t)(warp * NS + slot) * kStageBytes;
+        const uint32_t* ca = reinterpret_cast<const uint32_t*>(rs + g * kRowPitch) + t;
+        const uint32_t* cb = reinterpret_cast<const uint32_t*>(rs + (g + 8) * kRowPitch) + t;
+        const unsigned short* sca = reinterpret_cast<const unsigned short*>(rs + 16 * kRowPitch + g * 16);
+        const unsigned short* scb = reinterpret_cast<const unsigned short*>(rs + 16 * kRowPitch + (g + 8) * 16);
+        const int jb = j0 + st * kStageBlocks;
+#pragma unroll
+        for (int jj = 0; jj < kStageBlocks; ++jj) {
+            const uint32_t wa = ca[4 * jj], wb = cb[4 * jj];
+            const float da = __half2float(__ushort_as_half(sca[jj]));
+            const float db = __half2float(__ushort_as_half(scb[jj]));
+            const int j = jb + jj;
+            const uint4 X = has_col ? xcol[4 * j + t] : make_uint4(0u, 0u, 0u, 0u);
+            const float2 bz = *reinterpret_cast<const float2*>(bias + j * 8 + 2 * t);
+            float c[4] = {bz.x, bz.y, bz.x, bz.y};
+            const uint32_t sa8 = wa >> 8, sb8 = wb >> 8;
+            mma16816(c, (wa & 0x000F000Fu) | 0x64006400u, (wb & 0x000F000Fu) | 0x64006400u,
+                     (sa8 & 0x000F000Fu) | 0x64006400u, (sb8 & 0x000F000Fu) | 0x64006400u, X.x, X.y);
+            mma16816(c, (wa & 0x00F000F0u) | 0x64006400u, (wb & 0x00F000F0u) | 0x64006400u,
+                     (sa8 & 0x00F000F0u) | 0x64006400u, (sb8 & 0x00F000F0u) | 0x64006400u, X.z, X.w);
+            acc[0] = fmaf(da, c[0], acc[0]);
+            acc[1] = fmaf(da, c[1], acc[1]);
+            acc[2] = fmaf(db, c[2], acc[2]);
+            acc[3] = fmaf(db, c[3], acc[3]);
+        }
+        __syncwarp();
+        if (st + NS < nst) {
+            // the slot's generic-proxy reads are done; order them before the async-proxy refill
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue_stage(p, ring, bar, lane, row_r, ok_r, j0 + (st + NS) * kStageBlocks, stage_bytes);
+        }
+    }
+    if (failed && lane == 0) record_device_error(err, kErrGemvStage, tile, seg);
+    // fragment rows of this lane
+    bool oka, okb;
+    if (silu_mul) {
+        oka = okb = live && tile * 8 + g < half_rows;
+    } else {
+        oka = live && tile * 16 + g < p.rows;
+        okb = live && tile * 16 + g + 8 < p.rows;
+    }
+    finish_tile(p, red, kred, tile, seg, acc, oka, okb);
+}
+
 }  // namespace
 
 // Kernel attributes are set once per device, outside any stream capture.
@@ -387,8 +558,10 @@ int gemv_prepare() {
     QL_TRY_CUDA(cudaGetDevice(&dev));
     std::lock_guard<std::mutex> lk(mu);
     if (done.count(dev)) return QL_OK;
-    const cudaError_t e = cudaFuncSetAttribute(gemv_q4_0_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)kMaxStageBytes);
+    cudaError_t e = cudaFuncSetAttribute(gemv_q4_0_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kMaxStageBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gemv_q4_0_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e != cudaSuccess) return cuda_error(e, "gemv: cudaFuncSetAttribute");
     done.insert(dev);
     return QL_OK;
@@ -446,17 +619,35 @@ int gemv_launch(const GemvArgs& a, cudaStream_t s, bool pdl) {
         p.keys = a.argmax_keys ? a.argmax_keys + b0 : nullptr;
         p.active = a.active ? a.active + b0 : nullptr;
         p.ntile = silu ? (int)((a.rows / 2 + 7) / 8) : (int)((a.rows + 15) / 16);
-        // split K over the warps of a CTA until the grid holds ~3 warps per SM sub-partition
-        int S = 1;
-        while (S < kWarps && (long long)p.ntile * S < 12ll * sms && nblk / (2 * S) >= 8) S *= 2;
-        p.S = S;
-        p.seg_blocks = (nblk + S - 1) / S;
         p.cstride = cstride;
-        const int tiles_per_cta = kWarps / S;
-        const int grid = (p.ntile + tiles_per_cta - 1) / tiles_per_cta;
-        const size_t smem = fixed + (size_t)nb * cstride * 16;
-        const cudaError_t e = launch(gemv_q4_0_mma_kernel, dim3(grid), dim3(kThreads), smem, s, pdl, p,
-                                     device_error_record());
+        const size_t stage_smem = fixed + (size_t)nb * cstride * 16;
+        // The bulk-copy kernel needs whole 8-block stages and 16-byte aligned scale rows.
+        const bool bulk = nblk % kStageBlocks == 0 && (reinterpret_cast<uintptr_t>(a.scales) & 15) == 0;
+        int S = 1;
+        cudaError_t e;
+        if (bulk) {
+            // split K over the warps of a CTA until the grid holds ~3 warps per SM sub-partition,
+            // keeping whole stages and at least two of them per segment
+            while (S < kWarps && (long long)p.ntile * S < 12ll * sms && nblk % (16 * S) == 0 &&
+                   nblk / (2 * S) >= 2 * kStageBlocks)
+                S *= 2;
+            p.S = S;
+            p.seg_blocks = nblk / S;
+            const size_t per_stage = (size_t)kWarps * (kStageBytes + 8);
+            int NS = (int)(((size_t)113 * 1024 - stage_smem) / per_stage);
+            NS = NS > 4 ? 4 : NS < 2 ? 2 : NS;
+            const size_t smem = (size_t)NS * per_stage + stage_smem;
+            const int grid = (p.ntile + kWarps / S - 1) / (kWarps / S);
+            e = launch(gemv_q4_0_bulk_kernel, dim3(grid), dim3(kThreads), smem, s, pdl, p, NS,
+                       device_error_record());
+        } else {
+            while (S < kWarps && (long long)p.ntile * S < 12ll * sms && nblk / (2 * S) >= 8) S *= 2;
+            p.S = S;
+            p.seg_blocks = (nblk + S - 1) / S;
+            const int grid = (p.ntile + kWarps / S - 1) / (kWarps / S);
+            e = launch(gemv_q4_0_mma_kernel, dim3(grid), dim3(kThreads), stage_smem, s, pdl, p,
+                       device_error_record());
+        }
         if (e != cudaSuccess) return cuda_error(e, "gemv launch");
     }
     return QL_OK;

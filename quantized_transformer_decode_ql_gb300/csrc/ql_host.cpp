@@ -78,6 +78,7 @@ static const char* where_name(int w) {
         case kErrAttnLength: return "attention: context length outside the block table";
         case kErrPackNonFinite: return "q4_0 pack: non-finite weight";
         case kErrPackOverflow: return "q4_0 pack: block scale overflows f16";
+        case kErrGemvStage: return "gemv: a staged weight copy did not arrive (bounded wait expired)";
         default: return "unknown";
     }
 }

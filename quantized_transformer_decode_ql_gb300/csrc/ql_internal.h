@@ -43,6 +43,7 @@ enum DevErrWhere {
     kErrAttnLength = 5,
     kErrPackNonFinite = 6,
     kErrPackOverflow = 7,
+    kErrGemvStage = 8,
 };
 // The current device's record (allocated on first use, zero-filled).
 DevError* device_error_record();
