@@ -561,7 +561,7 @@ int gemv_prepare() {
     cudaError_t e = cudaFuncSetAttribute(gemv_q4_0_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kMaxStageBytes);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(gemv_q4_0_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        e = cudaFuncSetAttribute(gemv_q4_0_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
     if (e != cudaSuccess) return cuda_error(e, "gemv: cudaFuncSetAttribute");
     done.insert(dev);
     return QL_OK;
