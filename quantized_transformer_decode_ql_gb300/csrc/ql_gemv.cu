@@ -125,53 +125,53 @@ __device__ void stage_x(const KParams& p, uint4* xs, float* bias, float* red) {
         }
         __syncthreads();   // red is reused later
     }
-    for (int item = tid; item < 8 * p.nblk; item += kThreads) {
-        const int b = item / p.nblk, j = item - b * p.nblk;
-        if (b >= p.batch) {
-            bias[j * 8 + b] = 0.f;
-            continue;
-        }
-        float v[32];
-        const size_t base = (size_t)b * cols + 32 * j;
-        if (p.prologue == kProRmsF32) {
-            float rr = rs[0];
+    // one item = one 16-byte chunk (column b, block j, lane slot t); the 4 chunks of a block are
+    // handled by 4 consecutive threads, which reduce the block's offset term with shuffles
+    const int nitems = 8 * p.nblk * 4;
+    for (int base_item = tid - (tid & 3); base_item < nitems; base_item += kThreads) {
+        const int item = base_item + (tid & 3);
+        const int t = item & 3, bj = item >> 2;
+        const int b = bj / p.nblk, j = bj - b * p.nblk;
+        float lo[4] = {0.f, 0.f, 0.f, 0.f}, hi[4] = {0.f, 0.f, 0.f, 0.f};
+        if (b < p.batch) {
+            const size_t off = (size_t)b * cols + 32 * j + 4 * t;
+            if (p.prologue == kProRmsF32) {
+                float rr = rs[0];
 #pragma unroll
-            for (int bb = 1; bb < 8; ++bb)
-                if (bb == b) rr = rs[bb];
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const float4 a = *reinterpret_cast<const float4*>(p.xf + base + 4 * c);
-                const float4 w = *reinterpret_cast<const float4*>(p.norm_w + 32 * j + 4 * c);
-                v[4 * c + 0] = __half2float(__float2half_rn(a.x * rr * w.x));
-                v[4 * c + 1] = __half2float(__float2half_rn(a.y * rr * w.y));
-                v[4 * c + 2] = __half2float(__float2half_rn(a.z * rr * w.z));
-                v[4 * c + 3] = __half2float(__float2half_rn(a.w * rr * w.w));
-            }
-        } else {
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const uint4 u = *reinterpret_cast<const uint4*>(p.x16 + base + 8 * c);
-                const float2 f0 = __half22float2(h2(u.x)), f1 = __half22float2(h2(u.y));
-                const float2 f2 = __half22float2(h2(u.z)), f3 = __half22float2(h2(u.w));
-                v[8 * c + 0] = f0.x; v[8 * c + 1] = f0.y; v[8 * c + 2] = f1.x; v[8 * c + 3] = f1.y;
-                v[8 * c + 4] = f2.x; v[8 * c + 5] = f2.y; v[8 * c + 6] = f3.x; v[8 * c + 7] = f3.y;
+                for (int bb = 1; bb < 8; ++bb)
+                    if (bb == b) rr = rs[bb];
+                const float4 a4 = *reinterpret_cast<const float4*>(p.xf + off);
+                const float4 h4 = *reinterpret_cast<const float4*>(p.xf + off + 16);
+                const float4 wa = *reinterpret_cast<const float4*>(p.norm_w + 32 * j + 4 * t);
+                const float4 wh = *reinterpret_cast<const float4*>(p.norm_w + 32 * j + 16 + 4 * t);
+                lo[0] = a4.x * rr * wa.x; lo[1] = a4.y * rr * wa.y; lo[2] = a4.z * rr * wa.z; lo[3] = a4.w * rr * wa.w;
+                hi[0] = h4.x * rr * wh.x; hi[1] = h4.y * rr * wh.y; hi[2] = h4.z * rr * wh.z; hi[3] = h4.w * rr * wh.w;
+            } else {
+                const uint2 a2 = *reinterpret_cast<const uint2*>(p.x16 + off);
+                const uint2 h2v = *reinterpret_cast<const uint2*>(p.x16 + off + 16);
+                const float2 f0 = __half22float2(h2(a2.x)), f1 = __half22float2(h2(a2.y));
+                const float2 f2 = __half22float2(h2(h2v.x)), f3 = __half22float2(h2(h2v.y));
+                lo[0] = f0.x; lo[1] = f0.y; lo[2] = f1.x; lo[3] = f1.y;
+                hi[0] = f2.x; hi[1] = f2.y; hi[2] = f3.x; hi[3] = f3.y;
             }
         }
-        float lo = 0.f, hi = 0.f;
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            const __half2 p0 = __floats2half2_rn(v[4 * t], v[4 * t + 2]);
-            const __half2 p1 = __floats2half2_rn(v[4 * t + 1], v[4 * t + 3]);
-            const __half2 p2 = __floats2half2_rn(v[16 + 4 * t] * 0.0625f, v[18 + 4 * t] * 0.0625f);
-            const __half2 p3 = __floats2half2_rn(v[17 + 4 * t] * 0.0625f, v[19 + 4 * t] * 0.0625f);
-            const float2 f0 = __half22float2(p0), f1 = __half22float2(p1);
-            const float2 f2 = __half22float2(p2), f3 = __half22float2(p3);
-            lo += (f0.x + f0.y) + (f1.x + f1.y);
-            hi += (f2.x + f2.y) + (f3.x + f3.y);
-            xs[b * p.cstride + 4 * j + t] = make_uint4(u32(p0), u32(p1), u32(p2), u32(p3));
-        }
+        // activations rounded to f16 (the GEMV's input precision); high ones pre-divided by 16
+        const __half2 p0 = __floats2half2_rn(lo[0], lo[2]);
+        const __half2 p1 = __floats2half2_rn(lo[1], lo[3]);
+        const __half2 p2 = __floats2half2_rn(__half2float(__float2half_rn(hi[0])) * 0.0625f,
+                                             __half2float(__float2half_rn(hi[2])) * 0.0625f);
+        const __half2 p3 = __floats2half2_rn(__half2float(__float2half_rn(hi[1])) * 0.0625f,
+                                             __half2float(__float2half_rn(hi[3])) * 0.0625f);
+        const float2 f0 = __half22float2(p0), f1 = __half22float2(p1);
+        const float2 f2 = __half22float2(p2), f3 = __half22float2(p3);
         // sum (1024 + q) x_lo + (1024 + 16 q) x_hi/16 = sum (q - 8) x + 1032 sum x_lo + 1152 sum x_hi/16
-        bias[j * 8 + b] = -(1032.0f * lo + 1152.0f * hi);
+        float part = 1032.0f * ((f0.x + f0.y) + (f1.x + f1.y)) + 1152.0f * ((f2.x + f2.y) + (f3.x + f3.y));
+        part += __shfl_xor_sync(0xffffffffu, part, 1);
+        part += __shfl_xor_sync(0xffffffffu, part, 2);
+        if (item < nitems) {
+            if (b < p.batch) xs[b * p.cstride + 4 * j + t] = make_uint4(u32(p0), u32(p1), u32(p2), u32(p3));
+            if (t == 0) bias[j * 8 + b] = -part;
+        }
     }
 }
 
@@ -389,62 +389,32 @@ __global__ void __launch_bounds__(kThreads, 3) gemv_q4_0_mma_kernel(KParams p, D
 
 
 // ---------------------------------------------------------------------------------------------
-// The same GEMV with the codes streamed into shared memory by the bulk-copy engine. Each warp
-// owns a ring of NS stages; a stage holds 8 blocks (256 k) of its 16 rows: 128 code bytes per
-// row (rows padded to 144 B so the 8 row-lanes of a load hit distinct banks) and 16 scale bytes
-// per row. Lanes 0..15 each issue the two copies of one row; completion is tracked by one
-// mbarrier per stage (expect-tx bytes). The first NS stages are issued before the kernel waits
-// on its predecessor, so the weight stream starts while the previous kernel drains.
-constexpr int kStageBlocks = 8;
-constexpr int kRowPitch = 144;
-constexpr int kStageBytes = 16 * kRowPitch + 16 * 16;   // codes + scales of 16 rows
-constexpr long long kSpinLimit = 1ll << 26;             // bounded mbarrier waits
+// The main GEMV kernel (K % 128 == 0). Code bytes are read with 16-byte coalesced loads - lane l
+// loads block (l >> 3) of tile row (l & 7), and of tile row (l & 7) + 8, so one warp load covers
+// 8 rows x 4 blocks - and kRing iterations (4 blocks each) of loads stay in flight per lane; the
+// first ones are issued before the kernel waits on its predecessor. Each iteration passes the
+// 1 KB of codes through a per-warp shared-memory tile: one 16-byte store per lane and two
+// ldmatrix.x4 hand every lane exactly the 32-bit code words its MMA fragments need (word t of
+// block j for rows g and g + 8), since an 8x8 b16 ldmatrix tile is 8 rows of 16 bytes - one
+// q4_0 block per row. The f16 scales of a fragment row's 4 blocks come in one 8-byte load.
+constexpr int kGroupBlocks = 4;
+constexpr int kRing = 3;
 
-__device__ __forceinline__ uint32_t smem_u32(const void* ptr) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(ptr));
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
 }
 
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-    for (long long i = 0; i < kSpinLimit; ++i) {
-        uint32_t ok;
-        asm volatile(
-            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-            " selp.u32 %0, 1, 0, p;\n}"
-            : "=r"(ok)
-            : "r"(bar), "r"(parity)
-            : "memory");
-        if (ok) return true;
-    }
-    return false;
-}
-
-// Issue the copies of one stage: lane r < 16 copies row r's 128 code bytes and 16 scale bytes.
-__device__ __forceinline__ void issue_stage(const KParams& p, uint32_t ring, uint32_t bar, int lane,
-                                            int row_r, bool ok_r, int jblk, uint32_t bytes) {
-    if (lane == 0)
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-    __syncwarp();
-    if (lane < 16 && ok_r) {
-        const uint8_t* src = p.quants + ((size_t)row_r * p.nblk + jblk) * 16;
-        const __half* ssrc = p.scales + (size_t)row_r * p.nblk + jblk;
-        asm volatile(
-            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], 128, [%2];"
-            ::"r"(ring + lane * kRowPitch), "l"(src), "r"(bar) : "memory");
-        asm volatile(
-            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], 16, [%2];"
-            ::"r"(ring + 16 * kRowPitch + lane * 16), "l"(ssrc), "r"(bar) : "memory");
-    }
-}
-
-__global__ void __launch_bounds__(kThreads, 2) gemv_q4_0_bulk_kernel(KParams p, int NS, DevError* err) {
+__global__ void __launch_bounds__(kThreads, 2) gemv_q4_0_lsm_kernel(KParams p, DevError* err) {
     extern __shared__ __align__(16) unsigned char smem[];
-    // layout: rings | mbarriers | xs | bias | red
-    unsigned char* rings = smem;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(rings + (size_t)kWarps * NS * kStageBytes);
-    uint4* xs = reinterpret_cast<uint4*>(bars + kWarps * NS);
+    // layout: per-warp code tiles (1 KB each) | xs | bias | red
+    uint4* tiles = reinterpret_cast<uint4*>(smem);
+    uint4* xs = tiles + kWarps * 64;
     float* bias = reinterpret_cast<float*>(xs + (size_t)p.batch * p.cstride);
     float* red = bias + (size_t)p.nblk * 8;
     __shared__ unsigned long long kred[kWarps][8];
+    (void)err;
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, t = lane & 3;
@@ -455,96 +425,127 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q4_0_bulk_kernel(KParams p, 
     const int seg = warp % p.S;
     const bool live = tile < p.ntile;
 
-    // the weight row each lane copies (lanes 0..15 -> tile rows 0..15)
-    const int rr = lane & 15;
-    int row_r;
-    bool ok_r;
+    // rows loaded by this lane (tile rows lr and lr + 8) and the fragment rows it computes (g, g + 8)
+    const int lr = lane & 7, lb = lane >> 3;
+    int rowA, rowB, ra, rb;
+    bool oka, okb, okA, okB;
     if (silu_mul) {
-        const int i = tile * 8 + (rr & 7);
-        ok_r = live && i < half_rows;
-        row_r = rr < 8 ? i : half_rows + i;
+        const int i0 = tile * 8;
+        okA = okB = live && i0 + lr < half_rows;
+        rowA = okA ? i0 + lr : 0;
+        rowB = okB ? half_rows + i0 + lr : 0;
+        oka = okb = live && i0 + g < half_rows;
+        ra = oka ? i0 + g : 0;
+        rb = okb ? half_rows + i0 + g : 0;
     } else {
-        row_r = tile * 16 + rr;
-        ok_r = live && row_r < p.rows;
+        rowA = tile * 16 + lr;
+        rowB = rowA + 8;
+        okA = live && rowA < p.rows;
+        okB = live && rowB < p.rows;
+        rowA = okA ? rowA : 0;
+        rowB = okB ? rowB : 0;
+        ra = tile * 16 + g;
+        rb = ra + 8;
+        oka = live && ra < p.rows;
+        okb = live && rb < p.rows;
+        ra = oka ? ra : 0;
+        rb = okb ? rb : 0;
     }
-    // bytes one stage delivers: 144 per valid row
-    uint32_t valid = __ballot_sync(0xffffffffu, lane < 16 && ok_r);
-    const uint32_t stage_bytes = (uint32_t)__popc(valid) * (128u + 16u);
-
-    const uint32_t ring0 = smem_u32(rings + (size_t)warp * NS * kStageBytes);
-    const uint32_t bar0 = smem_u32(bars + warp * NS);
-    if (lane == 0) {
-        for (int s2 = 0; s2 < NS; ++s2)
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar0 + 8 * s2) : "memory");
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncwarp();
     const int j0 = seg * p.seg_blocks;
-    const int nst = live ? p.seg_blocks / kStageBlocks : 0;
-    // weights do not depend on the previous kernel: start streaming before the PDL wait
-    for (int s2 = 0; s2 < NS && s2 < nst; ++s2)
-        issue_stage(p, ring0 + s2 * kStageBytes, bar0 + 8 * s2, lane, row_r, ok_r, j0 + s2 * kStageBlocks,
-                    stage_bytes);
+    const int nit = live ? p.seg_blocks / kGroupBlocks : 0;
+    const uint4* qA = reinterpret_cast<const uint4*>(p.quants) + (size_t)rowA * p.nblk + j0 + lb;
+    const uint4* qB = reinterpret_cast<const uint4*>(p.quants) + (size_t)rowB * p.nblk + j0 + lb;
+    const uint2* sA = reinterpret_cast<const uint2*>(p.scales + (size_t)ra * p.nblk + j0);
+    const uint2* sB = reinterpret_cast<const uint2*>(p.scales + (size_t)rb * p.nblk + j0);
 
+    uint4 rA[kRing], rB[kRing];
+    uint2 rsa[kRing], rsb[kRing];
+    // the weights do not depend on the previous kernel: start loading them before the PDL wait
+#pragma unroll
+    for (int u = 0; u < kRing; ++u) {
+        if (u < nit) {
+            rA[u] = __ldg(qA + kGroupBlocks * u);
+            rB[u] = __ldg(qB + kGroupBlocks * u);
+            rsa[u] = __ldg(sA + u);
+            rsb[u] = __ldg(sB + u);
+        }
+    }
+    if (threadIdx.x == 0 && live) {
+        // warm L2 with more of this CTA's rows
+        const size_t row_bytes = (size_t)p.nblk * 16;
+        const int rows_per_tile = silu_mul ? 8 : 16;
+        const int limit = silu_mul ? half_rows : p.rows;
+        const int r0 = blockIdx.x * tiles_per_cta * rows_per_tile;
+        size_t bytes = row_bytes * (size_t)min(tiles_per_cta * rows_per_tile, limit - r0);
+        bytes = bytes > 49152 ? 49152 : bytes;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.quants + (size_t)r0 * row_bytes),
+                     "r"((uint32_t)bytes) : "memory");
+        if (silu_mul)
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                         ::"l"(p.quants + (size_t)(half_rows + r0) * row_bytes), "r"((uint32_t)bytes)
+                         : "memory");
+    }
     pdl_wait();
     stage_x(p, xs, bias, red);
     __syncthreads();
     pdl_trigger();
 
+    uint4* tw = tiles + warp * 64;                 // [4 blocks][16 rows] x 16 B
+    const uint32_t tw_s = static_cast<uint32_t>(__cvta_generic_to_shared(tw));
+    // ldmatrix row address of this lane: matrix m = lane >> 3 -> (block m >> 1, rows (m & 1) * 8 + r)
+    const int lm = lane >> 3, lrow = lane & 7;
+    const uint32_t a_lo = tw_s + (uint32_t)(((lm >> 1) * 16 + (lm & 1) * 8 + lrow) * 16);
+    const uint32_t a_hi = a_lo + 2 * 16 * 16;      // blocks 2 and 3
     const bool has_col = g < p.batch;
     const uint4* xcol = xs + (size_t)(has_col ? g : 0) * p.cstride;
+
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    bool failed = false;
-    for (int st = 0; st < nst; ++st) {
-        const int slot = st % NS;
-        const uint32_t ring = ring0 + slot * kStageBytes, bar = bar0 + 8 * slot;
-        // every lane observes the phase (visibility of the copied bytes); the decision is uniform
-        const bool ok = __all_sync(0xffffffffu, mbar_wait(bar, (uint32_t)((st / NS) & 1)));
-        if (!ok) {
-            failed = true;
-            break;
-        }
-        const unsigned char* rs = rings + (size_t)(warp * NS + slot) * kStageBytes;
-        const uint32_t* ca = reinterpret_cast<const uint32_t*>(rs + g * kRowPitch) + t;
-        const uint32_t* cb = reinterpret_cast<const uint32_t*>(rs + (g + 8) * kRowPitch) + t;
-        const unsigned short* sca = reinterpret_cast<const unsigned short*>(rs + 16 * kRowPitch + g * 16);
-        const unsigned short* scb = reinterpret_cast<const unsigned short*>(rs + 16 * kRowPitch + (g + 8) * 16);
-        const int jb = j0 + st * kStageBlocks;
+    for (int it0 = 0; it0 < nit; it0 += kRing) {
 #pragma unroll
-        for (int jj = 0; jj < kStageBlocks; ++jj) {
-            const uint32_t wa = ca[4 * jj], wb = cb[4 * jj];
-            const float da = __half2float(__ushort_as_half(sca[jj]));
-            const float db = __half2float(__ushort_as_half(scb[jj]));
-            const int j = jb + jj;
-            const uint4 X = has_col ? xcol[4 * j + t] : make_uint4(0u, 0u, 0u, 0u);
-            const float2 bz = *reinterpret_cast<const float2*>(bias + j * 8 + 2 * t);
-            float c[4] = {bz.x, bz.y, bz.x, bz.y};
-            const uint32_t sa8 = wa >> 8, sb8 = wb >> 8;
-            mma16816(c, (wa & 0x000F000Fu) | 0x64006400u, (wb & 0x000F000Fu) | 0x64006400u,
-                     (sa8 & 0x000F000Fu) | 0x64006400u, (sb8 & 0x000F000Fu) | 0x64006400u, X.x, X.y);
-            mma16816(c, (wa & 0x00F000F0u) | 0x64006400u, (wb & 0x00F000F0u) | 0x64006400u,
-                     (sa8 & 0x00F000F0u) | 0x64006400u, (sb8 & 0x00F000F0u) | 0x64006400u, X.z, X.w);
-            acc[0] = fmaf(da, c[0], acc[0]);
-            acc[1] = fmaf(da, c[1], acc[1]);
-            acc[2] = fmaf(db, c[2], acc[2]);
-            acc[3] = fmaf(db, c[3], acc[3]);
-        }
-        __syncwarp();
-        if (st + NS < nst) {
-            // the slot's generic-proxy reads are done; order them before the async-proxy refill
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            issue_stage(p, ring, bar, lane, row_r, ok_r, j0 + (st + NS) * kStageBlocks, stage_bytes);
+        for (int u = 0; u < kRing; ++u) {
+            const int it = it0 + u;
+            if (it < nit) {
+                tw[lb * 16 + lr] = rA[u];
+                tw[lb * 16 + 8 + lr] = rB[u];
+                const uint2 sca = rsa[u], scb = rsb[u];
+                const int nx = it + kRing;
+                if (nx < nit) {
+                    rA[u] = __ldg(qA + kGroupBlocks * nx);
+                    rB[u] = __ldg(qB + kGroupBlocks * nx);
+                    rsa[u] = __ldg(sA + nx);
+                    rsb[u] = __ldg(sB + nx);
+                }
+                __syncwarp();
+                uint32_t w[8];   // wa0, wb0, wa1, wb1, wa2, wb2, wa3, wb3
+                ldsm_x4(a_lo, w[0], w[1], w[2], w[3]);
+                ldsm_x4(a_hi, w[4], w[5], w[6], w[7]);
+                __syncwarp();
+                const float2 da01 = __half22float2(h2(sca.x)), da23 = __half22float2(h2(sca.y));
+                const float2 db01 = __half22float2(h2(scb.x)), db23 = __half22float2(h2(scb.y));
+                const float da[4] = {da01.x, da01.y, da23.x, da23.y};
+                const float db[4] = {db01.x, db01.y, db23.x, db23.y};
+#pragma unroll
+                for (int q = 0; q < kGroupBlocks; ++q) {
+                    const int j = j0 + it * kGroupBlocks + q;
+                    const uint32_t wa = w[2 * q], wb = w[2 * q + 1];
+                    const uint4 X = has_col ? xcol[4 * j + t] : make_uint4(0u, 0u, 0u, 0u);
+                    const float2 bz = *reinterpret_cast<const float2*>(bias + j * 8 + 2 * t);
+                    float c[4] = {bz.x, bz.y, bz.x, bz.y};
+                    const uint32_t sa8 = wa >> 8, sb8 = wb >> 8;
+                    mma16816(c, (wa & 0x000F000Fu) | 0x64006400u, (wb & 0x000F000Fu) | 0x64006400u,
+                             (sa8 & 0x000F000Fu) | 0x64006400u, (sb8 & 0x000F000Fu) | 0x64006400u, X.x, X.y);
+                    mma16816(c, (wa & 0x00F000F0u) | 0x64006400u, (wb & 0x00F000F0u) | 0x64006400u,
+                             (sa8 & 0x00F000F0u) | 0x64006400u, (sb8 & 0x00F000F0u) | 0x64006400u, X.z, X.w);
+                    acc[0] = fmaf(da[q], c[0], acc[0]);
+                    acc[1] = fmaf(da[q], c[1], acc[1]);
+                    acc[2] = fmaf(db[q], c[2], acc[2]);
+                    acc[3] = fmaf(db[q], c[3], acc[3]);
+                }
+            }
         }
     }
-    if (failed && lane == 0) record_device_error(err, kErrGemvStage, tile, seg);
-    // fragment rows of this lane
-    bool oka, okb;
-    if (silu_mul) {
-        oka = okb = live && tile * 8 + g < half_rows;
-    } else {
-        oka = live && tile * 16 + g < p.rows;
-        okb = live && tile * 16 + g + 8 < p.rows;
-    }
+    (void)okA;
+    (void)okB;
     finish_tile(p, red, kred, tile, seg, acc, oka, okb);
 }
 
@@ -561,7 +562,8 @@ int gemv_prepare() {
     cudaError_t e = cudaFuncSetAttribute(gemv_q4_0_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kMaxStageBytes);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(gemv_q4_0_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+        e = cudaFuncSetAttribute(gemv_q4_0_lsm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kMaxStageBytes + kWarps * 1024);
     if (e != cudaSuccess) return cuda_error(e, "gemv: cudaFuncSetAttribute");
     done.insert(dev);
     return QL_OK;
@@ -621,25 +623,21 @@ int gemv_launch(const GemvArgs& a, cudaStream_t s, bool pdl) {
         p.ntile = silu ? (int)((a.rows / 2 + 7) / 8) : (int)((a.rows + 15) / 16);
         p.cstride = cstride;
         const size_t stage_smem = fixed + (size_t)nb * cstride * 16;
-        // The bulk-copy kernel needs whole 8-block stages and 16-byte aligned scale rows.
-        const bool bulk = nblk % kStageBlocks == 0 && (reinterpret_cast<uintptr_t>(a.scales) & 15) == 0;
+        // The main kernel needs whole 4-block groups and 8-byte aligned scale rows.
+        const bool main = nblk % kGroupBlocks == 0 && (reinterpret_cast<uintptr_t>(a.scales) & 7) == 0;
         int S = 1;
         cudaError_t e;
-        if (bulk) {
+        if (main) {
             // split K over the warps of a CTA until the grid holds ~3 warps per SM sub-partition,
-            // keeping whole stages and at least two of them per segment
-            while (S < kWarps && (long long)p.ntile * S < 12ll * sms && nblk % (16 * S) == 0 &&
-                   nblk / (2 * S) >= 2 * kStageBlocks)
+            // keeping whole groups and at least two groups per segment
+            while (S < kWarps && (long long)p.ntile * S < 12ll * sms && nblk % (2 * kGroupBlocks * S) == 0 &&
+                   nblk / (2 * S) >= 2 * kGroupBlocks)
                 S *= 2;
             p.S = S;
             p.seg_blocks = nblk / S;
-            const size_t per_stage = (size_t)kWarps * (kStageBytes + 8);
-            int NS = (int)(((size_t)113 * 1024 - stage_smem) / per_stage);
-            NS = NS > 4 ? 4 : NS < 2 ? 2 : NS;
-            const size_t smem = (size_t)NS * per_stage + stage_smem;
+            const size_t smem = (size_t)kWarps * 1024 + stage_smem;
             const int grid = (p.ntile + kWarps / S - 1) / (kWarps / S);
-            e = launch(gemv_q4_0_bulk_kernel, dim3(grid), dim3(kThreads), smem, s, pdl, p, NS,
-                       device_error_record());
+            e = launch(gemv_q4_0_lsm_kernel, dim3(grid), dim3(kThreads), smem, s, pdl, p, device_error_record());
         } else {
             while (S < kWarps && (long long)p.ntile * S < 12ll * sms && nblk / (2 * S) >= 8) S *= 2;
             p.S = S;
