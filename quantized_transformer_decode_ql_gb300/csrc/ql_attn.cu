@@ -22,6 +22,9 @@
 #include <cuda_fp16.h>
 #include <math.h>
 
+#include <mutex>
+#include <set>
+
 #include "ql_internal.h"
 
 namespace ql {
@@ -58,14 +61,24 @@ __device__ __forceinline__ float2 h2f(uint32_t u) {
     return __half22float2(h);
 }
 
+__device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 template <int HD, int G>
 __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AParams p, DevError* err) {
-    constexpr int HALF = HD / 2;         // dims per lane in the score phase
-    constexpr int DPL = HD / 32;         // output dims per lane in the P.V phase
-    __shared__ float q_s[G][HD];
-    __shared__ float p_s[kAttnWarps][kBS][G];
+    constexpr int KSTEPS = HD / 16;           // k-steps of the Q.K^T MMA
+    constexpr int NT = HD / 8;                // 8-dim output tiles of the P.V MMA
+    constexpr int PITCH = HD * 2 + 16;        // bytes per staged K/V row (padded: conflict-free ldmatrix)
+    constexpr int TILE = kBS * PITCH;         // one staged 16-key K or V tile
+    constexpr int CHUNKS = HD * 2 / 16;       // 16-byte chunks per K/V row
+    extern __shared__ __align__(16) unsigned char asmem[];   // staged tiles, later the merge buffers
     __shared__ float wm[kAttnWarps][G], wl[kAttnWarps][G];
-    __shared__ float wacc[kAttnWarps][G][HD];
     __shared__ int last_flag;
 
     const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -100,123 +113,137 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AParams p, Dev
     const int blk0 = s * p.spb;
     const int blk1 = min(nblocks, blk0 + p.spb);
 
-    for (int i = threadIdx.x; i < G * HD; i += kAttnThreads) {
-        const int h = i / HD, d = i - h * HD;
-        q_s[h][d] = __half2float(p.q[((size_t)b * p.n_heads + g * G + h) * HD + d]);
-    }
-    __syncthreads();
-
-    float m[G], l[G], acc[G][DPL];
+    // Q as the A operand of S = Q K^T: rows = the G heads of this kv head (rows >= G and the
+    // fragment's rows g + 8 are zero padding); lane (gq, tq) holds dims 16 kk + 2 tq (+8).
+    const int gq = lane >> 2, tq = lane & 3;
+    const bool hv = gq < G;
+    uint32_t qa[KSTEPS][2];
+    {
+        const uint32_t* qrow =
+            reinterpret_cast<const uint32_t*>(p.q + ((size_t)b * p.n_heads + g * G + (hv ? gq : 0)) * HD);
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-        m[h] = -INFINITY;
-        l[h] = 0.f;
-#pragma unroll
-        for (int e = 0; e < DPL; ++e) acc[h][e] = 0.f;
+        for (int kk = 0; kk < KSTEPS; ++kk) {
+            qa[kk][0] = hv ? qrow[8 * kk + tq] : 0u;
+            qa[kk][1] = hv ? qrow[8 * kk + 4 + tq] : 0u;
+        }
     }
-    const int t = lane & 15, half = lane >> 4;
+    float o[NT][4];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    float mrow = -INFINITY, lrow = 0.f;
     const int32_t* bt = p.block_tables + (size_t)b * p.maxb;
+    unsigned char* wtiles = asmem + (size_t)warp * 4 * TILE;        // [buffer][K | V]
+    const uint32_t wtiles_s = static_cast<uint32_t>(__cvta_generic_to_shared(wtiles));
+    const int nb_w = blk1 - blk0 > warp ? (blk1 - blk0 - warp + kAttnWarps - 1) / kAttnWarps : 0;
 
-    for (int blk = blk0 + warp; blk < blk1; blk += kAttnWarps) {
+    // stage block i of this warp into buffer (i & 1) with 16-byte asynchronous copies
+    auto stage = [&](int i) -> bool {
+        const int blk = blk0 + warp + kAttnWarps * i;
         const int phys = bt[blk];
-        if (phys < 0 || phys >= p.num_blocks) {
+        bool ok = phys >= 0 && phys < p.num_blocks;
+        if (!ok) {
             if (lane == 0) record_device_error(err, kErrAttnBlock, (long long)b * p.maxb + blk, phys);
-            continue;
-        }
-        const size_t tile = ((size_t)phys * p.n_kv + g) * kBS * HD;
-        const int nt = min(kBS, L - blk * kBS);      // valid keys in this block
-        // ---- scores
-        const uint4* kr = reinterpret_cast<const uint4*>(p.k_pool + tile + (size_t)t * HD + half * HALF);
-        uint4 kv[HALF / 8];
-#pragma unroll
-        for (int c = 0; c < HALF / 8; ++c) kv[c] = kr[c];
-        // V rows for this lane's output dims, all 16 keys (issued early)
-        uint32_t vv[kBS][DPL / 2];
-        const __half* vb = p.v_pool + tile + lane * DPL;
-#pragma unroll
-        for (int k = 0; k < kBS; ++k) {
-            if (DPL == 4) {
-                const uint2 u = *reinterpret_cast<const uint2*>(vb + (size_t)k * HD);
-                vv[k][0] = u.x;
-                if (DPL / 2 > 1) vv[k][DPL / 2 - 1] = u.y;
-            } else {
-                vv[k][0] = *reinterpret_cast<const uint32_t*>(vb + (size_t)k * HD);
+        } else {
+            const __half* ksrc = p.k_pool + ((size_t)phys * p.n_kv + g) * kBS * HD;
+            const __half* vsrc = p.v_pool + ((size_t)phys * p.n_kv + g) * kBS * HD;
+            const uint32_t kd = wtiles_s + (uint32_t)((i & 1) * 2 * TILE), vd = kd + TILE;
+            for (int c = lane; c < kBS * CHUNKS; c += 32) {
+                const int row = c / CHUNKS, col = c - row * CHUNKS;
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(kd + row * PITCH + col * 16),
+                             "l"(ksrc + row * HD + col * 8) : "memory");
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(vd + row * PITCH + col * 16),
+                             "l"(vsrc + row * HD + col * 8) : "memory");
             }
         }
-        float sc[G];
-#pragma unroll
-        for (int h = 0; h < G; ++h) sc[h] = 0.f;
-#pragma unroll
-        for (int c = 0; c < HALF / 8; ++c) {
-            const float2 k0 = h2f(kv[c].x), k1 = h2f(kv[c].y), k2 = h2f(kv[c].z), k3 = h2f(kv[c].w);
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const float* qq = &q_s[h][half * HALF + c * 8];
-                float a = sc[h];
-                a = fmaf(qq[0], k0.x, a); a = fmaf(qq[1], k0.y, a);
-                a = fmaf(qq[2], k1.x, a); a = fmaf(qq[3], k1.y, a);
-                a = fmaf(qq[4], k2.x, a); a = fmaf(qq[5], k2.y, a);
-                a = fmaf(qq[6], k3.x, a); a = fmaf(qq[7], k3.y, a);
-                sc[h] = a;
-            }
-        }
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-            sc[h] += __shfl_xor_sync(0xffffffffu, sc[h], 16);
-            sc[h] = (t < nt) ? sc[h] * p.scale_log2 : -INFINITY;
-        }
-        // ---- online softmax (16 keys live in lanes 0..15, mirrored in 16..31)
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-            float mb = sc[h];
-#pragma unroll
-            for (int o = 8; o; o >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, o));
-            const float mn = fmaxf(m[h], mb);
-            const float pr = exp2f(sc[h] - mn);
-            float ls = pr;
-#pragma unroll
-            for (int o = 8; o; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
-            const float alpha = exp2f(m[h] - mn);
-            l[h] = l[h] * alpha + ls;
-            m[h] = mn;
-#pragma unroll
-            for (int e = 0; e < DPL; ++e) acc[h][e] *= alpha;
-            if (half == 0) p_s[warp][t][h] = pr;
-        }
-        __syncwarp();
-        // ---- P.V
-#pragma unroll
-        for (int k = 0; k < kBS; ++k) {
-            if (k < nt) {
-                float pv[G];
-#pragma unroll
-                for (int h = 0; h < G; ++h) pv[h] = p_s[warp][k][h];
-#pragma unroll
-                for (int e2 = 0; e2 < DPL / 2; ++e2) {
-                    const float2 v = h2f(vv[k][e2]);
-#pragma unroll
-                    for (int h = 0; h < G; ++h) {
-                        acc[h][2 * e2] = fmaf(pv[h], v.x, acc[h][2 * e2]);
-                        acc[h][2 * e2 + 1] = fmaf(pv[h], v.y, acc[h][2 * e2 + 1]);
-                    }
-                }
-            }
-        }
-        __syncwarp();
-    }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        return ok;
+    };
 
-    // ---- merge the warps of this CTA
-    if (lane == 0) {
+    bool vcur = nb_w > 0 ? stage(0) : false;
+    for (int i = 0; i < nb_w; ++i) {
+        bool vnext = false;
+        if (i + 1 < nb_w) vnext = stage(i + 1);
+        else asm volatile("cp.async.commit_group;" ::: "memory");
+        asm volatile("cp.async.wait_group 1;" ::: "memory");
+        __syncwarp();
+        const int blk = blk0 + warp + kAttnWarps * i;
+        const int nt = min(kBS, L - blk * kBS);      // valid keys in this block
+        if (vcur) {
+            unsigned char* vtile = wtiles + (size_t)(i & 1) * 2 * TILE + TILE;
+            if (nt < kBS) {
+                // keys past the context: their P is 0, but a stale V row must not be NaN/Inf
+                for (int c = lane; c < (kBS - nt) * CHUNKS; c += 32) {
+                    const int row = nt + c / CHUNKS, col = c % CHUNKS;
+                    *reinterpret_cast<uint4*>(vtile + row * PITCH + col * 16) = make_uint4(0u, 0u, 0u, 0u);
+                }
+                __syncwarp();
+            }
+            const uint32_t ks = wtiles_s + (uint32_t)((i & 1) * 2 * TILE), vs = ks + TILE;
+            // ---- S = Q K^T for the 16 keys (two 8-key tiles)
+            float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+            const int lm = lane >> 3, lr = lane & 7;
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-            wm[warp][h] = m[h];
-            wl[warp][h] = l[h];
+            for (int kk = 0; kk < KSTEPS; ++kk) {
+                uint32_t b0, b1, b2, b3;
+                const uint32_t addr = ks + (uint32_t)(((lm >> 1) * 8 + lr) * PITCH + (16 * kk + (lm & 1) * 8) * 2);
+                asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                             : "=r"(b0), "=r"(b1), "=r"(b2), "=r"(b3) : "r"(addr));
+                mma_f16(s0, qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
+                mma_f16(s1, qa[kk][0], 0u, qa[kk][1], 0u, b2, b3);
+            }
+            // ---- online softmax of head row gq over the block's keys (exp2 domain)
+            const int k0 = 2 * tq;
+            const float x0 = k0 < nt ? s0[0] * p.scale_log2 : -INFINITY;
+            const float x1 = k0 + 1 < nt ? s0[1] * p.scale_log2 : -INFINITY;
+            const float x2 = k0 + 8 < nt ? s1[0] * p.scale_log2 : -INFINITY;
+            const float x3 = k0 + 9 < nt ? s1[1] * p.scale_log2 : -INFINITY;
+            float mb = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+            mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+            mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+            const float mn = fmaxf(mrow, mb);
+            const float alpha = exp2f(mrow - mn);
+            const float p0 = exp2f(x0 - mn), p1 = exp2f(x1 - mn), p2 = exp2f(x2 - mn), p3 = exp2f(x3 - mn);
+            float ls = (p0 + p1) + (p2 + p3);
+            ls += __shfl_xor_sync(0xffffffffu, ls, 1);
+            ls += __shfl_xor_sync(0xffffffffu, ls, 2);
+            lrow = lrow * alpha + ls;
+            mrow = mn;
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                o[n][0] *= alpha;
+                o[n][1] *= alpha;
+            }
+            const __half2 pa0 = __floats2half2_rn(p0, p1), pa1 = __floats2half2_rn(p2, p3);
+            const uint32_t ua0 = *reinterpret_cast<const uint32_t*>(&pa0);
+            const uint32_t ua1 = *reinterpret_cast<const uint32_t*>(&pa1);
+            // ---- O += P V (V^T fragments by transposing ldmatrix)
+#pragma unroll
+            for (int pp = 0; pp < NT / 2; ++pp) {
+                uint32_t r0, r1, r2, r3;
+                const uint32_t addr = vs + (uint32_t)(((lm & 1) * 8 + lr) * PITCH + (16 * pp + (lm >> 1) * 8) * 2);
+                asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                             : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+                mma_f16(o[2 * pp], ua0, 0u, ua1, 0u, r0, r1);
+                mma_f16(o[2 * pp + 1], ua0, 0u, ua1, 0u, r2, r3);
+            }
+        }
+        __syncwarp();
+        vcur = vnext;
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncthreads();   // every warp is done with its tiles: the buffer now holds the merge state
+    float* wacc = reinterpret_cast<float*>(asmem);   // [warp][G][HD]
+    if (hv) {
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            wacc[(warp * G + gq) * HD + 8 * n + 2 * tq] = o[n][0];
+            wacc[(warp * G + gq) * HD + 8 * n + 2 * tq + 1] = o[n][1];
+        }
+        if (tq == 0) {
+            wm[warp][gq] = mrow;
+            wl[warp][gq] = lrow;
         }
     }
-#pragma unroll
-    for (int h = 0; h < G; ++h)
-#pragma unroll
-        for (int e = 0; e < DPL; ++e) wacc[warp][h][lane * DPL + e] = acc[h][e];
     __syncthreads();
 
     const int n_heads = p.n_heads;
@@ -230,7 +257,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AParams p, Dev
         for (int w = 0; w < kAttnWarps; ++w) {
             const float f = (wm[w][h] == -INFINITY) ? 0.f : exp2f(wm[w][h] - M);
             Ls += wl[w][h] * f;
-            A += wacc[w][h][d] * f;
+            A += wacc[(w * G + h) * HD + d] * f;
         }
         const int hg = g * G + h;
         if (n_active == 1) {
@@ -257,7 +284,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AParams p, Dev
     __threadfence();
     // merge: per-split weights exp2(m_k - M) / L into shared memory (one warp per head), then
     // every thread sums float4 chunks of the partial outputs with independent loads
-    __shared__ float sw[G][kMaxSplit];
+    float (*sw)[kMaxSplit] = reinterpret_cast<float (*)[kMaxSplit]>(asmem + (size_t)kAttnWarps * G * HD * 4);
     for (int h = warp; h < G; h += kAttnWarps) {
         const size_t base = ((size_t)b * n_heads + g * G + h) * p.nsplit;
         float M = -INFINITY;
@@ -338,10 +365,25 @@ Layout layout(int64_t batch, int n_heads, int n_kv, int head_dim, int64_t maxb, 
     return lo;
 }
 
+// Dynamic shared memory of one CTA: the warps' double-buffered K/V tiles, reused afterwards for
+// the warp-merge state and the split-merge weights.
+template <int HD, int G>
+constexpr size_t attn_smem() {
+    const size_t tiles = (size_t)kAttnWarps * 4 * kBS * (HD * 2 + 16);
+    const size_t merge = (size_t)kAttnWarps * G * HD * 4 + (size_t)G * kMaxSplit * 4;
+    return tiles > merge ? tiles : merge;
+}
+
+template <int HD, int G>
+cudaError_t allow_attn_smem() {
+    return cudaFuncSetAttribute(attn_split_kernel<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)attn_smem<HD, G>());
+}
+
 template <int HD, int G>
 cudaError_t launch_hg(const AParams& p, int batch, cudaStream_t s, bool pdl) {
     dim3 grid(p.nsplit, p.n_kv, batch);
-    return launch(attn_split_kernel<HD, G>, grid, dim3(kAttnThreads), 0, s, pdl, p,
+    return launch(attn_split_kernel<HD, G>, grid, dim3(kAttnThreads), attn_smem<HD, G>(), s, pdl, p,
                   device_error_record());
 }
 
@@ -357,6 +399,27 @@ cudaError_t launch_h(const AParams& p, int G, int batch, cudaStream_t s, bool pd
 }
 
 }  // namespace
+
+// Kernel attributes (dynamic shared memory above 48 KB) once per device, outside any capture.
+int attn_prepare() {
+    static std::mutex mu;
+    static std::set<int> done;
+    int dev = 0;
+    QL_TRY_CUDA(cudaGetDevice(&dev));
+    std::lock_guard<std::mutex> lk(mu);
+    if (done.count(dev)) return QL_OK;
+    cudaError_t e = allow_attn_smem<128, 1>();
+    if (e == cudaSuccess) e = allow_attn_smem<128, 2>();
+    if (e == cudaSuccess) e = allow_attn_smem<128, 4>();
+    if (e == cudaSuccess) e = allow_attn_smem<128, 8>();
+    if (e == cudaSuccess) e = allow_attn_smem<64, 1>();
+    if (e == cudaSuccess) e = allow_attn_smem<64, 2>();
+    if (e == cudaSuccess) e = allow_attn_smem<64, 4>();
+    if (e == cudaSuccess) e = allow_attn_smem<64, 8>();
+    if (e != cudaSuccess) return cuda_error(e, "attention: cudaFuncSetAttribute");
+    done.insert(dev);
+    return QL_OK;
+}
 
 size_t attn_workspace_bytes(int64_t batch, int n_heads, int n_kv_heads, int head_dim,
                             int block_size, int64_t max_blocks_per_seq) {
@@ -386,6 +449,7 @@ int attn_launch(const AttnArgs& a, cudaStream_t s, bool pdl) {
                    (reinterpret_cast<uintptr_t>(a.out) & 3) == 0 && (reinterpret_cast<uintptr_t>(a.q) & 1) == 0,
                "attention: K/V pools must be 16-byte aligned, the output 4-byte aligned");
     if (!device_error_record()) return set_error(QL_ECUDA, "attention: no device error record");
+    if (int rc = attn_prepare()) return rc;
     AParams p = {};
     p.q = a.q;
     p.k_pool = a.k_pool;
@@ -492,7 +556,7 @@ int noalloc_scratch_address(void** out) {
 template <int HD, int G>
 cudaError_t launch_hg_err(const AParams& p, int batch, cudaStream_t s, DevError* err) {
     dim3 grid(p.nsplit, p.n_kv, batch);
-    return launch(attn_split_kernel<HD, G>, grid, dim3(kAttnThreads), 0, s, true, p, err);
+    return launch(attn_split_kernel<HD, G>, grid, dim3(kAttnThreads), attn_smem<HD, G>(), s, true, p, err);
 }
 
 template <int HD>
@@ -537,6 +601,7 @@ extern "C" int ql_paged_attn_decode_noalloc(const void* d_q, const void* d_k_poo
                                         " bytes built into the library; use ql_paged_attn_decode with a workspace");
     void* scratch = nullptr;
     if (int rc = noalloc_scratch_address(&scratch)) return rc;
+    if (int rc = attn_prepare()) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // the split tickets must start at zero; the array keeps whatever the last call left
     QL_TRY_CUDA(cudaMemsetAsync(static_cast<char*>(scratch) + lo.tickets_off, 0,

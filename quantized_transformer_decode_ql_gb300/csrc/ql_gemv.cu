@@ -127,13 +127,19 @@ __device__ void stage_x(const KParams& p, uint4* xs, float* bias, float* red) {
     }
     // one item = one 16-byte chunk (column b, block j, lane slot t); the 4 chunks of a block are
     // handled by 4 consecutive threads, which reduce the block's offset term with shuffles
-    const int nitems = 8 * p.nblk * 4;
-    for (int base_item = tid - (tid & 3); base_item < nitems; base_item += kThreads) {
-        const int item = base_item + (tid & 3);
+    // columns past the batch contribute nothing: their offset terms are zero
+    for (int i = tid; i < (8 - p.batch) * p.nblk; i += kThreads) {
+        const int b = p.batch + i / p.nblk, j = i % p.nblk;
+        bias[j * 8 + b] = 0.f;
+    }
+    // the loop bound is warp-uniform (whole warps iterate together) because of the shuffles
+    const int nitems = p.batch * p.nblk * 4;
+    for (int wbase = tid & ~31; wbase < nitems; wbase += kThreads) {
+        const int item = wbase + (tid & 31);
         const int t = item & 3, bj = item >> 2;
         const int b = bj / p.nblk, j = bj - b * p.nblk;
         float lo[4] = {0.f, 0.f, 0.f, 0.f}, hi[4] = {0.f, 0.f, 0.f, 0.f};
-        if (b < p.batch) {
+        if (item < nitems) {
             const size_t off = (size_t)b * cols + 32 * j + 4 * t;
             if (p.prologue == kProRmsF32) {
                 float rr = rs[0];
@@ -169,7 +175,7 @@ __device__ void stage_x(const KParams& p, uint4* xs, float* bias, float* red) {
         part += __shfl_xor_sync(0xffffffffu, part, 1);
         part += __shfl_xor_sync(0xffffffffu, part, 2);
         if (item < nitems) {
-            if (b < p.batch) xs[b * p.cstride + 4 * j + t] = make_uint4(u32(p0), u32(p1), u32(p2), u32(p3));
+            xs[b * p.cstride + 4 * j + t] = make_uint4(u32(p0), u32(p1), u32(p2), u32(p3));
             if (t == 0) bias[j * 8 + b] = -part;
         }
     }

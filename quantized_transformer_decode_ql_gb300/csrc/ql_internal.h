@@ -136,6 +136,7 @@ struct AttnArgs {
 size_t attn_workspace_bytes(int64_t batch, int n_heads, int n_kv_heads, int head_dim,
                             int block_size, int64_t max_blocks_per_seq);
 int attn_launch(const AttnArgs& a, cudaStream_t s, bool pdl);
+int attn_prepare();   // per-device kernel attributes; call outside stream capture
 
 // ---------------------------------------------------------------- norm + rope (internal)
 struct RopeArgs {

@@ -286,6 +286,7 @@ extern "C" int ql_model_create(const ql_model_desc* desc, ql_model** out) {
     }
     if (!device_error_record()) return set_error(QL_ECUDA, "ql_model_create: cannot allocate the device error record");
     if (int rc0 = gemv_prepare()) return rc0;
+    if (int rc0 = attn_prepare()) return rc0;
 
     ql_model* m = new (std::nothrow) ql_model();
     if (!m) return set_error(QL_ENOMEM, "ql_model_create: out of host memory");
