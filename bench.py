@@ -477,7 +477,8 @@ def micro_attn(batches, iters):
         o = torch.empty((B, nh * hd), dtype=torch.float16, device="cuda")
         cl = torch.from_numpy(lens).cuda()
         ws = torch.zeros(ql.ql_paged_attn_workspace_bytes(B, nh, nkv, hd, 16, maxb), dtype=torch.uint8, device="cuda")
-        flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        flush = torch.ones(64 << 20, dtype=torch.float32, device="cuda")
+        flush_sum = torch.zeros((), dtype=torch.float32, device="cuda")
         torch.cuda.synchronize()
 
         def run():
@@ -489,12 +490,12 @@ def micro_attn(batches, iters):
 
         def flush_then_run():
             for _ in range(iters):
-                flush.fill_(1)          # evict the KV from L2 between launches
+                flush_sum.copy_(flush.sum())   # read 256 MB: evicts the KV from L2, leaves no dirty lines
                 run()
 
         def flush_only():
             for _ in range(iters):
-                flush.fill_(1)
+                flush_sum.copy_(flush.sum())
         us = (graph_ms(flush_then_run, s, 3) - graph_ms(flush_only, s, 3)) * 1e3 / iters
         nbytes = sum(2 * int(L) * nkv * hd * 2 + 4 * ((int(L) + 15) // 16) for L in lens) + B * nh * hd * 4
         gbs = nbytes / (us * 1e-6) / 1e9

@@ -395,16 +395,17 @@ __global__ void __launch_bounds__(kThreads, 3) gemv_q4_0_mma_kernel(KParams p, D
 
 
 // ---------------------------------------------------------------------------------------------
-// The main GEMV kernel (K % 128 == 0). Code bytes are read with 16-byte coalesced loads - lane l
-// loads block (l >> 3) of tile row (l & 7), and of tile row (l & 7) + 8, so one warp load covers
-// 8 rows x 4 blocks - and kRing iterations (4 blocks each) of loads stay in flight per lane; the
-// first ones are issued before the kernel waits on its predecessor. Each iteration passes the
-// 1 KB of codes through a per-warp shared-memory tile: one 16-byte store per lane and two
-// ldmatrix.x4 hand every lane exactly the 32-bit code words its MMA fragments need (word t of
-// block j for rows g and g + 8), since an 8x8 b16 ldmatrix tile is 8 rows of 16 bytes - one
-// q4_0 block per row. The f16 scales of a fragment row's 4 blocks come in one 8-byte load.
+// The main GEMV kernel (K % 128 == 0). Each warp streams its tile through a ring of kStages
+// shared-memory stages filled by 16-byte asynchronous copies (cp.async, L2 only): a stage holds 4
+// blocks x 16 rows of codes (1 KB; lane l copies block l >> 3 of tile rows (l & 7) and (l & 7) + 8)
+// and the 16 rows' 4 f16 scales (128 B). No registers are held by loads in flight, so a warp keeps
+// kStages KB outstanding; the first stages are issued before the kernel waits on its predecessor.
+// An 8x8 b16 ldmatrix tile is 8 rows of 16 bytes - one q4_0 block per row - so two ldmatrix.x4 per
+// stage hand every lane exactly the 32-bit code words its MMA fragments need (word t of block j
+// for rows g and g + 8).
 constexpr int kGroupBlocks = 4;
-constexpr int kRing = 3;
+constexpr int kStages = 6;
+constexpr int kStageBytes = kGroupBlocks * 16 * 16 + 16 * 8;   // codes + scales of one stage
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -412,11 +413,11 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r
                  : "r"(addr));
 }
 
-__global__ void __launch_bounds__(kThreads, 2) gemv_q4_0_lsm_kernel(KParams p, DevError* err) {
+__global__ void __launch_bounds__(kThreads, 3) gemv_q4_0_lsm_kernel(KParams p, DevError* err) {
     extern __shared__ __align__(16) unsigned char smem[];
-    // layout: per-warp code tiles (1 KB each) | xs | bias | red
-    uint4* tiles = reinterpret_cast<uint4*>(smem);
-    uint4* xs = tiles + kWarps * 64;
+    // layout: per-warp rings (kStages x kStageBytes) | xs | bias | red
+    unsigned char* rings = smem;
+    uint4* xs = reinterpret_cast<uint4*>(rings + (size_t)kWarps * kStages * kStageBytes);
     float* bias = reinterpret_cast<float*>(xs + (size_t)p.batch * p.cstride);
     float* red = bias + (size_t)p.nblk * 8;
     __shared__ unsigned long long kred[kWarps][8];
@@ -431,127 +432,97 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q4_0_lsm_kernel(KParams p, D
     const int seg = warp % p.S;
     const bool live = tile < p.ntile;
 
-    // rows loaded by this lane (tile rows lr and lr + 8) and the fragment rows it computes (g, g + 8)
+    // global row of tile row r (invalid rows read row 0; their results are discarded)
+    auto tile_row = [&](int r, bool& ok) -> int {
+        if (silu_mul) {
+            const int i = tile * 8 + (r & 7);
+            ok = live && i < half_rows;
+            return ok ? (r < 8 ? i : half_rows + i) : 0;
+        }
+        const int row = tile * 16 + r;
+        ok = live && row < p.rows;
+        return ok ? row : 0;
+    };
     const int lr = lane & 7, lb = lane >> 3;
-    int rowA, rowB, ra, rb;
-    bool oka, okb, okA, okB;
-    if (silu_mul) {
-        const int i0 = tile * 8;
-        okA = okB = live && i0 + lr < half_rows;
-        rowA = okA ? i0 + lr : 0;
-        rowB = okB ? half_rows + i0 + lr : 0;
-        oka = okb = live && i0 + g < half_rows;
-        ra = oka ? i0 + g : 0;
-        rb = okb ? half_rows + i0 + g : 0;
-    } else {
-        rowA = tile * 16 + lr;
-        rowB = rowA + 8;
-        okA = live && rowA < p.rows;
-        okB = live && rowB < p.rows;
-        rowA = okA ? rowA : 0;
-        rowB = okB ? rowB : 0;
-        ra = tile * 16 + g;
-        rb = ra + 8;
-        oka = live && ra < p.rows;
-        okb = live && rb < p.rows;
-        ra = oka ? ra : 0;
-        rb = okb ? rb : 0;
-    }
+    bool okA, okB, okS, oka, okb;
+    const int rowA = tile_row(lr, okA), rowB = tile_row(lr + 8, okB);
+    const int rowS = tile_row(lane & 15, okS);       // scale row copied by lanes 0..15
+    (void)tile_row(g, oka);
+    (void)tile_row(g + 8, okb);
+    (void)okA; (void)okB; (void)okS;
     const int j0 = seg * p.seg_blocks;
     const int nit = live ? p.seg_blocks / kGroupBlocks : 0;
-    const uint4* qA = reinterpret_cast<const uint4*>(p.quants) + (size_t)rowA * p.nblk + j0 + lb;
-    const uint4* qB = reinterpret_cast<const uint4*>(p.quants) + (size_t)rowB * p.nblk + j0 + lb;
-    const uint2* sA = reinterpret_cast<const uint2*>(p.scales + (size_t)ra * p.nblk + j0);
-    const uint2* sB = reinterpret_cast<const uint2*>(p.scales + (size_t)rb * p.nblk + j0);
+    const uint8_t* srcA = p.quants + ((size_t)rowA * p.nblk + j0 + lb) * 16;
+    const uint8_t* srcB = p.quants + ((size_t)rowB * p.nblk + j0 + lb) * 16;
+    const __half* srcS = p.scales + (size_t)rowS * p.nblk + j0;
+    const uint32_t ring_s = static_cast<uint32_t>(__cvta_generic_to_shared(rings)) +
+                            (uint32_t)(warp * kStages * kStageBytes);
+    const uint32_t dA = (uint32_t)((lb * 16 + lr) * 16), dB = dA + 8 * 16;
+    const uint32_t dS = (uint32_t)(kGroupBlocks * 16 * 16 + (lane & 15) * 8);
 
-    uint4 rA[kRing], rB[kRing];
-    uint2 rsa[kRing], rsb[kRing];
-    // the weights do not depend on the previous kernel: start loading them before the PDL wait
-#pragma unroll
-    for (int u = 0; u < kRing; ++u) {
-        if (u < nit) {
-            rA[u] = __ldg(qA + kGroupBlocks * u);
-            rB[u] = __ldg(qB + kGroupBlocks * u);
-            rsa[u] = __ldg(sA + u);
-            rsb[u] = __ldg(sB + u);
+    auto issue = [&](int it) {
+        if (it < nit) {
+            const uint32_t st = ring_s + (uint32_t)((it % kStages) * kStageBytes);
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(st + dA), "l"(srcA + it * kGroupBlocks * 16) : "memory");
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(st + dB), "l"(srcB + it * kGroupBlocks * 16) : "memory");
+            if (lane < 16)
+                asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(st + dS), "l"(srcS + it * kGroupBlocks) : "memory");
         }
-    }
-    if (threadIdx.x == 0 && live) {
-        // warm L2 with more of this CTA's rows
-        const size_t row_bytes = (size_t)p.nblk * 16;
-        const int rows_per_tile = silu_mul ? 8 : 16;
-        const int limit = silu_mul ? half_rows : p.rows;
-        const int r0 = blockIdx.x * tiles_per_cta * rows_per_tile;
-        size_t bytes = row_bytes * (size_t)min(tiles_per_cta * rows_per_tile, limit - r0);
-        bytes = bytes > 49152 ? 49152 : bytes;
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.quants + (size_t)r0 * row_bytes),
-                     "r"((uint32_t)bytes) : "memory");
-        if (silu_mul)
-            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
-                         ::"l"(p.quants + (size_t)(half_rows + r0) * row_bytes), "r"((uint32_t)bytes)
-                         : "memory");
-    }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    // the weights do not depend on the previous kernel: start streaming before the PDL wait
+#pragma unroll 1
+    for (int it = 0; it < kStages; ++it) issue(it);
+
     pdl_wait();
     stage_x(p, xs, bias, red);
     __syncthreads();
     pdl_trigger();
 
-    uint4* tw = tiles + warp * 64;                 // [4 blocks][16 rows] x 16 B
-    const uint32_t tw_s = static_cast<uint32_t>(__cvta_generic_to_shared(tw));
     // ldmatrix row address of this lane: matrix m = lane >> 3 -> (block m >> 1, rows (m & 1) * 8 + r)
     const int lm = lane >> 3, lrow = lane & 7;
-    const uint32_t a_lo = tw_s + (uint32_t)(((lm >> 1) * 16 + (lm & 1) * 8 + lrow) * 16);
+    const uint32_t a_lo = (uint32_t)(((lm >> 1) * 16 + (lm & 1) * 8 + lrow) * 16);
     const uint32_t a_hi = a_lo + 2 * 16 * 16;      // blocks 2 and 3
     const bool has_col = g < p.batch;
     const uint4* xcol = xs + (size_t)(has_col ? g : 0) * p.cstride;
 
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int it0 = 0; it0 < nit; it0 += kRing) {
+#pragma unroll 1
+    for (int it = 0; it < nit; ++it) {
+        asm volatile("cp.async.wait_group %0;" ::"n"(kStages - 1) : "memory");
+        __syncwarp();
+        const uint32_t st = ring_s + (uint32_t)((it % kStages) * kStageBytes);
+        uint32_t w[8];   // wa0, wb0, wa1, wb1, wa2, wb2, wa3, wb3
+        ldsm_x4(st + a_lo, w[0], w[1], w[2], w[3]);
+        ldsm_x4(st + a_hi, w[4], w[5], w[6], w[7]);
+        const unsigned char* stg = rings + (size_t)(warp * kStages + it % kStages) * kStageBytes;
+        const uint2 sca = *reinterpret_cast<const uint2*>(stg + kGroupBlocks * 16 * 16 + g * 8);
+        const uint2 scb = *reinterpret_cast<const uint2*>(stg + kGroupBlocks * 16 * 16 + (g + 8) * 8);
+        __syncwarp();
+        issue(it + kStages);                         // refill this slot (the reads above are done)
+        const float2 da01 = __half22float2(h2(sca.x)), da23 = __half22float2(h2(sca.y));
+        const float2 db01 = __half22float2(h2(scb.x)), db23 = __half22float2(h2(scb.y));
+        const float da[4] = {da01.x, da01.y, da23.x, da23.y};
+        const float db[4] = {db01.x, db01.y, db23.x, db23.y};
 #pragma unroll
-        for (int u = 0; u < kRing; ++u) {
-            const int it = it0 + u;
-            if (it < nit) {
-                tw[lb * 16 + lr] = rA[u];
-                tw[lb * 16 + 8 + lr] = rB[u];
-                const uint2 sca = rsa[u], scb = rsb[u];
-                const int nx = it + kRing;
-                if (nx < nit) {
-                    rA[u] = __ldg(qA + kGroupBlocks * nx);
-                    rB[u] = __ldg(qB + kGroupBlocks * nx);
-                    rsa[u] = __ldg(sA + nx);
-                    rsb[u] = __ldg(sB + nx);
-                }
-                __syncwarp();
-                uint32_t w[8];   // wa0, wb0, wa1, wb1, wa2, wb2, wa3, wb3
-                ldsm_x4(a_lo, w[0], w[1], w[2], w[3]);
-                ldsm_x4(a_hi, w[4], w[5], w[6], w[7]);
-                __syncwarp();
-                const float2 da01 = __half22float2(h2(sca.x)), da23 = __half22float2(h2(sca.y));
-                const float2 db01 = __half22float2(h2(scb.x)), db23 = __half22float2(h2(scb.y));
-                const float da[4] = {da01.x, da01.y, da23.x, da23.y};
-                const float db[4] = {db01.x, db01.y, db23.x, db23.y};
-#pragma unroll
-                for (int q = 0; q < kGroupBlocks; ++q) {
-                    const int j = j0 + it * kGroupBlocks + q;
-                    const uint32_t wa = w[2 * q], wb = w[2 * q + 1];
-                    const uint4 X = has_col ? xcol[4 * j + t] : make_uint4(0u, 0u, 0u, 0u);
-                    const float2 bz = *reinterpret_cast<const float2*>(bias + j * 8 + 2 * t);
-                    float c[4] = {bz.x, bz.y, bz.x, bz.y};
-                    const uint32_t sa8 = wa >> 8, sb8 = wb >> 8;
-                    mma16816(c, (wa & 0x000F000Fu) | 0x64006400u, (wb & 0x000F000Fu) | 0x64006400u,
-                             (sa8 & 0x000F000Fu) | 0x64006400u, (sb8 & 0x000F000Fu) | 0x64006400u, X.x, X.y);
-                    mma16816(c, (wa & 0x00F000F0u) | 0x64006400u, (wb & 0x00F000F0u) | 0x64006400u,
-                             (sa8 & 0x00F000F0u) | 0x64006400u, (sb8 & 0x00F000F0u) | 0x64006400u, X.z, X.w);
-                    acc[0] = fmaf(da[q], c[0], acc[0]);
-                    acc[1] = fmaf(da[q], c[1], acc[1]);
-                    acc[2] = fmaf(db[q], c[2], acc[2]);
-                    acc[3] = fmaf(db[q], c[3], acc[3]);
-                }
-            }
+        for (int q = 0; q < kGroupBlocks; ++q) {
+            const int j = j0 + it * kGroupBlocks + q;
+            const uint32_t wa = w[2 * q], wb = w[2 * q + 1];
+            const uint4 X = has_col ? xcol[4 * j + t] : make_uint4(0u, 0u, 0u, 0u);
+            const float2 bz = *reinterpret_cast<const float2*>(bias + j * 8 + 2 * t);
+            float c[4] = {bz.x, bz.y, bz.x, bz.y};
+            const uint32_t sa8 = wa >> 8, sb8 = wb >> 8;
+            mma16816(c, (wa & 0x000F000Fu) | 0x64006400u, (wb & 0x000F000Fu) | 0x64006400u,
+                     (sa8 & 0x000F000Fu) | 0x64006400u, (sb8 & 0x000F000Fu) | 0x64006400u, X.x, X.y);
+            mma16816(c, (wa & 0x00F000F0u) | 0x64006400u, (wb & 0x00F000F0u) | 0x64006400u,
+                     (sa8 & 0x00F000F0u) | 0x64006400u, (sb8 & 0x00F000F0u) | 0x64006400u, X.z, X.w);
+            acc[0] = fmaf(da[q], c[0], acc[0]);
+            acc[1] = fmaf(da[q], c[1], acc[1]);
+            acc[2] = fmaf(db[q], c[2], acc[2]);
+            acc[3] = fmaf(db[q], c[3], acc[3]);
         }
     }
-    (void)okA;
-    (void)okB;
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
     finish_tile(p, red, kred, tile, seg, acc, oka, okb);
 }
 
@@ -569,7 +540,7 @@ int gemv_prepare() {
                                          (int)kMaxStageBytes);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(gemv_q4_0_lsm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kMaxStageBytes + kWarps * 1024);
+                                 (int)kMaxStageBytes + kWarps * kStages * kStageBytes);
     if (e != cudaSuccess) return cuda_error(e, "gemv: cudaFuncSetAttribute");
     done.insert(dev);
     return QL_OK;
@@ -641,7 +612,7 @@ int gemv_launch(const GemvArgs& a, cudaStream_t s, bool pdl) {
                 S *= 2;
             p.S = S;
             p.seg_blocks = nblk / S;
-            const size_t smem = (size_t)kWarps * 1024 + stage_smem;
+            const size_t smem = (size_t)kWarps * kStages * kStageBytes + stage_smem;
             const int grid = (p.ntile + kWarps / S - 1) / (kWarps / S);
             e = launch(gemv_q4_0_lsm_kernel, dim3(grid), dim3(kThreads), smem, s, pdl, p, device_error_record());
         } else {
