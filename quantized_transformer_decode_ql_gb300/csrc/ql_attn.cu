@@ -53,6 +53,7 @@ struct AParams {
     float* pacc;        // [batch][n_heads][nsplit][HD]
     int nsplit, spb;
     int prefetch;       // warm L2 with this CTA's K/V tiles before waiting on the predecessor
+    NextWeights next;   // weights of the following kernel, prefetched into L2
 };
 
 __device__ __forceinline__ float2 h2f(uint32_t u) {
@@ -83,6 +84,8 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AParams p, Dev
 
     const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    l2_prefetch_share(p.next.ptr[0], p.next.bytes[0]);
+    l2_prefetch_share(p.next.ptr[1], p.next.bytes[1]);
     if (p.prefetch && (p.active == nullptr || p.active[b] != 0)) {
         // In the decode step the context length comes from the position, which is final before
         // this kernel starts; only the newest slot is still being written (prefetch is a hint).
@@ -472,6 +475,7 @@ int attn_launch(const AttnArgs& a, cudaStream_t s, bool pdl) {
     p.nsplit = lo.nsplit;
     p.spb = lo.spb;
     p.prefetch = a.context_lens == nullptr ? 1 : 0;
+    p.next = a.next;
     cudaError_t e = a.head_dim == 128 ? launch_h<128>(p, G, a.batch, s, pdl)
                                       : launch_h<64>(p, G, a.batch, s, pdl);
     if (e != cudaSuccess) return cuda_error(e, "attention launch");

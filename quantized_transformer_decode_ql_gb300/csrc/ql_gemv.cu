@@ -90,6 +90,7 @@ struct KParams {
     int S;             // K segments per tile (1, 2, 4 or 8 warps)
     int seg_blocks;    // blocks per K segment
     int cstride;       // uint4 units between staged columns
+    NextWeights next;  // weights of the following kernel, prefetched into L2
 };
 
 // Stage the activations: per column, per block j, 4 chunks of 16 bytes (chunk t serves lane
@@ -319,6 +320,8 @@ __global__ void __launch_bounds__(kThreads, 3) gemv_q4_0_mma_kernel(KParams p, D
                              : "memory");
         }
     }
+    l2_prefetch_share(p.next.ptr[0], p.next.bytes[0]);
+    l2_prefetch_share(p.next.ptr[1], p.next.bytes[1]);
     pdl_wait();
     stage_x(p, xs, bias, red);
     __syncthreads();
@@ -473,6 +476,8 @@ __global__ void __launch_bounds__(kThreads, 3) gemv_q4_0_lsm_kernel(KParams p, D
     // the weights do not depend on the previous kernel: start streaming before the PDL wait
 #pragma unroll 1
     for (int it = 0; it < kStages; ++it) issue(it);
+    l2_prefetch_share(p.next.ptr[0], p.next.bytes[0]);
+    l2_prefetch_share(p.next.ptr[1], p.next.bytes[1]);
 
     pdl_wait();
     stage_x(p, xs, bias, red);
@@ -597,6 +602,7 @@ int gemv_launch(const GemvArgs& a, cudaStream_t s, bool pdl) {
         p.residual = a.residual ? a.residual + (size_t)b0 * out_ld : nullptr;
         p.keys = a.argmax_keys ? a.argmax_keys + b0 : nullptr;
         p.active = a.active ? a.active + b0 : nullptr;
+        if (b0 == 0) p.next = a.next;
         p.ntile = silu ? (int)((a.rows / 2 + 7) / 8) : (int)((a.rows + 15) / 16);
         p.cstride = cstride;
         const size_t stage_smem = fixed + (size_t)nb * cstride * 16;

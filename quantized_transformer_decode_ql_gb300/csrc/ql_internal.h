@@ -73,7 +73,33 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 __device__ __forceinline__ void pdl_trigger() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
+
+// Ask L2 to fetch this CTA's share of [base, base + bytes): the grid splits the range evenly,
+// each thread of a CTA issues 16 KB pieces. A hint only (no data is returned, nothing waits):
+// used to stream the NEXT kernel's weights while the current kernel runs.
+__device__ __forceinline__ void l2_prefetch_share(const void* base, size_t bytes) {
+    if (base == nullptr || bytes < 16) return;
+    const size_t nblocks = (size_t)gridDim.x * gridDim.y * gridDim.z;
+    const size_t bid = blockIdx.x + (size_t)gridDim.x * (blockIdx.y + (size_t)gridDim.y * blockIdx.z);
+    const size_t share = ((bytes + nblocks - 1) / nblocks + 15) & ~(size_t)15;
+    const size_t start = bid * share;
+    if (start >= bytes) return;
+    const size_t end = start + share < bytes ? start + share : bytes;
+    const size_t nthreads = (size_t)blockDim.x * blockDim.y * blockDim.z;
+    for (size_t off = start + (size_t)threadIdx.x * 16384; off < end; off += nthreads * 16384) {
+        const size_t n = ((end - off) < 16384 ? (end - off) : 16384) & ~(size_t)15;
+        if (n)
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(static_cast<const char*>(base) + off),
+                         "r"((uint32_t)n) : "memory");
+    }
+}
 #endif
+
+// An L2 prefetch request for the next kernel's weights (two ranges: codes and scales).
+struct NextWeights {
+    const void* ptr[2];
+    size_t bytes[2];
+};
 
 template <typename... KArgs, typename... Args>
 cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
@@ -113,6 +139,7 @@ struct GemvArgs {
     const float* residual;
     unsigned long long* argmax_keys;   // [batch], kEpiArgmax
     const int32_t* active;      // optional, kEpiArgmax: inactive columns skip the argmax
+    NextWeights next;           // optional L2 prefetch of the following kernel's weights
 };
 int gemv_launch(const GemvArgs& a, cudaStream_t s, bool pdl);
 int gemv_prepare();   // per-device kernel attributes; call outside stream capture
@@ -132,6 +159,7 @@ struct AttnArgs {
     __half* out;
     void* workspace;
     size_t workspace_bytes;
+    NextWeights next;
 };
 size_t attn_workspace_bytes(int64_t batch, int n_heads, int n_kv_heads, int head_dim,
                             int block_size, int64_t max_blocks_per_seq);
@@ -157,6 +185,7 @@ struct RopeArgs {
     int block_size;
     int64_t num_blocks;
     int64_t max_position;
+    NextWeights next;
 };
 int rope_launch(const RopeArgs& a, cudaStream_t s, bool pdl);
 

@@ -20,6 +20,7 @@
 //   finalize                   next token, position += 1, keys re-armed
 #include <cuda_fp16.h>
 
+#include <cstdlib>
 #include <map>
 #include <vector>
 
@@ -43,6 +44,7 @@ struct ql_model {
     size_t attn_ws_bytes = 0;
     std::vector<void*> owned;
     std::map<int64_t, cudaGraphExec_t> graphs;
+    bool next_prefetch = true;   // L2 prefetch of the following GEMV's weights (A/B: QL_NEXT_PREFETCH=0)
 };
 
 namespace ql {
@@ -50,8 +52,10 @@ namespace {
 
 __global__ void embed_kernel(const float* __restrict__ E, const int32_t* __restrict__ tokens,
                              const int32_t* __restrict__ active, float* __restrict__ x, int hidden,
-                             int vocab, DevError* err) {
+                             int vocab, DevError* err, NextWeights next) {
     const int b = blockIdx.x;
+    l2_prefetch_share(next.ptr[0], next.bytes[0]);
+    l2_prefetch_share(next.ptr[1], next.bytes[1]);
     pdl_wait();
     pdl_trigger();
     int tok = tokens[b];
@@ -103,8 +107,24 @@ int run_step(ql_model* m, const ql_step_args* a, cudaStream_t s) {
     const size_t layer_pool = (size_t)d.num_blocks * nkv * d.block_size * hd;
     int rc;
 
+    // Each kernel asks L2 to fetch the weights of a GEMV that follows it, so that HBM keeps
+    // streaming weights through kernel boundaries, launches and the small kernels:
+    //   embed -> qkv(0); qkv(l) -> o(l); norm_rope(l) -> gate|up(l); gate|up(l) -> down(l);
+    //   down(l) -> qkv(l+1), or the first 64 MB of lm_head after the last layer.
+    const bool pf = m->next_prefetch;
+    auto nw = [pf](const ql_q4_0_matrix& w, size_t cap) {
+        NextWeights n = {};
+        if (!pf) return n;
+        const size_t qb = (size_t)w.rows * w.cols / 2, sb = (size_t)w.rows * w.cols / 16;
+        n.ptr[0] = w.quants;
+        n.bytes[0] = qb < cap ? qb : cap;
+        n.ptr[1] = w.scales;
+        n.bytes[1] = sb < cap / 8 ? sb : cap / 8;
+        return n;
+    };
+    const size_t kAll = ~(size_t)0, kLmHead = (size_t)64 << 20;
     cudaError_t e = launch(embed_kernel, dim3(B), dim3(256), 0, s, pdl, d.embed, a->tokens, a->active,
-                           m->x, (int)d.hidden, (int)d.vocab, device_error_record());
+                           m->x, (int)d.hidden, (int)d.vocab, device_error_record(), nw(m->layers[0].qkv, kAll));
     if (e != cudaSuccess) return cuda_error(e, "embed launch");
 
     for (int li = 0; li < d.n_layers; ++li) {
@@ -123,6 +143,7 @@ int run_step(ql_model* m, const ql_step_args* a, cudaStream_t s) {
         g.epilogue = QL_EPI_NONE;
         g.y_dtype = QL_DTYPE_F32;
         g.y = m->qkv;
+        g.next = nw(L.o, kAll);
         if ((rc = gemv_launch(g, s, pdl)) != QL_OK) return rc;
 
         RopeArgs r = {};
@@ -146,6 +167,7 @@ int run_step(ql_model* m, const ql_step_args* a, cudaStream_t s) {
         r.block_size = d.block_size;
         r.num_blocks = d.num_blocks;
         r.max_position = d.max_blocks_per_seq * d.block_size;
+        r.next = nw(L.gate_up, kAll);
         if ((rc = rope_launch(r, s, pdl)) != QL_OK) return rc;
 
         AttnArgs at = {};
@@ -196,6 +218,7 @@ int run_step(ql_model* m, const ql_step_args* a, cudaStream_t s) {
         gu.epilogue = QL_EPI_SILU_MUL;
         gu.y_dtype = QL_DTYPE_F16;
         gu.y = m->act;
+        gu.next = nw(L.down, kAll);
         if ((rc = gemv_launch(gu, s, pdl)) != QL_OK) return rc;
 
         GemvArgs gd = {};
@@ -210,6 +233,7 @@ int run_step(ql_model* m, const ql_step_args* a, cudaStream_t s) {
         gd.y_dtype = QL_DTYPE_F32;
         gd.y = m->x;
         gd.residual = m->x;
+        gd.next = li + 1 < d.n_layers ? nw(m->layers[li + 1].qkv, kAll) : nw(d.lm_head, kLmHead);
         if ((rc = gemv_launch(gd, s, pdl)) != QL_OK) return rc;
     }
 
@@ -294,6 +318,7 @@ extern "C" int ql_model_create(const ql_model_desc* desc, ql_model** out) {
     m->layers.assign(d.layers, d.layers + d.n_layers);
     m->d.layers = m->layers.data();
     cudaGetDevice(&m->device);
+    if (const char* ev = std::getenv("QL_NEXT_PREFETCH")) m->next_prefetch = std::atoi(ev) != 0;
     const int64_t B = d.max_batch;
     const int64_t max_pos = d.max_blocks_per_seq * d.block_size;
     int rc = QL_OK;

@@ -32,6 +32,7 @@ struct RParams {
     int maxb, bs;
     long long num_blocks;
     long long max_position;
+    NextWeights next;
 };
 
 template <int HD>
@@ -40,6 +41,8 @@ __global__ void __launch_bounds__(HD / 2) norm_rope_kernel(RParams p, DevError* 
     constexpr int NW = (H2 + 31) / 32;
     __shared__ float red[NW];
     const int hh = blockIdx.x, b = blockIdx.y, i = threadIdx.x;
+    l2_prefetch_share(p.next.ptr[0], p.next.bytes[0]);
+    l2_prefetch_share(p.next.ptr[1], p.next.bytes[1]);
     pdl_wait();
     pdl_trigger();
     if (p.active && p.active[b] == 0) return;
@@ -125,6 +128,7 @@ int rope_launch(const RopeArgs& a, cudaStream_t s, bool pdl) {
     p.bs = a.block_size;
     p.num_blocks = a.num_blocks;
     p.max_position = a.max_position;
+    p.next = a.next;
     dim3 grid(a.n_heads + a.n_kv_heads, a.batch);
     cudaError_t e = a.head_dim == 128
                         ? launch(norm_rope_kernel<128>, grid, dim3(64), 0, s, pdl, p, device_error_record())

@@ -158,3 +158,60 @@ def test_replay_before_capture_is_an_error(tiny):
     with pytest.raises(ql.QLError) as e:
         gm.ql_decode_graph_replay(7, 1)
     assert e.value.status == ql.QL_ESTATE
+
+
+def test_batched_slots_with_replacement(tiny):
+    """Three slots at different context lengths (pre-filled f16 contexts in fragmented blocks
+    from the library's block allocator) decode together; after four steps slot 1 finishes, its
+    blocks go back to the pool and it restarts on a fresh 7-position context in newly allocated
+    blocks. Every step's logits of every slot match the oracle decoding each slot on its own."""
+    import quantized_transformer_decode_ql_gb300 as ql
+    gm, om = tiny
+    B, maxb = 3, 4
+    pool = ql.BlockPool(64)
+    order = [pool.alloc() for _ in range(64)]
+    pool.free(list(np.random.default_rng(3).permutation(order)))   # fragmented reuse order
+    lens = [5, 20, 33]
+    cache = decode.KVCache(CFG, B, maxb * 16)
+    bt = np.full((B, maxb), 0, np.int32)
+    blocks = [None] * B
+
+    def place(slot, n_pos, seed):
+        ids = [pool.alloc() for _ in range(maxb)]
+        blocks[slot] = ids
+        bt[slot] = ids
+        k, v = ql_inputs.kv_context(CFG.n_layers, CFG.n_kv_heads, CFG.head_dim, n_pos, seed=seed)
+        gm.write_context(ids, k, v)
+        cache.k[slot] = 0.0
+        cache.v[slot] = 0.0
+        cache.preload(slot, k, v)
+
+    for b in range(B):
+        place(b, lens[b], seed=40 + b)
+    tokens = dev(ql_inputs.prompt_tokens(B, CFG.vocab, seed=17).astype(np.int32))
+    positions = dev(np.array(lens, np.int32))
+    logits = torch.zeros((B, CFG.vocab), dtype=torch.float32, device="cuda")
+    d_bt = dev(bt)
+    args = gm.step_args(tokens, positions, d_bt, tokens, logits=logits)
+    toks = tokens.cpu().numpy().copy()
+    pos = np.array(lens)
+    for step in range(8):
+        if step == 4:
+            pool.free(blocks[1])
+            place(1, 7, seed=99)
+            d_bt.copy_(torch.from_numpy(bt))
+            pos[1] = 7
+            positions.copy_(torch.from_numpy(pos.astype(np.int32)))
+        want = decode.decode_step(om, cache, toks, pos)
+        tokens.copy_(torch.from_numpy(toks.astype(np.int32)))
+        gm.ql_decode_step(args)
+        torch.cuda.synchronize()
+        got = logits.cpu().numpy().astype(np.float64)
+        for b in range(B):
+            ok = decode.logits_close(got[b], want[b])
+            assert ok.all(), f"step {step} slot {b}: max err {np.abs(got[b] - want[b]).max():.3e}"
+        toks = decode.greedy(want)          # teacher forcing with the oracle's tokens
+        pos = pos + 1
+        assert positions.cpu().numpy().tolist() == pos.tolist()
+    gm.ql_check_device_error()
+    assert pool.in_use() == 2 * maxb + maxb   # slots 0 and 2 plus the replacement of slot 1
