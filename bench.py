@@ -341,6 +341,117 @@ def gpu_arm(args, rank, world, local_rank):
     return line
 
 
+def gpu_arm_e32(args, rank, world, local_rank):
+    """Batched decode: 32 sequences with initial context lengths uniform in [128, 8192], fragmented
+    block tables from the library's block allocator, K greedy steps; every sequence finishes at a
+    random step and is replaced by a fresh 128-position context in newly allocated blocks. The
+    replacement work runs between graph replays and is excluded from the decode time (reported
+    separately)."""
+    import torch
+
+    from quantized_transformer_decode_ql_gb300 import build as qbuild
+    if rank == 0 or world == 1:
+        qbuild.build()
+    barrier(world)
+    import quantized_transformer_decode_ql_gb300 as ql
+    from quantized_transformer_decode_ql_gb300.model import DeviceModel
+
+    torch.cuda.set_device(local_rank)
+    cfg = ql_inputs.QWEN3_8B
+    B, steps, warmup, fresh = 32, args.steps, args.warmup, 128
+    lens0 = ql_inputs.batched_lengths(B, 128, 8192, seed=7)
+    finish = ql_inputs.sub_rng(8, B).integers(0, steps, size=B)
+    cap = int(max(lens0.max(), fresh)) + warmup + steps + 2
+    maxb = (cap + 15) // 16
+    need = sum((int(L) + warmup + steps + 2 + 15) // 16 for L in lens0) + B * ((fresh + steps + 2 + 15) // 16) + 16
+    t_setup = time.time()
+    gm = DeviceModel.from_layer_fn(cfg, device_tensor_fn(cfg, seed=0), num_blocks=need, max_batch=B,
+                                   max_blocks_per_seq=maxb)
+    pool = ql.BlockPool(need)
+    order = [pool.alloc() for _ in range(need)]
+    pool.free([order[i] for i in ql_inputs.fragmented_block_ids(need, seed=5)])
+    g = torch.Generator(device="cuda")
+    g.manual_seed(4)
+    bt_host = np.zeros((B, maxb), np.int32)
+    owned = [None] * B
+
+    def place(b, n_pos, n_total):
+        ids = [pool.alloc() for _ in range((n_total + 15) // 16)]
+        owned[b] = ids
+        bt_host[b, :] = 0
+        bt_host[b, :len(ids)] = ids
+        nb = (n_pos + 15) // 16
+        idx = torch.tensor(ids[:nb], dtype=torch.long, device="cuda")
+        shape = (cfg.n_layers, nb, cfg.n_kv_heads, 16, cfg.head_dim)
+        gm.k_pool[:, idx] = torch.randn(shape, generator=g, device="cuda").half()
+        gm.v_pool[:, idx] = torch.randn(shape, generator=g, device="cuda").half()
+
+    for b in range(B):
+        place(b, int(lens0[b]), int(lens0[b]) + warmup + steps + 2)
+    bt = torch.from_numpy(bt_host).cuda()
+    tokens = torch.from_numpy(ql_inputs.prompt_tokens(B, cfg.vocab, seed=1)).cuda()
+    positions = torch.from_numpy(lens0.astype(np.int32)).cuda()
+    sargs = gm.step_args(tokens, positions, bt, tokens)
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    gm.ql_decode_graph_capture(sargs, s)
+    setup_s = time.time() - t_setup
+    with torch.cuda.stream(s):
+        gm.ql_decode_graph_replay(B, warmup, s)
+    s.synchronize()
+    gm.ql_check_device_error()
+
+    clock = ClockSampler(local_rank)
+    time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    kv_tok = cfg.n_layers * 2 * cfg.n_kv_heads * cfg.head_dim * 2
+    live_len = positions.cpu().numpy().astype(np.int64) + 1
+    step_bytes = []
+    repl_s = 0.0
+    for i in range(steps):
+        step_bytes.append(gm.weight_bytes() + kv_tok * int(live_len.sum()) + B * (kv_tok + cfg.hidden * 4 + cfg.vocab * 4))
+        with torch.cuda.stream(s):
+            ev[i][0].record(s)
+            gm.ql_decode_graph_replay(B, 1, s)
+            ev[i][1].record(s)
+        live_len += 1
+        done = np.flatnonzero(finish == i)
+        if len(done):
+            t0 = time.perf_counter()
+            s.synchronize()
+            pos_h = positions.cpu().numpy()
+            for b in done:
+                pool.free(owned[b])
+                place(int(b), fresh, fresh + steps + 2)
+                pos_h[b] = fresh
+                live_len[b] = fresh + 1
+            bt.copy_(torch.from_numpy(bt_host))
+            positions.copy_(torch.from_numpy(pos_h))
+            torch.cuda.synchronize()
+            repl_s += time.perf_counter() - t0
+    s.synchronize()
+    clocks = clock.stop()
+    gm.ql_check_device_error()
+    ms = sum(a.elapsed_time(b) for a, b in ev)
+    peak, peak_src = load_peaks()
+    value = B * steps / (ms / 1e3)
+    gbs = sum(step_bytes) / (ms / 1e3) / 1e9
+    return {
+        "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world, "steps": steps,
+        "warmup": warmup, "ms_per_step": round(ms / steps, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "q4_0 weights, f16 act/KV, f32 accum",
+        "data": "synthetic (seeded random-init weights, N(0,1) f16 KV contexts, random tokens)",
+        "config": {"workload": f"qwen3-8b-shaped q4_0 batched decode, 32 sequences, contexts uniform in [128, 8192], "
+                               f"{steps} greedy steps, finished sequences replaced by fresh 128-position contexts",
+                   "batch": B, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (4.26 GB of weights + KV per step)"},
+        "step_roofline": {"bytes_per_step_avg": int(np.mean(step_bytes)), "achieved_gbs": round(gbs, 1),
+                          "frac": round(gbs / peak, 4), "peak": peak, "peak_source": peak_src},
+        "replacement_s_excluded": round(repl_s, 3), "replacements": int((finish < steps).sum()),
+        "clocks": clocks, "gpu_launches": (4 + 6 * cfg.n_layers) * steps, "setup_s": round(setup_s, 1),
+    }
+
+
 # ----------------------------------------------------------------------------- CPU oracle arm
 def oracle_sample(budget_s: float = 20.0):
     """Time the f64 oracle on a bounded sample of the batch-1 8B-shaped decode: one full decode
@@ -510,7 +621,7 @@ def main():
     ap.add_argument("--steps", type=int, default=256)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ql", choices=["ql", "reference"])
-    ap.add_argument("--config", default="e1", choices=["e1"])
+    ap.add_argument("--config", default="e1", choices=["e1", "e32"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--micro", choices=["gemv", "attn"], help="time one kernel family alone")
     ap.add_argument("--shape", default=None, help="micro gemv: ROWSxCOLS (default: all shapes)")
@@ -543,6 +654,11 @@ def main():
             print(json.dumps(line), flush=True)
         return
     assert args.warmup >= 3, "at least 3 warm-up steps"
+    if args.config == "e32":
+        line = gpu_arm_e32(args, rank, world, local_rank)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        return
     line = gpu_arm(args, rank, world, local_rank)
     if rank == 0:
         if not args.no_cpu_baseline:

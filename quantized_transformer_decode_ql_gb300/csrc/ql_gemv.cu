@@ -30,6 +30,7 @@
 // activations. Fused epilogues: residual add, SiLU * up, greedy argmax over the rows (lm_head).
 #include <cuda_fp16.h>
 
+#include <cstdlib>
 #include <mutex>
 #include <set>
 
@@ -431,12 +432,21 @@ __global__ void __launch_bounds__(kThreads, 3) gemv_q4_0_lsm_kernel(KParams p, D
     const bool silu_mul = (p.epilogue == QL_EPI_SILU_MUL);
     const int half_rows = p.rows >> 1;
     const int tiles_per_cta = kWarps / p.S;
-    const int tile = blockIdx.x * tiles_per_cta + warp / p.S;
     const int seg = warp % p.S;
-    const bool live = tile < p.ntile;
+    // The CTA walks tile groups blockIdx.x, blockIdx.x + gridDim.x, ... (a grid of about one CTA
+    // per SM leaves room for the next kernel's CTAs, which PDL starts early); every warp runs
+    // the same number of (tile, segment) tasks, so the per-task barriers line up.
+    const int ngroups = (p.ntile + tiles_per_cta - 1) / tiles_per_cta;
+    const int my_groups = (int)blockIdx.x < ngroups ? (ngroups - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+    const int nit = p.seg_blocks / kGroupBlocks;      // iterations (4 blocks each) per task
+    const int total = my_groups * nit;
+    const int j0 = seg * p.seg_blocks;
+    const int lr = lane & 7, lb = lane >> 3;
 
+    auto tile_of = [&](int grp) { return ((int)blockIdx.x + grp * (int)gridDim.x) * tiles_per_cta + warp / p.S; };
     // global row of tile row r (invalid rows read row 0; their results are discarded)
-    auto tile_row = [&](int r, bool& ok) -> int {
+    auto tile_row = [&](int tile, int r, bool& ok) -> int {
+        const bool live = tile < p.ntile;
         if (silu_mul) {
             const int i = tile * 8 + (r & 7);
             ok = live && i < half_rows;
@@ -446,30 +456,37 @@ __global__ void __launch_bounds__(kThreads, 3) gemv_q4_0_lsm_kernel(KParams p, D
         ok = live && row < p.rows;
         return ok ? row : 0;
     };
-    const int lr = lane & 7, lb = lane >> 3;
-    bool okA, okB, okS, oka, okb;
-    const int rowA = tile_row(lr, okA), rowB = tile_row(lr + 8, okB);
-    const int rowS = tile_row(lane & 15, okS);       // scale row copied by lanes 0..15
-    (void)tile_row(g, oka);
-    (void)tile_row(g + 8, okb);
-    (void)okA; (void)okB; (void)okS;
-    const int j0 = seg * p.seg_blocks;
-    const int nit = live ? p.seg_blocks / kGroupBlocks : 0;
-    const uint8_t* srcA = p.quants + ((size_t)rowA * p.nblk + j0 + lb) * 16;
-    const uint8_t* srcB = p.quants + ((size_t)rowB * p.nblk + j0 + lb) * 16;
-    const __half* srcS = p.scales + (size_t)rowS * p.nblk + j0;
     const uint32_t ring_s = static_cast<uint32_t>(__cvta_generic_to_shared(rings)) +
                             (uint32_t)(warp * kStages * kStageBytes);
     const uint32_t dA = (uint32_t)((lb * 16 + lr) * 16), dB = dA + 8 * 16;
     const uint32_t dS = (uint32_t)(kGroupBlocks * 16 * 16 + (lane & 15) * 8);
 
+    // load cursor: (group, iteration) of the next stage to issue, and its source pointers
+    int l_grp = 0, l_it = 0;
+    const uint8_t* srcA = nullptr;
+    const uint8_t* srcB = nullptr;
+    const __half* srcS = nullptr;
+    auto set_task = [&](int grp) {
+        bool ok;
+        const int tile = tile_of(grp);
+        const int rowA = tile_row(tile, lr, ok), rowB = tile_row(tile, lr + 8, ok);
+        const int rowS = tile_row(tile, lane & 15, ok);
+        srcA = p.quants + ((size_t)rowA * p.nblk + j0 + lb) * 16;
+        srcB = p.quants + ((size_t)rowB * p.nblk + j0 + lb) * 16;
+        srcS = p.scales + (size_t)rowS * p.nblk + j0;
+    };
+    set_task(0);
     auto issue = [&](int it) {
-        if (it < nit) {
+        if (it < total) {
             const uint32_t st = ring_s + (uint32_t)((it % kStages) * kStageBytes);
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(st + dA), "l"(srcA + it * kGroupBlocks * 16) : "memory");
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(st + dB), "l"(srcB + it * kGroupBlocks * 16) : "memory");
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(st + dA), "l"(srcA + l_it * kGroupBlocks * 16) : "memory");
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(st + dB), "l"(srcB + l_it * kGroupBlocks * 16) : "memory");
             if (lane < 16)
-                asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(st + dS), "l"(srcS + it * kGroupBlocks) : "memory");
+                asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(st + dS), "l"(srcS + l_it * kGroupBlocks) : "memory");
+            if (++l_it == nit) {
+                l_it = 0;
+                if (++l_grp < my_groups) set_task(l_grp);
+            }
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
     };
@@ -492,8 +509,9 @@ __global__ void __launch_bounds__(kThreads, 3) gemv_q4_0_lsm_kernel(KParams p, D
     const uint4* xcol = xs + (size_t)(has_col ? g : 0) * p.cstride;
 
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    int c_grp = 0, c_it = 0;
 #pragma unroll 1
-    for (int it = 0; it < nit; ++it) {
+    for (int it = 0; it < total; ++it) {
         asm volatile("cp.async.wait_group %0;" ::"n"(kStages - 1) : "memory");
         __syncwarp();
         const uint32_t st = ring_s + (uint32_t)((it % kStages) * kStageBytes);
@@ -511,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 3) gemv_q4_0_lsm_kernel(KParams p, D
         const float db[4] = {db01.x, db01.y, db23.x, db23.y};
 #pragma unroll
         for (int q = 0; q < kGroupBlocks; ++q) {
-            const int j = j0 + it * kGroupBlocks + q;
+            const int j = j0 + c_it * kGroupBlocks + q;
             const uint32_t wa = w[2 * q], wb = w[2 * q + 1];
             const uint4 X = has_col ? xcol[4 * j + t] : make_uint4(0u, 0u, 0u, 0u);
             const float2 bz = *reinterpret_cast<const float2*>(bias + j * 8 + 2 * t);
@@ -526,12 +544,32 @@ __global__ void __launch_bounds__(kThreads, 3) gemv_q4_0_lsm_kernel(KParams p, D
             acc[2] = fmaf(db[q], c[2], acc[2]);
             acc[3] = fmaf(db[q], c[3], acc[3]);
         }
+        if (++c_it == nit) {
+            const int tile = tile_of(c_grp);
+            bool oka, okb;
+            (void)tile_row(tile, g, oka);
+            (void)tile_row(tile, g + 8, okb);
+            finish_tile(p, red, kred, tile, seg, acc, oka, okb);
+            acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+            c_it = 0;
+            ++c_grp;
+        }
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
-    finish_tile(p, red, kred, tile, seg, acc, oka, okb);
 }
 
 }  // namespace
+
+// CTAs per SM of the main GEMV grid (the CTAs loop over tile groups). One leaves room for the
+// next kernel of the step to become resident early; QL_GEMV_CTAS_PER_SM overrides it for A/B.
+int gemv_ctas_per_sm() {
+    static int v = [] {
+        const char* e = std::getenv("QL_GEMV_CTAS_PER_SM");
+        const int n = e ? std::atoi(e) : 1;
+        return n < 1 ? 1 : n > 8 ? 8 : n;
+    }();
+    return v;
+}
 
 // Kernel attributes are set once per device, outside any stream capture.
 int gemv_prepare() {
@@ -619,7 +657,9 @@ int gemv_launch(const GemvArgs& a, cudaStream_t s, bool pdl) {
             p.S = S;
             p.seg_blocks = nblk / S;
             const size_t smem = (size_t)kWarps * kStages * kStageBytes + stage_smem;
-            const int grid = (p.ntile + kWarps / S - 1) / (kWarps / S);
+            int grid = (p.ntile + kWarps / S - 1) / (kWarps / S);
+            const int cap = gemv_ctas_per_sm() * sms;
+            if (grid > cap) grid = cap;
             e = launch(gemv_q4_0_lsm_kernel, dim3(grid), dim3(kThreads), smem, s, pdl, p, device_error_record());
         } else {
             while (S < kWarps && (long long)p.ntile * S < 12ll * sms && nblk / (2 * S) >= 8) S *= 2;

@@ -44,7 +44,9 @@ struct ql_model {
     size_t attn_ws_bytes = 0;
     std::vector<void*> owned;
     std::map<int64_t, cudaGraphExec_t> graphs;
-    bool next_prefetch = true;   // L2 prefetch of the following GEMV's weights (A/B: QL_NEXT_PREFETCH=0)
+    // L2 prefetch of the following GEMV's weights by every kernel (A/B switch QL_NEXT_PREFETCH=1).
+    // Off by default: measured slower (kernels that issue megabytes of prefetch stall).
+    bool next_prefetch = false;
 };
 
 namespace ql {
