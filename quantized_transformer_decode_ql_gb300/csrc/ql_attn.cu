@@ -54,7 +54,51 @@ struct AParams {
     int nsplit, spb;
     int prefetch;       // warm L2 with this CTA's K/V tiles before waiting on the predecessor
     NextWeights next;   // weights of the following kernel, prefetched into L2
+    // fused qk-norm + RoPE + KV append (decode step): q and the new K/V come from the f32 qkv
+    // projection instead of q; the CTA whose split holds the new position writes K/V to the pool
+    const float* qkv;
+    const float* q_norm;
+    const float* k_norm;
+    const float* cos_t;
+    const float* sin_t;
+    float eps;
+    long long max_position;
+    __half* kw;
+    __half* vw;
 };
+
+// Physical block of logical block lb of sequence b, or -1 if the table entry is out of range.
+__device__ __forceinline__ int bt_row_phys(const AParams& p, int b, int lb) {
+    const int phys = p.block_tables[(size_t)b * p.maxb + lb];
+    return (phys >= 0 && phys < p.num_blocks) ? phys : -1;
+}
+
+// RMSNorm over one head (weight w) and NeoX rotation at table row `pos`, by one warp:
+// lane handles the pairs (i, i + HD/2) for i = lane, lane + 32, ...; writes f16 to dst.
+template <int HD>
+__device__ __forceinline__ void warp_norm_rope(const float* src, const float* w, const float* cos_row,
+                                               const float* sin_row, float eps, __half* dst, int lane) {
+    constexpr int H2 = HD / 2, PER = H2 / 32;
+    float xa[PER], xb[PER];
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+        xa[k] = src[lane + 32 * k];
+        xb[k] = src[lane + 32 * k + H2];
+        ss += xa[k] * xa[k] + xb[k] * xb[k];
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float r = 1.0f / sqrtf(ss / (float)HD + eps);
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+        const int i = lane + 32 * k;
+        const float a = xa[k] * r * w[i], bb = xb[k] * r * w[i + H2];
+        const float c = cos_row[i], sn = sin_row[i];
+        dst[i] = __float2half_rn(a * c - bb * sn);
+        dst[i + H2] = __float2half_rn(a * sn + bb * c);
+    }
+}
 
 __device__ __forceinline__ float2 h2f(uint32_t u) {
     __half2 h;
@@ -121,9 +165,42 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AParams p, Dev
     const int gq = lane >> 2, tq = lane & 3;
     const bool hv = gq < G;
     uint32_t qa[KSTEPS][2];
+    __shared__ __align__(16) __half qs[G][HD];
+    const __half* qsrc;
+    if (p.qkv) {
+        // fused step: normalise + rotate the G query heads here; the CTA holding the new
+        // position's block also normalises + rotates the new key and appends K and V
+        const int pos = L - 1;
+        const float* src = p.qkv + (size_t)b * (p.n_heads + 2 * p.n_kv) * HD;
+        const bool pos_ok = pos < p.max_position;
+        if (!pos_ok && s == 0 && threadIdx.x == 0) record_device_error(err, kErrRopePosition, b, pos);
+        const float* cr = p.cos_t + (size_t)(pos_ok ? pos : 0) * (HD / 2);
+        const float* sr = p.sin_t + (size_t)(pos_ok ? pos : 0) * (HD / 2);
+        for (int h = warp; h < G; h += kAttnWarps)
+            warp_norm_rope<HD>(src + (size_t)(g * G + h) * HD, p.q_norm, cr, sr, p.eps, qs[h], lane);
+        const int lblk = pos / kBS;
+        if (pos_ok && lblk >= blk0 && lblk < blk1 && warp < 2) {
+            const int phys = bt_row_phys(p, b, lblk);
+            if (phys < 0) {
+                if (lane == 0) record_device_error(err, kErrRopeBlock, (long long)b * p.maxb + lblk, phys);
+            } else {
+                const size_t off = (((size_t)phys * p.n_kv + g) * kBS + (pos % kBS)) * HD;
+                if (warp == 0) {
+                    warp_norm_rope<HD>(src + (size_t)(p.n_heads + g) * HD, p.k_norm, cr, sr, p.eps, p.kw + off, lane);
+                } else {
+                    const float* vs = src + (size_t)(p.n_heads + p.n_kv + g) * HD;
+                    for (int i = lane; i < HD; i += 32) p.vw[off + i] = __float2half_rn(vs[i]);
+                }
+            }
+        }
+        __threadfence_block();
+        __syncthreads();
+        qsrc = &qs[0][0];
+    } else {
+        qsrc = p.q + ((size_t)b * p.n_heads + g * G) * HD;
+    }
     {
-        const uint32_t* qrow =
-            reinterpret_cast<const uint32_t*>(p.q + ((size_t)b * p.n_heads + g * G + (hv ? gq : 0)) * HD);
+        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(qsrc + (size_t)(hv ? gq : 0) * HD);
 #pragma unroll
         for (int kk = 0; kk < KSTEPS; ++kk) {
             qa[kk][0] = hv ? qrow[8 * kk + tq] : 0u;
@@ -433,8 +510,10 @@ size_t attn_workspace_bytes(int64_t batch, int n_heads, int n_kv_heads, int head
 }
 
 int attn_launch(const AttnArgs& a, cudaStream_t s, bool pdl) {
-    QL_REQUIRE(a.q && a.k_pool && a.v_pool && a.block_tables && a.out && a.workspace,
+    QL_REQUIRE((a.q || a.qkv) && a.k_pool && a.v_pool && a.block_tables && a.out && a.workspace,
                "attention: null pointer");
+    QL_REQUIRE(!a.qkv || (a.q_norm && a.k_norm && a.cos_t && a.sin_t && a.positions && a.max_position > 0),
+               "attention: the fused qk-norm/RoPE form needs norms, tables and positions");
     QL_REQUIRE(a.context_lens || a.positions, "attention: need context lengths or positions");
     QL_REQUIRE(a.head_dim == 64 || a.head_dim == 128, "attention: head_dim must be 64 or 128");
     QL_REQUIRE(a.block_size == kBS, "attention: block_size must be 16");
@@ -476,6 +555,15 @@ int attn_launch(const AttnArgs& a, cudaStream_t s, bool pdl) {
     p.spb = lo.spb;
     p.prefetch = a.context_lens == nullptr ? 1 : 0;
     p.next = a.next;
+    p.qkv = a.qkv;
+    p.q_norm = a.q_norm;
+    p.k_norm = a.k_norm;
+    p.cos_t = a.cos_t;
+    p.sin_t = a.sin_t;
+    p.eps = a.eps;
+    p.max_position = a.max_position;
+    p.kw = const_cast<__half*>(a.k_pool);
+    p.vw = const_cast<__half*>(a.v_pool);
     cudaError_t e = a.head_dim == 128 ? launch_h<128>(p, G, a.batch, s, pdl)
                                       : launch_h<64>(p, G, a.batch, s, pdl);
     if (e != cudaSuccess) return cuda_error(e, "attention launch");

@@ -433,9 +433,8 @@ __global__ void __launch_bounds__(kThreads, 3) gemv_q4_0_lsm_kernel(KParams p, D
     const int half_rows = p.rows >> 1;
     const int tiles_per_cta = kWarps / p.S;
     const int seg = warp % p.S;
-    // The CTA walks tile groups blockIdx.x, blockIdx.x + gridDim.x, ... (a grid of about one CTA
-    // per SM leaves room for the next kernel's CTAs, which PDL starts early); every warp runs
-    // the same number of (tile, segment) tasks, so the per-task barriers line up.
+    // The CTA walks tile groups blockIdx.x, blockIdx.x + gridDim.x, ...; every warp runs the same
+    // number of (tile, segment) tasks, so the per-task barriers line up.
     const int ngroups = (p.ntile + tiles_per_cta - 1) / tiles_per_cta;
     const int my_groups = (int)blockIdx.x < ngroups ? (ngroups - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
     const int nit = p.seg_blocks / kGroupBlocks;      // iterations (4 blocks each) per task
@@ -560,12 +559,13 @@ __global__ void __launch_bounds__(kThreads, 3) gemv_q4_0_lsm_kernel(KParams p, D
 
 }  // namespace
 
-// CTAs per SM of the main GEMV grid (the CTAs loop over tile groups). One leaves room for the
-// next kernel of the step to become resident early; QL_GEMV_CTAS_PER_SM overrides it for A/B.
+// CTAs per SM of the main GEMV grid (the CTAs loop over tile groups): 3, the occupancy limit of
+// the kernel, measured fastest in the decode step (1 per SM, which would leave room for the next
+// kernel to start early, was slower). QL_GEMV_CTAS_PER_SM overrides it for A/B measurements.
 int gemv_ctas_per_sm() {
     static int v = [] {
         const char* e = std::getenv("QL_GEMV_CTAS_PER_SM");
-        const int n = e ? std::atoi(e) : 1;
+        const int n = e ? std::atoi(e) : 3;
         return n < 1 ? 1 : n > 8 ? 8 : n;
     }();
     return v;

@@ -160,6 +160,14 @@ struct AttnArgs {
     void* workspace;
     size_t workspace_bytes;
     NextWeights next;
+    // fused qk-norm + RoPE + KV append (decode step); q is unused when qkv is set
+    const float* qkv;
+    const float* q_norm;
+    const float* k_norm;
+    const float* cos_t;
+    const float* sin_t;
+    float eps;
+    int64_t max_position;
 };
 size_t attn_workspace_bytes(int64_t batch, int n_heads, int n_kv_heads, int head_dim,
                             int block_size, int64_t max_blocks_per_seq);

@@ -145,37 +145,21 @@ int run_step(ql_model* m, const ql_step_args* a, cudaStream_t s) {
         g.epilogue = QL_EPI_NONE;
         g.y_dtype = QL_DTYPE_F32;
         g.y = m->qkv;
-        g.next = nw(L.o, kAll);
+        g.next = nw(L.gate_up, kAll);
         if ((rc = gemv_launch(g, s, pdl)) != QL_OK) return rc;
 
-        RopeArgs r = {};
-        r.qkv = m->qkv;
-        r.q_norm = L.q_norm;
-        r.k_norm = L.k_norm;
-        r.cos_t = m->cos_t;
-        r.sin_t = m->sin_t;
-        r.positions = a->positions;
-        r.active = a->active;
-        r.eps = d.eps;
-        r.batch = B;
-        r.n_heads = nh;
-        r.n_kv_heads = nkv;
-        r.head_dim = hd;
-        r.q_out = m->q16;
-        r.k_pool = static_cast<__half*>(d.k_pool) + layer_pool * li;
-        r.v_pool = static_cast<__half*>(d.v_pool) + layer_pool * li;
-        r.block_tables = a->block_tables;
-        r.max_blocks_per_seq = d.max_blocks_per_seq;
-        r.block_size = d.block_size;
-        r.num_blocks = d.num_blocks;
-        r.max_position = d.max_blocks_per_seq * d.block_size;
-        r.next = nw(L.gate_up, kAll);
-        if ((rc = rope_launch(r, s, pdl)) != QL_OK) return rc;
-
+        // attention with the qk-norm + RoPE + KV append fused in (reads the f32 qkv projection)
         AttnArgs at = {};
-        at.q = m->q16;
-        at.k_pool = r.k_pool;
-        at.v_pool = r.v_pool;
+        at.q = nullptr;
+        at.qkv = m->qkv;
+        at.q_norm = L.q_norm;
+        at.k_norm = L.k_norm;
+        at.cos_t = m->cos_t;
+        at.sin_t = m->sin_t;
+        at.eps = d.eps;
+        at.max_position = d.max_blocks_per_seq * d.block_size;
+        at.k_pool = static_cast<__half*>(d.k_pool) + layer_pool * li;
+        at.v_pool = static_cast<__half*>(d.v_pool) + layer_pool * li;
         at.block_tables = a->block_tables;
         at.context_lens = nullptr;
         at.positions = a->positions;
