@@ -205,6 +205,30 @@ typedef struct ql_model ql_model;
 int ql_model_create(const ql_model_desc* desc, ql_model** out);
 int ql_model_destroy(ql_model* m);
 
+/* How a decode step runs. QL_STEP_PERSISTENT: the whole step as ONE cooperative kernel, one
+ * CTA per SM, that streams every layer's weights through shared-memory rings and separates the
+ * step's phases (q|k|v, attention, o, gate|up, down per layer; lm_head) with grid-wide
+ * barriers in device memory; it takes batches up to ql_model_persistent_max_batch() (at most
+ * 2). QL_STEP_LAUNCHES: one kernel per phase (any batch up to max_batch). QL_STEP_AUTO (the
+ * default): persistent when the batch allows it, else launches. Both compute the same step
+ * ([IL] CudaQwen3::step); their f32 sums differ only in rounding order.               */
+enum { QL_STEP_AUTO = 0, QL_STEP_LAUNCHES = 1, QL_STEP_PERSISTENT = 2 };
+/* Options of a model handle:
+ *   QL_OPT_STEP_KERNEL         one of QL_STEP_*; QL_STEP_PERSISTENT is QL_EINVAL when the
+ *                              model has no persistent kernel (max batch 0)
+ *   QL_OPT_BARRIER_TIMEOUT_NS  bound on every grid-barrier wait of the persistent step
+ *                              (default 2e9 ns). A wait that runs out records a device error
+ *                              (read with ql_check_device_error), every CTA leaves the step
+ *                              and the step's outputs are not written; the next step runs
+ *                              normally. Nothing else waits on another CTA.
+ * Applies to steps issued (or graphs captured) afterwards. QL_EINVAL for anything else.  */
+enum { QL_OPT_STEP_KERNEL = 1, QL_OPT_BARRIER_TIMEOUT_NS = 2 };
+int ql_model_set_option(ql_model* m, int option, int64_t value);
+/* Largest batch the persistent step kernel takes for this model on its device: 0 when the
+ * shape or the device does not allow it (matrix widths must be multiples of 128, codes 16-byte
+ * and scales 8-byte aligned, one CTA with ~200 KB of shared memory per SM).              */
+int64_t ql_model_persistent_max_batch(const ql_model* m);
+
 /* One decode step for `batch` slots ([IL] CudaQwen3::step, [FK] batch_decode_step).
  * Every per-step input lives in device memory so the step can be captured and replayed:
  *   tokens      int32 [batch]  this step's token per slot (read)

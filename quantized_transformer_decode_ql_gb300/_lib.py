@@ -16,6 +16,8 @@ LIB_PATH = os.path.join(PKG, "_build", "libql.so")
 QL_OK, QL_EINVAL, QL_ENOMEM, QL_ECUDA, QL_EPOOL, QL_ERANGE, QL_EDEVICE, QL_ESTATE = 0, -1, -2, -3, -4, -5, -6, -7
 QL_DTYPE_F32, QL_DTYPE_F16 = 0, 1
 QL_EPI_NONE, QL_EPI_ADD_RESIDUAL, QL_EPI_SILU_MUL = 0, 1, 2
+QL_STEP_AUTO, QL_STEP_LAUNCHES, QL_STEP_PERSISTENT = 0, 1, 2
+QL_OPT_STEP_KERNEL, QL_OPT_BARRIER_TIMEOUT_NS = 1, 2
 
 
 class QLError(RuntimeError):
@@ -74,6 +76,8 @@ SIGNATURES = {
     "ql_rope_tables": (c_int, [c_void_p, c_void_p, c_int64, c_int, c_double]),
     "ql_model_create": (c_int, [POINTER(ModelDesc), POINTER(c_void_p)]),
     "ql_model_destroy": (c_int, [c_void_p]),
+    "ql_model_set_option": (c_int, [c_void_p, c_int, c_int64]),
+    "ql_model_persistent_max_batch": (c_int64, [c_void_p]),
     "ql_decode_step": (c_int, [c_void_p, POINTER(StepArgs), c_void_p]),
     "ql_decode_graph_capture": (c_int, [c_void_p, POINTER(StepArgs), c_void_p]),
     "ql_decode_graph_replay": (c_int, [c_void_p, c_int64, c_int, c_void_p]),

@@ -79,6 +79,7 @@ static const char* where_name(int w) {
         case kErrPackNonFinite: return "q4_0 pack: non-finite weight";
         case kErrPackOverflow: return "q4_0 pack: block scale overflows f16";
         case kErrGemvStage: return "gemv: a staged weight copy did not arrive (bounded wait expired)";
+        case kErrStepBarrier: return "persistent step: a grid barrier wait ran out (index = barrier, value = CTA)";
         default: return "unknown";
     }
 }

@@ -44,6 +44,7 @@ enum DevErrWhere {
     kErrPackNonFinite = 6,
     kErrPackOverflow = 7,
     kErrGemvStage = 8,
+    kErrStepBarrier = 9,
 };
 // The current device's record (allocated on first use, zero-filled).
 DevError* device_error_record();
@@ -196,5 +197,64 @@ struct RopeArgs {
     NextWeights next;
 };
 int rope_launch(const RopeArgs& a, cudaStream_t s, bool pdl);
+
+// ---------------------------------------------------------------- persistent decode step
+// The whole step of a small batch as one cooperative kernel (one CTA per SM); see
+// ql_persist.cuh. Matrices are described as the kernel streams them.
+struct PMat {
+    const uint8_t* quants;
+    const __half* scales;
+    int rows, nblk;     // nblk = cols / 32, a multiple of 4
+    int silu;           // rows = [gate | up]; a tile is 8 gate rows + the matching 8 up rows
+    int ntile;          // 16-row tiles
+};
+struct PLayer {
+    PMat m[4];          // q|k|v, o, gate|up, down
+    const float* attn_norm;
+    const float* ffn_norm;
+    const float* q_norm;
+    const float* k_norm;
+};
+constexpr int kPersistMaxBatch = 2;
+struct PersistParams {
+    const PLayer* layers;   // device array [n_layers]
+    int n_layers;
+    PMat lm;
+    const float* final_norm;
+    const float* embed;
+    int hidden, inter, vocab, nh, nkv, B, maxb, nsplit, max_nblk;
+    float eps, scale_log2;
+    long long num_blocks, layer_pool, max_position, out_stride;
+    unsigned long long barrier_timeout_ns;
+    const int32_t* tokens;
+    int32_t* positions;
+    const int32_t* block_tables;
+    const int32_t* active;
+    int32_t* next_tokens;
+    int32_t* out_tokens;
+    float* logits;
+    float* x;       // [B][hidden] f32 residual stream
+    float* qkv;     // [B][(nh + 2 nkv) hd] f32
+    __half* attn;   // [B][nh hd]
+    __half* act;    // [B][inter]
+    unsigned long long* keys;   // [B] packed argmax keys, zero between steps
+    const float* cos_t;
+    const float* sin_t;
+    __half* k_pool;
+    __half* v_pool;
+    float* pm;      // [B][nh][nsplit] split partials of the attention
+    float* pl;
+    float* pacc;    // [B][nh][nsplit][hd]
+    int* tickets;   // [B][nkv], zero between steps
+    unsigned int* sync;   // [4], zero between steps: barrier arrivals, exits, abort flag
+    DevError* err;
+};
+// Dynamic shared memory of the step kernel for a batch of `batch` and matrices of at most
+// max_nblk blocks per row.
+size_t persist_smem_bytes(int batch, int max_nblk, int head_dim, int group);
+// Sets the kernel attributes for this shape and checks that one CTA fits on every SM with a
+// cooperative launch: QL_OK, or QL_EINVAL with the reason in ql_last_error().
+int persist_prepare(int batch, int max_nblk, int head_dim, int group);
+int persist_launch(const PersistParams& p, int head_dim, int group, cudaStream_t s);
 
 }  // namespace ql

@@ -6,8 +6,10 @@
 // and the position advance stay on the device. [FK] ferrum-kernels cuda_decode.rs
 // batch_decode_step: several sequences per step over a paged KV pool.
 //
-// Kernel sequence of one step (batch B), all launched with programmatic dependent launch so
-// that each GEMV starts streaming its weights into L2 while its predecessor drains:
+// Batches up to ql_model_persistent_max_batch() run the step as ONE cooperative kernel
+// (ql_persist.cuh) unless QL_OPT_STEP_KERNEL says otherwise. Larger batches run this kernel
+// sequence, all launched with programmatic dependent launch so that each GEMV starts streaming
+// its weights into L2 while its predecessor drains:
 //   embed                      x[b] = E[token[b]]                          (f32 residual)
 //   per layer:
 //     gemv  rms(x)*attn_norm -> W_qkv                                       -> qkv f32
@@ -47,6 +49,18 @@ struct ql_model {
     // L2 prefetch of the following GEMV's weights by every kernel (A/B switch QL_NEXT_PREFETCH=1).
     // Off by default: measured slower (kernels that issue megabytes of prefetch stall).
     bool next_prefetch = false;
+    // persistent step kernel (one cooperative launch per step) for batches up to persist_max_b
+    int persist_max_b = 0;                  // 0: not available for this shape / device
+    int step_kernel = QL_STEP_AUTO;
+    unsigned long long barrier_timeout_ns = 2000000000ull;
+    ql::PLayer* players = nullptr;          // device [n_layers]
+    ql::PMat plm = {};
+    int max_nblk = 0, persist_nsplit = 1;
+    float* ppm = nullptr;
+    float* ppl = nullptr;
+    float* ppacc = nullptr;
+    int* ptickets = nullptr;
+    unsigned int* psync = nullptr;
 };
 
 namespace ql {
@@ -101,9 +115,67 @@ int alloc(ql_model* m, void** p, size_t bytes) {
     return QL_OK;
 }
 
+// The whole step as one cooperative kernel (ql_persist.cuh).
+int run_persist(ql_model* m, const ql_step_args* a, cudaStream_t s) {
+    const ql_model_desc& d = m->d;
+    const int B = (int)a->batch;
+    PersistParams p = {};
+    p.layers = m->players;
+    p.n_layers = (int)d.n_layers;
+    p.lm = m->plm;
+    p.final_norm = d.final_norm;
+    p.embed = d.embed;
+    p.hidden = (int)d.hidden;
+    p.inter = (int)d.intermediate;
+    p.vocab = (int)d.vocab;
+    p.nh = (int)d.n_heads;
+    p.nkv = (int)d.n_kv_heads;
+    p.B = B;
+    p.maxb = (int)d.max_blocks_per_seq;
+    int nsplit = num_sms() / (B * (int)d.n_kv_heads);
+    nsplit = nsplit < 1 ? 1 : nsplit > m->persist_nsplit ? m->persist_nsplit : nsplit;
+    p.nsplit = nsplit;
+    p.max_nblk = m->max_nblk;
+    p.eps = d.eps;
+    p.scale_log2 = 1.4426950408889634f / sqrtf((float)d.head_dim);
+    p.num_blocks = d.num_blocks;
+    p.layer_pool = (long long)d.num_blocks * d.n_kv_heads * d.block_size * d.head_dim;
+    p.max_position = d.max_blocks_per_seq * d.block_size;
+    p.out_stride = a->out_tokens ? a->out_stride : 0;
+    p.barrier_timeout_ns = m->barrier_timeout_ns;
+    p.tokens = a->tokens;
+    p.positions = a->positions;
+    p.block_tables = a->block_tables;
+    p.active = a->active;
+    p.next_tokens = a->next_tokens;
+    p.out_tokens = a->out_tokens;
+    p.logits = a->logits ? a->logits : m->logits;
+    p.x = m->x;
+    p.qkv = m->qkv;
+    p.attn = m->attn;
+    p.act = m->act;
+    p.keys = m->keys;
+    p.cos_t = m->cos_t;
+    p.sin_t = m->sin_t;
+    p.k_pool = static_cast<__half*>(d.k_pool);
+    p.v_pool = static_cast<__half*>(d.v_pool);
+    p.pm = m->ppm;
+    p.pl = m->ppl;
+    p.pacc = m->ppacc;
+    p.tickets = m->ptickets;
+    p.sync = m->psync;
+    p.err = device_error_record();
+    if (!p.err) return set_error(QL_ECUDA, "decode step: no device error record");
+    return persist_launch(p, (int)d.head_dim, (int)(d.n_heads / d.n_kv_heads), s);
+}
+
 int run_step(ql_model* m, const ql_step_args* a, cudaStream_t s) {
     const ql_model_desc& d = m->d;
     const int B = (int)a->batch;
+    if (m->step_kernel == QL_STEP_PERSISTENT && B > m->persist_max_b)
+        return set_error(QL_EINVAL, "decode step: the persistent step kernel takes batches up to " +
+                                        std::to_string(m->persist_max_b) + " on this model");
+    if (m->step_kernel != QL_STEP_LAUNCHES && B <= m->persist_max_b) return run_persist(m, a, s);
     const bool pdl = true;
     const int hd = (int)d.head_dim, nh = (int)d.n_heads, nkv = (int)d.n_kv_heads;
     const size_t layer_pool = (size_t)d.num_blocks * nkv * d.block_size * hd;
@@ -246,6 +318,76 @@ int run_step(ql_model* m, const ql_step_args* a, cudaStream_t s) {
     return QL_OK;
 }
 
+PMat pmat(const ql_q4_0_matrix& w, bool silu) {
+    PMat p = {};
+    p.quants = static_cast<const uint8_t*>(w.quants);
+    p.scales = static_cast<const __half*>(w.scales);
+    p.rows = (int)w.rows;
+    p.nblk = (int)(w.cols / 32);
+    p.silu = silu ? 1 : 0;
+    p.ntile = silu ? (int)((w.rows / 2 + 7) / 8) : (int)((w.rows + 15) / 16);
+    return p;
+}
+
+// Enable the persistent step kernel when the shape and the device allow it (persist_max_b > 0).
+// A shape it does not take is not an error: the step then always runs as separate launches.
+int setup_persist(ql_model* m) {
+    const ql_model_desc& d = m->d;
+    auto al = [](const void* q, uintptr_t n) { return (reinterpret_cast<uintptr_t>(q) & (n - 1)) == 0; };
+    auto mat_ok = [&](const ql_q4_0_matrix& w) {
+        return w.cols % 128 == 0 && w.rows < (1ll << 30) && al(w.quants, 16) && al(w.scales, 8);
+    };
+    bool ok = d.vocab < (1ll << 30) && al(d.embed, 16) && al(d.final_norm, 16) && mat_ok(d.lm_head);
+    for (const ql_layer_desc& L : m->layers)
+        ok = ok && mat_ok(L.qkv) && mat_ok(L.o) && mat_ok(L.gate_up) && mat_ok(L.down) && al(L.attn_norm, 16) &&
+             al(L.ffn_norm, 16);
+    if (!ok) return QL_OK;
+    const int64_t widths[3] = {d.hidden, d.intermediate, d.n_heads * d.head_dim};
+    int64_t w = 0;
+    for (int64_t v : widths) w = v > w ? v : w;
+    m->max_nblk = (int)(w / 32);
+    const int G = (int)(d.n_heads / d.n_kv_heads);
+    int maxb = (int)(d.max_batch < kPersistMaxBatch ? d.max_batch : kPersistMaxBatch);
+    for (; maxb >= 1; --maxb)
+        if (persist_prepare(maxb, m->max_nblk, (int)d.head_dim, G) == QL_OK) break;
+    if (maxb < 1) return QL_OK;
+
+    std::vector<PLayer> hl(m->layers.size());
+    for (size_t i = 0; i < hl.size(); ++i) {
+        const ql_layer_desc& L = m->layers[i];
+        hl[i].m[0] = pmat(L.qkv, false);
+        hl[i].m[1] = pmat(L.o, false);
+        hl[i].m[2] = pmat(L.gate_up, true);
+        hl[i].m[3] = pmat(L.down, false);
+        hl[i].attn_norm = L.attn_norm;
+        hl[i].ffn_norm = L.ffn_norm;
+        hl[i].q_norm = L.q_norm;
+        hl[i].k_norm = L.k_norm;
+    }
+    m->plm = pmat(d.lm_head, false);
+    int nsplit = num_sms();
+    nsplit = nsplit > 256 ? 256 : nsplit;
+    nsplit = nsplit > d.max_blocks_per_seq ? (int)d.max_blocks_per_seq : nsplit;
+    m->persist_nsplit = nsplit < 1 ? 1 : nsplit;
+    const size_t parts = (size_t)maxb * d.n_heads * m->persist_nsplit;
+    int rc = QL_OK;
+    auto A = [&](void** p, size_t bytes) { if (rc == QL_OK) rc = alloc(m, p, bytes); };
+    A((void**)&m->players, hl.size() * sizeof(PLayer));
+    A((void**)&m->ppm, parts * 4);
+    A((void**)&m->ppl, parts * 4);
+    A((void**)&m->ppacc, parts * d.head_dim * 4);
+    A((void**)&m->ptickets, (size_t)maxb * d.n_kv_heads * 4);
+    A((void**)&m->psync, 16);
+    if (rc != QL_OK) return rc;
+    cudaError_t e = cudaMemcpy(m->players, hl.data(), hl.size() * sizeof(PLayer), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemset(m->ptickets, 0, (size_t)maxb * d.n_kv_heads * 4);
+    if (e == cudaSuccess) e = cudaMemset(m->psync, 0, 16);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_error(e, "ql_model_create: persistent step workspace");
+    m->persist_max_b = maxb;
+    return QL_OK;
+}
+
 int check_step_args(ql_model* m, const ql_step_args* a) {
     if (!m || !a) return set_error(QL_EINVAL, "decode step: null model or args");
     if (a->batch < 1 || a->batch > m->d.max_batch)
@@ -337,6 +479,7 @@ extern "C" int ql_model_create(const ql_model_desc* desc, ql_model** out) {
         if (rc == QL_OK && e == cudaSuccess) e = cudaDeviceSynchronize();
         if (rc == QL_OK && e != cudaSuccess) rc = cuda_error(e, "ql_model_create: workspace init");
     }
+    if (rc == QL_OK) rc = setup_persist(m);
     if (rc != QL_OK) {
         std::string msg = ql_last_error();
         ql_model_destroy(m);
@@ -353,6 +496,27 @@ extern "C" int ql_model_destroy(ql_model* m) {
     delete m;
     return QL_OK;
 }
+
+extern "C" int ql_model_set_option(ql_model* m, int option, int64_t value) {
+    if (!m) return set_error(QL_EINVAL, "ql_model_set_option: null model");
+    switch (option) {
+        case QL_OPT_STEP_KERNEL:
+            if (value != QL_STEP_AUTO && value != QL_STEP_LAUNCHES && value != QL_STEP_PERSISTENT)
+                return set_error(QL_EINVAL, "ql_model_set_option: unknown step kernel");
+            if (value == QL_STEP_PERSISTENT && m->persist_max_b < 1)
+                return set_error(QL_EINVAL, "ql_model_set_option: the persistent step kernel is not available for this model");
+            m->step_kernel = (int)value;
+            return QL_OK;
+        case QL_OPT_BARRIER_TIMEOUT_NS:
+            if (value < 0) return set_error(QL_EINVAL, "ql_model_set_option: negative timeout");
+            m->barrier_timeout_ns = (unsigned long long)value;
+            return QL_OK;
+        default:
+            return set_error(QL_EINVAL, "ql_model_set_option: unknown option");
+    }
+}
+
+extern "C" int64_t ql_model_persistent_max_batch(const ql_model* m) { return m ? m->persist_max_b : 0; }
 
 extern "C" int ql_decode_step(ql_model* m, const ql_step_args* args, void* stream) {
     int rc = check_step_args(m, args);

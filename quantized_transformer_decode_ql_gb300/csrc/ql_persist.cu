@@ -1,0 +1,52 @@
+// Persistent decode step: kernels for head_dim 128 and the host entry points (the kernel
+// itself is in ql_persist.cuh; head_dim 64 in ql_persist_hd64.cu).
+#include "ql_persist.cuh"
+
+#include <string>
+
+namespace ql {
+
+cudaError_t persist_dispatch_hd128(int G, bool launch, const PersistParams* p, size_t smem, int grid,
+                                   cudaStream_t s, int* occ) {
+    return persist::dispatch<128>(G, launch, p, smem, grid, s, occ);
+}
+
+size_t persist_smem_bytes(int batch, int max_nblk, int head_dim, int group) {
+    const size_t a = persist::gemv_region_bytes(batch, max_nblk);
+    const size_t b = persist::attn_region_bytes(head_dim, group);
+    return persist::kRingBytes + (a > b ? a : b);
+}
+
+int persist_prepare(int batch, int max_nblk, int head_dim, int group) {
+    QL_REQUIRE(batch >= 1 && batch <= kPersistMaxBatch, "persistent step: batch out of range");
+    QL_REQUIRE(head_dim == 64 || head_dim == 128, "persistent step: head_dim must be 64 or 128");
+    QL_REQUIRE(group == 1 || group == 2 || group == 4 || group == 8, "persistent step: GQA group must be 1, 2, 4 or 8");
+    QL_REQUIRE(max_nblk > 0 && max_nblk % persist::kUnitBlocks == 0,
+               "persistent step: matrix widths must be multiples of 128");
+    int dev = 0, coop = 0, optin = 0;
+    QL_TRY_CUDA(cudaGetDevice(&dev));
+    QL_TRY_CUDA(cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev));
+    QL_TRY_CUDA(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
+    QL_REQUIRE(coop != 0, "persistent step: the device has no cooperative launch");
+    const size_t smem = persist_smem_bytes(batch, max_nblk, head_dim, group);
+    if (smem > (size_t)optin)
+        return set_error(QL_EINVAL, "persistent step: needs " + std::to_string(smem) +
+                                        " bytes of shared memory per CTA, the device allows " + std::to_string(optin));
+    int occ = 0;
+    const cudaError_t e = head_dim == 128 ? persist_dispatch_hd128(group, false, nullptr, smem, 0, nullptr, &occ)
+                                          : persist_dispatch_hd64(group, false, nullptr, smem, 0, nullptr, &occ);
+    if (e != cudaSuccess) return cuda_error(e, "persistent step: kernel attributes");
+    QL_REQUIRE(occ >= 1, "persistent step: one CTA per SM does not fit (shared memory or registers)");
+    return QL_OK;
+}
+
+int persist_launch(const PersistParams& p, int head_dim, int group, cudaStream_t s) {
+    const size_t smem = persist_smem_bytes(p.B, p.max_nblk, head_dim, group);
+    const int grid = num_sms();
+    const cudaError_t e = head_dim == 128 ? persist_dispatch_hd128(group, true, &p, smem, grid, s, nullptr)
+                                          : persist_dispatch_hd64(group, true, &p, smem, grid, s, nullptr);
+    if (e != cudaSuccess) return cuda_error(e, "persistent step launch");
+    return QL_OK;
+}
+
+}  // namespace ql

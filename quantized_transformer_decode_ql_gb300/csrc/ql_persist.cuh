@@ -1,0 +1,1008 @@
+// Persistent decode step: the whole step of a batch of 1-2 sequences as ONE cooperative kernel.
+//
+// [IL] inferencelayer cuda_llm.rs, CudaQwen3::step (the step's dataflow: RMSNorm -> q|k|v ->
+// qk-norm + RoPE -> paged attention -> o + residual -> RMSNorm -> gate|up -> SiLU*up -> down +
+// residual; final norm, lm_head and greedy argmax; q4_0 weights with one GEMV per projection
+// group); [FK] ferrum-kernels cuda_decode.rs (split-K paged decode attention over 16-token
+// blocks of an f16 pool, valid length = position + 1).
+//
+// Why (GB300). At batch 1 a step streams 4.26 GB of q4_0 weights through 5 dependent phases per
+// layer. As separate launches each phase pays a ramp and a tail: a 10-60 MB stream reaches only
+// 2-4.6 TB/s of the ~6.7 TB/s the part sustains. Here one CTA per SM runs the whole step:
+//  * every warp owns a fixed sequence of weight "units" (16 rows x 4 q4_0 blocks: 1 KB of codes
+//    plus 128 B of scales) over ALL the step's matrices and streams them through a private
+//    shared-memory ring with cp.async. Weights do not depend on activations, so the ring fills
+//    with the next phase's weights while the CTA waits at a grid barrier, stages activations or
+//    runs attention: HBM keeps streaming across phase boundaries;
+//  * phases are separated by a grid-wide barrier (a counter in global memory, bounded wait:
+//    after a timeout the CTA records an error, raises an abort flag and leaves the step);
+//  * a matrix is split over CTAs by 16-row tiles, and inside a CTA over the 16 warps by flat
+//    (tile, 4-block group) units, so every warp streams the same number of bytes; a tile shared
+//    by several warps is reduced in shared memory in warp order (deterministic), the others are
+//    finished from registers;
+//  * the GEMV arithmetic is the one of the stand-alone q4_0 GEMV: nibbles OR'ed into the
+//    mantissa of 1024.0h give 1024 + q (low) and 1024 + 16 q (high, against activations staged
+//    pre-divided by 16) exactly; mma.sync m16n8k16 (f16 in, f32 accumulate) does the products;
+//    the offsets are folded into the accumulator start; one FFMA per block applies the scale;
+//  * attention: one CTA per (sequence, kv head, split), each warp one 16-token block at a
+//    time. K is loaded straight into MMA fragments with 16-byte loads (head_dim permuted the
+//    same way in Q and K, which leaves the dot products unchanged), S = Q K^T on mma.sync,
+//    online softmax in the exp2 domain, P.V on the CUDA cores with coalesced V rows; warps merge
+//    in shared memory, splits merge in the CTA that finishes last (atomic ticket, no waiting).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <math.h>
+
+#include "ql_internal.h"
+
+namespace ql {
+namespace persist {
+
+constexpr int kW = 16;                  // warps per CTA
+constexpr int kT = kW * 32;             // threads per CTA
+constexpr int kStages = 8;              // ring stages (units in flight) per warp
+constexpr int kUnitBlocks = 4;          // q4_0 blocks per row in one unit
+constexpr int kUnitBytes = kUnitBlocks * 16 * 16 + 16 * kUnitBlocks * 2;   // 1152
+constexpr int kRingBytes = kW * kStages * kUnitBytes;
+constexpr int kBS = 16;                 // tokens per KV block
+constexpr int kMaxB = kPersistMaxBatch;
+constexpr int kMaxSplit = 256;
+constexpr int kPartBytes = kW * 2 * 32 * 16;   // per-warp partial fragments of shared tiles
+
+enum Epi { kEpiF32 = 0, kEpiResid = 1, kEpiSilu = 2, kEpiLogits = 3 };
+
+// Shared memory behind the rings: the GEMV staging (activations, offset terms, partials) or
+// the attention merge buffers, whichever is larger.
+__host__ __device__ constexpr size_t gemv_region_bytes(int batch, int max_nblk) {
+    return (size_t)batch * (max_nblk * 4 + 4) * 16 + (size_t)max_nblk * 2 * 4 + kPartBytes;
+}
+__host__ __device__ constexpr size_t attn_region_bytes(int head_dim, int group) {
+    return (size_t)kW * (group * head_dim > 128 ? group * head_dim : 128) * 4 + (size_t)2 * kW * group * 4;
+}
+
+__device__ __forceinline__ __half2 as_h2(uint32_t u) {
+    __half2 h;
+    *reinterpret_cast<uint32_t*>(&h) = u;
+    return h;
+}
+__device__ __forceinline__ uint32_t as_u32(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+
+__device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
+
+// Order-preserving key: larger logit -> larger key; among equal logits the lower row wins.
+__device__ __forceinline__ unsigned long long argmax_key(float v, int row) {
+    uint32_t b = __float_as_uint(v);
+    b = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    return ((unsigned long long)b << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)row);
+}
+
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+// ------------------------------------------------------------------------------ grid barrier
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ unsigned int load_acquire(const unsigned int* a) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+    return v;
+}
+
+// Barrier over the co-resident CTAs of the launch. sync[0] counts arrivals over the whole
+// launch (the k-th barrier waits for k * gridDim.x of them); sync[2] is the abort flag. The wait
+// is bounded by the clock: after p.barrier_timeout_ns the CTA records an error, raises the flag
+// and returns false, as does every CTA that sees the flag; the caller then leaves the step.
+static __device__ __noinline__ bool grid_barrier(const PersistParams& p, unsigned int& target, int* ok_smem) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        target += gridDim.x;
+        int ok = 1;
+        __threadfence();
+        atomicAdd(p.sync, 1u);
+        if (load_acquire(p.sync) < target) {
+            const unsigned long long t0 = global_ns();
+            for (unsigned int spin = 1;; ++spin) {
+                if (load_acquire(p.sync) >= target) break;
+                if ((spin & 15u) == 0) {
+                    if (load_acquire(p.sync + 2) != 0u) {
+                        ok = 0;
+                        break;
+                    }
+                    if (global_ns() - t0 > p.barrier_timeout_ns) {
+                        record_device_error(p.err, kErrStepBarrier, (long long)(target / gridDim.x),
+                                            (long long)blockIdx.x);
+                        atomicExch(p.sync + 2, 1u);
+                        ok = 0;
+                        break;
+                    }
+                }
+            }
+        }
+        __threadfence();
+        *ok_smem = ok;
+    }
+    __syncthreads();
+    return *ok_smem != 0;
+}
+
+// Every CTA calls this once, last. The CTA that leaves last re-arms the counters for the next
+// launch (all others are past their last wait by then); after an abort it also clears the
+// attention tickets, which an interrupted phase may have left counted.
+static __device__ void leave_step(const PersistParams& p) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(p.sync + 1, 1u) == gridDim.x - 1) {
+            if (atomicAdd(p.sync + 2, 0u) != 0u)
+                for (int i = 0; i < p.B * p.nkv; ++i) atomicExch(p.tickets + i, 0);
+            atomicExch(p.sync, 0u);
+            atomicExch(p.sync + 2, 0u);
+            __threadfence();
+            atomicExch(p.sync + 1, 0u);
+        }
+    }
+}
+
+// ------------------------------------------------------------------------------ weight ring
+// The step's matrices in streaming order: 4 per layer (q|k|v, o, gate|up, down), then lm_head.
+__device__ __forceinline__ PMat mat_at(const PersistParams& p, int wp) {
+    return wp < 4 * p.n_layers ? p.layers[wp >> 2].m[wp & 3] : p.lm;
+}
+// Tiles [t0, t1) of a matrix handled by this CTA (balanced to one tile).
+__device__ __forceinline__ void cta_tiles(int ntile, int& t0, int& t1) {
+    t0 = (int)(((long long)blockIdx.x * ntile) / gridDim.x);
+    t1 = (int)(((long long)(blockIdx.x + 1) * ntile) / gridDim.x);
+}
+// First unit of warp w among the U units of its CTA (balanced to one unit).
+__device__ __forceinline__ int warp_unit(int U, int w) { return (int)(((long long)w * U) / kW); }
+
+// Global row of row r (0..15) of a tile; rows past the matrix read row 0 and are discarded.
+__device__ __forceinline__ int tile_row(const PMat& M, int tile, int r, bool& ok) {
+    if (M.silu) {
+        const int half = M.rows >> 1, i = tile * 8 + (r & 7);
+        ok = i < half;
+        return ok ? (r < 8 ? i : half + i) : 0;
+    }
+    const int row = tile * 16 + r;
+    ok = row < M.rows;
+    return ok ? row : 0;
+}
+
+// Issue side of a warp's ring (per-lane state). A unit is stored as codes [block 0..3][row
+// 0..15] x 16 B, then the 16 rows' 4 scales (8 B each): lane l copies block l >> 3 of rows
+// (l & 7) and (l & 7) + 8, lanes 0..15 the scales of row l.
+struct Ring {
+    int wp, nmat;          // matrix of the next unit to issue; nmat = end of the step
+    int u, u_end;          // unit (within the warp's range of that matrix) and range end
+    int k, nst, tile;      // 4-block group inside the tile, groups per tile, tile
+    const uint8_t* a;      // this lane's copy sources at group 0 of the tile
+    const uint8_t* b;
+    const __half* s;
+    unsigned int issued, consumed;   // ring slot = count % kStages
+    uint32_t base;         // shared-memory address of this warp's ring
+};
+
+__device__ __forceinline__ void ring_set_tile(Ring& r, const PMat& M, int lane) {
+    bool ok;
+    const int lr = lane & 7, lb = lane >> 3;
+    const int ra = tile_row(M, r.tile, lr, ok), rb = tile_row(M, r.tile, lr + 8, ok);
+    const int rs = tile_row(M, r.tile, lane & 15, ok);
+    r.a = M.quants + ((size_t)ra * M.nblk + lb) * 16;
+    r.b = M.quants + ((size_t)rb * M.nblk + lb) * 16;
+    r.s = M.scales + (size_t)rs * M.nblk;
+}
+
+// Move to the first matrix at or after r.wp in which this warp has units.
+__device__ __forceinline__ void ring_seek(Ring& r, const PersistParams& p, int warp, int lane) {
+    for (; r.wp < r.nmat; ++r.wp) {
+        const PMat M = mat_at(p, r.wp);
+        int t0, t1;
+        cta_tiles(M.ntile, t0, t1);
+        const int nst = M.nblk / kUnitBlocks;
+        const int U = (t1 - t0) * nst;
+        const int u0 = warp_unit(U, warp), u1 = warp_unit(U, warp + 1);
+        if (u1 > u0) {
+            r.u = u0;
+            r.u_end = u1;
+            r.nst = nst;
+            r.tile = t0 + u0 / nst;
+            r.k = u0 % nst;
+            ring_set_tile(r, M, lane);
+            return;
+        }
+    }
+}
+
+// Copy the next unit into its ring slot (one commit group per call, empty past the end).
+__device__ __forceinline__ void ring_issue(Ring& r, const PersistParams& p, int warp, int lane) {
+    if (r.wp < r.nmat) {
+        const uint32_t st = r.base + (r.issued % kStages) * kUnitBytes;
+        const uint32_t dA = (uint32_t)(((lane >> 3) * 16 + (lane & 7)) * 16);
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(st + dA), "l"(r.a + r.k * 64) : "memory");
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(st + dA + 128), "l"(r.b + r.k * 64)
+                     : "memory");
+        if (lane < 16)
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(st + 1024 + lane * 8),
+                         "l"(r.s + r.k * kUnitBlocks) : "memory");
+        if (++r.u == r.u_end) {
+            ++r.wp;
+            ring_seek(r, p, warp, lane);
+        } else if (++r.k == r.nst) {
+            r.k = 0;
+            ++r.tile;
+            ring_set_tile(r, mat_at(p, r.wp), lane);
+        }
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    ++r.issued;
+}
+
+// ------------------------------------------------------------------------------ GEMV phase
+// Stage the activations of all B columns: per column and block j, 4 chunks of 16 bytes (chunk t
+// feeds MMA lane t: f16 pairs (x0, x2), (x1, x3), (x16, x18)/16, (x17, x19)/16 of elements
+// 32 j + 4 t + ...), plus the accumulator start -(1032 sum x_lo + 1152 sum x_hi/16) of every
+// (block, column). RMS: the input is the f32 residual stream, normalised (RMSNorm with weight
+// w) on the way; its first two items per thread stay in registers between the two passes.
+// Data written earlier in the launch by other CTAs is read with ld.global.cg (L2).
+template <bool RMS>
+__device__ __noinline__ void stage_x(const PersistParams& p, int nblk, int cstride, const float* xf,
+                                     const __half* x16, const float* w, uint4* xs, float* bias, float* red) {
+    constexpr int kHeld = 2;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int B = p.B, cols = nblk * 32, nitems = B * nblk * 4;
+    if (B < 2)
+        for (int j = tid; j < nblk; j += kT) bias[2 * j + 1] = 0.f;   // absent second column
+
+    auto load = [&](int item, float (&v)[8]) {
+        const int t = item & 3, bj = item >> 2, b = bj / nblk, j = bj - b * nblk;
+        const size_t off = (size_t)b * cols + 32 * j + 4 * t;
+        if (RMS) {
+            const float4 a = __ldcg(reinterpret_cast<const float4*>(xf + off));
+            const float4 h = __ldcg(reinterpret_cast<const float4*>(xf + off + 16));
+            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+            v[4] = h.x; v[5] = h.y; v[6] = h.z; v[7] = h.w;
+        } else {
+            const uint2 a = __ldcg(reinterpret_cast<const uint2*>(x16 + off));
+            const uint2 h = __ldcg(reinterpret_cast<const uint2*>(x16 + off + 16));
+            const float2 f0 = __half22float2(as_h2(a.x)), f1 = __half22float2(as_h2(a.y));
+            const float2 f2 = __half22float2(as_h2(h.x)), f3 = __half22float2(as_h2(h.y));
+            v[0] = f0.x; v[1] = f0.y; v[2] = f1.x; v[3] = f1.y;
+            v[4] = f2.x; v[5] = f2.y; v[6] = f3.x; v[7] = f3.y;
+        }
+    };
+
+    float held[kHeld][8];
+    float rs0 = 1.f, rs1 = 1.f;
+    if (RMS) {
+        float ss0 = 0.f, ss1 = 0.f;
+#pragma unroll
+        for (int r = 0; r < kHeld; ++r) {
+            const int item = tid + r * kT;
+            if (item < nitems) {
+                load(item, held[r]);
+                float s = 0.f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) s += held[r][i] * held[r][i];
+                if (item < nblk * 4) ss0 += s; else ss1 += s;
+            }
+        }
+        for (int item = tid + kHeld * kT; item < nitems; item += kT) {
+            float v[8];
+            load(item, v);
+            float s = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) s += v[i] * v[i];
+            if (item < nblk * 4) ss0 += s; else ss1 += s;
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            ss0 += __shfl_xor_sync(0xffffffffu, ss0, o);
+            ss1 += __shfl_xor_sync(0xffffffffu, ss1, o);
+        }
+        if (lane == 0) {
+            red[warp * 2] = ss0;
+            red[warp * 2 + 1] = ss1;
+        }
+        __syncthreads();
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int i = 0; i < kW; ++i) {
+            a0 += red[i * 2];
+            a1 += red[i * 2 + 1];
+        }
+        rs0 = 1.0f / sqrtf(a0 / (float)cols + p.eps);
+        rs1 = 1.0f / sqrtf(a1 / (float)cols + p.eps);
+    }
+
+    // item -> staged chunk and (t == 0) the block's offset term; whole warps run together
+    // (the loop bound is warp-uniform) because of the shuffles
+    auto emit = [&](int item, float (&v)[8]) {
+        const int t = item & 3, bj = item >> 2, b = bj / nblk, j = bj - b * nblk;
+        const bool live = item < nitems;
+        if (RMS && live) {
+            const float rr = b == 0 ? rs0 : rs1;
+            const float4 wa = __ldg(reinterpret_cast<const float4*>(w + 32 * j + 4 * t));
+            const float4 wh = __ldg(reinterpret_cast<const float4*>(w + 32 * j + 16 + 4 * t));
+            v[0] *= rr * wa.x; v[1] *= rr * wa.y; v[2] *= rr * wa.z; v[3] *= rr * wa.w;
+            v[4] *= rr * wh.x; v[5] *= rr * wh.y; v[6] *= rr * wh.z; v[7] *= rr * wh.w;
+        }
+        if (!live) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = 0.f;
+        }
+        const __half2 p0 = __floats2half2_rn(v[0], v[2]);
+        const __half2 p1 = __floats2half2_rn(v[1], v[3]);
+        const __half2 p2 = __floats2half2_rn(__half2float(__float2half_rn(v[4])) * 0.0625f,
+                                             __half2float(__float2half_rn(v[6])) * 0.0625f);
+        const __half2 p3 = __floats2half2_rn(__half2float(__float2half_rn(v[5])) * 0.0625f,
+                                             __half2float(__float2half_rn(v[7])) * 0.0625f);
+        const float2 f0 = __half22float2(p0), f1 = __half22float2(p1);
+        const float2 f2 = __half22float2(p2), f3 = __half22float2(p3);
+        // sum (1024 + q) x_lo + (1024 + 16 q) x_hi/16 = sum (q - 8) x + 1032 sum x_lo + 1152 sum x_hi/16
+        float part = 1032.0f * ((f0.x + f0.y) + (f1.x + f1.y)) + 1152.0f * ((f2.x + f2.y) + (f3.x + f3.y));
+        part += __shfl_xor_sync(0xffffffffu, part, 1);
+        part += __shfl_xor_sync(0xffffffffu, part, 2);
+        if (live) {
+            xs[(size_t)b * cstride + 4 * j + t] = make_uint4(as_u32(p0), as_u32(p1), as_u32(p2), as_u32(p3));
+            if (t == 0) bias[2 * j + b] = -part;
+        }
+    };
+#pragma unroll
+    for (int r = 0; r < kHeld; ++r) {
+        const int base = r * kT;
+        if (base < nitems) {
+            float v[8];
+            if (RMS) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[i] = held[r][i];
+            } else if (base + tid < nitems) {
+                load(base + tid, v);
+            }
+            emit(base + tid, v);
+        }
+    }
+    for (int base = kHeld * kT; base < nitems; base += kT) {
+        float v[8];
+        if (base + tid < nitems) load(base + tid, v);
+        emit(base + tid, v);
+    }
+}
+
+// Epilogue of one finished 16-row tile for this lane's fragment: rows g, g + 8 and columns
+// 2t, 2t + 1 (SiLU*up: acc[0..1] = gate row i, acc[2..3] = up row i, i = 8 tile + g).
+template <int EPI>
+__device__ __forceinline__ void finish_tile(const PersistParams& p, const PMat& M, int tile, const float (&acc)[4],
+                                            void* y, int ld, unsigned long long& best0, unsigned long long& best1,
+                                            int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    const int n0 = 2 * t, n1 = n0 + 1;
+    if (EPI == kEpiSilu) {
+        const int i = tile * 8 + g;
+        if (i < (M.rows >> 1)) {
+            __half* act = static_cast<__half*>(y);
+            if (n0 < p.B) act[(size_t)n0 * ld + i] = __float2half_rn(silu(acc[0]) * acc[2]);
+            if (n1 < p.B) act[(size_t)n1 * ld + i] = __float2half_rn(silu(acc[1]) * acc[3]);
+        }
+        return;
+    }
+    float* yf = static_cast<float*>(y);
+    const int ra = tile * 16 + g, rb = ra + 8;
+    auto put = [&](int n, int row, float v, unsigned long long& best) {
+        float* dst = yf + (size_t)n * ld + row;
+        if (EPI == kEpiResid) {
+            *dst = __ldcg(dst) + v;
+        } else {
+            *dst = v;
+            if (EPI == kEpiLogits) {
+                const unsigned long long key = argmax_key(v, row);
+                best = key > best ? key : best;
+            }
+        }
+    };
+    if (n0 < p.B) {
+        if (ra < M.rows) put(n0, ra, acc[0], best0);
+        if (rb < M.rows) put(n0, rb, acc[2], best0);
+    }
+    if (n1 < p.B) {
+        if (ra < M.rows) put(n1, ra, acc[1], best1);
+        if (rb < M.rows) put(n1, rb, acc[3], best1);
+    }
+}
+
+// One GEMV phase of the step: y = epilogue(W x) for this CTA's tiles of M. All threads of the
+// CTA call it. The warp consumes its units from the ring (issuing one unit further for each
+// one consumed), in the order the issue side produced them.
+template <int EPI, bool RMS>
+__device__ __noinline__ void gemv_phase(const PersistParams& p, const PMat M, Ring& ring, const float* xf,
+                                        const __half* x16, const float* norm_w, void* y, int ld,
+                                        unsigned char* region, float* red,
+                                        unsigned long long (*kred)[kMaxB]) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const int cstride = p.max_nblk * 4 + 4;   // uint4 units between staged columns (+64 B)
+    uint4* xs = reinterpret_cast<uint4*>(region);
+    float* bias = reinterpret_cast<float*>(xs + (size_t)p.B * cstride);   // [nblk][2]
+    float4* part = reinterpret_cast<float4*>(bias + 2 * p.max_nblk);    // [kW][2][32]
+
+    stage_x<RMS>(p, M.nblk, cstride, xf, x16, norm_w, xs, bias, red);
+    __syncthreads();
+
+    Ring r = ring;   // a register copy for the loop; written back at the end
+    const int nst = M.nblk / kUnitBlocks;
+    int T0, T1;
+    cta_tiles(M.ntile, T0, T1);
+    const int U = (T1 - T0) * nst;
+    const int u0 = warp_unit(U, warp), u1 = warp_unit(U, warp + 1);
+    const bool has_col = g < p.B;
+    const uint4* xcol = xs + (size_t)(has_col ? g : 0) * cstride;
+    // ldmatrix row address of this lane: matrix m = lane >> 3 -> (block m >> 1, rows (m & 1) * 8 + r)
+    const int lm = lane >> 3, lrow = lane & 7;
+    const uint32_t a_lo = (uint32_t)(((lm >> 1) * 16 + (lm & 1) * 8 + lrow) * 16);
+    const unsigned char* ring_g = reinterpret_cast<const unsigned char*>(region) - kRingBytes +
+                                  (size_t)warp * kStages * kUnitBytes;
+
+    unsigned long long best0 = 0ull, best1 = 0ull;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    int tile = T0 + (u1 > u0 ? u0 / nst : 0), k = u1 > u0 ? u0 % nst : 0;
+    const int first_tile = tile;
+#pragma unroll 1
+    for (int u = u0; u < u1; ++u) {
+        asm volatile("cp.async.wait_group %0;" ::"n"(kStages - 1) : "memory");
+        __syncwarp();
+        const unsigned int slot = r.consumed % kStages;
+        const uint32_t st = r.base + slot * kUnitBytes;
+        uint32_t w[8];   // rows g / g + 8 of blocks 0..3: wa0, wb0, wa1, wb1, ...
+        ldsm_x4(st + a_lo, w[0], w[1], w[2], w[3]);
+        ldsm_x4(st + a_lo + 2 * 16 * 16, w[4], w[5], w[6], w[7]);
+        const unsigned char* stg = ring_g + (size_t)slot * kUnitBytes;
+        const uint2 sca = *reinterpret_cast<const uint2*>(stg + 1024 + g * 8);
+        const uint2 scb = *reinterpret_cast<const uint2*>(stg + 1024 + (g + 8) * 8);
+        __syncwarp();
+        ++r.consumed;
+        ring_issue(r, p, warp, lane);   // refill the slot just read
+        const float2 da01 = __half22float2(as_h2(sca.x)), da23 = __half22float2(as_h2(sca.y));
+        const float2 db01 = __half22float2(as_h2(scb.x)), db23 = __half22float2(as_h2(scb.y));
+        const float da[4] = {da01.x, da01.y, da23.x, da23.y};
+        const float db[4] = {db01.x, db01.y, db23.x, db23.y};
+#pragma unroll
+        for (int q = 0; q < kUnitBlocks; ++q) {
+            const int j = k * kUnitBlocks + q;
+            const uint32_t wa = w[2 * q], wb = w[2 * q + 1];
+            const uint4 X = has_col ? xcol[4 * j + t] : make_uint4(0u, 0u, 0u, 0u);
+            const float2 bz = t == 0 ? *reinterpret_cast<const float2*>(bias + 2 * j) : make_float2(0.f, 0.f);
+            float c[4] = {bz.x, bz.y, bz.x, bz.y};
+            const uint32_t sa8 = wa >> 8, sb8 = wb >> 8;
+            mma16816(c, (wa & 0x000F000Fu) | 0x64006400u, (wb & 0x000F000Fu) | 0x64006400u,
+                     (sa8 & 0x000F000Fu) | 0x64006400u, (sb8 & 0x000F000Fu) | 0x64006400u, X.x, X.y);
+            mma16816(c, (wa & 0x00F000F0u) | 0x64006400u, (wb & 0x00F000F0u) | 0x64006400u,
+                     (sa8 & 0x00F000F0u) | 0x64006400u, (sb8 & 0x00F000F0u) | 0x64006400u, X.z, X.w);
+            acc[0] = fmaf(da[q], c[0], acc[0]);
+            acc[1] = fmaf(da[q], c[1], acc[1]);
+            acc[2] = fmaf(db[q], c[2], acc[2]);
+            acc[3] = fmaf(db[q], c[3], acc[3]);
+        }
+        if (++k == nst || u + 1 == u1) {
+            // end of this warp's part of a tile: finish it if the warp covered all of it, else
+            // park the partial (slot 0: the warp's first tile, slot 1: its last)
+            const int ts = (tile - T0) * nst;
+            if (u0 <= ts && u + 1 == ts + nst)
+                finish_tile<EPI>(p, M, tile, acc, y, ld, best0, best1, lane);
+            else
+                part[(warp * 2 + (tile == first_tile ? 0 : 1)) * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+            k = 0;
+            ++tile;
+        }
+    }
+    ring = r;
+    __syncthreads();
+    // A tile shared by several warps is finished by the warp holding its last unit: the partials
+    // of every warp that touched it, summed in warp order.
+    if (u1 > u0) {
+        const int ts = (first_tile - T0) * nst;
+        if (u0 > ts && u1 >= ts + nst) {
+            float s[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int w2 = 0; w2 <= warp; ++w2) {
+                const int a0 = warp_unit(U, w2), a1 = warp_unit(U, w2 + 1);
+                if (a1 <= a0 || a1 <= ts || a0 >= ts + nst) continue;
+                const int sl = (T0 + a0 / nst == first_tile) ? 0 : 1;
+                const float4 v = part[(w2 * 2 + sl) * 32 + lane];
+                s[0] += v.x;
+                s[1] += v.y;
+                s[2] += v.z;
+                s[3] += v.w;
+            }
+            finish_tile<EPI>(p, M, first_tile, s, y, ld, best0, best1, lane);
+        }
+    }
+    if (EPI == kEpiLogits) {
+        // lane t = 0 holds columns 0 and 1: reduce over the 8 row groups, then over the warps
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            const unsigned long long k0 = __shfl_xor_sync(0xffffffffu, best0, o);
+            const unsigned long long k1 = __shfl_xor_sync(0xffffffffu, best1, o);
+            best0 = k0 > best0 ? k0 : best0;
+            best1 = k1 > best1 ? k1 : best1;
+        }
+        if (lane == 0) {
+            kred[warp][0] = best0;
+            kred[warp][1] = best1;
+        }
+        __syncthreads();
+        if (tid < p.B) {
+            unsigned long long m = 0ull;
+#pragma unroll
+            for (int i = 0; i < kW; ++i) m = kred[i][tid] > m ? kred[i][tid] : m;
+            const bool act = p.active == nullptr || p.active[tid] != 0;
+            if (m && act) atomicMax(p.keys + tid, m);
+        }
+    }
+}
+
+// ------------------------------------------------------------------------------ attention
+// RMSNorm over one head (weight w) and NeoX rotation with the table rows of the position, by
+// one warp: lane handles the pairs (i, i + HD/2), i = lane, lane + 32, ...; writes f16 to dst.
+template <int HD>
+__device__ __forceinline__ void norm_rope(const float* src, const float* w, const float* cr, const float* sr,
+                                          float eps, __half* dst, int lane) {
+    constexpr int H2 = HD / 2, PER = H2 / 32;
+    float xa[PER], xb[PER];
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+        xa[k] = __ldcg(src + lane + 32 * k);
+        xb[k] = __ldcg(src + lane + 32 * k + H2);
+        ss += xa[k] * xa[k] + xb[k] * xb[k];
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float r = 1.0f / sqrtf(ss / (float)HD + eps);
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+        const int i = lane + 32 * k;
+        const float a = xa[k] * r * w[i], bb = xb[k] * r * w[i + H2];
+        const float c = cr[i], sn = sr[i];
+        dst[i] = __float2half_rn(a * c - bb * sn);
+        dst[i + H2] = __float2half_rn(a * sn + bb * c);
+    }
+}
+
+template <int DPL> struct VRow;
+template <> struct VRow<2> {
+    using T = unsigned int;
+    static __device__ __forceinline__ void f(T u, float (&v)[2]) {
+        const float2 a = __half22float2(as_h2(u));
+        v[0] = a.x; v[1] = a.y;
+    }
+};
+template <> struct VRow<4> {
+    using T = uint2;
+    static __device__ __forceinline__ void f(T u, float (&v)[4]) {
+        const float2 a = __half22float2(as_h2(u.x)), b = __half22float2(as_h2(u.y));
+        v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+    }
+};
+
+// Attention of one layer for every (sequence, kv head, split) item; item i runs on CTA
+// i mod gridDim.x. Splits: the sequence's blocks are cut into nsplit ranges of spb blocks; the
+// range holding the newest position also normalises, rotates and appends the new K/V first.
+template <int HD, int G>
+__device__ __noinline__ void attn_phase(const PersistParams& p, int layer, unsigned char* region,
+                                        __half (*qs)[HD], int* flag) {
+    constexpr int NCH = HD / 32;   // 32-dim chunks of a K row (one 16-byte load per lane each)
+    constexpr int DPL = HD / 32;   // P.V output dims per lane
+    constexpr int WST = G * HD > 128 ? G * HD : 128;   // floats per warp in the merge buffer
+    using VT = typename VRow<DPL>::T;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    float* wacc = reinterpret_cast<float*>(region);   // [kW][WST] (first [G][16]: probabilities)
+    float* wm = wacc + kW * WST;                        // [kW][G]
+    float* wl = wm + kW * G;
+    const PLayer& Ly = p.layers[layer];
+    const size_t lp = (size_t)layer * p.layer_pool;
+    __half* kpool = p.k_pool + lp;
+    __half* vpool = p.v_pool + lp;
+    const int nitems = p.B * p.nkv * p.nsplit;
+    const size_t qkv_ld = (size_t)(p.nh + 2 * p.nkv) * HD;
+
+    for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
+        const int s = item % p.nsplit, bk = item / p.nsplit, kvh = bk % p.nkv, b = bk / p.nkv;
+        if (p.active && p.active[b] == 0) continue;
+        const int pos = p.positions[b];
+        const int L = pos + 1;
+        if (pos < 0 || L > p.maxb * kBS || pos >= p.max_position) {
+            if (s == 0 && kvh == 0 && tid == 0) record_device_error(p.err, kErrAttnLength, b, L);
+            continue;
+        }
+        const int nblocks = (L + kBS - 1) / kBS;
+        const int spb = (nblocks + p.nsplit - 1) / p.nsplit;
+        const int n_active = (nblocks + spb - 1) / spb;
+        if (s >= n_active) continue;
+        const int blk0 = s * spb, blk1 = min(nblocks, blk0 + spb);
+        __syncthreads();   // the previous item's readers of qs and the merge buffers are done
+
+        const float* src = p.qkv + (size_t)b * qkv_ld;
+        const float* cr = p.cos_t + (size_t)pos * (HD / 2);
+        const float* sr = p.sin_t + (size_t)pos * (HD / 2);
+        if (warp < G) norm_rope<HD>(src + (size_t)(kvh * G + warp) * HD, Ly.q_norm, cr, sr, p.eps, qs[warp], lane);
+        const int lblk = pos / kBS;
+        if (lblk >= blk0 && lblk < blk1 && warp >= kW - 2) {
+            const int phys = p.block_tables[(size_t)b * p.maxb + lblk];
+            if (phys < 0 || phys >= p.num_blocks) {
+                if (lane == 0 && warp == kW - 1)
+                    record_device_error(p.err, kErrRopeBlock, (long long)b * p.maxb + lblk, phys);
+            } else {
+                const size_t off = (((size_t)phys * p.nkv + kvh) * kBS + (pos % kBS)) * HD;
+                if (warp == kW - 1) {
+                    norm_rope<HD>(src + (size_t)(p.nh + kvh) * HD, Ly.k_norm, cr, sr, p.eps, kpool + off, lane);
+                } else {
+                    const float* vs = src + (size_t)(p.nh + p.nkv + kvh) * HD;
+                    for (int i = lane; i < HD; i += 32) vpool[off + i] = __float2half_rn(__ldcg(vs + i));
+                }
+            }
+        }
+        __threadfence();
+        __syncthreads();
+
+        // Q as the A operand of S = Q K^T (rows = the G heads, rows >= G zero). head_dim is
+        // permuted: in k-steps 2m, 2m + 1 lane t holds dims 32 m + 8 t + {0,1 | 2,3} and
+        // {4,5 | 6,7}, so both Q and K fragments come from one 16-byte load per chunk.
+        uint4 qf[NCH];
+#pragma unroll
+        for (int m = 0; m < NCH; ++m)
+            qf[m] = g < G ? *reinterpret_cast<const uint4*>(&qs[g][32 * m + 8 * t]) : make_uint4(0u, 0u, 0u, 0u);
+        float o[G][DPL];
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int d = 0; d < DPL; ++d) o[h][d] = 0.f;
+        float mrun = -INFINITY, lrun = 0.f;   // running max / sum of head g (lanes g < G)
+        float* pb = wacc + warp * WST;
+        const int32_t* bt = p.block_tables + (size_t)b * p.maxb;
+        bool any = false;
+        for (int blk = blk0 + warp; blk < blk1; blk += kW) {
+            const int phys = bt[blk];
+            if (phys < 0 || phys >= p.num_blocks) {
+                if (lane == 0) record_device_error(p.err, kErrAttnBlock, (long long)b * p.maxb + blk, phys);
+                continue;
+            }
+            any = true;
+            const __half* kb = kpool + ((size_t)phys * p.nkv + kvh) * kBS * HD;
+            const __half* vb = vpool + ((size_t)phys * p.nkv + kvh) * kBS * HD;
+            const int nt = min(kBS, L - blk * kBS);   // valid keys of the block
+            uint4 k0[NCH], k1[NCH];
+#pragma unroll
+            for (int m = 0; m < NCH; ++m) {
+                k0[m] = __ldcg(reinterpret_cast<const uint4*>(kb + (size_t)g * HD + 32 * m + 8 * t));
+                k1[m] = __ldcg(reinterpret_cast<const uint4*>(kb + (size_t)(g + 8) * HD + 32 * m + 8 * t));
+            }
+            VT vv[kBS];
+#pragma unroll
+            for (int kk = 0; kk < kBS; ++kk)
+                if (kk < nt) vv[kk] = __ldcg(reinterpret_cast<const VT*>(vb + (size_t)kk * HD + lane * DPL));
+            float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int m = 0; m < NCH; ++m) {
+                mma16816(s0, qf[m].x, 0u, qf[m].y, 0u, k0[m].x, k0[m].y);
+                mma16816(s0, qf[m].z, 0u, qf[m].w, 0u, k0[m].z, k0[m].w);
+                mma16816(s1, qf[m].x, 0u, qf[m].y, 0u, k1[m].x, k1[m].y);
+                mma16816(s1, qf[m].z, 0u, qf[m].w, 0u, k1[m].z, k1[m].w);
+            }
+            // online softmax of head row g over keys 2t, 2t + 1, 2t + 8, 2t + 9 (exp2 domain);
+            // keys past the context are excluded by selection (their K rows may be garbage)
+            const int c0 = 2 * t;
+            const float x0 = c0 < nt ? s0[0] * p.scale_log2 : -INFINITY;
+            const float x1 = c0 + 1 < nt ? s0[1] * p.scale_log2 : -INFINITY;
+            const float x2 = c0 + 8 < nt ? s1[0] * p.scale_log2 : -INFINITY;
+            const float x3 = c0 + 9 < nt ? s1[1] * p.scale_log2 : -INFINITY;
+            float mb = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+            mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+            mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+            const float mn = fmaxf(mrun, mb);   // finite: key 0 of the block is valid
+            const float alpha = exp2f(mrun - mn);
+            const float e0 = exp2f(x0 - mn), e1 = exp2f(x1 - mn), e2 = exp2f(x2 - mn), e3 = exp2f(x3 - mn);
+            float ls = (e0 + e1) + (e2 + e3);
+            ls += __shfl_xor_sync(0xffffffffu, ls, 1);
+            ls += __shfl_xor_sync(0xffffffffu, ls, 2);
+            lrun = lrun * alpha + ls;
+            mrun = mn;
+            if (g < G) {
+                pb[g * 16 + c0] = e0;
+                pb[g * 16 + c0 + 1] = e1;
+                pb[g * 16 + c0 + 8] = e2;
+                pb[g * 16 + c0 + 9] = e3;
+            }
+            __syncwarp();
+            // O = alpha O + P V: lane owns dims DPL * lane .. + DPL - 1 of every head
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float ah = __shfl_sync(0xffffffffu, alpha, 4 * h);
+#pragma unroll
+                for (int d = 0; d < DPL; ++d) o[h][d] *= ah;
+            }
+#pragma unroll
+            for (int kk = 0; kk < kBS; ++kk) {
+                if (kk < nt) {
+                    float v[DPL];
+                    VRow<DPL>::f(vv[kk], v);
+#pragma unroll
+                    for (int h = 0; h < G; ++h) {
+                        const float pv = pb[h * 16 + kk];
+#pragma unroll
+                        for (int d = 0; d < DPL; ++d) o[h][d] = fmaf(pv, v[d], o[h][d]);
+                    }
+                }
+            }
+            __syncwarp();
+        }
+        // this warp's state: lane 4h holds (m, l) of head h; every lane its dims of every head
+        if (any) {
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+#pragma unroll
+                for (int d = 0; d < DPL; ++d) pb[h * HD + DPL * lane + d] = o[h][d];
+            if (t == 0 && g < G) {
+                wm[warp * G + g] = mrun;
+                wl[warp * G + g] = lrun;
+            }
+        } else if (lane < G) {
+            wm[warp * G + lane] = -INFINITY;
+            wl[warp * G + lane] = 0.f;
+        }
+        __syncthreads();
+        for (int i = tid; i < G * HD; i += kT) {
+            const int h = i / HD, d = i - h * HD;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kW; ++w) M = fmaxf(M, wm[w * G + h]);
+            float Ls = 0.f, A = 0.f;
+#pragma unroll
+            for (int w = 0; w < kW; ++w) {
+                const float mw = wm[w * G + h];
+                if (mw != -INFINITY) {
+                    const float f = exp2f(mw - M);
+                    Ls += wl[w * G + h] * f;
+                    A += wacc[w * WST + h * HD + d] * f;
+                }
+            }
+            const int hg = kvh * G + h;
+            if (n_active == 1) {
+                p.attn[((size_t)b * p.nh + hg) * HD + d] = __float2half_rn(A / Ls);
+            } else {
+                const size_t slot = ((size_t)b * p.nh + hg) * p.nsplit + s;
+                p.pacc[slot * HD + d] = A;
+                if (d == 0) {
+                    p.pm[slot] = M;
+                    p.pl[slot] = Ls;
+                }
+            }
+        }
+        if (n_active == 1) continue;
+
+        // split merge in the CTA that arrives last (no waiting)
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) *flag = atomicAdd(p.tickets + b * p.nkv + kvh, 1) == n_active - 1;
+        __syncthreads();
+        if (!*flag) continue;
+        __threadfence();
+        float* sw = wacc;   // [G][kMaxSplit] weights exp2(m_k - M) / L
+        for (int h = warp; h < G; h += kW) {
+            const size_t base = ((size_t)b * p.nh + kvh * G + h) * p.nsplit;
+            float M = -INFINITY;
+            for (int k = lane; k < n_active; k += 32) M = fmaxf(M, __ldcg(p.pm + base + k));
+#pragma unroll
+            for (int o2 = 16; o2; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
+            float Ls = 0.f;
+            for (int k = lane; k < n_active; k += 32) {
+                const float f = exp2f(__ldcg(p.pm + base + k) - M);
+                sw[h * kMaxSplit + k] = f;
+                Ls += f * __ldcg(p.pl + base + k);
+            }
+#pragma unroll
+            for (int o2 = 16; o2; o2 >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o2);
+            const float inv = 1.0f / Ls;
+            __syncwarp();
+            for (int k = lane; k < n_active; k += 32) sw[h * kMaxSplit + k] *= inv;
+        }
+        __syncthreads();
+        for (int i = tid; i < G * HD / 4; i += kT) {
+            const int h = i / (HD / 4), d4 = i - h * (HD / 4);
+            const size_t base = ((size_t)b * p.nh + kvh * G + h) * p.nsplit;
+            const float4* srcp = reinterpret_cast<const float4*>(p.pacc) + base * (HD / 4) + d4;
+            float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+            int k = 0;
+            for (; k + 4 <= n_active; k += 4) {
+                float4 v[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) v[u] = __ldcg(srcp + (size_t)(k + u) * (HD / 4));
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float wgt = sw[h * kMaxSplit + k + u];
+                    A.x = fmaf(wgt, v[u].x, A.x); A.y = fmaf(wgt, v[u].y, A.y);
+                    A.z = fmaf(wgt, v[u].z, A.z); A.w = fmaf(wgt, v[u].w, A.w);
+                }
+            }
+            for (; k < n_active; ++k) {
+                const float4 v = __ldcg(srcp + (size_t)k * (HD / 4));
+                const float wgt = sw[h * kMaxSplit + k];
+                A.x = fmaf(wgt, v.x, A.x); A.y = fmaf(wgt, v.y, A.y);
+                A.z = fmaf(wgt, v.z, A.z); A.w = fmaf(wgt, v.w, A.w);
+            }
+            __half* out = p.attn + ((size_t)b * p.nh + kvh * G + h) * HD + d4 * 4;
+            *reinterpret_cast<__half2*>(out) = __floats2half2_rn(A.x, A.y);
+            *reinterpret_cast<__half2*>(out + 2) = __floats2half2_rn(A.z, A.w);
+        }
+        if (tid == 0) p.tickets[b * p.nkv + kvh] = 0;   // re-arm for the next layer / step
+    }
+}
+
+// ------------------------------------------------------------------------------ the step
+// x[b] = E[token[b]] (f32 residual stream), split evenly over the CTAs.
+static __device__ void embed_phase(const PersistParams& p) {
+    const int n4 = p.hidden / 4;
+    const long long total = (long long)p.B * n4;
+    const long long i0 = (long long)blockIdx.x * total / gridDim.x;
+    const long long i1 = (long long)(blockIdx.x + 1) * total / gridDim.x;
+    for (long long i = i0 + threadIdx.x; i < i1; i += kT) {
+        const int b = (int)(i / n4), c = (int)(i - (long long)b * n4);
+        int tok = p.tokens[b];
+        if (tok < 0 || tok >= p.vocab) {
+            if (c == 0 && (p.active == nullptr || p.active[b] != 0))
+                record_device_error(p.err, kErrEmbedToken, b, tok);
+            tok = 0;
+        }
+        reinterpret_cast<float4*>(p.x)[i] = __ldg(reinterpret_cast<const float4*>(p.embed + (size_t)tok * p.hidden) + c);
+    }
+}
+
+// Next token (argmax key), position + 1, keys re-armed; CTA 0 after the last barrier.
+static __device__ void finalize(const PersistParams& p) {
+    const int b = threadIdx.x;
+    if (b >= p.B) return;
+    const unsigned long long k = atomicExch(p.keys + b, 0ull);
+    if (p.active && p.active[b] == 0) return;
+    const int tok = (int)(0xFFFFFFFFu - (uint32_t)(k & 0xFFFFFFFFull));
+    const int pos = p.positions[b];
+    p.next_tokens[b] = tok;
+    if (p.out_tokens && pos + 1 >= 0 && pos + 1 < p.out_stride)
+        p.out_tokens[(size_t)b * p.out_stride + pos + 1] = tok;
+    p.positions[b] = pos + 1;
+}
+
+template <int HD, int G>
+__device__ void step_body(const PersistParams& p, Ring& r, unsigned char* region, __half (*qs)[HD], float* red,
+                          unsigned long long (*kred)[kMaxB], int* flag) {
+    unsigned int target = 0;
+    embed_phase(p);
+    if (!grid_barrier(p, target, flag)) return;
+    const int qkv_ld = (p.nh + 2 * p.nkv) * HD;
+    for (int l = 0; l < p.n_layers; ++l) {
+        const PLayer* Ly = p.layers + l;
+        // q|k|v = W_qkv rmsnorm(x, attn_norm)
+        gemv_phase<kEpiF32, true>(p, Ly->m[0], r, p.x, nullptr, Ly->attn_norm, p.qkv, qkv_ld, region, red, kred);
+        if (!grid_barrier(p, target, flag)) return;
+        // qk-norm + RoPE + KV append + paged attention -> attn
+        attn_phase<HD, G>(p, l, region, qs, flag);
+        if (!grid_barrier(p, target, flag)) return;
+        // x += W_o attn
+        gemv_phase<kEpiResid, false>(p, Ly->m[1], r, nullptr, p.attn, nullptr, p.x, p.hidden, region, red, kred);
+        if (!grid_barrier(p, target, flag)) return;
+        // act = silu(gate) * up, [gate | up] = W_gu rmsnorm(x, ffn_norm)
+        gemv_phase<kEpiSilu, true>(p, Ly->m[2], r, p.x, nullptr, Ly->ffn_norm, p.act, p.inter, region, red, kred);
+        if (!grid_barrier(p, target, flag)) return;
+        // x += W_down act
+        gemv_phase<kEpiResid, false>(p, Ly->m[3], r, nullptr, p.act, nullptr, p.x, p.hidden, region, red, kred);
+        if (!grid_barrier(p, target, flag)) return;
+    }
+    // logits = W_lm rmsnorm(x, final_norm), greedy argmax keys
+    gemv_phase<kEpiLogits, true>(p, p.lm, r, p.x, nullptr, p.final_norm, p.logits, p.vocab, region, red, kred);
+    if (!grid_barrier(p, target, flag)) return;
+    if (blockIdx.x == 0) finalize(p);
+}
+
+template <int HD, int G>
+__global__ void __launch_bounds__(kT, 1) step_kernel(const __grid_constant__ PersistParams p) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ __align__(16) __half qs[G][HD];
+    __shared__ float red[kW * 2];
+    __shared__ unsigned long long kred[kW][kMaxB];
+    __shared__ int flag;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    Ring r;
+    r.wp = 0;
+    r.nmat = 4 * p.n_layers + 1;
+    r.issued = r.consumed = 0;
+    r.base = static_cast<uint32_t>(__cvta_generic_to_shared(smem)) + (uint32_t)(warp * kStages * kUnitBytes);
+    r.u = r.u_end = r.k = r.tile = 0;
+    r.nst = 1;
+    r.a = r.b = nullptr;
+    r.s = nullptr;
+    ring_seek(r, p, warp, lane);
+    // the weights do not depend on anything computed in the step: start streaming at once
+#pragma unroll 1
+    for (int i = 0; i < kStages; ++i) ring_issue(r, p, warp, lane);
+    step_body<HD, G>(p, r, smem + kRingBytes, qs, red, kred, &flag);
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    leave_step(p);
+}
+
+}  // namespace persist
+}  // namespace ql
+
+// ------------------------------------------------------------------------------ host side
+namespace ql {
+namespace persist {
+
+// Set the kernel's attributes and report its occupancy (launch == false), or launch it as a
+// cooperative grid of `grid` CTAs (launch == true).
+template <int HD, int G>
+cudaError_t run_one(bool launch, const PersistParams* p, size_t smem, int grid, cudaStream_t s, int* occ) {
+    if (!launch) {
+        // allow the device's whole opt-in shared memory (models of other shapes share the kernel),
+        // then check that `smem` bytes leave one CTA per SM
+        int dev = 0, optin = 0;
+        cudaFuncAttributes fa = {};
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, step_kernel<HD, G>);
+        if (e == cudaSuccess && smem + fa.sharedSizeBytes > (size_t)optin) {
+            *occ = 0;
+            return cudaSuccess;
+        }
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(step_kernel<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     optin - (int)fa.sharedSizeBytes);
+        if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, step_kernel<HD, G>, kT, smem);
+        return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kT);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, step_kernel<HD, G>, *p);
+}
+
+template <int HD>
+cudaError_t dispatch(int G, bool launch, const PersistParams* p, size_t smem, int grid, cudaStream_t s, int* occ) {
+    switch (G) {
+        case 1: return run_one<HD, 1>(launch, p, smem, grid, s, occ);
+        case 2: return run_one<HD, 2>(launch, p, smem, grid, s, occ);
+        case 4: return run_one<HD, 4>(launch, p, smem, grid, s, occ);
+        case 8: return run_one<HD, 8>(launch, p, smem, grid, s, occ);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace persist
+
+// One translation unit per head_dim (they compile in parallel).
+cudaError_t persist_dispatch_hd64(int G, bool launch, const PersistParams* p, size_t smem, int grid,
+                                  cudaStream_t s, int* occ);
+cudaError_t persist_dispatch_hd128(int G, bool launch, const PersistParams* p, size_t smem, int grid,
+                                   cudaStream_t s, int* occ);
+
+}  // namespace ql

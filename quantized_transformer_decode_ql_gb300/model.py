@@ -137,6 +137,12 @@ class DeviceModel:
         a.out_stride = out_tokens.shape[1] if out_tokens is not None else 0
         return a
 
+    def ql_model_set_option(self, option: int, value: int):
+        check(lib().ql_model_set_option(self.handle, option, value))
+
+    def ql_model_persistent_max_batch(self) -> int:
+        return int(lib().ql_model_persistent_max_batch(self.handle))
+
     def ql_decode_step(self, args: StepArgs, stream=None):
         check(lib().ql_decode_step(self.handle, ctypes.byref(args), stream_ptr(stream)))
 

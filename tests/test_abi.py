@@ -136,5 +136,7 @@ def test_argument_validation_without_gpu(ql):
                                 None) == ql.QL_EINVAL
     assert L.ql_model_create(None, None) == ql.QL_EINVAL
     assert L.ql_decode_graph_replay(None, 1, 1, None) == ql.QL_EINVAL
+    assert L.ql_model_set_option(None, ql.QL_OPT_STEP_KERNEL, ql.QL_STEP_AUTO) == ql.QL_EINVAL
+    assert L.ql_model_persistent_max_batch(None) == 0
     assert L.ql_block_pool_create(0, ctypes.byref(ctypes.c_void_p())) == ql.QL_EINVAL
     assert ql.ql_paged_attn_workspace_bytes(0, 4, 2, 64, 16, 4) == 0
