@@ -190,6 +190,8 @@ def gpu_arm(args, rank, world, local_rank):
     t_setup = time.time()
     gm = DeviceModel.from_layer_fn(cfg, device_tensor_fn(cfg, seed=0), num_blocks=num_blocks,
                                    max_batch=B, max_blocks_per_seq=maxb)
+    gm.ql_model_set_option(ql.QL_OPT_STEP_KERNEL, STEP_KERNELS[args.step_kernel])
+    persistent = args.step_kernel != "launches" and B <= gm.ql_model_persistent_max_batch()
     # fragmented block tables; pre-filled synthetic context of CTX positions N(0,1) f16 per slot
     perm = torch.from_numpy(ql_inputs.fragmented_block_ids(num_blocks, seed=5)).cuda()
     bt = perm[: B * maxb].reshape(B, maxb).contiguous()
@@ -242,6 +244,7 @@ def gpu_arm(args, rank, world, local_rank):
     ms_max = max_over_ranks(ms, world)
     gm.ql_check_device_error()
     toks = out_tokens.cpu().numpy()
+    phases = step_phases(gm, sargs, s, cfg) if persistent else None
 
     # ---- algorithmic bytes per step (weights + KV read/write + embedding row + logits)
     wbytes = gm.weight_bytes()
@@ -313,7 +316,7 @@ def gpu_arm(args, rank, world, local_rank):
     }
     gu_gbs = per_kernel["gemv_gate_up"]["achieved_gbs"]
     step_gbs = step_bytes * steps / (ms_max / 1e3) / 1e9
-    kernels_per_step = 2 + 6 * cfg.n_layers + 2
+    kernels_per_step = 1 if persistent else 3 + 5 * cfg.n_layers   # embed, 5 per layer, lm_head, finalize
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world,
         "steps": steps, "warmup": warmup, "ms_per_step": round(ms_max / steps, 4),
@@ -337,8 +340,66 @@ def gpu_arm(args, rank, world, local_rank):
         "gpu_launches": kernels_per_step * steps,
         "setup_s": round(setup_s, 1),
         "tokens_head": toks[0, CTX + 1: CTX + 9].tolist(),
+        "step_kernel": "persistent (one cooperative launch per step)" if persistent else "one launch per phase",
     }
+    if phases:
+        line["step_phases_us"] = phases
     return line
+
+
+STEP_KERNELS = {"auto": 0, "launches": 1, "persistent": 2}
+
+
+def gemv_passes(cols, batch):
+    """Launches of one q4_0 GEMV call: the batch goes in passes of as many columns as the
+    kernel's 100 KB activation staging holds (at most 8)."""
+    nblk = cols // 32
+    fixed = nblk * 8 * 4 + 8 * 32 * 16
+    nb_max = min(8, (100 * 1024 - fixed) // ((nblk * 4 + 4) * 16))
+    return -(-batch // nb_max)
+
+
+def launches_per_step(cfg, B):
+    """Kernel launches of one step in the one-launch-per-phase form."""
+    per_layer = (gemv_passes(cfg.hidden, B) * 2 + gemv_passes(cfg.n_heads * cfg.head_dim, B)
+                 + gemv_passes(cfg.intermediate, B) + 1)
+    return 2 + per_layer * cfg.n_layers + gemv_passes(cfg.hidden, B)
+
+
+def step_phases(gm, sargs, s, cfg):
+    """Per-phase times of the persistent step from its globaltimer trace (untimed eager steps
+    after the timed region): for each phase kind the mean over layers of the critical work time
+    (last CTA arriving at the phase's barrier minus the last CTA leaving the previous one) and of
+    the barrier time (last exit minus last arrival), plus the mean per-CTA work time."""
+    import numpy as np
+    import torch
+    import quantized_transformer_decode_ql_gb300 as ql
+    grid = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    rows = 3 + 5 * cfg.n_layers
+    buf = torch.zeros(rows * grid * 2, dtype=torch.int64, device="cuda")
+    gm.ql_model_set_option(ql.QL_OPT_STEP_TRACE, buf.data_ptr())
+    try:
+        for _ in range(3):
+            gm.ql_decode_step(sargs, s)
+        s.synchronize()
+    finally:
+        gm.ql_model_set_option(ql.QL_OPT_STEP_TRACE, 0)
+    gm.ql_check_device_error()
+    t = buf.cpu().numpy().reshape(rows, grid, 2).astype(np.float64)
+    arrive, leave = t[:, :, 0], t[:, :, 1]
+    kinds = ["embed"] + [k for _ in range(cfg.n_layers) for k in ("qkv", "attn", "o", "gate_up", "down")] + ["lm_head"]
+    acc = {}
+    for k in range(1, rows):
+        name = kinds[k - 1]
+        work = arrive[k].max() - leave[k - 1].max()
+        bar = leave[k].max() - arrive[k].max()
+        mean_cta = (arrive[k] - leave[k - 1]).mean()
+        a = acc.setdefault(name, [0.0, 0.0, 0.0, 0])
+        a[0] += work; a[1] += bar; a[2] += mean_cta; a[3] += 1
+    out = {n: {"work": round(a[0] / a[3] / 1e3, 2), "barrier": round(a[1] / a[3] / 1e3, 2),
+               "mean_cta_work": round(a[2] / a[3] / 1e3, 2), "count": a[3]} for n, a in acc.items()}
+    out["total_step_us"] = round((leave[rows - 1].max() - leave[0].min()) / 1e3, 1)
+    return out
 
 
 def gpu_arm_e32(args, rank, world, local_rank):
@@ -448,7 +509,7 @@ def gpu_arm_e32(args, rank, world, local_rank):
         "step_roofline": {"bytes_per_step_avg": int(np.mean(step_bytes)), "achieved_gbs": round(gbs, 1),
                           "frac": round(gbs / peak, 4), "peak": peak, "peak_source": peak_src},
         "replacement_s_excluded": round(repl_s, 3), "replacements": int((finish < steps).sum()),
-        "clocks": clocks, "gpu_launches": (4 + 6 * cfg.n_layers) * steps, "setup_s": round(setup_s, 1),
+        "clocks": clocks, "gpu_launches": launches_per_step(cfg, B) * steps, "setup_s": round(setup_s, 1),
     }
 
 
@@ -623,6 +684,8 @@ def main():
     ap.add_argument("--impl", default="ql", choices=["ql", "reference"])
     ap.add_argument("--config", default="e1", choices=["e1", "e32"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--step-kernel", default="auto", choices=["auto", "persistent", "launches"],
+                    help="decode step implementation (auto: persistent when the batch allows it)")
     ap.add_argument("--micro", choices=["gemv", "attn"], help="time one kernel family alone")
     ap.add_argument("--shape", default=None, help="micro gemv: ROWSxCOLS (default: all shapes)")
     ap.add_argument("--batch", default=None, help="micro: comma-separated batch sizes")

@@ -221,8 +221,17 @@ enum { QL_STEP_AUTO = 0, QL_STEP_LAUNCHES = 1, QL_STEP_PERSISTENT = 2 };
  *                              (read with ql_check_device_error), every CTA leaves the step
  *                              and the step's outputs are not written; the next step runs
  *                              normally. Nothing else waits on another CTA.
+ *   QL_OPT_TEST_BARRIER_EXTRA  0 (default) or 1: every barrier of the persistent step also
+ *                              waits for one arrival that never comes, so the bounded wait
+ *                              runs out (failure-path tests; no fault, the context stays usable)
+ *   QL_OPT_STEP_TRACE          device address of a uint64 buffer of at least
+ *                              (2 + 5 n_layers + 1) * num_SMs * 2 entries, or 0 (default, off):
+ *                              the persistent step writes globaltimer stamps (ns) there, row 0
+ *                              = each CTA's start, row k = arrival and exit of barrier k
+ *                              ([row][CTA][arrive, exit]); a profiling aid
  * Applies to steps issued (or graphs captured) afterwards. QL_EINVAL for anything else.  */
-enum { QL_OPT_STEP_KERNEL = 1, QL_OPT_BARRIER_TIMEOUT_NS = 2 };
+enum { QL_OPT_STEP_KERNEL = 1, QL_OPT_BARRIER_TIMEOUT_NS = 2, QL_OPT_TEST_BARRIER_EXTRA = 3,
+       QL_OPT_STEP_TRACE = 4 };
 int ql_model_set_option(ql_model* m, int option, int64_t value);
 /* Largest batch the persistent step kernel takes for this model on its device: 0 when the
  * shape or the device does not allow it (matrix widths must be multiples of 128, codes 16-byte

@@ -13,6 +13,7 @@ from ._lib import (QLError, QL_OK, QL_EINVAL, QL_ENOMEM, QL_ECUDA, QL_EPOOL, QL_
                    QL_EDEVICE, QL_ESTATE, QL_DTYPE_F32, QL_DTYPE_F16, QL_EPI_NONE,
                    QL_EPI_ADD_RESIDUAL, QL_EPI_SILU_MUL, QL_STEP_AUTO, QL_STEP_LAUNCHES,
                    QL_STEP_PERSISTENT, QL_OPT_STEP_KERNEL, QL_OPT_BARRIER_TIMEOUT_NS,
+                   QL_OPT_TEST_BARRIER_EXTRA, QL_OPT_STEP_TRACE,
                    Q4Matrix, LayerDesc, ModelDesc,
                    StepArgs, SIGNATURES, LIB_PATH, lib, check, ptr, stream_ptr)
 

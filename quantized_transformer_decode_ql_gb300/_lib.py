@@ -17,7 +17,7 @@ QL_OK, QL_EINVAL, QL_ENOMEM, QL_ECUDA, QL_EPOOL, QL_ERANGE, QL_EDEVICE, QL_ESTAT
 QL_DTYPE_F32, QL_DTYPE_F16 = 0, 1
 QL_EPI_NONE, QL_EPI_ADD_RESIDUAL, QL_EPI_SILU_MUL = 0, 1, 2
 QL_STEP_AUTO, QL_STEP_LAUNCHES, QL_STEP_PERSISTENT = 0, 1, 2
-QL_OPT_STEP_KERNEL, QL_OPT_BARRIER_TIMEOUT_NS = 1, 2
+QL_OPT_STEP_KERNEL, QL_OPT_BARRIER_TIMEOUT_NS, QL_OPT_TEST_BARRIER_EXTRA, QL_OPT_STEP_TRACE = 1, 2, 3, 4
 
 
 class QLError(RuntimeError):

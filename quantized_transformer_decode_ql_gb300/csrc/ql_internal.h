@@ -226,6 +226,8 @@ struct PersistParams {
     float eps, scale_log2;
     long long num_blocks, layer_pool, max_position, out_stride;
     unsigned long long barrier_timeout_ns;
+    unsigned int barrier_extra;     // arrivals every barrier waits for beyond the grid (tests: 1)
+    unsigned long long* trace;      // optional [1 + barriers][grid][2] globaltimer stamps
     const int32_t* tokens;
     int32_t* positions;
     const int32_t* block_tables;

@@ -53,6 +53,8 @@ struct ql_model {
     int persist_max_b = 0;                  // 0: not available for this shape / device
     int step_kernel = QL_STEP_AUTO;
     unsigned long long barrier_timeout_ns = 2000000000ull;
+    unsigned int barrier_extra = 0;
+    unsigned long long* trace = nullptr;    // caller-owned, see QL_OPT_STEP_TRACE
     ql::PLayer* players = nullptr;          // device [n_layers]
     ql::PMat plm = {};
     int max_nblk = 0, persist_nsplit = 1;
@@ -143,6 +145,8 @@ int run_persist(ql_model* m, const ql_step_args* a, cudaStream_t s) {
     p.max_position = d.max_blocks_per_seq * d.block_size;
     p.out_stride = a->out_tokens ? a->out_stride : 0;
     p.barrier_timeout_ns = m->barrier_timeout_ns;
+    p.barrier_extra = m->barrier_extra;
+    p.trace = m->trace;
     p.tokens = a->tokens;
     p.positions = a->positions;
     p.block_tables = a->block_tables;
@@ -510,6 +514,14 @@ extern "C" int ql_model_set_option(ql_model* m, int option, int64_t value) {
         case QL_OPT_BARRIER_TIMEOUT_NS:
             if (value < 0) return set_error(QL_EINVAL, "ql_model_set_option: negative timeout");
             m->barrier_timeout_ns = (unsigned long long)value;
+            return QL_OK;
+        case QL_OPT_TEST_BARRIER_EXTRA:
+            if (value < 0 || value > 1) return set_error(QL_EINVAL, "ql_model_set_option: extra arrivals must be 0 or 1");
+            m->barrier_extra = (unsigned int)value;
+            return QL_OK;
+        case QL_OPT_STEP_TRACE:
+            if ((value & 7) != 0) return set_error(QL_EINVAL, "ql_model_set_option: trace buffer must be 8-byte aligned");
+            m->trace = reinterpret_cast<unsigned long long*>(static_cast<uintptr_t>(value));
             return QL_OK;
         default:
             return set_error(QL_EINVAL, "ql_model_set_option: unknown option");

@@ -106,20 +106,26 @@ __device__ __forceinline__ unsigned int load_acquire(const unsigned int* a) {
 }
 
 // Barrier over the co-resident CTAs of the launch. sync[0] counts arrivals over the whole
-// launch (the k-th barrier waits for k * gridDim.x of them); sync[2] is the abort flag. The wait
-// is bounded by the clock: after p.barrier_timeout_ns the CTA records an error, raises the flag
-// and returns false, as does every CTA that sees the flag; the caller then leaves the step.
+// launch (the k-th barrier waits for k * gridDim.x of them, plus p.barrier_extra, which only a
+// test sets: an arrival that never comes); sync[2] is the abort flag. The wait is bounded by the
+// clock: after p.barrier_timeout_ns the CTA records an error, raises the flag and returns false,
+// as does every CTA that sees the flag; the caller then leaves the step. With p.trace set,
+// thread 0 stamps its arrival and its exit (globaltimer, ns) in row k of the trace.
 static __device__ __noinline__ bool grid_barrier(const PersistParams& p, unsigned int& target, int* ok_smem) {
     __syncthreads();
     if (threadIdx.x == 0) {
         target += gridDim.x;
+        unsigned long long* tr =
+            p.trace ? p.trace + ((size_t)(target / gridDim.x) * gridDim.x + blockIdx.x) * 2 : nullptr;
+        if (tr) tr[0] = global_ns();
+        const unsigned int need = target + p.barrier_extra;
         int ok = 1;
         __threadfence();
         atomicAdd(p.sync, 1u);
-        if (load_acquire(p.sync) < target) {
+        if (load_acquire(p.sync) < need) {
             const unsigned long long t0 = global_ns();
             for (unsigned int spin = 1;; ++spin) {
-                if (load_acquire(p.sync) >= target) break;
+                if (load_acquire(p.sync) >= need) break;
                 if ((spin & 15u) == 0) {
                     if (load_acquire(p.sync + 2) != 0u) {
                         ok = 0;
@@ -136,6 +142,7 @@ static __device__ __noinline__ bool grid_barrier(const PersistParams& p, unsigne
             }
         }
         __threadfence();
+        if (tr) tr[1] = global_ns();
         *ok_smem = ok;
     }
     __syncthreads();
@@ -935,6 +942,7 @@ __global__ void __launch_bounds__(kT, 1) step_kernel(const __grid_constant__ Per
     r.nst = 1;
     r.a = r.b = nullptr;
     r.s = nullptr;
+    if (p.trace && threadIdx.x == 0) p.trace[2 * blockIdx.x] = p.trace[2 * blockIdx.x + 1] = global_ns();
     ring_seek(r, p, warp, lane);
     // the weights do not depend on anything computed in the step: start streaming at once
 #pragma unroll 1

@@ -44,6 +44,7 @@ def tiny(tiny_model):
     yield tiny_model
     tiny_model[0].ql_model_set_option(ql.QL_OPT_STEP_KERNEL, ql.QL_STEP_AUTO)
     tiny_model[0].ql_model_set_option(ql.QL_OPT_BARRIER_TIMEOUT_NS, 2_000_000_000)
+    tiny_model[0].ql_model_set_option(ql.QL_OPT_TEST_BARRIER_EXTRA, 0)
 
 
 def set_mode(gm, mode):
@@ -256,9 +257,10 @@ def test_batched_slots_with_replacement(tiny, B):
 
 
 def test_persistent_barrier_wait_is_bounded(tiny):
-    """A grid barrier whose wait runs out (a zero bound: any wait at all expires) ends the step
-    on every CTA without a fault: the device error says which barrier, the position does not
-    advance, and the next step with the normal bound is correct again."""
+    """A grid barrier whose wait runs out (every barrier made to wait for one arrival that
+    never comes, bound 1 ms) ends the step on every CTA without a fault: the device error says
+    which barrier, the position does not advance, and the next step without the missing
+    arrival is correct again."""
     ql = lib()
     gm, om = tiny
     set_mode(gm, "persistent")
@@ -268,12 +270,14 @@ def test_persistent_barrier_wait_is_bounded(tiny):
     nxt = torch.full((1,), -5, dtype=torch.int32, device="cuda")
     logits = torch.zeros((1, CFG.vocab), dtype=torch.float32, device="cuda")
     args = gm.step_args(tokens, positions, dev(slot_tables(1, 4, seed=51)), nxt, logits=logits)
-    gm.ql_model_set_option(ql.QL_OPT_BARRIER_TIMEOUT_NS, 0)
+    gm.ql_model_set_option(ql.QL_OPT_BARRIER_TIMEOUT_NS, 1_000_000)
+    gm.ql_model_set_option(ql.QL_OPT_TEST_BARRIER_EXTRA, 1)
     gm.ql_decode_step(args)
     with pytest.raises(ql.QLError) as e:
         gm.ql_check_device_error()
     assert e.value.status == ql.QL_EDEVICE and "barrier" in str(e.value)
     assert int(positions.item()) == 0 and int(nxt.item()) == -5
+    gm.ql_model_set_option(ql.QL_OPT_TEST_BARRIER_EXTRA, 0)
     gm.ql_model_set_option(ql.QL_OPT_BARRIER_TIMEOUT_NS, 2_000_000_000)
     for _ in range(2):   # the interrupted step left nothing behind (counters, tickets, keys)
         positions.fill_(0)
