@@ -376,7 +376,7 @@ def step_phases(gm, sargs, s, cfg):
     import quantized_transformer_decode_ql_gb300 as ql
     grid = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     rows = 3 + 5 * cfg.n_layers
-    buf = torch.zeros(rows * grid * 2, dtype=torch.int64, device="cuda")
+    buf = torch.zeros(rows * grid * 8, dtype=torch.int64, device="cuda")
     gm.ql_model_set_option(ql.QL_OPT_STEP_TRACE, buf.data_ptr())
     try:
         for _ in range(3):
@@ -385,7 +385,7 @@ def step_phases(gm, sargs, s, cfg):
     finally:
         gm.ql_model_set_option(ql.QL_OPT_STEP_TRACE, 0)
     gm.ql_check_device_error()
-    t = buf.cpu().numpy().reshape(rows, grid, 2).astype(np.float64)
+    t = buf.cpu().numpy().reshape(rows, grid, 8).astype(np.float64)
     arrive, leave = t[:, :, 0], t[:, :, 1]
     kinds = ["embed"] + [k for _ in range(cfg.n_layers) for k in ("qkv", "attn", "o", "gate_up", "down")] + ["lm_head"]
     acc = {}
@@ -394,10 +394,17 @@ def step_phases(gm, sargs, s, cfg):
         work = arrive[k].max() - leave[k - 1].max()
         bar = leave[k].max() - arrive[k].max()
         mean_cta = (arrive[k] - leave[k - 1]).mean()
-        a = acc.setdefault(name, [0.0, 0.0, 0.0, 0])
-        a[0] += work; a[1] += bar; a[2] += mean_cta; a[3] += 1
+        # steps inside the phase (mean over the CTAs that stamped them), from the previous exit
+        st = []
+        for i in range(2, 6):
+            v = t[k, :, i]
+            ok = v > 0
+            st.append(float((v[ok] - leave[k - 1][ok]).mean()) if ok.any() else float("nan"))
+        a = acc.setdefault(name, [0.0, 0.0, 0.0, 0, np.zeros(4)])
+        a[0] += work; a[1] += bar; a[2] += mean_cta; a[3] += 1; a[4] += np.array(st)
     out = {n: {"work": round(a[0] / a[3] / 1e3, 2), "barrier": round(a[1] / a[3] / 1e3, 2),
-               "mean_cta_work": round(a[2] / a[3] / 1e3, 2), "count": a[3]} for n, a in acc.items()}
+               "mean_cta_work": round(a[2] / a[3] / 1e3, 2), "count": a[3],
+               "steps": [round(x / a[3] / 1e3, 2) for x in a[4]]} for n, a in acc.items()}
     out["total_step_us"] = round((leave[rows - 1].max() - leave[0].min()) / 1e3, 1)
     return out
 

@@ -225,10 +225,14 @@ enum { QL_STEP_AUTO = 0, QL_STEP_LAUNCHES = 1, QL_STEP_PERSISTENT = 2 };
  *                              waits for one arrival that never comes, so the bounded wait
  *                              runs out (failure-path tests; no fault, the context stays usable)
  *   QL_OPT_STEP_TRACE          device address of a uint64 buffer of at least
- *                              (2 + 5 n_layers + 1) * num_SMs * 2 entries, or 0 (default, off):
- *                              the persistent step writes globaltimer stamps (ns) there, row 0
- *                              = each CTA's start, row k = arrival and exit of barrier k
- *                              ([row][CTA][arrive, exit]); a profiling aid
+ *                              (2 + 5 n_layers + 1) * num_SMs * 8 entries, or 0 (default, off):
+ *                              the persistent step writes globaltimer stamps (ns) there as
+ *                              [row][CTA][8]: row 0 entry 0/1 = the CTA's start; row k >= 1,
+ *                              entries 0/1 = arrival at / exit from barrier k, entries 2..5 =
+ *                              steps of the phase that ends at barrier k (GEMV: activations
+ *                              staged, warp 0's units done, all warps done, epilogues done;
+ *                              attention: q ready, blocks merged, split ticket taken, end); a
+ *                              profiling aid
  * Applies to steps issued (or graphs captured) afterwards. QL_EINVAL for anything else.  */
 enum { QL_OPT_STEP_KERNEL = 1, QL_OPT_BARRIER_TIMEOUT_NS = 2, QL_OPT_TEST_BARRIER_EXTRA = 3,
        QL_OPT_STEP_TRACE = 4 };

@@ -49,6 +49,7 @@ constexpr int kBS = 16;                 // tokens per KV block
 constexpr int kMaxB = kPersistMaxBatch;
 constexpr int kMaxSplit = 256;
 constexpr int kPartBytes = kW * 2 * 32 * 16;   // per-warp partial fragments of shared tiles
+constexpr int kTraceWords = 8;                 // trace entries per (row, CTA)
 
 enum Epi { kEpiF32 = 0, kEpiResid = 1, kEpiSilu = 2, kEpiLogits = 3 };
 
@@ -99,6 +100,10 @@ __device__ __forceinline__ unsigned long long global_ns() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
+// Thread 0 stamps step `i` of the current phase (trace entries 2..5), when tracing.
+__device__ __forceinline__ void stamp(unsigned long long* tr, int i) {
+    if (tr != nullptr && threadIdx.x == 0) tr[i] = global_ns();
+}
 __device__ __forceinline__ unsigned int load_acquire(const unsigned int* a) {
     unsigned int v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
@@ -110,13 +115,14 @@ __device__ __forceinline__ unsigned int load_acquire(const unsigned int* a) {
 // test sets: an arrival that never comes); sync[2] is the abort flag. The wait is bounded by the
 // clock: after p.barrier_timeout_ns the CTA records an error, raises the flag and returns false,
 // as does every CTA that sees the flag; the caller then leaves the step. With p.trace set,
-// thread 0 stamps its arrival and its exit (globaltimer, ns) in row k of the trace.
+// thread 0 stamps its arrival and its exit (globaltimer, ns) in row k of the trace (entries 0
+// and 1 of kTraceWords; the phase that ends at barrier k stamps its own steps in 2..5).
 static __device__ __noinline__ bool grid_barrier(const PersistParams& p, unsigned int& target, int* ok_smem) {
     __syncthreads();
     if (threadIdx.x == 0) {
         target += gridDim.x;
         unsigned long long* tr =
-            p.trace ? p.trace + ((size_t)(target / gridDim.x) * gridDim.x + blockIdx.x) * 2 : nullptr;
+            p.trace ? p.trace + ((size_t)(target / gridDim.x) * gridDim.x + blockIdx.x) * kTraceWords : nullptr;
         if (tr) tr[0] = global_ns();
         const unsigned int need = target + p.barrier_extra;
         int ok = 1;
@@ -440,7 +446,7 @@ template <int EPI, bool RMS>
 __device__ __noinline__ void gemv_phase(const PersistParams& p, const PMat M, Ring& ring, const float* xf,
                                         const __half* x16, const float* norm_w, void* y, int ld,
                                         unsigned char* region, float* red,
-                                        unsigned long long (*kred)[kMaxB]) {
+                                        unsigned long long (*kred)[kMaxB], unsigned long long* tr) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t = lane & 3;
     const int cstride = p.max_nblk * 4 + 4;   // uint4 units between staged columns (+64 B)
@@ -450,6 +456,7 @@ __device__ __noinline__ void gemv_phase(const PersistParams& p, const PMat M, Ri
 
     stage_x<RMS>(p, M.nblk, cstride, xf, x16, norm_w, xs, bias, red);
     __syncthreads();
+    stamp(tr, 2);
 
     Ring r = ring;   // a register copy for the loop; written back at the end
     const int nst = M.nblk / kUnitBlocks;
@@ -519,7 +526,9 @@ __device__ __noinline__ void gemv_phase(const PersistParams& p, const PMat M, Ri
         }
     }
     ring = r;
+    stamp(tr, 3);
     __syncthreads();
+    stamp(tr, 4);
     // A tile shared by several warps is finished by the warp holding its last unit: the partials
     // of every warp that touched it, summed in warp order.
     if (u1 > u0) {
@@ -561,6 +570,7 @@ __device__ __noinline__ void gemv_phase(const PersistParams& p, const PMat M, Ri
             if (m && act) atomicMax(p.keys + tid, m);
         }
     }
+    stamp(tr, 5);
 }
 
 // ------------------------------------------------------------------------------ attention
@@ -612,7 +622,7 @@ template <> struct VRow<4> {
 // range holding the newest position also normalises, rotates and appends the new K/V first.
 template <int HD, int G>
 __device__ __noinline__ void attn_phase(const PersistParams& p, int layer, unsigned char* region,
-                                        __half (*qs)[HD], int* flag) {
+                                        __half (*qs)[HD], int* flag, unsigned long long* tr) {
     constexpr int NCH = HD / 32;   // 32-dim chunks of a K row (one 16-byte load per lane each)
     constexpr int DPL = HD / 32;   // P.V output dims per lane
     constexpr int WST = G * HD > 128 ? G * HD : 128;   // floats per warp in the merge buffer
@@ -667,6 +677,7 @@ __device__ __noinline__ void attn_phase(const PersistParams& p, int layer, unsig
         }
         __threadfence();
         __syncthreads();
+        stamp(tr, 2);
 
         // Q as the A operand of S = Q K^T (rows = the G heads, rows >= G zero). head_dim is
         // permuted: in k-steps 2m, 2m + 1 lane t holds dims 32 m + 8 t + {0,1 | 2,3} and
@@ -774,6 +785,7 @@ __device__ __noinline__ void attn_phase(const PersistParams& p, int layer, unsig
             wl[warp * G + lane] = 0.f;
         }
         __syncthreads();
+        stamp(tr, 3);
         for (int i = tid; i < G * HD; i += kT) {
             const int h = i / HD, d = i - h * HD;
             float M = -INFINITY;
@@ -808,6 +820,7 @@ __device__ __noinline__ void attn_phase(const PersistParams& p, int layer, unsig
         __syncthreads();
         if (tid == 0) *flag = atomicAdd(p.tickets + b * p.nkv + kvh, 1) == n_active - 1;
         __syncthreads();
+        stamp(tr, 4);
         if (!*flag) continue;
         __threadfence();
         float* sw = wacc;   // [G][kMaxSplit] weights exp2(m_k - M) / L
@@ -858,6 +871,7 @@ __device__ __noinline__ void attn_phase(const PersistParams& p, int layer, unsig
             *reinterpret_cast<__half2*>(out + 2) = __floats2half2_rn(A.z, A.w);
         }
         if (tid == 0) p.tickets[b * p.nkv + kvh] = 0;   // re-arm for the next layer / step
+        stamp(tr, 5);
     }
 }
 
@@ -898,29 +912,33 @@ template <int HD, int G>
 __device__ void step_body(const PersistParams& p, Ring& r, unsigned char* region, __half (*qs)[HD], float* red,
                           unsigned long long (*kred)[kMaxB], int* flag) {
     unsigned int target = 0;
+    // trace row of the barrier that ends the next phase
+    auto row = [&]() -> unsigned long long* {
+        return p.trace ? p.trace + ((size_t)(target / gridDim.x + 1) * gridDim.x + blockIdx.x) * kTraceWords : nullptr;
+    };
     embed_phase(p);
     if (!grid_barrier(p, target, flag)) return;
     const int qkv_ld = (p.nh + 2 * p.nkv) * HD;
     for (int l = 0; l < p.n_layers; ++l) {
         const PLayer* Ly = p.layers + l;
         // q|k|v = W_qkv rmsnorm(x, attn_norm)
-        gemv_phase<kEpiF32, true>(p, Ly->m[0], r, p.x, nullptr, Ly->attn_norm, p.qkv, qkv_ld, region, red, kred);
+        gemv_phase<kEpiF32, true>(p, Ly->m[0], r, p.x, nullptr, Ly->attn_norm, p.qkv, qkv_ld, region, red, kred, row());
         if (!grid_barrier(p, target, flag)) return;
         // qk-norm + RoPE + KV append + paged attention -> attn
-        attn_phase<HD, G>(p, l, region, qs, flag);
+        attn_phase<HD, G>(p, l, region, qs, flag, row());
         if (!grid_barrier(p, target, flag)) return;
         // x += W_o attn
-        gemv_phase<kEpiResid, false>(p, Ly->m[1], r, nullptr, p.attn, nullptr, p.x, p.hidden, region, red, kred);
+        gemv_phase<kEpiResid, false>(p, Ly->m[1], r, nullptr, p.attn, nullptr, p.x, p.hidden, region, red, kred, row());
         if (!grid_barrier(p, target, flag)) return;
         // act = silu(gate) * up, [gate | up] = W_gu rmsnorm(x, ffn_norm)
-        gemv_phase<kEpiSilu, true>(p, Ly->m[2], r, p.x, nullptr, Ly->ffn_norm, p.act, p.inter, region, red, kred);
+        gemv_phase<kEpiSilu, true>(p, Ly->m[2], r, p.x, nullptr, Ly->ffn_norm, p.act, p.inter, region, red, kred, row());
         if (!grid_barrier(p, target, flag)) return;
         // x += W_down act
-        gemv_phase<kEpiResid, false>(p, Ly->m[3], r, nullptr, p.act, nullptr, p.x, p.hidden, region, red, kred);
+        gemv_phase<kEpiResid, false>(p, Ly->m[3], r, nullptr, p.act, nullptr, p.x, p.hidden, region, red, kred, row());
         if (!grid_barrier(p, target, flag)) return;
     }
     // logits = W_lm rmsnorm(x, final_norm), greedy argmax keys
-    gemv_phase<kEpiLogits, true>(p, p.lm, r, p.x, nullptr, p.final_norm, p.logits, p.vocab, region, red, kred);
+    gemv_phase<kEpiLogits, true>(p, p.lm, r, p.x, nullptr, p.final_norm, p.logits, p.vocab, region, red, kred, row());
     if (!grid_barrier(p, target, flag)) return;
     if (blockIdx.x == 0) finalize(p);
 }
@@ -942,7 +960,7 @@ __global__ void __launch_bounds__(kT, 1) step_kernel(const __grid_constant__ Per
     r.nst = 1;
     r.a = r.b = nullptr;
     r.s = nullptr;
-    if (p.trace && threadIdx.x == 0) p.trace[2 * blockIdx.x] = p.trace[2 * blockIdx.x + 1] = global_ns();
+    if (p.trace && threadIdx.x == 0) p.trace[kTraceWords * blockIdx.x] = p.trace[kTraceWords * blockIdx.x + 1] = global_ns();
     ring_seek(r, p, warp, lane);
     // the weights do not depend on anything computed in the step: start streaming at once
 #pragma unroll 1
