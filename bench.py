@@ -379,8 +379,11 @@ def step_phases(gm, sargs, s, cfg):
     buf = torch.zeros(rows * grid * 8, dtype=torch.int64, device="cuda")
     gm.ql_model_set_option(ql.QL_OPT_STEP_TRACE, buf.data_ptr())
     try:
-        for _ in range(3):
+        for _ in range(2):
             gm.ql_decode_step(sargs, s)
+        s.synchronize()
+        buf.zero_()   # stamps of the last step only (a CTA stamps only the phases it works in)
+        gm.ql_decode_step(sargs, s)
         s.synchronize()
     finally:
         gm.ql_model_set_option(ql.QL_OPT_STEP_TRACE, 0)

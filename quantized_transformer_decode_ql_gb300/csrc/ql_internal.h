@@ -251,12 +251,12 @@ struct PersistParams {
     unsigned int* sync;   // [4], zero between steps: barrier arrivals, exits, abort flag
     DevError* err;
 };
-// Dynamic shared memory of the step kernel for a batch of `batch` and matrices of at most
-// max_nblk blocks per row.
-size_t persist_smem_bytes(int batch, int max_nblk, int head_dim, int group);
+// Dynamic shared memory of the step kernel for a batch of `batch`, matrices of at most max_nblk
+// blocks per row and n_layers layers.
+size_t persist_smem_bytes(int batch, int max_nblk, int head_dim, int group, int n_layers);
 // Sets the kernel attributes for this shape and checks that one CTA fits on every SM with a
 // cooperative launch: QL_OK, or QL_EINVAL with the reason in ql_last_error().
-int persist_prepare(int batch, int max_nblk, int head_dim, int group);
+int persist_prepare(int batch, int max_nblk, int head_dim, int group, int n_layers);
 int persist_launch(const PersistParams& p, int head_dim, int group, cudaStream_t s);
 
 }  // namespace ql

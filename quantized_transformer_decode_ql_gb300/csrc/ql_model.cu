@@ -353,7 +353,7 @@ int setup_persist(ql_model* m) {
     const int G = (int)(d.n_heads / d.n_kv_heads);
     int maxb = (int)(d.max_batch < kPersistMaxBatch ? d.max_batch : kPersistMaxBatch);
     for (; maxb >= 1; --maxb)
-        if (persist_prepare(maxb, m->max_nblk, (int)d.head_dim, G) == QL_OK) break;
+        if (persist_prepare(maxb, m->max_nblk, (int)d.head_dim, G, (int)d.n_layers) == QL_OK) break;
     if (maxb < 1) return QL_OK;
 
     std::vector<PLayer> hl(m->layers.size());

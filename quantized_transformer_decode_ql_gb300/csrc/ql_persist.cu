@@ -11,13 +11,12 @@ cudaError_t persist_dispatch_hd128(int G, bool launch, const PersistParams* p, s
     return persist::dispatch<128>(G, launch, p, smem, grid, s, occ);
 }
 
-size_t persist_smem_bytes(int batch, int max_nblk, int head_dim, int group) {
-    const size_t a = persist::gemv_region_bytes(batch, max_nblk);
-    const size_t b = persist::attn_region_bytes(head_dim, group);
-    return persist::kRingBytes + (a > b ? a : b);
+size_t persist_smem_bytes(int batch, int max_nblk, int head_dim, int group, int n_layers) {
+    return persist::kRingBytes + persist::region_bytes(batch, max_nblk, head_dim, group) +
+           persist::mat_table_bytes(n_layers);
 }
 
-int persist_prepare(int batch, int max_nblk, int head_dim, int group) {
+int persist_prepare(int batch, int max_nblk, int head_dim, int group, int n_layers) {
     QL_REQUIRE(batch >= 1 && batch <= kPersistMaxBatch, "persistent step: batch out of range");
     QL_REQUIRE(head_dim == 64 || head_dim == 128, "persistent step: head_dim must be 64 or 128");
     QL_REQUIRE(group == 1 || group == 2 || group == 4 || group == 8, "persistent step: GQA group must be 1, 2, 4 or 8");
@@ -28,7 +27,7 @@ int persist_prepare(int batch, int max_nblk, int head_dim, int group) {
     QL_TRY_CUDA(cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev));
     QL_TRY_CUDA(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
     QL_REQUIRE(coop != 0, "persistent step: the device has no cooperative launch");
-    const size_t smem = persist_smem_bytes(batch, max_nblk, head_dim, group);
+    const size_t smem = persist_smem_bytes(batch, max_nblk, head_dim, group, n_layers);
     if (smem > (size_t)optin)
         return set_error(QL_EINVAL, "persistent step: needs " + std::to_string(smem) +
                                         " bytes of shared memory per CTA, the device allows " + std::to_string(optin));
@@ -41,7 +40,7 @@ int persist_prepare(int batch, int max_nblk, int head_dim, int group) {
 }
 
 int persist_launch(const PersistParams& p, int head_dim, int group, cudaStream_t s) {
-    const size_t smem = persist_smem_bytes(p.B, p.max_nblk, head_dim, group);
+    const size_t smem = persist_smem_bytes(p.B, p.max_nblk, head_dim, group, p.n_layers);
     const int grid = num_sms();
     const cudaError_t e = head_dim == 128 ? persist_dispatch_hd128(group, true, &p, smem, grid, s, nullptr)
                                           : persist_dispatch_hd64(group, true, &p, smem, grid, s, nullptr);

@@ -175,16 +175,18 @@ static __device__ void leave_step(const PersistParams& p) {
 
 // ------------------------------------------------------------------------------ weight ring
 // The step's matrices in streaming order: 4 per layer (q|k|v, o, gate|up, down), then lm_head.
-__device__ __forceinline__ PMat mat_at(const PersistParams& p, int wp) {
+// The kernel copies their descriptors into shared memory (`mats`) once at the start.
+__device__ __forceinline__ PMat mat_global(const PersistParams& p, int wp) {
     return wp < 4 * p.n_layers ? p.layers[wp >> 2].m[wp & 3] : p.lm;
 }
-// Tiles [t0, t1) of a matrix handled by this CTA (balanced to one tile).
+__host__ __device__ constexpr size_t mat_table_bytes(int n_layers) { return (size_t)(4 * n_layers + 1) * sizeof(PMat); }
+// Tiles [t0, t1) of a matrix handled by this CTA (balanced to one tile; ntile * grid < 2^32).
 __device__ __forceinline__ void cta_tiles(int ntile, int& t0, int& t1) {
-    t0 = (int)(((long long)blockIdx.x * ntile) / gridDim.x);
-    t1 = (int)(((long long)(blockIdx.x + 1) * ntile) / gridDim.x);
+    t0 = (int)((blockIdx.x * (unsigned)ntile) / gridDim.x);
+    t1 = (int)(((blockIdx.x + 1) * (unsigned)ntile) / gridDim.x);
 }
 // First unit of warp w among the U units of its CTA (balanced to one unit).
-__device__ __forceinline__ int warp_unit(int U, int w) { return (int)(((long long)w * U) / kW); }
+__device__ __forceinline__ int warp_unit(int U, int w) { return (w * U) / kW; }
 
 // Global row of row r (0..15) of a tile; rows past the matrix read row 0 and are discarded.
 __device__ __forceinline__ int tile_row(const PMat& M, int tile, int r, bool& ok) {
@@ -223,9 +225,9 @@ __device__ __forceinline__ void ring_set_tile(Ring& r, const PMat& M, int lane) 
 }
 
 // Move to the first matrix at or after r.wp in which this warp has units.
-__device__ __forceinline__ void ring_seek(Ring& r, const PersistParams& p, int warp, int lane) {
+__device__ __forceinline__ void ring_seek(Ring& r, const PMat* mats, int warp, int lane) {
     for (; r.wp < r.nmat; ++r.wp) {
-        const PMat M = mat_at(p, r.wp);
+        const PMat& M = mats[r.wp];
         int t0, t1;
         cta_tiles(M.ntile, t0, t1);
         const int nst = M.nblk / kUnitBlocks;
@@ -244,7 +246,7 @@ __device__ __forceinline__ void ring_seek(Ring& r, const PersistParams& p, int w
 }
 
 // Copy the next unit into its ring slot (one commit group per call, empty past the end).
-__device__ __forceinline__ void ring_issue(Ring& r, const PersistParams& p, int warp, int lane) {
+__device__ __forceinline__ void ring_issue(Ring& r, const PMat* mats, int warp, int lane) {
     if (r.wp < r.nmat) {
         const uint32_t st = r.base + (r.issued % kStages) * kUnitBytes;
         const uint32_t dA = (uint32_t)(((lane >> 3) * 16 + (lane & 7)) * 16);
@@ -256,11 +258,11 @@ __device__ __forceinline__ void ring_issue(Ring& r, const PersistParams& p, int 
                          "l"(r.s + r.k * kUnitBlocks) : "memory");
         if (++r.u == r.u_end) {
             ++r.wp;
-            ring_seek(r, p, warp, lane);
+            ring_seek(r, mats, warp, lane);
         } else if (++r.k == r.nst) {
             r.k = 0;
             ++r.tile;
-            ring_set_tile(r, mat_at(p, r.wp), lane);
+            ring_set_tile(r, mats[r.wp], lane);
         }
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
@@ -272,90 +274,44 @@ __device__ __forceinline__ void ring_issue(Ring& r, const PersistParams& p, int 
 // feeds MMA lane t: f16 pairs (x0, x2), (x1, x3), (x16, x18)/16, (x17, x19)/16 of elements
 // 32 j + 4 t + ...), plus the accumulator start -(1032 sum x_lo + 1152 sum x_hi/16) of every
 // (block, column). RMS: the input is the f32 residual stream, normalised (RMSNorm with weight
-// w) on the way; its first two items per thread stay in registers between the two passes.
-// Data written earlier in the launch by other CTAs is read with ld.global.cg (L2).
+// w) on the way; the first kHeld items of a thread and their weights are loaded together and
+// stay in registers between the two passes. f16 input: kChunk items per thread are loaded
+// together. Data written earlier in the launch by other CTAs is read with ld.global.cg (L2).
 template <bool RMS>
 __device__ __noinline__ void stage_x(const PersistParams& p, int nblk, int cstride, const float* xf,
                                      const __half* x16, const float* w, uint4* xs, float* bias, float* red) {
-    constexpr int kHeld = 2;
+    constexpr int kHeld = 2, kChunk = 4;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int B = p.B, cols = nblk * 32, nitems = B * nblk * 4;
     if (B < 2)
         for (int j = tid; j < nblk; j += kT) bias[2 * j + 1] = 0.f;   // absent second column
 
-    auto load = [&](int item, float (&v)[8]) {
-        const int t = item & 3, bj = item >> 2, b = bj / nblk, j = bj - b * nblk;
-        const size_t off = (size_t)b * cols + 32 * j + 4 * t;
-        if (RMS) {
-            const float4 a = __ldcg(reinterpret_cast<const float4*>(xf + off));
-            const float4 h = __ldcg(reinterpret_cast<const float4*>(xf + off + 16));
-            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-            v[4] = h.x; v[5] = h.y; v[6] = h.z; v[7] = h.w;
-        } else {
-            const uint2 a = __ldcg(reinterpret_cast<const uint2*>(x16 + off));
-            const uint2 h = __ldcg(reinterpret_cast<const uint2*>(x16 + off + 16));
-            const float2 f0 = __half22float2(as_h2(a.x)), f1 = __half22float2(as_h2(a.y));
-            const float2 f2 = __half22float2(as_h2(h.x)), f3 = __half22float2(as_h2(h.y));
-            v[0] = f0.x; v[1] = f0.y; v[2] = f1.x; v[3] = f1.y;
-            v[4] = f2.x; v[5] = f2.y; v[6] = f3.x; v[7] = f3.y;
-        }
+    // item -> (column b, block j, chunk t) and its element offset
+    auto where = [&](int item, int& b, int& j, int& t) -> size_t {
+        t = item & 3;
+        const int bj = item >> 2;
+        b = bj / nblk;
+        j = bj - b * nblk;
+        return (size_t)b * cols + 32 * j + 4 * t;
     };
-
-    float held[kHeld][8];
-    float rs0 = 1.f, rs1 = 1.f;
-    if (RMS) {
-        float ss0 = 0.f, ss1 = 0.f;
-#pragma unroll
-        for (int r = 0; r < kHeld; ++r) {
-            const int item = tid + r * kT;
-            if (item < nitems) {
-                load(item, held[r]);
-                float s = 0.f;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) s += held[r][i] * held[r][i];
-                if (item < nblk * 4) ss0 += s; else ss1 += s;
-            }
-        }
-        for (int item = tid + kHeld * kT; item < nitems; item += kT) {
-            float v[8];
-            load(item, v);
-            float s = 0.f;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) s += v[i] * v[i];
-            if (item < nblk * 4) ss0 += s; else ss1 += s;
-        }
-#pragma unroll
-        for (int o = 16; o; o >>= 1) {
-            ss0 += __shfl_xor_sync(0xffffffffu, ss0, o);
-            ss1 += __shfl_xor_sync(0xffffffffu, ss1, o);
-        }
-        if (lane == 0) {
-            red[warp * 2] = ss0;
-            red[warp * 2 + 1] = ss1;
-        }
-        __syncthreads();
-        float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-        for (int i = 0; i < kW; ++i) {
-            a0 += red[i * 2];
-            a1 += red[i * 2 + 1];
-        }
-        rs0 = 1.0f / sqrtf(a0 / (float)cols + p.eps);
-        rs1 = 1.0f / sqrtf(a1 / (float)cols + p.eps);
-    }
-
-    // item -> staged chunk and (t == 0) the block's offset term; whole warps run together
-    // (the loop bound is warp-uniform) because of the shuffles
+    auto load_f32 = [&](const float* src, size_t off, float (&v)[8]) {
+        const float4 a = __ldcg(reinterpret_cast<const float4*>(src + off));
+        const float4 h = __ldcg(reinterpret_cast<const float4*>(src + off + 16));
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = h.x; v[5] = h.y; v[6] = h.z; v[7] = h.w;
+    };
+    auto load_w = [&](int j, int t, float (&v)[8]) {
+        const float4 a = __ldg(reinterpret_cast<const float4*>(w + 32 * j + 4 * t));
+        const float4 h = __ldg(reinterpret_cast<const float4*>(w + 32 * j + 16 + 4 * t));
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = h.x; v[5] = h.y; v[6] = h.z; v[7] = h.w;
+    };
+    // item -> staged chunk and (t == 0) the block's offset term; whole warps call it together
+    // (warp-uniform loop bounds) because of the shuffles
     auto emit = [&](int item, float (&v)[8]) {
-        const int t = item & 3, bj = item >> 2, b = bj / nblk, j = bj - b * nblk;
+        int b, j, t;
+        where(item, b, j, t);
         const bool live = item < nitems;
-        if (RMS && live) {
-            const float rr = b == 0 ? rs0 : rs1;
-            const float4 wa = __ldg(reinterpret_cast<const float4*>(w + 32 * j + 4 * t));
-            const float4 wh = __ldg(reinterpret_cast<const float4*>(w + 32 * j + 16 + 4 * t));
-            v[0] *= rr * wa.x; v[1] *= rr * wa.y; v[2] *= rr * wa.z; v[3] *= rr * wa.w;
-            v[4] *= rr * wh.x; v[5] *= rr * wh.y; v[6] *= rr * wh.z; v[7] *= rr * wh.w;
-        }
         if (!live) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) v[i] = 0.f;
@@ -377,24 +333,111 @@ __device__ __noinline__ void stage_x(const PersistParams& p, int nblk, int cstri
             if (t == 0) bias[2 * j + b] = -part;
         }
     };
+
+    if (RMS) {
+        float hx[kHeld][8], hw[kHeld][8];
+        float ss0 = 0.f, ss1 = 0.f;
 #pragma unroll
-    for (int r = 0; r < kHeld; ++r) {
-        const int base = r * kT;
-        if (base < nitems) {
-            float v[8];
-            if (RMS) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) v[i] = held[r][i];
-            } else if (base + tid < nitems) {
-                load(base + tid, v);
+        for (int r = 0; r < kHeld; ++r) {
+            const int item = tid + r * kT;
+            if (item < nitems) {
+                int b, j, t;
+                const size_t off = where(item, b, j, t);
+                load_f32(xf, off, hx[r]);
+                load_w(j, t, hw[r]);
             }
-            emit(base + tid, v);
         }
-    }
-    for (int base = kHeld * kT; base < nitems; base += kT) {
-        float v[8];
-        if (base + tid < nitems) load(base + tid, v);
-        emit(base + tid, v);
+#pragma unroll
+        for (int r = 0; r < kHeld; ++r) {
+            const int item = tid + r * kT;
+            if (item < nitems) {
+                float s2 = 0.f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) s2 += hx[r][i] * hx[r][i];
+                if (item < nblk * 4) ss0 += s2; else ss1 += s2;
+            }
+        }
+        for (int item = tid + kHeld * kT; item < nitems; item += kT) {
+            int b, j, t;
+            float v[8];
+            load_f32(xf, where(item, b, j, t), v);
+            float s2 = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) s2 += v[i] * v[i];
+            if (item < nblk * 4) ss0 += s2; else ss1 += s2;
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            ss0 += __shfl_xor_sync(0xffffffffu, ss0, o);
+            ss1 += __shfl_xor_sync(0xffffffffu, ss1, o);
+        }
+        if (lane == 0) {
+            red[warp * 2] = ss0;
+            red[warp * 2 + 1] = ss1;
+        }
+        __syncthreads();
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int i = 0; i < kW; ++i) {
+            a0 += red[i * 2];
+            a1 += red[i * 2 + 1];
+        }
+        const float rs0 = 1.0f / sqrtf(a0 / (float)cols + p.eps);
+        const float rs1 = 1.0f / sqrtf(a1 / (float)cols + p.eps);
+#pragma unroll
+        for (int r = 0; r < kHeld; ++r) {
+            const int base = r * kT;
+            if (base < nitems) {
+                const int item = base + tid;
+                const float rr = item < nblk * 4 ? rs0 : rs1;
+                float v[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[i] = hx[r][i] * rr * hw[r][i];
+                emit(item, v);
+            }
+        }
+        for (int base = kHeld * kT; base < nitems; base += kT) {
+            const int item = base + tid;
+            float v[8];
+            if (item < nitems) {
+                int b, j, t;
+                float wv[8];
+                load_f32(xf, where(item, b, j, t), v);
+                load_w(j, t, wv);
+                const float rr = b == 0 ? rs0 : rs1;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[i] *= rr * wv[i];
+            }
+            emit(item, v);
+        }
+    } else {
+        for (int base = 0; base < nitems; base += kChunk * kT) {
+            uint2 ra[kChunk], rh[kChunk];
+#pragma unroll
+            for (int c = 0; c < kChunk; ++c) {
+                const int item = base + c * kT + tid;
+                if (item < nitems) {
+                    int b, j, t;
+                    const size_t off = where(item, b, j, t);
+                    ra[c] = __ldcg(reinterpret_cast<const uint2*>(x16 + off));
+                    rh[c] = __ldcg(reinterpret_cast<const uint2*>(x16 + off + 16));
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < kChunk; ++c) {
+                if (base + c * kT < nitems) {
+                    const int item = base + c * kT + tid;
+                    float v[8];
+                    if (item < nitems) {
+                        const float2 f0 = __half22float2(as_h2(ra[c].x)), f1 = __half22float2(as_h2(ra[c].y));
+                        const float2 f2 = __half22float2(as_h2(rh[c].x)), f3 = __half22float2(as_h2(rh[c].y));
+                        v[0] = f0.x; v[1] = f0.y; v[2] = f1.x; v[3] = f1.y;
+                        v[4] = f2.x; v[5] = f2.y; v[6] = f3.x; v[7] = f3.y;
+                    }
+                    emit(item, v);
+                }
+            }
+        }
     }
 }
 
@@ -443,12 +486,13 @@ __device__ __forceinline__ void finish_tile(const PersistParams& p, const PMat& 
 // CTA call it. The warp consumes its units from the ring (issuing one unit further for each
 // one consumed), in the order the issue side produced them.
 template <int EPI, bool RMS>
-__device__ __noinline__ void gemv_phase(const PersistParams& p, const PMat M, Ring& ring, const float* xf,
+__device__ __noinline__ void gemv_phase(const PersistParams& p, const PMat* mats, int wp, Ring& ring, const float* xf,
                                         const __half* x16, const float* norm_w, void* y, int ld,
                                         unsigned char* region, float* red,
                                         unsigned long long (*kred)[kMaxB], unsigned long long* tr) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t = lane & 3;
+    const PMat M = mats[wp];
     const int cstride = p.max_nblk * 4 + 4;   // uint4 units between staged columns (+64 B)
     uint4* xs = reinterpret_cast<uint4*>(region);
     float* bias = reinterpret_cast<float*>(xs + (size_t)p.B * cstride);   // [nblk][2]
@@ -490,7 +534,7 @@ __device__ __noinline__ void gemv_phase(const PersistParams& p, const PMat M, Ri
         const uint2 scb = *reinterpret_cast<const uint2*>(stg + 1024 + (g + 8) * 8);
         __syncwarp();
         ++r.consumed;
-        ring_issue(r, p, warp, lane);   // refill the slot just read
+        ring_issue(r, mats, warp, lane);   // refill the slot just read
         const float2 da01 = __half22float2(as_h2(sca.x)), da23 = __half22float2(as_h2(sca.y));
         const float2 db01 = __half22float2(as_h2(scb.x)), db23 = __half22float2(as_h2(scb.y));
         const float da[4] = {da01.x, da01.y, da23.x, da23.y};
@@ -675,7 +719,7 @@ __device__ __noinline__ void attn_phase(const PersistParams& p, int layer, unsig
                 }
             }
         }
-        __threadfence();
+        __threadfence_block();   // the new K/V row is read by this CTA only
         __syncthreads();
         stamp(tr, 2);
 
@@ -908,9 +952,33 @@ static __device__ void finalize(const PersistParams& p) {
     p.positions[b] = pos + 1;
 }
 
+// Ask L2 for the K/V tiles this CTA's attention items of `layer` will read (a hint: issued at
+// the start of the layer's q|k|v phase, so that the attention phase finds them in L2).
+template <int HD>
+__device__ void attn_prefetch(const PersistParams& p, int layer) {
+    const int nitems = p.B * p.nkv * p.nsplit;
+    const size_t lp = (size_t)layer * p.layer_pool;
+    for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
+        const int s = item % p.nsplit, bk = item / p.nsplit, kvh = bk % p.nkv, b = bk / p.nkv;
+        if (p.active && p.active[b] == 0) continue;
+        const int L = p.positions[b] + 1;
+        if (L <= 0 || L > p.maxb * kBS) continue;
+        const int nblocks = (L + kBS - 1) / kBS;
+        const int spb = (nblocks + p.nsplit - 1) / p.nsplit;
+        const int blk0 = s * spb, blk1 = min(nblocks, blk0 + spb);
+        for (int i = threadIdx.x; i < 2 * (blk1 - blk0); i += kT) {
+            const int phys = p.block_tables[(size_t)b * p.maxb + blk0 + (i >> 1)];
+            if (phys < 0 || phys >= p.num_blocks) continue;
+            const __half* base = ((i & 1) ? p.v_pool : p.k_pool) + lp + ((size_t)phys * p.nkv + kvh) * kBS * HD;
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base), "r"((uint32_t)(kBS * HD * 2))
+                         : "memory");
+        }
+    }
+}
+
 template <int HD, int G>
-__device__ void step_body(const PersistParams& p, Ring& r, unsigned char* region, __half (*qs)[HD], float* red,
-                          unsigned long long (*kred)[kMaxB], int* flag) {
+__device__ void step_body(const PersistParams& p, const PMat* mats, Ring& r, unsigned char* region, __half (*qs)[HD],
+                          float* red, unsigned long long (*kred)[kMaxB], int* flag) {
     unsigned int target = 0;
     // trace row of the barrier that ends the next phase
     auto row = [&]() -> unsigned long long* {
@@ -921,26 +989,38 @@ __device__ void step_body(const PersistParams& p, Ring& r, unsigned char* region
     const int qkv_ld = (p.nh + 2 * p.nkv) * HD;
     for (int l = 0; l < p.n_layers; ++l) {
         const PLayer* Ly = p.layers + l;
+        attn_prefetch<HD>(p, l);
         // q|k|v = W_qkv rmsnorm(x, attn_norm)
-        gemv_phase<kEpiF32, true>(p, Ly->m[0], r, p.x, nullptr, Ly->attn_norm, p.qkv, qkv_ld, region, red, kred, row());
+        gemv_phase<kEpiF32, true>(p, mats, 4 * l, r, p.x, nullptr, Ly->attn_norm, p.qkv, qkv_ld, region, red, kred,
+                                  row());
         if (!grid_barrier(p, target, flag)) return;
         // qk-norm + RoPE + KV append + paged attention -> attn
         attn_phase<HD, G>(p, l, region, qs, flag, row());
         if (!grid_barrier(p, target, flag)) return;
         // x += W_o attn
-        gemv_phase<kEpiResid, false>(p, Ly->m[1], r, nullptr, p.attn, nullptr, p.x, p.hidden, region, red, kred, row());
+        gemv_phase<kEpiResid, false>(p, mats, 4 * l + 1, r, nullptr, p.attn, nullptr, p.x, p.hidden, region, red,
+                                     kred, row());
         if (!grid_barrier(p, target, flag)) return;
         // act = silu(gate) * up, [gate | up] = W_gu rmsnorm(x, ffn_norm)
-        gemv_phase<kEpiSilu, true>(p, Ly->m[2], r, p.x, nullptr, Ly->ffn_norm, p.act, p.inter, region, red, kred, row());
+        gemv_phase<kEpiSilu, true>(p, mats, 4 * l + 2, r, p.x, nullptr, Ly->ffn_norm, p.act, p.inter, region, red,
+                                   kred, row());
         if (!grid_barrier(p, target, flag)) return;
         // x += W_down act
-        gemv_phase<kEpiResid, false>(p, Ly->m[3], r, nullptr, p.act, nullptr, p.x, p.hidden, region, red, kred, row());
+        gemv_phase<kEpiResid, false>(p, mats, 4 * l + 3, r, nullptr, p.act, nullptr, p.x, p.hidden, region, red,
+                                     kred, row());
         if (!grid_barrier(p, target, flag)) return;
     }
     // logits = W_lm rmsnorm(x, final_norm), greedy argmax keys
-    gemv_phase<kEpiLogits, true>(p, p.lm, r, p.x, nullptr, p.final_norm, p.logits, p.vocab, region, red, kred, row());
+    gemv_phase<kEpiLogits, true>(p, mats, 4 * p.n_layers, r, p.x, nullptr, p.final_norm, p.logits, p.vocab, region,
+                                 red, kred, row());
     if (!grid_barrier(p, target, flag)) return;
     if (blockIdx.x == 0) finalize(p);
+}
+
+// Dynamic shared memory: [weight rings][GEMV staging | attention merge][matrix descriptors].
+__host__ __device__ constexpr size_t region_bytes(int batch, int max_nblk, int head_dim, int group) {
+    return gemv_region_bytes(batch, max_nblk) > attn_region_bytes(head_dim, group) ? gemv_region_bytes(batch, max_nblk)
+                                                                                   : attn_region_bytes(head_dim, group);
 }
 
 template <int HD, int G>
@@ -951,21 +1031,27 @@ __global__ void __launch_bounds__(kT, 1) step_kernel(const __grid_constant__ Per
     __shared__ unsigned long long kred[kW][kMaxB];
     __shared__ int flag;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    unsigned char* region = smem + kRingBytes;
+    PMat* mats = reinterpret_cast<PMat*>(region + region_bytes(p.B, p.max_nblk, HD, G));
+    if (p.trace && threadIdx.x == 0)
+        p.trace[kTraceWords * blockIdx.x] = p.trace[kTraceWords * blockIdx.x + 1] = global_ns();
+    const int nmat = 4 * p.n_layers + 1;
+    for (int i = threadIdx.x; i < nmat; i += kT) mats[i] = mat_global(p, i);
+    __syncthreads();
     Ring r;
     r.wp = 0;
-    r.nmat = 4 * p.n_layers + 1;
+    r.nmat = nmat;
     r.issued = r.consumed = 0;
     r.base = static_cast<uint32_t>(__cvta_generic_to_shared(smem)) + (uint32_t)(warp * kStages * kUnitBytes);
     r.u = r.u_end = r.k = r.tile = 0;
     r.nst = 1;
     r.a = r.b = nullptr;
     r.s = nullptr;
-    if (p.trace && threadIdx.x == 0) p.trace[kTraceWords * blockIdx.x] = p.trace[kTraceWords * blockIdx.x + 1] = global_ns();
-    ring_seek(r, p, warp, lane);
+    ring_seek(r, mats, warp, lane);
     // the weights do not depend on anything computed in the step: start streaming at once
 #pragma unroll 1
-    for (int i = 0; i < kStages; ++i) ring_issue(r, p, warp, lane);
-    step_body<HD, G>(p, r, smem + kRingBytes, qs, red, kred, &flag);
+    for (int i = 0; i < kStages; ++i) ring_issue(r, mats, warp, lane);
+    step_body<HD, G>(p, mats, r, region, qs, red, kred, &flag);
     asm volatile("cp.async.wait_group 0;" ::: "memory");
     leave_step(p);
 }
