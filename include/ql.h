@@ -237,7 +237,11 @@ enum { QL_STEP_AUTO = 0, QL_STEP_LAUNCHES = 1, QL_STEP_PERSISTENT = 2 };
 enum { QL_OPT_STEP_KERNEL = 1, QL_OPT_BARRIER_TIMEOUT_NS = 2, QL_OPT_TEST_BARRIER_EXTRA = 3,
        QL_OPT_STEP_TRACE = 4 };
 int ql_model_set_option(ql_model* m, int option, int64_t value);
-/* Largest batch the persistent step kernel takes for this model on its device: 0 when the
+/* When the persistent kernel is available, ql_model_create also keeps a copy of every q4_0
+ * matrix re-laid as a tile stream (16 rows x 4 blocks of codes and their scales contiguous,
+ * 1152 B per unit) for the kernel's bulk copies: device memory equal to the weights again.
+ * The weights must not change after ql_model_create.
+ * Largest batch the persistent step kernel takes for this model on its device: 0 when the
  * shape or the device does not allow it (matrix widths must be multiples of 128, codes 16-byte
  * and scales 8-byte aligned, one CTA with ~200 KB of shared memory per SM).              */
 int64_t ql_model_persistent_max_batch(const ql_model* m);

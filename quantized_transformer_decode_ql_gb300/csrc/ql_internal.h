@@ -202,12 +202,18 @@ int rope_launch(const RopeArgs& a, cudaStream_t s, bool pdl);
 // The whole step of a small batch as one cooperative kernel (one CTA per SM); see
 // ql_persist.cuh. Matrices are described as the kernel streams them.
 struct PMat {
-    const uint8_t* quants;
-    const __half* scales;
+    const uint8_t* stream;   // the matrix in the tile stream layout (persist_pack_streams)
+    const uint8_t* quants;   // the row-major q4_0 source: codes [rows][nblk][16]
+    const __half* scales;    //                            scales [rows][nblk]
     int rows, nblk;     // nblk = cols / 32, a multiple of 4
     int silu;           // rows = [gate | up]; a tile is 8 gate rows + the matching 8 up rows
     int ntile;          // 16-row tiles
 };
+// Bytes of a matrix in the tile stream layout: ntile * (nblk / 4) units of 1152 B.
+size_t persist_stream_bytes(const PMat& m);
+// Re-lay n matrices (quants/scales set) into `buf` (persist_stream_bytes of each, back to back)
+// and set their `stream` pointers; runs on stream s.
+int persist_pack_streams(PMat* mats, int n, uint8_t* buf, cudaStream_t s);
 struct PLayer {
     PMat m[4];          // q|k|v, o, gate|up, down
     const float* attn_norm;

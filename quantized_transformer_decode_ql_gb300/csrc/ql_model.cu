@@ -56,6 +56,8 @@ struct ql_model {
     unsigned int barrier_extra = 0;
     unsigned long long* trace = nullptr;    // caller-owned, see QL_OPT_STEP_TRACE
     ql::PLayer* players = nullptr;          // device [n_layers]
+    uint8_t* pstreams = nullptr;            // all matrices in the tile stream layout
+    size_t persist_stream_bytes = 0;
     ql::PMat plm = {};
     int max_nblk = 0, persist_nsplit = 1;
     float* ppm = nullptr;
@@ -324,6 +326,7 @@ int run_step(ql_model* m, const ql_step_args* a, cudaStream_t s) {
 
 PMat pmat(const ql_q4_0_matrix& w, bool silu) {
     PMat p = {};
+    p.stream = nullptr;
     p.quants = static_cast<const uint8_t*>(w.quants);
     p.scales = static_cast<const __half*>(w.scales);
     p.rows = (int)w.rows;
@@ -357,18 +360,21 @@ int setup_persist(ql_model* m) {
     if (maxb < 1) return QL_OK;
 
     std::vector<PLayer> hl(m->layers.size());
+    std::vector<PMat> all;
     for (size_t i = 0; i < hl.size(); ++i) {
         const ql_layer_desc& L = m->layers[i];
-        hl[i].m[0] = pmat(L.qkv, false);
-        hl[i].m[1] = pmat(L.o, false);
-        hl[i].m[2] = pmat(L.gate_up, true);
-        hl[i].m[3] = pmat(L.down, false);
+        all.push_back(pmat(L.qkv, false));
+        all.push_back(pmat(L.o, false));
+        all.push_back(pmat(L.gate_up, true));
+        all.push_back(pmat(L.down, false));
         hl[i].attn_norm = L.attn_norm;
         hl[i].ffn_norm = L.ffn_norm;
         hl[i].q_norm = L.q_norm;
         hl[i].k_norm = L.k_norm;
     }
-    m->plm = pmat(d.lm_head, false);
+    all.push_back(pmat(d.lm_head, false));
+    size_t stream_bytes = 0;
+    for (const PMat& pm : all) stream_bytes += persist_stream_bytes(pm);
     int nsplit = num_sms();
     nsplit = nsplit > 256 ? 256 : nsplit;
     nsplit = nsplit > d.max_blocks_per_seq ? (int)d.max_blocks_per_seq : nsplit;
@@ -376,6 +382,7 @@ int setup_persist(ql_model* m) {
     const size_t parts = (size_t)maxb * d.n_heads * m->persist_nsplit;
     int rc = QL_OK;
     auto A = [&](void** p, size_t bytes) { if (rc == QL_OK) rc = alloc(m, p, bytes); };
+    A((void**)&m->pstreams, stream_bytes);
     A((void**)&m->players, hl.size() * sizeof(PLayer));
     A((void**)&m->ppm, parts * 4);
     A((void**)&m->ppl, parts * 4);
@@ -383,11 +390,17 @@ int setup_persist(ql_model* m) {
     A((void**)&m->ptickets, (size_t)maxb * d.n_kv_heads * 4);
     A((void**)&m->psync, 16);
     if (rc != QL_OK) return rc;
+    // the weights re-laid into the tile stream layout that the persistent kernel copies from
+    if ((rc = persist_pack_streams(all.data(), (int)all.size(), m->pstreams, nullptr)) != QL_OK) return rc;
+    for (size_t i = 0; i < hl.size(); ++i)
+        for (int k = 0; k < 4; ++k) hl[i].m[k] = all[4 * i + k];
+    m->plm = all.back();
     cudaError_t e = cudaMemcpy(m->players, hl.data(), hl.size() * sizeof(PLayer), cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemset(m->ptickets, 0, (size_t)maxb * d.n_kv_heads * 4);
     if (e == cudaSuccess) e = cudaMemset(m->psync, 0, 16);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_error(e, "ql_model_create: persistent step workspace");
+    m->persist_stream_bytes = stream_bytes;
     m->persist_max_b = maxb;
     return QL_OK;
 }

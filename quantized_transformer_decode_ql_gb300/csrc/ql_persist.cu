@@ -39,6 +39,23 @@ int persist_prepare(int batch, int max_nblk, int head_dim, int group, int n_laye
     return QL_OK;
 }
 
+size_t persist_stream_bytes(const PMat& m) {
+    return (size_t)m.ntile * (m.nblk / persist::kUnitBlocks) * persist::kUnitBytes;
+}
+
+int persist_pack_streams(PMat* mats, int n, uint8_t* buf, cudaStream_t s) {
+    size_t off = 0;
+    const int grid = 4 * num_sms();
+    for (int i = 0; i < n; ++i) {
+        mats[i].stream = buf + off;
+        persist::stream_pack_kernel<<<grid, 256, 0, s>>>(mats[i], buf + off);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_error(e, "persistent step: stream pack launch");
+        off += persist_stream_bytes(mats[i]);
+    }
+    return QL_OK;
+}
+
 int persist_launch(const PersistParams& p, int head_dim, int group, cudaStream_t s) {
     const size_t smem = persist_smem_bytes(p.B, p.max_nblk, head_dim, group, p.n_layers);
     const int grid = num_sms();

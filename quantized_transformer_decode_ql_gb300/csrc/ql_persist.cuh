@@ -11,9 +11,12 @@
 // 2-4.6 TB/s of the ~6.7 TB/s the part sustains. Here one CTA per SM runs the whole step:
 //  * every warp owns a fixed sequence of weight "units" (16 rows x 4 q4_0 blocks: 1 KB of codes
 //    plus 128 B of scales) over ALL the step's matrices and streams them through a private
-//    shared-memory ring with cp.async. Weights do not depend on activations, so the ring fills
-//    with the next phase's weights while the CTA waits at a grid barrier, stages activations or
-//    runs attention: HBM keeps streaming across phase boundaries;
+//    shared-memory ring, one bulk copy (TMA) per unit completing on the slot's mbarrier; the
+//    matrices are re-laid once into a tile stream layout in which every unit is contiguous.
+//    (Per-lane 16-byte cp.async copies from the row-major layout, measured first, sustained
+//    only ~26 GB/s per SM.) Weights do not depend on activations, so the ring fills with the
+//    next phase's weights while the CTA waits at a grid barrier, stages activations or runs
+//    attention: HBM keeps streaming across phase boundaries;
 //  * phases are separated by a grid-wide barrier (a counter in global memory, bounded wait:
 //    after a timeout the CTA records an error, raises an abort flag and leaves the step);
 //  * a matrix is split over CTAs by 16-row tiles, and inside a CTA over the 16 warps by flat
@@ -200,32 +203,23 @@ __device__ __forceinline__ int tile_row(const PMat& M, int tile, int r, bool& ok
     return ok ? row : 0;
 }
 
-// Issue side of a warp's ring (per-lane state). A unit is stored as codes [block 0..3][row
-// 0..15] x 16 B, then the 16 rows' 4 scales (8 B each): lane l copies block l >> 3 of rows
-// (l & 7) and (l & 7) + 8, lanes 0..15 the scales of row l.
+// Issue side of a warp's ring. The matrices are stored in the tile stream layout
+// (stream_pack_kernel): unit (tile, k) is 1152 contiguous bytes at stream + (tile nst + k) 1152,
+// codes [block 0..3][row 0..15] x 16 B, then the 16 rows' 4 scales (8 B each), so a warp's
+// units of one matrix are one contiguous byte range. Lane 0 copies each unit into its ring
+// slot with one bulk copy (TMA, cp.async.bulk) that completes on the slot's mbarrier.
 struct Ring {
     int wp, nmat;          // matrix of the next unit to issue; nmat = end of the step
     int u, u_end;          // unit (within the warp's range of that matrix) and range end
-    int k, nst, tile;      // 4-block group inside the tile, groups per tile, tile
-    const uint8_t* a;      // this lane's copy sources at group 0 of the tile
-    const uint8_t* b;
-    const __half* s;
-    unsigned int issued, consumed;   // ring slot = count % kStages
+    const uint8_t* src;    // stream address of unit u
+    unsigned int issued, consumed;   // units; ring slot = count % kStages
     uint32_t base;         // shared-memory address of this warp's ring
+    uint32_t mbar;         // shared-memory address of this warp's kStages mbarriers
+    int dead;              // a wait ran out: issue and wait no more (the step is aborted)
 };
 
-__device__ __forceinline__ void ring_set_tile(Ring& r, const PMat& M, int lane) {
-    bool ok;
-    const int lr = lane & 7, lb = lane >> 3;
-    const int ra = tile_row(M, r.tile, lr, ok), rb = tile_row(M, r.tile, lr + 8, ok);
-    const int rs = tile_row(M, r.tile, lane & 15, ok);
-    r.a = M.quants + ((size_t)ra * M.nblk + lb) * 16;
-    r.b = M.quants + ((size_t)rb * M.nblk + lb) * 16;
-    r.s = M.scales + (size_t)rs * M.nblk;
-}
-
 // Move to the first matrix at or after r.wp in which this warp has units.
-__device__ __forceinline__ void ring_seek(Ring& r, const PMat* mats, int warp, int lane) {
+__device__ __forceinline__ void ring_seek(Ring& r, const PMat* mats, int warp) {
     for (; r.wp < r.nmat; ++r.wp) {
         const PMat& M = mats[r.wp];
         int t0, t1;
@@ -236,37 +230,58 @@ __device__ __forceinline__ void ring_seek(Ring& r, const PMat* mats, int warp, i
         if (u1 > u0) {
             r.u = u0;
             r.u_end = u1;
-            r.nst = nst;
-            r.tile = t0 + u0 / nst;
-            r.k = u0 % nst;
-            ring_set_tile(r, M, lane);
+            r.src = M.stream + ((size_t)t0 * nst + u0) * kUnitBytes;
             return;
         }
     }
 }
 
-// Copy the next unit into its ring slot (one commit group per call, empty past the end).
+// Copy the next unit into its ring slot.
 __device__ __forceinline__ void ring_issue(Ring& r, const PMat* mats, int warp, int lane) {
-    if (r.wp < r.nmat) {
-        const uint32_t st = r.base + (r.issued % kStages) * kUnitBytes;
-        const uint32_t dA = (uint32_t)(((lane >> 3) * 16 + (lane & 7)) * 16);
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(st + dA), "l"(r.a + r.k * 64) : "memory");
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(st + dA + 128), "l"(r.b + r.k * 64)
-                     : "memory");
-        if (lane < 16)
-            asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(st + 1024 + lane * 8),
-                         "l"(r.s + r.k * kUnitBlocks) : "memory");
-        if (++r.u == r.u_end) {
-            ++r.wp;
-            ring_seek(r, mats, warp, lane);
-        } else if (++r.k == r.nst) {
-            r.k = 0;
-            ++r.tile;
-            ring_set_tile(r, mats[r.wp], lane);
-        }
+    if (r.wp >= r.nmat || r.dead) return;
+    if (lane == 0) {
+        const unsigned int slot = r.issued % kStages;
+        const uint32_t mb = r.mbar + slot * 8, dst = r.base + slot * kUnitBytes;
+        // order this warp's earlier generic-proxy reads of the slot before the async-proxy write
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mb), "r"(kUnitBytes) : "memory");
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                     ::"r"(dst), "l"(r.src), "r"(kUnitBytes), "r"(mb) : "memory");
     }
-    asm volatile("cp.async.commit_group;" ::: "memory");
+    r.src += kUnitBytes;
     ++r.issued;
+    if (++r.u == r.u_end) {
+        ++r.wp;
+        ring_seek(r, mats, warp);
+    }
+}
+
+__device__ __forceinline__ bool mbar_test(uint32_t mb, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred q;\n mbarrier.try_wait.parity.shared::cta.b64 q, [%1], %2;\n selp.u32 %0, 1, 0, q;\n}"
+        : "=r"(done)
+        : "r"(mb), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Wait until the unit r.consumed has landed in its slot. Bounded by the clock: when the bound
+// runs out the warp records an error, raises the step's abort flag and stops using the ring.
+__device__ __forceinline__ void ring_wait(Ring& r, const PersistParams& p) {
+    if (r.dead) return;
+    const uint32_t mb = r.mbar + (r.consumed % kStages) * 8, parity = (r.consumed / kStages) & 1u;
+    if (mbar_test(mb, parity)) return;
+    const unsigned long long t0 = global_ns();
+    for (unsigned int spin = 1;; ++spin) {
+        if (mbar_test(mb, parity)) return;
+        if ((spin & 63u) == 0 && global_ns() - t0 > p.barrier_timeout_ns) break;
+    }
+    if ((threadIdx.x & 31) == 0) {
+        record_device_error(p.err, kErrGemvStage, blockIdx.x, (long long)r.consumed);
+        atomicExch(p.sync + 2, 1u);
+    }
+    r.dead = 1;
 }
 
 // ------------------------------------------------------------------------------ GEMV phase
@@ -522,7 +537,7 @@ __device__ __noinline__ void gemv_phase(const PersistParams& p, const PMat* mats
     const int first_tile = tile;
 #pragma unroll 1
     for (int u = u0; u < u1; ++u) {
-        asm volatile("cp.async.wait_group %0;" ::"n"(kStages - 1) : "memory");
+        ring_wait(r, p);
         __syncwarp();
         const unsigned int slot = r.consumed % kStages;
         const uint32_t st = r.base + slot * kUnitBytes;
@@ -1038,22 +1053,69 @@ __global__ void __launch_bounds__(kT, 1) step_kernel(const __grid_constant__ Per
     const int nmat = 4 * p.n_layers + 1;
     for (int i = threadIdx.x; i < nmat; i += kT) mats[i] = mat_global(p, i);
     __syncthreads();
+    // per-warp ring slots, one mbarrier each (arrival count 1: the issuing lane)
+    __shared__ __align__(8) unsigned long long mbar[kW * kStages];
+    if (lane == 0)
+        for (int i = 0; i < kStages; ++i)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(
+                             static_cast<uint32_t>(__cvta_generic_to_shared(&mbar[warp * kStages + i]))) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    __syncthreads();
     Ring r;
     r.wp = 0;
     r.nmat = nmat;
+    r.u = r.u_end = 0;
+    r.src = nullptr;
     r.issued = r.consumed = 0;
+    r.dead = 0;
     r.base = static_cast<uint32_t>(__cvta_generic_to_shared(smem)) + (uint32_t)(warp * kStages * kUnitBytes);
-    r.u = r.u_end = r.k = r.tile = 0;
-    r.nst = 1;
-    r.a = r.b = nullptr;
-    r.s = nullptr;
-    ring_seek(r, mats, warp, lane);
+    r.mbar = static_cast<uint32_t>(__cvta_generic_to_shared(&mbar[warp * kStages]));
+    ring_seek(r, mats, warp);
     // the weights do not depend on anything computed in the step: start streaming at once
 #pragma unroll 1
     for (int i = 0; i < kStages; ++i) ring_issue(r, mats, warp, lane);
     step_body<HD, G>(p, mats, r, region, qs, red, kred, &flag);
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    // after an early exit, let this warp's copies still in flight land before leaving (bounded:
+    // past the bound the CTA leaves anyway)
+    const unsigned long long t0 = global_ns();
+    while (r.consumed < r.issued) {
+        const uint32_t mb = r.mbar + (r.consumed % kStages) * 8, parity = (r.consumed / kStages) & 1u;
+        bool landed = mbar_test(mb, parity);
+        while (!landed && global_ns() - t0 <= p.barrier_timeout_ns) landed = mbar_test(mb, parity);
+        if (!landed) break;
+        ++r.consumed;
+    }
     leave_step(p);
+}
+
+// ------------------------------------------------------------------------------ stream layout
+// Re-lay a q4_0 matrix (codes [rows][nblk][16], f16 scales [rows][nblk]) into the tile stream
+// layout, one warp per 1152-byte unit; rows past the matrix are zero (a zero scale: no
+// contribution). An exact byte permutation.
+static __global__ void stream_pack_kernel(PMat M, uint8_t* out) {
+    const int lane = threadIdx.x & 31;
+    const int nst = M.nblk / kUnitBlocks;
+    const long long nunits = (long long)M.ntile * nst;
+    const long long wpb = blockDim.x / 32;
+    for (long long u = blockIdx.x * wpb + (threadIdx.x >> 5); u < nunits; u += (long long)gridDim.x * wpb) {
+        const int tile = (int)(u / nst), k = (int)(u % nst);
+        uint8_t* dst = out + u * kUnitBytes;
+        for (int c = lane; c < kUnitBlocks * 16; c += 32) {
+            const int q = c >> 4, r = c & 15;
+            bool ok;
+            const int row = tile_row(M, tile, r, ok);
+            const uint4 v = ok ? *reinterpret_cast<const uint4*>(M.quants + ((size_t)row * M.nblk + kUnitBlocks * k + q) * 16)
+                               : make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(dst + c * 16) = v;
+        }
+        if (lane < 16) {
+            bool ok;
+            const int row = tile_row(M, tile, lane, ok);
+            const uint2 v = ok ? *reinterpret_cast<const uint2*>(M.scales + (size_t)row * M.nblk + kUnitBlocks * k)
+                               : make_uint2(0u, 0u);
+            *reinterpret_cast<uint2*>(dst + kUnitBlocks * 16 * 16 + lane * 8) = v;
+        }
+    }
 }
 
 }  // namespace persist
