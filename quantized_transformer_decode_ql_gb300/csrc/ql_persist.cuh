@@ -53,6 +53,7 @@ constexpr int kMaxB = kPersistMaxBatch;
 constexpr int kMaxSplit = 256;
 constexpr int kPartBytes = kW * 2 * 32 * 16;   // per-warp partial fragments of shared tiles
 constexpr int kTraceWords = 8;                 // trace entries per (row, CTA)
+constexpr int kFastSpins = 4096;               // polls of a wait before its clock starts
 
 enum Epi { kEpiF32 = 0, kEpiResid = 1, kEpiSilu = 2, kEpiLogits = 3 };
 
@@ -131,6 +132,8 @@ static __device__ __noinline__ bool grid_barrier(const PersistParams& p, unsigne
         int ok = 1;
         __threadfence();
         atomicAdd(p.sync, 1u);
+        for (int spin = 0; spin < kFastSpins && load_acquire(p.sync) < need; ++spin) {
+        }
         if (load_acquire(p.sync) < need) {
             const unsigned long long t0 = global_ns();
             for (unsigned int spin = 1;; ++spin) {
@@ -271,7 +274,9 @@ __device__ __forceinline__ bool mbar_test(uint32_t mb, uint32_t parity) {
 __device__ __forceinline__ void ring_wait(Ring& r, const PersistParams& p) {
     if (r.dead) return;
     const uint32_t mb = r.mbar + (r.consumed % kStages) * 8, parity = (r.consumed / kStages) & 1u;
-    if (mbar_test(mb, parity)) return;
+    // fast path without the clock (reading %globaltimer is slow); the clock bounds the rest
+    for (int spin = 0; spin < kFastSpins; ++spin)
+        if (mbar_test(mb, parity)) return;
     const unsigned long long t0 = global_ns();
     for (unsigned int spin = 1;; ++spin) {
         if (mbar_test(mb, parity)) return;
