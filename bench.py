@@ -15,6 +15,7 @@ bounded sample of the same workload. Under torchrun each rank runs an independen
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -182,6 +183,8 @@ def gpu_arm(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     cfg = ql_inputs.QWEN3_8B
+    if args.layers:   # profiling aid: the same layer shapes, fewer layers (not a bench line)
+        cfg = dataclasses.replace(cfg, n_layers=args.layers)
     B = 1 if args.config == "e1" else 32
     steps, warmup = args.steps, args.warmup
     max_ctx = CTX + warmup + steps + 2
@@ -694,6 +697,8 @@ def main():
     ap.add_argument("--impl", default="ql", choices=["ql", "reference"])
     ap.add_argument("--config", default="e1", choices=["e1", "e32"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="profiling aid: run the 8B-shaped step with this many layers (default: all 36)")
     ap.add_argument("--step-kernel", default="auto", choices=["auto", "persistent", "launches"],
                     help="decode step implementation (auto: persistent when the batch allows it)")
     ap.add_argument("--micro", choices=["gemv", "attn"], help="time one kernel family alone")
