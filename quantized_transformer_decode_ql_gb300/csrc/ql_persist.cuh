@@ -130,8 +130,9 @@ static __device__ __noinline__ bool grid_barrier(const PersistParams& p, unsigne
         if (tr) tr[0] = global_ns();
         const unsigned int need = target + p.barrier_extra;
         int ok = 1;
-        __threadfence();
-        atomicAdd(p.sync, 1u);
+        // release: the CTA's writes (ordered before this by the bar.sync above) become visible
+        // to every CTA whose acquire load reads the count
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(p.sync) : "memory");
         for (int spin = 0; spin < kFastSpins && load_acquire(p.sync) < need; ++spin) {
         }
         if (load_acquire(p.sync) < need) {
@@ -153,7 +154,6 @@ static __device__ __noinline__ bool grid_barrier(const PersistParams& p, unsigne
                 }
             }
         }
-        __threadfence();
         if (tr) tr[1] = global_ns();
         *ok_smem = ok;
     }
@@ -269,11 +269,12 @@ __device__ __forceinline__ bool mbar_test(uint32_t mb, uint32_t parity) {
     return done != 0;
 }
 
-// Wait until the unit r.consumed has landed in its slot. Bounded by the clock: when the bound
-// runs out the warp records an error, raises the step's abort flag and stops using the ring.
-__device__ __forceinline__ void ring_wait(Ring& r, const PersistParams& p) {
+// Wait until unit n (n >= r.consumed) has landed in its slot. Bounded by the clock: when the
+// bound runs out the warp records an error, raises the step's abort flag and stops using the
+// ring.
+__device__ __forceinline__ void ring_wait(Ring& r, const PersistParams& p, unsigned int n) {
     if (r.dead) return;
-    const uint32_t mb = r.mbar + (r.consumed % kStages) * 8, parity = (r.consumed / kStages) & 1u;
+    const uint32_t mb = r.mbar + (n % kStages) * 8, parity = (n / kStages) & 1u;
     // fast path without the clock (reading %globaltimer is slow); the clock bounds the rest
     for (int spin = 0; spin < kFastSpins; ++spin)
         if (mbar_test(mb, parity)) return;
@@ -283,7 +284,7 @@ __device__ __forceinline__ void ring_wait(Ring& r, const PersistParams& p) {
         if ((spin & 63u) == 0 && global_ns() - t0 > p.barrier_timeout_ns) break;
     }
     if ((threadIdx.x & 31) == 0) {
-        record_device_error(p.err, kErrGemvStage, blockIdx.x, (long long)r.consumed);
+        record_device_error(p.err, kErrGemvStage, blockIdx.x, (long long)n);
         atomicExch(p.sync + 2, 1u);
     }
     r.dead = 1;
@@ -540,28 +541,27 @@ __device__ __noinline__ void gemv_phase(const PersistParams& p, const PMat* mats
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     int tile = T0 + (u1 > u0 ? u0 / nst : 0), k = u1 > u0 ? u0 % nst : 0;
     const int first_tile = tile;
-#pragma unroll 1
-    for (int u = u0; u < u1; ++u) {
-        ring_wait(r, p);
-        __syncwarp();
-        const unsigned int slot = r.consumed % kStages;
+
+    // codes of rows g / g + 8 of blocks 0..3 (wa0, wb0, wa1, wb1, ...) and the rows' scales
+    auto load_unit = [&](unsigned int slot, uint32_t (&w)[8], uint2& sca, uint2& scb) {
         const uint32_t st = r.base + slot * kUnitBytes;
-        uint32_t w[8];   // rows g / g + 8 of blocks 0..3: wa0, wb0, wa1, wb1, ...
         ldsm_x4(st + a_lo, w[0], w[1], w[2], w[3]);
         ldsm_x4(st + a_lo + 2 * 16 * 16, w[4], w[5], w[6], w[7]);
         const unsigned char* stg = ring_g + (size_t)slot * kUnitBytes;
-        const uint2 sca = *reinterpret_cast<const uint2*>(stg + 1024 + g * 8);
-        const uint2 scb = *reinterpret_cast<const uint2*>(stg + 1024 + (g + 8) * 8);
-        __syncwarp();
-        ++r.consumed;
-        ring_issue(r, mats, warp, lane);   // refill the slot just read
+        sca = *reinterpret_cast<const uint2*>(stg + 1024 + g * 8);
+        scb = *reinterpret_cast<const uint2*>(stg + 1024 + (g + 8) * 8);
+    };
+    // sum over the unit's 4 blocks of d * (offset + MMA): no dependence on acc, so the two units
+    // of an iteration interleave
+    auto unit_partial = [&](const uint32_t (&w)[8], uint2 sca, uint2 scb, int kk, float (&pu)[4]) {
         const float2 da01 = __half22float2(as_h2(sca.x)), da23 = __half22float2(as_h2(sca.y));
         const float2 db01 = __half22float2(as_h2(scb.x)), db23 = __half22float2(as_h2(scb.y));
         const float da[4] = {da01.x, da01.y, da23.x, da23.y};
         const float db[4] = {db01.x, db01.y, db23.x, db23.y};
+        pu[0] = pu[1] = pu[2] = pu[3] = 0.f;
 #pragma unroll
         for (int q = 0; q < kUnitBlocks; ++q) {
-            const int j = k * kUnitBlocks + q;
+            const int j = kk * kUnitBlocks + q;
             const uint32_t wa = w[2 * q], wb = w[2 * q + 1];
             const uint4 X = has_col ? xcol[4 * j + t] : make_uint4(0u, 0u, 0u, 0u);
             const float2 bz = t == 0 ? *reinterpret_cast<const float2*>(bias + 2 * j) : make_float2(0.f, 0.f);
@@ -571,14 +571,20 @@ __device__ __noinline__ void gemv_phase(const PersistParams& p, const PMat* mats
                      (sa8 & 0x000F000Fu) | 0x64006400u, (sb8 & 0x000F000Fu) | 0x64006400u, X.x, X.y);
             mma16816(c, (wa & 0x00F000F0u) | 0x64006400u, (wb & 0x00F000F0u) | 0x64006400u,
                      (sa8 & 0x00F000F0u) | 0x64006400u, (sb8 & 0x00F000F0u) | 0x64006400u, X.z, X.w);
-            acc[0] = fmaf(da[q], c[0], acc[0]);
-            acc[1] = fmaf(da[q], c[1], acc[1]);
-            acc[2] = fmaf(db[q], c[2], acc[2]);
-            acc[3] = fmaf(db[q], c[3], acc[3]);
+            pu[0] = fmaf(da[q], c[0], pu[0]);
+            pu[1] = fmaf(da[q], c[1], pu[1]);
+            pu[2] = fmaf(db[q], c[2], pu[2]);
+            pu[3] = fmaf(db[q], c[3], pu[3]);
         }
+    };
+    // add unit u's partial; at the end of this warp's part of a tile finish the tile if the warp
+    // covered all of it, else park the partial (slot 0: the warp's first tile, slot 1: its last)
+    auto advance = [&](const float (&pu)[4], int u) {
+        acc[0] += pu[0];
+        acc[1] += pu[1];
+        acc[2] += pu[2];
+        acc[3] += pu[3];
         if (++k == nst || u + 1 == u1) {
-            // end of this warp's part of a tile: finish it if the warp covered all of it, else
-            // park the partial (slot 0: the warp's first tile, slot 1: its last)
             const int ts = (tile - T0) * nst;
             if (u0 <= ts && u + 1 == ts + nst)
                 finish_tile<EPI>(p, M, tile, acc, y, ld, best0, best1, lane);
@@ -588,6 +594,33 @@ __device__ __noinline__ void gemv_phase(const PersistParams& p, const PMat* mats
             k = 0;
             ++tile;
         }
+    };
+    // two units per iteration: both waits, both refills, then the two (independent) partials
+#pragma unroll 1
+    for (int u = u0; u < u1; u += 2) {
+        const bool two = u + 1 < u1;   // warp-uniform
+        ring_wait(r, p, r.consumed);
+        if (two) ring_wait(r, p, r.consumed + 1);
+        __syncwarp();
+        uint32_t w0[8], w1[8];
+        uint2 sa0, sb0, sa1 = make_uint2(0u, 0u), sb1 = make_uint2(0u, 0u);
+        load_unit(r.consumed % kStages, w0, sa0, sb0);
+        if (two) {
+            load_unit((r.consumed + 1) % kStages, w1, sa1, sb1);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) w1[i] = 0u;
+        }
+        __syncwarp();
+        r.consumed += two ? 2 : 1;
+        ring_issue(r, mats, warp, lane);   // refill the slots just read
+        if (two) ring_issue(r, mats, warp, lane);
+        const int k1 = k + 1 == nst ? 0 : k + 1;
+        float pa[4], pb[4];
+        unit_partial(w0, sa0, sb0, k, pa);
+        unit_partial(w1, sa1, sb1, k1, pb);
+        advance(pa, u);
+        if (two) advance(pb, u + 1);
     }
     ring = r;
     stamp(tr, 3);
