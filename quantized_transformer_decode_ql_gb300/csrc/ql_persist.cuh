@@ -44,10 +44,12 @@ namespace persist {
 
 constexpr int kW = 16;                  // warps per CTA
 constexpr int kT = kW * 32;             // threads per CTA
-constexpr int kStages = 8;              // ring stages (units in flight) per warp
+constexpr int kStages = 2;              // ring slots per warp
+constexpr int kSlotUnits = 4;           // units per slot (one bulk copy)
 constexpr int kUnitBlocks = 4;          // q4_0 blocks per row in one unit
 constexpr int kUnitBytes = kUnitBlocks * 16 * 16 + 16 * kUnitBlocks * 2;   // 1152
-constexpr int kRingBytes = kW * kStages * kUnitBytes;
+constexpr int kSlotBytes = kSlotUnits * kUnitBytes;
+constexpr int kRingBytes = kW * kStages * kSlotBytes;
 constexpr int kBS = 16;                 // tokens per KV block
 constexpr int kMaxB = kPersistMaxBatch;
 constexpr int kMaxSplit = 256;
@@ -60,7 +62,7 @@ enum Epi { kEpiF32 = 0, kEpiResid = 1, kEpiSilu = 2, kEpiLogits = 3 };
 // Shared memory behind the rings: the GEMV staging (activations, offset terms, partials) or
 // the attention merge buffers, whichever is larger.
 __host__ __device__ constexpr size_t gemv_region_bytes(int batch, int max_nblk) {
-    return (size_t)batch * (max_nblk * 4 + 4) * 16 + (size_t)max_nblk * 2 * 4 + kPartBytes;
+    return (size_t)batch * (max_nblk * 4 + 4) * 16 + kPartBytes;
 }
 __host__ __device__ constexpr size_t attn_region_bytes(int head_dim, int group) {
     return (size_t)kW * (group * head_dim > 128 ? group * head_dim : 128) * 4 + (size_t)2 * kW * group * 4;
@@ -89,13 +91,6 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
         "{%8,%9}, {%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                        uint32_t& r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
 }
 
 // ------------------------------------------------------------------------------ grid barrier
@@ -209,13 +204,15 @@ __device__ __forceinline__ int tile_row(const PMat& M, int tile, int r, bool& ok
 // Issue side of a warp's ring. The matrices are stored in the tile stream layout
 // (stream_pack_kernel): unit (tile, k) is 1152 contiguous bytes at stream + (tile nst + k) 1152,
 // codes [block 0..3][row 0..15] x 16 B, then the 16 rows' 4 scales (8 B each), so a warp's
-// units of one matrix are one contiguous byte range. Lane 0 copies each unit into its ring
-// slot with one bulk copy (TMA, cp.async.bulk) that completes on the slot's mbarrier.
+// units of one matrix are one contiguous byte range. Lane 0 copies up to kSlotUnits units at a
+// time into a ring slot with one bulk copy (TMA, cp.async.bulk) that completes on the slot's
+// mbarrier (a copy never crosses the end of the warp's range in a matrix). A bulk copy costs its
+// issuing warp a fixed time, so copies of several units stream faster than one unit each.
 struct Ring {
-    int wp, nmat;          // matrix of the next unit to issue; nmat = end of the step
+    int wp, nmat;          // matrix of the next copy; nmat = end of the step
     int u, u_end;          // unit (within the warp's range of that matrix) and range end
     const uint8_t* src;    // stream address of unit u
-    unsigned int issued, consumed;   // units; ring slot = count % kStages
+    unsigned int issued, consumed;   // slots; ring slot = count % kStages
     uint32_t base;         // shared-memory address of this warp's ring
     uint32_t mbar;         // shared-memory address of this warp's kStages mbarriers
     int dead;              // a wait ran out: issue and wait no more (the step is aborted)
@@ -239,21 +236,24 @@ __device__ __forceinline__ void ring_seek(Ring& r, const PMat* mats, int warp) {
     }
 }
 
-// Copy the next unit into its ring slot.
+// Copy the next slot's units (up to kSlotUnits, not past the warp's range end).
 __device__ __forceinline__ void ring_issue(Ring& r, const PMat* mats, int warp, int lane) {
     if (r.wp >= r.nmat || r.dead) return;
+    const int n = min(kSlotUnits, r.u_end - r.u);
     if (lane == 0) {
         const unsigned int slot = r.issued % kStages;
-        const uint32_t mb = r.mbar + slot * 8, dst = r.base + slot * kUnitBytes;
+        const uint32_t mb = r.mbar + slot * 8, dst = r.base + slot * kSlotBytes;
+        const uint32_t bytes = (uint32_t)(n * kUnitBytes);
         // order this warp's earlier generic-proxy reads of the slot before the async-proxy write
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mb), "r"(kUnitBytes) : "memory");
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mb), "r"(bytes) : "memory");
         asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                     ::"r"(dst), "l"(r.src), "r"(kUnitBytes), "r"(mb) : "memory");
+                     ::"r"(dst), "l"(r.src), "r"(bytes), "r"(mb) : "memory");
     }
-    r.src += kUnitBytes;
+    r.src += (size_t)n * kUnitBytes;
     ++r.issued;
-    if (++r.u == r.u_end) {
+    r.u += n;
+    if (r.u == r.u_end) {
         ++r.wp;
         ring_seek(r, mats, warp);
     }
@@ -291,21 +291,19 @@ __device__ __forceinline__ void ring_wait(Ring& r, const PersistParams& p, unsig
 }
 
 // ------------------------------------------------------------------------------ GEMV phase
-// Stage the activations of all B columns: per column and block j, 4 chunks of 16 bytes (chunk t
-// feeds MMA lane t: f16 pairs (x0, x2), (x1, x3), (x16, x18)/16, (x17, x19)/16 of elements
-// 32 j + 4 t + ...), plus the accumulator start -(1032 sum x_lo + 1152 sum x_hi/16) of every
-// (block, column). RMS: the input is the f32 residual stream, normalised (RMSNorm with weight
+// Stage the activations of all B columns in f16: per column and block j, 4 chunks of 16 bytes
+// (chunk t: f16 pairs (x0, x2), (x1, x3), (x16, x18)/16, (x17, x19)/16 of elements 32 j + 4 t
+// + ...: the pairs that one 32-bit code word expands to, the high-nibble ones pre-divided by 16,
+// which is exact). RMS: the input is the f32 residual stream, normalised (RMSNorm with weight
 // w) on the way; the first kHeld items of a thread and their weights are loaded together and
 // stay in registers between the two passes. f16 input: kChunk items per thread are loaded
 // together. Data written earlier in the launch by other CTAs is read with ld.global.cg (L2).
 template <bool RMS>
 __device__ __noinline__ void stage_x(const PersistParams& p, int nblk, int cstride, const float* xf,
-                                     const __half* x16, const float* w, uint4* xs, float* bias, float* red) {
+                                     const __half* x16, const float* w, uint4* xs, float* red) {
     constexpr int kHeld = 2, kChunk = 4;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int B = p.B, cols = nblk * 32, nitems = B * nblk * 4;
-    if (B < 2)
-        for (int j = tid; j < nblk; j += kT) bias[2 * j + 1] = 0.f;   // absent second column
 
     // item -> (column b, block j, chunk t) and its element offset
     auto where = [&](int item, int& b, int& j, int& t) -> size_t {
@@ -327,32 +325,16 @@ __device__ __noinline__ void stage_x(const PersistParams& p, int nblk, int cstri
         v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
         v[4] = h.x; v[5] = h.y; v[6] = h.z; v[7] = h.w;
     };
-    // item -> staged chunk and (t == 0) the block's offset term; whole warps call it together
-    // (warp-uniform loop bounds) because of the shuffles
-    auto emit = [&](int item, float (&v)[8]) {
+    auto emit = [&](int item, const float (&v)[8]) {
         int b, j, t;
         where(item, b, j, t);
-        const bool live = item < nitems;
-        if (!live) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = 0.f;
-        }
         const __half2 p0 = __floats2half2_rn(v[0], v[2]);
         const __half2 p1 = __floats2half2_rn(v[1], v[3]);
         const __half2 p2 = __floats2half2_rn(__half2float(__float2half_rn(v[4])) * 0.0625f,
                                              __half2float(__float2half_rn(v[6])) * 0.0625f);
         const __half2 p3 = __floats2half2_rn(__half2float(__float2half_rn(v[5])) * 0.0625f,
                                              __half2float(__float2half_rn(v[7])) * 0.0625f);
-        const float2 f0 = __half22float2(p0), f1 = __half22float2(p1);
-        const float2 f2 = __half22float2(p2), f3 = __half22float2(p3);
-        // sum (1024 + q) x_lo + (1024 + 16 q) x_hi/16 = sum (q - 8) x + 1032 sum x_lo + 1152 sum x_hi/16
-        float part = 1032.0f * ((f0.x + f0.y) + (f1.x + f1.y)) + 1152.0f * ((f2.x + f2.y) + (f3.x + f3.y));
-        part += __shfl_xor_sync(0xffffffffu, part, 1);
-        part += __shfl_xor_sync(0xffffffffu, part, 2);
-        if (live) {
-            xs[(size_t)b * cstride + 4 * j + t] = make_uint4(as_u32(p0), as_u32(p1), as_u32(p2), as_u32(p3));
-            if (t == 0) bias[2 * j + b] = -part;
-        }
+        xs[(size_t)b * cstride + 4 * j + t] = make_uint4(as_u32(p0), as_u32(p1), as_u32(p2), as_u32(p3));
     };
 
     if (RMS) {
@@ -407,9 +389,8 @@ __device__ __noinline__ void stage_x(const PersistParams& p, int nblk, int cstri
         const float rs1 = 1.0f / sqrtf(a1 / (float)cols + p.eps);
 #pragma unroll
         for (int r = 0; r < kHeld; ++r) {
-            const int base = r * kT;
-            if (base < nitems) {
-                const int item = base + tid;
+            const int item = tid + r * kT;
+            if (item < nitems) {
                 const float rr = item < nblk * 4 ? rs0 : rs1;
                 float v[8];
 #pragma unroll
@@ -417,18 +398,14 @@ __device__ __noinline__ void stage_x(const PersistParams& p, int nblk, int cstri
                 emit(item, v);
             }
         }
-        for (int base = kHeld * kT; base < nitems; base += kT) {
-            const int item = base + tid;
-            float v[8];
-            if (item < nitems) {
-                int b, j, t;
-                float wv[8];
-                load_f32(xf, where(item, b, j, t), v);
-                load_w(j, t, wv);
-                const float rr = b == 0 ? rs0 : rs1;
+        for (int item = tid + kHeld * kT; item < nitems; item += kT) {
+            int b, j, t;
+            float v[8], wv[8];
+            load_f32(xf, where(item, b, j, t), v);
+            load_w(j, t, wv);
+            const float rr = b == 0 ? rs0 : rs1;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) v[i] *= rr * wv[i];
-            }
+            for (int i = 0; i < 8; ++i) v[i] *= rr * wv[i];
             emit(item, v);
         }
     } else {
@@ -446,15 +423,11 @@ __device__ __noinline__ void stage_x(const PersistParams& p, int nblk, int cstri
             }
 #pragma unroll
             for (int c = 0; c < kChunk; ++c) {
-                if (base + c * kT < nitems) {
-                    const int item = base + c * kT + tid;
-                    float v[8];
-                    if (item < nitems) {
-                        const float2 f0 = __half22float2(as_h2(ra[c].x)), f1 = __half22float2(as_h2(ra[c].y));
-                        const float2 f2 = __half22float2(as_h2(rh[c].x)), f3 = __half22float2(as_h2(rh[c].y));
-                        v[0] = f0.x; v[1] = f0.y; v[2] = f1.x; v[3] = f1.y;
-                        v[4] = f2.x; v[5] = f2.y; v[6] = f3.x; v[7] = f3.y;
-                    }
+                const int item = base + c * kT + tid;
+                if (item < nitems) {
+                    const float2 f0 = __half22float2(as_h2(ra[c].x)), f1 = __half22float2(as_h2(ra[c].y));
+                    const float2 f2 = __half22float2(as_h2(rh[c].x)), f3 = __half22float2(as_h2(rh[c].y));
+                    const float v[8] = {f0.x, f0.y, f1.x, f1.y, f2.x, f2.y, f3.x, f3.y};
                     emit(item, v);
                 }
             }
@@ -462,64 +435,70 @@ __device__ __noinline__ void stage_x(const PersistParams& p, int nblk, int cstri
     }
 }
 
-// Epilogue of one finished 16-row tile for this lane's fragment: rows g, g + 8 and columns
-// 2t, 2t + 1 (SiLU*up: acc[0..1] = gate row i, acc[2..3] = up row i, i = 8 tile + g).
-template <int EPI>
-__device__ __forceinline__ void finish_tile(const PersistParams& p, const PMat& M, int tile, const float (&acc)[4],
-                                            void* y, int ld, unsigned long long& best0, unsigned long long& best1,
-                                            int lane) {
-    const int g = lane >> 2, t = lane & 3;
-    const int n0 = 2 * t, n1 = n0 + 1;
+// Epilogue of one finished 16-row tile. acc[b] is this lane's half-row sum for column b (row
+// lane & 15 of the tile, blocks of half lane >> 4); the halves are added here, then lanes
+// 0..15 hold rows 0..15 (SiLU*up: rows 0..7 gate, 8..15 the matching up rows). All 32 lanes
+// of the warp call it.
+template <int EPI, int NB>
+__device__ __forceinline__ void finish_tile(const PersistParams& p, const PMat& M, int tile, const float (&acc)[NB],
+                                            void* y, int ld, unsigned long long (&best)[NB], int lane) {
+    float v[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) v[b] = acc[b] + __shfl_xor_sync(0xffffffffu, acc[b], 16);
+    const int hr = lane & 15;
     if (EPI == kEpiSilu) {
-        const int i = tile * 8 + g;
-        if (i < (M.rows >> 1)) {
+        float up[NB];
+#pragma unroll
+        for (int b = 0; b < NB; ++b) up[b] = __shfl_down_sync(0xffffffffu, v[b], 8);
+        const int i = tile * 8 + hr;
+        if (lane < 8 && i < (M.rows >> 1)) {
             __half* act = static_cast<__half*>(y);
-            if (n0 < p.B) act[(size_t)n0 * ld + i] = __float2half_rn(silu(acc[0]) * acc[2]);
-            if (n1 < p.B) act[(size_t)n1 * ld + i] = __float2half_rn(silu(acc[1]) * acc[3]);
+#pragma unroll
+            for (int b = 0; b < NB; ++b) act[(size_t)b * ld + i] = __float2half_rn(silu(v[b]) * up[b]);
         }
         return;
     }
-    float* yf = static_cast<float*>(y);
-    const int ra = tile * 16 + g, rb = ra + 8;
-    auto put = [&](int n, int row, float v, unsigned long long& best) {
-        float* dst = yf + (size_t)n * ld + row;
-        if (EPI == kEpiResid) {
-            *dst = __ldcg(dst) + v;
-        } else {
-            *dst = v;
-            if (EPI == kEpiLogits) {
-                const unsigned long long key = argmax_key(v, row);
-                best = key > best ? key : best;
+    const int row = tile * 16 + hr;
+    if (lane < 16 && row < M.rows) {
+        float* yf = static_cast<float*>(y);
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            float* dst = yf + (size_t)b * ld + row;
+            if (EPI == kEpiResid) {
+                *dst = __ldcg(dst) + v[b];
+            } else {
+                *dst = v[b];
+                if (EPI == kEpiLogits) {
+                    const unsigned long long key = argmax_key(v[b], row);
+                    best[b] = key > best[b] ? key : best[b];
+                }
             }
         }
-    };
-    if (n0 < p.B) {
-        if (ra < M.rows) put(n0, ra, acc[0], best0);
-        if (rb < M.rows) put(n0, rb, acc[2], best0);
-    }
-    if (n1 < p.B) {
-        if (ra < M.rows) put(n1, ra, acc[1], best1);
-        if (rb < M.rows) put(n1, rb, acc[3], best1);
     }
 }
 
-// One GEMV phase of the step: y = epilogue(W x) for this CTA's tiles of M. All threads of the
-// CTA call it. The warp consumes its units from the ring (issuing one unit further for each
-// one consumed), in the order the issue side produced them.
-template <int EPI, bool RMS>
+// One GEMV phase of the step: y = epilogue(W x) for this CTA's tiles of M, NB = batch columns.
+// All threads of the CTA call it. The warp consumes its ring slots in the order the issue side
+// produced them and refills each slot once its units are done. Per unit, lane (row r = lane &
+// 15, half h = lane >> 4) takes blocks 2h, 2h + 1 of row r: one 32-bit code word gives 4 f16
+// pairs (1024 + q and 1024 + 16 q, nibbles OR'ed into the mantissa of 1024.0h), HSUB2 turns them
+// into q - 8 and 16 (q - 8) exactly, HFMA2 accumulates the block's 32 products in f16 (low and
+// high nibbles in separate accumulators), one FFMA per block applies the f16 scale in f32. (The
+// MMA form of the same product wastes 7 of the 8 columns of an m16n8k16 tile at batch 1-2, and
+// measured slower than the CUDA cores here.)
+template <int EPI, bool RMS, int NB>
 __device__ __noinline__ void gemv_phase(const PersistParams& p, const PMat* mats, int wp, Ring& ring, const float* xf,
                                         const __half* x16, const float* norm_w, void* y, int ld,
                                         unsigned char* region, float* red,
                                         unsigned long long (*kred)[kMaxB], unsigned long long* tr) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int g = lane >> 2, t = lane & 3;
+    const int hr = lane & 15, hh = lane >> 4;
     const PMat M = mats[wp];
     const int cstride = p.max_nblk * 4 + 4;   // uint4 units between staged columns (+64 B)
     uint4* xs = reinterpret_cast<uint4*>(region);
-    float* bias = reinterpret_cast<float*>(xs + (size_t)p.B * cstride);   // [nblk][2]
-    float4* part = reinterpret_cast<float4*>(bias + 2 * p.max_nblk);    // [kW][2][32]
+    float4* part = reinterpret_cast<float4*>(xs + (size_t)NB * cstride);   // [kW][2][32]
 
-    stage_x<RMS>(p, M.nblk, cstride, xf, x16, norm_w, xs, bias, red);
+    stage_x<RMS>(p, M.nblk, cstride, xf, x16, norm_w, xs, red);
     __syncthreads();
     stamp(tr, 2);
 
@@ -529,137 +508,134 @@ __device__ __noinline__ void gemv_phase(const PersistParams& p, const PMat* mats
     cta_tiles(M.ntile, T0, T1);
     const int U = (T1 - T0) * nst;
     const int u0 = warp_unit(U, warp), u1 = warp_unit(U, warp + 1);
-    const bool has_col = g < p.B;
-    const uint4* xcol = xs + (size_t)(has_col ? g : 0) * cstride;
-    // ldmatrix row address of this lane: matrix m = lane >> 3 -> (block m >> 1, rows (m & 1) * 8 + r)
-    const int lm = lane >> 3, lrow = lane & 7;
-    const uint32_t a_lo = (uint32_t)(((lm >> 1) * 16 + (lm & 1) * 8 + lrow) * 16);
     const unsigned char* ring_g = reinterpret_cast<const unsigned char*>(region) - kRingBytes +
-                                  (size_t)warp * kStages * kUnitBytes;
+                                  (size_t)warp * kStages * kSlotBytes;
 
-    unsigned long long best0 = 0ull, best1 = 0ull;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    unsigned long long best[NB];
+    float acc[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+        best[b] = 0ull;
+        acc[b] = 0.f;
+    }
     int tile = T0 + (u1 > u0 ? u0 / nst : 0), k = u1 > u0 ? u0 % nst : 0;
     const int first_tile = tile;
 
-    // codes of rows g / g + 8 of blocks 0..3 (wa0, wb0, wa1, wb1, ...) and the rows' scales
-    auto load_unit = [&](unsigned int slot, uint32_t (&w)[8], uint2& sca, uint2& scb) {
-        const uint32_t st = r.base + slot * kUnitBytes;
-        ldsm_x4(st + a_lo, w[0], w[1], w[2], w[3]);
-        ldsm_x4(st + a_lo + 2 * 16 * 16, w[4], w[5], w[6], w[7]);
-        const unsigned char* stg = ring_g + (size_t)slot * kUnitBytes;
-        sca = *reinterpret_cast<const uint2*>(stg + 1024 + g * 8);
-        scb = *reinterpret_cast<const uint2*>(stg + 1024 + (g + 8) * 8);
-    };
-    // sum over the unit's 4 blocks of d * (offset + MMA): no dependence on acc, so the two units
-    // of an iteration interleave
-    auto unit_partial = [&](const uint32_t (&w)[8], uint2 sca, uint2 scb, int kk, float (&pu)[4]) {
-        const float2 da01 = __half22float2(as_h2(sca.x)), da23 = __half22float2(as_h2(sca.y));
-        const float2 db01 = __half22float2(as_h2(scb.x)), db23 = __half22float2(as_h2(scb.y));
-        const float da[4] = {da01.x, da01.y, da23.x, da23.y};
-        const float db[4] = {db01.x, db01.y, db23.x, db23.y};
-        pu[0] = pu[1] = pu[2] = pu[3] = 0.f;
+    // this lane's share of one unit (group kk of the tile): sum over blocks 2h, 2h + 1 of row r
+    auto unit = [&](const unsigned char* stg, int kk, float (&pu)[NB]) {
+        const uint4 c0 = *reinterpret_cast<const uint4*>(stg + ((2 * hh) * 16 + hr) * 16);
+        const uint4 c1 = *reinterpret_cast<const uint4*>(stg + ((2 * hh + 1) * 16 + hr) * 16);
+        const uint32_t sc = *reinterpret_cast<const uint32_t*>(stg + kUnitBlocks * 16 * 16 + hr * 8 + 4 * hh);
+        const float2 d = __half22float2(as_h2(sc));
+        const __half2 off_lo = as_h2(0x64086408u), off_hi = as_h2(0x64806480u);   // 1032, 1152
 #pragma unroll
-        for (int q = 0; q < kUnitBlocks; ++q) {
-            const int j = kk * kUnitBlocks + q;
-            const uint32_t wa = w[2 * q], wb = w[2 * q + 1];
-            const uint4 X = has_col ? xcol[4 * j + t] : make_uint4(0u, 0u, 0u, 0u);
-            const float2 bz = t == 0 ? *reinterpret_cast<const float2*>(bias + 2 * j) : make_float2(0.f, 0.f);
-            float c[4] = {bz.x, bz.y, bz.x, bz.y};
-            const uint32_t sa8 = wa >> 8, sb8 = wb >> 8;
-            mma16816(c, (wa & 0x000F000Fu) | 0x64006400u, (wb & 0x000F000Fu) | 0x64006400u,
-                     (sa8 & 0x000F000Fu) | 0x64006400u, (sb8 & 0x000F000Fu) | 0x64006400u, X.x, X.y);
-            mma16816(c, (wa & 0x00F000F0u) | 0x64006400u, (wb & 0x00F000F0u) | 0x64006400u,
-                     (sa8 & 0x00F000F0u) | 0x64006400u, (sb8 & 0x00F000F0u) | 0x64006400u, X.z, X.w);
-            pu[0] = fmaf(da[q], c[0], pu[0]);
-            pu[1] = fmaf(da[q], c[1], pu[1]);
-            pu[2] = fmaf(db[q], c[2], pu[2]);
-            pu[3] = fmaf(db[q], c[3], pu[3]);
+        for (int b = 0; b < NB; ++b) pu[b] = 0.f;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const uint4 cw = e ? c1 : c0;
+            const uint32_t ws[4] = {cw.x, cw.y, cw.z, cw.w};
+            const int j = kk * kUnitBlocks + 2 * hh + e;
+            __half2 alo[NB], ahi[NB];
+#pragma unroll
+            for (int b = 0; b < NB; ++b) alo[b] = ahi[b] = as_h2(0u);
+#pragma unroll
+            for (int tt = 0; tt < 4; ++tt) {
+                const uint32_t w = ws[tt], w8 = w >> 8;
+                const __half2 q0 = __hsub2(as_h2((w & 0x000F000Fu) | 0x64006400u), off_lo);
+                const __half2 q1 = __hsub2(as_h2((w8 & 0x000F000Fu) | 0x64006400u), off_lo);
+                const __half2 q2 = __hsub2(as_h2((w & 0x00F000F0u) | 0x64006400u), off_hi);
+                const __half2 q3 = __hsub2(as_h2((w8 & 0x00F000F0u) | 0x64006400u), off_hi);
+#pragma unroll
+                for (int b = 0; b < NB; ++b) {
+                    const uint4 X = xs[(size_t)b * cstride + 4 * j + tt];
+                    alo[b] = __hfma2(q0, as_h2(X.x), alo[b]);
+                    alo[b] = __hfma2(q1, as_h2(X.y), alo[b]);
+                    ahi[b] = __hfma2(q2, as_h2(X.z), ahi[b]);
+                    ahi[b] = __hfma2(q3, as_h2(X.w), ahi[b]);
+                }
+            }
+            const float de = e ? d.y : d.x;
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                const float2 fl = __half22float2(alo[b]), fh = __half22float2(ahi[b]);
+                pu[b] = fmaf(de, (fl.x + fl.y) + (fh.x + fh.y), pu[b]);
+            }
         }
     };
-    // add unit u's partial; at the end of this warp's part of a tile finish the tile if the warp
-    // covered all of it, else park the partial (slot 0: the warp's first tile, slot 1: its last)
-    auto advance = [&](const float (&pu)[4], int u) {
-        acc[0] += pu[0];
-        acc[1] += pu[1];
-        acc[2] += pu[2];
-        acc[3] += pu[3];
+    // add unit u's share; at the end of this warp's part of a tile finish the tile if the warp
+    // covered all of it, else park the shares (slot 0: the warp's first tile, slot 1: its last)
+    auto advance = [&](const float (&pu)[NB], int u) {
+#pragma unroll
+        for (int b = 0; b < NB; ++b) acc[b] += pu[b];
         if (++k == nst || u + 1 == u1) {
             const int ts = (tile - T0) * nst;
-            if (u0 <= ts && u + 1 == ts + nst)
-                finish_tile<EPI>(p, M, tile, acc, y, ld, best0, best1, lane);
-            else
-                part[(warp * 2 + (tile == first_tile ? 0 : 1)) * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-            acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+            if (u0 <= ts && u + 1 == ts + nst) {
+                finish_tile<EPI, NB>(p, M, tile, acc, y, ld, best, lane);
+            } else {
+                float4 v = make_float4(acc[0], 0.f, 0.f, 0.f);
+                if (NB > 1) v.y = acc[NB > 1 ? 1 : 0];
+                part[(warp * 2 + (tile == first_tile ? 0 : 1)) * 32 + lane] = v;
+            }
+#pragma unroll
+            for (int b = 0; b < NB; ++b) acc[b] = 0.f;
             k = 0;
             ++tile;
         }
     };
-    // two units per iteration: both waits, both refills, then the two (independent) partials
 #pragma unroll 1
-    for (int u = u0; u < u1; u += 2) {
-        const bool two = u + 1 < u1;   // warp-uniform
+    for (int u = u0; u < u1;) {
+        const int n = min(kSlotUnits, u1 - u);   // the units of this slot (as issued)
         ring_wait(r, p, r.consumed);
-        if (two) ring_wait(r, p, r.consumed + 1);
         __syncwarp();
-        uint32_t w0[8], w1[8];
-        uint2 sa0, sb0, sa1 = make_uint2(0u, 0u), sb1 = make_uint2(0u, 0u);
-        load_unit(r.consumed % kStages, w0, sa0, sb0);
-        if (two) {
-            load_unit((r.consumed + 1) % kStages, w1, sa1, sb1);
-        } else {
+        const unsigned char* sg = ring_g + (size_t)(r.consumed % kStages) * kSlotBytes;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) w1[i] = 0u;
+        for (int i = 0; i < kSlotUnits; ++i) {
+            if (i < n) {
+                float pu[NB];
+                unit(sg + i * kUnitBytes, k, pu);
+                advance(pu, u + i);
+            }
         }
         __syncwarp();
-        r.consumed += two ? 2 : 1;
-        ring_issue(r, mats, warp, lane);   // refill the slots just read
-        if (two) ring_issue(r, mats, warp, lane);
-        const int k1 = k + 1 == nst ? 0 : k + 1;
-        float pa[4], pb[4];
-        unit_partial(w0, sa0, sb0, k, pa);
-        unit_partial(w1, sa1, sb1, k1, pb);
-        advance(pa, u);
-        if (two) advance(pb, u + 1);
+        ++r.consumed;
+        ring_issue(r, mats, warp, lane);   // refill the slot just read
+        u += n;
     }
     ring = r;
     stamp(tr, 3);
     __syncthreads();
     stamp(tr, 4);
-    // A tile shared by several warps is finished by the warp holding its last unit: the partials
+    // A tile shared by several warps is finished by the warp holding its last unit: the shares
     // of every warp that touched it, summed in warp order.
     if (u1 > u0) {
         const int ts = (first_tile - T0) * nst;
         if (u0 > ts && u1 >= ts + nst) {
-            float s[4] = {0.f, 0.f, 0.f, 0.f};
+            float s2[NB];
+#pragma unroll
+            for (int b = 0; b < NB; ++b) s2[b] = 0.f;
             for (int w2 = 0; w2 <= warp; ++w2) {
                 const int a0 = warp_unit(U, w2), a1 = warp_unit(U, w2 + 1);
                 if (a1 <= a0 || a1 <= ts || a0 >= ts + nst) continue;
                 const int sl = (T0 + a0 / nst == first_tile) ? 0 : 1;
                 const float4 v = part[(w2 * 2 + sl) * 32 + lane];
-                s[0] += v.x;
-                s[1] += v.y;
-                s[2] += v.z;
-                s[3] += v.w;
+                s2[0] += v.x;
+                if (NB > 1) s2[NB > 1 ? 1 : 0] += v.y;
             }
-            finish_tile<EPI>(p, M, first_tile, s, y, ld, best0, best1, lane);
+            finish_tile<EPI, NB>(p, M, first_tile, s2, y, ld, best, lane);
         }
     }
     if (EPI == kEpiLogits) {
-        // lane t = 0 holds columns 0 and 1: reduce over the 8 row groups, then over the warps
 #pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
-            const unsigned long long k0 = __shfl_xor_sync(0xffffffffu, best0, o);
-            const unsigned long long k1 = __shfl_xor_sync(0xffffffffu, best1, o);
-            best0 = k0 > best0 ? k0 : best0;
-            best1 = k1 > best1 ? k1 : best1;
-        }
-        if (lane == 0) {
-            kred[warp][0] = best0;
-            kred[warp][1] = best1;
+        for (int b = 0; b < NB; ++b) {
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned long long k2 = __shfl_xor_sync(0xffffffffu, best[b], o);
+                best[b] = k2 > best[b] ? k2 : best[b];
+            }
+            if (lane == 0) kred[warp][b] = best[b];
         }
         __syncthreads();
-        if (tid < p.B) {
+        if (tid < NB) {
             unsigned long long m = 0ull;
 #pragma unroll
             for (int i = 0; i < kW; ++i) m = kred[i][tid] > m ? kred[i][tid] : m;
@@ -1029,7 +1005,7 @@ __device__ void attn_prefetch(const PersistParams& p, int layer) {
     }
 }
 
-template <int HD, int G>
+template <int HD, int G, int NB>
 __device__ void step_body(const PersistParams& p, const PMat* mats, Ring& r, unsigned char* region, __half (*qs)[HD],
                           float* red, unsigned long long (*kred)[kMaxB], int* flag) {
     unsigned int target = 0;
@@ -1044,28 +1020,28 @@ __device__ void step_body(const PersistParams& p, const PMat* mats, Ring& r, uns
         const PLayer* Ly = p.layers + l;
         attn_prefetch<HD>(p, l);
         // q|k|v = W_qkv rmsnorm(x, attn_norm)
-        gemv_phase<kEpiF32, true>(p, mats, 4 * l, r, p.x, nullptr, Ly->attn_norm, p.qkv, qkv_ld, region, red, kred,
-                                  row());
+        gemv_phase<kEpiF32, true, NB>(p, mats, 4 * l, r, p.x, nullptr, Ly->attn_norm, p.qkv, qkv_ld, region, red,
+                                      kred, row());
         if (!grid_barrier(p, target, flag)) return;
         // qk-norm + RoPE + KV append + paged attention -> attn
         attn_phase<HD, G>(p, l, region, qs, flag, row());
         if (!grid_barrier(p, target, flag)) return;
         // x += W_o attn
-        gemv_phase<kEpiResid, false>(p, mats, 4 * l + 1, r, nullptr, p.attn, nullptr, p.x, p.hidden, region, red,
-                                     kred, row());
+        gemv_phase<kEpiResid, false, NB>(p, mats, 4 * l + 1, r, nullptr, p.attn, nullptr, p.x, p.hidden, region, red,
+                                         kred, row());
         if (!grid_barrier(p, target, flag)) return;
         // act = silu(gate) * up, [gate | up] = W_gu rmsnorm(x, ffn_norm)
-        gemv_phase<kEpiSilu, true>(p, mats, 4 * l + 2, r, p.x, nullptr, Ly->ffn_norm, p.act, p.inter, region, red,
-                                   kred, row());
+        gemv_phase<kEpiSilu, true, NB>(p, mats, 4 * l + 2, r, p.x, nullptr, Ly->ffn_norm, p.act, p.inter, region, red,
+                                       kred, row());
         if (!grid_barrier(p, target, flag)) return;
         // x += W_down act
-        gemv_phase<kEpiResid, false>(p, mats, 4 * l + 3, r, nullptr, p.act, nullptr, p.x, p.hidden, region, red,
-                                     kred, row());
+        gemv_phase<kEpiResid, false, NB>(p, mats, 4 * l + 3, r, nullptr, p.act, nullptr, p.x, p.hidden, region, red,
+                                         kred, row());
         if (!grid_barrier(p, target, flag)) return;
     }
     // logits = W_lm rmsnorm(x, final_norm), greedy argmax keys
-    gemv_phase<kEpiLogits, true>(p, mats, 4 * p.n_layers, r, p.x, nullptr, p.final_norm, p.logits, p.vocab, region,
-                                 red, kred, row());
+    gemv_phase<kEpiLogits, true, NB>(p, mats, 4 * p.n_layers, r, p.x, nullptr, p.final_norm, p.logits, p.vocab, region,
+                                     red, kred, row());
     if (!grid_barrier(p, target, flag)) return;
     if (blockIdx.x == 0) finalize(p);
 }
@@ -1106,13 +1082,16 @@ __global__ void __launch_bounds__(kT, 1) step_kernel(const __grid_constant__ Per
     r.src = nullptr;
     r.issued = r.consumed = 0;
     r.dead = 0;
-    r.base = static_cast<uint32_t>(__cvta_generic_to_shared(smem)) + (uint32_t)(warp * kStages * kUnitBytes);
+    r.base = static_cast<uint32_t>(__cvta_generic_to_shared(smem)) + (uint32_t)(warp * kStages * kSlotBytes);
     r.mbar = static_cast<uint32_t>(__cvta_generic_to_shared(&mbar[warp * kStages]));
     ring_seek(r, mats, warp);
     // the weights do not depend on anything computed in the step: start streaming at once
 #pragma unroll 1
     for (int i = 0; i < kStages; ++i) ring_issue(r, mats, warp, lane);
-    step_body<HD, G>(p, mats, r, region, qs, red, kred, &flag);
+    if (p.B == 1)
+        step_body<HD, G, 1>(p, mats, r, region, qs, red, kred, &flag);
+    else
+        step_body<HD, G, 2>(p, mats, r, region, qs, red, kred, &flag);
     // after an early exit, let this warp's copies still in flight land before leaving (bounded:
     // past the bound the CTA leaves anyway)
     const unsigned long long t0 = global_ns();
