@@ -692,14 +692,21 @@ template <> struct VRow<4> {
 
 // Attention of one layer for every (sequence, kv head, split) item; item i runs on CTA
 // i mod gridDim.x. Splits: the sequence's blocks are cut into nsplit ranges of spb blocks; the
-// range holding the newest position also normalises, rotates and appends the new K/V first.
+// range holding the newest position also normalises, rotates and appends the new K/V. Each warp
+// issues the loads of its first block before anything else (the new row, not yet in the pool
+// then, is patched in from shared memory), so the K/V latency overlaps the q normalisation.
 template <int HD, int G>
 __device__ __noinline__ void attn_phase(const PersistParams& p, int layer, unsigned char* region,
                                         __half (*qs)[HD], int* flag, unsigned long long* tr) {
     constexpr int NCH = HD / 32;   // 32-dim chunks of a K row (one 16-byte load per lane each)
     constexpr int DPL = HD / 32;   // P.V output dims per lane
     constexpr int WST = G * HD > 128 ? G * HD : 128;   // floats per warp in the merge buffer
+    constexpr int ITEMS = G * HD / 4;                   // float4 outputs of a split merge
+    constexpr int TPI = kT / ITEMS;                     // threads per output in the split merge
+    static_assert(TPI >= 1 && TPI <= 32 && (TPI & (TPI - 1)) == 0, "split merge layout");
     using VT = typename VRow<DPL>::T;
+    __shared__ __align__(16) __half knew[HD];   // the appended K row (normed, rotated) and V row
+    __shared__ __align__(16) __half vnew[HD];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t = lane & 3;
     float* wacc = reinterpret_cast<float*>(region);   // [kW][WST] (first [G][16]: probabilities)
@@ -726,35 +733,66 @@ __device__ __noinline__ void attn_phase(const PersistParams& p, int layer, unsig
         const int n_active = (nblocks + spb - 1) / spb;
         if (s >= n_active) continue;
         const int blk0 = s * spb, blk1 = min(nblocks, blk0 + spb);
-        __syncthreads();   // the previous item's readers of qs and the merge buffers are done
+        const int lblk = pos / kBS, kp = pos % kBS;
+        const int32_t* bt = p.block_tables + (size_t)b * p.maxb;
+        __syncthreads();   // the previous item's readers of qs, knew/vnew and the merge buffers are done
+
+        // K/V of block blk straight into registers: K as MMA B fragments (key g and g + 8 of
+        // the block, head_dim permuted: lane t of chunk m holds dims 32 m + 8 t .. + 7), V rows
+        // as DPL dims per lane; false (error recorded) if the table entry is out of range
+        uint4 k0[NCH], k1[NCH];
+        VT vv[kBS];
+        auto load_block = [&](int blk) -> bool {
+            const int phys = bt[blk];
+            if (phys < 0 || phys >= p.num_blocks) {
+                if (lane == 0) record_device_error(p.err, kErrAttnBlock, (long long)b * p.maxb + blk, phys);
+                return false;
+            }
+            const __half* kb = kpool + ((size_t)phys * p.nkv + kvh) * kBS * HD;
+            const __half* vb = vpool + ((size_t)phys * p.nkv + kvh) * kBS * HD;
+            const int nt = min(kBS, L - blk * kBS);
+#pragma unroll
+            for (int m = 0; m < NCH; ++m) {
+                k0[m] = __ldcg(reinterpret_cast<const uint4*>(kb + (size_t)g * HD + 32 * m + 8 * t));
+                k1[m] = __ldcg(reinterpret_cast<const uint4*>(kb + (size_t)(g + 8) * HD + 32 * m + 8 * t));
+            }
+#pragma unroll
+            for (int kk = 0; kk < kBS; ++kk)
+                if (kk < nt) vv[kk] = __ldcg(reinterpret_cast<const VT*>(vb + (size_t)kk * HD + lane * DPL));
+            return true;
+        };
+        bool okA = blk0 + warp < blk1 ? load_block(blk0 + warp) : false;
 
         const float* src = p.qkv + (size_t)b * qkv_ld;
         const float* cr = p.cos_t + (size_t)pos * (HD / 2);
         const float* sr = p.sin_t + (size_t)pos * (HD / 2);
         if (warp < G) norm_rope<HD>(src + (size_t)(kvh * G + warp) * HD, Ly.q_norm, cr, sr, p.eps, qs[warp], lane);
-        const int lblk = pos / kBS;
         if (lblk >= blk0 && lblk < blk1 && warp >= kW - 2) {
-            const int phys = p.block_tables[(size_t)b * p.maxb + lblk];
+            const int phys = bt[lblk];
             if (phys < 0 || phys >= p.num_blocks) {
                 if (lane == 0 && warp == kW - 1)
                     record_device_error(p.err, kErrRopeBlock, (long long)b * p.maxb + lblk, phys);
             } else {
-                const size_t off = (((size_t)phys * p.nkv + kvh) * kBS + (pos % kBS)) * HD;
+                const size_t off = (((size_t)phys * p.nkv + kvh) * kBS + kp) * HD;
                 if (warp == kW - 1) {
-                    norm_rope<HD>(src + (size_t)(p.nh + kvh) * HD, Ly.k_norm, cr, sr, p.eps, kpool + off, lane);
+                    norm_rope<HD>(src + (size_t)(p.nh + kvh) * HD, Ly.k_norm, cr, sr, p.eps, knew, lane);
+                    __syncwarp();
+                    for (int i = lane; i < HD / 8; i += 32)
+                        reinterpret_cast<uint4*>(kpool + off)[i] = reinterpret_cast<const uint4*>(knew)[i];
                 } else {
                     const float* vs = src + (size_t)(p.nh + p.nkv + kvh) * HD;
-                    for (int i = lane; i < HD; i += 32) vpool[off + i] = __float2half_rn(__ldcg(vs + i));
+                    for (int i = lane; i < HD; i += 32) {
+                        const __half v = __float2half_rn(__ldcg(vs + i));
+                        vnew[i] = v;
+                        vpool[off + i] = v;
+                    }
                 }
             }
         }
-        __threadfence_block();   // the new K/V row is read by this CTA only
-        __syncthreads();
+        __syncthreads();   // qs, knew and vnew are complete
         stamp(tr, 2);
 
-        // Q as the A operand of S = Q K^T (rows = the G heads, rows >= G zero). head_dim is
-        // permuted: in k-steps 2m, 2m + 1 lane t holds dims 32 m + 8 t + {0,1 | 2,3} and
-        // {4,5 | 6,7}, so both Q and K fragments come from one 16-byte load per chunk.
+        // Q as the A operand of S = Q K^T (rows = the G heads, rows >= G zero), permuted like K
         uint4 qf[NCH];
 #pragma unroll
         for (int m = 0; m < NCH; ++m)
@@ -766,28 +804,22 @@ __device__ __noinline__ void attn_phase(const PersistParams& p, int layer, unsig
             for (int d = 0; d < DPL; ++d) o[h][d] = 0.f;
         float mrun = -INFINITY, lrun = 0.f;   // running max / sum of head g (lanes g < G)
         float* pb = wacc + warp * WST;
-        const int32_t* bt = p.block_tables + (size_t)b * p.maxb;
         bool any = false;
-        for (int blk = blk0 + warp; blk < blk1; blk += kW) {
-            const int phys = bt[blk];
-            if (phys < 0 || phys >= p.num_blocks) {
-                if (lane == 0) record_device_error(p.err, kErrAttnBlock, (long long)b * p.maxb + blk, phys);
-                continue;
-            }
+        for (int blk = blk0 + warp, i = 0; blk < blk1; blk += kW, ++i) {
+            const bool ok = i == 0 ? okA : load_block(blk);
+            if (!ok) continue;
             any = true;
-            const __half* kb = kpool + ((size_t)phys * p.nkv + kvh) * kBS * HD;
-            const __half* vb = vpool + ((size_t)phys * p.nkv + kvh) * kBS * HD;
             const int nt = min(kBS, L - blk * kBS);   // valid keys of the block
-            uint4 k0[NCH], k1[NCH];
+            if (blk == lblk) {   // the appended row (its pool copy may postdate the loads above)
 #pragma unroll
-            for (int m = 0; m < NCH; ++m) {
-                k0[m] = __ldcg(reinterpret_cast<const uint4*>(kb + (size_t)g * HD + 32 * m + 8 * t));
-                k1[m] = __ldcg(reinterpret_cast<const uint4*>(kb + (size_t)(g + 8) * HD + 32 * m + 8 * t));
+                for (int m = 0; m < NCH; ++m) {
+                    if (g == kp) k0[m] = *reinterpret_cast<const uint4*>(&knew[32 * m + 8 * t]);
+                    if (g + 8 == kp) k1[m] = *reinterpret_cast<const uint4*>(&knew[32 * m + 8 * t]);
+                }
+#pragma unroll
+                for (int kk = 0; kk < kBS; ++kk)
+                    if (kk == kp) vv[kk] = *reinterpret_cast<const VT*>(&vnew[lane * DPL]);
             }
-            VT vv[kBS];
-#pragma unroll
-            for (int kk = 0; kk < kBS; ++kk)
-                if (kk < nt) vv[kk] = __ldcg(reinterpret_cast<const VT*>(vb + (size_t)kk * HD + lane * DPL));
             float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int m = 0; m < NCH; ++m) {
@@ -888,60 +920,79 @@ __device__ __noinline__ void attn_phase(const PersistParams& p, int layer, unsig
         }
         if (n_active == 1) continue;
 
-        // split merge in the CTA that arrives last (no waiting)
-        __threadfence();
+        // split merge in the CTA that arrives last (no waiting): an acq_rel ticket publishes
+        // this CTA's partials (ordered before it by the bar.sync) and, for the last CTA, makes
+        // every other CTA's partials visible
         __syncthreads();
-        if (tid == 0) *flag = atomicAdd(p.tickets + b * p.nkv + kvh, 1) == n_active - 1;
+        if (tid == 0) {
+            unsigned int old;
+            asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                         : "=r"(old)
+                         : "l"(p.tickets + b * p.nkv + kvh)
+                         : "memory");
+            *flag = (int)old == n_active - 1;
+        }
         __syncthreads();
         stamp(tr, 4);
         if (!*flag) continue;
-        __threadfence();
-        float* sw = wacc;   // [G][kMaxSplit] weights exp2(m_k - M) / L
-        for (int h = warp; h < G; h += kW) {
-            const size_t base = ((size_t)b * p.nh + kvh * G + h) * p.nsplit;
-            float M = -INFINITY;
-            for (int k = lane; k < n_active; k += 32) M = fmaxf(M, __ldcg(p.pm + base + k));
-#pragma unroll
-            for (int o2 = 16; o2; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
-            float Ls = 0.f;
-            for (int k = lane; k < n_active; k += 32) {
-                const float f = exp2f(__ldcg(p.pm + base + k) - M);
-                sw[h * kMaxSplit + k] = f;
-                Ls += f * __ldcg(p.pl + base + k);
-            }
-#pragma unroll
-            for (int o2 = 16; o2; o2 >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o2);
-            const float inv = 1.0f / Ls;
-            __syncwarp();
-            for (int k = lane; k < n_active; k += 32) sw[h * kMaxSplit + k] *= inv;
-        }
-        __syncthreads();
-        for (int i = tid; i < G * HD / 4; i += kT) {
-            const int h = i / (HD / 4), d4 = i - h * (HD / 4);
+        // TPI threads per float4 output, each over splits sub, sub + TPI, ... (online softmax),
+        // all loads of a thread issued together; the TPI states are then combined by shuffles
+        {
+            const int it = tid / TPI, sub = tid % TPI;
+            const int h = it / (HD / 4), d4 = it - h * (HD / 4);
             const size_t base = ((size_t)b * p.nh + kvh * G + h) * p.nsplit;
             const float4* srcp = reinterpret_cast<const float4*>(p.pacc) + base * (HD / 4) + d4;
+            float M = -INFINITY, Ls = 0.f;
             float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
-            int k = 0;
-            for (; k + 4 <= n_active; k += 4) {
-                float4 v[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) v[u] = __ldcg(srcp + (size_t)(k + u) * (HD / 4));
+            for (int k0s = sub; k0s < n_active; k0s += 4 * TPI) {
+                float mk[4], lk[4];
+                float4 ak[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    const float wgt = sw[h * kMaxSplit + k + u];
-                    A.x = fmaf(wgt, v[u].x, A.x); A.y = fmaf(wgt, v[u].y, A.y);
-                    A.z = fmaf(wgt, v[u].z, A.z); A.w = fmaf(wgt, v[u].w, A.w);
+                    const int k = k0s + u * TPI;
+                    if (k < n_active) {
+                        mk[u] = __ldcg(p.pm + base + k);
+                        lk[u] = __ldcg(p.pl + base + k);
+                        ak[u] = __ldcg(srcp + (size_t)k * (HD / 4));
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int k = k0s + u * TPI;
+                    if (k < n_active && mk[u] != -INFINITY) {
+                        const float mn = fmaxf(M, mk[u]);
+                        const float fo = exp2f(M - mn), fk = exp2f(mk[u] - mn);
+                        Ls = Ls * fo + lk[u] * fk;
+                        A.x = A.x * fo + ak[u].x * fk; A.y = A.y * fo + ak[u].y * fk;
+                        A.z = A.z * fo + ak[u].z * fk; A.w = A.w * fo + ak[u].w * fk;
+                        M = mn;
+                    }
                 }
             }
-            for (; k < n_active; ++k) {
-                const float4 v = __ldcg(srcp + (size_t)k * (HD / 4));
-                const float wgt = sw[h * kMaxSplit + k];
-                A.x = fmaf(wgt, v.x, A.x); A.y = fmaf(wgt, v.y, A.y);
-                A.z = fmaf(wgt, v.z, A.z); A.w = fmaf(wgt, v.w, A.w);
+#pragma unroll
+            for (int o2 = 1; o2 < TPI; o2 <<= 1) {
+                const float Mo = __shfl_xor_sync(0xffffffffu, M, o2);
+                const float Lo = __shfl_xor_sync(0xffffffffu, Ls, o2);
+                float4 Ao;
+                Ao.x = __shfl_xor_sync(0xffffffffu, A.x, o2);
+                Ao.y = __shfl_xor_sync(0xffffffffu, A.y, o2);
+                Ao.z = __shfl_xor_sync(0xffffffffu, A.z, o2);
+                Ao.w = __shfl_xor_sync(0xffffffffu, A.w, o2);
+                const float mn = fmaxf(M, Mo);
+                if (mn != -INFINITY) {
+                    const float fa = exp2f(M - mn), fb = exp2f(Mo - mn);
+                    Ls = Ls * fa + Lo * fb;
+                    A.x = A.x * fa + Ao.x * fb; A.y = A.y * fa + Ao.y * fb;
+                    A.z = A.z * fa + Ao.z * fb; A.w = A.w * fa + Ao.w * fb;
+                    M = mn;
+                }
             }
-            __half* out = p.attn + ((size_t)b * p.nh + kvh * G + h) * HD + d4 * 4;
-            *reinterpret_cast<__half2*>(out) = __floats2half2_rn(A.x, A.y);
-            *reinterpret_cast<__half2*>(out + 2) = __floats2half2_rn(A.z, A.w);
+            if (sub == 0) {
+                const float inv = 1.0f / Ls;
+                __half* out = p.attn + ((size_t)b * p.nh + kvh * G + h) * HD + d4 * 4;
+                *reinterpret_cast<__half2*>(out) = __floats2half2_rn(A.x * inv, A.y * inv);
+                *reinterpret_cast<__half2*>(out + 2) = __floats2half2_rn(A.z * inv, A.w * inv);
+            }
         }
         if (tid == 0) p.tickets[b * p.nkv + kvh] = 0;   // re-arm for the next layer / step
         stamp(tr, 5);
