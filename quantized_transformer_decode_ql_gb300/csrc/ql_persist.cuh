@@ -56,7 +56,6 @@ constexpr int kMaxSplit = 256;
 constexpr int kPartBytes = kW * 2 * 32 * 16;   // per-warp partial fragments of shared tiles
 constexpr int kTraceWords = 8;                 // trace entries per (row, CTA)
 constexpr int kFastSpins = 4096;               // polls of a wait before its clock starts
-constexpr int kLookaheadBytes = 24 * 1024;     // L2 prefetch of the next matrix, per warp
 
 enum Epi { kEpiF32 = 0, kEpiResid = 1, kEpiSilu = 2, kEpiLogits = 3 };
 
@@ -257,26 +256,6 @@ __device__ __forceinline__ void ring_issue(Ring& r, const PMat* mats, int warp, 
     if (r.u == r.u_end) {
         ++r.wp;
         ring_seek(r, mats, warp);
-    }
-}
-
-// Ask L2 for this warp's units of matrix wp (at most kLookaheadBytes): issued when a phase
-// starts, while HBM would otherwise idle (the rings are full during staging and barriers), so
-// the ring copies of the next phase find most of their units in L2. A hint only.
-__device__ __forceinline__ void prefetch_matrix(const PMat* mats, int wp, int nmat, int warp, int lane) {
-    if (wp >= nmat || lane != 0) return;
-    const PMat& M = mats[wp];
-    int t0, t1;
-    cta_tiles(M.ntile, t0, t1);
-    const int nst = M.nblk / kUnitBlocks;
-    const int U = (t1 - t0) * nst;
-    const int u0 = warp_unit(U, warp), u1 = warp_unit(U, warp + 1);
-    const uint8_t* a = M.stream + ((size_t)t0 * nst + u0) * kUnitBytes;
-    size_t bytes = (size_t)(u1 - u0) * kUnitBytes;
-    bytes = bytes < (size_t)kLookaheadBytes ? bytes : (size_t)kLookaheadBytes;
-    for (size_t off = 0; off < bytes; off += 8192) {
-        const uint32_t n = (uint32_t)(bytes - off < 8192 ? bytes - off : 8192);
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a + off), "r"(n) : "memory");
     }
 }
 
@@ -519,7 +498,6 @@ __device__ __noinline__ void gemv_phase(const PersistParams& p, const PMat* mats
     uint4* xs = reinterpret_cast<uint4*>(region);
     float4* part = reinterpret_cast<float4*>(xs + (size_t)NB * cstride);   // [kW][2][32]
 
-    prefetch_matrix(mats, wp + 1, ring.nmat, warp, lane);
     stage_x<RMS>(p, M.nblk, cstride, xf, x16, norm_w, xs, red);
     __syncthreads();
     stamp(tr, 2);
