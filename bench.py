@@ -411,6 +411,13 @@ def step_phases(gm, sargs, s, cfg):
     out = {n: {"work": round(a[0] / a[3] / 1e3, 2), "barrier": round(a[1] / a[3] / 1e3, 2),
                "mean_cta_work": round(a[2] / a[3] / 1e3, 2), "count": a[3],
                "steps": [round(x / a[3] / 1e3, 2) for x in a[4]]} for n, a in acc.items()}
+    # GEMV phases: warp 0's share of its unit loop spent waiting for ring slots (clock cycles)
+    for n in ("qkv", "o", "gate_up", "down", "lm_head"):
+        ks = [k for k in range(1, rows) if kinds[k - 1] == n]
+        wait = t[ks, :, 6].sum()
+        loop = t[ks, :, 7].sum()
+        if loop > 0:
+            out[n]["ring_wait_frac"] = round(float(wait / loop), 3)
     out["total_step_us"] = round((leave[rows - 1].max() - leave[0].min()) / 1e3, 1)
     return out
 

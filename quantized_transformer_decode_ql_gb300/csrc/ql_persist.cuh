@@ -582,10 +582,18 @@ __device__ __noinline__ void gemv_phase(const PersistParams& p, const PMat* mats
             ++tile;
         }
     };
+    long long wait_cyc = 0;
+    const long long loop_t0 = clock64();
 #pragma unroll 1
     for (int u = u0; u < u1;) {
         const int n = min(kSlotUnits, u1 - u);   // the units of this slot (as issued)
-        ring_wait(r, p, r.consumed);
+        if (tr != nullptr) {
+            const long long c0 = clock64();
+            ring_wait(r, p, r.consumed);
+            wait_cyc += clock64() - c0;
+        } else {
+            ring_wait(r, p, r.consumed);
+        }
         __syncwarp();
         const unsigned char* sg = ring_g + (size_t)(r.consumed % kStages) * kSlotBytes;
 #pragma unroll
@@ -603,6 +611,10 @@ __device__ __noinline__ void gemv_phase(const PersistParams& p, const PMat* mats
     }
     ring = r;
     stamp(tr, 3);
+    if (tr != nullptr && threadIdx.x == 0) {   // warp 0: cycles waiting for ring slots / in the loop
+        tr[6] = (unsigned long long)wait_cyc;
+        tr[7] = (unsigned long long)(clock64() - loop_t0);
+    }
     __syncthreads();
     stamp(tr, 4);
     // A tile shared by several warps is finished by the warp holding its last unit: the shares
