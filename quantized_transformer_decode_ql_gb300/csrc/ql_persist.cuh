@@ -438,15 +438,15 @@ __device__ __noinline__ void stage_x(const PersistParams& p, int nblk, int cstri
 // Epilogue of one finished 16-row tile. acc[b] is this lane's half-row sum for column b (row
 // lane & 15 of the tile, blocks of half lane >> 4); the halves are added here, then lanes
 // 0..15 hold rows 0..15 (SiLU*up: rows 0..7 gate, 8..15 the matching up rows). All 32 lanes
-// of the warp call it.
-template <int EPI, int NB>
-__device__ __forceinline__ void finish_tile(const PersistParams& p, const PMat& M, int tile, const float (&acc)[NB],
-                                            void* y, int ld, unsigned long long (&best)[NB], int lane) {
+// of the warp call it. Out of line: it runs once per tile, and the unit loop stays small.
+template <int NB>
+__device__ __noinline__ void finish_tile(const PersistParams& p, const PMat& M, int epi, int tile, const float (&acc)[NB],
+                                         void* y, int ld, unsigned long long (&best)[NB], int lane) {
     float v[NB];
 #pragma unroll
     for (int b = 0; b < NB; ++b) v[b] = acc[b] + __shfl_xor_sync(0xffffffffu, acc[b], 16);
     const int hr = lane & 15;
-    if (EPI == kEpiSilu) {
+    if (epi == kEpiSilu) {
         float up[NB];
 #pragma unroll
         for (int b = 0; b < NB; ++b) up[b] = __shfl_down_sync(0xffffffffu, v[b], 8);
@@ -464,11 +464,11 @@ __device__ __forceinline__ void finish_tile(const PersistParams& p, const PMat& 
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
             float* dst = yf + (size_t)b * ld + row;
-            if (EPI == kEpiResid) {
+            if (epi == kEpiResid) {
                 *dst = __ldcg(dst) + v[b];
             } else {
                 *dst = v[b];
-                if (EPI == kEpiLogits) {
+                if (epi == kEpiLogits) {
                     const unsigned long long key = argmax_key(v[b], row);
                     best[b] = key > best[b] ? key : best[b];
                 }
@@ -486,8 +486,9 @@ __device__ __forceinline__ void finish_tile(const PersistParams& p, const PMat& 
 // high nibbles in separate accumulators), one FFMA per block applies the f16 scale in f32. (The
 // MMA form of the same product wastes 7 of the 8 columns of an m16n8k16 tile at batch 1-2, and
 // measured slower than the CUDA cores here.)
-template <int EPI, bool RMS, int NB>
-__device__ __noinline__ void gemv_phase(const PersistParams& p, const PMat* mats, int wp, Ring& ring, const float* xf,
+template <int NB>
+__device__ __noinline__ void gemv_phase(const PersistParams& p, const PMat* mats, int wp, int epi, bool rms,
+                                        Ring& ring, const float* xf,
                                         const __half* x16, const float* norm_w, void* y, int ld,
                                         unsigned char* region, float* red,
                                         unsigned long long (*kred)[kMaxB], unsigned long long* tr) {
@@ -498,7 +499,10 @@ __device__ __noinline__ void gemv_phase(const PersistParams& p, const PMat* mats
     uint4* xs = reinterpret_cast<uint4*>(region);
     float4* part = reinterpret_cast<float4*>(xs + (size_t)NB * cstride);   // [kW][2][32]
 
-    stage_x<RMS>(p, M.nblk, cstride, xf, x16, norm_w, xs, red);
+    if (rms)
+        stage_x<true>(p, M.nblk, cstride, xf, x16, norm_w, xs, red);
+    else
+        stage_x<false>(p, M.nblk, cstride, xf, x16, norm_w, xs, red);
     __syncthreads();
     stamp(tr, 2);
 
@@ -570,7 +574,7 @@ __device__ __noinline__ void gemv_phase(const PersistParams& p, const PMat* mats
         if (++k == nst || u + 1 == u1) {
             const int ts = (tile - T0) * nst;
             if (u0 <= ts && u + 1 == ts + nst) {
-                finish_tile<EPI, NB>(p, M, tile, acc, y, ld, best, lane);
+                finish_tile<NB>(p, M, epi, tile, acc, y, ld, best, lane);
             } else {
                 float4 v = make_float4(acc[0], 0.f, 0.f, 0.f);
                 if (NB > 1) v.y = acc[NB > 1 ? 1 : 0];
@@ -596,13 +600,11 @@ __device__ __noinline__ void gemv_phase(const PersistParams& p, const PMat* mats
         }
         __syncwarp();
         const unsigned char* sg = ring_g + (size_t)(r.consumed % kStages) * kSlotBytes;
-#pragma unroll
-        for (int i = 0; i < kSlotUnits; ++i) {
-            if (i < n) {
-                float pu[NB];
-                unit(sg + i * kUnitBytes, k, pu);
-                advance(pu, u + i);
-            }
+#pragma unroll 1
+        for (int i = 0; i < n; ++i) {
+            float pu[NB];
+            unit(sg + i * kUnitBytes, k, pu);
+            advance(pu, u + i);
         }
         __syncwarp();
         ++r.consumed;
@@ -633,10 +635,10 @@ __device__ __noinline__ void gemv_phase(const PersistParams& p, const PMat* mats
                 s2[0] += v.x;
                 if (NB > 1) s2[NB > 1 ? 1 : 0] += v.y;
             }
-            finish_tile<EPI, NB>(p, M, first_tile, s2, y, ld, best, lane);
+            finish_tile<NB>(p, M, epi, first_tile, s2, y, ld, best, lane);
         }
     }
-    if (EPI == kEpiLogits) {
+    if (epi == kEpiLogits) {
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
 #pragma unroll
@@ -1083,27 +1085,27 @@ __device__ void step_body(const PersistParams& p, const PMat* mats, Ring& r, uns
         const PLayer* Ly = p.layers + l;
         attn_prefetch<HD>(p, l);
         // q|k|v = W_qkv rmsnorm(x, attn_norm)
-        gemv_phase<kEpiF32, true, NB>(p, mats, 4 * l, r, p.x, nullptr, Ly->attn_norm, p.qkv, qkv_ld, region, red,
+        gemv_phase<NB>(p, mats, 4 * l, kEpiF32, true, r, p.x, nullptr, Ly->attn_norm, p.qkv, qkv_ld, region, red,
                                       kred, row());
         if (!grid_barrier(p, target, flag)) return;
         // qk-norm + RoPE + KV append + paged attention -> attn
         attn_phase<HD, G>(p, l, region, qs, flag, row());
         if (!grid_barrier(p, target, flag)) return;
         // x += W_o attn
-        gemv_phase<kEpiResid, false, NB>(p, mats, 4 * l + 1, r, nullptr, p.attn, nullptr, p.x, p.hidden, region, red,
+        gemv_phase<NB>(p, mats, 4 * l + 1, kEpiResid, false, r, nullptr, p.attn, nullptr, p.x, p.hidden, region, red,
                                          kred, row());
         if (!grid_barrier(p, target, flag)) return;
         // act = silu(gate) * up, [gate | up] = W_gu rmsnorm(x, ffn_norm)
-        gemv_phase<kEpiSilu, true, NB>(p, mats, 4 * l + 2, r, p.x, nullptr, Ly->ffn_norm, p.act, p.inter, region, red,
+        gemv_phase<NB>(p, mats, 4 * l + 2, kEpiSilu, true, r, p.x, nullptr, Ly->ffn_norm, p.act, p.inter, region, red,
                                        kred, row());
         if (!grid_barrier(p, target, flag)) return;
         // x += W_down act
-        gemv_phase<kEpiResid, false, NB>(p, mats, 4 * l + 3, r, nullptr, p.act, nullptr, p.x, p.hidden, region, red,
+        gemv_phase<NB>(p, mats, 4 * l + 3, kEpiResid, false, r, nullptr, p.act, nullptr, p.x, p.hidden, region, red,
                                          kred, row());
         if (!grid_barrier(p, target, flag)) return;
     }
     // logits = W_lm rmsnorm(x, final_norm), greedy argmax keys
-    gemv_phase<kEpiLogits, true, NB>(p, mats, 4 * p.n_layers, r, p.x, nullptr, p.final_norm, p.logits, p.vocab, region,
+    gemv_phase<NB>(p, mats, 4 * p.n_layers, kEpiLogits, true, r, p.x, nullptr, p.final_norm, p.logits, p.vocab, region,
                                      red, kred, row());
     if (!grid_barrier(p, target, flag)) return;
     if (blockIdx.x == 0) finalize(p);
