@@ -265,4 +265,25 @@ size_t persist_smem_bytes(int batch, int max_nblk, int head_dim, int group, int 
 int persist_prepare(int batch, int max_nblk, int head_dim, int group, int n_layers);
 int persist_launch(const PersistParams& p, int head_dim, int group, cudaStream_t s);
 
+// One GEMV over a matrix in the tile stream layout, batch 1 or 2, as a stand-alone kernel
+// (one CTA per SM; HFMA2 products, ring of bulk copies): the launch-per-phase step's GEMV.
+// epilogue: QL_EPI_NONE (f32 y), QL_EPI_ADD_RESIDUAL (f32 y += ...), QL_EPI_SILU_MUL (f16 y,
+// matrix packed with silu), kEpiArgmax (f32 logits + keys). rms: xf f32 normalised with
+// norm_w, else x16 f16.
+struct StreamGemvArgs {
+    PMat M;
+    int batch, epilogue, rms;
+    const float* xf;
+    const __half* x16;
+    const float* norm_w;
+    float eps;
+    void* y;
+    int ld;
+    unsigned long long* keys;
+    const int32_t* active;
+    unsigned int* sync;   // [4] zero: the abort flag of the kernel's bounded waits
+};
+int stream_gemv_prepare();
+int stream_gemv_launch(const StreamGemvArgs& a, cudaStream_t s, bool pdl);
+
 }  // namespace ql

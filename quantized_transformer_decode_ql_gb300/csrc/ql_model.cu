@@ -58,6 +58,8 @@ struct ql_model {
     ql::PLayer* players = nullptr;          // device [n_layers]
     uint8_t* pstreams = nullptr;            // all matrices in the tile stream layout
     size_t persist_stream_bytes = 0;
+    std::vector<ql::PMat> hmats;            // host copies: 4 per layer, then lm_head
+    unsigned int* ssync = nullptr;          // abort flag of the stand-alone stream GEMVs
     ql::PMat plm = {};
     int max_nblk = 0, persist_nsplit = 1;
     float* ppm = nullptr;
@@ -207,8 +209,65 @@ int run_step(ql_model* m, const ql_step_args* a, cudaStream_t s) {
                            m->x, (int)d.hidden, (int)d.vocab, device_error_record(), nw(m->layers[0].qkv, kAll));
     if (e != cudaSuccess) return cuda_error(e, "embed launch");
 
+    // batch 1-2: the GEMVs stream the tile stream copy of the weights (stream_gemv_launch)
+    const bool streamed = B <= kPersistMaxBatch && !m->hmats.empty();
+    auto sg = [&](const PMat& M, int epi, bool rms, const float* xf, const __half* x16, const float* nw, void* y,
+                  int ld) {
+        StreamGemvArgs ga = {};
+        ga.M = M;
+        ga.batch = B;
+        ga.epilogue = epi;
+        ga.rms = rms ? 1 : 0;
+        ga.xf = xf;
+        ga.x16 = x16;
+        ga.norm_w = nw;
+        ga.eps = d.eps;
+        ga.y = y;
+        ga.ld = ld;
+        ga.keys = m->keys;
+        ga.active = a->active;
+        ga.sync = m->ssync;
+        return stream_gemv_launch(ga, s, pdl);
+    };
     for (int li = 0; li < d.n_layers; ++li) {
         const ql_layer_desc& L = m->layers[li];
+        if (streamed) {
+            const PMat* Ms = &m->hmats[4 * li];
+            const int qkv_ld = (int)((d.n_heads + 2 * d.n_kv_heads) * d.head_dim);
+            if ((rc = sg(Ms[0], QL_EPI_NONE, true, m->x, nullptr, L.attn_norm, m->qkv, qkv_ld)) != QL_OK) return rc;
+            AttnArgs at = {};
+            at.qkv = m->qkv;
+            at.q_norm = L.q_norm;
+            at.k_norm = L.k_norm;
+            at.cos_t = m->cos_t;
+            at.sin_t = m->sin_t;
+            at.eps = d.eps;
+            at.max_position = d.max_blocks_per_seq * d.block_size;
+            at.k_pool = static_cast<__half*>(d.k_pool) + layer_pool * li;
+            at.v_pool = static_cast<__half*>(d.v_pool) + layer_pool * li;
+            at.block_tables = a->block_tables;
+            at.positions = a->positions;
+            at.active = a->active;
+            at.batch = B;
+            at.n_heads = nh;
+            at.n_kv_heads = nkv;
+            at.head_dim = hd;
+            at.block_size = d.block_size;
+            at.max_blocks_per_seq = d.max_blocks_per_seq;
+            at.num_blocks = d.num_blocks;
+            at.scale = 1.0f / sqrtf((float)hd);
+            at.out = m->attn;
+            at.workspace = m->attn_ws;
+            at.workspace_bytes = m->attn_ws_bytes;
+            if ((rc = attn_launch(at, s, pdl)) != QL_OK) return rc;
+            if ((rc = sg(Ms[1], QL_EPI_ADD_RESIDUAL, false, nullptr, m->attn, nullptr, m->x, (int)d.hidden)) != QL_OK)
+                return rc;
+            if ((rc = sg(Ms[2], QL_EPI_SILU_MUL, true, m->x, nullptr, L.ffn_norm, m->act, (int)d.intermediate)) != QL_OK)
+                return rc;
+            if ((rc = sg(Ms[3], QL_EPI_ADD_RESIDUAL, false, nullptr, m->act, nullptr, m->x, (int)d.hidden)) != QL_OK)
+                return rc;
+            continue;
+        }
         GemvArgs g = {};
         g.batch = B;
         // qkv projection with the attention RMSNorm as prologue
@@ -301,6 +360,15 @@ int run_step(ql_model* m, const ql_step_args* a, cudaStream_t s) {
         if ((rc = gemv_launch(gd, s, pdl)) != QL_OK) return rc;
     }
 
+    if (streamed) {
+        if ((rc = sg(m->hmats.back(), kEpiArgmax, true, m->x, nullptr, d.final_norm,
+                     a->logits ? a->logits : m->logits, (int)d.vocab)) != QL_OK)
+            return rc;
+        e = launch(finalize_kernel, dim3(1), dim3(64), 0, s, pdl, m->keys, a->active, a->positions,
+                   a->next_tokens, a->out_tokens, (long long)a->out_stride, (float*)nullptr, B);
+        if (e != cudaSuccess) return cuda_error(e, "finalize launch");
+        return QL_OK;
+    }
     GemvArgs gl = {};
     gl.batch = B;
     gl.scales = static_cast<const __half*>(d.lm_head.scales);
@@ -358,6 +426,7 @@ int setup_persist(ql_model* m) {
     for (; maxb >= 1; --maxb)
         if (persist_prepare(maxb, m->max_nblk, (int)d.head_dim, G, (int)d.n_layers) == QL_OK) break;
     if (maxb < 1) return QL_OK;
+    if (int rc0 = stream_gemv_prepare()) return rc0;
 
     std::vector<PLayer> hl(m->layers.size());
     std::vector<PMat> all;
@@ -389,15 +458,18 @@ int setup_persist(ql_model* m) {
     A((void**)&m->ppacc, parts * d.head_dim * 4);
     A((void**)&m->ptickets, (size_t)maxb * d.n_kv_heads * 4);
     A((void**)&m->psync, 16);
+    A((void**)&m->ssync, 16);
     if (rc != QL_OK) return rc;
     // the weights re-laid into the tile stream layout that the persistent kernel copies from
     if ((rc = persist_pack_streams(all.data(), (int)all.size(), m->pstreams, nullptr)) != QL_OK) return rc;
     for (size_t i = 0; i < hl.size(); ++i)
         for (int k = 0; k < 4; ++k) hl[i].m[k] = all[4 * i + k];
     m->plm = all.back();
+    m->hmats = all;
     cudaError_t e = cudaMemcpy(m->players, hl.data(), hl.size() * sizeof(PLayer), cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemset(m->ptickets, 0, (size_t)maxb * d.n_kv_heads * 4);
     if (e == cudaSuccess) e = cudaMemset(m->psync, 0, 16);
+    if (e == cudaSuccess) e = cudaMemset(m->ssync, 0, 16);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_error(e, "ql_model_create: persistent step workspace");
     m->persist_stream_bytes = stream_bytes;

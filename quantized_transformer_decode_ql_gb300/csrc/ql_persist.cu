@@ -2,6 +2,8 @@
 // itself is in ql_persist.cuh; head_dim 64 in ql_persist_hd64.cu).
 #include "ql_persist.cuh"
 
+#include <mutex>
+#include <set>
 #include <string>
 
 namespace ql {
@@ -53,6 +55,59 @@ int persist_pack_streams(PMat* mats, int n, uint8_t* buf, cudaStream_t s) {
         if (e != cudaSuccess) return cuda_error(e, "persistent step: stream pack launch");
         off += persist_stream_bytes(mats[i]);
     }
+    return QL_OK;
+}
+
+static_assert(persist::kEpiF32 == QL_EPI_NONE && persist::kEpiResid == QL_EPI_ADD_RESIDUAL &&
+                  persist::kEpiSilu == QL_EPI_SILU_MUL && persist::kEpiLogits == kEpiArgmax,
+              "epilogue codes");
+
+int stream_gemv_prepare() {
+    static std::mutex mu;
+    static std::set<int> done;
+    int dev = 0;
+    QL_TRY_CUDA(cudaGetDevice(&dev));
+    std::lock_guard<std::mutex> lk(mu);
+    if (done.count(dev)) return QL_OK;
+    cudaError_t e = persist::stream_gemv_one<1>(false, nullptr, nullptr, 0, 0, nullptr, false);
+    if (e == cudaSuccess) e = persist::stream_gemv_one<2>(false, nullptr, nullptr, 0, 0, nullptr, false);
+    if (e != cudaSuccess) return cuda_error(e, "stream gemv: kernel attributes");
+    done.insert(dev);
+    return QL_OK;
+}
+
+int stream_gemv_launch(const StreamGemvArgs& a, cudaStream_t s, bool pdl) {
+    QL_REQUIRE(a.M.stream && a.M.nblk > 0 && a.M.nblk % persist::kUnitBlocks == 0, "stream gemv: bad matrix");
+    QL_REQUIRE(a.batch == 1 || a.batch == 2, "stream gemv: batch must be 1 or 2");
+    QL_REQUIRE(a.rms ? (a.xf && a.norm_w) : a.x16 != nullptr, "stream gemv: null input");
+    QL_REQUIRE(a.y && a.sync, "stream gemv: null output");
+    QL_REQUIRE(a.epilogue != kEpiArgmax || a.keys, "stream gemv: argmax needs keys");
+    QL_REQUIRE((a.epilogue == QL_EPI_SILU_MUL) == (a.M.silu != 0), "stream gemv: SiLU*up needs a matrix packed for it");
+    DevError* err = device_error_record();
+    if (!err) return set_error(QL_ECUDA, "stream gemv: no device error record");
+    if (int rc = stream_gemv_prepare()) return rc;
+    PersistParams p = {};
+    p.B = a.batch;
+    p.max_nblk = a.M.nblk;
+    p.eps = a.eps;
+    p.barrier_timeout_ns = 2000000000ull;
+    p.keys = a.keys;
+    p.active = a.active;
+    p.sync = a.sync;
+    p.err = err;
+    persist::StreamGemv g = {};
+    g.M = a.M;
+    g.epi = a.epilogue;
+    g.rms = a.rms;
+    g.xf = a.xf;
+    g.x16 = a.x16;
+    g.norm_w = a.norm_w;
+    g.y = a.y;
+    g.ld = a.ld;
+    const size_t smem = persist::kRingBytes + persist::gemv_region_bytes(a.batch, a.M.nblk);
+    const cudaError_t e = a.batch == 1 ? persist::stream_gemv_one<1>(true, &p, &g, smem, num_sms(), s, pdl)
+                                       : persist::stream_gemv_one<2>(true, &p, &g, smem, num_sms(), s, pdl);
+    if (e != cudaSuccess) return cuda_error(e, "stream gemv launch");
     return QL_OK;
 }
 

@@ -1200,6 +1200,62 @@ static __global__ void stream_pack_kernel(PMat M, uint8_t* out) {
     }
 }
 
+// ------------------------------------------------------------------------------ stand-alone GEMV
+// One GEMV phase as its own kernel (one CTA per SM), for the step that runs one launch per
+// phase: the ring's first slots are filled before the kernel waits on its predecessor
+// (programmatic dependent launch), since the weights do not depend on it.
+struct StreamGemv {
+    PMat M;
+    int epi, rms;
+    const float* xf;       // rms: f32 [B][cols], normalised with norm_w
+    const __half* x16;     // else: f16 [B][cols]
+    const float* norm_w;
+    void* y;
+    int ld;
+};
+
+template <int NB>
+__global__ void __launch_bounds__(kT, 1) gemv_stream_kernel(const __grid_constant__ PersistParams p,
+                                                             const __grid_constant__ StreamGemv g) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ PMat mat;
+    __shared__ float red[kW * 2];
+    __shared__ unsigned long long kred[kW][kMaxB];
+    __shared__ __align__(8) unsigned long long mbar[kW * kStages];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) mat = g.M;
+    if (lane == 0)
+        for (int i = 0; i < kStages; ++i)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(
+                             static_cast<uint32_t>(__cvta_generic_to_shared(&mbar[warp * kStages + i]))) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    __syncthreads();
+    Ring r;
+    r.wp = 0;
+    r.nmat = 1;
+    r.u = r.u_end = 0;
+    r.src = nullptr;
+    r.issued = r.consumed = 0;
+    r.dead = 0;
+    r.base = static_cast<uint32_t>(__cvta_generic_to_shared(smem)) + (uint32_t)(warp * kStages * kSlotBytes);
+    r.mbar = static_cast<uint32_t>(__cvta_generic_to_shared(&mbar[warp * kStages]));
+    ring_seek(r, &mat, warp);
+#pragma unroll 1
+    for (int i = 0; i < kStages; ++i) ring_issue(r, &mat, warp, lane);
+    pdl_trigger();
+    pdl_wait();
+    gemv_phase<NB>(p, &mat, 0, g.epi, g.rms != 0, r, g.xf, g.x16, g.norm_w, g.y, g.ld, smem + kRingBytes, red, kred,
+                   nullptr);
+    const unsigned long long t0 = global_ns();
+    while (r.consumed < r.issued) {   // only after a wait ran out: let copies land (bounded)
+        const uint32_t mb = r.mbar + (r.consumed % kStages) * 8, parity = (r.consumed / kStages) & 1u;
+        bool landed = mbar_test(mb, parity);
+        while (!landed && global_ns() - t0 <= p.barrier_timeout_ns) landed = mbar_test(mb, parity);
+        if (!landed) break;
+        ++r.consumed;
+    }
+}
+
 }  // namespace persist
 }  // namespace ql
 
@@ -1251,6 +1307,28 @@ cudaError_t dispatch(int G, bool launch, const PersistParams* p, size_t smem, in
         case 8: return run_one<HD, 8>(launch, p, smem, grid, s, occ);
         default: return cudaErrorInvalidValue;
     }
+}
+
+template <typename K, typename... Args>
+cudaError_t launch_kernel_pdl(K kernel, int grid, size_t smem, cudaStream_t s, bool pdl, const Args&... args) {
+    return ql::launch(kernel, dim3(grid), dim3(kT), smem, s, pdl, args...);
+}
+
+template <int NB>
+cudaError_t stream_gemv_one(bool launch, const PersistParams* p, const StreamGemv* g, size_t smem, int grid,
+                            cudaStream_t s, bool pdl) {
+    if (!launch) {
+        int dev = 0, optin = 0;
+        cudaFuncAttributes fa = {};
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, gemv_stream_kernel<NB>);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gemv_stream_kernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     optin - (int)fa.sharedSizeBytes);
+        return e;
+    }
+    return launch_kernel_pdl(gemv_stream_kernel<NB>, grid, smem, s, pdl, *p, *g);
 }
 
 }  // namespace persist
