@@ -194,7 +194,8 @@ def gpu_arm(args, rank, world, local_rank):
     gm = DeviceModel.from_layer_fn(cfg, device_tensor_fn(cfg, seed=0), num_blocks=num_blocks,
                                    max_batch=B, max_blocks_per_seq=maxb)
     gm.ql_model_set_option(ql.QL_OPT_STEP_KERNEL, STEP_KERNELS[args.step_kernel])
-    persistent = args.step_kernel != "launches" and B <= gm.ql_model_persistent_max_batch()
+    persistent = args.step_kernel == "persistent" and B <= gm.ql_model_persistent_max_batch()
+    streamed = not persistent and B <= gm.ql_model_persistent_max_batch()   # stream GEMVs in the step
     # fragmented block tables; pre-filled synthetic context of CTX positions N(0,1) f16 per slot
     perm = torch.from_numpy(ql_inputs.fragmented_block_ids(num_blocks, seed=5)).cuda()
     bt = perm[: B * maxb].reshape(B, maxb).contiguous()
@@ -261,15 +262,35 @@ def gpu_arm(args, rank, world, local_rank):
     act = torch.empty((B, cfg.intermediate), dtype=torch.float16, device="cuda")
     reps = 3
 
-    def gu_all():
-        for L in gm.layers:
-            W = L["wgu"]
-            ql.ql_gemv_q4_0(W.scales, W.quants, W.rows, W.cols, x16, B, act, ql.QL_DTYPE_F16,
-                            ql.QL_EPI_SILU_MUL, None, s)
-    gu_ms_rep = graph_ms(gu_all, s, reps)
-    gu_launches = reps * cfg.n_layers
-    gu_ms = gu_ms_rep / cfg.n_layers
     W = gm.layers[0]["wgu"]
+    if streamed:
+        # the kernel the step runs at this batch: the GEMV over the tile stream layout, on
+        # 8 layers' gate|up matrices in turn (453 MB: no L2 reuse between launches)
+        n_mats = min(8, cfg.n_layers)
+        streams = []
+        for L in gm.layers[:n_mats]:
+            Wl = L["wgu"]
+            buf = torch.empty(ql.ql_q4_0_stream_bytes(Wl.rows, Wl.cols, 1), dtype=torch.uint8, device="cuda")
+            ql.ql_q4_0_stream_pack(Wl.scales, Wl.quants, Wl.rows, Wl.cols, 1, buf, s)
+            streams.append(buf)
+        s.synchronize()
+
+        def gu_all():
+            for buf in streams:
+                ql.ql_gemv_q4_0_stream(buf, W.rows, W.cols, x16, B, act, ql.QL_EPI_SILU_MUL, s)
+        gu_kernel = "q4_0 GEMV over the tile stream layout (gate|up, SiLU*up epilogue, batch %d)" % B
+    else:
+        n_mats = cfg.n_layers
+
+        def gu_all():
+            for L in gm.layers:
+                Wl = L["wgu"]
+                ql.ql_gemv_q4_0(Wl.scales, Wl.quants, Wl.rows, Wl.cols, x16, B, act, ql.QL_DTYPE_F16,
+                                ql.QL_EPI_SILU_MUL, None, s)
+        gu_kernel = "q4_0 GEMV (gate|up, SiLU*up epilogue, batch %d)" % B
+    gu_ms_rep = graph_ms(gu_all, s, reps)
+    gu_launches = reps * n_mats
+    gu_ms = gu_ms_rep / n_mats
     gu_bytes = W.nbytes() + B * cfg.hidden * 2 + B * cfg.intermediate * 2
 
     # ---- attention alone at this workload (context CTX + steps/2), 36 layers' pools in turn
@@ -330,7 +351,7 @@ def gpu_arm(args, rank, world, local_rank):
                    "head_dim": cfg.head_dim, "intermediate": cfg.intermediate, "vocab": cfg.vocab,
                    "batch": B, "context": CTX, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (%.2f GB of q4_0 weights streamed per step)" % (wbytes / 1e9)},
-        "roofline": {"bound": "hbm", "kernel": "q4_0 GEMV (gate|up, SiLU*up epilogue, batch %d)" % B,
+        "roofline": {"bound": "hbm", "kernel": gu_kernel,
                      "achieved": round(gu_gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(gu_gbs / peak, 4), "traffic": None, "peak_source": peak_src},
         "step_roofline": {"bytes_per_step": int(step_bytes), "achieved_gbs": round(step_gbs, 1),

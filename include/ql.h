@@ -100,6 +100,29 @@ int ql_gemv_q4_0(const void* d_scales, const void* d_quants, int64_t rows, int64
                  const void* d_x, int64_t batch, void* d_y, int y_dtype, int epilogue,
                  const float* d_residual, void* stream);
 
+/* --------------------------------------------------------------- q4_0 tile stream (GPU)
+ * The layout that the batch 1-2 GEMV copies with bulk (TMA) copies: the rows in 16-row tiles
+ * (silu != 0: tile i = gate rows 8i..8i+7 followed by the matching up rows rows/2 + 8i..),
+ * each tile as cols/128 units of 1152 contiguous bytes: the codes of 4 blocks x 16 rows
+ * ([block][row], 16 B each) then the 16 rows' 4 f16 scales (8 B per row). Rows past the
+ * matrix are zero. An exact byte permutation of the q4_0 arrays. cols % 128 == 0; with silu,
+ * rows is even. Bytes needed: ql_q4_0_stream_bytes (0 on a bad shape).                   */
+int64_t ql_q4_0_stream_bytes(int64_t rows, int64_t cols, int silu);
+/* Re-lay d_scales / d_quants (the q4_0 arrays above, device) into d_stream. d_quants and
+ * d_stream 16-byte aligned, d_scales 8-byte aligned. Asynchronous on stream.              */
+int ql_q4_0_stream_pack(const void* d_scales, const void* d_quants, int64_t rows, int64_t cols,
+                        int silu, void* d_stream, void* stream);
+/* [IL] CudaQwen3::gemv at batch 1-2 from the tile stream: y = epilogue(W x).
+ * d_x: f16 [batch][cols], 16-byte aligned. epilogue QL_EPI_NONE: d_y f32 [batch][rows];
+ * QL_EPI_ADD_RESIDUAL: d_y f32 [batch][rows], y += W x in place; QL_EPI_SILU_MUL (d_stream
+ * packed with silu): d_y f16 [batch][rows/2]. Products: each code becomes q - 8 (low nibble)
+ * or 16 (q - 8) (high nibble, against x/16) exactly in f16, the 32 products of a block are
+ * summed in f16 (HFMA2; low and high nibbles apart), and each block is scaled by its f16 scale
+ * and accumulated in f32. One CTA per SM; its waits for the bulk copies are bounded (2 s, then
+ * the device error record says so). batch must be 1 or 2 (QL_EINVAL otherwise).          */
+int ql_gemv_q4_0_stream(const void* d_stream, int64_t rows, int64_t cols, const void* d_x,
+                        int64_t batch, void* d_y, int epilogue, void* stream);
+
 /* --------------------------------------------------------------- paged decode attention
  * [FK] launch_paged_decode_attention / attention_paged, split-K over the context:
  *   out[b][h][:] = sum_{t < context_lens[b]} softmax_t(q[b][h] . K_t * scale) V_t
@@ -205,13 +228,15 @@ typedef struct ql_model ql_model;
 int ql_model_create(const ql_model_desc* desc, ql_model** out);
 int ql_model_destroy(ql_model* m);
 
-/* How a decode step runs. QL_STEP_PERSISTENT: the whole step as ONE cooperative kernel, one
- * CTA per SM, that streams every layer's weights through shared-memory rings and separates the
- * step's phases (q|k|v, attention, o, gate|up, down per layer; lm_head) with grid-wide
- * barriers in device memory; it takes batches up to ql_model_persistent_max_batch() (at most
- * 2). QL_STEP_LAUNCHES: one kernel per phase (any batch up to max_batch). QL_STEP_AUTO (the
- * default): persistent when the batch allows it, else launches. Both compute the same step
- * ([IL] CudaQwen3::step); their f32 sums differ only in rounding order.               */
+/* How a decode step runs. QL_STEP_LAUNCHES: one kernel per phase (q|k|v, attention, o,
+ * gate|up, down per layer; lm_head), any batch up to max_batch; at batch 1-2 the GEMVs read
+ * the tile stream copy of the weights (see ql_gemv_q4_0_stream). QL_STEP_PERSISTENT: the whole
+ * step as ONE cooperative kernel, one CTA per SM, that streams every layer's weights through
+ * shared-memory rings and separates the phases with grid-wide barriers in device memory;
+ * batches up to ql_model_persistent_max_batch() (at most 2). QL_STEP_AUTO (the default):
+ * QL_STEP_LAUNCHES, the faster of the two on GB300 (2.12 vs 3.09 ms per batch-1 step of the
+ * 8B-shaped model). Both compute the same step ([IL] CudaQwen3::step); their sums differ only
+ * in rounding order.                                                                     */
 enum { QL_STEP_AUTO = 0, QL_STEP_LAUNCHES = 1, QL_STEP_PERSISTENT = 2 };
 /* Options of a model handle:
  *   QL_OPT_STEP_KERNEL         one of QL_STEP_*; QL_STEP_PERSISTENT is QL_EINVAL when the

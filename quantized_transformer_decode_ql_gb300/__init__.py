@@ -19,6 +19,7 @@ from ._lib import (QLError, QL_OK, QL_EINVAL, QL_ENOMEM, QL_ECUDA, QL_EPOOL, QL_
 
 __all__ = [
     "QLError", "lib", "ql_q4_0_pack", "ql_q4_0_unpack", "ql_q4_0_pack_device", "ql_gemv_q4_0",
+    "ql_q4_0_stream_bytes", "ql_q4_0_stream_pack", "ql_gemv_q4_0_stream",
     "ql_paged_attn_workspace_bytes", "ql_paged_attn_decode", "ql_paged_attn_decode_noalloc",
     "ql_fused_norm_rope",
     "ql_rope_tables", "ql_check_device_error", "BlockPool", "SIGNATURES",
@@ -45,6 +46,19 @@ def ql_gemv_q4_0(scales, quants, rows, cols, x, batch, y, y_dtype=QL_DTYPE_F32,
                  epilogue=QL_EPI_NONE, residual=None, stream=None):
     check(lib().ql_gemv_q4_0(ptr(scales), ptr(quants), rows, cols, ptr(x), batch, ptr(y), y_dtype,
                              epilogue, ptr(residual), stream_ptr(stream)))
+
+
+def ql_q4_0_stream_bytes(rows, cols, silu=0):
+    return int(lib().ql_q4_0_stream_bytes(rows, cols, silu))
+
+
+def ql_q4_0_stream_pack(scales, quants, rows, cols, silu, out, stream=None):
+    check(lib().ql_q4_0_stream_pack(ptr(scales), ptr(quants), rows, cols, silu, ptr(out), stream_ptr(stream)))
+
+
+def ql_gemv_q4_0_stream(w_stream, rows, cols, x, batch, y, epilogue=QL_EPI_NONE, stream=None):
+    check(lib().ql_gemv_q4_0_stream(ptr(w_stream), rows, cols, ptr(x), batch, ptr(y), epilogue,
+                                    stream_ptr(stream)))
 
 
 def ql_paged_attn_workspace_bytes(batch, n_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq):

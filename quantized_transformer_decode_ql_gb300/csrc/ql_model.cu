@@ -6,10 +6,11 @@
 // and the position advance stay on the device. [FK] ferrum-kernels cuda_decode.rs
 // batch_decode_step: several sequences per step over a paged KV pool.
 //
-// Batches up to ql_model_persistent_max_batch() run the step as ONE cooperative kernel
-// (ql_persist.cuh) unless QL_OPT_STEP_KERNEL says otherwise. Larger batches run this kernel
-// sequence, all launched with programmatic dependent launch so that each GEMV starts streaming
-// its weights into L2 while its predecessor drains:
+// With QL_OPT_STEP_KERNEL = QL_STEP_PERSISTENT (batches up to ql_model_persistent_max_batch())
+// the step runs as ONE cooperative kernel (ql_persist.cuh). Otherwise (the default) it runs
+// this kernel sequence, all launched with programmatic dependent launch so that each GEMV
+// starts streaming its weights while its predecessor drains; at batch 1-2 the GEMVs read the
+// tile stream copy of the weights (stream_gemv_launch), above that the row-major q4_0 arrays:
 //   embed                      x[b] = E[token[b]]                          (f32 residual)
 //   per layer:
 //     gemv  rms(x)*attn_norm -> W_qkv                                       -> qkv f32
@@ -183,7 +184,7 @@ int run_step(ql_model* m, const ql_step_args* a, cudaStream_t s) {
     if (m->step_kernel == QL_STEP_PERSISTENT && B > m->persist_max_b)
         return set_error(QL_EINVAL, "decode step: the persistent step kernel takes batches up to " +
                                         std::to_string(m->persist_max_b) + " on this model");
-    if (m->step_kernel != QL_STEP_LAUNCHES && B <= m->persist_max_b) return run_persist(m, a, s);
+    if (m->step_kernel == QL_STEP_PERSISTENT) return run_persist(m, a, s);
     const bool pdl = true;
     const int hd = (int)d.head_dim, nh = (int)d.n_heads, nkv = (int)d.n_kv_heads;
     const size_t layer_pool = (size_t)d.num_blocks * nkv * d.block_size * hd;

@@ -121,3 +121,72 @@ int persist_launch(const PersistParams& p, int head_dim, int group, cudaStream_t
 }
 
 }  // namespace ql
+
+// ---------------------------------------------------------------------------------------------
+// C ABI: the tile stream layout and the batch 1-2 GEMV over it.
+namespace {
+
+// abort flag of the stand-alone GEMV's bounded waits (written only when a wait runs out)
+__device__ unsigned int g_stream_gemv_sync[4];
+
+bool stream_shape_ok(int64_t rows, int64_t cols, int silu) {
+    return rows > 0 && cols > 0 && cols % 128 == 0 && rows < (1ll << 30) && cols < (1ll << 24) &&
+           (!silu || rows % 2 == 0);
+}
+
+ql::PMat stream_mat(const void* d_stream, int64_t rows, int64_t cols, int silu) {
+    ql::PMat m = {};
+    m.stream = static_cast<const uint8_t*>(d_stream);
+    m.rows = (int)rows;
+    m.nblk = (int)(cols / 32);
+    m.silu = silu ? 1 : 0;
+    m.ntile = silu ? (int)((rows / 2 + 7) / 8) : (int)((rows + 15) / 16);
+    return m;
+}
+
+bool aligned(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) & (n - 1)) == 0; }
+
+}  // namespace
+
+extern "C" int64_t ql_q4_0_stream_bytes(int64_t rows, int64_t cols, int silu) {
+    if (!stream_shape_ok(rows, cols, silu)) return 0;
+    return (int64_t)ql::persist_stream_bytes(stream_mat(nullptr, rows, cols, silu));
+}
+
+extern "C" int ql_q4_0_stream_pack(const void* d_scales, const void* d_quants, int64_t rows, int64_t cols,
+                                   int silu, void* d_stream, void* stream) {
+    using namespace ql;
+    QL_REQUIRE(d_scales && d_quants && d_stream, "ql_q4_0_stream_pack: null pointer");
+    QL_REQUIRE(stream_shape_ok(rows, cols, silu), "ql_q4_0_stream_pack: need cols % 128 == 0 (and even rows with silu)");
+    QL_REQUIRE(aligned(d_quants, 16) && aligned(d_stream, 16) && aligned(d_scales, 8),
+               "ql_q4_0_stream_pack: codes and stream must be 16-byte aligned, scales 8-byte");
+    PMat m = stream_mat(nullptr, rows, cols, silu);
+    m.quants = static_cast<const uint8_t*>(d_quants);
+    m.scales = static_cast<const __half*>(d_scales);
+    return persist_pack_streams(&m, 1, static_cast<uint8_t*>(d_stream), static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int ql_gemv_q4_0_stream(const void* d_stream, int64_t rows, int64_t cols, const void* d_x, int64_t batch,
+                                   void* d_y, int epilogue, void* stream) {
+    using namespace ql;
+    QL_REQUIRE(d_stream && d_x && d_y, "ql_gemv_q4_0_stream: null pointer");
+    QL_REQUIRE(epilogue == QL_EPI_NONE || epilogue == QL_EPI_ADD_RESIDUAL || epilogue == QL_EPI_SILU_MUL,
+               "ql_gemv_q4_0_stream: unknown epilogue");
+    const int silu = epilogue == QL_EPI_SILU_MUL;
+    QL_REQUIRE(stream_shape_ok(rows, cols, silu), "ql_gemv_q4_0_stream: need cols % 128 == 0 (and even rows with SiLU*up)");
+    QL_REQUIRE(batch == 1 || batch == 2, "ql_gemv_q4_0_stream: batch must be 1 or 2");
+    QL_REQUIRE(aligned(d_stream, 16) && aligned(d_x, 16) && aligned(d_y, 4),
+               "ql_gemv_q4_0_stream: stream and x must be 16-byte aligned, y 4-byte");
+    void* sync = nullptr;
+    QL_TRY_CUDA(cudaGetSymbolAddress(&sync, g_stream_gemv_sync));
+    StreamGemvArgs a = {};
+    a.M = stream_mat(d_stream, rows, cols, silu);
+    a.batch = (int)batch;
+    a.epilogue = epilogue;
+    a.rms = 0;
+    a.x16 = static_cast<const __half*>(d_x);
+    a.y = d_y;
+    a.ld = (int)(silu ? rows / 2 : rows);
+    a.sync = static_cast<unsigned int*>(sync);
+    return stream_gemv_launch(a, static_cast<cudaStream_t>(stream), true);
+}

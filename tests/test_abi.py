@@ -138,5 +138,19 @@ def test_argument_validation_without_gpu(ql):
     assert L.ql_decode_graph_replay(None, 1, 1, None) == ql.QL_EINVAL
     assert L.ql_model_set_option(None, ql.QL_OPT_STEP_KERNEL, ql.QL_STEP_AUTO) == ql.QL_EINVAL
     assert L.ql_model_persistent_max_batch(None) == 0
+    assert L.ql_q4_0_stream_pack(None, None, 16, 128, 0, None, None) == ql.QL_EINVAL
+    assert L.ql_gemv_q4_0_stream(None, 16, 128, None, 1, None, 0, None) == ql.QL_EINVAL
     assert L.ql_block_pool_create(0, ctypes.byref(ctypes.c_void_p())) == ql.QL_EINVAL
     assert ql.ql_paged_attn_workspace_bytes(0, 4, 2, 64, 16, 4) == 0
+
+
+def test_stream_layout_sizes(ql):
+    """Tile stream bytes: 16-row tiles (SiLU*up: 8 gate + 8 up rows) x cols/128 units of 1152 B;
+    0 for shapes the layout does not take."""
+    assert ql.ql_q4_0_stream_bytes(24576, 4096, 1) == 24576 * 4096 * 18 // 32
+    assert ql.ql_q4_0_stream_bytes(4096, 12288, 0) == 4096 * 12288 * 18 // 32
+    assert ql.ql_q4_0_stream_bytes(17, 128, 0) == 2 * 1152
+    assert ql.ql_q4_0_stream_bytes(18, 128, 1) == 2 * 1152
+    assert ql.ql_q4_0_stream_bytes(16, 96, 0) == 0
+    assert ql.ql_q4_0_stream_bytes(15, 128, 1) == 0
+    assert ql.ql_q4_0_stream_bytes(0, 128, 0) == 0

@@ -1,0 +1,159 @@
+"""The batch 1-2 q4_0 GEMV over the tile stream layout (ql_q4_0_stream_pack, ql_gemv_q4_0_stream).
+
+Layout: bit-exact against a NumPy restatement of the documented layout (16-row tiles, units of
+4 blocks x 16 rows of codes then the rows' 4 scales, gate/up row pairing for SiLU*up, zero
+rows past the matrix).
+
+GEMV: against the oracle (f64 dense product of the dequantised weights). Tolerance, from the
+kernel's arithmetic: activations are staged in f16 (exact here, the tests give f16), every code
+becomes q - 8 or 16 (q - 8) exactly in f16, a block's 32 products are summed in f16 (16
+products per accumulator, relative rounding 2^-11 per step), blocks are scaled and summed in
+f32. For N(0, 0.02) weights and N(0, 1) activations that is ~1e-3 of the output rms, so the bar
+is ``|y - y_ref| <= 1e-2 * rms(y_ref) + 1e-2 * |y_ref|``, the same as the row-major GEMV.
+"""
+import numpy as np
+import pytest
+import torch
+
+import ql_inputs
+from oracle import ops, q4_0 as oq
+
+from gpu_util import lib, dev, q4_dev, rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+def tile_rows(rows, silu, tile):
+    """Global rows of tile rows 0..15 (-1: past the matrix)."""
+    if silu:
+        half = rows // 2
+        i = tile * 8 + np.arange(8)
+        gate = np.where(i < half, i, -1)
+        up = np.where(i < half, half + i, -1)
+        return np.concatenate([gate, up])
+    r = tile * 16 + np.arange(16)
+    return np.where(r < rows, r, -1)
+
+
+def expected_stream(scales, quants, silu):
+    """The documented tile stream layout, restated with NumPy from the q4_0 arrays."""
+    rows, nblk = scales.shape
+    ntile = (rows // 2 + 7) // 8 if silu else (rows + 15) // 16
+    nst = nblk // 4
+    out = np.zeros((ntile, nst, 1152), np.uint8)
+    sbytes = scales.view(np.uint8).reshape(rows, nblk, 2)
+    for tile in range(ntile):
+        rr = tile_rows(rows, silu, tile)
+        for k in range(nst):
+            unit = out[tile, k]
+            for q in range(4):
+                for r in range(16):
+                    if rr[r] >= 0:
+                        unit[(q * 16 + r) * 16:(q * 16 + r + 1) * 16] = quants[rr[r], 4 * k + q]
+            for r in range(16):
+                if rr[r] >= 0:
+                    unit[1024 + r * 8:1024 + r * 8 + 8] = sbytes[rr[r], 4 * k:4 * k + 4].reshape(8)
+    return out.reshape(-1)
+
+
+def packed(w, silu):
+    ql = lib()
+    rows, cols = w.shape
+    s, q = oq.quantize(w)
+    ds, dq = q4_dev(s, q)
+    n = ql.ql_q4_0_stream_bytes(rows, cols, silu)
+    buf = torch.full((n,), 0xAB, dtype=torch.uint8, device="cuda")
+    ql.ql_q4_0_stream_pack(ds, dq, rows, cols, silu, buf)
+    torch.cuda.synchronize()
+    return s, q, buf
+
+
+@pytest.mark.parametrize("rows,cols,silu", [(16, 128, 0), (37, 256, 0), (200, 384, 1), (18, 128, 1)])
+def test_stream_layout_bit_exact(rows, cols, silu):
+    w = ql_inputs.gemv_weight(rows, cols, seed=21)
+    s, q, buf = packed(w, silu)
+    want = expected_stream(s, q, silu)
+    assert np.array_equal(buf.cpu().numpy(), want)
+
+
+def run(w, x, epilogue, residual=None):
+    ql = lib()
+    rows, cols = w.shape
+    silu = 1 if epilogue == ql.QL_EPI_SILU_MUL else 0
+    s, q, buf = packed(w, silu)
+    ref = ops.gemv(oq.dequantize(s, q), x.astype(np.float64))
+    B = x.shape[0]
+    if epilogue == ql.QL_EPI_SILU_MUL:
+        y = torch.full((B, rows // 2), float("nan"), dtype=torch.float16, device="cuda")
+    elif epilogue == ql.QL_EPI_ADD_RESIDUAL:
+        y = dev(residual.astype(np.float32))
+    else:
+        y = torch.full((B, rows), float("nan"), dtype=torch.float32, device="cuda")
+    ql.ql_gemv_q4_0_stream(buf, rows, cols, dev(x), B, y, epilogue)
+    torch.cuda.synchronize()
+    return y.float().cpu().numpy().astype(np.float64), ref
+
+
+def check_close(got, want, what):
+    rms = np.sqrt(np.mean(want * want))
+    err = np.abs(got - want)
+    bad = err > 1e-2 * rms + 1e-2 * np.abs(want)
+    assert not np.any(np.isnan(got)), what
+    assert not bad.any(), f"{what}: {bad.sum()} outside tolerance, max rel err {rel_err(got, want):.3e}"
+
+
+@pytest.mark.parametrize("rows,cols", [(16, 128), (37, 256), (1000, 4096), (4099, 1024), (96, 12288), (6144, 4096)])
+@pytest.mark.parametrize("batch", [1, 2])
+def test_stream_gemv_plain(rows, cols, batch):
+    ql = lib()
+    w = ql_inputs.gemv_weight(rows, cols, seed=2)
+    x = ql_inputs.gemv_activations(batch, cols, seed=3)
+    got, ref = run(w, x, ql.QL_EPI_NONE)
+    check_close(got, ref, f"stream gemv {rows}x{cols} b{batch}")
+
+
+@pytest.mark.parametrize("batch", [1, 2])
+def test_stream_gemv_residual(batch):
+    ql = lib()
+    w = ql_inputs.gemv_weight(300, 512, seed=5)
+    x = ql_inputs.gemv_activations(batch, 512, seed=6)
+    res = np.random.default_rng(1).standard_normal((batch, 300))
+    got, ref = run(w, x, ql.QL_EPI_ADD_RESIDUAL, residual=res)
+    check_close(got, ref + res.astype(np.float32).astype(np.float64), "residual")
+
+
+@pytest.mark.parametrize("batch", [1, 2])
+@pytest.mark.parametrize("inter", [8, 100, 768, 12288])
+def test_stream_gemv_silu_mul(batch, inter):
+    ql = lib()
+    w = ql_inputs.gemv_weight(2 * inter, 256, seed=7)
+    x = ql_inputs.gemv_activations(batch, 256, seed=8)
+    got, ref = run(w, x, ql.QL_EPI_SILU_MUL)
+    want = ops.swiglu(ref[:, :inter], ref[:, inter:])
+    check_close(got, want, f"silu_mul {inter}")
+
+
+def test_stream_gemv_zero_and_extreme_blocks():
+    ql = lib()
+    w = np.zeros((64, 256), np.float32)
+    w[1, ::32] = 5.0
+    w[2, 5::32] = -3.0
+    w[3] = np.linspace(-1, 1, 256, dtype=np.float32)
+    w[4:] = ql_inputs.gemv_weight(60, 256, seed=9)
+    x = ql_inputs.gemv_activations(2, 256, seed=10)
+    got, ref = run(w, x, ql.QL_EPI_NONE)
+    assert np.all(got[:, 0] == 0.0)
+    check_close(got, ref, "extreme blocks")
+
+
+def test_stream_gemv_rejects_bad_arguments():
+    ql = lib()
+    t = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+    x = torch.zeros((3, 128), dtype=torch.float16, device="cuda")
+    y = torch.zeros((3, 16), dtype=torch.float32, device="cuda")
+    for args in ((16, 128, 3), (16, 96, 1), (15, 128, 1)):
+        rows, cols, batch = args
+        epi = ql.QL_EPI_SILU_MUL if rows % 2 else ql.QL_EPI_NONE
+        with pytest.raises(ql.QLError) as e:
+            ql.ql_gemv_q4_0_stream(t, rows, cols, x, batch, y, epi)
+        assert e.value.status == ql.QL_EINVAL
