@@ -2,6 +2,7 @@
 // itself is in ql_persist.cuh; head_dim 64 in ql_persist_hd64.cu).
 #include "ql_persist.cuh"
 
+#include <cstdlib>
 #include <mutex>
 #include <set>
 #include <string>
@@ -62,6 +63,14 @@ static_assert(persist::kEpiF32 == QL_EPI_NONE && persist::kEpiResid == QL_EPI_AD
                   persist::kEpiSilu == QL_EPI_SILU_MUL && persist::kEpiLogits == kEpiArgmax,
               "epilogue codes");
 
+static int stream_gemv_warps() {
+    static const int w = [] {
+        const char* e = std::getenv("QL_STREAM_GEMV_WARPS");
+        return e && std::atoi(e) == 16 ? 16 : 8;
+    }();
+    return w;
+}
+
 int stream_gemv_prepare() {
     static std::mutex mu;
     static std::set<int> done;
@@ -69,8 +78,10 @@ int stream_gemv_prepare() {
     QL_TRY_CUDA(cudaGetDevice(&dev));
     std::lock_guard<std::mutex> lk(mu);
     if (done.count(dev)) return QL_OK;
-    cudaError_t e = persist::stream_gemv_one<1>(false, nullptr, nullptr, 0, 0, nullptr, false);
-    if (e == cudaSuccess) e = persist::stream_gemv_one<2>(false, nullptr, nullptr, 0, 0, nullptr, false);
+    cudaError_t e = persist::stream_gemv_one<1, 8>(false, nullptr, nullptr, 0, 0, nullptr, false);
+    if (e == cudaSuccess) e = persist::stream_gemv_one<2, 8>(false, nullptr, nullptr, 0, 0, nullptr, false);
+    if (e == cudaSuccess) e = persist::stream_gemv_one<1, 16>(false, nullptr, nullptr, 0, 0, nullptr, false);
+    if (e == cudaSuccess) e = persist::stream_gemv_one<2, 16>(false, nullptr, nullptr, 0, 0, nullptr, false);
     if (e != cudaSuccess) return cuda_error(e, "stream gemv: kernel attributes");
     done.insert(dev);
     return QL_OK;
@@ -104,9 +115,20 @@ int stream_gemv_launch(const StreamGemvArgs& a, cudaStream_t s, bool pdl) {
     g.norm_w = a.norm_w;
     g.y = a.y;
     g.ld = a.ld;
-    const size_t smem = persist::kRingBytes + persist::gemv_region_bytes(a.batch, a.M.nblk);
-    const cudaError_t e = a.batch == 1 ? persist::stream_gemv_one<1>(true, &p, &g, smem, num_sms(), s, pdl)
-                                       : persist::stream_gemv_one<2>(true, &p, &g, smem, num_sms(), s, pdl);
+    // CTAs of 8 warps (half-size rings): two fit on an SM, so a kernel's CTAs start, set up
+    // their rings and issue their first copies while the previous kernel's last CTAs finish;
+    // QL_STREAM_GEMV_WARPS=16 (one CTA per SM) for A/B measurements
+    const int warps = stream_gemv_warps();
+    const size_t smem = (size_t)warps * persist::kStages * persist::kSlotBytes +
+                        persist::gemv_region_bytes(a.batch, a.M.nblk, warps);
+    const int grid = num_sms() * (warps == 8 ? 2 : 1);
+    cudaError_t e;
+    if (warps == 8)
+        e = a.batch == 1 ? persist::stream_gemv_one<1, 8>(true, &p, &g, smem, grid, s, pdl)
+                         : persist::stream_gemv_one<2, 8>(true, &p, &g, smem, grid, s, pdl);
+    else
+        e = a.batch == 1 ? persist::stream_gemv_one<1, 16>(true, &p, &g, smem, grid, s, pdl)
+                         : persist::stream_gemv_one<2, 16>(true, &p, &g, smem, grid, s, pdl);
     if (e != cudaSuccess) return cuda_error(e, "stream gemv launch");
     return QL_OK;
 }

@@ -61,8 +61,8 @@ enum Epi { kEpiF32 = 0, kEpiResid = 1, kEpiSilu = 2, kEpiLogits = 3 };
 
 // Shared memory behind the rings: the GEMV staging (activations, offset terms, partials) or
 // the attention merge buffers, whichever is larger.
-__host__ __device__ constexpr size_t gemv_region_bytes(int batch, int max_nblk) {
-    return (size_t)batch * (max_nblk * 4 + 4) * 16 + kPartBytes;
+__host__ __device__ constexpr size_t gemv_region_bytes(int batch, int max_nblk, int warps = kW) {
+    return (size_t)batch * (max_nblk * 4 + 4) * 16 + (size_t)warps * 2 * 32 * 16;
 }
 __host__ __device__ constexpr size_t attn_region_bytes(int head_dim, int group) {
     return (size_t)kW * (group * head_dim > 128 ? group * head_dim : 128) * 4 + (size_t)2 * kW * group * 4;
@@ -186,8 +186,9 @@ __device__ __forceinline__ void cta_tiles(int ntile, int& t0, int& t1) {
     t0 = (int)((blockIdx.x * (unsigned)ntile) / gridDim.x);
     t1 = (int)(((blockIdx.x + 1) * (unsigned)ntile) / gridDim.x);
 }
-// First unit of warp w among the U units of its CTA (balanced to one unit).
-__device__ __forceinline__ int warp_unit(int U, int w) { return (w * U) / kW; }
+// First unit of warp w among the U units of its CTA of W warps (balanced to one unit).
+template <int W>
+__device__ __forceinline__ int warp_unit(int U, int w) { return (w * U) / W; }
 
 // Global row of row r (0..15) of a tile; rows past the matrix read row 0 and are discarded.
 __device__ __forceinline__ int tile_row(const PMat& M, int tile, int r, bool& ok) {
@@ -218,7 +219,8 @@ struct Ring {
     int dead;              // a wait ran out: issue and wait no more (the step is aborted)
 };
 
-// Move to the first matrix at or after r.wp in which this warp has units.
+// Move to the first matrix at or after r.wp in which this warp (of W) has units.
+template <int W>
 __device__ __forceinline__ void ring_seek(Ring& r, const PMat* mats, int warp) {
     for (; r.wp < r.nmat; ++r.wp) {
         const PMat& M = mats[r.wp];
@@ -226,7 +228,7 @@ __device__ __forceinline__ void ring_seek(Ring& r, const PMat* mats, int warp) {
         cta_tiles(M.ntile, t0, t1);
         const int nst = M.nblk / kUnitBlocks;
         const int U = (t1 - t0) * nst;
-        const int u0 = warp_unit(U, warp), u1 = warp_unit(U, warp + 1);
+        const int u0 = warp_unit<W>(U, warp), u1 = warp_unit<W>(U, warp + 1);
         if (u1 > u0) {
             r.u = u0;
             r.u_end = u1;
@@ -237,6 +239,7 @@ __device__ __forceinline__ void ring_seek(Ring& r, const PMat* mats, int warp) {
 }
 
 // Copy the next slot's units (up to kSlotUnits, not past the warp's range end).
+template <int W>
 __device__ __forceinline__ void ring_issue(Ring& r, const PMat* mats, int warp, int lane) {
     if (r.wp >= r.nmat || r.dead) return;
     const int n = min(kSlotUnits, r.u_end - r.u);
@@ -255,7 +258,7 @@ __device__ __forceinline__ void ring_issue(Ring& r, const PMat* mats, int warp, 
     r.u += n;
     if (r.u == r.u_end) {
         ++r.wp;
-        ring_seek(r, mats, warp);
+        ring_seek<W>(r, mats, warp);
     }
 }
 
@@ -298,10 +301,10 @@ __device__ __forceinline__ void ring_wait(Ring& r, const PersistParams& p, unsig
 // w) on the way; the first kHeld items of a thread and their weights are loaded together and
 // stay in registers between the two passes. f16 input: kChunk items per thread are loaded
 // together. Data written earlier in the launch by other CTAs is read with ld.global.cg (L2).
-template <bool RMS>
+template <bool RMS, int W>
 __device__ __noinline__ void stage_x(const PersistParams& p, int nblk, int cstride, const float* xf,
                                      const __half* x16, const float* w, uint4* xs, float* red) {
-    constexpr int kHeld = 2, kChunk = 4;
+    constexpr int kHeld = 2, kChunk = 4, kT = W * 32;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int B = p.B, cols = nblk * 32, nitems = B * nblk * 4;
 
@@ -381,7 +384,7 @@ __device__ __noinline__ void stage_x(const PersistParams& p, int nblk, int cstri
         __syncthreads();
         float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-        for (int i = 0; i < kW; ++i) {
+        for (int i = 0; i < W; ++i) {
             a0 += red[i * 2];
             a1 += red[i * 2 + 1];
         }
@@ -486,7 +489,7 @@ __device__ __noinline__ void finish_tile(const PersistParams& p, const PMat& M, 
 // high nibbles in separate accumulators), one FFMA per block applies the f16 scale in f32. (The
 // MMA form of the same product wastes 7 of the 8 columns of an m16n8k16 tile at batch 1-2, and
 // measured slower than the CUDA cores here.)
-template <int NB>
+template <int NB, int W>
 __device__ __noinline__ void gemv_phase(const PersistParams& p, const PMat* mats, int wp, int epi, bool rms,
                                         Ring& ring, const float* xf,
                                         const __half* x16, const float* norm_w, void* y, int ld,
@@ -497,12 +500,12 @@ __device__ __noinline__ void gemv_phase(const PersistParams& p, const PMat* mats
     const PMat M = mats[wp];
     const int cstride = p.max_nblk * 4 + 4;   // uint4 units between staged columns (+64 B)
     uint4* xs = reinterpret_cast<uint4*>(region);
-    float4* part = reinterpret_cast<float4*>(xs + (size_t)NB * cstride);   // [kW][2][32]
+    float4* part = reinterpret_cast<float4*>(xs + (size_t)NB * cstride);   // [W][2][32]
 
     if (rms)
-        stage_x<true>(p, M.nblk, cstride, xf, x16, norm_w, xs, red);
+        stage_x<true, W>(p, M.nblk, cstride, xf, x16, norm_w, xs, red);
     else
-        stage_x<false>(p, M.nblk, cstride, xf, x16, norm_w, xs, red);
+        stage_x<false, W>(p, M.nblk, cstride, xf, x16, norm_w, xs, red);
     __syncthreads();
     stamp(tr, 2);
 
@@ -511,8 +514,8 @@ __device__ __noinline__ void gemv_phase(const PersistParams& p, const PMat* mats
     int T0, T1;
     cta_tiles(M.ntile, T0, T1);
     const int U = (T1 - T0) * nst;
-    const int u0 = warp_unit(U, warp), u1 = warp_unit(U, warp + 1);
-    const unsigned char* ring_g = reinterpret_cast<const unsigned char*>(region) - kRingBytes +
+    const int u0 = warp_unit<W>(U, warp), u1 = warp_unit<W>(U, warp + 1);
+    const unsigned char* ring_g = reinterpret_cast<const unsigned char*>(region) - (size_t)W * kStages * kSlotBytes +
                                   (size_t)warp * kStages * kSlotBytes;
 
     unsigned long long best[NB];
@@ -608,7 +611,7 @@ __device__ __noinline__ void gemv_phase(const PersistParams& p, const PMat* mats
         }
         __syncwarp();
         ++r.consumed;
-        ring_issue(r, mats, warp, lane);   // refill the slot just read
+        ring_issue<W>(r, mats, warp, lane);   // refill the slot just read
         u += n;
     }
     ring = r;
@@ -628,7 +631,7 @@ __device__ __noinline__ void gemv_phase(const PersistParams& p, const PMat* mats
 #pragma unroll
             for (int b = 0; b < NB; ++b) s2[b] = 0.f;
             for (int w2 = 0; w2 <= warp; ++w2) {
-                const int a0 = warp_unit(U, w2), a1 = warp_unit(U, w2 + 1);
+                const int a0 = warp_unit<W>(U, w2), a1 = warp_unit<W>(U, w2 + 1);
                 if (a1 <= a0 || a1 <= ts || a0 >= ts + nst) continue;
                 const int sl = (T0 + a0 / nst == first_tile) ? 0 : 1;
                 const float4 v = part[(w2 * 2 + sl) * 32 + lane];
@@ -652,7 +655,7 @@ __device__ __noinline__ void gemv_phase(const PersistParams& p, const PMat* mats
         if (tid < NB) {
             unsigned long long m = 0ull;
 #pragma unroll
-            for (int i = 0; i < kW; ++i) m = kred[i][tid] > m ? kred[i][tid] : m;
+            for (int i = 0; i < W; ++i) m = kred[i][tid] > m ? kred[i][tid] : m;
             const bool act = p.active == nullptr || p.active[tid] != 0;
             if (m && act) atomicMax(p.keys + tid, m);
         }
@@ -1085,27 +1088,27 @@ __device__ void step_body(const PersistParams& p, const PMat* mats, Ring& r, uns
         const PLayer* Ly = p.layers + l;
         attn_prefetch<HD>(p, l);
         // q|k|v = W_qkv rmsnorm(x, attn_norm)
-        gemv_phase<NB>(p, mats, 4 * l, kEpiF32, true, r, p.x, nullptr, Ly->attn_norm, p.qkv, qkv_ld, region, red,
+        gemv_phase<NB, kW>(p, mats, 4 * l, kEpiF32, true, r, p.x, nullptr, Ly->attn_norm, p.qkv, qkv_ld, region, red,
                                       kred, row());
         if (!grid_barrier(p, target, flag)) return;
         // qk-norm + RoPE + KV append + paged attention -> attn
         attn_phase<HD, G>(p, l, region, qs, flag, row());
         if (!grid_barrier(p, target, flag)) return;
         // x += W_o attn
-        gemv_phase<NB>(p, mats, 4 * l + 1, kEpiResid, false, r, nullptr, p.attn, nullptr, p.x, p.hidden, region, red,
+        gemv_phase<NB, kW>(p, mats, 4 * l + 1, kEpiResid, false, r, nullptr, p.attn, nullptr, p.x, p.hidden, region, red,
                                          kred, row());
         if (!grid_barrier(p, target, flag)) return;
         // act = silu(gate) * up, [gate | up] = W_gu rmsnorm(x, ffn_norm)
-        gemv_phase<NB>(p, mats, 4 * l + 2, kEpiSilu, true, r, p.x, nullptr, Ly->ffn_norm, p.act, p.inter, region, red,
+        gemv_phase<NB, kW>(p, mats, 4 * l + 2, kEpiSilu, true, r, p.x, nullptr, Ly->ffn_norm, p.act, p.inter, region, red,
                                        kred, row());
         if (!grid_barrier(p, target, flag)) return;
         // x += W_down act
-        gemv_phase<NB>(p, mats, 4 * l + 3, kEpiResid, false, r, nullptr, p.act, nullptr, p.x, p.hidden, region, red,
+        gemv_phase<NB, kW>(p, mats, 4 * l + 3, kEpiResid, false, r, nullptr, p.act, nullptr, p.x, p.hidden, region, red,
                                          kred, row());
         if (!grid_barrier(p, target, flag)) return;
     }
     // logits = W_lm rmsnorm(x, final_norm), greedy argmax keys
-    gemv_phase<NB>(p, mats, 4 * p.n_layers, kEpiLogits, true, r, p.x, nullptr, p.final_norm, p.logits, p.vocab, region,
+    gemv_phase<NB, kW>(p, mats, 4 * p.n_layers, kEpiLogits, true, r, p.x, nullptr, p.final_norm, p.logits, p.vocab, region,
                                      red, kred, row());
     if (!grid_barrier(p, target, flag)) return;
     if (blockIdx.x == 0) finalize(p);
@@ -1149,10 +1152,10 @@ __global__ void __launch_bounds__(kT, 1) step_kernel(const __grid_constant__ Per
     r.dead = 0;
     r.base = static_cast<uint32_t>(__cvta_generic_to_shared(smem)) + (uint32_t)(warp * kStages * kSlotBytes);
     r.mbar = static_cast<uint32_t>(__cvta_generic_to_shared(&mbar[warp * kStages]));
-    ring_seek(r, mats, warp);
+    ring_seek<kW>(r, mats, warp);
     // the weights do not depend on anything computed in the step: start streaming at once
 #pragma unroll 1
-    for (int i = 0; i < kStages; ++i) ring_issue(r, mats, warp, lane);
+    for (int i = 0; i < kStages; ++i) ring_issue<kW>(r, mats, warp, lane);
     if (p.B == 1)
         step_body<HD, G, 1>(p, mats, r, region, qs, red, kred, &flag);
     else
@@ -1214,14 +1217,14 @@ struct StreamGemv {
     int ld;
 };
 
-template <int NB>
-__global__ void __launch_bounds__(kT, 1) gemv_stream_kernel(const __grid_constant__ PersistParams p,
-                                                             const __grid_constant__ StreamGemv g) {
+template <int NB, int W>
+__global__ void __launch_bounds__(W * 32, 16 / W) gemv_stream_kernel(const __grid_constant__ PersistParams p,
+                                                                      const __grid_constant__ StreamGemv g) {
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ PMat mat;
-    __shared__ float red[kW * 2];
-    __shared__ unsigned long long kred[kW][kMaxB];
-    __shared__ __align__(8) unsigned long long mbar[kW * kStages];
+    __shared__ float red[W * 2];
+    __shared__ unsigned long long kred[W][kMaxB];
+    __shared__ __align__(8) unsigned long long mbar[W * kStages];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) mat = g.M;
     if (lane == 0)
@@ -1239,13 +1242,13 @@ __global__ void __launch_bounds__(kT, 1) gemv_stream_kernel(const __grid_constan
     r.dead = 0;
     r.base = static_cast<uint32_t>(__cvta_generic_to_shared(smem)) + (uint32_t)(warp * kStages * kSlotBytes);
     r.mbar = static_cast<uint32_t>(__cvta_generic_to_shared(&mbar[warp * kStages]));
-    ring_seek(r, &mat, warp);
+    ring_seek<W>(r, &mat, warp);
 #pragma unroll 1
-    for (int i = 0; i < kStages; ++i) ring_issue(r, &mat, warp, lane);
+    for (int i = 0; i < kStages; ++i) ring_issue<W>(r, &mat, warp, lane);
     pdl_trigger();
     pdl_wait();
-    gemv_phase<NB>(p, &mat, 0, g.epi, g.rms != 0, r, g.xf, g.x16, g.norm_w, g.y, g.ld, smem + kRingBytes, red, kred,
-                   nullptr);
+    gemv_phase<NB, W>(p, &mat, 0, g.epi, g.rms != 0, r, g.xf, g.x16, g.norm_w, g.y, g.ld,
+                      smem + (size_t)W * kStages * kSlotBytes, red, kred, nullptr);
     const unsigned long long t0 = global_ns();
     while (r.consumed < r.issued) {   // only after a wait ran out: let copies land (bounded)
         const uint32_t mb = r.mbar + (r.consumed % kStages) * 8, parity = (r.consumed / kStages) & 1u;
@@ -1310,11 +1313,12 @@ cudaError_t dispatch(int G, bool launch, const PersistParams* p, size_t smem, in
 }
 
 template <typename K, typename... Args>
-cudaError_t launch_kernel_pdl(K kernel, int grid, size_t smem, cudaStream_t s, bool pdl, const Args&... args) {
-    return ql::launch(kernel, dim3(grid), dim3(kT), smem, s, pdl, args...);
+cudaError_t launch_kernel_pdl(K kernel, int grid, int threads, size_t smem, cudaStream_t s, bool pdl,
+                              const Args&... args) {
+    return ql::launch(kernel, dim3(grid), dim3(threads), smem, s, pdl, args...);
 }
 
-template <int NB>
+template <int NB, int W>
 cudaError_t stream_gemv_one(bool launch, const PersistParams* p, const StreamGemv* g, size_t smem, int grid,
                             cudaStream_t s, bool pdl) {
     if (!launch) {
@@ -1322,13 +1326,13 @@ cudaError_t stream_gemv_one(bool launch, const PersistParams* p, const StreamGem
         cudaFuncAttributes fa = {};
         cudaError_t e = cudaGetDevice(&dev);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, gemv_stream_kernel<NB>);
+        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, gemv_stream_kernel<NB, W>);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(gemv_stream_kernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            e = cudaFuncSetAttribute(gemv_stream_kernel<NB, W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      optin - (int)fa.sharedSizeBytes);
         return e;
     }
-    return launch_kernel_pdl(gemv_stream_kernel<NB>, grid, smem, s, pdl, *p, *g);
+    return launch_kernel_pdl(gemv_stream_kernel<NB, W>, grid, W * 32, smem, s, pdl, *p, *g);
 }
 
 }  // namespace persist
