@@ -66,7 +66,7 @@ static_assert(persist::kEpiF32 == QL_EPI_NONE && persist::kEpiResid == QL_EPI_AD
 static int stream_gemv_warps() {
     static const int w = [] {
         const char* e = std::getenv("QL_STREAM_GEMV_WARPS");
-        return e && std::atoi(e) == 16 ? 16 : 8;
+        return e && std::atoi(e) == 8 ? 8 : 16;
     }();
     return w;
 }
@@ -115,9 +115,9 @@ int stream_gemv_launch(const StreamGemvArgs& a, cudaStream_t s, bool pdl) {
     g.norm_w = a.norm_w;
     g.y = a.y;
     g.ld = a.ld;
-    // CTAs of 8 warps (half-size rings): two fit on an SM, so a kernel's CTAs start, set up
-    // their rings and issue their first copies while the previous kernel's last CTAs finish;
-    // QL_STREAM_GEMV_WARPS=16 (one CTA per SM) for A/B measurements
+    // one CTA of 16 warps per SM (measured faster in the step than two CTAs of 8 warps, which
+    // would let a kernel's set-up overlap the previous kernel's tail); QL_STREAM_GEMV_WARPS=8
+    // selects the two-CTA form for A/B measurements
     const int warps = stream_gemv_warps();
     const size_t smem = (size_t)warps * persist::kStages * persist::kSlotBytes +
                         persist::gemv_region_bytes(a.batch, a.M.nblk, warps);
