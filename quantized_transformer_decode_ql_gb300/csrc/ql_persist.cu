@@ -3,6 +3,7 @@
 #include "ql_persist.cuh"
 
 #include <cstdlib>
+#include <map>
 #include <mutex>
 #include <set>
 #include <string>
@@ -199,8 +200,23 @@ extern "C" int ql_gemv_q4_0_stream(const void* d_stream, int64_t rows, int64_t c
     QL_REQUIRE(batch == 1 || batch == 2, "ql_gemv_q4_0_stream: batch must be 1 or 2");
     QL_REQUIRE(aligned(d_stream, 16) && aligned(d_x, 16) && aligned(d_y, 4),
                "ql_gemv_q4_0_stream: stream and x must be 16-byte aligned, y 4-byte");
+    // the flag's address, resolved once per device (the lookup may load the module lazily,
+    // which a stream capture does not allow; the first call should come before any capture)
+    static std::mutex mu;
+    static std::map<int, void*> addr;
+    int dev = 0;
+    QL_TRY_CUDA(cudaGetDevice(&dev));
     void* sync = nullptr;
-    QL_TRY_CUDA(cudaGetSymbolAddress(&sync, g_stream_gemv_sync));
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        auto it = addr.find(dev);
+        if (it == addr.end()) {
+            QL_TRY_CUDA(cudaGetSymbolAddress(&sync, g_stream_gemv_sync));
+            addr[dev] = sync;
+        } else {
+            sync = it->second;
+        }
+    }
     StreamGemvArgs a = {};
     a.M = stream_mat(d_stream, rows, cols, silu);
     a.batch = (int)batch;
