@@ -128,25 +128,19 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AParams p, Dev
 
     const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    // Fused decode-step form (qkv set): the context length and the K/V of earlier positions are
+    // final before this kernel starts (every kernel of the step triggers its successor only
+    // after its own wait, so everything two launches back has completed), and the new
+    // position's row is appended by this kernel: the first K/V tiles are staged before the
+    // wait and the new row is patched into them. Otherwise q, K/V or the lengths may come from
+    // the previous kernel: wait first.
+    const bool fused = p.qkv != nullptr;
     l2_prefetch_share(p.next.ptr[0], p.next.bytes[0]);
     l2_prefetch_share(p.next.ptr[1], p.next.bytes[1]);
-    if (p.prefetch && (p.active == nullptr || p.active[b] != 0)) {
-        // In the decode step the context length comes from the position, which is final before
-        // this kernel starts; only the newest slot is still being written (prefetch is a hint).
-        const int Lp = p.positions[b] + 1;
-        const int b0 = s * p.spb, b1 = min((Lp + kBS - 1) / kBS, b0 + p.spb);
-        if (Lp <= p.maxb * kBS && (int)threadIdx.x < 2 * (b1 - b0) && b0 < b1) {
-            const int blk = b0 + (threadIdx.x >> 1);
-            const int phys = p.block_tables[(size_t)b * p.maxb + blk];
-            if (phys >= 0 && phys < p.num_blocks) {
-                const __half* base = (threadIdx.x & 1) ? p.v_pool : p.k_pool;
-                const __half* t = base + ((size_t)phys * p.n_kv + g) * kBS * HD;
-                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(t), "r"((uint32_t)(kBS * HD * 2)) : "memory");
-            }
-        }
+    if (!fused) {
+        pdl_wait();
+        pdl_trigger();
     }
-    pdl_wait();
-    pdl_trigger();
     if (p.active && p.active[b] == 0) return;
     const int L = p.context_lens ? p.context_lens[b] : p.positions[b] + 1;
     if (L <= 0) return;   // idle slot
@@ -159,58 +153,8 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AParams p, Dev
     if (s >= n_active) return;
     const int blk0 = s * p.spb;
     const int blk1 = min(nblocks, blk0 + p.spb);
+    const int pos = L - 1, lblk = pos / kBS, kp = pos % kBS;
 
-    // Q as the A operand of S = Q K^T: rows = the G heads of this kv head (rows >= G and the
-    // fragment's rows g + 8 are zero padding); lane (gq, tq) holds dims 16 kk + 2 tq (+8).
-    const int gq = lane >> 2, tq = lane & 3;
-    const bool hv = gq < G;
-    uint32_t qa[KSTEPS][2];
-    __shared__ __align__(16) __half qs[G][HD];
-    const __half* qsrc;
-    if (p.qkv) {
-        // fused step: normalise + rotate the G query heads here; the CTA holding the new
-        // position's block also normalises + rotates the new key and appends K and V
-        const int pos = L - 1;
-        const float* src = p.qkv + (size_t)b * (p.n_heads + 2 * p.n_kv) * HD;
-        const bool pos_ok = pos < p.max_position;
-        if (!pos_ok && s == 0 && threadIdx.x == 0) record_device_error(err, kErrRopePosition, b, pos);
-        const float* cr = p.cos_t + (size_t)(pos_ok ? pos : 0) * (HD / 2);
-        const float* sr = p.sin_t + (size_t)(pos_ok ? pos : 0) * (HD / 2);
-        for (int h = warp; h < G; h += kAttnWarps)
-            warp_norm_rope<HD>(src + (size_t)(g * G + h) * HD, p.q_norm, cr, sr, p.eps, qs[h], lane);
-        const int lblk = pos / kBS;
-        if (pos_ok && lblk >= blk0 && lblk < blk1 && warp < 2) {
-            const int phys = bt_row_phys(p, b, lblk);
-            if (phys < 0) {
-                if (lane == 0) record_device_error(err, kErrRopeBlock, (long long)b * p.maxb + lblk, phys);
-            } else {
-                const size_t off = (((size_t)phys * p.n_kv + g) * kBS + (pos % kBS)) * HD;
-                if (warp == 0) {
-                    warp_norm_rope<HD>(src + (size_t)(p.n_heads + g) * HD, p.k_norm, cr, sr, p.eps, p.kw + off, lane);
-                } else {
-                    const float* vs = src + (size_t)(p.n_heads + p.n_kv + g) * HD;
-                    for (int i = lane; i < HD; i += 32) p.vw[off + i] = __float2half_rn(vs[i]);
-                }
-            }
-        }
-        __threadfence_block();
-        __syncthreads();
-        qsrc = &qs[0][0];
-    } else {
-        qsrc = p.q + ((size_t)b * p.n_heads + g * G) * HD;
-    }
-    {
-        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(qsrc + (size_t)(hv ? gq : 0) * HD);
-#pragma unroll
-        for (int kk = 0; kk < KSTEPS; ++kk) {
-            qa[kk][0] = hv ? qrow[8 * kk + tq] : 0u;
-            qa[kk][1] = hv ? qrow[8 * kk + 4 + tq] : 0u;
-        }
-    }
-    float o[NT][4];
-#pragma unroll
-    for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-    float mrow = -INFINITY, lrow = 0.f;
     const int32_t* bt = p.block_tables + (size_t)b * p.maxb;
     unsigned char* wtiles = asmem + (size_t)warp * 4 * TILE;        // [buffer][K | V]
     const uint32_t wtiles_s = static_cast<uint32_t>(__cvta_generic_to_shared(wtiles));
@@ -238,8 +182,72 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AParams p, Dev
         asm volatile("cp.async.commit_group;" ::: "memory");
         return ok;
     };
+    bool vcur = false;
+    if (fused) {
+        if (nb_w > 0) vcur = stage(0);
+        pdl_wait();
+        pdl_trigger();
+    }
 
-    bool vcur = nb_w > 0 ? stage(0) : false;
+    // Q as the A operand of S = Q K^T: rows = the G heads of this kv head (rows >= G and the
+    // fragment's rows g + 8 are zero padding); lane (gq, tq) holds dims 16 kk + 2 tq (+8).
+    const int gq = lane >> 2, tq = lane & 3;
+    const bool hv = gq < G;
+    uint32_t qa[KSTEPS][2];
+    __shared__ __align__(16) __half qs[G][HD];
+    __shared__ __align__(16) __half knew[HD];   // the appended K row (normed, rotated) and V row
+    __shared__ __align__(16) __half vnew[HD];
+    const __half* qsrc;
+    if (fused) {
+        // normalise + rotate the G query heads here; the CTA holding the new position's block
+        // also normalises + rotates the new key and appends K and V
+        const float* src = p.qkv + (size_t)b * (p.n_heads + 2 * p.n_kv) * HD;
+        const bool pos_ok = pos < p.max_position;
+        if (!pos_ok && s == 0 && threadIdx.x == 0) record_device_error(err, kErrRopePosition, b, pos);
+        const float* cr = p.cos_t + (size_t)(pos_ok ? pos : 0) * (HD / 2);
+        const float* sr = p.sin_t + (size_t)(pos_ok ? pos : 0) * (HD / 2);
+        for (int h = warp; h < G; h += kAttnWarps)
+            warp_norm_rope<HD>(src + (size_t)(g * G + h) * HD, p.q_norm, cr, sr, p.eps, qs[h], lane);
+        if (pos_ok && lblk >= blk0 && lblk < blk1 && warp < 2) {
+            const int phys = bt_row_phys(p, b, lblk);
+            if (phys < 0) {
+                if (lane == 0) record_device_error(err, kErrRopeBlock, (long long)b * p.maxb + lblk, phys);
+            } else {
+                const size_t off = (((size_t)phys * p.n_kv + g) * kBS + kp) * HD;
+                if (warp == 0) {
+                    warp_norm_rope<HD>(src + (size_t)(p.n_heads + g) * HD, p.k_norm, cr, sr, p.eps, knew, lane);
+                    __syncwarp();
+                    for (int i = lane; i < HD / 8; i += 32)
+                        reinterpret_cast<uint4*>(p.kw + off)[i] = reinterpret_cast<const uint4*>(knew)[i];
+                } else {
+                    const float* vs = src + (size_t)(p.n_heads + p.n_kv + g) * HD;
+                    for (int i = lane; i < HD; i += 32) {
+                        const __half v = __float2half_rn(vs[i]);
+                        vnew[i] = v;
+                        p.vw[off + i] = v;
+                    }
+                }
+            }
+        }
+        __threadfence_block();
+        __syncthreads();
+        qsrc = &qs[0][0];
+    } else {
+        qsrc = p.q + ((size_t)b * p.n_heads + g * G) * HD;
+    }
+    {
+        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(qsrc + (size_t)(hv ? gq : 0) * HD);
+#pragma unroll
+        for (int kk = 0; kk < KSTEPS; ++kk) {
+            qa[kk][0] = hv ? qrow[8 * kk + tq] : 0u;
+            qa[kk][1] = hv ? qrow[8 * kk + 4 + tq] : 0u;
+        }
+    }
+    float o[NT][4];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    float mrow = -INFINITY, lrow = 0.f;
+    if (!fused && nb_w > 0) vcur = stage(0);
     for (int i = 0; i < nb_w; ++i) {
         bool vnext = false;
         if (i + 1 < nb_w) vnext = stage(i + 1);
@@ -248,6 +256,16 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AParams p, Dev
         __syncwarp();
         const int blk = blk0 + warp + kAttnWarps * i;
         const int nt = min(kBS, L - blk * kBS);      // valid keys in this block
+        if (vcur && fused && blk == lblk) {
+            // the new row: staged (possibly) before it was appended, so patch it in
+            unsigned char* kt = wtiles + (size_t)(i & 1) * 2 * TILE;
+            if (lane < CHUNKS)
+                *reinterpret_cast<uint4*>(kt + kp * PITCH + lane * 16) = reinterpret_cast<const uint4*>(knew)[lane];
+            else if (lane < 2 * CHUNKS)
+                *reinterpret_cast<uint4*>(kt + TILE + kp * PITCH + (lane - CHUNKS) * 16) =
+                    reinterpret_cast<const uint4*>(vnew)[lane - CHUNKS];
+            __syncwarp();
+        }
         if (vcur) {
             unsigned char* vtile = wtiles + (size_t)(i & 1) * 2 * TILE + TILE;
             if (nt < kBS) {

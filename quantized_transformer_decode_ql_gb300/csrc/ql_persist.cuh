@@ -1245,8 +1245,10 @@ __global__ void __launch_bounds__(W * 32, 16 / W) gemv_stream_kernel(const __gri
     ring_seek<W>(r, &mat, warp);
 #pragma unroll 1
     for (int i = 0; i < kStages; ++i) ring_issue<W>(r, &mat, warp, lane);
-    pdl_trigger();
+    // the trigger follows the wait in every kernel of the step: a kernel's code before its
+    // wait then runs only after the kernel two launches back has completed
     pdl_wait();
+    pdl_trigger();
     gemv_phase<NB, W>(p, &mat, 0, g.epi, g.rms != 0, r, g.xf, g.x16, g.norm_w, g.y, g.ld,
                       smem + (size_t)W * kStages * kSlotBytes, red, kred, nullptr);
     const unsigned long long t0 = global_ns();
