@@ -22,6 +22,8 @@
 #include <cuda_fp16.h>
 #include <math.h>
 
+#include <cstdlib>
+
 #include <mutex>
 #include <set>
 
@@ -443,7 +445,12 @@ Layout layout(int64_t batch, int n_heads, int n_kv, int head_dim, int64_t maxb, 
     const int64_t pairs = batch * n_kv;
     const int64_t target = 8ll * sms;
     int64_t spb = (maxb * pairs + target - 1) / target;
-    if (spb < 4) spb = 4;
+    static const int64_t min_spb = [] {   // QL_ATTN_MIN_SPB overrides the floor for A/B measurements
+        const char* e = std::getenv("QL_ATTN_MIN_SPB");
+        const int v = e ? std::atoi(e) : 4;
+        return (int64_t)(v < 1 ? 1 : v > 256 ? 256 : v);
+    }();
+    if (spb < min_spb) spb = min_spb;
     if (spb > maxb) spb = maxb;
     if (spb < 1) spb = 1;
     if ((maxb + spb - 1) / spb > kMaxSplit) spb = (maxb + kMaxSplit - 1) / kMaxSplit;
