@@ -382,54 +382,41 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AParams p, Dev
     __syncthreads();
     if (!last_flag) return;
     __threadfence();
-    // merge: per-split weights exp2(m_k - M) / L into shared memory (one warp per head), then
-    // every thread sums float4 chunks of the partial outputs with independent loads
-    float (*sw)[kMaxSplit] = reinterpret_cast<float (*)[kMaxSplit]>(asmem + (size_t)kAttnWarps * G * HD * 4);
-    for (int h = warp; h < G; h += kAttnWarps) {
-        const size_t base = ((size_t)b * n_heads + g * G + h) * p.nsplit;
-        float M = -INFINITY;
-        for (int k = lane; k < n_active; k += 32) M = fmaxf(M, __ldcg(p.pm + base + k));
-#pragma unroll
-        for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        float Ls = 0.f;
-        for (int k = lane; k < n_active; k += 32) {
-            const float f = exp2f(__ldcg(p.pm + base + k) - M);
-            sw[h][k] = f;
-            Ls += f * __ldcg(p.pl + base + k);
-        }
-#pragma unroll
-        for (int o = 16; o; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
-        const float inv = 1.0f / Ls;
-        __syncwarp();
-        for (int k = lane; k < n_active; k += 32) sw[h][k] *= inv;
-    }
-    __syncthreads();
+    // merge: one pass per float4 output over the splits (online softmax in the exp2 domain),
+    // the (m, l, acc) loads of 8 splits issued together
     for (int i = threadIdx.x; i < G * HD / 4; i += kAttnThreads) {
         const int h = i / (HD / 4), d4 = i - h * (HD / 4);
         const size_t base = ((size_t)b * n_heads + g * G + h) * p.nsplit;
-        const float4* src = reinterpret_cast<const float4*>(p.pacc) + base * (HD / 4) + d4;
+        const float4* srcp = reinterpret_cast<const float4*>(p.pacc) + base * (HD / 4) + d4;
+        float M = -INFINITY, Ls = 0.f;
         float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
-        int k = 0;
-        for (; k + 8 <= n_active; k += 8) {
-            float4 v[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) v[u] = __ldcg(src + (size_t)(k + u) * (HD / 4));
+        for (int k0 = 0; k0 < n_active; k0 += 8) {
+            float mk[8], lk[8];
+            float4 ak[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                const float w = sw[h][k + u];
-                A.x = fmaf(w, v[u].x, A.x); A.y = fmaf(w, v[u].y, A.y);
-                A.z = fmaf(w, v[u].z, A.z); A.w = fmaf(w, v[u].w, A.w);
+                if (k0 + u < n_active) {
+                    mk[u] = __ldcg(p.pm + base + k0 + u);
+                    lk[u] = __ldcg(p.pl + base + k0 + u);
+                    ak[u] = __ldcg(srcp + (size_t)(k0 + u) * (HD / 4));
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (k0 + u < n_active && mk[u] != -INFINITY) {
+                    const float mn = fmaxf(M, mk[u]);
+                    const float fo = exp2f(M - mn), fk = exp2f(mk[u] - mn);
+                    Ls = Ls * fo + lk[u] * fk;
+                    A.x = A.x * fo + ak[u].x * fk; A.y = A.y * fo + ak[u].y * fk;
+                    A.z = A.z * fo + ak[u].z * fk; A.w = A.w * fo + ak[u].w * fk;
+                    M = mn;
+                }
             }
         }
-        for (; k < n_active; ++k) {
-            const float4 v = __ldcg(src + (size_t)k * (HD / 4));
-            const float w = sw[h][k];
-            A.x = fmaf(w, v.x, A.x); A.y = fmaf(w, v.y, A.y);
-            A.z = fmaf(w, v.z, A.z); A.w = fmaf(w, v.w, A.w);
-        }
+        const float inv = 1.0f / Ls;
         __half* o = p.out + ((size_t)b * n_heads + g * G + h) * HD + d4 * 4;
-        *reinterpret_cast<__half2*>(o) = __floats2half2_rn(A.x, A.y);
-        *reinterpret_cast<__half2*>(o + 2) = __floats2half2_rn(A.z, A.w);
+        *reinterpret_cast<__half2*>(o) = __floats2half2_rn(A.x * inv, A.y * inv);
+        *reinterpret_cast<__half2*>(o + 2) = __floats2half2_rn(A.z * inv, A.w * inv);
     }
     if (threadIdx.x == 0) p.tickets[b * p.n_kv + g] = 0;   // re-arm for the next call
 }
@@ -445,9 +432,11 @@ Layout layout(int64_t batch, int n_heads, int n_kv, int head_dim, int64_t maxb, 
     const int64_t pairs = batch * n_kv;
     const int64_t target = 8ll * sms;
     int64_t spb = (maxb * pairs + target - 1) / target;
-    static const int64_t min_spb = [] {   // QL_ATTN_MIN_SPB overrides the floor for A/B measurements
+    // at least 8 blocks per split (measured best at batch 1: 4 gives more partials to merge,
+    // 16 too few CTAs); QL_ATTN_MIN_SPB overrides the floor for A/B measurements
+    static const int64_t min_spb = [] {
         const char* e = std::getenv("QL_ATTN_MIN_SPB");
-        const int v = e ? std::atoi(e) : 4;
+        const int v = e ? std::atoi(e) : 8;
         return (int64_t)(v < 1 ? 1 : v > 256 ? 256 : v);
     }();
     if (spb < min_spb) spb = min_spb;
@@ -475,7 +464,7 @@ Layout layout(int64_t batch, int n_heads, int n_kv, int head_dim, int64_t maxb, 
 template <int HD, int G>
 constexpr size_t attn_smem() {
     const size_t tiles = (size_t)kAttnWarps * 4 * kBS * (HD * 2 + 16);
-    const size_t merge = (size_t)kAttnWarps * G * HD * 4 + (size_t)G * kMaxSplit * 4;
+    const size_t merge = (size_t)kAttnWarps * G * HD * 4;
     return tiles > merge ? tiles : merge;
 }
 
