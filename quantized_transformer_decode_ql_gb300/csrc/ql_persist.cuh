@@ -56,6 +56,7 @@ constexpr int kMaxSplit = 256;
 constexpr int kPartBytes = kW * 2 * 32 * 16;   // per-warp partial fragments of shared tiles
 constexpr int kTraceWords = 8;                 // trace entries per (row, CTA)
 constexpr int kFastSpins = 4096;               // polls of a wait before its clock starts
+constexpr uint32_t kSuspendNs = 2000;          // suspend-time hint of one mbarrier poll
 
 enum Epi { kEpiF32 = 0, kEpiResid = 1, kEpiSilu = 2, kEpiLogits = 3 };
 
@@ -262,12 +263,15 @@ __device__ __forceinline__ void ring_issue(Ring& r, const PMat* mats, int warp, 
     }
 }
 
+// Test (and wait a while for) the completion of phase `parity` of an mbarrier: the hardware
+// suspends the warp until the phase completes or about kSuspendNs pass, so waiting warps do
+// not spin on issue slots that the warps with data need.
 __device__ __forceinline__ bool mbar_test(uint32_t mb, uint32_t parity) {
     uint32_t done;
     asm volatile(
-        "{\n .reg .pred q;\n mbarrier.try_wait.parity.shared::cta.b64 q, [%1], %2;\n selp.u32 %0, 1, 0, q;\n}"
+        "{\n .reg .pred q;\n mbarrier.try_wait.parity.shared::cta.b64 q, [%1], %2, %3;\n selp.u32 %0, 1, 0, q;\n}"
         : "=r"(done)
-        : "r"(mb), "r"(parity)
+        : "r"(mb), "r"(parity), "r"(kSuspendNs)
         : "memory");
     return done != 0;
 }
