@@ -36,10 +36,6 @@ constexpr int kAttnWarps = 4;
 constexpr int kAttnThreads = kAttnWarps * 32;
 constexpr int kBS = 16;   // tokens per KV block
 constexpr int kMaxSplit = 256;   // splits per (sequence, kv head), bounded by the host
-// K/V tile buffers per warp: one (35 KB per CTA at head_dim 128) leaves room on an SM for a
-// CTA of the next GEMV, whose set-up then overlaps the attention; with the default split size
-// a warp has one or two blocks, so a second buffer would overlap little.
-constexpr int kAttnBufs = 1;
 
 struct AParams {
     const __half* q;
@@ -162,7 +158,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AParams p, Dev
     const int pos = L - 1, lblk = pos / kBS, kp = pos % kBS;
 
     const int32_t* bt = p.block_tables + (size_t)b * p.maxb;
-    unsigned char* wtiles = asmem + (size_t)warp * 2 * kAttnBufs * TILE;   // [buffer][K | V]
+    unsigned char* wtiles = asmem + (size_t)warp * 4 * TILE;        // [buffer][K | V]
     const uint32_t wtiles_s = static_cast<uint32_t>(__cvta_generic_to_shared(wtiles));
     const int nb_w = blk1 - blk0 > warp ? (blk1 - blk0 - warp + kAttnWarps - 1) / kAttnWarps : 0;
 
@@ -176,7 +172,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AParams p, Dev
         } else {
             const __half* ksrc = p.k_pool + ((size_t)phys * p.n_kv + g) * kBS * HD;
             const __half* vsrc = p.v_pool + ((size_t)phys * p.n_kv + g) * kBS * HD;
-            const uint32_t kd = wtiles_s + (uint32_t)((i % kAttnBufs) * 2 * TILE), vd = kd + TILE;
+            const uint32_t kd = wtiles_s + (uint32_t)((i & 1) * 2 * TILE), vd = kd + TILE;
             for (int c = lane; c < kBS * CHUNKS; c += 32) {
                 const int row = c / CHUNKS, col = c - row * CHUNKS;
                 asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(kd + row * PITCH + col * 16),
@@ -256,19 +252,15 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AParams p, Dev
     if (!fused && nb_w > 0) vcur = stage(0);
     for (int i = 0; i < nb_w; ++i) {
         bool vnext = false;
-        if (kAttnBufs == 2) {
-            if (i + 1 < nb_w) vnext = stage(i + 1);
-            else asm volatile("cp.async.commit_group;" ::: "memory");
-            asm volatile("cp.async.wait_group 1;" ::: "memory");
-        } else {
-            asm volatile("cp.async.wait_group 0;" ::: "memory");
-        }
+        if (i + 1 < nb_w) vnext = stage(i + 1);
+        else asm volatile("cp.async.commit_group;" ::: "memory");
+        asm volatile("cp.async.wait_group 1;" ::: "memory");
         __syncwarp();
         const int blk = blk0 + warp + kAttnWarps * i;
         const int nt = min(kBS, L - blk * kBS);      // valid keys in this block
         if (vcur && fused && blk == lblk) {
             // the new row: staged (possibly) before it was appended, so patch it in
-            unsigned char* kt = wtiles + (size_t)(i % kAttnBufs) * 2 * TILE;
+            unsigned char* kt = wtiles + (size_t)(i & 1) * 2 * TILE;
             if (lane < CHUNKS)
                 *reinterpret_cast<uint4*>(kt + kp * PITCH + lane * 16) = reinterpret_cast<const uint4*>(knew)[lane];
             else if (lane < 2 * CHUNKS)
@@ -277,7 +269,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AParams p, Dev
             __syncwarp();
         }
         if (vcur) {
-            unsigned char* vtile = wtiles + (size_t)(i % kAttnBufs) * 2 * TILE + TILE;
+            unsigned char* vtile = wtiles + (size_t)(i & 1) * 2 * TILE + TILE;
             if (nt < kBS) {
                 // keys past the context: their P is 0, but a stale V row must not be NaN/Inf
                 for (int c = lane; c < (kBS - nt) * CHUNKS; c += 32) {
@@ -286,7 +278,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AParams p, Dev
                 }
                 __syncwarp();
             }
-            const uint32_t ks = wtiles_s + (uint32_t)((i % kAttnBufs) * 2 * TILE), vs = ks + TILE;
+            const uint32_t ks = wtiles_s + (uint32_t)((i & 1) * 2 * TILE), vs = ks + TILE;
             // ---- S = Q K^T for the 16 keys (two 8-key tiles)
             float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
             const int lm = lane >> 3, lr = lane & 7;
@@ -336,7 +328,6 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AParams p, Dev
             }
         }
         __syncwarp();
-        if (kAttnBufs == 1 && i + 1 < nb_w) vnext = stage(i + 1);   // the one buffer is free again
         vcur = vnext;
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
@@ -472,7 +463,7 @@ Layout layout(int64_t batch, int n_heads, int n_kv, int head_dim, int64_t maxb, 
 // the warp-merge state and the split-merge weights.
 template <int HD, int G>
 constexpr size_t attn_smem() {
-    const size_t tiles = (size_t)kAttnWarps * 2 * kAttnBufs * kBS * (HD * 2 + 16);
+    const size_t tiles = (size_t)kAttnWarps * 4 * kBS * (HD * 2 + 16);
     const size_t merge = (size_t)kAttnWarps * G * HD * 4;
     return tiles > merge ? tiles : merge;
 }
