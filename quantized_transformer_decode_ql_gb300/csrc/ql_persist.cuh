@@ -1222,7 +1222,7 @@ struct StreamGemv {
 };
 
 template <int NB, int W>
-__global__ void __maxnreg__(96) gemv_stream_kernel(const __grid_constant__ PersistParams p,
+__global__ void __launch_bounds__(W * 32, 16 / W) gemv_stream_kernel(const __grid_constant__ PersistParams p,
                                                                       const __grid_constant__ StreamGemv g) {
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ PMat mat;
