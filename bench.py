@@ -384,7 +384,10 @@ def gemv_passes(cols, batch):
 
 
 def launches_per_step(cfg, B):
-    """Kernel launches of one step in the one-launch-per-phase form."""
+    """Kernel launches of one step in the one-launch-per-phase form (batch <= 32: one launch per
+    GEMV over the tile stream layout; above: row-major passes)."""
+    if B <= 32:
+        return 3 + 5 * cfg.n_layers
     per_layer = (gemv_passes(cfg.hidden, B) * 2 + gemv_passes(cfg.n_heads * cfg.head_dim, B)
                  + gemv_passes(cfg.intermediate, B) + 1)
     return 2 + per_layer * cfg.n_layers + gemv_passes(cfg.hidden, B)

@@ -112,14 +112,16 @@ int64_t ql_q4_0_stream_bytes(int64_t rows, int64_t cols, int silu);
  * d_stream 16-byte aligned, d_scales 8-byte aligned. Asynchronous on stream.              */
 int ql_q4_0_stream_pack(const void* d_scales, const void* d_quants, int64_t rows, int64_t cols,
                         int silu, void* d_stream, void* stream);
-/* [IL] CudaQwen3::gemv at batch 1-2 from the tile stream: y = epilogue(W x).
+/* [IL] CudaQwen3::gemv at batch 1-32 from the tile stream: y = epilogue(W x).
  * d_x: f16 [batch][cols], 16-byte aligned. epilogue QL_EPI_NONE: d_y f32 [batch][rows];
  * QL_EPI_ADD_RESIDUAL: d_y f32 [batch][rows], y += W x in place; QL_EPI_SILU_MUL (d_stream
- * packed with silu): d_y f16 [batch][rows/2]. Products: each code becomes q - 8 (low nibble)
+ * packed with silu): d_y f16 [batch][rows/2]. Batch 1-2: each code becomes q - 8 (low nibble)
  * or 16 (q - 8) (high nibble, against x/16) exactly in f16, the 32 products of a block are
  * summed in f16 (HFMA2; low and high nibbles apart), and each block is scaled by its f16 scale
- * and accumulated in f32. One CTA per SM; its waits for the bulk copies are bounded (2 s, then
- * the device error record says so). batch must be 1 or 2 (QL_EINVAL otherwise).          */
+ * and accumulated in f32. Batch 3-32 (needs cols in 128..896 or a multiple of 1024): the
+ * tensor-core form of the row-major GEMV (f32 products and sums), K in windows of 1024 so
+ * that every weight byte is streamed once. One CTA per SM; its waits for the bulk copies are
+ * bounded (2 s, then the device error record says so). QL_EINVAL for other batches.       */
 int ql_gemv_q4_0_stream(const void* d_stream, int64_t rows, int64_t cols, const void* d_x,
                         int64_t batch, void* d_y, int epilogue, void* stream);
 

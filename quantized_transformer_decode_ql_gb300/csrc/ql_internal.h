@@ -285,5 +285,10 @@ struct StreamGemvArgs {
 };
 int stream_gemv_prepare();
 int stream_gemv_launch(const StreamGemvArgs& a, cudaStream_t s, bool pdl);
+// The same over batches of up to 32 (ql_batched.cu): tensor-core products, K in windows of
+// 1024, every weight byte streamed once. Needs nblk / 4 < 8 or a multiple of 8.
+bool batched_gemv_shape_ok(int nblk);
+int batched_gemv_prepare();
+int batched_gemv_launch(const StreamGemvArgs& a, cudaStream_t s, bool pdl);
 
 }  // namespace ql

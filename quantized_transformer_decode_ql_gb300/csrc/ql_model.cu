@@ -61,6 +61,7 @@ struct ql_model {
     size_t persist_stream_bytes = 0;
     std::vector<ql::PMat> hmats;            // host copies: 4 per layer, then lm_head
     unsigned int* ssync = nullptr;          // abort flag of the stand-alone stream GEMVs
+    bool batched_ok = false;                // every matrix width suits the batched stream GEMV
     ql::PMat plm = {};
     int max_nblk = 0, persist_nsplit = 1;
     float* ppm = nullptr;
@@ -210,8 +211,9 @@ int run_step(ql_model* m, const ql_step_args* a, cudaStream_t s) {
                            m->x, (int)d.hidden, (int)d.vocab, device_error_record(), nw(m->layers[0].qkv, kAll));
     if (e != cudaSuccess) return cuda_error(e, "embed launch");
 
-    // batch 1-2: the GEMVs stream the tile stream copy of the weights (stream_gemv_launch)
-    const bool streamed = B <= kPersistMaxBatch && !m->hmats.empty();
+    // batch 1-2: the GEMVs stream the tile stream copy of the weights (stream_gemv_launch);
+    // batch 3-32: the same copy, batched (batched_gemv_launch); above: row-major passes
+    const bool streamed = !m->hmats.empty() && (B <= kPersistMaxBatch || (m->batched_ok && B <= 32));
     auto sg = [&](const PMat& M, int epi, bool rms, const float* xf, const __half* x16, const float* nw, void* y,
                   int ld) {
         StreamGemvArgs ga = {};
@@ -228,7 +230,7 @@ int run_step(ql_model* m, const ql_step_args* a, cudaStream_t s) {
         ga.keys = m->keys;
         ga.active = a->active;
         ga.sync = m->ssync;
-        return stream_gemv_launch(ga, s, pdl);
+        return B <= kPersistMaxBatch ? stream_gemv_launch(ga, s, pdl) : batched_gemv_launch(ga, s, pdl);
     };
     for (int li = 0; li < d.n_layers; ++li) {
         const ql_layer_desc& L = m->layers[li];
@@ -428,6 +430,8 @@ int setup_persist(ql_model* m) {
         if (persist_prepare(maxb, m->max_nblk, (int)d.head_dim, G, (int)d.n_layers) == QL_OK) break;
     if (maxb < 1) return QL_OK;
     if (int rc0 = stream_gemv_prepare()) return rc0;
+    m->batched_ok = batched_gemv_shape_ok((int)(d.hidden / 32)) && batched_gemv_shape_ok((int)(d.intermediate / 32)) &&
+                    batched_gemv_shape_ok((int)(d.n_heads * d.head_dim / 32)) && batched_gemv_prepare() == QL_OK;
 
     std::vector<PLayer> hl(m->layers.size());
     std::vector<PMat> all;

@@ -197,7 +197,9 @@ extern "C" int ql_gemv_q4_0_stream(const void* d_stream, int64_t rows, int64_t c
                "ql_gemv_q4_0_stream: unknown epilogue");
     const int silu = epilogue == QL_EPI_SILU_MUL;
     QL_REQUIRE(stream_shape_ok(rows, cols, silu), "ql_gemv_q4_0_stream: need cols % 128 == 0 (and even rows with SiLU*up)");
-    QL_REQUIRE(batch == 1 || batch == 2, "ql_gemv_q4_0_stream: batch must be 1 or 2");
+    QL_REQUIRE(batch >= 1 && batch <= 32, "ql_gemv_q4_0_stream: batch must be in [1, 32]");
+    QL_REQUIRE(batch <= 2 || batched_gemv_shape_ok((int)(cols / 32)),
+               "ql_gemv_q4_0_stream: batches above 2 need cols in 128..896 or a multiple of 1024");
     QL_REQUIRE(aligned(d_stream, 16) && aligned(d_x, 16) && aligned(d_y, 4),
                "ql_gemv_q4_0_stream: stream and x must be 16-byte aligned, y 4-byte");
     // the flag's address, resolved once per device (the lookup may load the module lazily,
@@ -226,5 +228,6 @@ extern "C" int ql_gemv_q4_0_stream(const void* d_stream, int64_t rows, int64_t c
     a.y = d_y;
     a.ld = (int)(silu ? rows / 2 : rows);
     a.sync = static_cast<unsigned int*>(sync);
-    return stream_gemv_launch(a, static_cast<cudaStream_t>(stream), true);
+    return batch <= 2 ? stream_gemv_launch(a, static_cast<cudaStream_t>(stream), true)
+                      : batched_gemv_launch(a, static_cast<cudaStream_t>(stream), true);
 }

@@ -1,4 +1,4 @@
-"""The batch 1-2 q4_0 GEMV over the tile stream layout (ql_q4_0_stream_pack, ql_gemv_q4_0_stream).
+"""The q4_0 GEMV over the tile stream layout, batch 1-32 (ql_q4_0_stream_pack, ql_gemv_q4_0_stream).
 
 Layout: bit-exact against a NumPy restatement of the documented layout (16-row tiles, units of
 4 blocks x 16 rows of codes then the rows' 4 scales, gate/up row pairing for SiLU*up, zero
@@ -6,10 +6,11 @@ rows past the matrix).
 
 GEMV: against the oracle (f64 dense product of the dequantised weights). Tolerance, from the
 kernel's arithmetic: activations are staged in f16 (exact here, the tests give f16), every code
-becomes q - 8 or 16 (q - 8) exactly in f16, a block's 32 products are summed in f16 (16
-products per accumulator, relative rounding 2^-11 per step), blocks are scaled and summed in
-f32. For N(0, 0.02) weights and N(0, 1) activations that is ~1e-3 of the output rms, so the bar
-is ``|y - y_ref| <= 1e-2 * rms(y_ref) + 1e-2 * |y_ref|``, the same as the row-major GEMV.
+becomes q - 8 or 16 (q - 8) exactly in f16. Batch 1-2: a block's 32 products are summed in f16
+(16 products per accumulator, relative rounding 2^-11 per step); batch 3-32: tensor-core
+products and sums in f32. Blocks are scaled and summed in f32. For N(0, 0.02) weights and
+N(0, 1) activations that is ~1e-3 of the output rms or less, so the bar is
+``|y - y_ref| <= 1e-2 * rms(y_ref) + 1e-2 * |y_ref|``, the same as the row-major GEMV.
 """
 import numpy as np
 import pytest
@@ -146,12 +147,37 @@ def test_stream_gemv_zero_and_extreme_blocks():
     check_close(got, ref, "extreme blocks")
 
 
+@pytest.mark.parametrize("rows,cols", [(37, 256), (200, 384), (1000, 1024), (6144, 4096), (96, 12288)])
+@pytest.mark.parametrize("batch", [3, 5, 8, 17, 32])
+def test_stream_gemv_batched(rows, cols, batch):
+    """Batches 3-32: every weight streamed once, K in windows of 1024 columns."""
+    ql = lib()
+    w = ql_inputs.gemv_weight(rows, cols, seed=12)
+    x = ql_inputs.gemv_activations(batch, cols, seed=13)
+    got, ref = run(w, x, ql.QL_EPI_NONE)
+    check_close(got, ref, f"batched {rows}x{cols} b{batch}")
+
+
+@pytest.mark.parametrize("batch", [3, 16, 32])
+def test_stream_gemv_batched_epilogues(batch):
+    ql = lib()
+    w = ql_inputs.gemv_weight(300, 2048, seed=14)
+    x = ql_inputs.gemv_activations(batch, 2048, seed=15)
+    res = np.random.default_rng(2).standard_normal((batch, 300))
+    got, ref = run(w, x, ql.QL_EPI_ADD_RESIDUAL, residual=res)
+    check_close(got, ref + res.astype(np.float32).astype(np.float64), "batched residual")
+    wg = ql_inputs.gemv_weight(2 * 700, 1024, seed=16)
+    xg = ql_inputs.gemv_activations(batch, 1024, seed=17)
+    got, ref = run(wg, xg, ql.QL_EPI_SILU_MUL)
+    check_close(got, ops.swiglu(ref[:, :700], ref[:, 700:]), "batched silu_mul")
+
+
 def test_stream_gemv_rejects_bad_arguments():
     ql = lib()
-    t = torch.zeros(4096, dtype=torch.uint8, device="cuda")
-    x = torch.zeros((3, 128), dtype=torch.float16, device="cuda")
-    y = torch.zeros((3, 16), dtype=torch.float32, device="cuda")
-    for args in ((16, 128, 3), (16, 96, 1), (15, 128, 1)):
+    t = torch.zeros(8192, dtype=torch.uint8, device="cuda")
+    x = torch.zeros((33, 1152), dtype=torch.float16, device="cuda")
+    y = torch.zeros((33, 16), dtype=torch.float32, device="cuda")
+    for args in ((16, 128, 33), (16, 96, 1), (15, 128, 1), (16, 1152, 3)):
         rows, cols, batch = args
         epi = ql.QL_EPI_SILU_MUL if rows % 2 else ql.QL_EPI_NONE
         with pytest.raises(ql.QLError) as e:
