@@ -52,6 +52,7 @@ struct BParams {
     const float* xf;       // rms: f32 [B][cols]
     const __half* x16;     // else f16 [B][cols]
     const float* norm_w;
+    const float* rs_in;    // rms: [B] 1 / rms of each column (rms_stats_kernel)
     float eps;
     void* y;
     int ld;
@@ -158,26 +159,10 @@ __device__ __forceinline__ void bring_wait(BRing& r, const BParams& p, unsigned 
     r.dead = 1;
 }
 
-// Per-column RMS statistics over the full K (rms input only): rs[c] = 1/sqrt(mean x^2 + eps).
-__device__ void column_rms(const BParams& p, int cols, float* rs, float* red) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int c = 0; c < p.B; ++c) {
-        float ss = 0.f;
-        const float4* xc = reinterpret_cast<const float4*>(p.xf + (size_t)c * cols);
-        for (int i = tid; i < cols / 4; i += kT) {
-            const float4 v = __ldcg(xc + i);
-            ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-        }
-#pragma unroll
-        for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        if (lane == 0) red[warp * kMaxCols + c] = ss;
-    }
-    __syncthreads();
-    if (tid < p.B) {
-        float t = 0.f;
-        for (int w = 0; w < kW; ++w) t += red[w * kMaxCols + tid];
-        rs[tid] = 1.0f / sqrtf(t / (float)cols + p.eps);
-    }
+// 1 / rms of every column (the RMSNorm statistics over the full K), computed once by
+// rms_stats_kernel for all CTAs.
+__device__ void load_column_rms(const BParams& p, float* rs) {
+    if ((int)threadIdx.x < p.B) rs[threadIdx.x] = __ldcg(p.rs_in + threadIdx.x);
     __syncthreads();
 }
 
@@ -192,45 +177,63 @@ __device__ void stage_window(const BParams& p, const Geo& G, int w, const float*
     for (int i = tid; i < nb * kMaxCols; i += kT) bias[i] = 0.f;
     __syncthreads();
     const int nitems = p.B * nb * 4;
-    for (int base = 0; base < nitems; base += kT) {   // warp-uniform bound: the shuffles below
-        const int item = base + tid;
-        const bool live = item < nitems;
-        const int t = item & 3, cj = item >> 2, c = cj / nb, j = cj - c * nb;
-        float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        if (live) {
-            const size_t off = (size_t)c * cols + 32 * (j0 + j) + 4 * t;
-            if (p.rms) {
-                const float4 a = __ldcg(reinterpret_cast<const float4*>(p.xf + off));
-                const float4 h = __ldcg(reinterpret_cast<const float4*>(p.xf + off + 16));
-                const float4 wa = __ldg(reinterpret_cast<const float4*>(p.norm_w + 32 * (j0 + j) + 4 * t));
-                const float4 wh = __ldg(reinterpret_cast<const float4*>(p.norm_w + 32 * (j0 + j) + 16 + 4 * t));
-                const float r = rs[c];
-                v[0] = a.x * r * wa.x; v[1] = a.y * r * wa.y; v[2] = a.z * r * wa.z; v[3] = a.w * r * wa.w;
-                v[4] = h.x * r * wh.x; v[5] = h.y * r * wh.y; v[6] = h.z * r * wh.z; v[7] = h.w * r * wh.w;
-            } else {
-                const uint2 a = __ldcg(reinterpret_cast<const uint2*>(p.x16 + off));
-                const uint2 h = __ldcg(reinterpret_cast<const uint2*>(p.x16 + off + 16));
-                const float2 f0 = __half22float2(as_h2(a.x)), f1 = __half22float2(as_h2(a.y));
-                const float2 f2 = __half22float2(as_h2(h.x)), f3 = __half22float2(as_h2(h.y));
-                v[0] = f0.x; v[1] = f0.y; v[2] = f1.x; v[3] = f1.y;
-                v[4] = f2.x; v[5] = f2.y; v[6] = f3.x; v[7] = f3.y;
+    constexpr int kChunk = 4;   // items per thread whose loads are in flight together
+    for (int base = 0; base < nitems; base += kChunk * kT) {   // warp-uniform bounds (shuffles)
+        float4 la[kChunk], lh[kChunk];
+        uint2 ha[kChunk], hh[kChunk];
+#pragma unroll
+        for (int r = 0; r < kChunk; ++r) {
+            const int item = base + r * kT + tid;
+            if (item < nitems) {
+                const int t = item & 3, cj = item >> 2, c = cj / nb, j = cj - c * nb;
+                const size_t off = (size_t)c * cols + 32 * (j0 + j) + 4 * t;
+                if (p.rms) {
+                    la[r] = __ldcg(reinterpret_cast<const float4*>(p.xf + off));
+                    lh[r] = __ldcg(reinterpret_cast<const float4*>(p.xf + off + 16));
+                } else {
+                    ha[r] = __ldcg(reinterpret_cast<const uint2*>(p.x16 + off));
+                    hh[r] = __ldcg(reinterpret_cast<const uint2*>(p.x16 + off + 16));
+                }
             }
         }
-        const __half2 p0 = __floats2half2_rn(v[0], v[2]);
-        const __half2 p1 = __floats2half2_rn(v[1], v[3]);
-        const __half2 p2 = __floats2half2_rn(__half2float(__float2half_rn(v[4])) * 0.0625f,
-                                             __half2float(__float2half_rn(v[6])) * 0.0625f);
-        const __half2 p3 = __floats2half2_rn(__half2float(__float2half_rn(v[5])) * 0.0625f,
-                                             __half2float(__float2half_rn(v[7])) * 0.0625f);
-        const float2 f0 = __half22float2(p0), f1 = __half22float2(p1);
-        const float2 f2 = __half22float2(p2), f3 = __half22float2(p3);
-        // sum (1024 + q) x_lo + (1024 + 16 q) x_hi/16 = sum (q - 8) x + 1032 sum x_lo + 1152 sum x_hi/16
-        float part = 1032.0f * ((f0.x + f0.y) + (f1.x + f1.y)) + 1152.0f * ((f2.x + f2.y) + (f3.x + f3.y));
-        part += __shfl_xor_sync(0xffffffffu, part, 1);
-        part += __shfl_xor_sync(0xffffffffu, part, 2);
-        if (live) {
-            xs[(size_t)c * kXStride + 4 * j + t] = make_uint4(as_u32(p0), as_u32(p1), as_u32(p2), as_u32(p3));
-            if (t == 0) bias[j * kMaxCols + c] = -part;
+#pragma unroll
+        for (int r = 0; r < kChunk; ++r) {
+            if (base + r * kT >= nitems) break;   // warp-uniform
+            const int item = base + r * kT + tid;
+            const bool live = item < nitems;
+            const int t = item & 3, cj = item >> 2, c = cj / nb, j = cj - c * nb;
+            float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            if (live) {
+                if (p.rms) {
+                    const float4 wa = __ldg(reinterpret_cast<const float4*>(p.norm_w + 32 * (j0 + j) + 4 * t));
+                    const float4 wh = __ldg(reinterpret_cast<const float4*>(p.norm_w + 32 * (j0 + j) + 16 + 4 * t));
+                    const float rr = rs[c];
+                    const float4 a = la[r], h = lh[r];
+                    v[0] = a.x * rr * wa.x; v[1] = a.y * rr * wa.y; v[2] = a.z * rr * wa.z; v[3] = a.w * rr * wa.w;
+                    v[4] = h.x * rr * wh.x; v[5] = h.y * rr * wh.y; v[6] = h.z * rr * wh.z; v[7] = h.w * rr * wh.w;
+                } else {
+                    const float2 f0 = __half22float2(as_h2(ha[r].x)), f1 = __half22float2(as_h2(ha[r].y));
+                    const float2 f2 = __half22float2(as_h2(hh[r].x)), f3 = __half22float2(as_h2(hh[r].y));
+                    v[0] = f0.x; v[1] = f0.y; v[2] = f1.x; v[3] = f1.y;
+                    v[4] = f2.x; v[5] = f2.y; v[6] = f3.x; v[7] = f3.y;
+                }
+            }
+            const __half2 p0 = __floats2half2_rn(v[0], v[2]);
+            const __half2 p1 = __floats2half2_rn(v[1], v[3]);
+            const __half2 p2 = __floats2half2_rn(__half2float(__float2half_rn(v[4])) * 0.0625f,
+                                                 __half2float(__float2half_rn(v[6])) * 0.0625f);
+            const __half2 p3 = __floats2half2_rn(__half2float(__float2half_rn(v[5])) * 0.0625f,
+                                                 __half2float(__float2half_rn(v[7])) * 0.0625f);
+            const float2 f0 = __half22float2(p0), f1 = __half22float2(p1);
+            const float2 f2 = __half22float2(p2), f3 = __half22float2(p3);
+            // sum (1024 + q) x_lo + (1024 + 16 q) x_hi/16 = sum (q - 8) x + 1032 sum x_lo + 1152 sum x_hi/16
+            float part = 1032.0f * ((f0.x + f0.y) + (f1.x + f1.y)) + 1152.0f * ((f2.x + f2.y) + (f3.x + f3.y));
+            part += __shfl_xor_sync(0xffffffffu, part, 1);
+            part += __shfl_xor_sync(0xffffffffu, part, 2);
+            if (live) {
+                xs[(size_t)c * kXStride + 4 * j + t] = make_uint4(as_u32(p0), as_u32(p1), as_u32(p2), as_u32(p3));
+                if (t == 0) bias[j * kMaxCols + c] = -part;
+            }
         }
     }
 }
@@ -287,7 +290,6 @@ __global__ void __launch_bounds__(kT, 1) gemv_batched_kernel(const __grid_consta
     __shared__ __align__(8) unsigned long long mbar[kW * kStages];
     __shared__ unsigned long long kred[kMaxCols];
     __shared__ float rs[kMaxCols];
-    __shared__ float red[kW * kMaxCols];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t = lane & 3;
     uint4* xs = reinterpret_cast<uint4*>(smem + kRing);
@@ -317,7 +319,7 @@ __global__ void __launch_bounds__(kT, 1) gemv_batched_kernel(const __grid_consta
     for (int i = 0; i < kStages; ++i) bring_issue(r, M, G, warp, lane);
     pdl_wait();
     pdl_trigger();
-    if (p.rms) column_rms(p, M.nblk * 32, rs, red);
+    if (p.rms) load_column_rms(p, rs);
 
     const int lm = lane >> 3, lrow = lane & 7;
     const uint32_t a_lo = (uint32_t)(((lm >> 1) * 16 + (lm & 1) * 8 + lrow) * 16);
@@ -463,6 +465,32 @@ __global__ void __launch_bounds__(kT, 1) gemv_batched_kernel(const __grid_consta
     }
 }
 
+// rs[b] = 1 / sqrt(mean_k x[b][k]^2 + eps): one CTA per column, fixed summation order.
+__global__ void __launch_bounds__(256) rms_stats_kernel(const float* x, int cols, float eps, float* rs) {
+    __shared__ float red[8];
+    const int b = blockIdx.x, tid = threadIdx.x;
+    pdl_wait();
+    pdl_trigger();
+    const float4* xb = reinterpret_cast<const float4*>(x + (size_t)b * cols);
+    float ss = 0.f;
+    for (int i = tid; i < cols / 4; i += 4 * 256) {
+        float4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[u] = i + u * 256 < cols / 4 ? __ldcg(xb + i + u * 256) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) ss += v[u].x * v[u].x + v[u].y * v[u].y + v[u].z * v[u].z + v[u].w * v[u].w;
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if ((tid & 31) == 0) red[tid >> 5] = ss;
+    __syncthreads();
+    if (tid == 0) {
+        float t = 0.f;
+        for (int w = 0; w < 8; ++w) t += red[w];
+        rs[b] = 1.0f / sqrtf(t / (float)cols + eps);
+    }
+}
+
 template <int NT>
 cudaError_t run(bool launch, const BParams* p, int grid, cudaStream_t s, bool pdl) {
     if (!launch) {
@@ -506,7 +534,7 @@ int batched_gemv_launch(const StreamGemvArgs& a, cudaStream_t s, bool pdl) {
     QL_REQUIRE(a.M.stream && batched_gemv_shape_ok(a.M.nblk),
                "batched gemv: cols must be 128, 256, ..., 896 or a multiple of 1024");
     QL_REQUIRE(a.batch >= 1 && a.batch <= batched::kMaxCols, "batched gemv: batch must be in [1, 32]");
-    QL_REQUIRE(a.rms ? (a.xf && a.norm_w) : a.x16 != nullptr, "batched gemv: null input");
+    QL_REQUIRE(a.rms ? (a.xf && a.norm_w && a.rs) : a.x16 != nullptr, "batched gemv: null input");
     QL_REQUIRE(a.y && a.sync, "batched gemv: null output");
     QL_REQUIRE(a.epilogue != kEpiArgmax || a.keys, "batched gemv: argmax needs keys");
     QL_REQUIRE((a.epilogue == QL_EPI_SILU_MUL) == (a.M.silu != 0), "batched gemv: SiLU*up needs a matrix packed for it");
@@ -523,6 +551,12 @@ int batched_gemv_launch(const StreamGemvArgs& a, cudaStream_t s, bool pdl) {
     p.norm_w = a.norm_w;
     p.eps = a.eps;
     p.y = a.y;
+    if (a.rms) {   // the RMSNorm statistics of every column, once, for all CTAs
+        const cudaError_t e0 = ql::launch(batched::rms_stats_kernel, dim3(a.batch), dim3(256), 0, s, pdl, a.xf,
+                                          a.M.nblk * 32, a.eps, a.rs);
+        if (e0 != cudaSuccess) return cuda_error(e0, "rms stats launch");
+        p.rs_in = a.rs;
+    }
     p.ld = a.ld;
     p.keys = a.keys;
     p.active = a.active;

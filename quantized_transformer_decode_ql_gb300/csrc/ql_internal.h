@@ -282,6 +282,7 @@ struct StreamGemvArgs {
     unsigned long long* keys;
     const int32_t* active;
     unsigned int* sync;   // [4] zero: the abort flag of the kernel's bounded waits
+    float* rs;            // batch 3-32 with rms: [batch] scratch for the columns' RMS statistics
 };
 int stream_gemv_prepare();
 int stream_gemv_launch(const StreamGemvArgs& a, cudaStream_t s, bool pdl);

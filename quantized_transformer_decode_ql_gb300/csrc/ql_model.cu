@@ -61,6 +61,7 @@ struct ql_model {
     size_t persist_stream_bytes = 0;
     std::vector<ql::PMat> hmats;            // host copies: 4 per layer, then lm_head
     unsigned int* ssync = nullptr;          // abort flag of the stand-alone stream GEMVs
+    float* rs = nullptr;                    // [max_batch] RMS statistics of the batched GEMV
     bool batched_ok = false;                // every matrix width suits the batched stream GEMV
     ql::PMat plm = {};
     int max_nblk = 0, persist_nsplit = 1;
@@ -230,6 +231,7 @@ int run_step(ql_model* m, const ql_step_args* a, cudaStream_t s) {
         ga.keys = m->keys;
         ga.active = a->active;
         ga.sync = m->ssync;
+        ga.rs = m->rs;
         return B <= kPersistMaxBatch ? stream_gemv_launch(ga, s, pdl) : batched_gemv_launch(ga, s, pdl);
     };
     for (int li = 0; li < d.n_layers; ++li) {
@@ -464,6 +466,7 @@ int setup_persist(ql_model* m) {
     A((void**)&m->ptickets, (size_t)maxb * d.n_kv_heads * 4);
     A((void**)&m->psync, 16);
     A((void**)&m->ssync, 16);
+    A((void**)&m->rs, (size_t)d.max_batch * 4);
     if (rc != QL_OK) return rc;
     // the weights re-laid into the tile stream layout that the persistent kernel copies from
     if ((rc = persist_pack_streams(all.data(), (int)all.size(), m->pstreams, nullptr)) != QL_OK) return rc;
