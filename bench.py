@@ -273,11 +273,15 @@ def gpu_arm(args, rank, world, local_rank):
             buf = torch.empty(ql.ql_q4_0_stream_bytes(Wl.rows, Wl.cols, 1), dtype=torch.uint8, device="cuda")
             ql.ql_q4_0_stream_pack(Wl.scales, Wl.quants, Wl.rows, Wl.cols, 1, buf, s)
             streams.append(buf)
+        ws = None
+        if B > 2:
+            ws = torch.zeros(ql.ql_gemv_q4_0_stream_workspace_bytes(W.rows, W.cols, 1), dtype=torch.uint8,
+                             device="cuda")
         s.synchronize()
 
         def gu_all():
             for buf in streams:
-                ql.ql_gemv_q4_0_stream(buf, W.rows, W.cols, x16, B, act, ql.QL_EPI_SILU_MUL, s)
+                ql.ql_gemv_q4_0_stream(buf, W.rows, W.cols, x16, B, act, ql.QL_EPI_SILU_MUL, ws, s)
         gu_kernel = "q4_0 GEMV over the tile stream layout (gate|up, SiLU*up epilogue, batch %d)" % B
     else:
         n_mats = cfg.n_layers

@@ -119,11 +119,19 @@ int ql_q4_0_stream_pack(const void* d_scales, const void* d_quants, int64_t rows
  * or 16 (q - 8) (high nibble, against x/16) exactly in f16, the 32 products of a block are
  * summed in f16 (HFMA2; low and high nibbles apart), and each block is scaled by its f16 scale
  * and accumulated in f32. Batch 3-32 (needs cols in 128..896 or a multiple of 1024): the
- * tensor-core form of the row-major GEMV (f32 products and sums), K in windows of 1024 so
- * that every weight byte is streamed once. One CTA per SM; its waits for the bulk copies are
+ * tensor-core form of the row-major GEMV (f32 products and sums), split over K in windows of
+ * 1024 columns so that every weight byte is streamed once; each window's f32 partial sums go
+ * to d_workspace and are added in window order (deterministic). d_workspace (device, 256-byte
+ * aligned, at least ql_gemv_q4_0_stream_workspace_bytes) is caller-owned, zero-filled before
+ * its first use and left ready for the next call; calls that run concurrently need separate
+ * workspaces. It may be NULL at batch 1-2. One CTA per SM; its waits for the bulk copies are
  * bounded (2 s, then the device error record says so). QL_EINVAL for other batches.       */
 int ql_gemv_q4_0_stream(const void* d_stream, int64_t rows, int64_t cols, const void* d_x,
-                        int64_t batch, void* d_y, int epilogue, void* stream);
+                        int64_t batch, void* d_y, int epilogue, void* d_workspace,
+                        int64_t workspace_bytes, void* stream);
+/* Workspace bytes ql_gemv_q4_0_stream needs at batch 3-32 for this shape on the current
+ * device (the split depends on its SM count); 0 on a bad shape.                           */
+int64_t ql_gemv_q4_0_stream_workspace_bytes(int64_t rows, int64_t cols, int silu);
 
 /* --------------------------------------------------------------- paged decode attention
  * [FK] launch_paged_decode_attention / attention_paged, split-K over the context:

@@ -20,6 +20,7 @@ from ._lib import (QLError, QL_OK, QL_EINVAL, QL_ENOMEM, QL_ECUDA, QL_EPOOL, QL_
 __all__ = [
     "QLError", "lib", "ql_q4_0_pack", "ql_q4_0_unpack", "ql_q4_0_pack_device", "ql_gemv_q4_0",
     "ql_q4_0_stream_bytes", "ql_q4_0_stream_pack", "ql_gemv_q4_0_stream",
+    "ql_gemv_q4_0_stream_workspace_bytes",
     "ql_paged_attn_workspace_bytes", "ql_paged_attn_decode", "ql_paged_attn_decode_noalloc",
     "ql_fused_norm_rope",
     "ql_rope_tables", "ql_check_device_error", "BlockPool", "SIGNATURES",
@@ -56,9 +57,16 @@ def ql_q4_0_stream_pack(scales, quants, rows, cols, silu, out, stream=None):
     check(lib().ql_q4_0_stream_pack(ptr(scales), ptr(quants), rows, cols, silu, ptr(out), stream_ptr(stream)))
 
 
-def ql_gemv_q4_0_stream(w_stream, rows, cols, x, batch, y, epilogue=QL_EPI_NONE, stream=None):
+def ql_gemv_q4_0_stream_workspace_bytes(rows, cols, silu=0):
+    return int(lib().ql_gemv_q4_0_stream_workspace_bytes(rows, cols, silu))
+
+
+def ql_gemv_q4_0_stream(w_stream, rows, cols, x, batch, y, epilogue=QL_EPI_NONE, workspace=None, stream=None):
+    """``workspace``: a zero-filled device byte tensor of ql_gemv_q4_0_stream_workspace_bytes
+    (batch 3-32; None at batch 1-2)."""
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     check(lib().ql_gemv_q4_0_stream(ptr(w_stream), rows, cols, ptr(x), batch, ptr(y), epilogue,
-                                    stream_ptr(stream)))
+                                    ptr(workspace), nbytes, stream_ptr(stream)))
 
 
 def ql_paged_attn_workspace_bytes(batch, n_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq):

@@ -64,7 +64,9 @@ SIGNATURES = {
                              c_int, c_int, c_void_p, c_void_p]),
     "ql_q4_0_stream_bytes": (c_int64, [c_int64, c_int64, c_int]),
     "ql_q4_0_stream_pack": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_int, c_void_p, c_void_p]),
-    "ql_gemv_q4_0_stream": (c_int, [c_void_p, c_int64, c_int64, c_void_p, c_int64, c_void_p, c_int, c_void_p]),
+    "ql_gemv_q4_0_stream": (c_int, [c_void_p, c_int64, c_int64, c_void_p, c_int64, c_void_p, c_int, c_void_p,
+                                    c_int64, c_void_p]),
+    "ql_gemv_q4_0_stream_workspace_bytes": (c_int64, [c_int64, c_int64, c_int]),
     "ql_paged_attn_workspace_bytes": (c_size_t, [c_int64, c_int, c_int, c_int, c_int, c_int64]),
     "ql_paged_attn_decode": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int64,
                                      c_int, c_int, c_int, c_int, c_int64, c_int64, c_float,

@@ -10,13 +10,13 @@
 // Why this shape (GB300): the activations of all batch columns for the full K (32 columns x
 // 12288 x f16 = 768 KB for the down projection) do not fit in shared memory next to the weight
 // ring, and re-reading the weights per column group multiplies the step's dominant traffic. So
-// K is cut into windows of 1024 (8 units per tile): the CTA stages one window of every column,
-// its warps consume that window's units, then the CTA stages the next window. Within a group of
-// up to 16 tiles, the units of a window are split over the 16 warps in the same way in every
-// window, so each warp meets the same (at most two) tiles every time and keeps their
-// accumulators in registers; tiles shared by warps are reduced in shared memory in warp order at
-// the end of the group (deterministic). The weights arrive through the same per-warp ring of
-// bulk copies (TMA) as the batch-1 kernel, in the order the windows consume them.
+// the GEMV is split over K: a CTA takes one K window of 1024 columns and one group of rows,
+// stages that window of every batch column once, and streams the window's units of its tiles
+// (at 1-3 tiles per CTA a row split alone would leave a window less than one unit per warp).
+// The CTA writes f32 partial sums; the CTA that takes the last ticket of a row group (no
+// waiting) adds the windows' partials in window order (deterministic) and applies the
+// epilogue. The weights arrive through the same per-warp ring of bulk copies (TMA) as the
+// batch-1 kernel.
 #include "ql_persist.cuh"
 
 #include <cstdlib>
@@ -36,7 +36,6 @@ using persist::kUnitBytes;
 
 constexpr int kW = 16, kT = kW * 32;
 constexpr int kWinUnits = 8;                       // units per tile per K window (1024 columns)
-constexpr int kGroupTiles = 16;                    // tiles per group
 constexpr int kMaxCols = 32;                       // batch columns per call
 constexpr int kXStride = kWinUnits * kUnitBlocks * 4 + 4;   // uint4 per staged column (+64 B)
 constexpr size_t kRing = (size_t)kW * kStages * kSlotBytes;
@@ -61,62 +60,43 @@ struct BParams {
     unsigned int* sync;    // [4]: [2] is the abort flag of the bounded waits
     DevError* err;
     unsigned long long timeout_ns;
+    float* part;           // [nwin][ntile * 16][kMaxCols] f32 partial sums of the K windows
+    int* tickets;          // [ngr] (at the start of the workspace), zero between calls
+    int ngr;               // row groups (grid = nwin * ngr)
 };
 
-// This CTA's tiles, K windows and groups.
+// This CTA's K window and row group: CTA c = (window c % nwin, row group c / nwin).
 struct Geo {
-    int T0, T1, nst, kwu, nwin, ngroups;
+    int T0, T1, nst, kwu, nwin, w, rg;
 };
-__device__ __forceinline__ Geo geometry(const PMat& M) {
+__device__ __forceinline__ Geo geometry(const BParams& p) {
     Geo G;
-    persist::cta_tiles(M.ntile, G.T0, G.T1);
-    G.nst = M.nblk / kUnitBlocks;
+    G.nst = p.M.nblk / kUnitBlocks;
     G.kwu = G.nst < kWinUnits ? G.nst : kWinUnits;
     G.nwin = G.nst / G.kwu;
-    G.ngroups = (G.T1 - G.T0 + kGroupTiles - 1) / kGroupTiles;
+    G.w = (int)blockIdx.x % G.nwin;
+    G.rg = (int)blockIdx.x / G.nwin;
+    G.T0 = (int)(((long long)G.rg * p.M.ntile) / p.ngr);
+    G.T1 = (int)(((long long)(G.rg + 1) * p.M.ntile) / p.ngr);
     return G;
 }
-__device__ __forceinline__ int group_tiles(const Geo& G, int g) {
-    const int t = G.T1 - G.T0 - kGroupTiles * g;
-    return t < kGroupTiles ? t : kGroupTiles;
-}
-// This warp's units [a, b) of a (group, window): the same split in every window of a group.
-__device__ __forceinline__ void warp_range(const Geo& G, int g, int warp, int& a, int& b) {
-    const int U = group_tiles(G, g) * G.kwu;
-    a = persist::warp_unit<kW>(U, warp);
-    b = persist::warp_unit<kW>(U, warp + 1);
-}
 
-// Issue side of the ring: (group, window, unit) in consumption order; a copy never crosses a
-// tile's run of kwu units.
+// Issue side of the ring: this warp's units [u, b) of the CTA's (tile, unit-of-window) list,
+// tile-major; a copy never crosses a tile's run of kwu units.
 struct BRing {
-    int g, w, u, b;
+    int u, b;
     unsigned int issued, consumed;
     uint32_t base, mbar;
     int dead;
 };
-__device__ __forceinline__ void bring_seek(BRing& r, const Geo& G, int warp) {
-    while (r.g < G.ngroups) {
-        int a, b;
-        warp_range(G, r.g, warp, a, b);
-        if (a < b) {
-            if (r.u < a || r.u >= b) r.u = a;
-            r.b = b;
-            return;
-        }
-        ++r.g;   // no units for this warp in the whole group
-        r.w = 0;
-        r.u = -1;
-    }
-}
-__device__ __forceinline__ void bring_issue(BRing& r, const PMat& M, const Geo& G, int warp, int lane) {
-    if (r.g >= G.ngroups || r.dead) return;
+__device__ __forceinline__ void bring_issue(BRing& r, const PMat& M, const Geo& G, int lane) {
+    if (r.u >= r.b || r.dead) return;
     const int tl = r.u / G.kwu, kk = r.u - tl * G.kwu;
     int n = r.b - r.u;
     n = n < kSlotUnits ? n : kSlotUnits;
     n = n < G.kwu - kk ? n : G.kwu - kk;
     if (lane == 0) {
-        const int tile = G.T0 + kGroupTiles * r.g + tl, k = G.kwu * r.w + kk;
+        const int tile = G.T0 + tl, k = G.kwu * G.w + kk;
         const unsigned int slot = r.issued % kStages;
         const uint32_t mb = r.mbar + slot * 8, dst = r.base + slot * kSlotBytes;
         const uint32_t bytes = (uint32_t)(n * kUnitBytes);
@@ -128,18 +108,6 @@ __device__ __forceinline__ void bring_issue(BRing& r, const PMat& M, const Geo& 
     }
     ++r.issued;
     r.u += n;
-    if (r.u == r.b) {
-        if (++r.w == G.nwin) {
-            r.w = 0;
-            ++r.g;
-            r.u = -1;
-        } else {
-            int a, b;
-            warp_range(G, r.g, warp, a, b);
-            r.u = a;
-        }
-        bring_seek(r, G, warp);
-    }
 }
 
 __device__ __forceinline__ void bring_wait(BRing& r, const BParams& p, unsigned int n) {
@@ -244,41 +212,87 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r
                  : "r"(addr));
 }
 
-// Epilogue of one finished tile for this lane's fragment (rows g, g + 8; columns 8 nt + 2t, +1).
+// Write this lane's fragment of a tile's partial sums for the CTA's window (rows g, g + 8 of
+// the tile; columns 8 nt + 2t, +1).
 template <int NT>
-__device__ __forceinline__ void finish_tile(const BParams& p, int tile, const float (&acc)[NT][4],
-                                            unsigned long long* kred, int lane) {
+__device__ __forceinline__ void write_partial(const BParams& p, const Geo& G, int tile, const float (&acc)[NT][4],
+                                              int lane) {
     const int g = lane >> 2, t = lane & 3;
+    float* base = p.part + ((size_t)G.w * p.M.ntile + tile) * 16 * kMaxCols;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
+        const int c = nt * 8 + 2 * t;
+        if (c < p.B) {
+            base[g * kMaxCols + c] = acc[nt][0];
+            base[(g + 8) * kMaxCols + c] = acc[nt][2];
+        }
+        if (c + 1 < p.B) {
+            base[g * kMaxCols + c + 1] = acc[nt][1];
+            base[(g + 8) * kMaxCols + c + 1] = acc[nt][3];
+        }
+    }
+}
+
+// The row group's result: sum of the windows' partials in window order, then the epilogue.
+// An item is one output row and 8 columns (one 32-byte sector of a partial row per window);
+// consecutive threads take consecutive rows, so the stores to y [column][row] coalesce. The
+// loads of up to kMergeWin windows are in flight together.
+constexpr int kMergeWin = 4;
+__device__ void merge_group(const BParams& p, const Geo& G, unsigned long long* kred) {
+    const bool silu = p.epi == QL_EPI_SILU_MUL;
+    const int rpt = silu ? 8 : 16;                         // output rows per tile
+    const int nrows = (G.T1 - G.T0) * rpt, c8n = (p.B + 7) >> 3;
+    const int lim = silu ? (p.M.rows >> 1) : p.M.rows;
+    const size_t wstride = (size_t)p.M.ntile * 16 * (kMaxCols / 4);   // float4 per window
+    const float4* part = reinterpret_cast<const float4*>(p.part);
+    for (int i = threadIdx.x; i < nrows * c8n; i += kT) {
+        const int c8 = i / nrows, lr = i - c8 * nrows;
+        const int tile = G.T0 + lr / rpt, r = lr % rpt;
+        const int row = tile * rpt + r;
+        if (row >= lim) continue;
+        const float4* q = part + ((size_t)tile * 16 + r) * (kMaxCols / 4) + 2 * c8;
+        float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        float su[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int w0 = 0; w0 < G.nwin; w0 += kMergeWin) {
+            float4 v[kMergeWin][2], vu[kMergeWin][2];
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int c = nt * 8 + 2 * t + e;
-            if (c >= p.B) continue;
-            const float va = acc[nt][e], vb = acc[nt][2 + e];   // rows g and g + 8
-            if (p.epi == QL_EPI_SILU_MUL) {
-                const int i = tile * 8 + g;
-                if (i < (p.M.rows >> 1))
-                    static_cast<__half*>(p.y)[(size_t)c * p.ld + i] = __float2half_rn(persist::silu(va) * vb);
-                continue;
+            for (int k = 0; k < kMergeWin; ++k) {
+                if (w0 + k < G.nwin) {
+                    const float4* qw = q + (size_t)(w0 + k) * wstride;
+                    v[k][0] = __ldcg(qw);
+                    v[k][1] = __ldcg(qw + 1);
+                    if (silu) {   // the up row: 8 rows further in the tile
+                        vu[k][0] = __ldcg(qw + 8 * (kMaxCols / 4));
+                        vu[k][1] = __ldcg(qw + 8 * (kMaxCols / 4) + 1);
+                    }
+                }
             }
-            float* yf = static_cast<float*>(p.y);
-            const int ra = tile * 16 + g, rb = ra + 8;
-            if (p.epi == QL_EPI_ADD_RESIDUAL) {
-                if (ra < p.M.rows) yf[(size_t)c * p.ld + ra] = __ldcg(yf + (size_t)c * p.ld + ra) + va;
-                if (rb < p.M.rows) yf[(size_t)c * p.ld + rb] = __ldcg(yf + (size_t)c * p.ld + rb) + vb;
+#pragma unroll
+            for (int k = 0; k < kMergeWin; ++k) {
+                if (w0 + k < G.nwin) {
+                    s[0] += v[k][0].x; s[1] += v[k][0].y; s[2] += v[k][0].z; s[3] += v[k][0].w;
+                    s[4] += v[k][1].x; s[5] += v[k][1].y; s[6] += v[k][1].z; s[7] += v[k][1].w;
+                    if (silu) {
+                        su[0] += vu[k][0].x; su[1] += vu[k][0].y; su[2] += vu[k][0].z; su[3] += vu[k][0].w;
+                        su[4] += vu[k][1].x; su[5] += vu[k][1].y; su[6] += vu[k][1].z; su[7] += vu[k][1].w;
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int c = 8 * c8 + k;
+            if (c >= p.B) break;
+            if (silu) {
+                static_cast<__half*>(p.y)[(size_t)c * p.ld + row] = __float2half_rn(persist::silu(s[k]) * su[k]);
             } else {
-                unsigned long long best = 0ull;
-                if (ra < p.M.rows) {
-                    yf[(size_t)c * p.ld + ra] = va;
-                    best = persist::argmax_key(va, ra);
+                float* dst = static_cast<float*>(p.y) + (size_t)c * p.ld + row;
+                if (p.epi == QL_EPI_ADD_RESIDUAL) {
+                    *dst = __ldcg(dst) + s[k];
+                } else {
+                    *dst = s[k];
+                    if (p.epi == kEpiArgmax) atomicMax(kred + c, persist::argmax_key(s[k], row));
                 }
-                if (rb < p.M.rows) {
-                    yf[(size_t)c * p.ld + rb] = vb;
-                    const unsigned long long k2 = persist::argmax_key(vb, rb);
-                    best = k2 > best ? k2 : best;
-                }
-                if (p.epi == kEpiArgmax && best) atomicMax(kred + c, best);
             }
         }
     }
@@ -290,13 +304,16 @@ __global__ void __launch_bounds__(kT, 1) gemv_batched_kernel(const __grid_consta
     __shared__ __align__(8) unsigned long long mbar[kW * kStages];
     __shared__ unsigned long long kred[kMaxCols];
     __shared__ float rs[kMaxCols];
+    __shared__ int last;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t = lane & 3;
     uint4* xs = reinterpret_cast<uint4*>(smem + kRing);
-    float4* part = reinterpret_cast<float4*>(smem + kRing);   // aliases xs between groups
+    float4* part = reinterpret_cast<float4*>(smem + kRing);   // after the units: the shared tiles
     float* bias = reinterpret_cast<float*>(smem + kRing + kXPart);
     const PMat& M = p.M;
-    const Geo G = geometry(M);
+    const Geo G = geometry(p);
+    const int U = (G.T1 - G.T0) * G.kwu;
+    const int a = persist::warp_unit<kW>(U, warp), b = persist::warp_unit<kW>(U, warp + 1);
 
     if (lane == 0)
         for (int i = 0; i < kStages; ++i)
@@ -306,152 +323,161 @@ __global__ void __launch_bounds__(kT, 1) gemv_batched_kernel(const __grid_consta
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     __syncthreads();
     BRing r;
-    r.g = 0;
-    r.w = 0;
-    r.u = -1;
-    r.b = 0;
+    r.u = a;
+    r.b = b;
     r.issued = r.consumed = 0;
     r.dead = 0;
     r.base = static_cast<uint32_t>(__cvta_generic_to_shared(smem)) + (uint32_t)(warp * kStages * kSlotBytes);
     r.mbar = static_cast<uint32_t>(__cvta_generic_to_shared(&mbar[warp * kStages]));
-    bring_seek(r, G, warp);
 #pragma unroll 1
-    for (int i = 0; i < kStages; ++i) bring_issue(r, M, G, warp, lane);
+    for (int i = 0; i < kStages; ++i) bring_issue(r, M, G, lane);
     pdl_wait();
     pdl_trigger();
     if (p.rms) load_column_rms(p, rs);
+    stage_window(p, G, G.w, rs, xs, bias);
+    __syncthreads();
 
     const int lm = lane >> 3, lrow = lane & 7;
     const uint32_t a_lo = (uint32_t)(((lm >> 1) * 16 + (lm & 1) * 8 + lrow) * 16);
     const unsigned char* ring_g = smem + (size_t)warp * kStages * kSlotBytes;
+    const int tl_first = a < b ? a / G.kwu : 0;
+    float acc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[nt][i] = 0.f;
+    float first[NT][4];   // the warp's first tile, when it shares it with the previous warp
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) first[nt][i] = 0.f;
+    bool first_parked = false, last_parked = false;
 #pragma unroll 1
-    for (int gi = 0; gi < G.ngroups; ++gi) {
-        int a, b;
-        warp_range(G, gi, warp, a, b);
-        const int tl0 = a < b ? a / G.kwu : 0, tl1 = a < b ? (b - 1) / G.kwu : 0;
-        float acc0[NT][4], acc1[NT][4];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) acc0[nt][i] = acc1[nt][i] = 0.f;
+    for (int u = a; u < b;) {
+        const int tl = u / G.kwu, kk = u - tl * G.kwu;
+        int n = b - u;
+        n = n < kSlotUnits ? n : kSlotUnits;
+        n = n < G.kwu - kk ? n : G.kwu - kk;
+        bring_wait(r, p, r.consumed);
+        __syncwarp();
+        const unsigned int slot = r.consumed % kStages;
 #pragma unroll 1
-        for (int w = 0; w < G.nwin; ++w) {
-            __syncthreads();   // the previous window's (or group's) readers of xs / part are done
-            stage_window(p, G, w, rs, xs, bias);
-            __syncthreads();
-#pragma unroll 1
-            for (int u = a; u < b;) {
-                const int tl = u / G.kwu, kk = u - tl * G.kwu;
-                int n = b - u;
-                n = n < kSlotUnits ? n : kSlotUnits;
-                n = n < G.kwu - kk ? n : G.kwu - kk;
-                bring_wait(r, p, r.consumed);
-                __syncwarp();
-                const unsigned int slot = r.consumed % kStages;
-#pragma unroll 1
-                for (int i = 0; i < n; ++i) {
-                    const uint32_t st = r.base + slot * kSlotBytes + i * kUnitBytes;
-                    const unsigned char* stg = ring_g + (size_t)slot * kSlotBytes + (size_t)i * kUnitBytes;
-                    uint32_t wv[8];
-                    ldsm_x4(st + a_lo, wv[0], wv[1], wv[2], wv[3]);
-                    ldsm_x4(st + a_lo + 2 * 16 * 16, wv[4], wv[5], wv[6], wv[7]);
-                    const uint2 sca = *reinterpret_cast<const uint2*>(stg + 1024 + g * 8);
-                    const uint2 scb = *reinterpret_cast<const uint2*>(stg + 1024 + (g + 8) * 8);
-                    const float2 da01 = __half22float2(as_h2(sca.x)), da23 = __half22float2(as_h2(sca.y));
-                    const float2 db01 = __half22float2(as_h2(scb.x)), db23 = __half22float2(as_h2(scb.y));
-                    const float da[4] = {da01.x, da01.y, da23.x, da23.y};
-                    const float db[4] = {db01.x, db01.y, db23.x, db23.y};
-                    const bool first = tl == tl0;
+        for (int i = 0; i < n; ++i) {
+            const uint32_t st = r.base + slot * kSlotBytes + i * kUnitBytes;
+            const unsigned char* stg = ring_g + (size_t)slot * kSlotBytes + (size_t)i * kUnitBytes;
+            uint32_t wv[8];
+            ldsm_x4(st + a_lo, wv[0], wv[1], wv[2], wv[3]);
+            ldsm_x4(st + a_lo + 2 * 16 * 16, wv[4], wv[5], wv[6], wv[7]);
+            const uint2 sca = *reinterpret_cast<const uint2*>(stg + 1024 + g * 8);
+            const uint2 scb = *reinterpret_cast<const uint2*>(stg + 1024 + (g + 8) * 8);
+            const float2 da01 = __half22float2(as_h2(sca.x)), da23 = __half22float2(as_h2(sca.y));
+            const float2 db01 = __half22float2(as_h2(scb.x)), db23 = __half22float2(as_h2(scb.y));
+            const float da[4] = {da01.x, da01.y, da23.x, da23.y};
+            const float db[4] = {db01.x, db01.y, db23.x, db23.y};
 #pragma unroll
-                    for (int q = 0; q < kUnitBlocks; ++q) {
-                        const int j = (kk + i) * kUnitBlocks + q;   // block within the window
-                        const uint32_t wa = wv[2 * q], wb = wv[2 * q + 1];
-                        const uint32_t sa8 = wa >> 8, sb8 = wb >> 8;
-                        const uint32_t l0 = (wa & 0x000F000Fu) | 0x64006400u, l1 = (wb & 0x000F000Fu) | 0x64006400u;
-                        const uint32_t l2 = (sa8 & 0x000F000Fu) | 0x64006400u, l3 = (sb8 & 0x000F000Fu) | 0x64006400u;
-                        const uint32_t h0 = (wa & 0x00F000F0u) | 0x64006400u, h1 = (wb & 0x00F000F0u) | 0x64006400u;
-                        const uint32_t h2 = (sa8 & 0x00F000F0u) | 0x64006400u, h3 = (sb8 & 0x00F000F0u) | 0x64006400u;
+            for (int q = 0; q < kUnitBlocks; ++q) {
+                const int j = (kk + i) * kUnitBlocks + q;   // block within the window
+                const uint32_t wa = wv[2 * q], wb = wv[2 * q + 1];
+                const uint32_t sa8 = wa >> 8, sb8 = wb >> 8;
+                const uint32_t l0 = (wa & 0x000F000Fu) | 0x64006400u, l1 = (wb & 0x000F000Fu) | 0x64006400u;
+                const uint32_t l2 = (sa8 & 0x000F000Fu) | 0x64006400u, l3 = (sb8 & 0x000F000Fu) | 0x64006400u;
+                const uint32_t h0 = (wa & 0x00F000F0u) | 0x64006400u, h1 = (wb & 0x00F000F0u) | 0x64006400u;
+                const uint32_t h2 = (sa8 & 0x00F000F0u) | 0x64006400u, h3 = (sb8 & 0x00F000F0u) | 0x64006400u;
 #pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) {
-                            const int col = nt * 8 + g;
-                            const uint4 X = col < p.B ? xs[(size_t)col * kXStride + 4 * j + t] : make_uint4(0u, 0u, 0u, 0u);
-                            const float2 bz = *reinterpret_cast<const float2*>(bias + j * kMaxCols + nt * 8 + 2 * t);
-                            float c[4] = {bz.x, bz.y, bz.x, bz.y};
-                            persist::mma16816(c, l0, l1, l2, l3, X.x, X.y);
-                            persist::mma16816(c, h0, h1, h2, h3, X.z, X.w);
-                            if (first) {
-                                acc0[nt][0] = fmaf(da[q], c[0], acc0[nt][0]);
-                                acc0[nt][1] = fmaf(da[q], c[1], acc0[nt][1]);
-                                acc0[nt][2] = fmaf(db[q], c[2], acc0[nt][2]);
-                                acc0[nt][3] = fmaf(db[q], c[3], acc0[nt][3]);
-                            } else {
-                                acc1[nt][0] = fmaf(da[q], c[0], acc1[nt][0]);
-                                acc1[nt][1] = fmaf(da[q], c[1], acc1[nt][1]);
-                                acc1[nt][2] = fmaf(db[q], c[2], acc1[nt][2]);
-                                acc1[nt][3] = fmaf(db[q], c[3], acc1[nt][3]);
-                            }
-                        }
-                    }
-                }
-                __syncwarp();
-                ++r.consumed;
-                bring_issue(r, M, G, warp, lane);   // refill the slot just read
-                u += n;
-            }
-        }
-        // end of the group: finish the tiles this warp covered entirely, park the others
-        __syncthreads();   // xs is free: part aliases it
-        const int gt0 = G.T0 + kGroupTiles * gi;
-        if (a < b) {
-#pragma unroll
-            for (int s2 = 0; s2 < 2; ++s2) {
-                const int tl = s2 == 0 ? tl0 : tl1;
-                if (s2 == 1 && tl1 == tl0) break;
-                const float (&acc)[NT][4] = s2 == 0 ? acc0 : acc1;
-                const bool owned = a <= tl * G.kwu && b >= (tl + 1) * G.kwu;
-                if (owned) {
-                    finish_tile<NT>(p, gt0 + tl, acc, kred, lane);
-                } else {
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-                        part[((warp * 2 + s2) * NT + nt) * 32 + lane] =
-                            make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
+                for (int nt = 0; nt < NT; ++nt) {
+                    const int col = nt * 8 + g;
+                    const uint4 X = col < p.B ? xs[(size_t)col * kXStride + 4 * j + t] : make_uint4(0u, 0u, 0u, 0u);
+                    const float2 bz = *reinterpret_cast<const float2*>(bias + j * kMaxCols + nt * 8 + 2 * t);
+                    float c[4] = {bz.x, bz.y, bz.x, bz.y};
+                    persist::mma16816(c, l0, l1, l2, l3, X.x, X.y);
+                    persist::mma16816(c, h0, h1, h2, h3, X.z, X.w);
+                    acc[nt][0] = fmaf(da[q], c[0], acc[nt][0]);
+                    acc[nt][1] = fmaf(da[q], c[1], acc[nt][1]);
+                    acc[nt][2] = fmaf(db[q], c[2], acc[nt][2]);
+                    acc[nt][3] = fmaf(db[q], c[3], acc[nt][3]);
                 }
             }
         }
-        __syncthreads();
-        // a shared tile is finished by the warp holding its last unit, summing in warp order
-        if (a < b) {
-            const int ts = tl0 * G.kwu;
-            if (a > ts && b >= ts + G.kwu) {
-                const int U = group_tiles(G, gi) * G.kwu;
-                float s[NT][4];
+        __syncwarp();
+        if (!r.dead) ++r.consumed;   // after a timeout the drain below still waits for this copy
+        bring_issue(r, M, G, lane);   // refill the slot just read
+        u += n;
+        if (u == b || u % G.kwu == 0) {
+            // end of this warp's part of tile tl: write it if the warp had all of the tile's
+            // units of the window, else keep it for the reduction below (first or last tile)
+            const int ts = tl * G.kwu;
+            if (a <= ts && u == ts + G.kwu) {
+                write_partial<NT>(p, G, G.T0 + tl, acc, lane);
+            } else if (tl == tl_first && !first_parked) {
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) s[nt][i] = 0.f;
-                for (int w2 = 0; w2 <= warp; ++w2) {
-                    const int a2 = persist::warp_unit<kW>(U, w2), b2 = persist::warp_unit<kW>(U, w2 + 1);
-                    if (b2 <= a2 || b2 <= ts || a2 >= ts + G.kwu) continue;
-                    const int sl = (a2 / G.kwu == tl0) ? 0 : 1;
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        const float4 v = part[((w2 * 2 + sl) * NT + nt) * 32 + lane];
-                        s[nt][0] += v.x;
-                        s[nt][1] += v.y;
-                        s[nt][2] += v.z;
-                        s[nt][3] += v.w;
-                    }
-                }
-                finish_tile<NT>(p, gt0 + tl0, s, kred, lane);
+                    for (int i = 0; i < 4; ++i) first[nt][i] = acc[nt][i];
+                first_parked = true;
+            } else {
+                last_parked = true;   // the last tile's part stays in acc
+                break;
             }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[nt][i] = 0.f;
         }
     }
-    if (p.epi == kEpiArgmax) {
-        __syncthreads();
-        if (tid < p.B) {
-            const bool act = p.active == nullptr || p.active[tid] != 0;
-            if (kred[tid] && act) atomicMax(p.keys + tid, kred[tid]);
+    __syncthreads();   // xs and bias are no longer read: part aliases them
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        part[((warp * 2 + 0) * NT + nt) * 32 + lane] =
+            first_parked ? make_float4(first[nt][0], first[nt][1], first[nt][2], first[nt][3]) : make_float4(0.f, 0.f, 0.f, 0.f);
+        part[((warp * 2 + 1) * NT + nt) * 32 + lane] =
+            last_parked ? make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    __syncthreads();
+    // a tile shared by warps is completed by the warp holding its last unit (its first tile),
+    // summing the parts in warp order
+    if (a < b) {
+        const int ts = tl_first * G.kwu;
+        if (a > ts && b >= ts + G.kwu) {
+            float s2[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) s2[nt][i] = 0.f;
+            for (int w2 = 0; w2 <= warp; ++w2) {
+                const int a2 = persist::warp_unit<kW>(U, w2), b2 = persist::warp_unit<kW>(U, w2 + 1);
+                if (b2 <= a2 || b2 <= ts || a2 >= ts + G.kwu) continue;
+                const int sl = (a2 / G.kwu == tl_first) ? 0 : 1;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const float4 v = part[((w2 * 2 + sl) * NT + nt) * 32 + lane];
+                    s2[nt][0] += v.x;
+                    s2[nt][1] += v.y;
+                    s2[nt][2] += v.z;
+                    s2[nt][3] += v.w;
+                }
+            }
+            write_partial<NT>(p, G, G.T0 + tl_first, s2, lane);
+        }
+    }
+    // the last CTA of the row group (acq_rel ticket: this CTA's partials published, everyone
+    // else's visible) adds the windows and applies the epilogue
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        unsigned int old;
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(p.tickets + G.rg) : "memory");
+        last = (int)old == G.nwin - 1;
+    }
+    __syncthreads();
+    if (last) {
+        merge_group(p, G, kred);
+        if (tid == 0) p.tickets[G.rg] = 0;   // re-arm for the next call
+        if (p.epi == kEpiArgmax) {
+            __syncthreads();
+            if (tid < p.B) {
+                const bool act = p.active == nullptr || p.active[tid] != 0;
+                if (kred[tid] && act) atomicMax(p.keys + tid, kred[tid]);
+            }
         }
     }
     // after a wait ran out: let the copies in flight land (bounded) before leaving
@@ -514,6 +540,28 @@ bool batched_gemv_shape_ok(int nblk) {
     return nblk % batched::kUnitBlocks == 0 && nst > 0 && (nst < batched::kWinUnits || nst % batched::kWinUnits == 0);
 }
 
+// K windows and row groups of the split: grid = nwin * ngr <= SMs.
+static void batched_split(int nblk, int ntile, int sms, int& nwin, int& ngr) {
+    const int nst = nblk / batched::kUnitBlocks;
+    const int kwu = nst < batched::kWinUnits ? nst : batched::kWinUnits;
+    nwin = nst / kwu;
+    ngr = sms / nwin;
+    if (ngr > ntile) ngr = ntile;
+    if (ngr < 1) ngr = 1;
+}
+
+// Workspace: the tickets first, at a place that does not depend on the matrix (so that
+// matrices of any shape can share one workspace), then the partial sums.
+static size_t ticket_bytes(int sms) { return ((size_t)sms * sizeof(int) + 255) & ~(size_t)255; }
+
+size_t batched_gemv_workspace_bytes(int rows, int nblk, int silu) {
+    const int ntile = silu ? (rows / 2 + 7) / 8 : (rows + 15) / 16;
+    const int sms = num_sms();
+    int nwin, ngr;
+    batched_split(nblk, ntile, sms, nwin, ngr);
+    return ticket_bytes(sms) + (size_t)nwin * ntile * 16 * batched::kMaxCols * sizeof(float);
+}
+
 int batched_gemv_prepare() {
     static std::mutex mu;
     static std::set<int> done;
@@ -535,12 +583,16 @@ int batched_gemv_launch(const StreamGemvArgs& a, cudaStream_t s, bool pdl) {
                "batched gemv: cols must be 128, 256, ..., 896 or a multiple of 1024");
     QL_REQUIRE(a.batch >= 1 && a.batch <= batched::kMaxCols, "batched gemv: batch must be in [1, 32]");
     QL_REQUIRE(a.rms ? (a.xf && a.norm_w && a.rs) : a.x16 != nullptr, "batched gemv: null input");
-    QL_REQUIRE(a.y && a.sync, "batched gemv: null output");
+    QL_REQUIRE(a.y && a.sync && a.workspace, "batched gemv: null output or workspace");
+    QL_REQUIRE(a.workspace_bytes >= batched_gemv_workspace_bytes(a.M.rows, a.M.nblk, a.M.silu),
+               "batched gemv: workspace too small");
     QL_REQUIRE(a.epilogue != kEpiArgmax || a.keys, "batched gemv: argmax needs keys");
     QL_REQUIRE((a.epilogue == QL_EPI_SILU_MUL) == (a.M.silu != 0), "batched gemv: SiLU*up needs a matrix packed for it");
     DevError* err = device_error_record();
     if (!err) return set_error(QL_ECUDA, "batched gemv: no device error record");
     if (int rc = batched_gemv_prepare()) return rc;
+    int nwin, ngr;
+    batched_split(a.M.nblk, a.M.ntile, num_sms(), nwin, ngr);
     batched::BParams p = {};
     p.M = a.M;
     p.B = a.batch;
@@ -551,19 +603,22 @@ int batched_gemv_launch(const StreamGemvArgs& a, cudaStream_t s, bool pdl) {
     p.norm_w = a.norm_w;
     p.eps = a.eps;
     p.y = a.y;
-    if (a.rms) {   // the RMSNorm statistics of every column, once, for all CTAs
-        const cudaError_t e0 = ql::launch(batched::rms_stats_kernel, dim3(a.batch), dim3(256), 0, s, pdl, a.xf,
-                                          a.M.nblk * 32, a.eps, a.rs);
-        if (e0 != cudaSuccess) return cuda_error(e0, "rms stats launch");
-        p.rs_in = a.rs;
-    }
     p.ld = a.ld;
     p.keys = a.keys;
     p.active = a.active;
     p.sync = a.sync;
     p.err = err;
     p.timeout_ns = 2000000000ull;
-    const int nt = (a.batch + 7) / 8, grid = num_sms();
+    p.tickets = static_cast<int*>(a.workspace);
+    p.part = reinterpret_cast<float*>(static_cast<char*>(a.workspace) + ticket_bytes(num_sms()));
+    p.ngr = ngr;
+    if (a.rms) {   // the RMSNorm statistics of every column, once, for all CTAs
+        const cudaError_t e0 = ql::launch(batched::rms_stats_kernel, dim3(a.batch), dim3(256), 0, s, pdl, a.xf,
+                                          a.M.nblk * 32, a.eps, a.rs);
+        if (e0 != cudaSuccess) return cuda_error(e0, "rms stats launch");
+        p.rs_in = a.rs;
+    }
+    const int nt = (a.batch + 7) / 8, grid = nwin * ngr;
     cudaError_t e = nt == 1   ? batched::run<1>(true, &p, grid, s, pdl)
                     : nt == 2 ? batched::run<2>(true, &p, grid, s, pdl)
                     : nt == 3 ? batched::run<3>(true, &p, grid, s, pdl)

@@ -283,12 +283,15 @@ struct StreamGemvArgs {
     const int32_t* active;
     unsigned int* sync;   // [4] zero: the abort flag of the kernel's bounded waits
     float* rs;            // batch 3-32 with rms: [batch] scratch for the columns' RMS statistics
+    void* workspace;      // batch 3-32: partial sums + tickets (batched_gemv_workspace_bytes),
+    size_t workspace_bytes;   // tickets zero before the first call (each call re-arms them)
 };
 int stream_gemv_prepare();
 int stream_gemv_launch(const StreamGemvArgs& a, cudaStream_t s, bool pdl);
 // The same over batches of up to 32 (ql_batched.cu): tensor-core products, K in windows of
 // 1024, every weight byte streamed once. Needs nblk / 4 < 8 or a multiple of 8.
 bool batched_gemv_shape_ok(int nblk);
+size_t batched_gemv_workspace_bytes(int rows, int nblk, int silu);
 int batched_gemv_prepare();
 int batched_gemv_launch(const StreamGemvArgs& a, cudaStream_t s, bool pdl);
 

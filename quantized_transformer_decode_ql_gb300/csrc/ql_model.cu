@@ -62,6 +62,8 @@ struct ql_model {
     std::vector<ql::PMat> hmats;            // host copies: 4 per layer, then lm_head
     unsigned int* ssync = nullptr;          // abort flag of the stand-alone stream GEMVs
     float* rs = nullptr;                    // [max_batch] RMS statistics of the batched GEMV
+    void* bws = nullptr;                    // batched GEMV partial sums + tickets
+    size_t bws_bytes = 0;
     bool batched_ok = false;                // every matrix width suits the batched stream GEMV
     ql::PMat plm = {};
     int max_nblk = 0, persist_nsplit = 1;
@@ -232,6 +234,8 @@ int run_step(ql_model* m, const ql_step_args* a, cudaStream_t s) {
         ga.active = a->active;
         ga.sync = m->ssync;
         ga.rs = m->rs;
+        ga.workspace = m->bws;
+        ga.workspace_bytes = m->bws_bytes;
         return B <= kPersistMaxBatch ? stream_gemv_launch(ga, s, pdl) : batched_gemv_launch(ga, s, pdl);
     };
     for (int li = 0; li < d.n_layers; ++li) {
@@ -432,7 +436,8 @@ int setup_persist(ql_model* m) {
         if (persist_prepare(maxb, m->max_nblk, (int)d.head_dim, G, (int)d.n_layers) == QL_OK) break;
     if (maxb < 1) return QL_OK;
     if (int rc0 = stream_gemv_prepare()) return rc0;
-    m->batched_ok = batched_gemv_shape_ok((int)(d.hidden / 32)) && batched_gemv_shape_ok((int)(d.intermediate / 32)) &&
+    m->batched_ok = d.max_batch > kPersistMaxBatch && batched_gemv_shape_ok((int)(d.hidden / 32)) &&
+                    batched_gemv_shape_ok((int)(d.intermediate / 32)) &&
                     batched_gemv_shape_ok((int)(d.n_heads * d.head_dim / 32)) && batched_gemv_prepare() == QL_OK;
 
     std::vector<PLayer> hl(m->layers.size());
@@ -474,6 +479,15 @@ int setup_persist(ql_model* m) {
         for (int k = 0; k < 4; ++k) hl[i].m[k] = all[4 * i + k];
     m->plm = all.back();
     m->hmats = all;
+    if (m->batched_ok) {
+        for (const PMat& pm : all) {
+            const size_t need = batched_gemv_workspace_bytes(pm.rows, pm.nblk, pm.silu);
+            m->bws_bytes = need > m->bws_bytes ? need : m->bws_bytes;
+        }
+        A(&m->bws, m->bws_bytes);
+        if (rc != QL_OK) return rc;
+        if (cudaMemset(m->bws, 0, m->bws_bytes) != cudaSuccess) return set_error(QL_ECUDA, "ql_model_create: workspace init");
+    }
     cudaError_t e = cudaMemcpy(m->players, hl.data(), hl.size() * sizeof(PLayer), cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemset(m->ptickets, 0, (size_t)maxb * d.n_kv_heads * 4);
     if (e == cudaSuccess) e = cudaMemset(m->psync, 0, 16);

@@ -189,8 +189,15 @@ extern "C" int ql_q4_0_stream_pack(const void* d_scales, const void* d_quants, i
     return persist_pack_streams(&m, 1, static_cast<uint8_t*>(d_stream), static_cast<cudaStream_t>(stream));
 }
 
+extern "C" int64_t ql_gemv_q4_0_stream_workspace_bytes(int64_t rows, int64_t cols, int silu) {
+    using namespace ql;
+    if (!stream_shape_ok(rows, cols, silu) || !batched_gemv_shape_ok((int)(cols / 32))) return 0;
+    return (int64_t)batched_gemv_workspace_bytes((int)rows, (int)(cols / 32), silu ? 1 : 0);
+}
+
 extern "C" int ql_gemv_q4_0_stream(const void* d_stream, int64_t rows, int64_t cols, const void* d_x, int64_t batch,
-                                   void* d_y, int epilogue, void* stream) {
+                                   void* d_y, int epilogue, void* d_workspace, int64_t workspace_bytes,
+                                   void* stream) {
     using namespace ql;
     QL_REQUIRE(d_stream && d_x && d_y, "ql_gemv_q4_0_stream: null pointer");
     QL_REQUIRE(epilogue == QL_EPI_NONE || epilogue == QL_EPI_ADD_RESIDUAL || epilogue == QL_EPI_SILU_MUL,
@@ -202,6 +209,8 @@ extern "C" int ql_gemv_q4_0_stream(const void* d_stream, int64_t rows, int64_t c
                "ql_gemv_q4_0_stream: batches above 2 need cols in 128..896 or a multiple of 1024");
     QL_REQUIRE(aligned(d_stream, 16) && aligned(d_x, 16) && aligned(d_y, 4),
                "ql_gemv_q4_0_stream: stream and x must be 16-byte aligned, y 4-byte");
+    QL_REQUIRE(batch <= 2 || (d_workspace && aligned(d_workspace, 256) && workspace_bytes >= 0),
+               "ql_gemv_q4_0_stream: batches above 2 need a 256-byte aligned workspace");
     // the flag's address, resolved once per device (the lookup may load the module lazily,
     // which a stream capture does not allow; the first call should come before any capture)
     static std::mutex mu;
@@ -228,6 +237,8 @@ extern "C" int ql_gemv_q4_0_stream(const void* d_stream, int64_t rows, int64_t c
     a.y = d_y;
     a.ld = (int)(silu ? rows / 2 : rows);
     a.sync = static_cast<unsigned int*>(sync);
+    a.workspace = d_workspace;
+    a.workspace_bytes = (size_t)workspace_bytes;
     return batch <= 2 ? stream_gemv_launch(a, static_cast<cudaStream_t>(stream), true)
                       : batched_gemv_launch(a, static_cast<cudaStream_t>(stream), true);
 }

@@ -139,7 +139,7 @@ def test_argument_validation_without_gpu(ql):
     assert L.ql_model_set_option(None, ql.QL_OPT_STEP_KERNEL, ql.QL_STEP_AUTO) == ql.QL_EINVAL
     assert L.ql_model_persistent_max_batch(None) == 0
     assert L.ql_q4_0_stream_pack(None, None, 16, 128, 0, None, None) == ql.QL_EINVAL
-    assert L.ql_gemv_q4_0_stream(None, 16, 128, None, 1, None, 0, None) == ql.QL_EINVAL
+    assert L.ql_gemv_q4_0_stream(None, 16, 128, None, 1, None, 0, None, 0, None) == ql.QL_EINVAL
     assert L.ql_block_pool_create(0, ctypes.byref(ctypes.c_void_p())) == ql.QL_EINVAL
     assert ql.ql_paged_attn_workspace_bytes(0, 4, 2, 64, 16, 4) == 0
 
@@ -154,3 +154,10 @@ def test_stream_layout_sizes(ql):
     assert ql.ql_q4_0_stream_bytes(16, 96, 0) == 0
     assert ql.ql_q4_0_stream_bytes(15, 128, 1) == 0
     assert ql.ql_q4_0_stream_bytes(0, 128, 0) == 0
+
+
+def test_stream_workspace_bad_shapes(ql):
+    """The batched GEMV's workspace size is 0 for shapes it does not take (no device needed)."""
+    assert ql.ql_gemv_q4_0_stream_workspace_bytes(16, 96, 0) == 0
+    assert ql.ql_gemv_q4_0_stream_workspace_bytes(16, 1152, 0) == 0
+    assert ql.ql_gemv_q4_0_stream_workspace_bytes(15, 1024, 1) == 0

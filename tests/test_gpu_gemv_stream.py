@@ -90,8 +90,18 @@ def run(w, x, epilogue, residual=None):
         y = dev(residual.astype(np.float32))
     else:
         y = torch.full((B, rows), float("nan"), dtype=torch.float32, device="cuda")
-    ql.ql_gemv_q4_0_stream(buf, rows, cols, dev(x), B, y, epilogue)
+    ws = None
+    if B > 2:
+        ws = torch.zeros(ql.ql_gemv_q4_0_stream_workspace_bytes(rows, cols, silu), dtype=torch.uint8, device="cuda")
+    y0 = y.clone()
+    ql.ql_gemv_q4_0_stream(buf, rows, cols, dev(x), B, y, epilogue, ws)
     torch.cuda.synchronize()
+    if ws is not None and epilogue != ql.QL_EPI_ADD_RESIDUAL:
+        # the workspace is left ready (tickets re-armed): a second call gives the same bits
+        y2 = y0.clone()
+        ql.ql_gemv_q4_0_stream(buf, rows, cols, dev(x), B, y2, epilogue, ws)
+        torch.cuda.synchronize()
+        assert torch.equal(y, y2)
     return y.float().cpu().numpy().astype(np.float64), ref
 
 
@@ -183,3 +193,44 @@ def test_stream_gemv_rejects_bad_arguments():
         with pytest.raises(ql.QLError) as e:
             ql.ql_gemv_q4_0_stream(t, rows, cols, x, batch, y, epi)
         assert e.value.status == ql.QL_EINVAL
+    # batches above 2 need a workspace of the size the shape asks for
+    need = ql.ql_gemv_q4_0_stream_workspace_bytes(16, 1024, 0)
+    assert need > 0
+    for ws in (None, torch.zeros(need - 256, dtype=torch.uint8, device="cuda")):
+        with pytest.raises(ql.QLError) as e:
+            ql.ql_gemv_q4_0_stream(t, 16, 1024, x, 3, y, ql.QL_EPI_NONE, ws)
+        assert e.value.status == ql.QL_EINVAL
+
+
+def test_stream_gemv_batched_shared_workspace():
+    """Matrices of different shapes take turns on one workspace (as the decode step's projections
+    do): the results equal those of separate workspaces, bit for bit."""
+    ql = lib()
+    B = 8
+    shapes = [(6144, 4096, 0), (1400, 1024, 1), (4096, 12288, 0), (300, 2048, 0)]
+    mats, outs_sep, xs = [], [], []
+    for i, (rows, cols, silu) in enumerate(shapes):
+        w = ql_inputs.gemv_weight(rows, cols, seed=40 + i)
+        _, _, buf = packed(w, silu)
+        x = dev(ql_inputs.gemv_activations(B, cols, seed=50 + i))
+        mats.append((rows, cols, silu, buf))
+        xs.append(x)
+
+    def call(k, ws):
+        rows, cols, silu, buf = mats[k]
+        epi = ql.QL_EPI_SILU_MUL if silu else ql.QL_EPI_NONE
+        y = torch.zeros((B, rows // 2), dtype=torch.float16, device="cuda") if silu else \
+            torch.zeros((B, rows), dtype=torch.float32, device="cuda")
+        ql.ql_gemv_q4_0_stream(buf, rows, cols, xs[k], B, y, epi, ws)
+        return y
+
+    for k, (rows, cols, silu, _) in enumerate(mats):
+        ws = torch.zeros(ql.ql_gemv_q4_0_stream_workspace_bytes(rows, cols, silu), dtype=torch.uint8, device="cuda")
+        outs_sep.append(call(k, ws))
+    shared = torch.zeros(max(ql.ql_gemv_q4_0_stream_workspace_bytes(r, c, s) for r, c, s, _ in mats),
+                         dtype=torch.uint8, device="cuda")
+    for _ in range(3):
+        got = [call(k, shared) for k in range(len(mats))]
+        torch.cuda.synchronize()
+        for k in range(len(mats)):
+            assert torch.equal(got[k], outs_sep[k]), f"matrix {k}"
