@@ -248,7 +248,7 @@ def gpu_arm(args, rank, world, local_rank):
     ms_max = max_over_ranks(ms, world)
     gm.ql_check_device_error()
     toks = out_tokens.cpu().numpy()
-    phases = step_phases(gm, sargs, s, cfg) if persistent else None
+    phases = step_phases(gm, sargs, s, cfg) if persistent else launch_phases(gm, sargs, s, cfg)
 
     # ---- algorithmic bytes per step (weights + KV read/write + embedding row + logits)
     wbytes = gm.weight_bytes()
@@ -395,6 +395,58 @@ def launches_per_step(cfg, B):
     per_layer = (gemv_passes(cfg.hidden, B) * 2 + gemv_passes(cfg.n_heads * cfg.head_dim, B)
                  + gemv_passes(cfg.intermediate, B) + 1)
     return 2 + per_layer * cfg.n_layers + gemv_passes(cfg.hidden, B)
+
+
+def launch_phases(gm, sargs, s, cfg):
+    """Per-GEMV phase times of a step of separate launches (batch 1-2) from the GEMV kernels'
+    globaltimer trace (untimed eager steps after the timed region). Per matrix kind, means over
+    layers, in us: "gap" = first CTA start minus the previous GEMV's last CTA end (covers the
+    launches in between, e.g. attention before o), "wait" = last CTA past its wait on the
+    predecessor minus first CTA start, "stage" / "loop" / "finish" = per-CTA mean durations of
+    activation staging, the unit loop and the epilogues, "tail" = last CTA end minus the mean
+    CTA end, "span" = last end minus first start."""
+    import numpy as np
+    import torch
+    import quantized_transformer_decode_ql_gb300 as ql
+    grid = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    rows = 4 * cfg.n_layers + 1
+    B = int(sargs.batch) if hasattr(sargs, "batch") else 1
+    buf = torch.zeros(rows * grid * 8, dtype=torch.int64, device="cuda")
+    gm.ql_model_set_option(ql.QL_OPT_STEP_TRACE, buf.data_ptr())
+    try:   # a graph captured with the trace on, replayed as the timed graph is
+        gm.ql_decode_graph_capture(sargs, s)
+        with torch.cuda.stream(s):
+            gm.ql_decode_graph_replay(B, 2, s)
+        s.synchronize()
+        buf.zero_()
+        with torch.cuda.stream(s):
+            gm.ql_decode_graph_replay(B, 1, s)
+        s.synchronize()
+    finally:
+        gm.ql_model_set_option(ql.QL_OPT_STEP_TRACE, 0)
+        gm.ql_decode_graph_capture(sargs, s)
+    gm.ql_check_device_error()
+    t = buf.cpu().numpy().reshape(rows, grid, 8).astype(np.float64)
+    if not (t[:, :, 0] > 0).all():
+        return None   # another GEMV form ran (not traced)
+    kinds = [k for _ in range(cfg.n_layers) for k in ("qkv", "o", "gate_up", "down")] + ["lm_head"]
+    acc = {}
+    for k in range(rows):
+        r = t[k]
+        v = {"gap": (r[:, 0].min() - t[k - 1][:, 5].max()) if k > 0 else float("nan"),
+             "wait": r[:, 1].max() - r[:, 0].min(),
+             "stage": (r[:, 2] - r[:, 1]).mean(), "loop": (r[:, 3] - r[:, 2]).mean(),
+             "finish": (r[:, 5] - r[:, 3]).mean(), "tail": r[:, 5].max() - r[:, 5].mean(),
+             "span": r[:, 5].max() - r[:, 0].min(),
+             "ring_wait_frac": r[:, 6].sum() / max(r[:, 7].sum(), 1.0)}
+        a = acc.setdefault(kinds[k], [])
+        a.append(v)
+    out = {}
+    for n, lst in acc.items():
+        out[n] = {key: round(float(np.nanmean([d[key] for d in lst])) / (1.0 if key == "ring_wait_frac" else 1e3), 3)
+                  for key in lst[0]}
+    out["total_step_us"] = round((t[rows - 1][:, 5].max() - t[0][:, 0].min()) / 1e3, 1)
+    return out
 
 
 def step_phases(gm, sargs, s, cfg):
@@ -669,8 +721,9 @@ def micro_gemv(shapes, batches, iters):
     return out
 
 
-def micro_attn(batches, iters):
-    """Paged GQA decode attention alone: 32/8 heads, hd 128, lengths uniform in [512, 32768]."""
+def micro_attn(batches, iters, ctx=0):
+    """Paged GQA decode attention alone: 32/8 heads, hd 128, lengths uniform in [512, 32768]
+    (ctx > 0: every sequence ctx tokens long)."""
     import torch
     from quantized_transformer_decode_ql_gb300 import build as qbuild
     qbuild.build()
@@ -681,7 +734,7 @@ def micro_attn(batches, iters):
     g = torch.Generator(device="cuda")
     g.manual_seed(4)
     for B in batches:
-        lens = ql_inputs.batched_lengths(B, 512, 32768, seed=6)
+        lens = ql_inputs.batched_lengths(B, 512, 32768, seed=6) if ctx <= 0 else np.full(B, ctx, dtype=np.int32)
         nblk = [(int(L) + 15) // 16 for L in lens]
         maxb = max(nblk)
         num_blocks = sum(nblk)
@@ -740,6 +793,7 @@ def main():
     ap.add_argument("--shape", default=None, help="micro gemv: ROWSxCOLS (default: all shapes)")
     ap.add_argument("--batch", default=None, help="micro: comma-separated batch sizes")
     ap.add_argument("--iters", type=int, default=50)
+    ap.add_argument("--ctx", type=int, default=0, help="micro attn: one context length for every sequence")
     args = ap.parse_args()
     if args.micro == "gemv":
         shapes = [tuple(int(v) for v in args.shape.split("x"))] if args.shape else ql_inputs.GEMV_SHAPES
@@ -748,7 +802,7 @@ def main():
         return
     if args.micro == "attn":
         batches = [int(b) for b in args.batch.split(",")] if args.batch else [1, 2, 4, 8, 16, 32, 64]
-        micro_attn(batches, args.iters)
+        micro_attn(batches, args.iters, args.ctx)
         return
     rank, world, local_rank = dist_env()
     if world > 1:

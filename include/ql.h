@@ -266,8 +266,13 @@ enum { QL_STEP_AUTO = 0, QL_STEP_LAUNCHES = 1, QL_STEP_PERSISTENT = 2 };
  *                              entries 0/1 = arrival at / exit from barrier k, entries 2..5 =
  *                              steps of the phase that ends at barrier k (GEMV: activations
  *                              staged, warp 0's units done, all warps done, epilogues done;
- *                              attention: q ready, blocks merged, split ticket taken, end); a
- *                              profiling aid
+ *                              attention: q ready, blocks merged, split ticket taken, end).
+ *                              A step of separate launches at batch 1-2 stamps its GEMV
+ *                              launches instead: launch k (qkv, o, gate_up, down of each layer,
+ *                              then lm_head) fills row k, per CTA: 0 start, 1 predecessor
+ *                              done, 2 activations staged, 3 warp 0's units done, 4 all warps
+ *                              done, 5 epilogues done (6, 7: warp 0's cycles waiting for bulk
+ *                              copies / in its unit loop). A profiling aid
  * Applies to steps issued (or graphs captured) afterwards. QL_EINVAL for anything else.  */
 enum { QL_OPT_STEP_KERNEL = 1, QL_OPT_BARRIER_TIMEOUT_NS = 2, QL_OPT_TEST_BARRIER_EXTRA = 3,
        QL_OPT_STEP_TRACE = 4 };

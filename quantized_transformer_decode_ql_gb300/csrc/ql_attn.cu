@@ -75,18 +75,41 @@ __device__ __forceinline__ int bt_row_phys(const AParams& p, int b, int lb) {
     return (phys >= 0 && phys < p.num_blocks) ? phys : -1;
 }
 
+// What one lane needs of a norm weight and of the rotation table row for warp_norm_rope:
+// elements i and i + HD/2 for i = lane, lane + 32, ... (loaded before the kernel waits on its
+// predecessor: weights and tables are constants of the step).
+template <int HD>
+struct RopeLane {
+    static constexpr int PER = HD / 64;
+    float wa[PER], wb[PER], c[PER], s[PER];
+};
+template <int HD>
+__device__ __forceinline__ RopeLane<HD> rope_lane(const float* w, const float* cos_row, const float* sin_row,
+                                                  int lane) {
+    RopeLane<HD> r;
+#pragma unroll
+    for (int k = 0; k < RopeLane<HD>::PER; ++k) {
+        const int i = lane + 32 * k;
+        r.wa[k] = __ldg(w + i);
+        r.wb[k] = __ldg(w + i + HD / 2);
+        r.c[k] = __ldg(cos_row + i);
+        r.s[k] = __ldg(sin_row + i);
+    }
+    return r;
+}
+
 // RMSNorm over one head (weight w) and NeoX rotation at table row `pos`, by one warp:
 // lane handles the pairs (i, i + HD/2) for i = lane, lane + 32, ...; writes f16 to dst.
 template <int HD>
-__device__ __forceinline__ void warp_norm_rope(const float* src, const float* w, const float* cos_row,
-                                               const float* sin_row, float eps, __half* dst, int lane) {
-    constexpr int H2 = HD / 2, PER = H2 / 32;
+__device__ __forceinline__ void warp_norm_rope(const float* src, const RopeLane<HD>& rl, float eps, __half* dst,
+                                               int lane) {
+    constexpr int H2 = HD / 2, PER = RopeLane<HD>::PER;
     float xa[PER], xb[PER];
     float ss = 0.f;
 #pragma unroll
     for (int k = 0; k < PER; ++k) {
-        xa[k] = src[lane + 32 * k];
-        xb[k] = src[lane + 32 * k + H2];
+        xa[k] = __ldcg(src + lane + 32 * k);
+        xb[k] = __ldcg(src + lane + 32 * k + H2);
         ss += xa[k] * xa[k] + xb[k] * xb[k];
     }
 #pragma unroll
@@ -95,10 +118,9 @@ __device__ __forceinline__ void warp_norm_rope(const float* src, const float* w,
 #pragma unroll
     for (int k = 0; k < PER; ++k) {
         const int i = lane + 32 * k;
-        const float a = xa[k] * r * w[i], bb = xb[k] * r * w[i + H2];
-        const float c = cos_row[i], sn = sin_row[i];
-        dst[i] = __float2half_rn(a * c - bb * sn);
-        dst[i + H2] = __float2half_rn(a * sn + bb * c);
+        const float a = xa[k] * r * rl.wa[k], bb = xb[k] * r * rl.wb[k];
+        dst[i] = __float2half_rn(a * rl.c[k] - bb * rl.s[k]);
+        dst[i + H2] = __float2half_rn(a * rl.s[k] + bb * rl.c[k]);
     }
 }
 
@@ -184,9 +206,22 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AParams p, Dev
         asm volatile("cp.async.commit_group;" ::: "memory");
         return ok;
     };
-    bool vcur = false;
+    // both buffers of the warp in flight from the start (blocks 0 and 1; an empty group when the
+    // warp has one block): in the fused form before the wait
+    bool vbuf[2] = {false, false};
+    auto stage_first = [&]() {
+        if (nb_w > 0) vbuf[0] = stage(0);
+        if (nb_w > 1) vbuf[1] = stage(1);
+        else asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    const bool pos_ok = pos < p.max_position;
+    RopeLane<HD> rq, rk;
     if (fused) {
-        if (nb_w > 0) vcur = stage(0);
+        stage_first();
+        const float* cr = p.cos_t + (size_t)(pos_ok ? pos : 0) * (HD / 2);
+        const float* sr = p.sin_t + (size_t)(pos_ok ? pos : 0) * (HD / 2);
+        rq = rope_lane<HD>(p.q_norm, cr, sr, lane);
+        if (warp == 0) rk = rope_lane<HD>(p.k_norm, cr, sr, lane);
         pdl_wait();
         pdl_trigger();
     }
@@ -204,12 +239,9 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AParams p, Dev
         // normalise + rotate the G query heads here; the CTA holding the new position's block
         // also normalises + rotates the new key and appends K and V
         const float* src = p.qkv + (size_t)b * (p.n_heads + 2 * p.n_kv) * HD;
-        const bool pos_ok = pos < p.max_position;
         if (!pos_ok && s == 0 && threadIdx.x == 0) record_device_error(err, kErrRopePosition, b, pos);
-        const float* cr = p.cos_t + (size_t)(pos_ok ? pos : 0) * (HD / 2);
-        const float* sr = p.sin_t + (size_t)(pos_ok ? pos : 0) * (HD / 2);
         for (int h = warp; h < G; h += kAttnWarps)
-            warp_norm_rope<HD>(src + (size_t)(g * G + h) * HD, p.q_norm, cr, sr, p.eps, qs[h], lane);
+            warp_norm_rope<HD>(src + (size_t)(g * G + h) * HD, rq, p.eps, qs[h], lane);
         if (pos_ok && lblk >= blk0 && lblk < blk1 && warp < 2) {
             const int phys = bt_row_phys(p, b, lblk);
             if (phys < 0) {
@@ -217,7 +249,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AParams p, Dev
             } else {
                 const size_t off = (((size_t)phys * p.n_kv + g) * kBS + kp) * HD;
                 if (warp == 0) {
-                    warp_norm_rope<HD>(src + (size_t)(p.n_heads + g) * HD, p.k_norm, cr, sr, p.eps, knew, lane);
+                    warp_norm_rope<HD>(src + (size_t)(p.n_heads + g) * HD, rk, p.eps, knew, lane);
                     __syncwarp();
                     for (int i = lane; i < HD / 8; i += 32)
                         reinterpret_cast<uint4*>(p.kw + off)[i] = reinterpret_cast<const uint4*>(knew)[i];
@@ -249,13 +281,13 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AParams p, Dev
 #pragma unroll
     for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
     float mrow = -INFINITY, lrow = 0.f;
-    if (!fused && nb_w > 0) vcur = stage(0);
+    if (!fused) stage_first();
     for (int i = 0; i < nb_w; ++i) {
-        bool vnext = false;
-        if (i + 1 < nb_w) vnext = stage(i + 1);
-        else asm volatile("cp.async.commit_group;" ::: "memory");
+        // groups committed so far: blocks 0 .. i + 1 (one per block, empty past the end); block i
+        // has landed when at most one group is pending
         asm volatile("cp.async.wait_group 1;" ::: "memory");
         __syncwarp();
+        const bool vcur = vbuf[i & 1];
         const int blk = blk0 + warp + kAttnWarps * i;
         const int nt = min(kBS, L - blk * kBS);      // valid keys in this block
         if (vcur && fused && blk == lblk) {
@@ -327,8 +359,9 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AParams p, Dev
                 mma_f16(o[2 * pp + 1], ua0, 0u, ua1, 0u, r2, r3);
             }
         }
-        __syncwarp();
-        vcur = vnext;
+        __syncwarp();   // every lane is done with buffer i & 1: block i + 2 may land there
+        if (i + 2 < nb_w) vbuf[i & 1] = stage(i + 2);
+        else asm volatile("cp.async.commit_group;" ::: "memory");
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
     __syncthreads();   // every warp is done with its tiles: the buffer now holds the merge state

@@ -285,7 +285,10 @@ struct StreamGemvArgs {
     float* rs;            // batch 3-32 with rms: [batch] scratch for the columns' RMS statistics
     void* workspace;      // batch 3-32: partial sums + tickets (batched_gemv_workspace_bytes),
     size_t workspace_bytes;   // tickets zero before the first call (each call re-arms them)
+    unsigned long long* trace;   // batch 1-2, optional: [grid][8] globaltimer stamps per CTA
+    NextWeights next;     // batch 1-2: constants of a later kernel, prefetched into L2
 };
+int persist_trace_words();   // trace entries per CTA and row
 int stream_gemv_prepare();
 int stream_gemv_launch(const StreamGemvArgs& a, cudaStream_t s, bool pdl);
 // The same over batches of up to 32 (ql_batched.cu): tensor-core products, K in windows of

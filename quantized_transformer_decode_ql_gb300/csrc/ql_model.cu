@@ -217,9 +217,13 @@ int run_step(ql_model* m, const ql_step_args* a, cudaStream_t s) {
     // batch 1-2: the GEMVs stream the tile stream copy of the weights (stream_gemv_launch);
     // batch 3-32: the same copy, batched (batched_gemv_launch); above: row-major passes
     const bool streamed = !m->hmats.empty() && (B <= kPersistMaxBatch || (m->batched_ok && B <= 32));
+    int gemv_k = 0;   // GEMV launches so far (their trace rows)
     auto sg = [&](const PMat& M, int epi, bool rms, const float* xf, const __half* x16, const float* nw, void* y,
-                  int ld) {
+                  int ld, NextWeights next) {
         StreamGemvArgs ga = {};
+        ga.next = next;
+        if (m->trace && B <= kPersistMaxBatch) ga.trace = m->trace + (size_t)gemv_k * num_sms() * persist_trace_words();
+        ++gemv_k;
         ga.M = M;
         ga.batch = B;
         ga.epilogue = epi;
@@ -243,7 +247,14 @@ int run_step(ql_model* m, const ql_step_args* a, cudaStream_t s) {
         if (streamed) {
             const PMat* Ms = &m->hmats[4 * li];
             const int qkv_ld = (int)((d.n_heads + 2 * d.n_kv_heads) * d.head_dim);
-            if ((rc = sg(Ms[0], QL_EPI_NONE, true, m->x, nullptr, L.attn_norm, m->qkv, qkv_ld)) != QL_OK) return rc;
+            // each GEMV warms L2 with the norm weights that the kernel after it reads first
+            const NextWeights qk_norms = {{L.q_norm, L.k_norm}, {(size_t)hd * 4, (size_t)hd * 4}};
+            const NextWeights ffn_norm = {{L.ffn_norm, nullptr}, {(size_t)d.hidden * 4, 0}};
+            const float* next_norm = li + 1 < d.n_layers ? m->layers[li + 1].attn_norm : d.final_norm;
+            const NextWeights next_attn_norm = {{next_norm, nullptr}, {(size_t)d.hidden * 4, 0}};
+            const NextWeights none = {{nullptr, nullptr}, {0, 0}};
+            if ((rc = sg(Ms[0], QL_EPI_NONE, true, m->x, nullptr, L.attn_norm, m->qkv, qkv_ld, qk_norms)) != QL_OK)
+                return rc;
             AttnArgs at = {};
             at.qkv = m->qkv;
             at.q_norm = L.q_norm;
@@ -269,11 +280,14 @@ int run_step(ql_model* m, const ql_step_args* a, cudaStream_t s) {
             at.workspace = m->attn_ws;
             at.workspace_bytes = m->attn_ws_bytes;
             if ((rc = attn_launch(at, s, pdl)) != QL_OK) return rc;
-            if ((rc = sg(Ms[1], QL_EPI_ADD_RESIDUAL, false, nullptr, m->attn, nullptr, m->x, (int)d.hidden)) != QL_OK)
+            if ((rc = sg(Ms[1], QL_EPI_ADD_RESIDUAL, false, nullptr, m->attn, nullptr, m->x, (int)d.hidden,
+                         ffn_norm)) != QL_OK)
                 return rc;
-            if ((rc = sg(Ms[2], QL_EPI_SILU_MUL, true, m->x, nullptr, L.ffn_norm, m->act, (int)d.intermediate)) != QL_OK)
+            if ((rc = sg(Ms[2], QL_EPI_SILU_MUL, true, m->x, nullptr, L.ffn_norm, m->act, (int)d.intermediate,
+                         none)) != QL_OK)
                 return rc;
-            if ((rc = sg(Ms[3], QL_EPI_ADD_RESIDUAL, false, nullptr, m->act, nullptr, m->x, (int)d.hidden)) != QL_OK)
+            if ((rc = sg(Ms[3], QL_EPI_ADD_RESIDUAL, false, nullptr, m->act, nullptr, m->x, (int)d.hidden,
+                         next_attn_norm)) != QL_OK)
                 return rc;
             continue;
         }
@@ -370,8 +384,9 @@ int run_step(ql_model* m, const ql_step_args* a, cudaStream_t s) {
     }
 
     if (streamed) {
+        const NextWeights first_norm = {{m->layers[0].attn_norm, nullptr}, {(size_t)d.hidden * 4, 0}};
         if ((rc = sg(m->hmats.back(), kEpiArgmax, true, m->x, nullptr, d.final_norm,
-                     a->logits ? a->logits : m->logits, (int)d.vocab)) != QL_OK)
+                     a->logits ? a->logits : m->logits, (int)d.vocab, first_norm)) != QL_OK)
             return rc;
         e = launch(finalize_kernel, dim3(1), dim3(64), 0, s, pdl, m->keys, a->active, a->positions,
                    a->next_tokens, a->out_tokens, (long long)a->out_stride, (float*)nullptr, B);

@@ -88,6 +88,8 @@ int stream_gemv_prepare() {
     return QL_OK;
 }
 
+int persist_trace_words() { return persist::kTraceWords; }
+
 int stream_gemv_launch(const StreamGemvArgs& a, cudaStream_t s, bool pdl) {
     QL_REQUIRE(a.M.stream && a.M.nblk > 0 && a.M.nblk % persist::kUnitBlocks == 0, "stream gemv: bad matrix");
     QL_REQUIRE(a.batch == 1 || a.batch == 2, "stream gemv: batch must be 1 or 2");
@@ -116,6 +118,17 @@ int stream_gemv_launch(const StreamGemvArgs& a, cudaStream_t s, bool pdl) {
     g.norm_w = a.norm_w;
     g.y = a.y;
     g.ld = a.ld;
+    g.trace = stream_gemv_warps() == 16 ? a.trace : nullptr;   // the trace rows hold one CTA per SM
+    g.next = a.next;
+    // one ring slot per warp before the wait, the other after the activations are staged (their
+    // loads then queue behind half as much weight data; measured faster than both slots or none
+    // in the decode step); QL_STREAM_PREWAIT=0..2 selects another count for A/B measurements
+    static const int prewait = [] {
+        const char* e = std::getenv("QL_STREAM_PREWAIT");
+        const int v = e ? std::atoi(e) : 1;
+        return v < 0 ? 0 : (v > persist::kStages ? persist::kStages : v);
+    }();
+    g.prewait = prewait;
     // one CTA of 16 warps per SM (measured faster in the step than two CTAs of 8 warps, which
     // would let a kernel's set-up overlap the previous kernel's tail); QL_STREAM_GEMV_WARPS=8
     // selects the two-CTA form for A/B measurements

@@ -514,6 +514,9 @@ __device__ __noinline__ void gemv_phase(const PersistParams& p, const PMat* mats
     stamp(tr, 2);
 
     Ring r = ring;   // a register copy for the loop; written back at the end
+    // slots not yet in flight (a kernel may issue fewer than kStages before it waits on its
+    // predecessor, so that its activation loads do not queue behind a full ring)
+    for (unsigned int i = r.issued - r.consumed; i < (unsigned int)kStages; ++i) ring_issue<W>(r, mats, warp, lane);
     const int nst = M.nblk / kUnitBlocks;
     int T0, T1;
     cta_tiles(M.ntile, T0, T1);
@@ -1219,6 +1222,10 @@ struct StreamGemv {
     const float* norm_w;
     void* y;
     int ld;
+    unsigned long long* trace;   // optional [grid][kTraceWords]: 0 start, 1 after the wait, 2-7 as
+                                 // in gemv_phase
+    NextWeights next;            // prefetched into L2 before the wait
+    int prewait;                 // ring slots issued before the wait (the rest after staging)
 };
 
 template <int NB, int W>
@@ -1230,6 +1237,8 @@ __global__ void __launch_bounds__(W * 32, 16 / W) gemv_stream_kernel(const __gri
     __shared__ unsigned long long kred[W][kMaxB];
     __shared__ __align__(8) unsigned long long mbar[W * kStages];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    unsigned long long* tr = g.trace ? g.trace + (size_t)blockIdx.x * kTraceWords : nullptr;
+    stamp(tr, 0);
     if (threadIdx.x == 0) mat = g.M;
     if (lane == 0)
         for (int i = 0; i < kStages; ++i)
@@ -1248,13 +1257,17 @@ __global__ void __launch_bounds__(W * 32, 16 / W) gemv_stream_kernel(const __gri
     r.mbar = static_cast<uint32_t>(__cvta_generic_to_shared(&mbar[warp * kStages]));
     ring_seek<W>(r, &mat, warp);
 #pragma unroll 1
-    for (int i = 0; i < kStages; ++i) ring_issue<W>(r, &mat, warp, lane);
+    for (int i = 0; i < g.prewait; ++i) ring_issue<W>(r, &mat, warp, lane);
+    // constants of a later kernel of the step (its norm weights), into L2 off its critical path
+    l2_prefetch_share(g.next.ptr[0], g.next.bytes[0]);
+    l2_prefetch_share(g.next.ptr[1], g.next.bytes[1]);
     // the trigger follows the wait in every kernel of the step: a kernel's code before its
     // wait then runs only after the kernel two launches back has completed
     pdl_wait();
     pdl_trigger();
+    stamp(tr, 1);
     gemv_phase<NB, W>(p, &mat, 0, g.epi, g.rms != 0, r, g.xf, g.x16, g.norm_w, g.y, g.ld,
-                      smem + (size_t)W * kStages * kSlotBytes, red, kred, nullptr);
+                      smem + (size_t)W * kStages * kSlotBytes, red, kred, tr);
     const unsigned long long t0 = global_ns();
     while (r.consumed < r.issued) {   // only after a wait ran out: let copies land (bounded)
         const uint32_t mb = r.mbar + (r.consumed % kStages) * 8, parity = (r.consumed / kStages) & 1u;
