@@ -3,9 +3,11 @@
 //
 // [IL] inferencelayer cuda_llm.rs, CudaQwen3::gemv (the q4_0 format, one GEMV per projection
 // group) at the batch sizes where it becomes a skinny GEMM: each weight is used batch times, so
-// the products go to the tensor cores (mma.sync m16n8k16, f16 in, f32 accumulate) with the exact
-// nibble expansion of the batch-1 kernel (1024 + q and 1024 + 16 q in the A fragment, offsets
-// folded into the accumulator start, one FFMA per block and column for the f16 scale).
+// the products go to the tensor cores (mma.sync m16n8k16, f16 in, f32 accumulate). The A
+// fragment is the dequantised weight: the nibble expansion of the batch-1 kernel (1024 + q and
+// 1024 + 16 q, exact) less its offset (q - 8 and 16 (q - 8), exact), times the block's f16 scale
+// (one rounding to f16); a block's products then go straight into the f32 accumulator, so the
+// dequantisation is paid once per weight for all batch columns.
 //
 // Why this shape (GB300): the activations of all batch columns for the full K (32 columns x
 // 12288 x f16 = 768 KB for the down projection) do not fit in shared memory next to the weight
@@ -42,8 +44,7 @@ constexpr size_t kRing = (size_t)kW * kStages * kSlotBytes;
 constexpr size_t kXBytes = (size_t)kMaxCols * kXStride * 16;   // one window of every column
 constexpr size_t kPartBytes = (size_t)kW * 2 * 4 * 32 * 16;    // [warp][slot][n-tile][lane] float4
 constexpr size_t kXPart = kXBytes > kPartBytes ? kXBytes : kPartBytes;
-constexpr size_t kBiasBytes = (size_t)kWinUnits * kUnitBlocks * kMaxCols * 4;
-constexpr size_t kSmem = kRing + kXPart + kBiasBytes;
+constexpr size_t kSmem = kRing + kXPart;
 
 struct BParams {
     PMat M;
@@ -135,15 +136,12 @@ __device__ void load_column_rms(const BParams& p, float* rs) {
 }
 
 // Stage window w of every column: f16 pairs in the order a code word expands to (high ones
-// pre-divided by 16) and the accumulator start -(1032 sum x_lo + 1152 sum x_hi / 16) of every
-// (block, column); columns past the batch have zero offsets (their activations are never read).
-__device__ void stage_window(const BParams& p, const Geo& G, int w, const float* rs, uint4* xs, float* bias) {
+// pre-divided by 16, which is exact). Columns past the batch are never read.
+__device__ void stage_window(const BParams& p, const Geo& G, int w, const float* rs, uint4* xs) {
     const int tid = threadIdx.x;
     const int nb = G.kwu * kUnitBlocks;        // blocks in the window
     const int cols = p.M.nblk * 32;
     const int j0 = w * nb;
-    for (int i = tid; i < nb * kMaxCols; i += kT) bias[i] = 0.f;
-    __syncthreads();
     const int nitems = p.B * nb * 4;
     constexpr int kChunk = 4;   // items per thread whose loads are in flight together
     for (int base = 0; base < nitems; base += kChunk * kT) {   // warp-uniform bounds (shuffles)
@@ -192,16 +190,7 @@ __device__ void stage_window(const BParams& p, const Geo& G, int w, const float*
                                                  __half2float(__float2half_rn(v[6])) * 0.0625f);
             const __half2 p3 = __floats2half2_rn(__half2float(__float2half_rn(v[5])) * 0.0625f,
                                                  __half2float(__float2half_rn(v[7])) * 0.0625f);
-            const float2 f0 = __half22float2(p0), f1 = __half22float2(p1);
-            const float2 f2 = __half22float2(p2), f3 = __half22float2(p3);
-            // sum (1024 + q) x_lo + (1024 + 16 q) x_hi/16 = sum (q - 8) x + 1032 sum x_lo + 1152 sum x_hi/16
-            float part = 1032.0f * ((f0.x + f0.y) + (f1.x + f1.y)) + 1152.0f * ((f2.x + f2.y) + (f3.x + f3.y));
-            part += __shfl_xor_sync(0xffffffffu, part, 1);
-            part += __shfl_xor_sync(0xffffffffu, part, 2);
-            if (live) {
-                xs[(size_t)c * kXStride + 4 * j + t] = make_uint4(as_u32(p0), as_u32(p1), as_u32(p2), as_u32(p3));
-                if (t == 0) bias[j * kMaxCols + c] = -part;
-            }
+            if (live) xs[(size_t)c * kXStride + 4 * j + t] = make_uint4(as_u32(p0), as_u32(p1), as_u32(p2), as_u32(p3));
         }
     }
 }
@@ -309,7 +298,6 @@ __global__ void __launch_bounds__(kT, 1) gemv_batched_kernel(const __grid_consta
     const int g = lane >> 2, t = lane & 3;
     uint4* xs = reinterpret_cast<uint4*>(smem + kRing);
     float4* part = reinterpret_cast<float4*>(smem + kRing);   // after the units: the shared tiles
-    float* bias = reinterpret_cast<float*>(smem + kRing + kXPart);
     const PMat& M = p.M;
     const Geo G = geometry(p);
     const int U = (G.T1 - G.T0) * G.kwu;
@@ -334,7 +322,7 @@ __global__ void __launch_bounds__(kT, 1) gemv_batched_kernel(const __grid_consta
     pdl_wait();
     pdl_trigger();
     if (p.rms) load_column_rms(p, rs);
-    stage_window(p, G, G.w, rs, xs, bias);
+    stage_window(p, G, G.w, rs, xs);
     __syncthreads();
 
     const int lm = lane >> 3, lrow = lane & 7;
@@ -370,31 +358,31 @@ __global__ void __launch_bounds__(kT, 1) gemv_batched_kernel(const __grid_consta
             ldsm_x4(st + a_lo + 2 * 16 * 16, wv[4], wv[5], wv[6], wv[7]);
             const uint2 sca = *reinterpret_cast<const uint2*>(stg + 1024 + g * 8);
             const uint2 scb = *reinterpret_cast<const uint2*>(stg + 1024 + (g + 8) * 8);
-            const float2 da01 = __half22float2(as_h2(sca.x)), da23 = __half22float2(as_h2(sca.y));
-            const float2 db01 = __half22float2(as_h2(scb.x)), db23 = __half22float2(as_h2(scb.y));
-            const float da[4] = {da01.x, da01.y, da23.x, da23.y};
-            const float db[4] = {db01.x, db01.y, db23.x, db23.y};
+            const __half2 off_lo = as_h2(0x64086408u), off_hi = as_h2(0x64806480u);   // 1032, 1152
 #pragma unroll
             for (int q = 0; q < kUnitBlocks; ++q) {
                 const int j = (kk + i) * kUnitBlocks + q;   // block within the window
+                // the scales of rows g and g + 8 for block q, in both halves of a half2
+                const uint32_t sa = (q & 2) ? sca.y : sca.x, sb = (q & 2) ? scb.y : scb.x;
+                const __half2 da = (q & 1) ? __high2half2(as_h2(sa)) : __low2half2(as_h2(sa));
+                const __half2 db = (q & 1) ? __high2half2(as_h2(sb)) : __low2half2(as_h2(sb));
                 const uint32_t wa = wv[2 * q], wb = wv[2 * q + 1];
                 const uint32_t sa8 = wa >> 8, sb8 = wb >> 8;
-                const uint32_t l0 = (wa & 0x000F000Fu) | 0x64006400u, l1 = (wb & 0x000F000Fu) | 0x64006400u;
-                const uint32_t l2 = (sa8 & 0x000F000Fu) | 0x64006400u, l3 = (sb8 & 0x000F000Fu) | 0x64006400u;
-                const uint32_t h0 = (wa & 0x00F000F0u) | 0x64006400u, h1 = (wb & 0x00F000F0u) | 0x64006400u;
-                const uint32_t h2 = (sa8 & 0x00F000F0u) | 0x64006400u, h3 = (sb8 & 0x00F000F0u) | 0x64006400u;
+                // (q - 8) d and 16 (q - 8) d (against x / 16) in the A fragment: rows g (a0, a2) and g + 8
+                const uint32_t l0 = as_u32(__hmul2(__hsub2(as_h2((wa & 0x000F000Fu) | 0x64006400u), off_lo), da));
+                const uint32_t l1 = as_u32(__hmul2(__hsub2(as_h2((wb & 0x000F000Fu) | 0x64006400u), off_lo), db));
+                const uint32_t l2 = as_u32(__hmul2(__hsub2(as_h2((sa8 & 0x000F000Fu) | 0x64006400u), off_lo), da));
+                const uint32_t l3 = as_u32(__hmul2(__hsub2(as_h2((sb8 & 0x000F000Fu) | 0x64006400u), off_lo), db));
+                const uint32_t h0 = as_u32(__hmul2(__hsub2(as_h2((wa & 0x00F000F0u) | 0x64006400u), off_hi), da));
+                const uint32_t h1 = as_u32(__hmul2(__hsub2(as_h2((wb & 0x00F000F0u) | 0x64006400u), off_hi), db));
+                const uint32_t h2 = as_u32(__hmul2(__hsub2(as_h2((sa8 & 0x00F000F0u) | 0x64006400u), off_hi), da));
+                const uint32_t h3 = as_u32(__hmul2(__hsub2(as_h2((sb8 & 0x00F000F0u) | 0x64006400u), off_hi), db));
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     const int col = nt * 8 + g;
                     const uint4 X = col < p.B ? xs[(size_t)col * kXStride + 4 * j + t] : make_uint4(0u, 0u, 0u, 0u);
-                    const float2 bz = *reinterpret_cast<const float2*>(bias + j * kMaxCols + nt * 8 + 2 * t);
-                    float c[4] = {bz.x, bz.y, bz.x, bz.y};
-                    persist::mma16816(c, l0, l1, l2, l3, X.x, X.y);
-                    persist::mma16816(c, h0, h1, h2, h3, X.z, X.w);
-                    acc[nt][0] = fmaf(da[q], c[0], acc[nt][0]);
-                    acc[nt][1] = fmaf(da[q], c[1], acc[nt][1]);
-                    acc[nt][2] = fmaf(db[q], c[2], acc[nt][2]);
-                    acc[nt][3] = fmaf(db[q], c[3], acc[nt][3]);
+                    persist::mma16816(acc[nt], l0, l1, l2, l3, X.x, X.y);
+                    persist::mma16816(acc[nt], h0, h1, h2, h3, X.z, X.w);
                 }
             }
         }
@@ -424,7 +412,7 @@ __global__ void __launch_bounds__(kT, 1) gemv_batched_kernel(const __grid_consta
                 for (int i = 0; i < 4; ++i) acc[nt][i] = 0.f;
         }
     }
-    __syncthreads();   // xs and bias are no longer read: part aliases them
+    __syncthreads();   // xs is no longer read: part aliases it
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         part[((warp * 2 + 0) * NT + nt) * 32 + lane] =
