@@ -388,10 +388,14 @@ def gemv_passes(cols, batch):
 
 
 def launches_per_step(cfg, B):
-    """Kernel launches of one step in the one-launch-per-phase form (batch <= 32: one launch per
-    GEMV over the tile stream layout; above: row-major passes)."""
-    if B <= 32:
+    """Kernel launches of one step in the one-launch-per-phase form. Batch 1-2: embed, per layer
+    qkv / attention / o / gate_up / down GEMVs over the tile stream layout, lm_head, finalize.
+    Batch 3-32: each GEMV is the split-K kernel plus its merge kernel, and the two RMSNorm'd
+    GEMVs of a layer (and lm_head) get a statistics kernel first. Above 32: row-major passes."""
+    if B <= 2:
         return 3 + 5 * cfg.n_layers
+    if B <= 32:
+        return 5 + 11 * cfg.n_layers
     per_layer = (gemv_passes(cfg.hidden, B) * 2 + gemv_passes(cfg.n_heads * cfg.head_dim, B)
                  + gemv_passes(cfg.intermediate, B) + 1)
     return 2 + per_layer * cfg.n_layers + gemv_passes(cfg.hidden, B)
@@ -413,10 +417,10 @@ def launch_phases(gm, sargs, s, cfg):
     B = int(sargs.batch) if hasattr(sargs, "batch") else 1
     buf = torch.zeros(rows * grid * 8, dtype=torch.int64, device="cuda")
     gm.ql_model_set_option(ql.QL_OPT_STEP_TRACE, buf.data_ptr())
-    try:   # a graph captured with the trace on, replayed as the timed graph is
+    try:   # a graph captured with the trace on, replayed as the timed graph is (2 steps: one warm)
         gm.ql_decode_graph_capture(sargs, s)
         with torch.cuda.stream(s):
-            gm.ql_decode_graph_replay(B, 2, s)
+            gm.ql_decode_graph_replay(B, 1, s)
         s.synchronize()
         buf.zero_()
         with torch.cuda.stream(s):
@@ -427,13 +431,14 @@ def launch_phases(gm, sargs, s, cfg):
         gm.ql_decode_graph_capture(sargs, s)
     gm.ql_check_device_error()
     t = buf.cpu().numpy().reshape(rows, grid, 8).astype(np.float64)
-    if not (t[:, :, 0] > 0).all():
+    if not (t[:, 0, 0] > 0).all():
         return None   # another GEMV form ran (not traced)
     kinds = [k for _ in range(cfg.n_layers) for k in ("qkv", "o", "gate_up", "down")] + ["lm_head"]
     acc = {}
     for k in range(rows):
-        r = t[k]
-        v = {"gap": (r[:, 0].min() - t[k - 1][:, 5].max()) if k > 0 else float("nan"),
+        r = t[k][t[k][:, 0] > 0]   # the launch's CTAs (a grid may be smaller than the SM count)
+        prev_end = t[k - 1][t[k - 1][:, 0] > 0][:, 5].max() if k > 0 else float("nan")
+        v = {"gap": (r[:, 0].min() - prev_end) if k > 0 else float("nan"),
              "wait": r[:, 1].max() - r[:, 0].min(),
              "stage": (r[:, 2] - r[:, 1]).mean(), "loop": (r[:, 3] - r[:, 2]).mean(),
              "finish": (r[:, 5] - r[:, 3]).mean(), "tail": r[:, 5].max() - r[:, 5].mean(),
@@ -445,7 +450,7 @@ def launch_phases(gm, sargs, s, cfg):
     for n, lst in acc.items():
         out[n] = {key: round(float(np.nanmean([d[key] for d in lst])) / (1.0 if key == "ring_wait_frac" else 1e3), 3)
                   for key in lst[0]}
-    out["total_step_us"] = round((t[rows - 1][:, 5].max() - t[0][:, 0].min()) / 1e3, 1)
+    out["total_step_us"] = round((t[rows - 1][:, 5].max() - t[0][t[0][:, 0] > 0][:, 0].min()) / 1e3, 1)
     return out
 
 
@@ -594,6 +599,7 @@ def gpu_arm_e32(args, rank, world, local_rank):
     clocks = clock.stop()
     gm.ql_check_device_error()
     ms = sum(a.elapsed_time(b) for a, b in ev)
+    phases = launch_phases(gm, sargs, s, cfg)   # untimed, after the timed region
     peak, peak_src = load_peaks()
     value = B * steps / (ms / 1e3)
     gbs = sum(step_bytes) / (ms / 1e3) / 1e9
@@ -610,6 +616,7 @@ def gpu_arm_e32(args, rank, world, local_rank):
                           "frac": round(gbs / peak, 4), "peak": peak, "peak_source": peak_src},
         "replacement_s_excluded": round(repl_s, 3), "replacements": int((finish < steps).sum()),
         "clocks": clocks, "gpu_launches": launches_per_step(cfg, B) * steps, "setup_s": round(setup_s, 1),
+        **({"step_phases_us": phases} if phases else {}),
     }
 
 

@@ -119,12 +119,12 @@ int ql_q4_0_stream_pack(const void* d_scales, const void* d_quants, int64_t rows
  * or 16 (q - 8) (high nibble, against x/16) exactly in f16, the 32 products of a block are
  * summed in f16 (HFMA2; low and high nibbles apart), and each block is scaled by its f16 scale
  * and accumulated in f32. Batch 3-32 (needs cols in 128..896 or a multiple of 1024): the
- * tensor-core form of the row-major GEMV (f32 products and sums), split over K in windows of
- * 1024 columns so that every weight byte is streamed once; each window's f32 partial sums go
- * to d_workspace and are added in window order (deterministic). d_workspace (device, 256-byte
- * aligned, at least ql_gemv_q4_0_stream_workspace_bytes) is caller-owned, zero-filled before
- * its first use and left ready for the next call; calls that run concurrently need separate
- * workspaces. It may be NULL at batch 1-2. One CTA per SM; its waits for the bulk copies are
+ * tensor-core form (A = (q - 8) d rounded once to f16, f16 x, f32 products and sums), split
+ * over K in windows of 1024 columns so that every weight byte is streamed once; each window's
+ * f32 partial sums go to d_workspace and a second kernel adds them in window order
+ * (deterministic) and applies the epilogue. d_workspace (device, 256-byte aligned, at least
+ * ql_gemv_q4_0_stream_workspace_bytes) is caller-owned scratch; calls that run concurrently
+ * need separate workspaces. It may be NULL at batch 1-2. One CTA per SM; its waits for the bulk copies are
  * bounded (2 s, then the device error record says so). QL_EINVAL for other batches.       */
 int ql_gemv_q4_0_stream(const void* d_stream, int64_t rows, int64_t cols, const void* d_x,
                         int64_t batch, void* d_y, int epilogue, void* d_workspace,
@@ -267,12 +267,13 @@ enum { QL_STEP_AUTO = 0, QL_STEP_LAUNCHES = 1, QL_STEP_PERSISTENT = 2 };
  *                              steps of the phase that ends at barrier k (GEMV: activations
  *                              staged, warp 0's units done, all warps done, epilogues done;
  *                              attention: q ready, blocks merged, split ticket taken, end).
- *                              A step of separate launches at batch 1-2 stamps its GEMV
- *                              launches instead: launch k (qkv, o, gate_up, down of each layer,
- *                              then lm_head) fills row k, per CTA: 0 start, 1 predecessor
- *                              done, 2 activations staged, 3 warp 0's units done, 4 all warps
- *                              done, 5 epilogues done (6, 7: warp 0's cycles waiting for bulk
- *                              copies / in its unit loop). A profiling aid
+ *                              A step of separate launches stamps its GEMV launches
+ *                              instead: launch k (qkv, o, gate_up, down of each layer, then
+ *                              lm_head) fills row k, per CTA (at most num_SMs CTAs): 0 start,
+ *                              1 predecessor done, 2 activations staged, 3 units done (batch
+ *                              1-2: warp 0's), 4 all warps done / partial sums written, 5 end
+ *                              (6, 7 at batch 1-2: warp 0's cycles waiting for bulk copies /
+ *                              in its unit loop; else 0). A profiling aid
  * Applies to steps issued (or graphs captured) afterwards. QL_EINVAL for anything else.  */
 enum { QL_OPT_STEP_KERNEL = 1, QL_OPT_BARRIER_TIMEOUT_NS = 2, QL_OPT_TEST_BARRIER_EXTRA = 3,
        QL_OPT_STEP_TRACE = 4 };

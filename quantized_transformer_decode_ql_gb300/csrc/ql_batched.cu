@@ -15,10 +15,10 @@
 // the GEMV is split over K: a CTA takes one K window of 1024 columns and one group of rows,
 // stages that window of every batch column once, and streams the window's units of its tiles
 // (at 1-3 tiles per CTA a row split alone would leave a window less than one unit per warp).
-// The CTA writes f32 partial sums; the CTA that takes the last ticket of a row group (no
-// waiting) adds the windows' partials in window order (deterministic) and applies the
-// epilogue. The weights arrive through the same per-warp ring of bulk copies (TMA) as the
-// batch-1 kernel.
+// The CTA writes f32 partial sums; a second kernel, over every SM, adds each output's windows
+// in window order (deterministic) and applies the epilogue (a merge left to one CTA per row
+// group made that CTA the launch's long tail). The weights arrive through the same per-warp
+// ring of bulk copies (TMA) as the batch-1 kernel.
 #include "ql_persist.cuh"
 
 #include <cstdlib>
@@ -62,8 +62,9 @@ struct BParams {
     DevError* err;
     unsigned long long timeout_ns;
     float* part;           // [nwin][ntile * 16][kMaxCols] f32 partial sums of the K windows
-    int* tickets;          // [ngr] (at the start of the workspace), zero between calls
     int ngr;               // row groups (grid = nwin * ngr)
+    unsigned long long* trace;   // optional [grid][8] globaltimer stamps: 0 start, 1 past the wait,
+                                 // 2 staged, 3 units done, 4 partials written, 5 end
 };
 
 // This CTA's K window and row group: CTA c = (window c % nwin, row group c / nwin).
@@ -142,6 +143,10 @@ __device__ void stage_window(const BParams& p, const Geo& G, int w, const float*
     const int nb = G.kwu * kUnitBlocks;        // blocks in the window
     const int cols = p.M.nblk * 32;
     const int j0 = w * nb;
+    // the columns of the last 8-column tile past the batch are zero (read, never stored)
+    const int pad = ((p.B + 7) & ~7) - p.B;
+    for (int i = tid; i < pad * nb * 4; i += kT)
+        xs[(size_t)(p.B + i / (nb * 4)) * kXStride + i % (nb * 4)] = make_uint4(0u, 0u, 0u, 0u);
     const int nitems = p.B * nb * 4;
     constexpr int kChunk = 4;   // items per thread whose loads are in flight together
     for (int base = 0; base < nitems; base += kChunk * kT) {   // warp-uniform bounds (shuffles)
@@ -222,31 +227,38 @@ __device__ __forceinline__ void write_partial(const BParams& p, const Geo& G, in
     }
 }
 
-// The row group's result: sum of the windows' partials in window order, then the epilogue.
-// An item is one output row and 8 columns (one 32-byte sector of a partial row per window);
+// The result: every output's window partials summed in window order, then the epilogue. An
+// item is one output row and 8 columns (one 32-byte sector of a partial row per window);
 // consecutive threads take consecutive rows, so the stores to y [column][row] coalesce. The
-// loads of up to kMergeWin windows are in flight together.
-constexpr int kMergeWin = 4;
-__device__ void merge_group(const BParams& p, const Geo& G, unsigned long long* kred) {
+// loads of up to kMergeWin windows are in flight together. Grid-stride over the whole matrix.
+constexpr int kMergeWin = 4, kMergeT = 256;
+__global__ void __launch_bounds__(kMergeT) merge_kernel(const __grid_constant__ BParams p) {
+    __shared__ unsigned long long kred[kMaxCols];
+    if (threadIdx.x < kMaxCols) kred[threadIdx.x] = 0ull;
+    pdl_wait();
+    pdl_trigger();
+    __syncthreads();
+    const int nst = p.M.nblk / kUnitBlocks, kwu = nst < kWinUnits ? nst : kWinUnits, nwin = nst / kwu;
     const bool silu = p.epi == QL_EPI_SILU_MUL;
     const int rpt = silu ? 8 : 16;                         // output rows per tile
-    const int nrows = (G.T1 - G.T0) * rpt, c8n = (p.B + 7) >> 3;
+    const int nrows = p.M.ntile * rpt, c8n = (p.B + 7) >> 3;
     const int lim = silu ? (p.M.rows >> 1) : p.M.rows;
     const size_t wstride = (size_t)p.M.ntile * 16 * (kMaxCols / 4);   // float4 per window
     const float4* part = reinterpret_cast<const float4*>(p.part);
-    for (int i = threadIdx.x; i < nrows * c8n; i += kT) {
-        const int c8 = i / nrows, lr = i - c8 * nrows;
-        const int tile = G.T0 + lr / rpt, r = lr % rpt;
+    const long long nitems = (long long)nrows * c8n;
+    for (long long i = blockIdx.x * (long long)kMergeT + threadIdx.x; i < nitems; i += (long long)gridDim.x * kMergeT) {
+        const int c8 = (int)(i / nrows), lr = (int)(i - (long long)c8 * nrows);
+        const int tile = lr / rpt, r = lr - tile * rpt;
         const int row = tile * rpt + r;
         if (row >= lim) continue;
         const float4* q = part + ((size_t)tile * 16 + r) * (kMaxCols / 4) + 2 * c8;
         float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         float su[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int w0 = 0; w0 < G.nwin; w0 += kMergeWin) {
+        for (int w0 = 0; w0 < nwin; w0 += kMergeWin) {
             float4 v[kMergeWin][2], vu[kMergeWin][2];
 #pragma unroll
             for (int k = 0; k < kMergeWin; ++k) {
-                if (w0 + k < G.nwin) {
+                if (w0 + k < nwin) {
                     const float4* qw = q + (size_t)(w0 + k) * wstride;
                     v[k][0] = __ldcg(qw);
                     v[k][1] = __ldcg(qw + 1);
@@ -258,7 +270,7 @@ __device__ void merge_group(const BParams& p, const Geo& G, unsigned long long* 
             }
 #pragma unroll
             for (int k = 0; k < kMergeWin; ++k) {
-                if (w0 + k < G.nwin) {
+                if (w0 + k < nwin) {
                     s[0] += v[k][0].x; s[1] += v[k][0].y; s[2] += v[k][0].z; s[3] += v[k][0].w;
                     s[4] += v[k][1].x; s[5] += v[k][1].y; s[6] += v[k][1].z; s[7] += v[k][1].w;
                     if (silu) {
@@ -285,21 +297,28 @@ __device__ void merge_group(const BParams& p, const Geo& G, unsigned long long* 
             }
         }
     }
+    if (p.epi == kEpiArgmax) {
+        __syncthreads();
+        if (threadIdx.x < p.B) {
+            const bool act = p.active == nullptr || p.active[threadIdx.x] != 0;
+            if (kred[threadIdx.x] && act) atomicMax(p.keys + threadIdx.x, kred[threadIdx.x]);
+        }
+    }
 }
 
 template <int NT>
 __global__ void __launch_bounds__(kT, 1) gemv_batched_kernel(const __grid_constant__ BParams p) {
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ __align__(8) unsigned long long mbar[kW * kStages];
-    __shared__ unsigned long long kred[kMaxCols];
     __shared__ float rs[kMaxCols];
-    __shared__ int last;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t = lane & 3;
     uint4* xs = reinterpret_cast<uint4*>(smem + kRing);
     float4* part = reinterpret_cast<float4*>(smem + kRing);   // after the units: the shared tiles
     const PMat& M = p.M;
     const Geo G = geometry(p);
+    unsigned long long* tr = p.trace ? p.trace + (size_t)blockIdx.x * persist::kTraceWords : nullptr;
+    persist::stamp(tr, 0);
     const int U = (G.T1 - G.T0) * G.kwu;
     const int a = persist::warp_unit<kW>(U, warp), b = persist::warp_unit<kW>(U, warp + 1);
 
@@ -307,7 +326,6 @@ __global__ void __launch_bounds__(kT, 1) gemv_batched_kernel(const __grid_consta
         for (int i = 0; i < kStages; ++i)
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(
                              static_cast<uint32_t>(__cvta_generic_to_shared(&mbar[warp * kStages + i]))) : "memory");
-    if (tid < kMaxCols) kred[tid] = 0ull;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     __syncthreads();
     BRing r;
@@ -321,12 +339,15 @@ __global__ void __launch_bounds__(kT, 1) gemv_batched_kernel(const __grid_consta
     for (int i = 0; i < kStages; ++i) bring_issue(r, M, G, lane);
     pdl_wait();
     pdl_trigger();
+    persist::stamp(tr, 1);
     if (p.rms) load_column_rms(p, rs);
     stage_window(p, G, G.w, rs, xs);
     __syncthreads();
+    persist::stamp(tr, 2);
 
     const int lm = lane >> 3, lrow = lane & 7;
     const uint32_t a_lo = (uint32_t)(((lm >> 1) * 16 + (lm & 1) * 8 + lrow) * 16);
+    const uint4* xcol = xs + (size_t)g * kXStride + t;   // this lane's B fragments: column 8 nt + g
     const unsigned char* ring_g = smem + (size_t)warp * kStages * kSlotBytes;
     const int tl_first = a < b ? a / G.kwu : 0;
     float acc[NT][4];
@@ -379,8 +400,7 @@ __global__ void __launch_bounds__(kT, 1) gemv_batched_kernel(const __grid_consta
                 const uint32_t h3 = as_u32(__hmul2(__hsub2(as_h2((sb8 & 0x00F000F0u) | 0x64006400u), off_hi), db));
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    const int col = nt * 8 + g;
-                    const uint4 X = col < p.B ? xs[(size_t)col * kXStride + 4 * j + t] : make_uint4(0u, 0u, 0u, 0u);
+                    const uint4 X = xcol[(size_t)nt * 8 * kXStride + 4 * j];
                     persist::mma16816(acc[nt], l0, l1, l2, l3, X.x, X.y);
                     persist::mma16816(acc[nt], h0, h1, h2, h3, X.z, X.w);
                 }
@@ -412,6 +432,7 @@ __global__ void __launch_bounds__(kT, 1) gemv_batched_kernel(const __grid_consta
                 for (int i = 0; i < 4; ++i) acc[nt][i] = 0.f;
         }
     }
+    persist::stamp(tr, 3);
     __syncthreads();   // xs is no longer read: part aliases it
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -447,27 +468,10 @@ __global__ void __launch_bounds__(kT, 1) gemv_batched_kernel(const __grid_consta
             write_partial<NT>(p, G, G.T0 + tl_first, s2, lane);
         }
     }
-    // the last CTA of the row group (acq_rel ticket: this CTA's partials published, everyone
-    // else's visible) adds the windows and applies the epilogue
-    __threadfence();
     __syncthreads();
-    if (tid == 0) {
-        unsigned int old;
-        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(p.tickets + G.rg) : "memory");
-        last = (int)old == G.nwin - 1;
-    }
-    __syncthreads();
-    if (last) {
-        merge_group(p, G, kred);
-        if (tid == 0) p.tickets[G.rg] = 0;   // re-arm for the next call
-        if (p.epi == kEpiArgmax) {
-            __syncthreads();
-            if (tid < p.B) {
-                const bool act = p.active == nullptr || p.active[tid] != 0;
-                if (kred[tid] && act) atomicMax(p.keys + tid, kred[tid]);
-            }
-        }
-    }
+    persist::stamp(tr, 4);
+    persist::stamp(tr, 5);
+    if (tr != nullptr && tid == 0) tr[6] = tr[7] = 0ull;
     // after a wait ran out: let the copies in flight land (bounded) before leaving
     const unsigned long long t0 = persist::global_ns();
     while (r.consumed < r.issued) {
@@ -538,16 +542,12 @@ static void batched_split(int nblk, int ntile, int sms, int& nwin, int& ngr) {
     if (ngr < 1) ngr = 1;
 }
 
-// Workspace: the tickets first, at a place that does not depend on the matrix (so that
-// matrices of any shape can share one workspace), then the partial sums.
-static size_t ticket_bytes(int sms) { return ((size_t)sms * sizeof(int) + 255) & ~(size_t)255; }
-
+// Workspace: the windows' partial sums.
 size_t batched_gemv_workspace_bytes(int rows, int nblk, int silu) {
     const int ntile = silu ? (rows / 2 + 7) / 8 : (rows + 15) / 16;
-    const int sms = num_sms();
     int nwin, ngr;
-    batched_split(nblk, ntile, sms, nwin, ngr);
-    return ticket_bytes(sms) + (size_t)nwin * ntile * 16 * batched::kMaxCols * sizeof(float);
+    batched_split(nblk, ntile, num_sms(), nwin, ngr);
+    return (size_t)nwin * ntile * 16 * batched::kMaxCols * sizeof(float);
 }
 
 int batched_gemv_prepare() {
@@ -597,9 +597,9 @@ int batched_gemv_launch(const StreamGemvArgs& a, cudaStream_t s, bool pdl) {
     p.sync = a.sync;
     p.err = err;
     p.timeout_ns = 2000000000ull;
-    p.tickets = static_cast<int*>(a.workspace);
-    p.part = reinterpret_cast<float*>(static_cast<char*>(a.workspace) + ticket_bytes(num_sms()));
+    p.part = static_cast<float*>(a.workspace);
     p.ngr = ngr;
+    p.trace = a.trace;
     if (a.rms) {   // the RMSNorm statistics of every column, once, for all CTAs
         const cudaError_t e0 = ql::launch(batched::rms_stats_kernel, dim3(a.batch), dim3(256), 0, s, pdl, a.xf,
                                           a.M.nblk * 32, a.eps, a.rs);
@@ -612,6 +612,9 @@ int batched_gemv_launch(const StreamGemvArgs& a, cudaStream_t s, bool pdl) {
                     : nt == 3 ? batched::run<3>(true, &p, grid, s, pdl)
                               : batched::run<4>(true, &p, grid, s, pdl);
     if (e != cudaSuccess) return cuda_error(e, "batched gemv launch");
+    // the windows added up and the epilogue, over every SM
+    e = ql::launch(batched::merge_kernel, dim3(2 * num_sms()), dim3(batched::kMergeT), 0, s, pdl, p);
+    if (e != cudaSuccess) return cuda_error(e, "batched gemv merge launch");
     return QL_OK;
 }
 

@@ -283,8 +283,8 @@ struct StreamGemvArgs {
     const int32_t* active;
     unsigned int* sync;   // [4] zero: the abort flag of the kernel's bounded waits
     float* rs;            // batch 3-32 with rms: [batch] scratch for the columns' RMS statistics
-    void* workspace;      // batch 3-32: partial sums + tickets (batched_gemv_workspace_bytes),
-    size_t workspace_bytes;   // tickets zero before the first call (each call re-arms them)
+    void* workspace;      // batch 3-32: the K windows' partial sums (batched_gemv_workspace_bytes)
+    size_t workspace_bytes;
     unsigned long long* trace;   // batch 1-2, optional: [grid][8] globaltimer stamps per CTA
     NextWeights next;     // batch 1-2: constants of a later kernel, prefetched into L2
 };

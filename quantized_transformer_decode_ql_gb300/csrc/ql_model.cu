@@ -62,7 +62,7 @@ struct ql_model {
     std::vector<ql::PMat> hmats;            // host copies: 4 per layer, then lm_head
     unsigned int* ssync = nullptr;          // abort flag of the stand-alone stream GEMVs
     float* rs = nullptr;                    // [max_batch] RMS statistics of the batched GEMV
-    void* bws = nullptr;                    // batched GEMV partial sums + tickets
+    void* bws = nullptr;                    // batched GEMV partial sums
     size_t bws_bytes = 0;
     bool batched_ok = false;                // every matrix width suits the batched stream GEMV
     ql::PMat plm = {};
@@ -222,7 +222,7 @@ int run_step(ql_model* m, const ql_step_args* a, cudaStream_t s) {
                   int ld, NextWeights next) {
         StreamGemvArgs ga = {};
         ga.next = next;
-        if (m->trace && B <= kPersistMaxBatch) ga.trace = m->trace + (size_t)gemv_k * num_sms() * persist_trace_words();
+        if (m->trace) ga.trace = m->trace + (size_t)gemv_k * num_sms() * persist_trace_words();
         ++gemv_k;
         ga.M = M;
         ga.batch = B;
@@ -501,7 +501,6 @@ int setup_persist(ql_model* m) {
         }
         A(&m->bws, m->bws_bytes);
         if (rc != QL_OK) return rc;
-        if (cudaMemset(m->bws, 0, m->bws_bytes) != cudaSuccess) return set_error(QL_ECUDA, "ql_model_create: workspace init");
     }
     cudaError_t e = cudaMemcpy(m->players, hl.data(), hl.size() * sizeof(PLayer), cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemset(m->ptickets, 0, (size_t)maxb * d.n_kv_heads * 4);

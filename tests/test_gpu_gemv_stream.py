@@ -91,13 +91,14 @@ def run(w, x, epilogue, residual=None):
     else:
         y = torch.full((B, rows), float("nan"), dtype=torch.float32, device="cuda")
     ws = None
-    if B > 2:
-        ws = torch.zeros(ql.ql_gemv_q4_0_stream_workspace_bytes(rows, cols, silu), dtype=torch.uint8, device="cuda")
+    if B > 2:   # scratch: its contents do not matter
+        ws = torch.full((ql.ql_gemv_q4_0_stream_workspace_bytes(rows, cols, silu),), 0x7F, dtype=torch.uint8,
+                        device="cuda")
     y0 = y.clone()
     ql.ql_gemv_q4_0_stream(buf, rows, cols, dev(x), B, y, epilogue, ws)
     torch.cuda.synchronize()
     if ws is not None:
-        # the workspace is left ready (tickets re-armed): a second call gives the same bits
+        # a second call on the same workspace gives the same bits (a fixed summation order)
         y2 = y0.clone()
         ql.ql_gemv_q4_0_stream(buf, rows, cols, dev(x), B, y2, epilogue, ws)
         torch.cuda.synchronize()
