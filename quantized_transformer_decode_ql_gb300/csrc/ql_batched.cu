@@ -48,12 +48,8 @@ constexpr size_t kSmem = kRing + kXPart;
 
 struct BParams {
     PMat M;
-    int B, epi, rms;
-    const float* xf;       // rms: f32 [B][cols]
-    const __half* x16;     // else f16 [B][cols]
-    const float* norm_w;
-    const float* rs_in;    // rms: [B] 1 / rms of each column (rms_stats_kernel)
-    float eps;
+    int B, epi;
+    const __half* x16;     // f16 [B][cols] (RMSNorm'd inputs: written by rms_norm_kernel)
     void* y;
     int ld;
     unsigned long long* keys;
@@ -129,16 +125,9 @@ __device__ __forceinline__ void bring_wait(BRing& r, const BParams& p, unsigned 
     r.dead = 1;
 }
 
-// 1 / rms of every column (the RMSNorm statistics over the full K), computed once by
-// rms_stats_kernel for all CTAs.
-__device__ void load_column_rms(const BParams& p, float* rs) {
-    if ((int)threadIdx.x < p.B) rs[threadIdx.x] = __ldcg(p.rs_in + threadIdx.x);
-    __syncthreads();
-}
-
 // Stage window w of every column: f16 pairs in the order a code word expands to (high ones
 // pre-divided by 16, which is exact). Columns past the batch are never read.
-__device__ void stage_window(const BParams& p, const Geo& G, int w, const float* rs, uint4* xs) {
+__device__ void stage_window(const BParams& p, const Geo& G, int w, uint4* xs) {
     const int tid = threadIdx.x;
     const int nb = G.kwu * kUnitBlocks;        // blocks in the window
     const int cols = p.M.nblk * 32;
@@ -149,8 +138,7 @@ __device__ void stage_window(const BParams& p, const Geo& G, int w, const float*
         xs[(size_t)(p.B + i / (nb * 4)) * kXStride + i % (nb * 4)] = make_uint4(0u, 0u, 0u, 0u);
     const int nitems = p.B * nb * 4;
     constexpr int kChunk = 4;   // items per thread whose loads are in flight together
-    for (int base = 0; base < nitems; base += kChunk * kT) {   // warp-uniform bounds (shuffles)
-        float4 la[kChunk], lh[kChunk];
+    for (int base = 0; base < nitems; base += kChunk * kT) {
         uint2 ha[kChunk], hh[kChunk];
 #pragma unroll
         for (int r = 0; r < kChunk; ++r) {
@@ -158,44 +146,23 @@ __device__ void stage_window(const BParams& p, const Geo& G, int w, const float*
             if (item < nitems) {
                 const int t = item & 3, cj = item >> 2, c = cj / nb, j = cj - c * nb;
                 const size_t off = (size_t)c * cols + 32 * (j0 + j) + 4 * t;
-                if (p.rms) {
-                    la[r] = __ldcg(reinterpret_cast<const float4*>(p.xf + off));
-                    lh[r] = __ldcg(reinterpret_cast<const float4*>(p.xf + off + 16));
-                } else {
-                    ha[r] = __ldcg(reinterpret_cast<const uint2*>(p.x16 + off));
-                    hh[r] = __ldcg(reinterpret_cast<const uint2*>(p.x16 + off + 16));
-                }
+                ha[r] = __ldcg(reinterpret_cast<const uint2*>(p.x16 + off));
+                hh[r] = __ldcg(reinterpret_cast<const uint2*>(p.x16 + off + 16));
             }
         }
 #pragma unroll
         for (int r = 0; r < kChunk; ++r) {
-            if (base + r * kT >= nitems) break;   // warp-uniform
             const int item = base + r * kT + tid;
-            const bool live = item < nitems;
+            if (item >= nitems) break;
             const int t = item & 3, cj = item >> 2, c = cj / nb, j = cj - c * nb;
-            float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            if (live) {
-                if (p.rms) {
-                    const float4 wa = __ldg(reinterpret_cast<const float4*>(p.norm_w + 32 * (j0 + j) + 4 * t));
-                    const float4 wh = __ldg(reinterpret_cast<const float4*>(p.norm_w + 32 * (j0 + j) + 16 + 4 * t));
-                    const float rr = rs[c];
-                    const float4 a = la[r], h = lh[r];
-                    v[0] = a.x * rr * wa.x; v[1] = a.y * rr * wa.y; v[2] = a.z * rr * wa.z; v[3] = a.w * rr * wa.w;
-                    v[4] = h.x * rr * wh.x; v[5] = h.y * rr * wh.y; v[6] = h.z * rr * wh.z; v[7] = h.w * rr * wh.w;
-                } else {
-                    const float2 f0 = __half22float2(as_h2(ha[r].x)), f1 = __half22float2(as_h2(ha[r].y));
-                    const float2 f2 = __half22float2(as_h2(hh[r].x)), f3 = __half22float2(as_h2(hh[r].y));
-                    v[0] = f0.x; v[1] = f0.y; v[2] = f1.x; v[3] = f1.y;
-                    v[4] = f2.x; v[5] = f2.y; v[6] = f3.x; v[7] = f3.y;
-                }
-            }
-            const __half2 p0 = __floats2half2_rn(v[0], v[2]);
-            const __half2 p1 = __floats2half2_rn(v[1], v[3]);
-            const __half2 p2 = __floats2half2_rn(__half2float(__float2half_rn(v[4])) * 0.0625f,
-                                                 __half2float(__float2half_rn(v[6])) * 0.0625f);
-            const __half2 p3 = __floats2half2_rn(__half2float(__float2half_rn(v[5])) * 0.0625f,
-                                                 __half2float(__float2half_rn(v[7])) * 0.0625f);
-            if (live) xs[(size_t)c * kXStride + 4 * j + t] = make_uint4(as_u32(p0), as_u32(p1), as_u32(p2), as_u32(p3));
+            // elements 4t..4t+3 (ha) and 16+4t.. (hh): pairs (x0, x2), (x1, x3), (x16, x18)/16, (x17, x19)/16
+            const float2 f0 = __half22float2(as_h2(ha[r].x)), f1 = __half22float2(as_h2(ha[r].y));
+            const float2 f2 = __half22float2(as_h2(hh[r].x)), f3 = __half22float2(as_h2(hh[r].y));
+            const __half2 p0 = __floats2half2_rn(f0.x, f1.x);
+            const __half2 p1 = __floats2half2_rn(f0.y, f1.y);
+            const __half2 p2 = __floats2half2_rn(f2.x * 0.0625f, f3.x * 0.0625f);
+            const __half2 p3 = __floats2half2_rn(f2.y * 0.0625f, f3.y * 0.0625f);
+            xs[(size_t)c * kXStride + 4 * j + t] = make_uint4(as_u32(p0), as_u32(p1), as_u32(p2), as_u32(p3));
         }
     }
 }
@@ -310,7 +277,6 @@ template <int NT>
 __global__ void __launch_bounds__(kT, 1) gemv_batched_kernel(const __grid_constant__ BParams p) {
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ __align__(8) unsigned long long mbar[kW * kStages];
-    __shared__ float rs[kMaxCols];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t = lane & 3;
     uint4* xs = reinterpret_cast<uint4*>(smem + kRing);
@@ -340,8 +306,7 @@ __global__ void __launch_bounds__(kT, 1) gemv_batched_kernel(const __grid_consta
     pdl_wait();
     pdl_trigger();
     persist::stamp(tr, 1);
-    if (p.rms) load_column_rms(p, rs);
-    stage_window(p, G, G.w, rs, xs);
+    stage_window(p, G, G.w, xs);
     __syncthreads();
     persist::stamp(tr, 2);
 
@@ -483,18 +448,22 @@ __global__ void __launch_bounds__(kT, 1) gemv_batched_kernel(const __grid_consta
     }
 }
 
-// rs[b] = 1 / sqrt(mean_k x[b][k]^2 + eps): one CTA per column, fixed summation order.
-__global__ void __launch_bounds__(256) rms_stats_kernel(const float* x, int cols, float eps, float* rs) {
-    __shared__ float red[8];
+// RMSNorm of every column, once for all CTAs of the GEMV: xn[b] = f16(x[b] / rms(x[b]) * w) with
+// rms = sqrt(mean_k x[b][k]^2 + eps); one CTA per column, fixed summation order.
+constexpr int kNormT = 256;
+__global__ void __launch_bounds__(kNormT) rms_norm_kernel(const float* x, int cols, float eps, const float* w,
+                                                          __half* xn) {
+    __shared__ float red[kNormT / 32];
+    __shared__ float rs;
     const int b = blockIdx.x, tid = threadIdx.x;
     pdl_wait();
     pdl_trigger();
     const float4* xb = reinterpret_cast<const float4*>(x + (size_t)b * cols);
     float ss = 0.f;
-    for (int i = tid; i < cols / 4; i += 4 * 256) {
+    for (int i = tid; i < cols / 4; i += 4 * kNormT) {
         float4 v[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) v[u] = i + u * 256 < cols / 4 ? __ldcg(xb + i + u * 256) : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int u = 0; u < 4; ++u) v[u] = i + u * kNormT < cols / 4 ? __ldcg(xb + i + u * kNormT) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int u = 0; u < 4; ++u) ss += v[u].x * v[u].x + v[u].y * v[u].y + v[u].z * v[u].z + v[u].w * v[u].w;
     }
@@ -504,8 +473,30 @@ __global__ void __launch_bounds__(256) rms_stats_kernel(const float* x, int cols
     __syncthreads();
     if (tid == 0) {
         float t = 0.f;
-        for (int w = 0; w < 8; ++w) t += red[w];
-        rs[b] = 1.0f / sqrtf(t / (float)cols + eps);
+        for (int k = 0; k < kNormT / 32; ++k) t += red[k];
+        rs = 1.0f / sqrtf(t / (float)cols + eps);
+    }
+    __syncthreads();
+    const float rr = rs;
+    const float4* wv = reinterpret_cast<const float4*>(w);
+    uint2* ob = reinterpret_cast<uint2*>(xn + (size_t)b * cols);
+    for (int i = tid; i < cols / 4; i += 4 * kNormT) {   // a chunk's loads are all issued first
+        float4 v[4], g[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (i + u * kNormT < cols / 4) {
+                v[u] = __ldcg(xb + i + u * kNormT);
+                g[u] = __ldg(wv + i + u * kNormT);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (i + u * kNormT < cols / 4) {
+                const __half2 lo = __floats2half2_rn(v[u].x * rr * g[u].x, v[u].y * rr * g[u].y);
+                const __half2 hi = __floats2half2_rn(v[u].z * rr * g[u].z, v[u].w * rr * g[u].w);
+                ob[i + u * kNormT] = make_uint2(as_u32(lo), as_u32(hi));
+            }
+        }
     }
 }
 
@@ -570,7 +561,7 @@ int batched_gemv_launch(const StreamGemvArgs& a, cudaStream_t s, bool pdl) {
     QL_REQUIRE(a.M.stream && batched_gemv_shape_ok(a.M.nblk),
                "batched gemv: cols must be 128, 256, ..., 896 or a multiple of 1024");
     QL_REQUIRE(a.batch >= 1 && a.batch <= batched::kMaxCols, "batched gemv: batch must be in [1, 32]");
-    QL_REQUIRE(a.rms ? (a.xf && a.norm_w && a.rs) : a.x16 != nullptr, "batched gemv: null input");
+    QL_REQUIRE(a.rms ? (a.xf && a.norm_w && a.xn) : a.x16 != nullptr, "batched gemv: null input");
     QL_REQUIRE(a.y && a.sync && a.workspace, "batched gemv: null output or workspace");
     QL_REQUIRE(a.workspace_bytes >= batched_gemv_workspace_bytes(a.M.rows, a.M.nblk, a.M.silu),
                "batched gemv: workspace too small");
@@ -585,11 +576,7 @@ int batched_gemv_launch(const StreamGemvArgs& a, cudaStream_t s, bool pdl) {
     p.M = a.M;
     p.B = a.batch;
     p.epi = a.epilogue;
-    p.rms = a.rms;
-    p.xf = a.xf;
-    p.x16 = a.x16;
-    p.norm_w = a.norm_w;
-    p.eps = a.eps;
+    p.x16 = a.rms ? a.xn : a.x16;
     p.y = a.y;
     p.ld = a.ld;
     p.keys = a.keys;
@@ -600,11 +587,10 @@ int batched_gemv_launch(const StreamGemvArgs& a, cudaStream_t s, bool pdl) {
     p.part = static_cast<float*>(a.workspace);
     p.ngr = ngr;
     p.trace = a.trace;
-    if (a.rms) {   // the RMSNorm statistics of every column, once, for all CTAs
-        const cudaError_t e0 = ql::launch(batched::rms_stats_kernel, dim3(a.batch), dim3(256), 0, s, pdl, a.xf,
-                                          a.M.nblk * 32, a.eps, a.rs);
-        if (e0 != cudaSuccess) return cuda_error(e0, "rms stats launch");
-        p.rs_in = a.rs;
+    if (a.rms) {   // the RMSNorm'd activations of every column, once, for all CTAs
+        const cudaError_t e0 = ql::launch(batched::rms_norm_kernel, dim3(a.batch), dim3(batched::kNormT), 0, s, pdl,
+                                          a.xf, a.M.nblk * 32, a.eps, a.norm_w, a.xn);
+        if (e0 != cudaSuccess) return cuda_error(e0, "rms norm launch");
     }
     const int nt = (a.batch + 7) / 8, grid = nwin * ngr;
     cudaError_t e = nt == 1   ? batched::run<1>(true, &p, grid, s, pdl)

@@ -282,7 +282,7 @@ struct StreamGemvArgs {
     unsigned long long* keys;
     const int32_t* active;
     unsigned int* sync;   // [4] zero: the abort flag of the kernel's bounded waits
-    float* rs;            // batch 3-32 with rms: [batch] scratch for the columns' RMS statistics
+    __half* xn;           // batch 3-32 with rms: [batch][cols] scratch for the RMSNorm'd input
     void* workspace;      // batch 3-32: the K windows' partial sums (batched_gemv_workspace_bytes)
     size_t workspace_bytes;
     unsigned long long* trace;   // batch 1-2, optional: [grid][8] globaltimer stamps per CTA

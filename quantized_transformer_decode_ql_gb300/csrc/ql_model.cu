@@ -61,7 +61,7 @@ struct ql_model {
     size_t persist_stream_bytes = 0;
     std::vector<ql::PMat> hmats;            // host copies: 4 per layer, then lm_head
     unsigned int* ssync = nullptr;          // abort flag of the stand-alone stream GEMVs
-    float* rs = nullptr;                    // [max_batch] RMS statistics of the batched GEMV
+    __half* xn = nullptr;                   // [max_batch][hidden] RMSNorm'd input of a batched GEMV
     void* bws = nullptr;                    // batched GEMV partial sums
     size_t bws_bytes = 0;
     bool batched_ok = false;                // every matrix width suits the batched stream GEMV
@@ -237,7 +237,7 @@ int run_step(ql_model* m, const ql_step_args* a, cudaStream_t s) {
         ga.keys = m->keys;
         ga.active = a->active;
         ga.sync = m->ssync;
-        ga.rs = m->rs;
+        ga.xn = m->xn;
         ga.workspace = m->bws;
         ga.workspace_bytes = m->bws_bytes;
         return B <= kPersistMaxBatch ? stream_gemv_launch(ga, s, pdl) : batched_gemv_launch(ga, s, pdl);
@@ -486,7 +486,7 @@ int setup_persist(ql_model* m) {
     A((void**)&m->ptickets, (size_t)maxb * d.n_kv_heads * 4);
     A((void**)&m->psync, 16);
     A((void**)&m->ssync, 16);
-    A((void**)&m->rs, (size_t)d.max_batch * 4);
+    A((void**)&m->xn, (size_t)d.max_batch * d.hidden * 2);
     if (rc != QL_OK) return rc;
     // the weights re-laid into the tile stream layout that the persistent kernel copies from
     if ((rc = persist_pack_streams(all.data(), (int)all.size(), m->pstreams, nullptr)) != QL_OK) return rc;
