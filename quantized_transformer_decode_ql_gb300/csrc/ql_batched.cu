@@ -198,7 +198,7 @@ __device__ __forceinline__ void write_partial(const BParams& p, const Geo& G, in
 // item is one output row and 8 columns (one 32-byte sector of a partial row per window);
 // consecutive threads take consecutive rows, so the stores to y [column][row] coalesce. The
 // loads of up to kMergeWin windows are in flight together. Grid-stride over the whole matrix.
-constexpr int kMergeWin = 4, kMergeT = 256;
+constexpr int kMergeWin = 8, kMergeT = 256;
 __global__ void __launch_bounds__(kMergeT) merge_kernel(const __grid_constant__ BParams p) {
     __shared__ unsigned long long kred[kMaxCols];
     if (threadIdx.x < kMaxCols) kred[threadIdx.x] = 0ull;
@@ -206,12 +206,13 @@ __global__ void __launch_bounds__(kMergeT) merge_kernel(const __grid_constant__ 
     pdl_trigger();
     __syncthreads();
     const int nst = p.M.nblk / kUnitBlocks, kwu = nst < kWinUnits ? nst : kWinUnits, nwin = nst / kwu;
-    const bool silu = p.epi == QL_EPI_SILU_MUL;
+    const bool silu = p.epi == QL_EPI_SILU_MUL, resid = p.epi == QL_EPI_ADD_RESIDUAL;
     const int rpt = silu ? 8 : 16;                         // output rows per tile
     const int nrows = p.M.ntile * rpt, c8n = (p.B + 7) >> 3;
     const int lim = silu ? (p.M.rows >> 1) : p.M.rows;
     const size_t wstride = (size_t)p.M.ntile * 16 * (kMaxCols / 4);   // float4 per window
     const float4* part = reinterpret_cast<const float4*>(p.part);
+    float* yf = static_cast<float*>(p.y);
     const long long nitems = (long long)nrows * c8n;
     for (long long i = blockIdx.x * (long long)kMergeT + threadIdx.x; i < nitems; i += (long long)gridDim.x * kMergeT) {
         const int c8 = (int)(i / nrows), lr = (int)(i - (long long)c8 * nrows);
@@ -221,29 +222,32 @@ __global__ void __launch_bounds__(kMergeT) merge_kernel(const __grid_constant__ 
         const float4* q = part + ((size_t)tile * 16 + r) * (kMaxCols / 4) + 2 * c8;
         float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         float su[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int w0 = 0; w0 < nwin; w0 += kMergeWin) {
-            float4 v[kMergeWin][2], vu[kMergeWin][2];
+        float res[8];   // the residual, loaded with the first windows
+        if (resid) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) res[k] = 8 * c8 + k < p.B ? __ldcg(yf + (size_t)(8 * c8 + k) * p.ld + row) : 0.f;
+        }
+        // SiLU*up reads two rows per window: half as many windows per round
+        const int wpr = silu ? kMergeWin / 2 : kMergeWin;
+        for (int w0 = 0; w0 < nwin; w0 += wpr) {
+            float4 v[kMergeWin][2];
 #pragma unroll
             for (int k = 0; k < kMergeWin; ++k) {
-                if (w0 + k < nwin) {
-                    const float4* qw = q + (size_t)(w0 + k) * wstride;
+                const int wk = silu ? w0 + (k >> 1) : w0 + k;
+                if ((silu ? (k >> 1) : k) < wpr && wk < nwin) {
+                    // SiLU*up: odd k is the up row (8 rows further in the tile)
+                    const float4* qw = q + (size_t)wk * wstride + (silu && (k & 1) ? 8 * (kMaxCols / 4) : 0);
                     v[k][0] = __ldcg(qw);
                     v[k][1] = __ldcg(qw + 1);
-                    if (silu) {   // the up row: 8 rows further in the tile
-                        vu[k][0] = __ldcg(qw + 8 * (kMaxCols / 4));
-                        vu[k][1] = __ldcg(qw + 8 * (kMaxCols / 4) + 1);
-                    }
                 }
             }
 #pragma unroll
             for (int k = 0; k < kMergeWin; ++k) {
-                if (w0 + k < nwin) {
-                    s[0] += v[k][0].x; s[1] += v[k][0].y; s[2] += v[k][0].z; s[3] += v[k][0].w;
-                    s[4] += v[k][1].x; s[5] += v[k][1].y; s[6] += v[k][1].z; s[7] += v[k][1].w;
-                    if (silu) {
-                        su[0] += vu[k][0].x; su[1] += vu[k][0].y; su[2] += vu[k][0].z; su[3] += vu[k][0].w;
-                        su[4] += vu[k][1].x; su[5] += vu[k][1].y; su[6] += vu[k][1].z; su[7] += vu[k][1].w;
-                    }
+                const int wk = silu ? w0 + (k >> 1) : w0 + k;
+                if ((silu ? (k >> 1) : k) < wpr && wk < nwin) {
+                    float* t = silu && (k & 1) ? su : s;
+                    t[0] += v[k][0].x; t[1] += v[k][0].y; t[2] += v[k][0].z; t[3] += v[k][0].w;
+                    t[4] += v[k][1].x; t[5] += v[k][1].y; t[6] += v[k][1].z; t[7] += v[k][1].w;
                 }
             }
         }
@@ -253,14 +257,11 @@ __global__ void __launch_bounds__(kMergeT) merge_kernel(const __grid_constant__ 
             if (c >= p.B) break;
             if (silu) {
                 static_cast<__half*>(p.y)[(size_t)c * p.ld + row] = __float2half_rn(persist::silu(s[k]) * su[k]);
+            } else if (resid) {
+                yf[(size_t)c * p.ld + row] = res[k] + s[k];
             } else {
-                float* dst = static_cast<float*>(p.y) + (size_t)c * p.ld + row;
-                if (p.epi == QL_EPI_ADD_RESIDUAL) {
-                    *dst = __ldcg(dst) + s[k];
-                } else {
-                    *dst = s[k];
-                    if (p.epi == kEpiArgmax) atomicMax(kred + c, persist::argmax_key(s[k], row));
-                }
+                yf[(size_t)c * p.ld + row] = s[k];
+                if (p.epi == kEpiArgmax) atomicMax(kred + c, persist::argmax_key(s[k], row));
             }
         }
     }
