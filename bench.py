@@ -343,6 +343,7 @@ def gpu_arm(args, rank, world, local_rank):
                             "bytes_per_launch": at_bytes, "context": L},
     }
     gu_gbs = per_kernel["gemv_gate_up"]["achieved_gbs"]
+    gu_traffic = GU_TRAFFIC_B1 if (streamed and B == 1 and cfg.hidden == 4096 and cfg.intermediate == 12288) else None
     step_gbs = step_bytes * steps / (ms_max / 1e3) / 1e9
     kernels_per_step = 1 if persistent else 3 + 5 * cfg.n_layers   # embed, 5 per layer, lm_head, finalize
     line = {
@@ -357,7 +358,8 @@ def gpu_arm(args, rank, world, local_rank):
                    "l2": "inputs larger than L2 (%.2f GB of q4_0 weights streamed per step)" % (wbytes / 1e9)},
         "roofline": {"bound": "hbm", "kernel": gu_kernel,
                      "achieved": round(gu_gbs, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(gu_gbs / peak, 4), "traffic": None, "peak_source": peak_src},
+                     "frac": round(gu_gbs / peak, 4), "traffic": gu_traffic, "peak_source": peak_src,
+                     **({"traffic_source": GU_TRAFFIC_SOURCE} if gu_traffic else {})},
         "step_roofline": {"bytes_per_step": int(step_bytes), "achieved_gbs": round(step_gbs, 1),
                           "frac": round(step_gbs / peak, 4),
                           "roofline_tokens_s": round(B * peak * 1e9 / step_bytes, 1)},
@@ -399,6 +401,14 @@ def launches_per_step(cfg, B):
     per_layer = (gemv_passes(cfg.hidden, B) * 2 + gemv_passes(cfg.n_heads * cfg.head_dim, B)
                  + gemv_passes(cfg.intermediate, B) + 1)
     return 2 + per_layer * cfg.n_layers + gemv_passes(cfg.hidden, B)
+
+
+# DRAM bytes (read + write) of one launch of the batch-1 tile stream GEMV at the gate|up shape
+# (24576 x 4096), from one ncu capture of that kernel (plain epilogue; the SiLU*up launch that
+# the roofline times writes 72 KB less); reported only for that kernel and batch.
+GU_TRAFFIC_B1 = 57007616 + 136704
+GU_TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum, profiles/"
+                     "gemv_stream_q4_0_24576x4096_b1_ncu.md (same kernel, plain epilogue)")
 
 
 def launch_phases(gm, sargs, s, cfg):
@@ -728,6 +738,60 @@ def micro_gemv(shapes, batches, iters):
     return out
 
 
+def micro_gemv_stream(shapes, batches, iters):
+    """q4_0 GEMV over the tile stream layout alone (batch 1-2: the CUDA-core stream kernel,
+    3-32: the split-K tensor-core kernel plus its merge), plain epilogue; rotates weight copies
+    totalling > 3x L2."""
+    import torch
+    from quantized_transformer_decode_ql_gb300 import build as qbuild
+    qbuild.build()
+    import quantized_transformer_decode_ql_gb300 as ql
+    from quantized_transformer_decode_ql_gb300.model import Q4Tensor
+    peak, src = load_peaks()
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    s = torch.cuda.Stream()
+    g = torch.Generator(device="cuda")
+    g.manual_seed(2)
+    out = []
+    for rows, cols in shapes:
+        one = rows * cols * 18 // 32
+        copies = max(1, min(64, -(-3 * l2 // one)))
+        Ws = []
+        for c in range(copies):
+            w = torch.randn((rows, cols), generator=g, device="cuda").mul_(0.02)
+            W = Q4Tensor.pack(w)
+            del w
+            buf = torch.empty(ql.ql_q4_0_stream_bytes(rows, cols, 0), dtype=torch.uint8, device="cuda")
+            ql.ql_q4_0_stream_pack(W.scales, W.quants, rows, cols, 0, buf)
+            del W
+            Ws.append(buf)
+        torch.cuda.synchronize()
+        for B in batches:
+            x = torch.randn((B, cols), generator=g, device="cuda").half()
+            y = torch.empty((B, rows), dtype=torch.float32, device="cuda")
+            ws = None
+            if B > 2:
+                ws = torch.empty(ql.ql_gemv_q4_0_stream_workspace_bytes(rows, cols, 0), dtype=torch.uint8,
+                                 device="cuda")
+
+            def run(n):
+                for i in range(n):
+                    ql.ql_gemv_q4_0_stream(Ws[i % copies], rows, cols, x, B, y, ql.QL_EPI_NONE, ws, s)
+            n = max(iters, copies)
+            with torch.cuda.stream(s):
+                run(1)                  # first call outside capture (per-device set-up)
+            s.synchronize()
+            us = graph_ms(lambda: run(n), s, 3) * 1e3 / n
+            nbytes = one + B * cols * 2 + B * rows * 4
+            gbs = nbytes / (us * 1e-6) / 1e9
+            out.append({"kernel": "ql_gemv_q4_0_stream", "rows": rows, "cols": cols, "batch": B,
+                        "us": round(us, 2), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
+                        "peak": peak, "peak_source": src, "copies": copies})
+            print(json.dumps(out[-1]), flush=True)
+        del Ws
+    return out
+
+
 def micro_attn(batches, iters, ctx=0):
     """Paged GQA decode attention alone: 32/8 heads, hd 128, lengths uniform in [512, 32768]
     (ctx > 0: every sequence ctx tokens long)."""
@@ -796,7 +860,7 @@ def main():
                     help="profiling aid: run the 8B-shaped step with this many layers (default: all 36)")
     ap.add_argument("--step-kernel", default="auto", choices=["auto", "persistent", "launches"],
                     help="decode step implementation (auto: persistent when the batch allows it)")
-    ap.add_argument("--micro", choices=["gemv", "attn"], help="time one kernel family alone")
+    ap.add_argument("--micro", choices=["gemv", "gemv_stream", "attn"], help="time one kernel family alone")
     ap.add_argument("--shape", default=None, help="micro gemv: ROWSxCOLS (default: all shapes)")
     ap.add_argument("--batch", default=None, help="micro: comma-separated batch sizes")
     ap.add_argument("--iters", type=int, default=50)
@@ -806,6 +870,11 @@ def main():
         shapes = [tuple(int(v) for v in args.shape.split("x"))] if args.shape else ql_inputs.GEMV_SHAPES
         batches = [int(b) for b in args.batch.split(",")] if args.batch else [1, 4, 16, 64]
         micro_gemv(shapes, batches, args.iters)
+        return
+    if args.micro == "gemv_stream":
+        shapes = [tuple(int(v) for v in args.shape.split("x"))] if args.shape else ql_inputs.GEMV_SHAPES
+        batches = [int(b) for b in args.batch.split(",")] if args.batch else [1, 2, 8, 32]
+        micro_gemv_stream(shapes, batches, args.iters)
         return
     if args.micro == "attn":
         batches = [int(b) for b in args.batch.split(",")] if args.batch else [1, 2, 4, 8, 16, 32, 64]
