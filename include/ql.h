@@ -132,6 +132,17 @@ int ql_gemv_q4_0_stream(const void* d_stream, int64_t rows, int64_t cols, const 
 /* Workspace bytes ql_gemv_q4_0_stream needs at batch 3-32 for this shape on the current
  * device (the split depends on its SM count); 0 on a bad shape.                           */
 int64_t ql_gemv_q4_0_stream_workspace_bytes(int64_t rows, int64_t cols, int silu);
+/* Tensor-core form of the batch 3-32 GEMV, for this process (ql_gemv_q4_0_stream and the
+ * decode step; graphs keep the form they were captured with):
+ *   QL_BATCHED_MMA_SYNC  (default) warps issue mma.sync m16n8k16 on the dequantised weights;
+ *   QL_BATCHED_TCGEN05   16 warps write (q - 8) d into tensor memory (tcgen05.st) and one warp
+ *                        issues tcgen05.mma (kind::f16, M 128, N 32, K 16) against the staged
+ *                        activations; same partial sums, same merge. Parity-tested; slower on
+ *                        the decode step so far (its expansion and copy pipeline is latency-bound).
+ * The initial form is QL_BATCHED_TCGEN05 when the environment sets QL_BATCHED_TC=1. Returns
+ * the previous form, or QL_EINVAL for an unknown one.                                     */
+enum { QL_BATCHED_MMA_SYNC = 0, QL_BATCHED_TCGEN05 = 1 };
+int ql_set_batched_gemv_form(int form);
 
 /* --------------------------------------------------------------- paged decode attention
  * [FK] launch_paged_decode_attention / attention_paged, split-K over the context:

@@ -13,14 +13,14 @@ from ._lib import (QLError, QL_OK, QL_EINVAL, QL_ENOMEM, QL_ECUDA, QL_EPOOL, QL_
                    QL_EDEVICE, QL_ESTATE, QL_DTYPE_F32, QL_DTYPE_F16, QL_EPI_NONE,
                    QL_EPI_ADD_RESIDUAL, QL_EPI_SILU_MUL, QL_STEP_AUTO, QL_STEP_LAUNCHES,
                    QL_STEP_PERSISTENT, QL_OPT_STEP_KERNEL, QL_OPT_BARRIER_TIMEOUT_NS,
-                   QL_OPT_TEST_BARRIER_EXTRA, QL_OPT_STEP_TRACE,
+                   QL_OPT_TEST_BARRIER_EXTRA, QL_OPT_STEP_TRACE, QL_BATCHED_MMA_SYNC, QL_BATCHED_TCGEN05,
                    Q4Matrix, LayerDesc, ModelDesc,
                    StepArgs, SIGNATURES, LIB_PATH, lib, check, ptr, stream_ptr)
 
 __all__ = [
     "QLError", "lib", "ql_q4_0_pack", "ql_q4_0_unpack", "ql_q4_0_pack_device", "ql_gemv_q4_0",
     "ql_q4_0_stream_bytes", "ql_q4_0_stream_pack", "ql_gemv_q4_0_stream",
-    "ql_gemv_q4_0_stream_workspace_bytes",
+    "ql_gemv_q4_0_stream_workspace_bytes", "ql_set_batched_gemv_form",
     "ql_paged_attn_workspace_bytes", "ql_paged_attn_decode", "ql_paged_attn_decode_noalloc",
     "ql_fused_norm_rope",
     "ql_rope_tables", "ql_check_device_error", "BlockPool", "SIGNATURES",
@@ -59,6 +59,14 @@ def ql_q4_0_stream_pack(scales, quants, rows, cols, silu, out, stream=None):
 
 def ql_gemv_q4_0_stream_workspace_bytes(rows, cols, silu=0):
     return int(lib().ql_gemv_q4_0_stream_workspace_bytes(rows, cols, silu))
+
+
+def ql_set_batched_gemv_form(form):
+    """Tensor-core form of the batch 3-32 GEMV for this process; returns the previous form."""
+    rc = int(lib().ql_set_batched_gemv_form(form))
+    if rc < 0:
+        check(rc)
+    return rc
 
 
 def ql_gemv_q4_0_stream(w_stream, rows, cols, x, batch, y, epilogue=QL_EPI_NONE, workspace=None, stream=None):

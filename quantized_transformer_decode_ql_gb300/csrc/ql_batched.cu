@@ -21,6 +21,7 @@
 // ring of bulk copies (TMA) as the batch-1 kernel.
 #include "ql_persist.cuh"
 
+#include <atomic>
 #include <cstdlib>
 #include <mutex>
 #include <set>
@@ -501,6 +502,344 @@ __global__ void __launch_bounds__(kNormT) rms_norm_kernel(const float* x, int co
     }
 }
 
+// ------------------------------------------------------------------ tcgen05 form
+// The same split over K, with the products on the 5th-generation tensor cores: per row block of
+// 8 tiles (128 rows, the MMA's M) and unit of the window, 16 dequantisation warps write the
+// block's (q - 8) d into tensor memory (one thread per row: its 16-byte code runs expand, with
+// LOP3 / HSUB2 / HMUL2, to the f16 values of the A operand, `tcgen05.st`), and one control warp
+// issues `tcgen05.mma` (kind::f16, M = 128, N = 32 batch columns, K = 16) against the window's
+// activations staged once in shared memory (the B operand, K-major core matrices), accumulating
+// in f32 in tensor memory. The K order inside a 32-bit code word is the same permutation on both
+// operands (the staged pairs of stage_window), so the sums are exact dot products. The codes
+// stream in by bulk copies (one per tile per row block, 2 row blocks in flight); the
+// accumulators of a row block are read back (`tcgen05.ld`) by 4 warps and written as the
+// window's partial sums for merge_kernel. Every wait is bounded.
+namespace tc {
+constexpr int kDW = 16;                        // dequantisation warps, 4 per tensor-memory lane quarter
+constexpr int kCtl = kDW;                      // the control warp (allocation, MMA issue)
+constexpr int kThreads = (kDW + 1) * 32;
+constexpr int kRB = 8;                         // tiles per row block: 128 rows
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kACol = 64;                 // A slots: kASlots x 64 columns from here; D: 2 x 32 below
+constexpr int kASlots = 7;                     // unit g of the CTA (row block x window units) uses slot g % 7
+constexpr size_t kCodesBytes = (size_t)kRB * kWinUnits * kUnitBytes;   // one row block's codes
+constexpr size_t kBBytes = (size_t)kWinUnits * kUnitBlocks * 4 * 4 * 128;   // window x 32 columns, f16
+constexpr size_t kSmem = 2 * kCodesBytes + kBBytes;
+// MMA instruction descriptor: D f32, A and B f16, both K-major, N = 32, M = 128
+constexpr uint32_t kIdesc = (1u << 4) | ((32u >> 3) << 17) | ((128u >> 4) << 24);
+enum { kFull = 0, kFree = 2, kAFull = 4, kAFree = 4 + kASlots, kDFull = 4 + 2 * kASlots, kDFree = kDFull + 2,
+       kDone = kDFree + 2, kBars = kDone + 1 };
+
+__device__ __forceinline__ uint32_t su32(const void* q) { return static_cast<uint32_t>(__cvta_generic_to_shared(q)); }
+
+// Wait for phase `parity` of an mbarrier, bounded; false (the CTA's abort flag set and the
+// error recorded) when the bound runs out, or when another warp has aborted. abort_flag may be
+// null (the final drain: the bound alone).
+__device__ __forceinline__ bool tc_wait(uint32_t mb, uint32_t parity, const BParams& p, int* abort_flag, int where) {
+    for (int spin = 0; spin < persist::kFastSpins; ++spin)
+        if (persist::mbar_test(mb, parity)) return true;
+    const unsigned long long t0 = persist::global_ns();
+    for (unsigned int spin = 1;; ++spin) {
+        if (persist::mbar_test(mb, parity)) return true;
+        if ((spin & 63u) == 0) {
+            if (abort_flag != nullptr && *reinterpret_cast<volatile int*>(abort_flag)) return false;
+            if (persist::global_ns() - t0 > p.timeout_ns) break;
+        }
+    }
+    if (abort_flag == nullptr || atomicExch(abort_flag, 1) == 0) {
+        record_device_error(p.err, kErrGemvStage, blockIdx.x, where);
+        atomicExch(p.sync + 2, 1u);
+    }
+    return false;
+}
+
+__device__ __forceinline__ void arrive(uint32_t mb) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(mb) : "memory");
+}
+
+// Stage window w of every column as the B operand: chunk kc = 4 j + t (8 f16: the pairs of
+// stage_window) of column c at ((kc * 4 + c / 8) * 8 + c % 8) * 16; columns past the batch zero.
+// An item is (column c, block j, chunk t); the 8 columns of a group are consecutive lanes, so a
+// warp's 16-byte stores fill whole 128-byte rows (no bank conflicts).
+__device__ void stage_b(const BParams& p, const Geo& G, unsigned char* bsm, int nthreads) {
+    const int tid = threadIdx.x;
+    const int nb = G.kwu * kUnitBlocks, cols = p.M.nblk * 32, j0 = G.w * nb;
+    const int ncg = (p.B + 7) >> 3;   // column groups holding batch columns
+    uint4* b4 = reinterpret_cast<uint4*>(bsm);
+    for (int i = tid; i < (4 - ncg) * 8 * nb * 4; i += nthreads) {   // groups past the batch
+        const int cg = ncg + i / (8 * nb * 4), r = i % (8 * nb * 4);
+        b4[((r >> 3) * 4 + cg) * 8 + (r & 7)] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    const int nitems = ncg * 8 * nb * 4;
+    constexpr int kChunk = 4;
+    for (int base = 0; base < nitems; base += kChunk * nthreads) {
+        uint2 ha[kChunk], hh[kChunk];
+#pragma unroll
+        for (int r = 0; r < kChunk; ++r) {
+            const int item = base + r * nthreads + tid;
+            const int cl = item & 7, t = (item >> 3) & 3, rest = item >> 5, j = rest % nb, c = (rest / nb) * 8 + cl;
+            if (item < nitems && c < p.B) {
+                const size_t off = (size_t)c * cols + 32 * (j0 + j) + 4 * t;
+                ha[r] = __ldcg(reinterpret_cast<const uint2*>(p.x16 + off));
+                hh[r] = __ldcg(reinterpret_cast<const uint2*>(p.x16 + off + 16));
+            } else {
+                ha[r] = hh[r] = make_uint2(0u, 0u);
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < kChunk; ++r) {
+            const int item = base + r * nthreads + tid;
+            if (item >= nitems) break;
+            const int cl = item & 7, t = (item >> 3) & 3, rest = item >> 5, j = rest % nb, cg = rest / nb;
+            const float2 f0 = __half22float2(as_h2(ha[r].x)), f1 = __half22float2(as_h2(ha[r].y));
+            const float2 f2 = __half22float2(as_h2(hh[r].x)), f3 = __half22float2(as_h2(hh[r].y));
+            const __half2 p0 = __floats2half2_rn(f0.x, f1.x);
+            const __half2 p1 = __floats2half2_rn(f0.y, f1.y);
+            const __half2 p2 = __floats2half2_rn(f2.x * 0.0625f, f3.x * 0.0625f);
+            const __half2 p3 = __floats2half2_rn(f2.y * 0.0625f, f3.y * 0.0625f);
+            b4[((4 * j + t) * 4 + cg) * 8 + cl] = make_uint4(as_u32(p0), as_u32(p1), as_u32(p2), as_u32(p3));
+        }
+    }
+}
+
+// Bulk copy of tile i of row block rb (its units of the window, contiguous) into the row
+// block's codes buffer; one lane. A tile past the row group only arrives.
+__device__ __forceinline__ void issue_tile(const BParams& p, const Geo& G, unsigned char* codes, uint32_t bar, int rb,
+                                           int i) {
+    const int tl = rb * kRB + i, b = rb & 1;
+    const uint32_t mb = bar + (kFull + b) * 8;
+    if (tl >= G.T1 - G.T0) {
+        arrive(mb);
+        return;
+    }
+    const uint32_t bytes = (uint32_t)(G.kwu * kUnitBytes);
+    const uint8_t* src = p.M.stream + ((size_t)(G.T0 + tl) * G.nst + (size_t)G.w * G.kwu) * kUnitBytes;
+    const uint32_t dst = su32(codes + (size_t)b * kCodesBytes + (size_t)i * G.kwu * kUnitBytes);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mb), "r"(bytes) : "memory");
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "l"(src), "r"(bytes), "r"(mb) : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_constant__ BParams p) {
+    extern __shared__ __align__(1024) unsigned char smem[];
+    __shared__ __align__(8) unsigned long long bars[kBars];
+    __shared__ uint32_t tmem_base;
+    __shared__ int abort_flag;
+    __shared__ int last_issued[2];   // per codes buffer: the last row block copied into it (-1: none)
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const Geo G = geometry(p);
+    const int T = G.T1 - G.T0, nrb = (T + kRB - 1) / kRB, kwu = G.kwu;
+    unsigned char* codes = smem;
+    unsigned char* bsm = smem + 2 * kCodesBytes;
+    const uint32_t bar = su32(bars);
+    unsigned long long* tr = p.trace ? p.trace + (size_t)blockIdx.x * persist::kTraceWords : nullptr;
+    persist::stamp(tr, 0);
+    if (tid == 0) {
+        for (int b = 0; b < 2; ++b) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar + (kFull + b) * 8), "r"(kRB) : "memory");
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar + (kFree + b) * 8), "r"(kDW) : "memory");
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar + (kDFull + b) * 8) : "memory");
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 4;" ::"r"(bar + (kDFree + b) * 8) : "memory");
+            last_issued[b] = -1;
+        }
+        for (int a = 0; a < kASlots; ++a) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 4;" ::"r"(bar + (kAFull + a) * 8) : "memory");
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar + (kAFree + a) * 8) : "memory");
+        }
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar + kDone * 8) : "memory");
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == kCtl) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&tmem_base)),
+                     "r"(kTmemCols) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tb = tmem_base;
+    int* abt = &abort_flag;
+
+    // the first two row blocks' codes before the wait (the weights do not depend on the predecessor)
+    if (warp < kRB && lane == 0) {
+        for (int rb = 0; rb < 2 && rb < nrb; ++rb) {
+            issue_tile(p, G, codes, bar, rb, warp);
+            last_issued[rb] = rb;
+        }
+    }
+    pdl_wait();
+    pdl_trigger();
+    persist::stamp(tr, 1);
+    if (warp < kDW) stage_b(p, G, bsm, kDW * 32);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // B is read by the tensor cores
+    __syncthreads();
+    persist::stamp(tr, 2);
+
+    if (warp < kDW) {
+        const int q = warp & 3, sub = warp >> 2;
+        const int nks = sub < kwu ? (kwu - sub + 3) / 4 : 0;   // units of the window this warp expands
+        const int tr_ = 2 * q + (lane >> 4), rit = lane & 15;   // this thread's row: tile, row in tile
+        const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+        const __half2 off_lo = as_h2(0x64086408u), off_hi = as_h2(0x64806480u);   // 1032, 1152
+        auto epilogue = [&](int rb) {
+            const int d = rb & 1;
+            if (!tc_wait(bar + (kDFull + d) * 8, (uint32_t)(rb >> 1) & 1u, p, abt, 1000 + rb)) return false;
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            uint32_t v[32];
+            asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                         "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                         : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+                           "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
+                           "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]),
+                           "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]),
+                           "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+                         : "r"(tb + lane_base + 32u * (uint32_t)d) : "memory");
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) arrive(bar + (kDFree + d) * 8);
+            const int tl = rb * kRB + tr_;
+            if (tl < T) {
+                float4* dst = reinterpret_cast<float4*>(p.part + (((size_t)G.w * p.M.ntile + G.T0 + tl) * 16 + rit) * kMaxCols);
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    dst[c] = make_float4(__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
+                                         __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3]));
+            }
+            return true;
+        };
+        bool ok = true;
+        for (int rb = 0; rb < nrb && ok; ++rb) {
+            const int b = rb & 1;
+            // refill the other buffer with row block rb + 1 once every warp is done with rb - 1
+            if (warp < kRB && rb >= 1 && rb + 1 < nrb) {
+                if (lane == 0) {
+                    ok = tc_wait(bar + (kFree + ((rb + 1) & 1)) * 8, (uint32_t)((rb - 1) >> 1) & 1u, p, abt, 2000 + rb);
+                    if (ok) {
+                        issue_tile(p, G, codes, bar, rb + 1, warp);
+                        last_issued[(rb + 1) & 1] = rb + 1;
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+            }
+            if (!tc_wait(bar + (kFull + b) * 8, (uint32_t)(rb >> 1) & 1u, p, abt, 3000 + rb)) {
+                ok = false;
+                break;
+            }
+            const unsigned char* cb = codes + (size_t)b * kCodesBytes;
+            for (int k2 = 0; k2 < nks; ++k2) {
+                const int kk = sub + 4 * k2, g = rb * kwu + kk, slot = g % kASlots, use = g / kASlots;
+                if (use > 0 && !tc_wait(bar + (kAFree + slot) * 8, (uint32_t)(use - 1) & 1u, p, abt, 4000 + rb)) {
+                    ok = false;
+                    break;
+                }
+                const int tl = rb * kRB + tr_;
+                const unsigned char* unit = cb + ((size_t)tr_ * kwu + kk) * kUnitBytes;
+                const uint32_t ta = tb + lane_base + kACol + 64u * (uint32_t)slot;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {   // blocks 2 half, 2 half + 1: 32 columns
+                    uint32_t v[32];
+                    if (tl < T) {
+                        const uint2 sc = *reinterpret_cast<const uint2*>(unit + 1024 + rit * 8);
+                        const uint32_t sw = half ? sc.y : sc.x;
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int qb = 2 * half + e;
+                            const uint4 cw = *reinterpret_cast<const uint4*>(unit + (qb * 16 + rit) * 16);
+                            const __half2 d2 = e ? __high2half2(as_h2(sw)) : __low2half2(as_h2(sw));
+                            const uint32_t ws[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+                            for (int t = 0; t < 4; ++t) {
+                                const uint32_t w = ws[t], w8 = w >> 8;
+                                v[(e * 4 + t) * 4 + 0] = as_u32(__hmul2(__hsub2(as_h2((w & 0x000F000Fu) | 0x64006400u), off_lo), d2));
+                                v[(e * 4 + t) * 4 + 1] = as_u32(__hmul2(__hsub2(as_h2((w8 & 0x000F000Fu) | 0x64006400u), off_lo), d2));
+                                v[(e * 4 + t) * 4 + 2] = as_u32(__hmul2(__hsub2(as_h2((w & 0x00F000F0u) | 0x64006400u), off_hi), d2));
+                                v[(e * 4 + t) * 4 + 3] = as_u32(__hmul2(__hsub2(as_h2((w8 & 0x00F000F0u) | 0x64006400u), off_hi), d2));
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = 0u;
+                    }
+                    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+                                 "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+                                 ::"r"(ta + 32u * (uint32_t)half), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]),
+                                   "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]),
+                                   "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+                                   "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]),
+                                   "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31]) : "memory");
+                }
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) arrive(bar + (kAFull + slot) * 8);
+            }
+            if (!ok) break;
+            __syncwarp();
+            if (lane == 0) arrive(bar + (kFree + b) * 8);   // this warp is done with the buffer
+            if (sub == 3 && rb >= 1) ok = epilogue(rb - 1);
+        }
+        if (ok && sub == 3 && nrb > 0) epilogue(nrb - 1);
+    } else if (lane == 0) {
+        // the control warp's single issuing thread
+        const uint32_t bbase = su32(bsm);
+        for (int rb = 0; rb < nrb; ++rb) {
+            const int d = rb & 1;
+            if (rb >= 2 && !tc_wait(bar + (kDFree + d) * 8, (uint32_t)((rb - 2) >> 1) & 1u, p, abt, 5000 + rb)) break;
+            bool ok = true;
+            for (int kk = 0; kk < kwu && ok; ++kk) {
+                const int g = rb * kwu + kk, s = g % kASlots, use = g / kASlots;
+                if (!tc_wait(bar + (kAFull + s) * 8, (uint32_t)use & 1u, p, abt, 6000 + rb)) {
+                    ok = false;
+                    break;
+                }
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t baddr = bbase + (uint32_t)(kk * 16 + ks * 2) * 512u;
+                    const unsigned long long desc = (unsigned long long)((baddr & 0x3FFFFu) >> 4) |
+                                                    ((unsigned long long)(512u >> 4) << 16) |
+                                                    ((unsigned long long)(128u >> 4) << 32) | (1ull << 46);
+                    const uint32_t acc = (kk | ks) ? 1u : 0u;
+                    asm volatile("{\n .reg .pred pa;\n setp.ne.u32 pa, %4, 0;\n"
+                                 " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pa;\n}"
+                                 ::"r"(tb + 32u * (uint32_t)d), "r"(tb + kACol + 64u * (uint32_t)s + 8u * (uint32_t)ks),
+                                   "l"(desc), "r"(kIdesc), "r"(acc) : "memory");
+                }
+                asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                             ::"r"(bar + (kAFree + s) * 8) : "memory");
+            }
+            if (!ok) break;
+            asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                         ::"r"(bar + (kDFull + d) * 8) : "memory");
+        }
+        // every MMA issued has completed before the tensor memory is released
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                     ::"r"(bar + kDone * 8) : "memory");
+        tc_wait(bar + kDone * 8, 0u, p, nullptr, 7000);
+    }
+    persist::stamp(tr, 3);
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    persist::stamp(tr, 4);
+    if (warp == kCtl) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tb), "r"(kTmemCols) : "memory");
+    }
+    // copies still in flight (only after an abort): let them land before the CTA leaves (bounded)
+    if (tid == 0) {
+        for (int b = 0; b < 2; ++b)
+            if (last_issued[b] >= 0)
+                tc_wait(bar + (kFull + b) * 8, (uint32_t)(last_issued[b] >> 1) & 1u, p, nullptr, 8000);
+    }
+    persist::stamp(tr, 5);
+    if (tr != nullptr && tid == 0) tr[6] = tr[7] = 0ull;
+}
+}  // namespace tc
+
 template <int NT>
 cudaError_t run(bool launch, const BParams* p, int grid, cudaStream_t s, bool pdl) {
     if (!launch) {
@@ -542,6 +881,22 @@ size_t batched_gemv_workspace_bytes(int rows, int nblk, int silu) {
     return (size_t)nwin * ntile * 16 * batched::kMaxCols * sizeof(float);
 }
 
+// The tensor-core form of batch 3-32 (process-wide): mma.sync by default (measured faster on the
+// decode step), tcgen05 with ql_set_batched_gemv_form or QL_BATCHED_TC=1.
+static std::atomic<int> g_form{-1};
+static int batched_form() {
+    int f = g_form.load();
+    if (f < 0) {
+        const char* e = std::getenv("QL_BATCHED_TC");
+        f = (e != nullptr && std::atoi(e) != 0) ? QL_BATCHED_TCGEN05 : QL_BATCHED_MMA_SYNC;
+        int expect = -1;
+        g_form.compare_exchange_strong(expect, f);
+        f = g_form.load();
+    }
+    return f;
+}
+static bool use_tc() { return batched_form() == QL_BATCHED_TCGEN05; }
+
 int batched_gemv_prepare() {
     static std::mutex mu;
     static std::set<int> done;
@@ -549,6 +904,17 @@ int batched_gemv_prepare() {
     QL_TRY_CUDA(cudaGetDevice(&dev));
     std::lock_guard<std::mutex> lk(mu);
     if (done.count(dev)) return QL_OK;
+    {
+        int optin = 0;
+        cudaFuncAttributes fa = {};
+        cudaError_t e0 = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e0 == cudaSuccess) e0 = cudaFuncGetAttributes(&fa, batched::tc::gemv_tc_kernel);
+        if (e0 == cudaSuccess && batched::tc::kSmem + fa.sharedSizeBytes > (size_t)optin) e0 = cudaErrorInvalidConfiguration;
+        if (e0 == cudaSuccess)
+            e0 = cudaFuncSetAttribute(batched::tc::gemv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)batched::tc::kSmem);
+        if (e0 != cudaSuccess) return cuda_error(e0, "batched gemv: tcgen05 kernel attributes");
+    }
     cudaError_t e = batched::run<1>(false, nullptr, 0, nullptr, false);
     if (e == cudaSuccess) e = batched::run<2>(false, nullptr, 0, nullptr, false);
     if (e == cudaSuccess) e = batched::run<3>(false, nullptr, 0, nullptr, false);
@@ -594,10 +960,15 @@ int batched_gemv_launch(const StreamGemvArgs& a, cudaStream_t s, bool pdl) {
         if (e0 != cudaSuccess) return cuda_error(e0, "rms norm launch");
     }
     const int nt = (a.batch + 7) / 8, grid = nwin * ngr;
-    cudaError_t e = nt == 1   ? batched::run<1>(true, &p, grid, s, pdl)
-                    : nt == 2 ? batched::run<2>(true, &p, grid, s, pdl)
-                    : nt == 3 ? batched::run<3>(true, &p, grid, s, pdl)
-                              : batched::run<4>(true, &p, grid, s, pdl);
+    cudaError_t e;
+    if (use_tc())
+        e = ql::launch(batched::tc::gemv_tc_kernel, dim3(grid), dim3(batched::tc::kThreads), batched::tc::kSmem, s,
+                       pdl, p);
+    else
+        e = nt == 1   ? batched::run<1>(true, &p, grid, s, pdl)
+            : nt == 2 ? batched::run<2>(true, &p, grid, s, pdl)
+            : nt == 3 ? batched::run<3>(true, &p, grid, s, pdl)
+                      : batched::run<4>(true, &p, grid, s, pdl);
     if (e != cudaSuccess) return cuda_error(e, "batched gemv launch");
     // the windows added up and the epilogue, over every SM
     e = ql::launch(batched::merge_kernel, dim3(2 * num_sms()), dim3(batched::kMergeT), 0, s, pdl, p);
@@ -606,3 +977,11 @@ int batched_gemv_launch(const StreamGemvArgs& a, cudaStream_t s, bool pdl) {
 }
 
 }  // namespace ql
+
+extern "C" int ql_set_batched_gemv_form(int form) {
+    using namespace ql;
+    QL_REQUIRE(form == QL_BATCHED_MMA_SYNC || form == QL_BATCHED_TCGEN05, "ql_set_batched_gemv_form: unknown form");
+    const int prev = batched_form();
+    g_form.store(form);
+    return prev;
+}

@@ -161,3 +161,12 @@ def test_stream_workspace_bad_shapes(ql):
     assert ql.ql_gemv_q4_0_stream_workspace_bytes(16, 96, 0) == 0
     assert ql.ql_gemv_q4_0_stream_workspace_bytes(16, 1152, 0) == 0
     assert ql.ql_gemv_q4_0_stream_workspace_bytes(15, 1024, 1) == 0
+
+
+def test_batched_gemv_form_switch(ql):
+    """The batch 3-32 GEMV form is a process-wide choice: unknown forms are rejected, the
+    previous form is returned (no device needed)."""
+    assert ql.lib().ql_set_batched_gemv_form(7) == ql.QL_EINVAL
+    prev = ql.ql_set_batched_gemv_form(ql.QL_BATCHED_TCGEN05)
+    assert prev in (ql.QL_BATCHED_MMA_SYNC, ql.QL_BATCHED_TCGEN05)
+    assert ql.ql_set_batched_gemv_form(prev) == ql.QL_BATCHED_TCGEN05

@@ -198,12 +198,22 @@ def test_replay_before_capture_is_an_error(tiny):
     assert e.value.status == ql.QL_ESTATE
 
 
-@pytest.mark.parametrize("B", (2, 3))   # 2: the persistent kernel; 3: one launch per phase
-def test_batched_slots_with_replacement(tiny, B):
+@pytest.mark.parametrize("B,form", [(2, "mma_sync"), (3, "mma_sync"), (3, "tcgen05")])
+def test_batched_slots_with_replacement(tiny, B, form):
     """Slots at different context lengths (pre-filled f16 contexts in fragmented blocks from
     the library's block allocator) decode together; after four steps slot 1 finishes, its
     blocks go back to the pool and it restarts on a fresh 7-position context in newly allocated
-    blocks. Every step's logits of every slot match the oracle decoding each slot on its own."""
+    blocks. Every step's logits of every slot match the oracle decoding each slot on its own
+    (batch 3: with either tensor-core form of the batched GEMV)."""
+    import quantized_transformer_decode_ql_gb300 as ql
+    prev = ql.ql_set_batched_gemv_form(ql.QL_BATCHED_TCGEN05 if form == "tcgen05" else ql.QL_BATCHED_MMA_SYNC)
+    try:
+        _slots_with_replacement(tiny, B)
+    finally:
+        ql.ql_set_batched_gemv_form(prev)
+
+
+def _slots_with_replacement(tiny, B):
     import quantized_transformer_decode_ql_gb300 as ql
     gm, om = tiny
     maxb = 4

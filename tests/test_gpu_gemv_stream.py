@@ -24,6 +24,16 @@ from gpu_util import lib, dev, q4_dev, rel_err
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(params=["mma_sync", "tcgen05"])
+def form(request):
+    """Both tensor-core forms of the batch 3-32 GEMV (restored afterwards)."""
+    ql = lib()
+    f = ql.QL_BATCHED_MMA_SYNC if request.param == "mma_sync" else ql.QL_BATCHED_TCGEN05
+    prev = ql.ql_set_batched_gemv_form(f)
+    yield request.param
+    ql.ql_set_batched_gemv_form(prev)
+
+
 def tile_rows(rows, silu, tile):
     """Global rows of tile rows 0..15 (-1: past the matrix)."""
     if silu:
@@ -160,7 +170,7 @@ def test_stream_gemv_zero_and_extreme_blocks():
 
 @pytest.mark.parametrize("rows,cols", [(37, 256), (200, 384), (1000, 1024), (6144, 4096), (96, 12288)])
 @pytest.mark.parametrize("batch", [3, 5, 8, 17, 32])
-def test_stream_gemv_batched(rows, cols, batch):
+def test_stream_gemv_batched(rows, cols, batch, form):
     """Batches 3-32: every weight streamed once, K in windows of 1024 columns."""
     ql = lib()
     w = ql_inputs.gemv_weight(rows, cols, seed=12)
@@ -170,7 +180,7 @@ def test_stream_gemv_batched(rows, cols, batch):
 
 
 @pytest.mark.parametrize("batch", [3, 16, 32])
-def test_stream_gemv_batched_epilogues(batch):
+def test_stream_gemv_batched_epilogues(batch, form):
     ql = lib()
     w = ql_inputs.gemv_weight(300, 2048, seed=14)
     x = ql_inputs.gemv_activations(batch, 2048, seed=15)
@@ -203,7 +213,7 @@ def test_stream_gemv_rejects_bad_arguments():
         assert e.value.status == ql.QL_EINVAL
 
 
-def test_stream_gemv_batched_shared_workspace():
+def test_stream_gemv_batched_shared_workspace(form):
     """Matrices of different shapes take turns on one workspace (as the decode step's projections
     do): the results equal those of separate workspaces, bit for bit."""
     ql = lib()
