@@ -425,7 +425,7 @@ def launch_phases(gm, sargs, s, cfg):
     grid = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     rows = 4 * cfg.n_layers + 1
     B = int(sargs.batch) if hasattr(sargs, "batch") else 1
-    buf = torch.zeros(rows * grid * 8, dtype=torch.int64, device="cuda")
+    buf = torch.zeros((rows + cfg.n_layers) * grid * 8, dtype=torch.int64, device="cuda")
     gm.ql_model_set_option(ql.QL_OPT_STEP_TRACE, buf.data_ptr())
     try:   # a graph captured with the trace on, replayed as the timed graph is (2 steps: one warm)
         gm.ql_decode_graph_capture(sargs, s)
@@ -440,7 +440,8 @@ def launch_phases(gm, sargs, s, cfg):
         gm.ql_model_set_option(ql.QL_OPT_STEP_TRACE, 0)
         gm.ql_decode_graph_capture(sargs, s)
     gm.ql_check_device_error()
-    t = buf.cpu().numpy().reshape(rows, grid, 8).astype(np.float64)
+    ta = buf.cpu().numpy().reshape(rows + cfg.n_layers, grid, 8).astype(np.float64)
+    t, tat = ta[:rows], ta[rows:]
     if not (t[:, 0, 0] > 0).all():
         return None   # another GEMV form ran (not traced)
     kinds = [k for _ in range(cfg.n_layers) for k in ("qkv", "o", "gate_up", "down")] + ["lm_head"]
@@ -450,6 +451,7 @@ def launch_phases(gm, sargs, s, cfg):
         prev_end = t[k - 1][t[k - 1][:, 0] > 0][:, 5].max() if k > 0 else float("nan")
         v = {"gap": (r[:, 0].min() - prev_end) if k > 0 else float("nan"),
              "wait": r[:, 1].max() - r[:, 0].min(),
+             "first_past_wait": (r[:, 1].min() - prev_end) if k > 0 else float("nan"),
              "stage": (r[:, 2] - r[:, 1]).mean(), "loop": (r[:, 3] - r[:, 2]).mean(),
              "finish": (r[:, 5] - r[:, 3]).mean(), "tail": r[:, 5].max() - r[:, 5].mean(),
              "span": r[:, 5].max() - r[:, 0].min(),
@@ -460,6 +462,25 @@ def launch_phases(gm, sargs, s, cfg):
     for n, lst in acc.items():
         out[n] = {key: round(float(np.nanmean([d[key] for d in lst])) / (1.0 if key == "ring_wait_frac" else 1e3), 3)
                   for key in lst[0]}
+    # attention (layer l between GEMV rows 4l and 4l+1), from the qkv GEMV's last CTA end:
+    # first CTA start, last CTA past its wait, means of q ready / blocks / ticket per CTA, the
+    # merging CTAs' merge, last CTA end; then the o GEMV's last CTA past its wait
+    att = []
+    for l in range(cfg.n_layers):
+        r = tat[l][tat[l][:, 5] > 0]
+        if len(r) == 0:
+            continue
+        qkv_end = t[4 * l][t[4 * l][:, 0] > 0][:, 5].max()
+        o = t[4 * l + 1][t[4 * l + 1][:, 0] > 0]
+        mg = r[r[:, 6] == 1]
+        att.append({"first_start": r[:, 0].min() - qkv_end, "first_past_wait": r[:, 1].min() - qkv_end,
+                    "last_past_wait": r[:, 1].max() - qkv_end,
+                    "q_ready": (r[:, 2] - r[:, 1]).mean(), "blocks": (r[:, 3] - r[:, 2]).mean(),
+                    "ticket": (r[:, 4] - r[:, 3]).mean(),
+                    "merge": (mg[:, 5] - mg[:, 4]).mean() if len(mg) else float("nan"),
+                    "last_end": r[:, 5].max() - qkv_end, "o_past_wait": o[:, 1].max() - qkv_end})
+    if att:
+        out["attention"] = {k: round(float(np.nanmean([a[k] for a in att])) / 1e3, 3) for k in att[0]}
     out["total_step_us"] = round((t[rows - 1][:, 5].max() - t[0][t[0][:, 0] > 0][:, 0].min()) / 1e3, 1)
     return out
 

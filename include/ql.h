@@ -279,12 +279,17 @@ enum { QL_STEP_AUTO = 0, QL_STEP_LAUNCHES = 1, QL_STEP_PERSISTENT = 2 };
  *                              staged, warp 0's units done, all warps done, epilogues done;
  *                              attention: q ready, blocks merged, split ticket taken, end).
  *                              A step of separate launches stamps its GEMV launches
- *                              instead: launch k (qkv, o, gate_up, down of each layer, then
- *                              lm_head) fills row k, per CTA (at most num_SMs CTAs): 0 start,
+ *                              instead (buffer: (5 n_layers + 1) * num_SMs * 8 entries): launch
+ *                              k (qkv, o, gate_up, down of each layer, then lm_head) fills row
+ *                              k, per CTA (at most num_SMs CTAs): 0 start,
  *                              1 predecessor done, 2 activations staged, 3 units done (batch
  *                              1-2: warp 0's), 4 all warps done / partial sums written, 5 end
  *                              (6, 7 at batch 1-2: warp 0's cycles waiting for bulk copies /
- *                              in its unit loop; else 0). A profiling aid
+ *                              in its unit loop; else 0); the attention launch of layer l fills
+ *                              row 4 n_layers + 1 + l for its first num_SMs CTAs: 0 start, 1
+ *                              predecessor done, 2 q ready, 3 blocks done, 4 split ticket
+ *                              taken, 5 end, 6 = 1 for the CTA that merged the splits. A
+ *                              profiling aid
  * Applies to steps issued (or graphs captured) afterwards. QL_EINVAL for anything else.  */
 enum { QL_OPT_STEP_KERNEL = 1, QL_OPT_BARRIER_TIMEOUT_NS = 2, QL_OPT_TEST_BARRIER_EXTRA = 3,
        QL_OPT_STEP_TRACE = 4 };

@@ -67,7 +67,17 @@ struct AParams {
     long long max_position;
     __half* kw;
     __half* vw;
+    unsigned long long* trace;   // optional stamps of the CTAs with linear index < trace_ctas
+    int trace_ctas;
 };
+
+__device__ __forceinline__ void attn_stamp(unsigned long long* tr, int i) {
+    if (tr != nullptr && threadIdx.x == 0) {
+        unsigned long long t;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+        tr[i] = t;
+    }
+}
 
 // Physical block of logical block lb of sequence b, or -1 if the table entry is out of range.
 __device__ __forceinline__ int bt_row_phys(const AParams& p, int b, int lb) {
@@ -159,6 +169,9 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AParams p, Dev
     // wait and the new row is patched into them. Otherwise q, K/V or the lengths may come from
     // the previous kernel: wait first.
     const bool fused = p.qkv != nullptr;
+    const int lin = (int)(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z));
+    unsigned long long* tr = (p.trace != nullptr && lin < p.trace_ctas) ? p.trace + (size_t)lin * 8 : nullptr;
+    attn_stamp(tr, 0);
     l2_prefetch_share(p.next.ptr[0], p.next.bytes[0]);
     l2_prefetch_share(p.next.ptr[1], p.next.bytes[1]);
     if (!fused) {
@@ -224,6 +237,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AParams p, Dev
         if (warp == 0) rk = rope_lane<HD>(p.k_norm, cr, sr, lane);
         pdl_wait();
         pdl_trigger();
+        attn_stamp(tr, 1);
     }
 
     // Q as the A operand of S = Q K^T: rows = the G heads of this kv head (rows >= G and the
@@ -265,6 +279,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AParams p, Dev
         }
         __threadfence_block();
         __syncthreads();
+        attn_stamp(tr, 2);
         qsrc = &qs[0][0];
     } else {
         qsrc = p.q + ((size_t)b * p.n_heads + g * G) * HD;
@@ -365,6 +380,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AParams p, Dev
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
     __syncthreads();   // every warp is done with its tiles: the buffer now holds the merge state
+    attn_stamp(tr, 3);
     float* wacc = reinterpret_cast<float*>(asmem);   // [warp][G][HD]
     if (hv) {
 #pragma unroll
@@ -404,30 +420,40 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AParams p, Dev
             }
         }
     }
-    if (n_active == 1) return;
+    if (n_active == 1) {
+        attn_stamp(tr, 4);
+        attn_stamp(tr, 5);
+        return;
+    }
 
-    __threadfence();
+    // the split ticket: the barrier orders every thread's partial stores before thread 0's
+    // release (cumulative), and thread 0's acquire before the merge's loads
     __syncthreads();
     if (threadIdx.x == 0) {
-        const int ticket = atomicAdd(&p.tickets[b * p.n_kv + g], 1);
+        int ticket;
+        asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(ticket) : "l"(&p.tickets[b * p.n_kv + g]) : "memory");
         last_flag = (ticket == n_active - 1);
     }
     __syncthreads();
-    if (!last_flag) return;
-    __threadfence();
+    attn_stamp(tr, 4);
+    if (!last_flag) {
+        attn_stamp(tr, 5);
+        return;
+    }
     // merge: one pass per float4 output over the splits (online softmax in the exp2 domain),
-    // the (m, l, acc) loads of 8 splits issued together
+    // the (m, l, acc) loads of kMergeSplits splits issued together
     for (int i = threadIdx.x; i < G * HD / 4; i += kAttnThreads) {
         const int h = i / (HD / 4), d4 = i - h * (HD / 4);
         const size_t base = ((size_t)b * n_heads + g * G + h) * p.nsplit;
         const float4* srcp = reinterpret_cast<const float4*>(p.pacc) + base * (HD / 4) + d4;
         float M = -INFINITY, Ls = 0.f;
         float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int k0 = 0; k0 < n_active; k0 += 8) {
-            float mk[8], lk[8];
-            float4 ak[8];
+        constexpr int kMergeSplits = 8;   // 16 raised the kernel to 186 registers (2 CTAs per SM)
+        for (int k0 = 0; k0 < n_active; k0 += kMergeSplits) {
+            float mk[kMergeSplits], lk[kMergeSplits];
+            float4 ak[kMergeSplits];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
+            for (int u = 0; u < kMergeSplits; ++u) {
                 if (k0 + u < n_active) {
                     mk[u] = __ldcg(p.pm + base + k0 + u);
                     lk[u] = __ldcg(p.pl + base + k0 + u);
@@ -435,7 +461,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AParams p, Dev
                 }
             }
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
+            for (int u = 0; u < kMergeSplits; ++u) {
                 if (k0 + u < n_active && mk[u] != -INFINITY) {
                     const float mn = fmaxf(M, mk[u]);
                     const float fo = exp2f(M - mn), fk = exp2f(mk[u] - mn);
@@ -452,6 +478,8 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AParams p, Dev
         *reinterpret_cast<__half2*>(o + 2) = __floats2half2_rn(A.z * inv, A.w * inv);
     }
     if (threadIdx.x == 0) p.tickets[b * p.n_kv + g] = 0;   // re-arm for the next call
+    if (tr != nullptr && threadIdx.x == 0) tr[6] = 1;   // this CTA merged the splits
+    attn_stamp(tr, 5);
 }
 
 struct Layout {
@@ -593,6 +621,8 @@ int attn_launch(const AttnArgs& a, cudaStream_t s, bool pdl) {
     p.num_blocks = a.num_blocks;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.out = a.out;
+    p.trace = a.trace;
+    p.trace_ctas = a.trace_ctas;
     char* ws = static_cast<char*>(a.workspace);
     p.tickets = reinterpret_cast<int*>(ws + lo.tickets_off);
     p.pm = reinterpret_cast<float*>(ws + lo.pm_off);

@@ -169,6 +169,9 @@ struct AttnArgs {
     const float* sin_t;
     float eps;
     int64_t max_position;
+    unsigned long long* trace;   // optional [CTAs][8] globaltimer stamps (CTAs with a linear index
+    int trace_ctas;              // below trace_ctas): 0 start, 1 past the wait, 2 q ready,
+                                 // 3 blocks done, 4 partial written / ticket taken, 5 end
 };
 size_t attn_workspace_bytes(int64_t batch, int n_heads, int n_kv_heads, int head_dim,
                             int block_size, int64_t max_blocks_per_seq);

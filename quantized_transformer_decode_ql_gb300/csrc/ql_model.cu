@@ -279,6 +279,10 @@ int run_step(ql_model* m, const ql_step_args* a, cudaStream_t s) {
             at.out = m->attn;
             at.workspace = m->attn_ws;
             at.workspace_bytes = m->attn_ws_bytes;
+            if (m->trace) {   // attention rows follow the GEMV rows
+                at.trace = m->trace + (size_t)(4 * d.n_layers + 1 + li) * num_sms() * persist_trace_words();
+                at.trace_ctas = num_sms();
+            }
             if ((rc = attn_launch(at, s, pdl)) != QL_OK) return rc;
             if ((rc = sg(Ms[1], QL_EPI_ADD_RESIDUAL, false, nullptr, m->attn, nullptr, m->x, (int)d.hidden,
                          ffn_norm)) != QL_OK)
