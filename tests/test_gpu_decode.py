@@ -310,3 +310,47 @@ def test_persistent_rejects_larger_batches(tiny):
     with pytest.raises(ql.QLError) as e:
         gm.ql_decode_step(args)
     assert e.value.status == ql.QL_EINVAL
+
+
+@pytest.mark.parametrize("B", (1, 3))   # 1: stream GEMVs; 3: split-K GEMVs (+ merge kernels)
+def test_launch_trace_stamps(tiny, B):
+    """QL_OPT_STEP_TRACE on the one-launch-per-phase step: every GEMV launch row has its CTAs'
+    stamps in order (start <= past the wait <= staged <= units done <= end), each GEMV starts
+    no earlier than the previous one started, and each layer's attention row is stamped in
+    order for the CTAs that took part; turning the option off leaves the buffer untouched."""
+    ql = lib()
+    gm, _ = tiny
+    set_mode(gm, "launches")
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    L = CFG.n_layers
+    buf = torch.zeros((5 * L + 1) * sms * 8, dtype=torch.int64, device="cuda")
+    tokens = torch.zeros(B, dtype=torch.int32, device="cuda")
+    positions = torch.full((B,), 3, dtype=torch.int32, device="cuda")
+    bt = dev(slot_tables(B, 4, seed=11))
+    args = gm.step_args(tokens, positions, bt, torch.zeros(B, dtype=torch.int32, device="cuda"))
+    gm.ql_model_set_option(ql.QL_OPT_STEP_TRACE, buf.data_ptr())
+    try:
+        gm.ql_decode_step(args)
+        torch.cuda.synchronize()
+    finally:
+        gm.ql_model_set_option(ql.QL_OPT_STEP_TRACE, 0)
+    gm.ql_check_device_error()
+    t = buf.cpu().numpy().reshape(5 * L + 1, sms, 8)
+    starts = []
+    for k in range(4 * L + 1):
+        r = t[k][t[k][:, 0] > 0]
+        assert len(r) > 0, f"GEMV launch {k} not stamped"
+        for a, b in ((0, 1), (1, 2), (2, 3), (3, 5)):
+            assert (r[:, a] <= r[:, b]).all(), f"GEMV launch {k}: stamp {a} after {b}"
+        starts.append(r[:, 0].min())
+    assert all(a <= b for a, b in zip(starts, starts[1:]))
+    for l in range(L):
+        r = t[4 * L + 1 + l]
+        r = r[r[:, 5] > 0]
+        assert len(r) > 0, f"attention of layer {l} not stamped"
+        for a, b in ((0, 1), (1, 2), (2, 3), (3, 4), (4, 5)):
+            assert (r[:, a] <= r[:, b]).all()
+    before = buf.clone()
+    gm.ql_decode_step(args)
+    torch.cuda.synchronize()
+    assert torch.equal(buf, before)
