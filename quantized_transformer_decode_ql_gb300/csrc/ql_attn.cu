@@ -32,8 +32,9 @@
 namespace ql {
 namespace {
 
-constexpr int kAttnWarps = 4;
-constexpr int kAttnThreads = kAttnWarps * 32;
+// warps per CTA: 8 at batch 1-2 (16-block splits, every block of a warp staged before the wait,
+// half the splits to merge), else 4 (more CTAs per SM for long batched contexts)
+constexpr int attn_warps(int64_t batch) { return batch <= 2 ? 8 : 4; }
 constexpr int kBS = 16;   // tokens per KV block
 constexpr int kMaxSplit = 256;   // splits per (sequence, kv head), bounded by the host
 
@@ -149,8 +150,9 @@ __device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1,
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-template <int HD, int G>
-__global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AParams p, DevError* err) {
+template <int HD, int G, int NW>
+__global__ void __launch_bounds__(NW * 32) attn_split_kernel(AParams p, DevError* err) {
+    constexpr int kAttnWarps = NW, kAttnThreads = NW * 32;
     constexpr int KSTEPS = HD / 16;           // k-steps of the Q.K^T MMA
     constexpr int NT = HD / 8;                // 8-dim output tiles of the P.V MMA
     constexpr int PITCH = HD * 2 + 16;        // bytes per staged K/V row (padded: conflict-free ldmatrix)
@@ -493,13 +495,14 @@ Layout layout(int64_t batch, int n_heads, int n_kv, int head_dim, int64_t maxb, 
     const int64_t pairs = batch * n_kv;
     const int64_t target = 8ll * sms;
     int64_t spb = (maxb * pairs + target - 1) / target;
-    // at least 8 blocks per split (measured best at batch 1: 4 gives more partials to merge,
-    // 16 too few CTAs); QL_ATTN_MIN_SPB overrides the floor for A/B measurements
-    static const int64_t min_spb = [] {
+    // at least two blocks per warp of a CTA, so that a split's blocks are all staged from the
+    // start (4 warps and 8 blocks measured best at batch 1 among 4-warp splits of 4, 8 and 16
+    // blocks); QL_ATTN_MIN_SPB overrides the floor for A/B measurements
+    static const int env_spb = [] {
         const char* e = std::getenv("QL_ATTN_MIN_SPB");
-        const int v = e ? std::atoi(e) : 8;
-        return (int64_t)(v < 1 ? 1 : v > 256 ? 256 : v);
+        return e ? std::atoi(e) : 0;
     }();
+    const int64_t min_spb = env_spb > 0 ? (int64_t)(env_spb > 256 ? 256 : env_spb) : 2 * attn_warps(batch);
     if (spb < min_spb) spb = min_spb;
     if (spb > maxb) spb = maxb;
     if (spb < 1) spb = 1;
@@ -522,23 +525,30 @@ Layout layout(int64_t batch, int n_heads, int n_kv, int head_dim, int64_t maxb, 
 
 // Dynamic shared memory of one CTA: the warps' double-buffered K/V tiles, reused afterwards for
 // the warp-merge state and the split-merge weights.
-template <int HD, int G>
+template <int HD, int G, int NW>
 constexpr size_t attn_smem() {
-    const size_t tiles = (size_t)kAttnWarps * 4 * kBS * (HD * 2 + 16);
-    const size_t merge = (size_t)kAttnWarps * G * HD * 4;
+    const size_t tiles = (size_t)NW * 4 * kBS * (HD * 2 + 16);
+    const size_t merge = (size_t)NW * G * HD * 4;
     return tiles > merge ? tiles : merge;
 }
 
 template <int HD, int G>
 cudaError_t allow_attn_smem() {
-    return cudaFuncSetAttribute(attn_split_kernel<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)attn_smem<HD, G>());
+    cudaError_t e = cudaFuncSetAttribute(attn_split_kernel<HD, G, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)attn_smem<HD, G, 4>());
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(attn_split_kernel<HD, G, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)attn_smem<HD, G, 8>());
+    return e;
 }
 
 template <int HD, int G>
 cudaError_t launch_hg(const AParams& p, int batch, cudaStream_t s, bool pdl) {
     dim3 grid(p.nsplit, p.n_kv, batch);
-    return launch(attn_split_kernel<HD, G>, grid, dim3(kAttnThreads), attn_smem<HD, G>(), s, pdl, p,
+    if (attn_warps(batch) == 8)
+        return launch(attn_split_kernel<HD, G, 8>, grid, dim3(8 * 32), attn_smem<HD, G, 8>(), s, pdl, p,
+                      device_error_record());
+    return launch(attn_split_kernel<HD, G, 4>, grid, dim3(4 * 32), attn_smem<HD, G, 4>(), s, pdl, p,
                   device_error_record());
 }
 
@@ -725,7 +735,9 @@ int noalloc_scratch_address(void** out) {
 template <int HD, int G>
 cudaError_t launch_hg_err(const AParams& p, int batch, cudaStream_t s, DevError* err) {
     dim3 grid(p.nsplit, p.n_kv, batch);
-    return launch(attn_split_kernel<HD, G>, grid, dim3(kAttnThreads), attn_smem<HD, G>(), s, true, p, err);
+    if (attn_warps(batch) == 8)
+        return launch(attn_split_kernel<HD, G, 8>, grid, dim3(8 * 32), attn_smem<HD, G, 8>(), s, true, p, err);
+    return launch(attn_split_kernel<HD, G, 4>, grid, dim3(4 * 32), attn_smem<HD, G, 4>(), s, true, p, err);
 }
 
 template <int HD>
