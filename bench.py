@@ -453,7 +453,8 @@ def launch_phases(gm, sargs, s, cfg):
              "wait": r[:, 1].max() - r[:, 0].min(),
              "first_past_wait": (r[:, 1].min() - prev_end) if k > 0 else float("nan"),
              "stage": (r[:, 2] - r[:, 1]).mean(), "loop": (r[:, 3] - r[:, 2]).mean(),
-             "finish": (r[:, 5] - r[:, 3]).mean(), "tail": r[:, 5].max() - r[:, 5].mean(),
+             "finish": (r[:, 5] - r[:, 3]).mean(), "sync": (r[:, 4] - r[:, 3]).mean(),
+             "epilogue": (r[:, 5] - r[:, 4]).mean(), "tail": r[:, 5].max() - r[:, 5].mean(),
              "span": r[:, 5].max() - r[:, 0].min(),
              "ring_wait_frac": r[:, 6].sum() / max(r[:, 7].sum(), 1.0)}
         a = acc.setdefault(kinds[k], [])

@@ -210,12 +210,13 @@ __global__ void __launch_bounds__(NW * 32) attn_split_kernel(AParams p, DevError
             const __half* ksrc = p.k_pool + ((size_t)phys * p.n_kv + g) * kBS * HD;
             const __half* vsrc = p.v_pool + ((size_t)phys * p.n_kv + g) * kBS * HD;
             const uint32_t kd = wtiles_s + (uint32_t)((i & 1) * 2 * TILE), vd = kd + TILE;
+            const unsigned long long pol = l2_evict_first();   // the context is read once per step
             for (int c = lane; c < kBS * CHUNKS; c += 32) {
                 const int row = c / CHUNKS, col = c - row * CHUNKS;
-                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(kd + row * PITCH + col * 16),
-                             "l"(ksrc + row * HD + col * 8) : "memory");
-                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(vd + row * PITCH + col * 16),
-                             "l"(vsrc + row * HD + col * 8) : "memory");
+                asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(kd + row * PITCH + col * 16),
+                             "l"(ksrc + row * HD + col * 8), "l"(pol) : "memory");
+                asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(vd + row * PITCH + col * 16),
+                             "l"(vsrc + row * HD + col * 8), "l"(pol) : "memory");
             }
         }
         asm volatile("cp.async.commit_group;" ::: "memory");

@@ -102,8 +102,8 @@ __device__ __forceinline__ void bring_issue(BRing& r, const PMat& M, const Geo& 
         const uint8_t* src = M.stream + ((size_t)tile * G.nst + k) * kUnitBytes;
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mb), "r"(bytes) : "memory");
-        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                     ::"r"(dst), "l"(src), "r"(bytes), "r"(mb) : "memory");
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+                     ::"r"(dst), "l"(src), "r"(bytes), "r"(mb), "l"(l2_evict_first()) : "memory");
     }
     ++r.issued;
     r.u += n;
@@ -617,8 +617,8 @@ __device__ __forceinline__ void issue_tile(const BParams& p, const Geo& G, unsig
     const uint32_t dst = su32(codes + (size_t)b * kCodesBytes + (size_t)i * G.kwu * kUnitBytes);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mb), "r"(bytes) : "memory");
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                 ::"r"(dst), "l"(src), "r"(bytes), "r"(mb) : "memory");
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+                 ::"r"(dst), "l"(src), "r"(bytes), "r"(mb), "l"(l2_evict_first()) : "memory");
 }
 
 __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_constant__ BParams p) {

@@ -97,6 +97,14 @@ __device__ __forceinline__ void l2_prefetch_share(const void* base, size_t bytes
 #endif
 
 // An L2 prefetch request for the next kernel's weights (two ranges: codes and scales).
+// L2 policy for data read once per step (weights, the K/V context): evicted first, so that the
+// step's small reused data (activations, norm weights, tables, kernel code) stays in L2.
+__device__ __forceinline__ unsigned long long l2_evict_first() {
+    unsigned long long pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 struct NextWeights {
     const void* ptr[2];
     size_t bytes[2];

@@ -251,8 +251,8 @@ __device__ __forceinline__ void ring_issue(Ring& r, const PMat* mats, int warp, 
         // order this warp's earlier generic-proxy reads of the slot before the async-proxy write
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mb), "r"(bytes) : "memory");
-        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                     ::"r"(dst), "l"(r.src), "r"(bytes), "r"(mb) : "memory");
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+                     ::"r"(dst), "l"(r.src), "r"(bytes), "r"(mb), "l"(l2_evict_first()) : "memory");
     }
     r.src += (size_t)n * kUnitBytes;
     ++r.issued;
@@ -667,6 +667,7 @@ __device__ __noinline__ void gemv_phase(const PersistParams& p, const PMat* mats
             if (m && act) atomicMax(p.keys + tid, m);
         }
     }
+    if (tr != nullptr) __syncthreads();   // the stamp marks the end of every warp's epilogue
     stamp(tr, 5);
 }
 
