@@ -148,27 +148,7 @@ def graph_ms(fn, stream, reps: int, warm: int = 1) -> float:
 
 
 # ----------------------------------------------------------------------------- GPU arm
-def device_tensor_fn(cfg, seed: int):
-    """Seeded device-side weight draws with the pages' distributions (N(0,0.02) matrices,
-    1 + N(0,0.1) norm weights, N(0,0.02) f32 embedding)."""
-    import torch
-
-    names = ("attn_norm", "ffn_norm", "q_norm", "k_norm", "wqkv", "wo", "wgu", "wd")
-    shapes = {"attn_norm": (cfg.hidden,), "ffn_norm": (cfg.hidden,), "q_norm": (cfg.head_dim,),
-              "k_norm": (cfg.head_dim,), "wqkv": (cfg.qkv_rows, cfg.hidden),
-              "wo": (cfg.hidden, cfg.n_heads * cfg.head_dim), "wgu": (2 * cfg.intermediate, cfg.hidden),
-              "wd": (cfg.hidden, cfg.intermediate), "embed": (cfg.vocab, cfg.hidden),
-              "final_norm": (cfg.hidden,), "lm_head": (cfg.vocab, cfg.hidden)}
-
-    def fn(layer, name):
-        key = (seed * 1000003 + (0 if layer is None else layer + 1) * 101 + (names.index(name) if name in names else 50 + len(name))) & 0x7FFFFFFF
-        g = torch.Generator(device="cuda")
-        g.manual_seed(key)
-        t = torch.randn(shapes[name], generator=g, device="cuda", dtype=torch.float32)
-        if name.endswith("norm"):
-            return t.mul_(0.1).add_(1.0)
-        return t.mul_(0.02)
-    return fn
+device_tensor_fn = ql_inputs.device_tensor_fn
 
 
 def gpu_arm(args, rank, world, local_rank):

@@ -47,6 +47,25 @@ class Q4Model:
                 layer[n] = quantize(lw[n])
             self.layers.append(layer)
 
+    @classmethod
+    def from_codes(cls, cfg, layers: list, final_norm, lm_head, embed=None) -> "Q4Model":
+        """A model from existing q4_0 arrays (``(scales u16 [rows][cols/32], quants u8
+        [rows][cols/32][16])`` per matrix, the layout :func:`oracle.q4_0.quantize` returns),
+        e.g. codes made by another implementation of the same codec. ``embed`` may be None
+        when only :func:`decode_hidden` is used."""
+        self = cls.__new__(cls)
+        self.cfg = cfg
+        self.embed = None if embed is None else np.asarray(embed, dtype=np.float64)
+        self.final_norm = np.asarray(final_norm, dtype=np.float64)
+        self.lm_head = lm_head
+        self.layers = []
+        for lw in layers:
+            layer = {n: np.asarray(lw[n], dtype=np.float64) for n in ("attn_norm", "ffn_norm", "q_norm", "k_norm")}
+            for n in LAYER_MATRICES:
+                layer[n] = lw[n]
+            self.layers.append(layer)
+        return self
+
     @staticmethod
     def dense(q4) -> np.ndarray:
         return dequantize(*q4)
@@ -88,12 +107,19 @@ def decode_step(model: Q4Model, cache: KVCache, tokens, positions) -> np.ndarray
     must already hold that slot's context. The step writes K and V of position
     ``positions[b]`` into the cache.
     """
-    cfg = model.cfg
     tokens = np.asarray(tokens, dtype=np.int64)
+    hf = decode_hidden(model, cache, model.embed[tokens], positions)
+    return ops.gemv(model.dense(model.lm_head), hf)
+
+
+def decode_hidden(model: Q4Model, cache: KVCache, x, positions) -> np.ndarray:
+    """Steps 2 and the final RMSNorm of 3 for embedded tokens ``x`` ``[B, hidden]``: the
+    normalised final hidden state ``[B, hidden]`` that the lm_head multiplies (f64)."""
+    cfg = model.cfg
     positions = np.asarray(positions, dtype=np.int64)
-    B = tokens.shape[0]
+    x = np.array(x, dtype=np.float64)                               # [B, hidden]
+    B = x.shape[0]
     scale = 1.0 / np.sqrt(cfg.head_dim)
-    x = model.embed[tokens].copy()                                  # [B, hidden]
     for li, L in enumerate(model.layers):
         hn = ops.rmsnorm(x, L["attn_norm"], cfg.eps)
         y = ops.gemv(model.dense(L["wqkv"]), hn)
@@ -112,8 +138,21 @@ def decode_step(model: Q4Model, cache: KVCache, tokens, positions) -> np.ndarray
         gu = ops.gemv(model.dense(L["wgu"]), hn)
         act = ops.swiglu(gu[:, : cfg.intermediate], gu[:, cfg.intermediate:])
         x = x + ops.gemv(model.dense(L["wd"]), act)
-    hf = ops.rmsnorm(x, model.final_norm, cfg.eps)
-    return ops.gemv(model.dense(model.lm_head), hf)
+    return ops.rmsnorm(x, model.final_norm, cfg.eps)
+
+
+def logits_by_rows(lm_head, hf, rows_per_chunk: int = 8192) -> np.ndarray:
+    """``W_lm hf`` for a q4_0 lm_head dequantised ``rows_per_chunk`` rows at a time (each
+    logit is the same dot product as in :func:`decode_step`; only the memory differs):
+    ``[B, vocab]`` f64."""
+    scales, quants = lm_head
+    rows = scales.shape[0]
+    hf = np.asarray(hf, dtype=np.float64)
+    out = np.empty((hf.shape[0], rows))
+    for r0 in range(0, rows, rows_per_chunk):
+        r1 = min(rows, r0 + rows_per_chunk)
+        out[:, r0:r1] = ops.gemv(dequantize(scales[r0:r1], quants[r0:r1]), hf)
+    return out
 
 
 def forward_full(model: Q4Model, tokens, k_ctx=None, v_ctx=None) -> np.ndarray:

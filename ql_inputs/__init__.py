@@ -29,7 +29,7 @@ __all__ = [
     "Config", "TINY", "QWEN3_8B", "qwen3_8b_layers",
     "weights", "prompt_tokens", "kv_context", "fragmented_block_ids",
     "gemv_weight", "gemv_activations", "attention_case", "batched_lengths",
-    "GEMV_SHAPES", "sub_rng",
+    "GEMV_SHAPES", "sub_rng", "device_tensor_fn",
 ]
 
 
@@ -126,6 +126,32 @@ def weights(cfg: Config, seed: int = 0) -> dict:
     for li in range(cfg.n_layers):
         w["layers"].append({n: layer_tensor(cfg, seed, li, n) for n in _LAYER_TENSORS})
     return w
+
+
+def device_tensor_fn(cfg: Config, seed: int):
+    """Seeded draws of a model's tensors on the GPU (torch generators), with the same
+    distributions as :func:`weights` (N(0, 0.02) matrices and embedding, 1 + N(0, 0.1) norm
+    weights), one tensor at a time: ``fn(layer or None, name) -> f32 CUDA tensor``. For shapes
+    too large to draw on the host; the values differ from :func:`weights`."""
+    import torch
+
+    names = ("attn_norm", "ffn_norm", "q_norm", "k_norm", "wqkv", "wo", "wgu", "wd")
+    shapes = {"attn_norm": (cfg.hidden,), "ffn_norm": (cfg.hidden,), "q_norm": (cfg.head_dim,),
+              "k_norm": (cfg.head_dim,), "wqkv": (cfg.qkv_rows, cfg.hidden),
+              "wo": (cfg.hidden, cfg.n_heads * cfg.head_dim), "wgu": (2 * cfg.intermediate, cfg.hidden),
+              "wd": (cfg.hidden, cfg.intermediate), "embed": (cfg.vocab, cfg.hidden),
+              "final_norm": (cfg.hidden,), "lm_head": (cfg.vocab, cfg.hidden)}
+
+    def fn(layer, name):
+        key = (seed * 1000003 + (0 if layer is None else layer + 1) * 101
+               + (names.index(name) if name in names else 50 + len(name))) & 0x7FFFFFFF
+        g = torch.Generator(device="cuda")
+        g.manual_seed(key)
+        t = torch.randn(shapes[name], generator=g, device="cuda", dtype=torch.float32)
+        if name.endswith("norm"):
+            return t.mul_(0.1).add_(1.0)
+        return t.mul_(0.02)
+    return fn
 
 
 def prompt_tokens(n: int, vocab: int, seed: int = 1) -> np.ndarray:

@@ -112,3 +112,20 @@ def test_block_pool_rule():
     with pytest.raises(PoolExhausted):
         p.alloc()
     assert p.in_use() == 3
+
+
+def test_hidden_and_chunked_head_equal_the_step():
+    """decode_step = lm_head x decode_hidden, and the lm_head taken in row chunks gives the
+    same logits (each is the same dot product); a model rebuilt from its own codes
+    (Q4Model.from_codes) decodes identically."""
+    cfg = ql_inputs.TINY
+    w = ql_inputs.weights(cfg, seed=0)
+    m = decode.Q4Model(cfg, w)
+    toks = ql_inputs.prompt_tokens(3, cfg.vocab, seed=9)
+    c1, c2 = decode.KVCache(cfg, 3, 8), decode.KVCache(cfg, 3, 8)
+    want = decode.decode_step(m, c1, toks, [0, 0, 0])
+    m2 = decode.Q4Model.from_codes(cfg, [{k: L[k] for k in L} for L in m.layers], m.final_norm, m.lm_head)
+    hf = decode.decode_hidden(m2, c2, m.embed[toks], [0, 0, 0])
+    got = decode.logits_by_rows(m2.lm_head, hf, rows_per_chunk=100)
+    assert np.array_equal(c1.k, c2.k) and np.array_equal(c1.v, c2.v)
+    assert np.allclose(got, want, rtol=0, atol=1e-12)
