@@ -422,7 +422,7 @@ __global__ void __launch_bounds__(kT, 1) gemv_batched_kernel(const __grid_consta
             for (int w2 = 0; w2 <= warp; ++w2) {
                 const int a2 = persist::warp_unit<kW>(U, w2), b2 = persist::warp_unit<kW>(U, w2 + 1);
                 if (b2 <= a2 || b2 <= ts || a2 >= ts + G.kwu) continue;
-                const int sl = (a2 / G.kwu == tl_first) ? 0 : 1;
+                const int sl = a2 >= ts ? 0 : 1;   // begun in this tile: parked as that warp's first
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     const float4 v = part[((w2 * 2 + sl) * NT + nt) * 32 + lane];

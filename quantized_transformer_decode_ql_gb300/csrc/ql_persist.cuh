@@ -640,7 +640,7 @@ __device__ __noinline__ void gemv_phase(const PersistParams& p, const PMat* mats
             for (int w2 = 0; w2 <= warp; ++w2) {
                 const int a0 = warp_unit<W>(U, w2), a1 = warp_unit<W>(U, w2 + 1);
                 if (a1 <= a0 || a1 <= ts || a0 >= ts + nst) continue;
-                const int sl = (T0 + a0 / nst == first_tile) ? 0 : 1;
+                const int sl = a0 >= ts ? 0 : 1;   // begun in this tile: parked as that warp's first
                 const float4 v = part[(w2 * 2 + sl) * 32 + lane];
                 s2[0] += v.x;
                 if (NB > 1) s2[NB > 1 ? 1 : 0] += v.y;
