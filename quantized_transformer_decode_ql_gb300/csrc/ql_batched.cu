@@ -145,7 +145,7 @@ __device__ void stage_window(const BParams& p, const Geo& G, int w, uint4* xs) {
         for (int r = 0; r < kChunk; ++r) {
             const int item = base + r * kT + tid;
             if (item < nitems) {
-                const int t = item & 3, cj = item >> 2, c = cj / nb, j = cj - c * nb;
+                const int t = item & 3, cj = item >> 2, c = nb == 32 ? cj >> 5 : cj / nb, j = cj - c * nb;
                 const size_t off = (size_t)c * cols + 32 * (j0 + j) + 4 * t;
                 ha[r] = __ldcg(reinterpret_cast<const uint2*>(p.x16 + off));
                 hh[r] = __ldcg(reinterpret_cast<const uint2*>(p.x16 + off + 16));
@@ -155,7 +155,7 @@ __device__ void stage_window(const BParams& p, const Geo& G, int w, uint4* xs) {
         for (int r = 0; r < kChunk; ++r) {
             const int item = base + r * kT + tid;
             if (item >= nitems) break;
-            const int t = item & 3, cj = item >> 2, c = cj / nb, j = cj - c * nb;
+            const int t = item & 3, cj = item >> 2, c = nb == 32 ? cj >> 5 : cj / nb, j = cj - c * nb;
             // elements 4t..4t+3 (ha) and 16+4t.. (hh): pairs (x0, x2), (x1, x3), (x16, x18)/16, (x17, x19)/16
             const float2 f0 = __half22float2(as_h2(ha[r].x)), f1 = __half22float2(as_h2(ha[r].y));
             const float2 f2 = __half22float2(as_h2(hh[r].x)), f3 = __half22float2(as_h2(hh[r].y));
@@ -216,8 +216,10 @@ __global__ void __launch_bounds__(kMergeT) merge_kernel(const __grid_constant__ 
     float* yf = static_cast<float*>(p.y);
     const long long nitems = (long long)nrows * c8n;
     for (long long i = blockIdx.x * (long long)kMergeT + threadIdx.x; i < nitems; i += (long long)gridDim.x * kMergeT) {
-        const int c8 = (int)(i / nrows), lr = (int)(i - (long long)c8 * nrows);
-        const int tile = lr / rpt, r = lr - tile * rpt;
+        // (no divisions: at most 4 column groups, 8 or 16 rows per tile)
+        const int c8 = i < nrows ? 0 : i < 2ll * nrows ? 1 : i < 3ll * nrows ? 2 : 3;
+        const int lr = (int)(i - (long long)c8 * nrows);
+        const int tile = silu ? lr >> 3 : lr >> 4, r = lr - tile * rpt;
         const int row = tile * rpt + r;
         if (row >= lim) continue;
         const float4* q = part + ((size_t)tile * 16 + r) * (kMaxCols / 4) + 2 * c8;
@@ -577,7 +579,8 @@ __device__ void stage_b(const BParams& p, const Geo& G, unsigned char* bsm, int 
 #pragma unroll
         for (int r = 0; r < kChunk; ++r) {
             const int item = base + r * nthreads + tid;
-            const int cl = item & 7, t = (item >> 3) & 3, rest = item >> 5, j = rest % nb, c = (rest / nb) * 8 + cl;
+            const int cl = item & 7, t = (item >> 3) & 3, rest = item >> 5;
+            const int cg0 = nb == 32 ? rest >> 5 : rest / nb, j = rest - cg0 * nb, c = cg0 * 8 + cl;
             if (item < nitems && c < p.B) {
                 const size_t off = (size_t)c * cols + 32 * (j0 + j) + 4 * t;
                 ha[r] = __ldcg(reinterpret_cast<const uint2*>(p.x16 + off));
@@ -590,7 +593,8 @@ __device__ void stage_b(const BParams& p, const Geo& G, unsigned char* bsm, int 
         for (int r = 0; r < kChunk; ++r) {
             const int item = base + r * nthreads + tid;
             if (item >= nitems) break;
-            const int cl = item & 7, t = (item >> 3) & 3, rest = item >> 5, j = rest % nb, cg = rest / nb;
+            const int cl = item & 7, t = (item >> 3) & 3, rest = item >> 5;
+            const int cg = nb == 32 ? rest >> 5 : rest / nb, j = rest - cg * nb;
             const float2 f0 = __half22float2(as_h2(ha[r].x)), f1 = __half22float2(as_h2(ha[r].y));
             const float2 f2 = __half22float2(as_h2(hh[r].x)), f3 = __half22float2(as_h2(hh[r].y));
             const __half2 p0 = __floats2half2_rn(f0.x, f1.x);

@@ -316,7 +316,7 @@ __device__ __noinline__ void stage_x(const PersistParams& p, int nblk, int cstri
     auto where = [&](int item, int& b, int& j, int& t) -> size_t {
         t = item & 3;
         const int bj = item >> 2;
-        b = bj / nblk;
+        b = bj < nblk ? 0 : (bj < 2 * nblk ? 1 : bj / nblk);   // batches of 1-2: no division
         j = bj - b * nblk;
         return (size_t)b * cols + 32 * j + 4 * t;
     };
