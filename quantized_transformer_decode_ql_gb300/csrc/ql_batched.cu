@@ -90,7 +90,7 @@ struct BRing {
 };
 __device__ __forceinline__ void bring_issue(BRing& r, const PMat& M, const Geo& G, int lane) {
     if (r.u >= r.b || r.dead) return;
-    const int tl = r.u / G.kwu, kk = r.u - tl * G.kwu;
+    const int tl = G.kwu == 8 ? r.u >> 3 : r.u / G.kwu, kk = r.u - tl * G.kwu;
     int n = r.b - r.u;
     n = n < kSlotUnits ? n : kSlotUnits;
     n = n < G.kwu - kk ? n : G.kwu - kk;
@@ -332,7 +332,7 @@ __global__ void __launch_bounds__(kT, 1) gemv_batched_kernel(const __grid_consta
     bool first_parked = false, last_parked = false;
 #pragma unroll 1
     for (int u = a; u < b;) {
-        const int tl = u / G.kwu, kk = u - tl * G.kwu;
+        const int tl = G.kwu == 8 ? u >> 3 : u / G.kwu, kk = u - tl * G.kwu;
         int n = b - u;
         n = n < kSlotUnits ? n : kSlotUnits;
         n = n < G.kwu - kk ? n : G.kwu - kk;
@@ -379,7 +379,7 @@ __global__ void __launch_bounds__(kT, 1) gemv_batched_kernel(const __grid_consta
         if (!r.dead) ++r.consumed;   // after a timeout the drain below still waits for this copy
         bring_issue(r, M, G, lane);   // refill the slot just read
         u += n;
-        if (u == b || u % G.kwu == 0) {
+        if (u == b || kk + n == G.kwu) {   // the end of this warp's part of the tile
             // end of this warp's part of tile tl: write it if the warp had all of the tile's
             // units of the window, else keep it for the reduction below (first or last tile)
             const int ts = tl * G.kwu;

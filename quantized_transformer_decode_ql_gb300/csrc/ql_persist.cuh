@@ -532,7 +532,8 @@ __device__ __noinline__ void gemv_phase(const PersistParams& p, const PMat* mats
         best[b] = 0ull;
         acc[b] = 0.f;
     }
-    int tile = T0 + (u1 > u0 ? u0 / nst : 0), k = u1 > u0 ? u0 % nst : 0;
+    const int q0 = u1 > u0 ? (nst == 32 ? u0 >> 5 : u0 / nst) : 0;   // 4096-column matrices: a shift
+    int tile = T0 + q0, k = u1 > u0 ? u0 - q0 * nst : 0;
     const int first_tile = tile;
 
     // this lane's share of one unit (group kk of the tile): sum over blocks 2h, 2h + 1 of row r
