@@ -187,6 +187,30 @@ int ql_paged_attn_decode_noalloc(const void* d_q, const void* d_k_pool, const vo
                                  int block_size, int64_t max_blocks_per_seq, int64_t num_blocks,
                                  float scale, void* d_out, void* stream);
 
+/* How the context splits of a (sequence, kv head) are merged, for this process (every
+ * attention entry point and the decode step; graphs keep the form they were captured with).
+ * Both forms take the same online-softmax merge over the splits in order, so their outputs
+ * are bit-identical ([FK] split-K flash-decode reduce, [IL] attn_reduce):
+ *   QL_ATTN_MERGE_TICKET  (default) each split writes its partial to the workspace and the
+ *                         last one to take an atomic ticket merges them all; the others exit
+ *                         at once, freeing their SMs for the next kernel.
+ *   QL_ATTN_MERGE_CLUSTER the splits are one thread-block cluster; each keeps its
+ *                         partial in shared memory and, after a cluster barrier, merges a
+ *                         slice of the outputs from the others' partials through distributed
+ *                         shared memory. Used at batch 1-2 with 2..16 splits when the device
+ *                         can hold every cluster of the launch at once; otherwise the ticket.
+ *                         Every split then lives until the merge ends (slower in the decode
+ *                         step: the next kernel's CTAs wait for those SMs).
+ * The initial form is QL_ATTN_MERGE_CLUSTER when the environment sets QL_ATTN_MERGE=1.
+ * Returns the previous form, or QL_EINVAL for an unknown one.                              */
+enum { QL_ATTN_MERGE_TICKET = 0, QL_ATTN_MERGE_CLUSTER = 1 };
+int ql_set_attn_merge_form(int form);
+/* The merge form an attention launch of this shape takes on the current device under the
+ * current setting (QL_ATTN_MERGE_TICKET or QL_ATTN_MERGE_CLUSTER), or a negative QL_E* code
+ * (QL_EINVAL for a shape the attention rejects).                                           */
+int ql_paged_attn_merge_form(int64_t batch, int n_heads, int n_kv_heads, int head_dim,
+                             int64_t max_blocks_per_seq);
+
 /* --------------------------------------------------------------- qk-norm + RoPE + KV append
  * [IL] CudaQwen3::step (qk_norm_rope kernel), [FK] decode_step / attention_paged:
  * for slot b at position p = d_positions[b]:

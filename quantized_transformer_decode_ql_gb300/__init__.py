@@ -14,6 +14,7 @@ from ._lib import (QLError, QL_OK, QL_EINVAL, QL_ENOMEM, QL_ECUDA, QL_EPOOL, QL_
                    QL_EPI_ADD_RESIDUAL, QL_EPI_SILU_MUL, QL_STEP_AUTO, QL_STEP_LAUNCHES,
                    QL_STEP_PERSISTENT, QL_OPT_STEP_KERNEL, QL_OPT_BARRIER_TIMEOUT_NS,
                    QL_OPT_TEST_BARRIER_EXTRA, QL_OPT_STEP_TRACE, QL_BATCHED_MMA_SYNC, QL_BATCHED_TCGEN05,
+                   QL_ATTN_MERGE_TICKET, QL_ATTN_MERGE_CLUSTER,
                    Q4Matrix, LayerDesc, ModelDesc,
                    StepArgs, SIGNATURES, LIB_PATH, lib, check, ptr, stream_ptr)
 
@@ -22,6 +23,7 @@ __all__ = [
     "ql_q4_0_stream_bytes", "ql_q4_0_stream_pack", "ql_gemv_q4_0_stream",
     "ql_gemv_q4_0_stream_workspace_bytes", "ql_set_batched_gemv_form",
     "ql_paged_attn_workspace_bytes", "ql_paged_attn_decode", "ql_paged_attn_decode_noalloc",
+    "ql_set_attn_merge_form", "ql_paged_attn_merge_form",
     "ql_fused_norm_rope",
     "ql_rope_tables", "ql_check_device_error", "BlockPool", "SIGNATURES",
 ]
@@ -64,6 +66,22 @@ def ql_gemv_q4_0_stream_workspace_bytes(rows, cols, silu=0):
 def ql_set_batched_gemv_form(form):
     """Tensor-core form of the batch 3-32 GEMV for this process; returns the previous form."""
     rc = int(lib().ql_set_batched_gemv_form(form))
+    if rc < 0:
+        check(rc)
+    return rc
+
+
+def ql_set_attn_merge_form(form):
+    """How attention merges its context splits, for this process; returns the previous form."""
+    rc = int(lib().ql_set_attn_merge_form(form))
+    if rc < 0:
+        check(rc)
+    return rc
+
+
+def ql_paged_attn_merge_form(batch, n_heads, n_kv_heads, head_dim, max_blocks_per_seq):
+    """The merge form an attention launch of this shape takes on the current device."""
+    rc = int(lib().ql_paged_attn_merge_form(batch, n_heads, n_kv_heads, head_dim, max_blocks_per_seq))
     if rc < 0:
         check(rc)
     return rc

@@ -19,6 +19,7 @@ QL_EPI_NONE, QL_EPI_ADD_RESIDUAL, QL_EPI_SILU_MUL = 0, 1, 2
 QL_STEP_AUTO, QL_STEP_LAUNCHES, QL_STEP_PERSISTENT = 0, 1, 2
 QL_OPT_STEP_KERNEL, QL_OPT_BARRIER_TIMEOUT_NS, QL_OPT_TEST_BARRIER_EXTRA, QL_OPT_STEP_TRACE = 1, 2, 3, 4
 QL_BATCHED_MMA_SYNC, QL_BATCHED_TCGEN05 = 0, 1
+QL_ATTN_MERGE_TICKET, QL_ATTN_MERGE_CLUSTER = 0, 1
 
 
 class QLError(RuntimeError):
@@ -76,6 +77,8 @@ SIGNATURES = {
     "ql_paged_attn_decode_noalloc": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                              c_int64, c_int, c_int, c_int, c_int, c_int64, c_int64,
                                              c_float, c_void_p, c_void_p]),
+    "ql_set_attn_merge_form": (c_int, [c_int]),
+    "ql_paged_attn_merge_form": (c_int, [c_int64, c_int, c_int, c_int, c_int64]),
     "ql_fused_norm_rope": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                    c_void_p, c_float, c_int64, c_int, c_int, c_int, c_void_p,
                                    c_void_p, c_void_p, c_void_p, c_int64, c_int, c_int64, c_int64,

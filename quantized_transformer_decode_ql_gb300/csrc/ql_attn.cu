@@ -7,23 +7,29 @@
 //
 // out[b][h] = sum_t softmax_t(q[b][h] . k[g][t] * scale) v[g][t], g = h / (n_heads / n_kv).
 //
-// Design (GB300): one CTA per (split, kv head, sequence), 4 warps. The CTA handles the whole
-// GQA group of its kv head, so each K/V byte is read from HBM once and used by all G query
-// heads. A warp takes one 16-token block at a time:
-//  * scores: lane (t, half) = (lane & 15, lane >> 4) dots key t's half of head_dim against the
-//    G queries (staged once in shared memory as f32), halves combined with one shuffle;
-//  * online softmax per head in the exp2 domain (scores pre-scaled by scale * log2 e);
-//  * P.V: lane owns head_dim/32 output dims of every head; probabilities go through a tiny
-//    per-warp shared buffer (one broadcast load per key); V rows are read with coalesced
-//    8-byte loads (256 contiguous bytes per key per warp at head_dim 128).
-// The 4 warps' states are merged in shared memory; with one split the CTA writes the output,
-// otherwise it writes its (m, l, acc) partial and the last CTA of its (sequence, kv head) -
-// found with an atomic ticket, no waiting - merges all partials and re-arms the ticket.
+// Design (GB300): one CTA per (split, kv head, sequence), 8 warps at batch 1-2, else 4. The CTA
+// handles the whole GQA group of its kv head, so each K/V byte is read from HBM once and used
+// by all G query heads. A warp takes 16-token blocks in turn, staged in shared memory with
+// cp.async (double-buffered); S = Q K^T and O += P V run on mma.sync (ldmatrix, .trans for V)
+// with an online softmax in the exp2 domain (scores pre-scaled by scale * log2 e). The warps'
+// states are merged in shared memory; with one split the CTA writes the output. Otherwise the
+// splits are merged in one of two forms:
+//  * ticket (default): each CTA writes its partial to global memory, and the last CTA of its
+//    (sequence, kv head) - found with an atomic ticket, no waiting - merges all partials and
+//    re-arms the ticket. Most CTAs exit right after their ticket, so the next kernel's CTAs
+//    find their SMs free early;
+//  * cluster (selectable; batch 1-2, up to 16 splits, when the device can hold one cluster per
+//    (sequence, kv head) at once): the splits of a (sequence, kv head) are one thread-block
+//    cluster; each CTA keeps its (m, l, acc) partial in shared memory, and after a cluster
+//    barrier every CTA merges a slice of the outputs, reading the others' partials through
+//    distributed shared memory; a second barrier keeps the partials alive until all reads are
+//    done. Every CTA then lives until the merge ends, and the decode step measured slower.
 #include <cuda_fp16.h>
 #include <math.h>
 
+#include <atomic>
 #include <cstdlib>
-
+#include <map>
 #include <mutex>
 #include <set>
 
@@ -150,7 +156,32 @@ __device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1,
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-template <int HD, int G, int NW>
+// Thread-block cluster primitives (PTX): a full cluster barrier (every thread of every CTA
+// arrives; release/acquire order the shared-memory partials), the cluster address of a shared
+// variable in the CTA of rank r, and loads through it.
+__device__ __forceinline__ void cluster_barrier() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t cta_addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(cta_addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr) : "memory");
+    return v;
+}
+
+// CL: the splits of a (sequence, kv head) form one cluster (grid x = cluster x = nsplit) and are
+// merged through distributed shared memory; otherwise by the ticket.
+template <int HD, int G, int NW, bool CL>
 __global__ void __launch_bounds__(NW * 32) attn_split_kernel(AParams p, DevError* err) {
     constexpr int kAttnWarps = NW, kAttnThreads = NW * 32;
     constexpr int KSTEPS = HD / 16;           // k-steps of the Q.K^T MMA
@@ -189,7 +220,15 @@ __global__ void __launch_bounds__(NW * 32) attn_split_kernel(AParams p, DevError
     }
     const int nblocks = (L + kBS - 1) / kBS;
     const int n_active = (nblocks + p.spb - 1) / p.spb;
-    if (s >= n_active) return;
+    if (s >= n_active) {
+        // an idle split of a cluster still takes part in both of its barriers (the decision is
+        // the same in every CTA of the cluster: one (sequence, kv head), one n_active)
+        if (CL && n_active > 1) {
+            cluster_barrier();
+            cluster_barrier();
+        }
+        return;
+    }
     const int blk0 = s * p.spb;
     const int blk1 = min(nblocks, blk0 + p.spb);
     const int pos = L - 1, lblk = pos / kBS, kp = pos % kBS;
@@ -399,6 +438,10 @@ __global__ void __launch_bounds__(NW * 32) attn_split_kernel(AParams p, DevError
     __syncthreads();
 
     const int n_heads = p.n_heads;
+    // the cluster form's partial of this split, after the warp-merge state: acc [G][HD], m, l [G]
+    float* cacc = wacc + kAttnWarps * G * HD;
+    float* cm = cacc + G * HD;
+    float* cl = cm + G;
     for (int i = threadIdx.x; i < G * HD; i += kAttnThreads) {
         const int h = i / HD, d = i - h * HD;
         float M = -INFINITY;
@@ -414,6 +457,12 @@ __global__ void __launch_bounds__(NW * 32) attn_split_kernel(AParams p, DevError
         const int hg = g * G + h;
         if (n_active == 1) {
             p.out[((size_t)b * n_heads + hg) * HD + d] = __float2half_rn(A / Ls);
+        } else if (CL) {
+            cacc[i] = A;
+            if (d == 0) {
+                cm[h] = M;
+                cl[h] = Ls;
+            }
         } else {
             const size_t slot = ((size_t)b * n_heads + hg) * p.nsplit + s;
             p.pacc[slot * HD + d] = A;
@@ -425,6 +474,56 @@ __global__ void __launch_bounds__(NW * 32) attn_split_kernel(AParams p, DevError
     }
     if (n_active == 1) {
         attn_stamp(tr, 4);
+        attn_stamp(tr, 5);
+        return;
+    }
+    if (CL) {
+        cluster_barrier();   // every split's partial is in its CTA's shared memory
+        attn_stamp(tr, 4);
+        // this CTA merges float4 outputs [s * per, s * per + per) of the group's G * HD / 4,
+        // over the splits in order (the ticket form's arithmetic and order)
+        constexpr int N4 = G * HD / 4, kMergeSplits = 8;
+        const int per = (N4 + n_active - 1) / n_active;
+        const uint32_t acc_s = static_cast<uint32_t>(__cvta_generic_to_shared(cacc));
+        const uint32_t m_s = static_cast<uint32_t>(__cvta_generic_to_shared(cm));
+        const uint32_t l_s = static_cast<uint32_t>(__cvta_generic_to_shared(cl));
+        for (int j = threadIdx.x; j < per; j += kAttnThreads) {
+            const int i = s * per + j;
+            if (i >= N4) break;
+            const int h = i / (HD / 4), d4 = i - h * (HD / 4);
+            float M = -INFINITY, Ls = 0.f;
+            float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int k0 = 0; k0 < n_active; k0 += kMergeSplits) {
+                float mk[kMergeSplits], lk[kMergeSplits];
+                float4 ak[kMergeSplits];
+#pragma unroll
+                for (int u = 0; u < kMergeSplits; ++u) {
+                    if (k0 + u < n_active) {
+                        const uint32_t r = (uint32_t)(k0 + u);   // split k is cluster rank k
+                        mk[u] = ld_cluster_f32(cluster_addr(m_s + 4u * h, r));
+                        lk[u] = ld_cluster_f32(cluster_addr(l_s + 4u * h, r));
+                        ak[u] = ld_cluster_f32x4(cluster_addr(acc_s + 16u * (uint32_t)i, r));
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kMergeSplits; ++u) {
+                    if (k0 + u < n_active && mk[u] != -INFINITY) {
+                        const float mn = fmaxf(M, mk[u]);
+                        const float fo = exp2f(M - mn), fk = exp2f(mk[u] - mn);
+                        Ls = Ls * fo + lk[u] * fk;
+                        A.x = A.x * fo + ak[u].x * fk; A.y = A.y * fo + ak[u].y * fk;
+                        A.z = A.z * fo + ak[u].z * fk; A.w = A.w * fo + ak[u].w * fk;
+                        M = mn;
+                    }
+                }
+            }
+            const float inv = 1.0f / Ls;
+            __half* o = p.out + ((size_t)b * n_heads + g * G + h) * HD + d4 * 4;
+            *reinterpret_cast<__half2*>(o) = __floats2half2_rn(A.x * inv, A.y * inv);
+            *reinterpret_cast<__half2*>(o + 2) = __floats2half2_rn(A.z * inv, A.w * inv);
+        }
+        cluster_barrier();   // the other CTAs are done reading this CTA's partial
+        if (tr != nullptr && threadIdx.x == 0) tr[6] = 1;
         attn_stamp(tr, 5);
         return;
     }
@@ -525,41 +624,126 @@ Layout layout(int64_t batch, int n_heads, int n_kv, int head_dim, int64_t maxb, 
 }
 
 // Dynamic shared memory of one CTA: the warps' double-buffered K/V tiles, reused afterwards for
-// the warp-merge state and the split-merge weights.
+// the warp-merge state and the cluster form's split partial.
 template <int HD, int G, int NW>
 constexpr size_t attn_smem() {
     const size_t tiles = (size_t)NW * 4 * kBS * (HD * 2 + 16);
-    const size_t merge = (size_t)NW * G * HD * 4;
+    const size_t merge = (size_t)NW * G * HD * 4 + (size_t)G * HD * 4 + 2 * G * 4;
     return tiles > merge ? tiles : merge;
 }
 
+constexpr int kMaxCluster = 16;   // splits merged through a cluster (the non-portable maximum)
+
+// Per device: how many clusters of each size (2..16) of the cluster-form kernel can be resident
+// at once, by (head_dim 64 | 128, G = 1, 2, 4, 8); filled by attn_prepare.
+struct ClusterFit {
+    int n[2][4][kMaxCluster + 1];
+};
+std::mutex g_fit_mu;
+std::map<int, ClusterFit> g_fit;
+std::atomic<int> g_attn_merge{-1};   // QL_ATTN_MERGE_TICKET / _CLUSTER; -1: from the environment
+
+int attn_merge_form() {
+    int f = g_attn_merge.load();
+    if (f < 0) {
+        const char* e = std::getenv("QL_ATTN_MERGE");
+        f = (e != nullptr && std::atoi(e) == QL_ATTN_MERGE_CLUSTER) ? QL_ATTN_MERGE_CLUSTER : QL_ATTN_MERGE_TICKET;
+        int expect = -1;
+        g_attn_merge.compare_exchange_strong(expect, f);
+        f = g_attn_merge.load();
+    }
+    return f;
+}
+
+constexpr int g_index(int G) { return G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3; }
+
 template <int HD, int G>
-cudaError_t allow_attn_smem() {
-    cudaError_t e = cudaFuncSetAttribute(attn_split_kernel<HD, G, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)attn_smem<HD, G, 4>());
+cudaError_t allow_attn_smem(ClusterFit& fit) {
+    cudaError_t e = cudaFuncSetAttribute(attn_split_kernel<HD, G, 4, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)attn_smem<HD, G, 4>());
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(attn_split_kernel<HD, G, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(attn_split_kernel<HD, G, 8, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)attn_smem<HD, G, 8>());
-    return e;
+    auto* kcl = attn_split_kernel<HD, G, 8, true>;
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kcl, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)attn_smem<HD, G, 8>());
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kcl, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    int* n = fit.n[HD == 64 ? 0 : 1][g_index(G)];
+    for (int c = 0; c <= kMaxCluster; ++c) n[c] = 0;
+    for (int c = 2; c <= kMaxCluster; ++c) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(c, 1, 1);
+        cfg.blockDim = dim3(8 * 32);
+        cfg.dynamicSmemBytes = attn_smem<HD, G, 8>();
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = c;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int k = 0;
+        if (cudaOccupancyMaxActiveClusters(&k, kcl, &cfg) != cudaSuccess) {
+            (void)cudaGetLastError();   // a size the device cannot form: no cluster of it
+            k = 0;
+        }
+        n[c] = k;
+    }
+    return cudaSuccess;
+}
+
+// The cluster form applies at batch 1-2 (8 warps) with 2..16 splits, when every (sequence, kv
+// head) of the launch can hold its cluster at the same time.
+bool use_cluster(int HD, int G, int nsplit, int n_kv, int batch) {
+    if (attn_warps(batch) != 8 || nsplit < 2 || nsplit > kMaxCluster) return false;
+    if (attn_merge_form() != QL_ATTN_MERGE_CLUSTER) return false;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    std::lock_guard<std::mutex> lk(g_fit_mu);
+    auto it = g_fit.find(dev);
+    if (it == g_fit.end()) return false;
+    return it->second.n[HD == 64 ? 0 : 1][g_index(G)][nsplit] >= n_kv * batch;
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                           bool pdl, unsigned int cx, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cx;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 template <int HD, int G>
-cudaError_t launch_hg(const AParams& p, int batch, cudaStream_t s, bool pdl) {
+cudaError_t launch_hg(const AParams& p, int batch, cudaStream_t s, bool pdl, DevError* err) {
     dim3 grid(p.nsplit, p.n_kv, batch);
+    if (use_cluster(HD, G, p.nsplit, p.n_kv, batch))
+        return launch_cluster(attn_split_kernel<HD, G, 8, true>, grid, dim3(8 * 32), attn_smem<HD, G, 8>(), s, pdl,
+                              (unsigned int)p.nsplit, p, err);
     if (attn_warps(batch) == 8)
-        return launch(attn_split_kernel<HD, G, 8>, grid, dim3(8 * 32), attn_smem<HD, G, 8>(), s, pdl, p,
-                      device_error_record());
-    return launch(attn_split_kernel<HD, G, 4>, grid, dim3(4 * 32), attn_smem<HD, G, 4>(), s, pdl, p,
-                  device_error_record());
+        return launch(attn_split_kernel<HD, G, 8, false>, grid, dim3(8 * 32), attn_smem<HD, G, 8>(), s, pdl, p, err);
+    return launch(attn_split_kernel<HD, G, 4, false>, grid, dim3(4 * 32), attn_smem<HD, G, 4>(), s, pdl, p, err);
 }
 
 template <int HD>
-cudaError_t launch_h(const AParams& p, int G, int batch, cudaStream_t s, bool pdl) {
+cudaError_t launch_h(const AParams& p, int G, int batch, cudaStream_t s, bool pdl, DevError* err) {
     switch (G) {
-        case 1: return launch_hg<HD, 1>(p, batch, s, pdl);
-        case 2: return launch_hg<HD, 2>(p, batch, s, pdl);
-        case 4: return launch_hg<HD, 4>(p, batch, s, pdl);
-        case 8: return launch_hg<HD, 8>(p, batch, s, pdl);
+        case 1: return launch_hg<HD, 1>(p, batch, s, pdl, err);
+        case 2: return launch_hg<HD, 2>(p, batch, s, pdl, err);
+        case 4: return launch_hg<HD, 4>(p, batch, s, pdl, err);
+        case 8: return launch_hg<HD, 8>(p, batch, s, pdl, err);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -574,15 +758,20 @@ int attn_prepare() {
     QL_TRY_CUDA(cudaGetDevice(&dev));
     std::lock_guard<std::mutex> lk(mu);
     if (done.count(dev)) return QL_OK;
-    cudaError_t e = allow_attn_smem<128, 1>();
-    if (e == cudaSuccess) e = allow_attn_smem<128, 2>();
-    if (e == cudaSuccess) e = allow_attn_smem<128, 4>();
-    if (e == cudaSuccess) e = allow_attn_smem<128, 8>();
-    if (e == cudaSuccess) e = allow_attn_smem<64, 1>();
-    if (e == cudaSuccess) e = allow_attn_smem<64, 2>();
-    if (e == cudaSuccess) e = allow_attn_smem<64, 4>();
-    if (e == cudaSuccess) e = allow_attn_smem<64, 8>();
+    ClusterFit fit = {};
+    cudaError_t e = allow_attn_smem<128, 1>(fit);
+    if (e == cudaSuccess) e = allow_attn_smem<128, 2>(fit);
+    if (e == cudaSuccess) e = allow_attn_smem<128, 4>(fit);
+    if (e == cudaSuccess) e = allow_attn_smem<128, 8>(fit);
+    if (e == cudaSuccess) e = allow_attn_smem<64, 1>(fit);
+    if (e == cudaSuccess) e = allow_attn_smem<64, 2>(fit);
+    if (e == cudaSuccess) e = allow_attn_smem<64, 4>(fit);
+    if (e == cudaSuccess) e = allow_attn_smem<64, 8>(fit);
     if (e != cudaSuccess) return cuda_error(e, "attention: cudaFuncSetAttribute");
+    {
+        std::lock_guard<std::mutex> lf(g_fit_mu);
+        g_fit[dev] = fit;
+    }
     done.insert(dev);
     return QL_OK;
 }
@@ -652,8 +841,8 @@ int attn_launch(const AttnArgs& a, cudaStream_t s, bool pdl) {
     p.max_position = a.max_position;
     p.kw = const_cast<__half*>(a.k_pool);
     p.vw = const_cast<__half*>(a.v_pool);
-    cudaError_t e = a.head_dim == 128 ? launch_h<128>(p, G, a.batch, s, pdl)
-                                      : launch_h<64>(p, G, a.batch, s, pdl);
+    cudaError_t e = a.head_dim == 128 ? launch_h<128>(p, G, a.batch, s, pdl, device_error_record())
+                                      : launch_h<64>(p, G, a.batch, s, pdl, device_error_record());
     if (e != cudaSuccess) return cuda_error(e, "attention launch");
     return QL_OK;
 }
@@ -733,25 +922,6 @@ int noalloc_scratch_address(void** out) {
     return QL_OK;
 }
 
-template <int HD, int G>
-cudaError_t launch_hg_err(const AParams& p, int batch, cudaStream_t s, DevError* err) {
-    dim3 grid(p.nsplit, p.n_kv, batch);
-    if (attn_warps(batch) == 8)
-        return launch(attn_split_kernel<HD, G, 8>, grid, dim3(8 * 32), attn_smem<HD, G, 8>(), s, true, p, err);
-    return launch(attn_split_kernel<HD, G, 4>, grid, dim3(4 * 32), attn_smem<HD, G, 4>(), s, true, p, err);
-}
-
-template <int HD>
-cudaError_t launch_h_err(const AParams& p, int G, int batch, cudaStream_t s, DevError* err) {
-    switch (G) {
-        case 1: return launch_hg_err<HD, 1>(p, batch, s, err);
-        case 2: return launch_hg_err<HD, 2>(p, batch, s, err);
-        case 4: return launch_hg_err<HD, 4>(p, batch, s, err);
-        case 8: return launch_hg_err<HD, 8>(p, batch, s, err);
-        default: return cudaErrorInvalidValue;
-    }
-}
-
 }  // namespace
 }  // namespace ql
 
@@ -813,8 +983,30 @@ extern "C" int ql_paged_attn_decode_noalloc(const void* d_q, const void* d_k_poo
     // out-of-range indices are skipped; they are recorded only if this device already has an
     // error record (this path never creates one, since that would allocate)
     DevError* err = device_error_record_existing();
-    const cudaError_t e = head_dim == 128 ? launch_h_err<128>(p, G, (int)batch, s, err)
-                                          : launch_h_err<64>(p, G, (int)batch, s, err);
+    const cudaError_t e = head_dim == 128 ? launch_h<128>(p, G, (int)batch, s, true, err)
+                                          : launch_h<64>(p, G, (int)batch, s, true, err);
     if (e != cudaSuccess) return cuda_error(e, "ql_paged_attn_decode_noalloc launch");
     return QL_OK;
+}
+
+extern "C" int ql_set_attn_merge_form(int form) {
+    using namespace ql;
+    if (form != QL_ATTN_MERGE_TICKET && form != QL_ATTN_MERGE_CLUSTER)
+        return set_error(QL_EINVAL, "ql_set_attn_merge_form: form must be QL_ATTN_MERGE_TICKET or QL_ATTN_MERGE_CLUSTER");
+    const int prev = attn_merge_form();
+    g_attn_merge.store(form);
+    return prev;
+}
+
+extern "C" int ql_paged_attn_merge_form(int64_t batch, int n_heads, int n_kv_heads, int head_dim,
+                                        int64_t max_blocks_per_seq) {
+    using namespace ql;
+    if (batch < 1 || batch > 65535 || n_kv_heads <= 0 || n_heads <= 0 || n_heads % n_kv_heads != 0 ||
+        (head_dim != 64 && head_dim != 128) || max_blocks_per_seq < 1)
+        return set_error(QL_EINVAL, "ql_paged_attn_merge_form: bad shape");
+    const int G = n_heads / n_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return set_error(QL_EINVAL, "ql_paged_attn_merge_form: bad GQA group");
+    if (int rc = attn_prepare()) return rc;
+    const Layout lo = layout(batch, n_heads, n_kv_heads, head_dim, max_blocks_per_seq, num_sms());
+    return use_cluster(head_dim, G, lo.nsplit, n_kv_heads, (int)batch) ? QL_ATTN_MERGE_CLUSTER : QL_ATTN_MERGE_TICKET;
 }

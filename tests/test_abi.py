@@ -170,3 +170,13 @@ def test_batched_gemv_form_switch(ql):
     prev = ql.ql_set_batched_gemv_form(ql.QL_BATCHED_TCGEN05)
     assert prev in (ql.QL_BATCHED_MMA_SYNC, ql.QL_BATCHED_TCGEN05)
     assert ql.ql_set_batched_gemv_form(prev) == ql.QL_BATCHED_TCGEN05
+
+
+def test_attn_merge_form_switch(ql):
+    """The attention merge form is a process-wide choice: unknown forms are rejected, the
+    previous form is returned (no device needed)."""
+    assert ql.lib().ql_set_attn_merge_form(5) == ql.QL_EINVAL
+    prev = ql.ql_set_attn_merge_form(ql.QL_ATTN_MERGE_TICKET)
+    assert prev in (ql.QL_ATTN_MERGE_TICKET, ql.QL_ATTN_MERGE_CLUSTER)
+    assert ql.ql_set_attn_merge_form(prev) == ql.QL_ATTN_MERGE_TICKET
+    assert ql.lib().ql_paged_attn_merge_form(1, 32, 8, 96, 16) == ql.QL_EINVAL

@@ -64,8 +64,19 @@ def test_attention_lengths(hd, n_heads, n_kv):
     check(got, oracle_attention(case, hd), f"hd{hd} {n_heads}/{n_kv}")
 
 
-@pytest.mark.parametrize("L", [1, 2, 16, 17, 63, 64, 65, 511, 2049, 4100])
-def test_attention_single_sequence(L):
+@pytest.fixture(params=["cluster", "ticket"])
+def merge(request):
+    """Runs a test under each split-merge form (batch 1-2 shapes with 2..16 splits take the
+    cluster form when it is selected and the device holds the launch's clusters)."""
+    ql = lib()
+    prev = ql.ql_set_attn_merge_form(ql.QL_ATTN_MERGE_CLUSTER if request.param == "cluster"
+                                     else ql.QL_ATTN_MERGE_TICKET)
+    yield request.param
+    ql.ql_set_attn_merge_form(prev)
+
+
+@pytest.mark.parametrize("L", [1, 2, 16, 17, 63, 64, 65, 511, 2049, 4096, 4100])
+def test_attention_single_sequence(L, merge):
     case = ql_inputs.attention_case(1, 32, 8, 128, [L], seed=L)
     check(gpu_attention(case, 32, 8, 128), oracle_attention(case, 128), f"L={L}")
 
@@ -99,7 +110,7 @@ def test_paged_equals_contiguous_bit_exact():
     assert np.array_equal(got_perm, got_id)
 
 
-def test_idle_slot_untouched_and_rows_sum():
+def test_idle_slot_untouched_and_rows_sum(merge):
     # context length 0 marks an idle slot: its output stays as it was (NaN sentinel here)
     case = ql_inputs.attention_case(2, 8, 2, 64, [40, 1], seed=13)
     got = gpu_attention(case, 8, 2, 64, lens=[40, 0])
@@ -110,6 +121,35 @@ def test_idle_slot_untouched_and_rows_sum():
     case2["v_pool"][:] = np.float16(0.375)
     got2 = gpu_attention(case2, 8, 2, 64)
     assert np.allclose(got2, 0.375, atol=1e-3)
+
+
+@pytest.mark.parametrize("B,lens", [(1, [511]), (1, [2049]), (1, [2304]), (1, [4096]), (1, [4100]),
+                                    (2, [1000, 333]), (2, [2049, 17])])
+def test_merge_forms_bit_identical(B, lens):
+    """The cluster merge (partials in shared memory, read through distributed shared memory)
+    and the ticket merge (partials in the workspace, merged by the last split) take the same
+    merge over the splits in order: bit-identical outputs, both within the oracle's tolerance.
+    The batch-1 shape of the decode benchmark (2049..2304 positions: 9-10 splits) must take
+    the cluster form; shapes with more than 16 splits take the ticket form."""
+    ql = lib()
+    case = ql_inputs.attention_case(B, 32, 8, 128, lens, seed=sum(lens) + B)
+    mb = case["max_blocks"]
+    prev = ql.ql_set_attn_merge_form(ql.QL_ATTN_MERGE_CLUSTER)
+    try:
+        form = ql.ql_paged_attn_merge_form(B, 32, 8, 128, mb)
+        a = gpu_attention(case, 32, 8, 128)
+        ql.ql_set_attn_merge_form(ql.QL_ATTN_MERGE_TICKET)
+        assert ql.ql_paged_attn_merge_form(B, 32, 8, 128, mb) == ql.QL_ATTN_MERGE_TICKET
+        b = gpu_attention(case, 32, 8, 128)
+    finally:
+        ql.ql_set_attn_merge_form(prev)
+    nsplit = -(-mb // 16)
+    if nsplit > 16:
+        assert form == ql.QL_ATTN_MERGE_TICKET
+    if B == 1 and 9 <= nsplit <= 10:
+        assert form == ql.QL_ATTN_MERGE_CLUSTER
+    assert np.array_equal(a, b), f"forms differ: max {np.abs(a - b).max():.3e} (form {form})"
+    check(a, oracle_attention(case, 128), f"B={B} lens={lens}")
 
 
 @pytest.mark.slow
