@@ -75,14 +75,18 @@ __device__ __forceinline__ void pdl_trigger() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Ask L2 to fetch this CTA's share of [base, base + bytes): the grid splits the range evenly,
-// each thread of a CTA issues 16 KB pieces. A hint only (no data is returned, nothing waits):
-// used to stream the NEXT kernel's weights while the current kernel runs.
+// Ask L2 to fetch this CTA's share of [base, base + bytes): the grid splits the range into
+// shares of bytes / 2^floor(log2(CTAs)) (rounded up to 16 B: between one and two even shares,
+// so the first CTAs cover it all, with no integer division - this runs before the kernel's wait,
+// on the path of a CTA that starts after its predecessor has ended), each thread of a CTA
+// issues 16 KB pieces. A hint only (no data is returned, nothing waits): used to stream a later
+// kernel's weights or constants while the current kernel runs.
 __device__ __forceinline__ void l2_prefetch_share(const void* base, size_t bytes) {
     if (base == nullptr || bytes < 16) return;
-    const size_t nblocks = (size_t)gridDim.x * gridDim.y * gridDim.z;
+    const unsigned int nblocks = gridDim.x * gridDim.y * gridDim.z;
     const size_t bid = blockIdx.x + (size_t)gridDim.x * (blockIdx.y + (size_t)gridDim.y * blockIdx.z);
-    const size_t share = ((bytes + nblocks - 1) / nblocks + 15) & ~(size_t)15;
+    const int lg = 31 - __clz((int)nblocks);   // 2^lg <= nblocks
+    const size_t share = (((bytes + ((size_t)1 << lg) - 1) >> lg) + 15) & ~(size_t)15;
     const size_t start = bid * share;
     if (start >= bytes) return;
     const size_t end = start + share < bytes ? start + share : bytes;
