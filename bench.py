@@ -391,6 +391,19 @@ GU_TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum, profiles
                      "gemv_stream_q4_0_24576x4096_b1_ncu.md (same kernel, plain epilogue)")
 
 
+def ns_relative(raw, nstamps):
+    """The trace as float64 with its first `nstamps` words (globaltimer ns, ~1.8e18) taken
+    relative to the earliest stamp, in int64 first: float64 cannot hold the absolute values to
+    better than 256 ns. Unwritten (zero) stamps stay zero, written ones are >= 1."""
+    import numpy as np
+    out = raw.astype(np.float64)
+    ts = raw[..., :nstamps]
+    if (ts > 0).any():
+        base = ts[ts > 0].min() - 1
+        out[..., :nstamps] = np.where(ts > 0, ts - base, 0).astype(np.float64)
+    return out
+
+
 def launch_phases(gm, sargs, s, cfg):
     """Per-GEMV phase times of a step of separate launches (batch 1-2) from the GEMV kernels'
     globaltimer trace (untimed eager steps after the timed region). Per matrix kind, means over
@@ -420,7 +433,7 @@ def launch_phases(gm, sargs, s, cfg):
         gm.ql_model_set_option(ql.QL_OPT_STEP_TRACE, 0)
         gm.ql_decode_graph_capture(sargs, s)
     gm.ql_check_device_error()
-    ta = buf.cpu().numpy().reshape(rows + cfg.n_layers, grid, 8).astype(np.float64)
+    ta = ns_relative(buf.cpu().numpy().reshape(rows + cfg.n_layers, grid, 8), 6)
     t, tat = ta[:rows], ta[rows:]
     if not (t[:, 0, 0] > 0).all():
         return None   # another GEMV form ran (not traced)
@@ -488,7 +501,7 @@ def step_phases(gm, sargs, s, cfg):
     finally:
         gm.ql_model_set_option(ql.QL_OPT_STEP_TRACE, 0)
     gm.ql_check_device_error()
-    t = buf.cpu().numpy().reshape(rows, grid, 8).astype(np.float64)
+    t = ns_relative(buf.cpu().numpy().reshape(rows, grid, 8), 8)
     arrive, leave = t[:, :, 0], t[:, :, 1]
     kinds = ["embed"] + [k for _ in range(cfg.n_layers) for k in ("qkv", "attn", "o", "gate_up", "down")] + ["lm_head"]
     acc = {}
