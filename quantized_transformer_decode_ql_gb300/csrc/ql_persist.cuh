@@ -298,6 +298,19 @@ __device__ __forceinline__ void ring_wait(Ring& r, const PersistParams& p, unsig
 }
 
 // ------------------------------------------------------------------------------ GEMV phase
+// Scalars of the step that a GEMV phase reads after its wait on the predecessor, passed by value:
+// read through the reference to the kernel parameters they were a cold load on the critical
+// path of every launch (the kernel reads them before its wait, see hot_scalars).
+struct Hot {
+    int B, max_nblk;
+    float eps;
+};
+__device__ __forceinline__ Hot hot_scalars(const PersistParams& p) {
+    Hot h{p.B, p.max_nblk, p.eps};
+    // opaque to the compiler from here on: kept in registers, not re-read after the wait
+    asm volatile("" : "+r"(h.B), "+r"(h.max_nblk), "+f"(h.eps));
+    return h;
+}
 // Stage the activations of all B columns in f16: per column and block j, 4 chunks of 16 bytes
 // (chunk t: f16 pairs (x0, x2), (x1, x3), (x16, x18)/16, (x17, x19)/16 of elements 32 j + 4 t
 // + ...: the pairs that one 32-bit code word expands to, the high-nibble ones pre-divided by 16,
@@ -306,11 +319,11 @@ __device__ __forceinline__ void ring_wait(Ring& r, const PersistParams& p, unsig
 // stay in registers between the two passes. f16 input: kChunk items per thread are loaded
 // together. Data written earlier in the launch by other CTAs is read with ld.global.cg (L2).
 template <bool RMS, int W>
-__device__ __noinline__ void stage_x(const PersistParams& p, int nblk, int cstride, const float* xf,
+__device__ __noinline__ void stage_x(int B, float eps, int nblk, int cstride, const float* xf,
                                      const __half* x16, const float* w, uint4* xs, float* red) {
     constexpr int kHeld = 2, kChunk = 4, kT = W * 32;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int B = p.B, cols = nblk * 32, nitems = B * nblk * 4;
+    const int cols = nblk * 32, nitems = B * nblk * 4;
 
     // item -> (column b, block j, chunk t) and its element offset
     auto where = [&](int item, int& b, int& j, int& t) -> size_t {
@@ -392,8 +405,8 @@ __device__ __noinline__ void stage_x(const PersistParams& p, int nblk, int cstri
             a0 += red[i * 2];
             a1 += red[i * 2 + 1];
         }
-        const float rs0 = 1.0f / sqrtf(a0 / (float)cols + p.eps);
-        const float rs1 = 1.0f / sqrtf(a1 / (float)cols + p.eps);
+        const float rs0 = 1.0f / sqrtf(a0 / (float)cols + eps);
+        const float rs1 = 1.0f / sqrtf(a1 / (float)cols + eps);
 #pragma unroll
         for (int r = 0; r < kHeld; ++r) {
             const int item = tid + r * kT;
@@ -494,7 +507,7 @@ __device__ __noinline__ void finish_tile(const PersistParams& p, const PMat& M, 
 // MMA form of the same product wastes 7 of the 8 columns of an m16n8k16 tile at batch 1-2, and
 // measured slower than the CUDA cores here.)
 template <int NB, int W>
-__device__ __noinline__ void gemv_phase(const PersistParams& p, const PMat* mats, int wp, int epi, bool rms,
+__device__ __noinline__ void gemv_phase(const PersistParams& p, Hot h, const PMat* mats, int wp, int epi, bool rms,
                                         Ring& ring, const float* xf,
                                         const __half* x16, const float* norm_w, void* y, int ld,
                                         unsigned char* region, float* red,
@@ -502,14 +515,14 @@ __device__ __noinline__ void gemv_phase(const PersistParams& p, const PMat* mats
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int hr = lane & 15, hh = lane >> 4;
     const PMat M = mats[wp];
-    const int cstride = p.max_nblk * 4 + 4;   // uint4 units between staged columns (+64 B)
+    const int cstride = h.max_nblk * 4 + 4;   // uint4 units between staged columns (+64 B)
     uint4* xs = reinterpret_cast<uint4*>(region);
     float4* part = reinterpret_cast<float4*>(xs + (size_t)NB * cstride);   // [W][2][32]
 
     if (rms)
-        stage_x<true, W>(p, M.nblk, cstride, xf, x16, norm_w, xs, red);
+        stage_x<true, W>(h.B, h.eps, M.nblk, cstride, xf, x16, norm_w, xs, red);
     else
-        stage_x<false, W>(p, M.nblk, cstride, xf, x16, norm_w, xs, red);
+        stage_x<false, W>(h.B, h.eps, M.nblk, cstride, xf, x16, norm_w, xs, red);
     __syncthreads();
     stamp(tr, 2);
 
@@ -1085,6 +1098,7 @@ __device__ void attn_prefetch(const PersistParams& p, int layer) {
 template <int HD, int G, int NB>
 __device__ void step_body(const PersistParams& p, const PMat* mats, Ring& r, unsigned char* region, __half (*qs)[HD],
                           float* red, unsigned long long (*kred)[kMaxB], int* flag) {
+    const Hot hot{p.B, p.max_nblk, p.eps};
     unsigned int target = 0;
     // trace row of the barrier that ends the next phase
     auto row = [&]() -> unsigned long long* {
@@ -1097,27 +1111,27 @@ __device__ void step_body(const PersistParams& p, const PMat* mats, Ring& r, uns
         const PLayer* Ly = p.layers + l;
         attn_prefetch<HD>(p, l);
         // q|k|v = W_qkv rmsnorm(x, attn_norm)
-        gemv_phase<NB, kW>(p, mats, 4 * l, kEpiF32, true, r, p.x, nullptr, Ly->attn_norm, p.qkv, qkv_ld, region, red,
+        gemv_phase<NB, kW>(p, hot, mats, 4 * l, kEpiF32, true, r, p.x, nullptr, Ly->attn_norm, p.qkv, qkv_ld, region, red,
                                       kred, row());
         if (!grid_barrier(p, target, flag)) return;
         // qk-norm + RoPE + KV append + paged attention -> attn
         attn_phase<HD, G>(p, l, region, qs, flag, row());
         if (!grid_barrier(p, target, flag)) return;
         // x += W_o attn
-        gemv_phase<NB, kW>(p, mats, 4 * l + 1, kEpiResid, false, r, nullptr, p.attn, nullptr, p.x, p.hidden, region, red,
+        gemv_phase<NB, kW>(p, hot, mats, 4 * l + 1, kEpiResid, false, r, nullptr, p.attn, nullptr, p.x, p.hidden, region, red,
                                          kred, row());
         if (!grid_barrier(p, target, flag)) return;
         // act = silu(gate) * up, [gate | up] = W_gu rmsnorm(x, ffn_norm)
-        gemv_phase<NB, kW>(p, mats, 4 * l + 2, kEpiSilu, true, r, p.x, nullptr, Ly->ffn_norm, p.act, p.inter, region, red,
+        gemv_phase<NB, kW>(p, hot, mats, 4 * l + 2, kEpiSilu, true, r, p.x, nullptr, Ly->ffn_norm, p.act, p.inter, region, red,
                                        kred, row());
         if (!grid_barrier(p, target, flag)) return;
         // x += W_down act
-        gemv_phase<NB, kW>(p, mats, 4 * l + 3, kEpiResid, false, r, nullptr, p.act, nullptr, p.x, p.hidden, region, red,
+        gemv_phase<NB, kW>(p, hot, mats, 4 * l + 3, kEpiResid, false, r, nullptr, p.act, nullptr, p.x, p.hidden, region, red,
                                          kred, row());
         if (!grid_barrier(p, target, flag)) return;
     }
     // logits = W_lm rmsnorm(x, final_norm), greedy argmax keys
-    gemv_phase<NB, kW>(p, mats, 4 * p.n_layers, kEpiLogits, true, r, p.x, nullptr, p.final_norm, p.logits, p.vocab, region,
+    gemv_phase<NB, kW>(p, hot, mats, 4 * p.n_layers, kEpiLogits, true, r, p.x, nullptr, p.final_norm, p.logits, p.vocab, region,
                                      red, kred, row());
     if (!grid_barrier(p, target, flag)) return;
     if (blockIdx.x == 0) finalize(p);
@@ -1263,12 +1277,13 @@ __global__ void __launch_bounds__(W * 32, 16 / W) gemv_stream_kernel(const __gri
     // constants of a later kernel of the step (its norm weights), into L2 off its critical path
     l2_prefetch_share(g.next.ptr[0], g.next.bytes[0]);
     l2_prefetch_share(g.next.ptr[1], g.next.bytes[1]);
+    const Hot hot = hot_scalars(p);
     // the trigger follows the wait in every kernel of the step: a kernel's code before its
     // wait then runs only after the kernel two launches back has completed
     pdl_wait();
     pdl_trigger();
     stamp(tr, 1);
-    gemv_phase<NB, W>(p, &mat, 0, g.epi, g.rms != 0, r, g.xf, g.x16, g.norm_w, g.y, g.ld,
+    gemv_phase<NB, W>(p, hot, &mat, 0, g.epi, g.rms != 0, r, g.xf, g.x16, g.norm_w, g.y, g.ld,
                       smem + (size_t)W * kStages * kSlotBytes, red, kred, tr);
     const unsigned long long t0 = global_ns();
     while (r.consumed < r.issued) {   // only after a wait ran out: let copies land (bounded)
