@@ -302,6 +302,7 @@ struct StreamGemvArgs {
     size_t workspace_bytes;
     unsigned long long* trace;   // batch 1-2, optional: [grid][8] globaltimer stamps per CTA
     NextWeights next;     // batch 1-2: constants of a later kernel, prefetched into L2
+    int grid;             // batch 1-2: CTAs (0: one per SM); fewer leave SMs to the kernel before
 };
 int persist_trace_words();   // trace entries per CTA and row
 int stream_gemv_prepare();

@@ -126,6 +126,20 @@ int alloc(ql_model* m, void** p, size_t bytes) {
     return QL_OK;
 }
 
+// CTAs of the o GEMV at batch 1-2: the SMs minus the attention's merging CTAs (they end last),
+// if that keeps the largest per-CTA tile count; else one per SM (0). QL_O_GEMV_FULL=1 keeps
+// one per SM for A/B measurements.
+int o_gemv_grid(int sms, int mergers, int ntile) {
+    static const bool full = [] {
+        const char* e = std::getenv("QL_O_GEMV_FULL");
+        return e != nullptr && std::atoi(e) != 0;
+    }();
+    const int g = sms - mergers;
+    if (full || g <= 0 || g >= sms) return 0;
+    const int per_full = (ntile + sms - 1) / sms, per_less = (ntile + g - 1) / g;
+    return per_less == per_full ? g : 0;
+}
+
 // The whole step as one cooperative kernel (ql_persist.cuh).
 int run_persist(ql_model* m, const ql_step_args* a, cudaStream_t s) {
     const ql_model_desc& d = m->d;
@@ -219,9 +233,10 @@ int run_step(ql_model* m, const ql_step_args* a, cudaStream_t s) {
     const bool streamed = !m->hmats.empty() && (B <= kPersistMaxBatch || (m->batched_ok && B <= 32));
     int gemv_k = 0;   // GEMV launches so far (their trace rows)
     auto sg = [&](const PMat& M, int epi, bool rms, const float* xf, const __half* x16, const float* nw, void* y,
-                  int ld, NextWeights next) {
+                  int ld, NextWeights next, int grid = 0) {
         StreamGemvArgs ga = {};
         ga.next = next;
+        ga.grid = grid;
         if (m->trace) ga.trace = m->trace + (size_t)gemv_k * num_sms() * persist_trace_words();
         ++gemv_k;
         ga.M = M;
@@ -284,8 +299,12 @@ int run_step(ql_model* m, const ql_step_args* a, cudaStream_t s) {
                 at.trace_ctas = num_sms();
             }
             if ((rc = attn_launch(at, s, pdl)) != QL_OK) return rc;
+            // the o GEMV leaves out one SM per attention merge (one CTA per sequence and kv head
+            // merges the splits, ending after the others): every o CTA then starts on an SM
+            // freed early, while the CTA with the most tiles keeps the same count
+            const int o_grid = o_gemv_grid(num_sms(), B * nkv, (int)Ms[1].ntile);
             if ((rc = sg(Ms[1], QL_EPI_ADD_RESIDUAL, false, nullptr, m->attn, nullptr, m->x, (int)d.hidden,
-                         ffn_norm)) != QL_OK)
+                         ffn_norm, o_grid)) != QL_OK)
                 return rc;
             if ((rc = sg(Ms[2], QL_EPI_SILU_MUL, true, m->x, nullptr, L.ffn_norm, m->act, (int)d.intermediate,
                          none)) != QL_OK)

@@ -135,7 +135,8 @@ int stream_gemv_launch(const StreamGemvArgs& a, cudaStream_t s, bool pdl) {
     const int warps = stream_gemv_warps();
     const size_t smem = (size_t)warps * persist::kStages * persist::kSlotBytes +
                         persist::gemv_region_bytes(a.batch, a.M.nblk, warps);
-    const int grid = num_sms() * (warps == 8 ? 2 : 1);
+    int grid = num_sms() * (warps == 8 ? 2 : 1);
+    if (a.grid > 0 && a.grid < grid) grid = a.grid;
     cudaError_t e;
     if (warps == 8)
         e = a.batch == 1 ? persist::stream_gemv_one<1, 8>(true, &p, &g, smem, grid, s, pdl)
