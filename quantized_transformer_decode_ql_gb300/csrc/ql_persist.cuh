@@ -360,6 +360,7 @@ __device__ __noinline__ void stage_x(int B, float eps, int nblk, int cstride, co
     if (RMS) {
         float hx[kHeld][8], hw[kHeld][8];
         float ss0 = 0.f, ss1 = 0.f;
+        const float inv_cols = 1.0f / (float)cols;   // while the loads are in flight
 #pragma unroll
         for (int r = 0; r < kHeld; ++r) {
             const int item = tid + r * kT;
@@ -389,24 +390,26 @@ __device__ __noinline__ void stage_x(int B, float eps, int nblk, int cstride, co
             for (int i = 0; i < 8; ++i) s2 += v[i] * v[i];
             if (item < nblk * 4) ss0 += s2; else ss1 += s2;
         }
+        // warp sums, then the warps' in warp order (a shared array of this function: direct
+        // shared-memory accesses); the second column only at batch 2
 #pragma unroll
-        for (int o = 16; o; o >>= 1) {
-            ss0 += __shfl_xor_sync(0xffffffffu, ss0, o);
-            ss1 += __shfl_xor_sync(0xffffffffu, ss1, o);
+        for (int o = 16; o; o >>= 1) ss0 += __shfl_xor_sync(0xffffffffu, ss0, o);
+        if (B > 1) {
+#pragma unroll
+            for (int o = 16; o; o >>= 1) ss1 += __shfl_xor_sync(0xffffffffu, ss1, o);
         }
-        if (lane == 0) {
-            red[warp * 2] = ss0;
-            red[warp * 2 + 1] = ss1;
-        }
+        __shared__ float2 wsum[W];
+        if (lane == 0) wsum[warp] = make_float2(ss0, ss1);
         __syncthreads();
         float a0 = 0.f, a1 = 0.f;
 #pragma unroll
         for (int i = 0; i < W; ++i) {
-            a0 += red[i * 2];
-            a1 += red[i * 2 + 1];
+            const float2 v = wsum[i];
+            a0 += v.x;
+            a1 += v.y;
         }
-        const float rs0 = 1.0f / sqrtf(a0 / (float)cols + eps);
-        const float rs1 = 1.0f / sqrtf(a1 / (float)cols + eps);
+        const float rs0 = rsqrtf(fmaf(a0, inv_cols, eps));
+        const float rs1 = rsqrtf(fmaf(a1, inv_cols, eps));
 #pragma unroll
         for (int r = 0; r < kHeld; ++r) {
             const int item = tid + r * kT;
