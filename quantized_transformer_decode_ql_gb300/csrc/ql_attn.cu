@@ -131,7 +131,7 @@ __device__ __forceinline__ void warp_norm_rope(const float* src, const RopeLane<
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    const float r = 1.0f / sqrtf(ss / (float)HD + eps);
+    const float r = rsqrtf(fmaf(ss, 1.0f / (float)HD, eps));
 #pragma unroll
     for (int k = 0; k < PER; ++k) {
         const int i = lane + 32 * k;

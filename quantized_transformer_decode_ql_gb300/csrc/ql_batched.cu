@@ -478,7 +478,7 @@ __global__ void __launch_bounds__(kNormT) rms_norm_kernel(const float* x, int co
     if (tid == 0) {
         float t = 0.f;
         for (int k = 0; k < kNormT / 32; ++k) t += red[k];
-        rs = 1.0f / sqrtf(t / (float)cols + eps);
+        rs = rsqrtf(fmaf(t, 1.0f / (float)cols, eps));
     }
     __syncthreads();
     const float rr = rs;

@@ -51,7 +51,8 @@ __device__ __forceinline__ __half2 h2(uint32_t u) {
 }
 __device__ __forceinline__ uint32_t u32(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 
-__device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
+// SiLU with the fast exponential and division (the result is rounded to f16)
+__device__ __forceinline__ float silu(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 // Order-preserving key: larger logit -> larger key; among equal logits the lower row wins.
 __device__ __forceinline__ unsigned long long argmax_key(float v, int row) {
@@ -120,7 +121,7 @@ __device__ void stage_x(const KParams& p, uint4* xs, float* bias, float* red) {
             float t = 0.f;
 #pragma unroll
             for (int w = 0; w < kWarps; ++w) t += red[w * 8 + b];
-            const float r = 1.0f / sqrtf(t / (float)cols + p.eps);
+            const float r = rsqrtf(fmaf(t, 1.0f / (float)cols, p.eps));
 #pragma unroll
             for (int bb = 0; bb < 8; ++bb)
                 if (bb == b) rs[bb] = r;

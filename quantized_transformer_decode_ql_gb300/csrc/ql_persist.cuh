@@ -76,7 +76,8 @@ __device__ __forceinline__ __half2 as_h2(uint32_t u) {
 }
 __device__ __forceinline__ uint32_t as_u32(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 
-__device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
+// SiLU with the fast exponential and division (the result is rounded to f16)
+__device__ __forceinline__ float silu(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 // Order-preserving key: larger logit -> larger key; among equal logits the lower row wins.
 __device__ __forceinline__ unsigned long long argmax_key(float v, int row) {
@@ -705,7 +706,7 @@ __device__ __forceinline__ void norm_rope(const float* src, const float* w, cons
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    const float r = 1.0f / sqrtf(ss / (float)HD + eps);
+    const float r = rsqrtf(fmaf(ss, 1.0f / (float)HD, eps));
 #pragma unroll
     for (int k = 0; k < PER; ++k) {
         const int i = lane + 32 * k;

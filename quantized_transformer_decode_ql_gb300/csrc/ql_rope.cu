@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(HD / 2) norm_rope_kernel(RParams p, DevError* 
 #pragma unroll
         for (int w = 0; w < NW; ++w) ss += red[w];
     }
-    const float r = 1.0f / sqrtf(ss / (float)HD + p.eps);
+    const float r = rsqrtf(fmaf(ss, 1.0f / (float)HD, p.eps));
     const float* w = is_q ? p.q_norm : p.k_norm;
     const float xn = x * r * w[i], yn = y * r * w[i + H2];
     if (pos < 0 || pos >= p.max_position) {
