@@ -386,7 +386,7 @@ def launches_per_step(cfg, B):
 # DRAM bytes (read + write) of one launch of the batch-1 tile stream GEMV at the gate|up shape
 # (24576 x 4096), from one ncu capture of that kernel (plain epilogue; the SiLU*up launch that
 # the roofline times writes 72 KB less); reported only for that kernel and batch.
-GU_TRAFFIC_B1 = 57007104 + 222208
+GU_TRAFFIC_B1 = 57008640 + 227840
 GU_TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum, profiles/"
                      "gemv_stream_q4_0_24576x4096_b1_ncu.md (same kernel, plain epilogue)")
 
