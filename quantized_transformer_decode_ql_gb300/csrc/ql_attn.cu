@@ -593,16 +593,26 @@ Layout layout(int64_t batch, int n_heads, int n_kv, int head_dim, int64_t maxb, 
     Layout lo = {};
     // Split the block table so that a full-capacity batch gives several CTAs per SM.
     const int64_t pairs = batch * n_kv;
-    const int64_t target = 8ll * sms;
+    // about 16 CTAs per SM for a full-capacity batch (mixed context lengths then spread over the
+    // SMs evenly; batch 32 over lengths in [128, 8192] measured 5292 tokens/s against 5122 with
+    // 8 and 5220 with 32); QL_ATTN_CTAS_PER_SM overrides it for A/B measurements
+    static const int env_target = [] {
+        const char* e = std::getenv("QL_ATTN_CTAS_PER_SM");
+        const int v = e ? std::atoi(e) : 0;
+        return v > 0 && v <= 64 ? v : 16;
+    }();
+    const int64_t target = (int64_t)env_target * sms;
     int64_t spb = (maxb * pairs + target - 1) / target;
-    // at least two blocks per warp of a CTA, so that a split's blocks are all staged from the
-    // start (4 warps and 8 blocks measured best at batch 1 among 4-warp splits of 4, 8 and 16
-    // blocks); QL_ATTN_MIN_SPB overrides the floor for A/B measurements
+    // batch 1-2: two blocks per warp of a CTA, so that a split's blocks are all staged from the
+    // start (8 warps, 16 blocks); QL_ATTN_MIN_SPB overrides the floor for A/B measurements
     static const int env_spb = [] {
         const char* e = std::getenv("QL_ATTN_MIN_SPB");
         return e ? std::atoi(e) : 0;
     }();
-    const int64_t min_spb = env_spb > 0 ? (int64_t)(env_spb > 256 ? 256 : env_spb) : 2 * attn_warps(batch);
+    // batch 3+: at least 7 blocks per warp, so that a split's pipeline fill and drain stay a
+    // small part of it (batch 32 at 2048 positions: 28-block splits 69.5 us, 14-block 79.9 us)
+    const int64_t min_spb = env_spb > 0 ? (int64_t)(env_spb > 256 ? 256 : env_spb)
+                                        : (batch <= 2 ? 2 * attn_warps(batch) : 7 * attn_warps(batch));
     if (spb < min_spb) spb = min_spb;
     if (spb > maxb) spb = maxb;
     if (spb < 1) spb = 1;
