@@ -321,7 +321,7 @@ __device__ __forceinline__ Hot hot_scalars(const PersistParams& p) {
 // together. Data written earlier in the launch by other CTAs is read with ld.global.cg (L2).
 template <bool RMS, int W>
 __device__ __noinline__ void stage_x(int B, float eps, int nblk, int cstride, const float* xf,
-                                     const __half* x16, const float* w, uint4* xs, float* red) {
+                                     const __half* x16, const float* w, uint4* xs) {
     constexpr int kHeld = 2, kChunk = 4, kT = W * 32;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cols = nblk * 32, nitems = B * nblk * 4;
@@ -514,7 +514,7 @@ template <int NB, int W>
 __device__ __noinline__ void gemv_phase(const PersistParams& p, Hot h, const PMat* mats, int wp, int epi, bool rms,
                                         Ring& ring, const float* xf,
                                         const __half* x16, const float* norm_w, void* y, int ld,
-                                        unsigned char* region, float* red,
+                                        unsigned char* region,
                                         unsigned long long (*kred)[kMaxB], unsigned long long* tr) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int hr = lane & 15, hh = lane >> 4;
@@ -524,9 +524,9 @@ __device__ __noinline__ void gemv_phase(const PersistParams& p, Hot h, const PMa
     float4* part = reinterpret_cast<float4*>(xs + (size_t)NB * cstride);   // [W][2][32]
 
     if (rms)
-        stage_x<true, W>(h.B, h.eps, M.nblk, cstride, xf, x16, norm_w, xs, red);
+        stage_x<true, W>(h.B, h.eps, M.nblk, cstride, xf, x16, norm_w, xs);
     else
-        stage_x<false, W>(h.B, h.eps, M.nblk, cstride, xf, x16, norm_w, xs, red);
+        stage_x<false, W>(h.B, h.eps, M.nblk, cstride, xf, x16, norm_w, xs);
     __syncthreads();
     stamp(tr, 2);
 
@@ -1101,7 +1101,7 @@ __device__ void attn_prefetch(const PersistParams& p, int layer) {
 
 template <int HD, int G, int NB>
 __device__ void step_body(const PersistParams& p, const PMat* mats, Ring& r, unsigned char* region, __half (*qs)[HD],
-                          float* red, unsigned long long (*kred)[kMaxB], int* flag) {
+                          unsigned long long (*kred)[kMaxB], int* flag) {
     const Hot hot{p.B, p.max_nblk, p.eps};
     unsigned int target = 0;
     // trace row of the barrier that ends the next phase
@@ -1115,28 +1115,28 @@ __device__ void step_body(const PersistParams& p, const PMat* mats, Ring& r, uns
         const PLayer* Ly = p.layers + l;
         attn_prefetch<HD>(p, l);
         // q|k|v = W_qkv rmsnorm(x, attn_norm)
-        gemv_phase<NB, kW>(p, hot, mats, 4 * l, kEpiF32, true, r, p.x, nullptr, Ly->attn_norm, p.qkv, qkv_ld, region, red,
+        gemv_phase<NB, kW>(p, hot, mats, 4 * l, kEpiF32, true, r, p.x, nullptr, Ly->attn_norm, p.qkv, qkv_ld, region,
                                       kred, row());
         if (!grid_barrier(p, target, flag)) return;
         // qk-norm + RoPE + KV append + paged attention -> attn
         attn_phase<HD, G>(p, l, region, qs, flag, row());
         if (!grid_barrier(p, target, flag)) return;
         // x += W_o attn
-        gemv_phase<NB, kW>(p, hot, mats, 4 * l + 1, kEpiResid, false, r, nullptr, p.attn, nullptr, p.x, p.hidden, region, red,
+        gemv_phase<NB, kW>(p, hot, mats, 4 * l + 1, kEpiResid, false, r, nullptr, p.attn, nullptr, p.x, p.hidden, region,
                                          kred, row());
         if (!grid_barrier(p, target, flag)) return;
         // act = silu(gate) * up, [gate | up] = W_gu rmsnorm(x, ffn_norm)
-        gemv_phase<NB, kW>(p, hot, mats, 4 * l + 2, kEpiSilu, true, r, p.x, nullptr, Ly->ffn_norm, p.act, p.inter, region, red,
+        gemv_phase<NB, kW>(p, hot, mats, 4 * l + 2, kEpiSilu, true, r, p.x, nullptr, Ly->ffn_norm, p.act, p.inter, region,
                                        kred, row());
         if (!grid_barrier(p, target, flag)) return;
         // x += W_down act
-        gemv_phase<NB, kW>(p, hot, mats, 4 * l + 3, kEpiResid, false, r, nullptr, p.act, nullptr, p.x, p.hidden, region, red,
+        gemv_phase<NB, kW>(p, hot, mats, 4 * l + 3, kEpiResid, false, r, nullptr, p.act, nullptr, p.x, p.hidden, region,
                                          kred, row());
         if (!grid_barrier(p, target, flag)) return;
     }
     // logits = W_lm rmsnorm(x, final_norm), greedy argmax keys
     gemv_phase<NB, kW>(p, hot, mats, 4 * p.n_layers, kEpiLogits, true, r, p.x, nullptr, p.final_norm, p.logits, p.vocab, region,
-                                     red, kred, row());
+                                     kred, row());
     if (!grid_barrier(p, target, flag)) return;
     if (blockIdx.x == 0) finalize(p);
 }
@@ -1151,7 +1151,6 @@ template <int HD, int G>
 __global__ void __launch_bounds__(kT, 1) step_kernel(const __grid_constant__ PersistParams p) {
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ __align__(16) __half qs[G][HD];
-    __shared__ float red[kW * 2];
     __shared__ unsigned long long kred[kW][kMaxB];
     __shared__ int flag;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -1184,9 +1183,9 @@ __global__ void __launch_bounds__(kT, 1) step_kernel(const __grid_constant__ Per
 #pragma unroll 1
     for (int i = 0; i < kStages; ++i) ring_issue<kW>(r, mats, warp, lane);
     if (p.B == 1)
-        step_body<HD, G, 1>(p, mats, r, region, qs, red, kred, &flag);
+        step_body<HD, G, 1>(p, mats, r, region, qs, kred, &flag);
     else
-        step_body<HD, G, 2>(p, mats, r, region, qs, red, kred, &flag);
+        step_body<HD, G, 2>(p, mats, r, region, qs, kred, &flag);
     // after an early exit, let this warp's copies still in flight land before leaving (bounded:
     // past the bound the CTA leaves anyway)
     const unsigned long long t0 = global_ns();
@@ -1253,7 +1252,6 @@ __global__ void __launch_bounds__(W * 32, 16 / W) gemv_stream_kernel(const __gri
                                                                       const __grid_constant__ StreamGemv g) {
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ PMat mat;
-    __shared__ float red[W * 2];
     __shared__ unsigned long long kred[W][kMaxB];
     __shared__ __align__(8) unsigned long long mbar[W * kStages];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -1288,7 +1286,7 @@ __global__ void __launch_bounds__(W * 32, 16 / W) gemv_stream_kernel(const __gri
     pdl_trigger();
     stamp(tr, 1);
     gemv_phase<NB, W>(p, hot, &mat, 0, g.epi, g.rms != 0, r, g.xf, g.x16, g.norm_w, g.y, g.ld,
-                      smem + (size_t)W * kStages * kSlotBytes, red, kred, tr);
+                      smem + (size_t)W * kStages * kSlotBytes, kred, tr);
     const unsigned long long t0 = global_ns();
     while (r.consumed < r.issued) {   // only after a wait ran out: let copies land (bounded)
         const uint32_t mb = r.mbar + (r.consumed % kStages) * 8, parity = (r.consumed / kStages) & 1u;
