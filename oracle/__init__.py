@@ -14,11 +14,14 @@ Sources (public web pages; cited by page and item):
   (16-token blocks, block table, valid length = current length + 1, scale 1/sqrt(hd)),
   ``alloc_block`` (free list then bump, "pool exhausted").
 * memra-engine ``qwen4exp_gpu.rs`` - ``host_rms_norm`` and ``host_rope_at`` twins
-  (RMSNorm with effective weights; NeoX split-half rotation).
+  (RMSNorm with effective weights; NeoX split-half rotation); the quantised-cache storage
+  (q8_0 key rows, q5_1 value rows) and its host twins ``host_quant_q8_row``,
+  ``host_deq_q8_rows``, ``host_quant_q5_row``, ``host_deq_q5_rows``.
 
 Modules: :mod:`oracle.q4_0` (codec), :mod:`oracle.ops` (per-op definitions),
 :mod:`oracle.decode` (decode step, full recomputation, greedy decoding),
-:mod:`oracle.blockpool` (the block allocator rule).
+:mod:`oracle.blockpool` (the block allocator rule), :mod:`oracle.kvq` (the quantised KV-row
+codecs and attention over a quantised pool).
 
 Pins: every function here is pinned in ``tests/test_oracle_*.py`` against closed forms,
 invariants, brute force on tiny inputs and hand-derived fixtures in ``tests/golden/``.
