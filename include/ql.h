@@ -144,6 +144,29 @@ int64_t ql_gemv_q4_0_stream_workspace_bytes(int64_t rows, int64_t cols, int silu
 enum { QL_BATCHED_MMA_SYNC = 0, QL_BATCHED_TCGEN05 = 1 };
 int ql_set_batched_gemv_form(int form);
 
+/* --------------------------------------------------------------- quantised KV rows (host)
+ * The quantised KV-cache rows of [ME] (the quantised-cache storage: q8_row_bytes /
+ * q5_row_bytes, the Q8Q5 store, and the host twins host_quant_q8_row, host_deq_q8_rows,
+ * host_quant_q5_row, host_deq_q5_rows): keys as q8_0, values as q5_1. A row of dim f32
+ * values is cut into 32-element blocks, a ragged last block padded with zeros that take part
+ * in its statistics; every step is an f32 operation, f16 conversions round to nearest even.
+ *   q8_0, 34 B per block: f16 d (little-endian), 32 int8 codes. d = max|x| / 127,
+ *     id = 1/d (0 when d == 0 or 1/d is not finite), code = clamp(rint(x id), -127, 127);
+ *     decoded f32(d) * code.
+ *   q5_1, 24 B per block: f16 d, f16 m, a 32-bit word (bit l = bit 4 of code l), 16 bytes
+ *     (byte l: code l's low nibble, code l+16's in the high nibble). d = (max - min) / 31,
+ *     code = clamp(rint((x - min) id), 0, 31), m = min (a zero minimum stored as +0);
+ *     decoded fma(f32(d), code, f32(m)).
+ * x: host f32 [rows][dim]; out / in: host bytes [rows][row bytes]. Quantising returns
+ * QL_EINVAL for a NULL pointer, rows or dim <= 0, a non-finite value, or a scale or minimum
+ * that overflows f16. Deterministic, single-threaded.                                     */
+int64_t ql_kv_q8_0_row_bytes(int64_t dim);
+int64_t ql_kv_q5_1_row_bytes(int64_t dim);
+int ql_kv_quantize_q8_0(const float* x, int64_t rows, int64_t dim, uint8_t* out);
+int ql_kv_dequantize_q8_0(const uint8_t* in, int64_t rows, int64_t dim, float* x);
+int ql_kv_quantize_q5_1(const float* x, int64_t rows, int64_t dim, uint8_t* out);
+int ql_kv_dequantize_q5_1(const uint8_t* in, int64_t rows, int64_t dim, float* x);
+
 /* --------------------------------------------------------------- paged decode attention
  * [FK] launch_paged_decode_attention / attention_paged, split-K over the context:
  *   out[b][h][:] = sum_{t < context_lens[b]} softmax_t(q[b][h] . K_t * scale) V_t

@@ -23,7 +23,9 @@ then 16 bytes whose byte l holds the low four bits of code l (low nibble) and of
     Decoded value: fma(f32(d), code, f32(m)) rounded once to f32. (d * code is exact in f32:
     an 11-bit mantissa times a 5-bit integer, so the fma is one f32 addition.)
 
-Inputs must be finite (the page's domain: projection outputs).
+Inputs must be finite (the page's domain: projection outputs). Reading where the page is
+silent: the sign of a zero block minimum (a -0 and a +0 both minimal) is not fixed by it; the
+minimum is taken as ``min + 0`` in f32, so a zero minimum is stored as +0.
 """
 from __future__ import annotations
 
@@ -104,7 +106,7 @@ def quantize_q5_1(rows) -> np.ndarray:
     """Rows [n, dim] -> bytes [n, q5_row_bytes(dim)]."""
     b = _blocks(rows)
     n, nblk, _ = b.shape
-    mn = np.min(b, axis=2)
+    mn = (np.min(b, axis=2) + np.float32(0.0)).astype(np.float32)   # a zero minimum is stored as +0
     mx = np.max(b, axis=2)
     d = ((mx - mn).astype(np.float32) / np.float32(31.0)).astype(np.float32)
     inv = _inverse(d)

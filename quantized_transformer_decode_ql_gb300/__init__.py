@@ -24,6 +24,8 @@ __all__ = [
     "ql_gemv_q4_0_stream_workspace_bytes", "ql_set_batched_gemv_form",
     "ql_paged_attn_workspace_bytes", "ql_paged_attn_decode", "ql_paged_attn_decode_noalloc",
     "ql_set_attn_merge_form", "ql_paged_attn_merge_form",
+    "ql_kv_q8_0_row_bytes", "ql_kv_q5_1_row_bytes", "ql_kv_quantize_q8_0", "ql_kv_dequantize_q8_0",
+    "ql_kv_quantize_q5_1", "ql_kv_dequantize_q5_1",
     "ql_fused_norm_rope",
     "ql_rope_tables", "ql_check_device_error", "BlockPool", "SIGNATURES",
 ]
@@ -85,6 +87,49 @@ def ql_paged_attn_merge_form(batch, n_heads, n_kv_heads, head_dim, max_blocks_pe
     if rc < 0:
         check(rc)
     return rc
+
+
+def ql_kv_q8_0_row_bytes(dim):
+    return int(lib().ql_kv_q8_0_row_bytes(dim))
+
+
+def ql_kv_q5_1_row_bytes(dim):
+    return int(lib().ql_kv_q5_1_row_bytes(dim))
+
+
+def _kv_quantize(fn, row_bytes, x):
+    import numpy as np
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    rows, dim = x.shape
+    out = np.zeros((rows, row_bytes(dim)), dtype=np.uint8)
+    check(fn(x.ctypes.data, rows, dim, out.ctypes.data))
+    return out
+
+
+def _kv_dequantize(fn, data, dim):
+    import numpy as np
+    data = np.ascontiguousarray(data, dtype=np.uint8)
+    x = np.zeros((data.shape[0], dim), dtype=np.float32)
+    check(fn(data.ctypes.data, data.shape[0], dim, x.ctypes.data))
+    return x
+
+
+def ql_kv_quantize_q8_0(x):
+    """Host codec: f32 rows [n, dim] numpy -> q8_0 bytes [n, ql_kv_q8_0_row_bytes(dim)]."""
+    return _kv_quantize(lib().ql_kv_quantize_q8_0, ql_kv_q8_0_row_bytes, x)
+
+
+def ql_kv_dequantize_q8_0(data, dim):
+    return _kv_dequantize(lib().ql_kv_dequantize_q8_0, data, dim)
+
+
+def ql_kv_quantize_q5_1(x):
+    """Host codec: f32 rows [n, dim] numpy -> q5_1 bytes [n, ql_kv_q5_1_row_bytes(dim)]."""
+    return _kv_quantize(lib().ql_kv_quantize_q5_1, ql_kv_q5_1_row_bytes, x)
+
+
+def ql_kv_dequantize_q5_1(data, dim):
+    return _kv_dequantize(lib().ql_kv_dequantize_q5_1, data, dim)
 
 
 def ql_gemv_q4_0_stream(w_stream, rows, cols, x, batch, y, epilogue=QL_EPI_NONE, workspace=None, stream=None):

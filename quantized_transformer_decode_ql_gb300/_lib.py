@@ -78,6 +78,12 @@ SIGNATURES = {
                                              c_int64, c_int, c_int, c_int, c_int, c_int64, c_int64,
                                              c_float, c_void_p, c_void_p]),
     "ql_set_attn_merge_form": (c_int, [c_int]),
+    "ql_kv_q8_0_row_bytes": (c_int64, [c_int64]),
+    "ql_kv_q5_1_row_bytes": (c_int64, [c_int64]),
+    "ql_kv_quantize_q8_0": (c_int, [c_void_p, c_int64, c_int64, c_void_p]),
+    "ql_kv_dequantize_q8_0": (c_int, [c_void_p, c_int64, c_int64, c_void_p]),
+    "ql_kv_quantize_q5_1": (c_int, [c_void_p, c_int64, c_int64, c_void_p]),
+    "ql_kv_dequantize_q5_1": (c_int, [c_void_p, c_int64, c_int64, c_void_p]),
     "ql_paged_attn_merge_form": (c_int, [c_int64, c_int, c_int, c_int, c_int64]),
     "ql_fused_norm_rope": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                    c_void_p, c_float, c_int64, c_int, c_int, c_int, c_void_p,

@@ -15,6 +15,7 @@
 
 #include "ql_f16.h"
 #include "ql_internal.h"
+#include "ql_kvq.h"
 
 namespace ql {
 
@@ -107,6 +108,57 @@ const char* ql_status_str(int s) {
 const char* ql_last_error(void) { return g_last_error.c_str(); }
 
 int ql_version(void) { return 1; }
+
+// ------------------------------------------------------------------ quantised KV rows
+// The q8_0 (keys) / q5_1 (values) row codecs of ql_kvq.h, on host rows.
+int64_t ql_kv_q8_0_row_bytes(int64_t dim) { return dim > 0 ? (dim + 31) / 32 * ql::kQ8Bytes : 0; }
+int64_t ql_kv_q5_1_row_bytes(int64_t dim) { return dim > 0 ? (dim + 31) / 32 * ql::kQ5Bytes : 0; }
+
+static int kv_quantize(const char* name, const float* x, int64_t rows, int64_t dim, uint8_t* out,
+                       int block_bytes, int (*block)(const float*, int, uint8_t*)) {
+    if (!x || !out) return set_error(QL_EINVAL, std::string(name) + ": null pointer");
+    if (rows <= 0 || dim <= 0) return set_error(QL_EINVAL, std::string(name) + ": need rows > 0 and dim > 0");
+    for (int64_t i = 0; i < rows * dim; ++i)
+        if (!std::isfinite(x[i]))
+            return set_error(QL_EINVAL, std::string(name) + ": non-finite value in row " + std::to_string(i / dim));
+    const int64_t nblk = (dim + 31) / 32, rb = nblk * block_bytes;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t j = 0; j < nblk; ++j) {
+            const int64_t e0 = j * 32;
+            const int n = (int)std::min<int64_t>(32, dim - e0);
+            if (block(x + r * dim + e0, n, out + r * rb + j * block_bytes))
+                return set_error(QL_EINVAL, std::string(name) + ": a block scale or minimum overflows f16 in row " +
+                                                std::to_string(r));
+        }
+    return QL_OK;
+}
+
+int ql_kv_quantize_q8_0(const float* x, int64_t rows, int64_t dim, uint8_t* out) {
+    return kv_quantize("ql_kv_quantize_q8_0", x, rows, dim, out, ql::kQ8Bytes, ql::kvq_q8_block);
+}
+
+int ql_kv_quantize_q5_1(const float* x, int64_t rows, int64_t dim, uint8_t* out) {
+    return kv_quantize("ql_kv_quantize_q5_1", x, rows, dim, out, ql::kQ5Bytes, ql::kvq_q5_block);
+}
+
+static int kv_dequantize(const char* name, const uint8_t* in, int64_t rows, int64_t dim, float* x,
+                         int block_bytes, float (*value)(const uint8_t*, int)) {
+    if (!in || !x) return set_error(QL_EINVAL, std::string(name) + ": null pointer");
+    if (rows <= 0 || dim <= 0) return set_error(QL_EINVAL, std::string(name) + ": need rows > 0 and dim > 0");
+    const int64_t rb = (dim + 31) / 32 * block_bytes;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t e = 0; e < dim; ++e)
+            x[r * dim + e] = value(in + r * rb + (e >> 5) * block_bytes, (int)(e & 31));
+    return QL_OK;
+}
+
+int ql_kv_dequantize_q8_0(const uint8_t* in, int64_t rows, int64_t dim, float* x) {
+    return kv_dequantize("ql_kv_dequantize_q8_0", in, rows, dim, x, ql::kQ8Bytes, ql::kvq_q8_value);
+}
+
+int ql_kv_dequantize_q5_1(const uint8_t* in, int64_t rows, int64_t dim, float* x) {
+    return kv_dequantize("ql_kv_dequantize_q5_1", in, rows, dim, x, ql::kQ5Bytes, ql::kvq_q5_value);
+}
 
 // ------------------------------------------------------------------ q4_0 codec
 static void parallel_rows(int64_t rows, int64_t min_rows_per_task,
