@@ -166,6 +166,19 @@ int ql_kv_quantize_q8_0(const float* x, int64_t rows, int64_t dim, uint8_t* out)
 int ql_kv_dequantize_q8_0(const uint8_t* in, int64_t rows, int64_t dim, float* x);
 int ql_kv_quantize_q5_1(const float* x, int64_t rows, int64_t dim, uint8_t* out);
 int ql_kv_dequantize_q5_1(const uint8_t* in, int64_t rows, int64_t dim, float* x);
+/* The same codecs on the GPU, bit-identical to the host ones (both run one set of block
+ * routines): d_x device f32 [rows][dim], d_out / d_in device bytes [rows][row bytes],
+ * asynchronous on the stream. A non-finite value, or a scale or minimum that overflows f16,
+ * is recorded in the device error record (ql_check_device_error) and the block's bytes are
+ * still written. QL_EINVAL for NULL pointers or rows / dim <= 0.                          */
+int ql_kv_quantize_q8_0_device(const float* d_x, int64_t rows, int64_t dim, uint8_t* d_out,
+                               void* stream);
+int ql_kv_dequantize_q8_0_device(const uint8_t* d_in, int64_t rows, int64_t dim, float* d_x,
+                                 void* stream);
+int ql_kv_quantize_q5_1_device(const float* d_x, int64_t rows, int64_t dim, uint8_t* d_out,
+                               void* stream);
+int ql_kv_dequantize_q5_1_device(const uint8_t* d_in, int64_t rows, int64_t dim, float* d_x,
+                                 void* stream);
 
 /* --------------------------------------------------------------- paged decode attention
  * [FK] launch_paged_decode_attention / attention_paged, split-K over the context:

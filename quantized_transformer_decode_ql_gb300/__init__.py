@@ -25,7 +25,7 @@ __all__ = [
     "ql_paged_attn_workspace_bytes", "ql_paged_attn_decode", "ql_paged_attn_decode_noalloc",
     "ql_set_attn_merge_form", "ql_paged_attn_merge_form",
     "ql_kv_q8_0_row_bytes", "ql_kv_q5_1_row_bytes", "ql_kv_quantize_q8_0", "ql_kv_dequantize_q8_0",
-    "ql_kv_quantize_q5_1", "ql_kv_dequantize_q5_1",
+    "ql_kv_quantize_q5_1", "ql_kv_dequantize_q5_1", "ql_kv_quantize_device", "ql_kv_dequantize_device",
     "ql_fused_norm_rope",
     "ql_rope_tables", "ql_check_device_error", "BlockPool", "SIGNATURES",
 ]
@@ -130,6 +130,18 @@ def ql_kv_quantize_q5_1(x):
 
 def ql_kv_dequantize_q5_1(data, dim):
     return _kv_dequantize(lib().ql_kv_dequantize_q5_1, data, dim)
+
+
+def ql_kv_quantize_device(x, out, fmt="q8_0", stream=None):
+    """Device codec: ``x`` f32 [rows, dim] CUDA tensor -> ``out`` uint8 [rows, row bytes]."""
+    fn = lib().ql_kv_quantize_q8_0_device if fmt == "q8_0" else lib().ql_kv_quantize_q5_1_device
+    check(fn(ptr(x), x.shape[0], x.shape[1], ptr(out), stream_ptr(stream)))
+
+
+def ql_kv_dequantize_device(data, x, fmt="q8_0", stream=None):
+    """Device codec: ``data`` uint8 [rows, row bytes] -> ``x`` f32 [rows, dim] CUDA tensor."""
+    fn = lib().ql_kv_dequantize_q8_0_device if fmt == "q8_0" else lib().ql_kv_dequantize_q5_1_device
+    check(fn(ptr(data), x.shape[0], x.shape[1], ptr(x), stream_ptr(stream)))
 
 
 def ql_gemv_q4_0_stream(w_stream, rows, cols, x, batch, y, epilogue=QL_EPI_NONE, workspace=None, stream=None):

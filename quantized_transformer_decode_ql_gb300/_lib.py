@@ -84,6 +84,10 @@ SIGNATURES = {
     "ql_kv_dequantize_q8_0": (c_int, [c_void_p, c_int64, c_int64, c_void_p]),
     "ql_kv_quantize_q5_1": (c_int, [c_void_p, c_int64, c_int64, c_void_p]),
     "ql_kv_dequantize_q5_1": (c_int, [c_void_p, c_int64, c_int64, c_void_p]),
+    "ql_kv_quantize_q8_0_device": (c_int, [c_void_p, c_int64, c_int64, c_void_p, c_void_p]),
+    "ql_kv_dequantize_q8_0_device": (c_int, [c_void_p, c_int64, c_int64, c_void_p, c_void_p]),
+    "ql_kv_quantize_q5_1_device": (c_int, [c_void_p, c_int64, c_int64, c_void_p, c_void_p]),
+    "ql_kv_dequantize_q5_1_device": (c_int, [c_void_p, c_int64, c_int64, c_void_p, c_void_p]),
     "ql_paged_attn_merge_form": (c_int, [c_int64, c_int, c_int, c_int, c_int64]),
     "ql_fused_norm_rope": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                    c_void_p, c_float, c_int64, c_int, c_int, c_int, c_void_p,

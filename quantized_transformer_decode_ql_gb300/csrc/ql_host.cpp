@@ -81,6 +81,8 @@ static const char* where_name(int w) {
         case kErrPackOverflow: return "q4_0 pack: block scale overflows f16";
         case kErrGemvStage: return "gemv: a staged weight copy did not arrive (bounded wait expired)";
         case kErrStepBarrier: return "persistent step: a grid barrier wait ran out (index = barrier, value = CTA)";
+        case kErrKvNonFinite: return "KV row quantiser: non-finite value (index = row, value = block)";
+        case kErrKvOverflow: return "KV row quantiser: block scale or minimum overflows f16 (index = row, value = block)";
         default: return "unknown";
     }
 }

@@ -45,6 +45,8 @@ enum DevErrWhere {
     kErrPackOverflow = 7,
     kErrGemvStage = 8,
     kErrStepBarrier = 9,
+    kErrKvNonFinite = 10,
+    kErrKvOverflow = 11,
 };
 // The current device's record (allocated on first use, zero-filled).
 DevError* device_error_record();
