@@ -191,6 +191,10 @@ int ql_kv_dequantize_q5_1_device(const uint8_t* d_in, int64_t rows, int64_t dim,
  * [1, max_blocks_per_seq * block_size] (0 is allowed and marks an idle slot: its output is
  * left untouched). d_out: f16 [batch][n_heads * head_dim].
  * head_dim in {64, 128}; block_size 16; n_heads % n_kv_heads == 0, group <= 8.
+ * Alignment: d_k_pool and d_v_pool 16-byte, d_q and d_out 4-byte (QL_EINVAL otherwise; nothing
+ * is launched). A length above max_blocks_per_seq * block_size, or a block id outside
+ * [0, num_blocks), is skipped on the device and recorded in the device error record; the output
+ * row of such a sequence is then undefined.
  * d_workspace: ql_paged_attn_workspace_bytes(...) bytes, ZERO-FILLED before its first use
  * (the kernels leave it zero-filled again for the next call); one workspace per stream.  */
 size_t ql_paged_attn_workspace_bytes(int64_t batch, int n_heads, int n_kv_heads,
@@ -215,8 +219,12 @@ int ql_paged_attn_decode(const void* d_q, const void* d_k_pool, const void* d_v_
  * make that first call before any stream capture. Every call clears the part of the array
  * that must start at zero, then shares the rest with every other call: calls whose kernels
  * overlap on the GPU (two streams, or two host threads) race on it and must be serialised by
- * the caller. Out-of-range block ids or lengths are skipped; they are recorded for
- * ql_check_device_error only if another libql call already created this device's record.  */
+ * the caller. The alignment rules and the host-side checks are those of ql_paged_attn_decode
+ * (a misaligned pointer is QL_EINVAL and nothing is launched). Out-of-range block ids or lengths
+ * are skipped on the device and the output rows of those sequences are undefined; they are
+ * recorded for ql_check_device_error only if another libql call already created this device's
+ * record. The looked-up address is kept for the life of the process: do not use this entry
+ * point on a device after cudaDeviceReset.                                                 */
 int ql_paged_attn_decode_noalloc(const void* d_q, const void* d_k_pool, const void* d_v_pool,
                                  const int32_t* d_block_tables, const int32_t* d_context_lens,
                                  int64_t batch, int n_heads, int n_kv_heads, int head_dim,

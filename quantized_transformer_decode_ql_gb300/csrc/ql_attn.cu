@@ -794,6 +794,19 @@ size_t attn_workspace_bytes(int64_t batch, int n_heads, int n_kv_heads, int head
     return layout(batch, n_heads, n_kv_heads, head_dim, max_blocks_per_seq, num_sms()).total;
 }
 
+// Alignment the kernel's accesses need: 16-byte cp.async staging of the K/V pools, 32-bit loads
+// of q (the non-fused form reads a head row as uint32 pairs) and half2 stores of the output.
+// Checked on the host by every entry point, so a misaligned buffer is QL_EINVAL, never a launch.
+int attn_check_alignment(const void* q, const void* k_pool, const void* v_pool, const void* out,
+                         const char* who) {
+    const uintptr_t kv = reinterpret_cast<uintptr_t>(k_pool) | reinterpret_cast<uintptr_t>(v_pool);
+    if ((kv & 15) != 0 || (reinterpret_cast<uintptr_t>(out) & 3) != 0 ||
+        (reinterpret_cast<uintptr_t>(q) & 3) != 0)
+        return set_error(QL_EINVAL, std::string(who) +
+                                        ": K/V pools must be 16-byte aligned, q and the output 4-byte aligned");
+    return QL_OK;
+}
+
 int attn_launch(const AttnArgs& a, cudaStream_t s, bool pdl) {
     QL_REQUIRE((a.q || a.qkv) && a.k_pool && a.v_pool && a.block_tables && a.out && a.workspace,
                "attention: null pointer");
@@ -812,9 +825,7 @@ int attn_launch(const AttnArgs& a, cudaStream_t s, bool pdl) {
     const Layout lo = layout(a.batch, a.n_heads, a.n_kv_heads, a.head_dim, a.max_blocks_per_seq, num_sms());
     if (a.workspace_bytes < lo.total)
         return set_error(QL_EINVAL, "attention: workspace too small (need " + std::to_string(lo.total) + " bytes)");
-    QL_REQUIRE(((reinterpret_cast<uintptr_t>(a.k_pool) | reinterpret_cast<uintptr_t>(a.v_pool)) & 15) == 0 &&
-                   (reinterpret_cast<uintptr_t>(a.out) & 3) == 0 && (reinterpret_cast<uintptr_t>(a.q) & 1) == 0,
-               "attention: K/V pools must be 16-byte aligned, the output 4-byte aligned");
+    if (int rc = attn_check_alignment(a.q, a.k_pool, a.v_pool, a.out, "attention")) return rc;
     if (!device_error_record()) return set_error(QL_ECUDA, "attention: no device error record");
     if (int rc = attn_prepare()) return rc;
     AParams p = {};
@@ -955,6 +966,7 @@ extern "C" int ql_paged_attn_decode_noalloc(const void* d_q, const void* d_k_poo
     QL_REQUIRE(max_blocks_per_seq >= 1 && max_blocks_per_seq * kBS < (1ll << 31),
                "ql_paged_attn_decode_noalloc: bad max_blocks_per_seq");
     QL_REQUIRE(num_blocks >= 1, "ql_paged_attn_decode_noalloc: bad num_blocks");
+    if (int rc = attn_check_alignment(d_q, d_k_pool, d_v_pool, d_out, "ql_paged_attn_decode_noalloc")) return rc;
     const Layout lo = layout(batch, n_heads, n_kv_heads, head_dim, max_blocks_per_seq, num_sms());
     if (lo.total > kNoAllocScratchBytes)
         return set_error(QL_EINVAL, "ql_paged_attn_decode_noalloc: this shape needs " +

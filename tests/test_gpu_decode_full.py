@@ -5,9 +5,11 @@ vocabulary and lm_head), in the configurations the benchmark times: batch 1 over
 2048-position pre-filled context (the stream GEMVs at batch 1, 8-warp attention) and batch 32
 over mixed context lengths (the split-K batched GEMVs, in both tensor-core forms, and their
 merge kernels). Weights are
-drawn on the GPU (``ql_inputs.device_tensor_fn``) and packed there; the oracle decodes from
-those same q4_0 codes, copied back (the device codec is pinned bit-exactly against the
-oracle's elsewhere), over the same f16 contexts, in f64 with the lm_head taken in row chunks.
+drawn on the GPU (``ql_inputs.device_tensor_fn``) and packed there by ``ql_q4_0_pack_device``.
+``test_device_codes_are_the_oracles`` first checks those codes, every byte of every matrix kind,
+against the oracle's own quantisation (``oracle.q4_0.quantize``) of the same f32 draws copied to
+the host; the step tests then hand the oracle those q4_0 codes and the same f16 contexts, and it
+decodes in f64 with the lm_head taken in row chunks.
 
 Every logit of every sequence is compared with the step tolerance
 (``|got - want| <= 2e-2 + 1e-2 |want|``), and the greedy token must equal the oracle's
@@ -42,6 +44,30 @@ def oracle_model(gm):
         d.update({n: q4(L[n]) for n in ("wqkv", "wo", "wgu", "wd")})
         layers.append(d)
     return decode.Q4Model.from_codes(CFG, layers, host(gm.final_norm), q4(gm.lm_head))
+
+
+def test_device_codes_are_the_oracles():
+    """Every byte the device quantiser wrote for the two layers and the full lm_head equals the
+    oracle's quantisation of the same f32 draw: q4_0 packing must be bit-exact."""
+    from oracle import q4_0 as oq
+    from quantized_transformer_decode_ql_gb300.model import DeviceModel
+    lib()
+    fn = ql_inputs.device_tensor_fn(CFG, seed=0)
+    gm = DeviceModel.from_layer_fn(CFG, fn, num_blocks=4, max_batch=1, max_blocks_per_seq=4)
+    try:
+        mats = [(li, n, gm.layers[li][n]) for li in range(CFG.n_layers) for n in ("wqkv", "wo", "wgu", "wd")]
+        mats.append((None, "lm_head", gm.lm_head))
+        for li, name, T in mats:
+            w = fn(li, name)
+            s_dev, q_dev = host(T.scales).view(np.uint16), host(T.quants)
+            step = 8192
+            for r0 in range(0, T.rows, step):
+                s_ref, q_ref = oq.quantize(host(w[r0:r0 + step]))
+                assert np.array_equal(s_dev[r0:r0 + step], s_ref), (li, name, r0)
+                assert np.array_equal(q_dev[r0:r0 + step], q_ref), (li, name, r0)
+            del w
+    finally:
+        gm.close()
 
 
 @pytest.mark.parametrize("B,form", [(1, "mma_sync"), (32, "mma_sync"), (32, "tcgen05")])
