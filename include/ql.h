@@ -115,10 +115,11 @@ int ql_q4_0_stream_pack(const void* d_scales, const void* d_quants, int64_t rows
 /* [IL] CudaQwen3::gemv at batch 1-32 from the tile stream: y = epilogue(W x).
  * d_x: f16 [batch][cols], 16-byte aligned. epilogue QL_EPI_NONE: d_y f32 [batch][rows];
  * QL_EPI_ADD_RESIDUAL: d_y f32 [batch][rows], y += W x in place; QL_EPI_SILU_MUL (d_stream
- * packed with silu): d_y f16 [batch][rows/2]. Batch 1-2: each code becomes q - 8 (low nibble)
- * or 16 (q - 8) (high nibble, against x/16) exactly in f16, the 32 products of a block are
- * summed in f16 (HFMA2; low and high nibbles apart), and each block is scaled by its f16 scale
- * and accumulated in f32. Batch 3-32 (needs cols in 128..896 or a multiple of 1024): the
+ * packed with silu): d_y f16 [batch][rows/2]. Batch 1-2: the activations are taken to 16-bit
+ * fixed point with one power-of-two scale per 32-element block (x_int = round(x 2^s), |x_int|
+ * < 2^15, relative error at most 2^-15 of the block's largest value); the products of codes and
+ * x_int and each block's sum are exact 32-bit integers (dp2a), the -8 offset is subtracted
+ * exactly, and each block is scaled by its f16 scale and 2^-s and accumulated in f32. Batch 3-32 (needs cols in 128..896 or a multiple of 1024): the
  * tensor-core form (A = (q - 8) d rounded once to f16, f16 x, f32 products and sums), split
  * over K in windows of 1024 columns so that every weight byte is streamed once; each window's
  * f32 partial sums go to d_workspace and a second kernel adds them in window order

@@ -23,10 +23,11 @@
 //    (tile, 4-block group) units, so every warp streams the same number of bytes; a tile shared
 //    by several warps is reduced in shared memory in warp order (deterministic), the others are
 //    finished from registers;
-//  * the GEMV arithmetic is the one of the stand-alone q4_0 GEMV: nibbles OR'ed into the
-//    mantissa of 1024.0h give 1024 + q (low) and 1024 + 16 q (high, against activations staged
-//    pre-divided by 16) exactly; mma.sync m16n8k16 (f16 in, f32 accumulate) does the products;
-//    the offsets are folded into the accumulator start; one FFMA per block applies the scale;
+//  * the GEMV arithmetic: activations staged once per CTA as 16-bit fixed point with one
+//    power-of-two scale per 32-element block; the codes masked into bytes (q and 16 q) and
+//    multiplied by dp2a, so that the products and each block's sum are exact integers; the -8
+//    offset enters as a staged per-block term; per row and block one I2F, FMUL and FFMA apply the
+//    f16 scale and the activation scale in f32 (gemv_phase);
 //  * attention: one CTA per (sequence, kv head, split), each warp one 16-token block at a
 //    time. K is loaded straight into MMA fragments with 16-byte loads (head_dim permuted the
 //    same way in Q and K, which leaves the dot products unchanged), S = Q K^T on mma.sync,
@@ -62,8 +63,10 @@ enum Epi { kEpiF32 = 0, kEpiResid = 1, kEpiSilu = 2, kEpiLogits = 3 };
 
 // Shared memory behind the rings: the GEMV staging (activations, offset terms, partials) or
 // the attention merge buffers, whichever is larger.
+// GEMV staging per batch column: the 16-bit activations ((max_nblk * 4 + 4) x 16 B) and the
+// per-block offset terms and scales ((max_nblk + 4) x 8 B); then the warps' parked tile partials.
 __host__ __device__ constexpr size_t gemv_region_bytes(int batch, int max_nblk, int warps = kW) {
-    return (size_t)batch * (max_nblk * 4 + 4) * 16 + (size_t)warps * 2 * 32 * 16;
+    return (size_t)batch * (max_nblk * 4 + 4) * 16 + (size_t)batch * (max_nblk + 4) * 8 + (size_t)warps * 2 * 32 * 16;
 }
 __host__ __device__ constexpr size_t attn_region_bytes(int head_dim, int group) {
     return (size_t)kW * (group * head_dim > 128 ? group * head_dim : 128) * 4 + (size_t)2 * kW * group * 4;
@@ -93,6 +96,19 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
         "{%8,%9}, {%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two-way dot product of two signed 16-bit activations (a) with two unsigned bytes of b (bytes
+// 0-1 for .lo, 2-3 for .hi), accumulated exactly in 32 bits: c + a.h0 * b.bk + a.h1 * b.bk+1.
+__device__ __forceinline__ int dp2a_lo(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp2a.lo.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ int dp2a_hi(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp2a.hi.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
 }
 
 // ------------------------------------------------------------------------------ grid barrier
@@ -312,19 +328,29 @@ __device__ __forceinline__ Hot hot_scalars(const PersistParams& p) {
     asm volatile("" : "+r"(h.B), "+r"(h.max_nblk), "+f"(h.eps));
     return h;
 }
-// Stage the activations of all B columns in f16: per column and block j, 4 chunks of 16 bytes
-// (chunk t: f16 pairs (x0, x2), (x1, x3), (x16, x18)/16, (x17, x19)/16 of elements 32 j + 4 t
-// + ...: the pairs that one 32-bit code word expands to, the high-nibble ones pre-divided by 16,
-// which is exact). RMS: the input is the f32 residual stream, normalised (RMSNorm with weight
-// w) on the way; the first kHeld items of a thread and their weights are loaded together and
-// stay in registers between the two passes. f16 input: kChunk items per thread are loaded
-// together. Data written earlier in the launch by other CTAs is read with ld.global.cg (L2).
+// Stage the activations of all B columns as 16-bit fixed point, one power-of-two scale per
+// 32-element block: x_int = rint(x 2^s), with s the largest shift that keeps the block's largest
+// |x| (times 1.001, a margin for the rounding) below 2^15. The scaling is exact; the rounding is
+// the only error, at most 2^-(s+1) per element, relative 2^-15 of the block's largest value. Per
+// column and block j: 4 chunks of 16 bytes (chunk t: int16 pairs (x[4t], x[4t+1]), (x[4t+2],
+// x[4t+3]), (x[16+4t], x[17+4t]), (x[18+4t], x[19+4t]) of the block's elements: the order in which
+// code word t holds their nibbles), and the block's pair (-128 sum_e x_int[e], 2^-(s+4)): the
+// offset term of the codes' -8 (times the 16 of the high nibbles' scale, see gemv_phase) and the
+// factor that undoes both scalings. rint is the round-to-nearest-even of an FFMA that adds
+// 1.5 * 2^23, whose low 16 bits are then the integer. RMS: the input is the f32 residual stream,
+// normalised (RMSNorm with weight w) on the way; the first kHeld items of a thread and their
+// weights stay in registers between the two passes. f16 input: kHeld items per thread are loaded
+// together. The 4 chunks of a block are 4 consecutive items (lanes 4k..4k+3 of a warp): their
+// largest magnitude and their sum take two shuffles each. Data written earlier in the launch by
+// other CTAs is read with ld.global.cg (L2).
 template <bool RMS, int W>
-__device__ __noinline__ void stage_x(int B, float eps, int nblk, int cstride, const float* xf,
-                                     const __half* x16, const float* w, uint4* xs) {
-    constexpr int kHeld = 2, kChunk = 4, kT = W * 32;
+__device__ __noinline__ void stage_x(int B, float eps, int nblk, int cstride, const float* xf, const __half* x16,
+                                     const float* w, uint4* xs, int2* sxs, int sxstride) {
+    constexpr int kHeld = RMS ? 2 : 4, kT = W * 32;
+    constexpr uint32_t kMagic = 0x4B400000u;   // bits of 1.5 * 2^23
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cols = nblk * 32, nitems = B * nblk * 4;
+    const int rounds = (nitems + kT - 1) / kT;
 
     // item -> (column b, block j, chunk t) and its element offset
     auto where = [&](int item, int& b, int& j, int& t) -> size_t {
@@ -334,65 +360,98 @@ __device__ __noinline__ void stage_x(int B, float eps, int nblk, int cstride, co
         j = bj - b * nblk;
         return (size_t)b * cols + 32 * j + 4 * t;
     };
-    auto load_f32 = [&](const float* src, size_t off, float (&v)[8]) {
-        const float4 a = __ldcg(reinterpret_cast<const float4*>(src + off));
-        const float4 h = __ldcg(reinterpret_cast<const float4*>(src + off + 16));
-        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-        v[4] = h.x; v[5] = h.y; v[6] = h.z; v[7] = h.w;
+    // the item's 8 values: elements 4t..4t+3 and 16+4t..19+4t of its block
+    auto load = [&](int item, float (&v)[8]) {
+        int b, j, t;
+        const size_t off = where(item, b, j, t);
+        if (RMS) {
+            const float4 a = __ldcg(reinterpret_cast<const float4*>(xf + off));
+            const float4 h = __ldcg(reinterpret_cast<const float4*>(xf + off + 16));
+            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+            v[4] = h.x; v[5] = h.y; v[6] = h.z; v[7] = h.w;
+        } else {
+            const uint2 a = __ldcg(reinterpret_cast<const uint2*>(x16 + off));
+            const uint2 h = __ldcg(reinterpret_cast<const uint2*>(x16 + off + 16));
+            const float2 f0 = __half22float2(as_h2(a.x)), f1 = __half22float2(as_h2(a.y));
+            const float2 f2 = __half22float2(as_h2(h.x)), f3 = __half22float2(as_h2(h.y));
+            v[0] = f0.x; v[1] = f0.y; v[2] = f1.x; v[3] = f1.y;
+            v[4] = f2.x; v[5] = f2.y; v[6] = f3.x; v[7] = f3.y;
+        }
     };
-    auto load_w = [&](int j, int t, float (&v)[8]) {
+    auto load_w = [&](int item, float (&v)[8]) {
+        const int j = (item >> 2) % nblk, t = item & 3;
         const float4 a = __ldg(reinterpret_cast<const float4*>(w + 32 * j + 4 * t));
         const float4 h = __ldg(reinterpret_cast<const float4*>(w + 32 * j + 16 + 4 * t));
         v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
         v[4] = h.x; v[5] = h.y; v[6] = h.z; v[7] = h.w;
     };
-    auto emit = [&](int item, const float (&v)[8]) {
-        int b, j, t;
-        where(item, b, j, t);
-        const __half2 p0 = __floats2half2_rn(v[0], v[2]);
-        const __half2 p1 = __floats2half2_rn(v[1], v[3]);
-        const __half2 p2 = __floats2half2_rn(__half2float(__float2half_rn(v[4])) * 0.0625f,
-                                             __half2float(__float2half_rn(v[6])) * 0.0625f);
-        const __half2 p3 = __floats2half2_rn(__half2float(__float2half_rn(v[5])) * 0.0625f,
-                                             __half2float(__float2half_rn(v[7])) * 0.0625f);
-        xs[(size_t)b * cstride + 4 * j + t] = make_uint4(as_u32(p0), as_u32(p1), as_u32(p2), as_u32(p3));
+    // fixed point of one item (all lanes of the warp call it: its shuffles pair the 4 lanes of a
+    // block, which are in range together)
+    auto emit = [&](int item, bool ok, const float (&v)[8]) {
+        float m = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        // s = 14 - floor(log2(1.001 m)): |x| 2^s < 2^15 / 1.001 (the exponent field; a zero or
+        // subnormal block gives a large s, clamped so that 2^s and 2^-(s+4) stay normal floats)
+        const int e = (int)((__float_as_uint(m * 1.001f) >> 23) & 0xFFu) - 127;
+        int sh = 14 - e;
+        sh = sh > 100 ? 100 : (sh < -100 ? -100 : sh);
+        const float sc = __uint_as_float((uint32_t)(sh + 127) << 23);
+        uint32_t u[8], sum = 0u;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            u[i] = __float_as_uint(fmaf(v[i], sc, 12582912.0f));   // kMagic + rint(x 2^s)
+            sum += u[i];
+        }
+        int n = (int)(sum - 8u * kMagic);   // the 8 integers' sum (exact: wraps back into range)
+        n += __shfl_xor_sync(0xffffffffu, n, 1);
+        n += __shfl_xor_sync(0xffffffffu, n, 2);
+        if (ok) {
+            int b, j, t;
+            where(item, b, j, t);
+            xs[(size_t)b * cstride + 4 * j + t] =
+                make_uint4(__byte_perm(u[0], u[1], 0x5410), __byte_perm(u[2], u[3], 0x5410),
+                           __byte_perm(u[4], u[5], 0x5410), __byte_perm(u[6], u[7], 0x5410));
+            if (t == 0) sxs[b * sxstride + j] = make_int2(-128 * n, (int)((uint32_t)(127 - sh - 4) << 23));
+        }
     };
 
+    float hx[kHeld][8], hw[kHeld][8];
+#pragma unroll
+    for (int r = 0; r < kHeld; ++r)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) hx[r][i] = hw[r][i] = 0.f;
+#pragma unroll
+    for (int r = 0; r < kHeld; ++r) {
+        const int item = tid + r * kT;
+        if (item < nitems) {
+            load(item, hx[r]);
+            if (RMS) load_w(item, hw[r]);
+        }
+    }
+    float rs0 = 1.0f, rs1 = 1.0f;
     if (RMS) {
-        float hx[kHeld][8], hw[kHeld][8];
+        // per column, the mean square: thread sums, warp sums, then the warps' in warp order (a
+        // shared array of this function: direct shared-memory accesses); column 1 only at batch 2
         float ss0 = 0.f, ss1 = 0.f;
         const float inv_cols = 1.0f / (float)cols;   // while the loads are in flight
 #pragma unroll
         for (int r = 0; r < kHeld; ++r) {
-            const int item = tid + r * kT;
-            if (item < nitems) {
-                int b, j, t;
-                const size_t off = where(item, b, j, t);
-                load_f32(xf, off, hx[r]);
-                load_w(j, t, hw[r]);
-            }
-        }
-#pragma unroll
-        for (int r = 0; r < kHeld; ++r) {
-            const int item = tid + r * kT;
-            if (item < nitems) {
-                float s2 = 0.f;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) s2 += hx[r][i] * hx[r][i];
-                if (item < nblk * 4) ss0 += s2; else ss1 += s2;
-            }
-        }
-        for (int item = tid + kHeld * kT; item < nitems; item += kT) {
-            int b, j, t;
-            float v[8];
-            load_f32(xf, where(item, b, j, t), v);
             float s2 = 0.f;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) s2 += v[i] * v[i];
+            for (int i = 0; i < 8; ++i) s2 = fmaf(hx[r][i], hx[r][i], s2);
+            if (tid + r * kT < nblk * 4) ss0 += s2; else ss1 += s2;
+        }
+        for (int item = tid + kHeld * kT; item < nitems; item += kT) {
+            float v[8];
+            load(item, v);
+            float s2 = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) s2 = fmaf(v[i], v[i], s2);
             if (item < nblk * 4) ss0 += s2; else ss1 += s2;
         }
-        // warp sums, then the warps' in warp order (a shared array of this function: direct
-        // shared-memory accesses); the second column only at batch 2
 #pragma unroll
         for (int o = 16; o; o >>= 1) ss0 += __shfl_xor_sync(0xffffffffu, ss0, o);
         if (B > 1) {
@@ -409,76 +468,67 @@ __device__ __noinline__ void stage_x(int B, float eps, int nblk, int cstride, co
             a0 += v.x;
             a1 += v.y;
         }
-        const float rs0 = rsqrtf(fmaf(a0, inv_cols, eps));
-        const float rs1 = rsqrtf(fmaf(a1, inv_cols, eps));
+        rs0 = rsqrtf(fmaf(a0, inv_cols, eps));
+        rs1 = rsqrtf(fmaf(a1, inv_cols, eps));
+    }
 #pragma unroll
-        for (int r = 0; r < kHeld; ++r) {
+    for (int r = 0; r < kHeld; ++r) {
+        if (r < rounds) {   // uniform over the CTA: every lane of a warp takes the shuffles
             const int item = tid + r * kT;
-            if (item < nitems) {
-                const float rr = item < nblk * 4 ? rs0 : rs1;
-                float v[8];
+            const float rr = item < nblk * 4 ? rs0 : rs1;
+            float v[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) v[i] = hx[r][i] * rr * hw[r][i];
-                emit(item, v);
-            }
+            for (int i = 0; i < 8; ++i) v[i] = RMS ? hx[r][i] * rr * hw[r][i] : hx[r][i];
+            emit(item, item < nitems, v);
         }
-        for (int item = tid + kHeld * kT; item < nitems; item += kT) {
-            int b, j, t;
-            float v[8], wv[8];
-            load_f32(xf, where(item, b, j, t), v);
-            load_w(j, t, wv);
-            const float rr = b == 0 ? rs0 : rs1;
+    }
+    for (int r = kHeld; r < rounds; ++r) {
+        const int item = tid + r * kT;
+        const bool ok = item < nitems;
+        const float rr = item < nblk * 4 ? rs0 : rs1;
+        float v[8], wv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = wv[i] = 0.f;
+        if (ok) {
+            load(item, v);
+            if (RMS) load_w(item, wv);
+        }
+        if (RMS) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) v[i] *= rr * wv[i];
-            emit(item, v);
         }
-    } else {
-        for (int base = 0; base < nitems; base += kChunk * kT) {
-            uint2 ra[kChunk], rh[kChunk];
-#pragma unroll
-            for (int c = 0; c < kChunk; ++c) {
-                const int item = base + c * kT + tid;
-                if (item < nitems) {
-                    int b, j, t;
-                    const size_t off = where(item, b, j, t);
-                    ra[c] = __ldcg(reinterpret_cast<const uint2*>(x16 + off));
-                    rh[c] = __ldcg(reinterpret_cast<const uint2*>(x16 + off + 16));
-                }
-            }
-#pragma unroll
-            for (int c = 0; c < kChunk; ++c) {
-                const int item = base + c * kT + tid;
-                if (item < nitems) {
-                    const float2 f0 = __half22float2(as_h2(ra[c].x)), f1 = __half22float2(as_h2(ra[c].y));
-                    const float2 f2 = __half22float2(as_h2(rh[c].x)), f3 = __half22float2(as_h2(rh[c].y));
-                    const float v[8] = {f0.x, f0.y, f1.x, f1.y, f2.x, f2.y, f3.x, f3.y};
-                    emit(item, v);
-                }
-            }
-        }
+        emit(item, ok, v);
     }
 }
 
-// Epilogue of one finished 16-row tile. acc[b] is this lane's half-row sum for column b (row
-// lane & 15 of the tile, blocks of half lane >> 4); the halves are added here, then lanes
-// 0..15 hold rows 0..15 (SiLU*up: rows 0..7 gate, 8..15 the matching up rows). All 32 lanes
-// of the warp call it. Out of line: it runs once per tile, and the unit loop stays small.
+// Epilogue of one finished 16-row tile. acc[b][0] / acc[b][1] are this lane's sums of rows
+// (lane & 7) and (lane & 7) + 8 of the tile over the blocks of its quarter (lane >> 3) of every
+// unit, for column b; the quarters are added here (lanes l, l ^ 8, l ^ 16, l ^ 24), then
+// lanes 0..15 hold rows 0..15 (SiLU*up:
+// lane l < 8 holds gate row l and its up row l + 8). All 32 lanes of the warp call it. Out of
+// line: it runs once per tile, and the unit loop stays small.
 template <int NB>
-__device__ __noinline__ void finish_tile(const PersistParams& p, const PMat& M, int epi, int tile, const float (&acc)[NB],
-                                         void* y, int ld, unsigned long long (&best)[NB], int lane) {
-    float v[NB];
+__device__ __noinline__ void finish_tile(const PersistParams& p, const PMat& M, int epi, int tile,
+                                         const float (&acc)[NB][2], void* y, int ld, unsigned long long (&best)[NB],
+                                         int lane) {
+    float v0[NB], v1[NB];
 #pragma unroll
-    for (int b = 0; b < NB; ++b) v[b] = acc[b] + __shfl_xor_sync(0xffffffffu, acc[b], 16);
+    for (int b = 0; b < NB; ++b) {
+        float a = acc[b][0], c = acc[b][1];
+        a += __shfl_xor_sync(0xffffffffu, a, 8);
+        c += __shfl_xor_sync(0xffffffffu, c, 8);
+        a += __shfl_xor_sync(0xffffffffu, a, 16);
+        c += __shfl_xor_sync(0xffffffffu, c, 16);
+        v0[b] = a;
+        v1[b] = c;
+    }
     const int hr = lane & 15;
     if (epi == kEpiSilu) {
-        float up[NB];
-#pragma unroll
-        for (int b = 0; b < NB; ++b) up[b] = __shfl_down_sync(0xffffffffu, v[b], 8);
         const int i = tile * 8 + hr;
         if (lane < 8 && i < (M.rows >> 1)) {
             __half* act = static_cast<__half*>(y);
 #pragma unroll
-            for (int b = 0; b < NB; ++b) act[(size_t)b * ld + i] = __float2half_rn(silu(v[b]) * up[b]);
+            for (int b = 0; b < NB; ++b) act[(size_t)b * ld + i] = __float2half_rn(silu(v0[b]) * v1[b]);
         }
         return;
     }
@@ -487,13 +537,14 @@ __device__ __noinline__ void finish_tile(const PersistParams& p, const PMat& M, 
         float* yf = static_cast<float*>(y);
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
+            const float v = hr < 8 ? v0[b] : v1[b];
             float* dst = yf + (size_t)b * ld + row;
             if (epi == kEpiResid) {
-                *dst = __ldcg(dst) + v[b];
+                *dst = __ldcg(dst) + v;
             } else {
-                *dst = v[b];
+                *dst = v;
                 if (epi == kEpiLogits) {
-                    const unsigned long long key = argmax_key(v[b], row);
+                    const unsigned long long key = argmax_key(v, row);
                     best[b] = key > best[b] ? key : best[b];
                 }
             }
@@ -503,13 +554,16 @@ __device__ __noinline__ void finish_tile(const PersistParams& p, const PMat& M, 
 
 // One GEMV phase of the step: y = epilogue(W x) for this CTA's tiles of M, NB = batch columns.
 // All threads of the CTA call it. The warp consumes its ring slots in the order the issue side
-// produced them and refills each slot once its units are done. Per unit, lane (row r = lane &
-// 15, half h = lane >> 4) takes blocks 2h, 2h + 1 of row r: one 32-bit code word gives 4 f16
-// pairs (1024 + q and 1024 + 16 q, nibbles OR'ed into the mantissa of 1024.0h), HSUB2 turns them
-// into q - 8 and 16 (q - 8) exactly, HFMA2 accumulates the block's 32 products in f16 (low and
-// high nibbles in separate accumulators), one FFMA per block applies the f16 scale in f32. (The
-// MMA form of the same product wastes 7 of the 8 columns of an m16n8k16 tile at batch 1-2, and
-// measured slower than the CUDA cores here.)
+// produced them and refills each slot once its units are done. Per unit, lane (quarter
+// bq = lane >> 3, rows r = lane & 7 and r + 8) takes block bq of both rows: code word t of a
+// block holds the nibbles of elements 4t..4t+3 (low) and 16+4t..19+4t (high); masking it gives
+// the low codes q as bytes and the high ones as bytes 16 q, and dp2a multiplies byte pairs with
+// the staged int16 activation pairs, summing exactly in 32 bits (low and high apart, the high
+// sum starting at the block's staged offset term -128 sum x_int). 16 lo + hi is then
+// 16 sum_e (q_e - 8) x_int[e] exactly; per row and block one I2F, and an FMUL and an FFMA apply
+// the f16 scale and the activation block's 2^-(s + 4) in f32. The two rows share every
+// activation load. (An MMA form wastes 7 of the 8 columns of an m16n8k16 tile at batch 1-2 and
+// measured slower; the f16 HFMA2 form of the same loop issued about twice the instructions.)
 template <int NB, int W>
 __device__ __noinline__ void gemv_phase(const PersistParams& p, Hot h, const PMat* mats, int wp, int epi, bool rms,
                                         Ring& ring, const float* xf,
@@ -517,16 +571,18 @@ __device__ __noinline__ void gemv_phase(const PersistParams& p, Hot h, const PMa
                                         unsigned char* region,
                                         unsigned long long (*kred)[kMaxB], unsigned long long* tr) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int hr = lane & 15, hh = lane >> 4;
+    const int bq = lane >> 3, rq = lane & 7;
     const PMat M = mats[wp];
     const int cstride = h.max_nblk * 4 + 4;   // uint4 units between staged columns (+64 B)
+    const int sxstride = h.max_nblk + 4;      // block (offset, scale) pairs between staged columns
     uint4* xs = reinterpret_cast<uint4*>(region);
-    float4* part = reinterpret_cast<float4*>(xs + (size_t)NB * cstride);   // [W][2][32]
+    int2* sxs = reinterpret_cast<int2*>(xs + (size_t)NB * cstride);
+    float4* part = reinterpret_cast<float4*>(sxs + (size_t)NB * sxstride);   // [W][2][32]
 
     if (rms)
-        stage_x<true, W>(h.B, h.eps, M.nblk, cstride, xf, x16, norm_w, xs);
+        stage_x<true, W>(h.B, h.eps, M.nblk, cstride, xf, x16, norm_w, xs, sxs, sxstride);
     else
-        stage_x<false, W>(h.B, h.eps, M.nblk, cstride, xf, x16, norm_w, xs);
+        stage_x<false, W>(h.B, h.eps, M.nblk, cstride, xf, x16, norm_w, xs, sxs, sxstride);
     __syncthreads();
     stamp(tr, 2);
 
@@ -543,73 +599,71 @@ __device__ __noinline__ void gemv_phase(const PersistParams& p, Hot h, const PMa
                                   (size_t)warp * kStages * kSlotBytes;
 
     unsigned long long best[NB];
-    float acc[NB];
+    float acc[NB][2];
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
         best[b] = 0ull;
-        acc[b] = 0.f;
+        acc[b][0] = acc[b][1] = 0.f;
     }
     const int q0 = u1 > u0 ? (nst == 32 ? u0 >> 5 : u0 / nst) : 0;   // 4096-column matrices: a shift
     int tile = T0 + q0, k = u1 > u0 ? u0 - q0 * nst : 0;
     const int first_tile = tile;
 
-    // this lane's share of one unit (group kk of the tile): sum over blocks 2h, 2h + 1 of row r
-    auto unit = [&](const unsigned char* stg, int kk, float (&pu)[NB]) {
-        const uint4 c0 = *reinterpret_cast<const uint4*>(stg + ((2 * hh) * 16 + hr) * 16);
-        const uint4 c1 = *reinterpret_cast<const uint4*>(stg + ((2 * hh + 1) * 16 + hr) * 16);
-        const uint32_t sc = *reinterpret_cast<const uint32_t*>(stg + kUnitBlocks * 16 * 16 + hr * 8 + 4 * hh);
-        const float2 d = __half22float2(as_h2(sc));
-        const __half2 off_lo = as_h2(0x64086408u), off_hi = as_h2(0x64806480u);   // 1032, 1152
+    // this lane's share of one unit (block group kk of the tile): block bq of rows rq, rq + 8
+    auto unit = [&](const unsigned char* stg, int kk) {
+        const uint4 c0 = *reinterpret_cast<const uint4*>(stg + (bq * 16 + rq) * 16);
+        const uint4 c1 = *reinterpret_cast<const uint4*>(stg + (bq * 16 + rq + 8) * 16);
+        const float d0 = __half2float(*reinterpret_cast<const __half*>(stg + kUnitBlocks * 256 + rq * 8 + 2 * bq));
+        const float d1 = __half2float(*reinterpret_cast<const __half*>(stg + kUnitBlocks * 256 + (rq + 8) * 8 + 2 * bq));
+        const int j = kk * kUnitBlocks + bq;
+        const uint32_t w0[4] = {c0.x, c0.y, c0.z, c0.w}, w1[4] = {c1.x, c1.y, c1.z, c1.w};
+        uint32_t l0[4], h0[4], l1[4], h1[4];
 #pragma unroll
-        for (int b = 0; b < NB; ++b) pu[b] = 0.f;
+        for (int t = 0; t < 4; ++t) {
+            l0[t] = w0[t] & 0x0F0F0F0Fu;
+            h0[t] = w0[t] & 0xF0F0F0F0u;
+            l1[t] = w1[t] & 0x0F0F0F0Fu;
+            h1[t] = w1[t] & 0xF0F0F0F0u;
+        }
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const uint4 cw = e ? c1 : c0;
-            const uint32_t ws[4] = {cw.x, cw.y, cw.z, cw.w};
-            const int j = kk * kUnitBlocks + 2 * hh + e;
-            __half2 alo[NB], ahi[NB];
+        for (int b = 0; b < NB; ++b) {
+            const int2 ov = sxs[b * sxstride + j];
+            const float f = __int_as_float(ov.y);   // 2^-(s + 4) of this activation block
+            int lo0 = 0, hi0 = ov.x, lo1 = 0, hi1 = ov.x;
+            const uint4* xb = xs + (size_t)b * cstride + 4 * j;
 #pragma unroll
-            for (int b = 0; b < NB; ++b) alo[b] = ahi[b] = as_h2(0u);
-#pragma unroll
-            for (int tt = 0; tt < 4; ++tt) {
-                const uint32_t w = ws[tt], w8 = w >> 8;
-                const __half2 q0 = __hsub2(as_h2((w & 0x000F000Fu) | 0x64006400u), off_lo);
-                const __half2 q1 = __hsub2(as_h2((w8 & 0x000F000Fu) | 0x64006400u), off_lo);
-                const __half2 q2 = __hsub2(as_h2((w & 0x00F000F0u) | 0x64006400u), off_hi);
-                const __half2 q3 = __hsub2(as_h2((w8 & 0x00F000F0u) | 0x64006400u), off_hi);
-#pragma unroll
-                for (int b = 0; b < NB; ++b) {
-                    const uint4 X = xs[(size_t)b * cstride + 4 * j + tt];
-                    alo[b] = __hfma2(q0, as_h2(X.x), alo[b]);
-                    alo[b] = __hfma2(q1, as_h2(X.y), alo[b]);
-                    ahi[b] = __hfma2(q2, as_h2(X.z), ahi[b]);
-                    ahi[b] = __hfma2(q3, as_h2(X.w), ahi[b]);
-                }
+            for (int t = 0; t < 4; ++t) {
+                const uint4 X = xb[t];
+                lo0 = dp2a_lo(X.x, l0[t], lo0);
+                lo1 = dp2a_lo(X.x, l1[t], lo1);
+                lo0 = dp2a_hi(X.y, l0[t], lo0);
+                lo1 = dp2a_hi(X.y, l1[t], lo1);
+                hi0 = dp2a_lo(X.z, h0[t], hi0);
+                hi1 = dp2a_lo(X.z, h1[t], hi1);
+                hi0 = dp2a_hi(X.w, h0[t], hi0);
+                hi1 = dp2a_hi(X.w, h1[t], hi1);
             }
-            const float de = e ? d.y : d.x;
-#pragma unroll
-            for (int b = 0; b < NB; ++b) {
-                const float2 fl = __half22float2(alo[b]), fh = __half22float2(ahi[b]);
-                pu[b] = fmaf(de, (fl.x + fl.y) + (fh.x + fh.y), pu[b]);
-            }
+            acc[b][0] = fmaf(d0 * f, (float)(lo0 * 16 + hi0), acc[b][0]);
+            acc[b][1] = fmaf(d1 * f, (float)(lo1 * 16 + hi1), acc[b][1]);
         }
     };
-    // add unit u's share; at the end of this warp's part of a tile finish the tile if the warp
-    // covered all of it, else park the shares (slot 0: the warp's first tile, slot 1: its last)
-    auto advance = [&](const float (&pu)[NB], int u) {
-#pragma unroll
-        for (int b = 0; b < NB; ++b) acc[b] += pu[b];
+    // after unit u: at the end of this warp's part of a tile finish the tile if the warp covered
+    // all of it, else park the sums (slot 0: the warp's first tile, slot 1: its last)
+    auto advance = [&](int u) {
         if (++k == nst || u + 1 == u1) {
             const int ts = (tile - T0) * nst;
             if (u0 <= ts && u + 1 == ts + nst) {
                 finish_tile<NB>(p, M, epi, tile, acc, y, ld, best, lane);
             } else {
-                float4 v = make_float4(acc[0], 0.f, 0.f, 0.f);
-                if (NB > 1) v.y = acc[NB > 1 ? 1 : 0];
+                float4 v = make_float4(acc[0][0], acc[0][1], 0.f, 0.f);
+                if (NB > 1) {
+                    v.z = acc[NB > 1 ? 1 : 0][0];
+                    v.w = acc[NB > 1 ? 1 : 0][1];
+                }
                 part[(warp * 2 + (tile == first_tile ? 0 : 1)) * 32 + lane] = v;
             }
 #pragma unroll
-            for (int b = 0; b < NB; ++b) acc[b] = 0.f;
+            for (int b = 0; b < NB; ++b) acc[b][0] = acc[b][1] = 0.f;
             k = 0;
             ++tile;
         }
@@ -630,9 +684,8 @@ __device__ __noinline__ void gemv_phase(const PersistParams& p, Hot h, const PMa
         const unsigned char* sg = ring_g + (size_t)(r.consumed % kStages) * kSlotBytes;
 #pragma unroll 1
         for (int i = 0; i < n; ++i) {
-            float pu[NB];
-            unit(sg + i * kUnitBytes, k, pu);
-            advance(pu, u + i);
+            unit(sg + i * kUnitBytes, k);
+            advance(u + i);
         }
         __syncwarp();
         ++r.consumed;
@@ -647,21 +700,25 @@ __device__ __noinline__ void gemv_phase(const PersistParams& p, Hot h, const PMa
     }
     __syncthreads();
     stamp(tr, 4);
-    // A tile shared by several warps is finished by the warp holding its last unit: the shares
-    // of every warp that touched it, summed in warp order.
+    // A tile shared by several warps is finished by the warp holding its last unit: the sums
+    // of every warp that touched it, added in warp order.
     if (u1 > u0) {
         const int ts = (first_tile - T0) * nst;
         if (u0 > ts && u1 >= ts + nst) {
-            float s2[NB];
+            float s2[NB][2];
 #pragma unroll
-            for (int b = 0; b < NB; ++b) s2[b] = 0.f;
+            for (int b = 0; b < NB; ++b) s2[b][0] = s2[b][1] = 0.f;
             for (int w2 = 0; w2 <= warp; ++w2) {
                 const int a0 = warp_unit<W>(U, w2), a1 = warp_unit<W>(U, w2 + 1);
                 if (a1 <= a0 || a1 <= ts || a0 >= ts + nst) continue;
                 const int sl = a0 >= ts ? 0 : 1;   // begun in this tile: parked as that warp's first
                 const float4 v = part[(w2 * 2 + sl) * 32 + lane];
-                s2[0] += v.x;
-                if (NB > 1) s2[NB > 1 ? 1 : 0] += v.y;
+                s2[0][0] += v.x;
+                s2[0][1] += v.y;
+                if (NB > 1) {
+                    s2[NB > 1 ? 1 : 0][0] += v.z;
+                    s2[NB > 1 ? 1 : 0][1] += v.w;
+                }
             }
             finish_tile<NB>(p, M, epi, first_tile, s2, y, ld, best, lane);
         }

@@ -5,11 +5,12 @@ Layout: bit-exact against a NumPy restatement of the documented layout (16-row t
 rows past the matrix).
 
 GEMV: against the oracle (f64 dense product of the dequantised weights). Tolerance, from the
-kernel's arithmetic: activations are staged in f16 (exact here, the tests give f16), every code
-becomes q - 8 or 16 (q - 8) exactly in f16. Batch 1-2: a block's 32 products are summed in f16
-(16 products per accumulator, relative rounding 2^-11 per step); batch 3-32: tensor-core
-products and sums in f32. Blocks are scaled and summed in f32. For N(0, 0.02) weights and
-N(0, 1) activations that is ~1e-3 of the output rms or less, so the bar is
+kernel's arithmetic. Batch 1-2: activations become 16-bit fixed point with a power-of-two scale
+per 32-element block (rounding error at most 2^-16 of the block's largest |x| per element), and
+the products and each block's sum are exact integers. Batch 3-32: activations f16, (q - 8) d
+rounded once to f16, tensor-core products and sums in f32. Blocks are scaled and summed in f32.
+For N(0, 0.02) weights and N(0, 1) activations that is ~1e-3 of the output rms or less, so the
+bar is
 ``|y - y_ref| <= 1e-2 * rms(y_ref) + 1e-2 * |y_ref|``, the same as the row-major GEMV.
 """
 import numpy as np
