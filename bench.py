@@ -150,6 +150,141 @@ def graph_ms(fn, stream, reps: int, warm: int = 1) -> float:
 # ----------------------------------------------------------------------------- GPU arm
 device_tensor_fn = ql_inputs.device_tensor_fn
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the batch-1 tile
+# stream GEMV at the gate|up shape (24576 x 4096, plain epilogue), from one ncu capture. It is
+# reported only while the kernel's source files hash to the value recorded with it: any change
+# to the kernel makes it null until the counters are taken again.
+GU_TRAFFIC_BYTES = 57250048
+GU_TRAFFIC_SOURCES = ("ql_persist.cuh", "ql_persist.cu", "ql_internal.h")
+GU_TRAFFIC_SHA16 = "459407f49b84da0e"
+
+
+def kernel_source_sha16(files) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "quantized_transformer_decode_ql_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def gemv_bytes(rows, cols, B, epilogue):
+    """Algorithmic bytes of one GEMV launch: q4_0 weights, f16 activations in, the output (f32,
+    or f16 halves for SiLU*up), and the residual read of the in-place add."""
+    out = B * (rows // 2) * 2 if epilogue == "silu" else B * rows * 4
+    return rows * cols * 18 // 32 + B * cols * 2 + out + (B * rows * 4 if epilogue == "resid" else 0)
+
+
+def gemv_kinds(gm, cfg, B, s, g):
+    """Each of the step's GEMV kinds alone, as the step runs them at batch 1-2 (tile stream
+    layout; f16 activations in), over enough layers' matrices in turn that the weights of one
+    pass exceed 3x L2 (lm_head: its own 350 MB); CUDA-event time per launch over 3 graph replays."""
+    import torch
+    import quantized_transformer_decode_ql_gb300 as ql
+    l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+    kinds = [("qkv", "wqkv", "none"), ("o", "wo", "resid"), ("gate_up", "wgu", "silu"), ("down", "wd", "resid"),
+             ("lm_head", None, "none")]
+    epi = {"none": ql.QL_EPI_NONE, "resid": ql.QL_EPI_ADD_RESIDUAL, "silu": ql.QL_EPI_SILU_MUL}
+    out = {}
+    for name, key, e in kinds:
+        mats = [gm.lm_head] if key is None else [L[key] for L in gm.layers]
+        W = mats[0]
+        one = W.rows * W.cols * 18 // 32
+        n = len(mats) if key is None else min(len(mats), max(1, -(-3 * l2 // one)))
+        silu = 1 if e == "silu" else 0
+        bufs = []
+        for Wl in mats[:n]:
+            buf = torch.empty(ql.ql_q4_0_stream_bytes(Wl.rows, Wl.cols, silu), dtype=torch.uint8, device="cuda")
+            ql.ql_q4_0_stream_pack(Wl.scales, Wl.quants, Wl.rows, Wl.cols, silu, buf, s)
+            bufs.append(buf)
+        x = torch.randn((B, W.cols), generator=g, device="cuda").half()
+        y = (torch.empty((B, W.rows // 2), dtype=torch.float16, device="cuda") if silu
+             else torch.zeros((B, W.rows), dtype=torch.float32, device="cuda"))
+        s.synchronize()
+        reps_per = 3 if key is None else 1
+
+        def run():
+            for buf in bufs:
+                for _ in range(reps_per):
+                    ql.ql_gemv_q4_0_stream(buf, W.rows, W.cols, x, B, y, epi[e], None, s)
+        launches = len(bufs) * reps_per
+        us = graph_ms(run, s, 3) * 1e3 / launches
+        nbytes = gemv_bytes(W.rows, W.cols, B, e)
+        out[name] = {"rows": W.rows, "cols": W.cols, "epilogue": e, "us_per_launch": round(us, 3),
+                     "bytes_per_launch": nbytes, "achieved_gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+                     "matrices_rotated": len(bufs), "launches_timed": 3 * launches}
+        del bufs
+    return out
+
+
+def attn_alone(B, lo, hi, s, g, seed=6, iters=10):
+    """Paged GQA decode attention alone at the attention workload's shape (32/8 heads, head_dim
+    128, 16-token blocks, randomly permuted block tables): B sequences with lengths uniform in
+    [lo, hi]; L2 flushed (a 256 MB read) before every launch, the flush timed apart and taken out."""
+    import torch
+    import quantized_transformer_decode_ql_gb300 as ql
+    nh, nkv, hd = 32, 8, 128
+    lens = ql_inputs.batched_lengths(B, lo, hi, seed=seed)
+    nblk = [(int(L) + 15) // 16 for L in lens]
+    maxb, num_blocks = max(nblk), sum(nblk)
+    perm = torch.from_numpy(ql_inputs.fragmented_block_ids(num_blocks, seed=5)).cuda()
+    bt = torch.full((B, maxb), -1, dtype=torch.int32, device="cuda")
+    off = 0
+    for b, n in enumerate(nblk):
+        bt[b, :n] = perm[off:off + n]
+        off += n
+    kp = torch.randn((num_blocks, nkv, 16, hd), generator=g, device="cuda").half()
+    vp = torch.randn((num_blocks, nkv, 16, hd), generator=g, device="cuda").half()
+    q = torch.randn((B, nh, hd), generator=g, device="cuda").half()
+    o = torch.empty((B, nh * hd), dtype=torch.float16, device="cuda")
+    cl = torch.from_numpy(lens).cuda()
+    ws = torch.zeros(ql.ql_paged_attn_workspace_bytes(B, nh, nkv, hd, 16, maxb), dtype=torch.uint8, device="cuda")
+    flush = torch.ones(64 << 20, dtype=torch.float32, device="cuda")
+    flush_sum = torch.zeros((), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+
+    def run():
+        ql.ql_paged_attn_decode(q, kp, vp, bt, cl, B, nh, nkv, hd, 16, maxb, num_blocks, 1 / math.sqrt(hd), o, ws, s)
+    with torch.cuda.stream(s):
+        run()                       # first call outside capture (per-device set-up)
+    s.synchronize()
+
+    def flush_then_run():
+        for _ in range(iters):
+            flush_sum.copy_(flush.sum())
+            run()
+
+    def flush_only():
+        for _ in range(iters):
+            flush_sum.copy_(flush.sum())
+    us = (graph_ms(flush_then_run, s, 3) - graph_ms(flush_only, s, 3)) * 1e3 / iters
+    nbytes = sum(2 * int(L) * nkv * hd * 2 + 4 * ((int(L) + 15) // 16) for L in lens) + B * nh * hd * 4
+    return {"batch": B, "lengths": f"uniform in [{lo}, {hi}] (seed {seed})", "sum_len": int(lens.sum()),
+            "us_per_launch": round(us, 2), "bytes_per_launch": int(nbytes),
+            "achieved_gbs": round(nbytes / (us * 1e-6) / 1e9, 1)}
+
+
+def prefill_context(gm, cfg, ids, n_pos, g):
+    """Synthetic pre-filled context (stands in for prefill): N(0,1) f16 K and V written straight
+    into a slot's blocks of every layer and kv head."""
+    import torch
+    nb = (n_pos + 15) // 16
+    idx = torch.as_tensor(list(ids[:nb]), dtype=torch.long, device="cuda")
+    shape = (cfg.n_layers, nb, cfg.n_kv_heads, 16, cfg.head_dim)
+    gm.k_pool[:, idx] = torch.randn(shape, generator=g, device="cuda").half()
+    gm.v_pool[:, idx] = torch.randn(shape, generator=g, device="cuda").half()
+
+
+def build_e1(cfg, steps, warmup):
+    """The 8B-shaped model (seeded device draws, q4_0 on the device) with a batch-1 pool."""
+    from quantized_transformer_decode_ql_gb300.model import DeviceModel
+    max_ctx = CTX + warmup + steps + 2
+    maxb = (max_ctx + 15) // 16
+    num_blocks = maxb + 8
+    gm = DeviceModel.from_layer_fn(cfg, device_tensor_fn(cfg, seed=0), num_blocks=num_blocks,
+                                   max_batch=1, max_blocks_per_seq=maxb)
+    return gm, maxb, num_blocks, max_ctx
+
 
 def gpu_arm(args, rank, world, local_rank):
     import torch
@@ -159,35 +294,24 @@ def gpu_arm(args, rank, world, local_rank):
         qbuild.build()
     barrier(world)
     import quantized_transformer_decode_ql_gb300 as ql
-    from quantized_transformer_decode_ql_gb300.model import DeviceModel
 
     torch.cuda.set_device(local_rank)
     cfg = ql_inputs.QWEN3_8B
     if args.layers:   # profiling aid: the same layer shapes, fewer layers (not a bench line)
         cfg = dataclasses.replace(cfg, n_layers=args.layers)
-    B = 1 if args.config == "e1" else 32
+    B = 1
     steps, warmup = args.steps, args.warmup
-    max_ctx = CTX + warmup + steps + 2
-    maxb = (max_ctx + 15) // 16
-    num_blocks = B * maxb + 8
     t_setup = time.time()
-    gm = DeviceModel.from_layer_fn(cfg, device_tensor_fn(cfg, seed=0), num_blocks=num_blocks,
-                                   max_batch=B, max_blocks_per_seq=maxb)
+    gm, maxb, num_blocks, max_ctx = build_e1(cfg, steps, warmup)
     gm.ql_model_set_option(ql.QL_OPT_STEP_KERNEL, STEP_KERNELS[args.step_kernel])
     persistent = args.step_kernel == "persistent" and B <= gm.ql_model_persistent_max_batch()
     streamed = not persistent and B <= gm.ql_model_persistent_max_batch()   # stream GEMVs in the step
-    # fragmented block tables; pre-filled synthetic context of CTX positions N(0,1) f16 per slot
+    # fragmented block table; pre-filled synthetic context of CTX positions N(0,1) f16
     perm = torch.from_numpy(ql_inputs.fragmented_block_ids(num_blocks, seed=5)).cuda()
-    bt = perm[: B * maxb].reshape(B, maxb).contiguous()
+    bt = perm[:maxb].reshape(1, maxb).contiguous()
     g = torch.Generator(device="cuda")
     g.manual_seed(4)
-    nctx_blocks = CTX // 16
-    for b in range(B):
-        ids = bt[b, :nctx_blocks].long()
-        gm.k_pool[:, ids] = torch.randn((cfg.n_layers, nctx_blocks, cfg.n_kv_heads, 16, cfg.head_dim),
-                                        generator=g, device="cuda").half()
-        gm.v_pool[:, ids] = torch.randn((cfg.n_layers, nctx_blocks, cfg.n_kv_heads, 16, cfg.head_dim),
-                                        generator=g, device="cuda").half()
+    prefill_context(gm, cfg, bt[0].tolist(), CTX, g)
     first = torch.from_numpy(ql_inputs.prompt_tokens(B, cfg.vocab, seed=1)).cuda()
     tokens = first.clone()
     positions = torch.full((B,), CTX, dtype=torch.int32, device="cuda")
@@ -236,64 +360,6 @@ def gpu_arm(args, rank, world, local_rank):
     ctx_avg = CTX + 1 + (steps - 1) / 2.0
     step_bytes = wbytes + B * (kv_tok * ctx_avg + kv_tok + cfg.hidden * 4 + cfg.vocab * 4)
 
-    # ---- dominant kernel: the gate|up q4_0 GEMV (SiLU*up epilogue), over the 36 layers'
-    # own matrices in turn (every launch streams a fresh 56.6 MB matrix: no L2 reuse)
-    x16 = torch.randn((B, cfg.hidden), generator=g, device="cuda").half()
-    act = torch.empty((B, cfg.intermediate), dtype=torch.float16, device="cuda")
-    reps = 3
-
-    W = gm.layers[0]["wgu"]
-    if streamed:
-        # the kernel the step runs at this batch: the GEMV over the tile stream layout, on
-        # 8 layers' gate|up matrices in turn (453 MB: no L2 reuse between launches)
-        n_mats = min(8, cfg.n_layers)
-        streams = []
-        for L in gm.layers[:n_mats]:
-            Wl = L["wgu"]
-            buf = torch.empty(ql.ql_q4_0_stream_bytes(Wl.rows, Wl.cols, 1), dtype=torch.uint8, device="cuda")
-            ql.ql_q4_0_stream_pack(Wl.scales, Wl.quants, Wl.rows, Wl.cols, 1, buf, s)
-            streams.append(buf)
-        ws = None
-        if B > 2:
-            ws = torch.zeros(ql.ql_gemv_q4_0_stream_workspace_bytes(W.rows, W.cols, 1), dtype=torch.uint8,
-                             device="cuda")
-        s.synchronize()
-
-        def gu_all():
-            for buf in streams:
-                ql.ql_gemv_q4_0_stream(buf, W.rows, W.cols, x16, B, act, ql.QL_EPI_SILU_MUL, ws, s)
-        gu_kernel = "q4_0 GEMV over the tile stream layout (gate|up, SiLU*up epilogue, batch %d)" % B
-    else:
-        n_mats = cfg.n_layers
-
-        def gu_all():
-            for L in gm.layers:
-                Wl = L["wgu"]
-                ql.ql_gemv_q4_0(Wl.scales, Wl.quants, Wl.rows, Wl.cols, x16, B, act, ql.QL_DTYPE_F16,
-                                ql.QL_EPI_SILU_MUL, None, s)
-        gu_kernel = "q4_0 GEMV (gate|up, SiLU*up epilogue, batch %d)" % B
-    gu_ms_rep = graph_ms(gu_all, s, reps)
-    gu_launches = reps * n_mats
-    gu_ms = gu_ms_rep / n_mats
-    gu_bytes = W.nbytes() + B * cfg.hidden * 2 + B * cfg.intermediate * 2
-
-    # ---- attention alone at this workload (context CTX + steps/2), 36 layers' pools in turn
-    at_ctx = torch.full((B,), int(ctx_avg), dtype=torch.int32, device="cuda")
-    qa = torch.randn((B, cfg.n_heads, cfg.head_dim), generator=g, device="cuda").half()
-    oa = torch.empty((B, cfg.n_heads * cfg.head_dim), dtype=torch.float16, device="cuda")
-    wsb = ql.ql_paged_attn_workspace_bytes(B, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim, 16, maxb)
-    ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
-
-    def attn_all():
-        for li in range(cfg.n_layers):
-            ql.ql_paged_attn_decode(qa, gm.k_pool[li], gm.v_pool[li], bt, at_ctx, B, cfg.n_heads,
-                                    cfg.n_kv_heads, cfg.head_dim, 16, maxb, num_blocks,
-                                    1.0 / math.sqrt(cfg.head_dim), oa, ws, s)
-    at_ms_rep = graph_ms(attn_all, s, reps)
-    at_ms = at_ms_rep / cfg.n_layers
-    L = int(ctx_avg)
-    at_bytes = B * (2 * L * cfg.n_kv_heads * cfg.head_dim * 2 + 4 * ((L + 15) // 16)) + B * cfg.n_heads * cfg.head_dim * 4
-
     # ---- end to end through the public API with host buffers: per step, H2D of the step's
     # token ids from pinned memory, one graph replay, D2H of the next tokens, host sync
     h_tok = torch.empty((B,), dtype=torch.int32, pin_memory=True)
@@ -313,37 +379,52 @@ def gpu_arm(args, rank, world, local_rank):
     e2e_s = time.perf_counter() - t0
     e2e_s = max_over_ranks(e2e_s, world)
 
+    # ---- the kernels alone (untimed region over): every GEMV kind at this batch, the dominant
+    # one (gate|up, the largest weight stream of a layer) is the roofline kernel; attention at
+    # this context and on the attention workload (batch 32, lengths in [512, 32768])
     peak, peak_src = load_peaks()
+    kernels = {}
+    if streamed:
+        kernels["gemv"] = gemv_kinds(gm, cfg, B, s, g)
+    kernels["paged_attention_e1"] = attn_alone(1, int(ctx_avg), int(ctx_avg), s, g)
+    if not args.layers:
+        kernels["paged_attention_a_b32"] = attn_alone(32, 512, 32768, s, g)
+    for k in kernels.values():
+        for v in (k.values() if "qkv" in k else [k]):
+            v["frac"] = round(v["achieved_gbs"] / peak, 4)
+
     tok_total = sum_over_ranks(float(B * steps), world)
     value = tok_total / (ms_max / 1e3)
-    per_kernel = {
-        "gemv_gate_up": {"achieved_gbs": gu_bytes / (gu_ms / 1e3) / 1e9, "us_per_launch": gu_ms * 1e3,
-                         "bytes_per_launch": gu_bytes, "launches": gu_launches},
-        "paged_attention": {"achieved_gbs": at_bytes / (at_ms / 1e3) / 1e9, "us_per_launch": at_ms * 1e3,
-                            "bytes_per_launch": at_bytes, "context": L},
-    }
-    gu_gbs = per_kernel["gemv_gate_up"]["achieved_gbs"]
-    gu_traffic = GU_TRAFFIC_B1 if (streamed and B == 1 and cfg.hidden == 4096 and cfg.intermediate == 12288) else None
     step_gbs = step_bytes * steps / (ms_max / 1e3) / 1e9
     kernels_per_step = 1 if persistent else 3 + 5 * cfg.n_layers   # embed, 5 per layer, lm_head, finalize
+    roof = {"bound": "hbm", "peak": peak, "unit": "GB/s", "peak_source": peak_src}
+    if streamed:
+        gu = kernels["gemv"]["gate_up"]
+        sha = kernel_source_sha16(GU_TRAFFIC_SOURCES)
+        traffic = GU_TRAFFIC_BYTES if sha == GU_TRAFFIC_SHA16 else None
+        roof.update({"kernel": "gemv_stream_kernel<1,16>: q4_0 GEMV over the tile stream layout, gate|up "
+                               "24576 x 4096, SiLU*up epilogue, batch 1",
+                     "achieved": gu["achieved_gbs"], "frac": round(gu["achieved_gbs"] / peak, 4),
+                     "traffic": traffic, "algorithmic_bytes": gu["bytes_per_launch"],
+                     "us_per_launch": gu["us_per_launch"],
+                     "traffic_note": ("one ncu capture of this kernel source (sha %s), plain epilogue" % sha
+                                      if traffic else "kernel source changed since the counters were taken")})
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world,
         "steps": steps, "warmup": warmup, "ms_per_step": round(ms_max / steps, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "q4_0 weights, f16 act/KV, f32 accum",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "q4_0 weights; int16 fixed-point activations at batch 1-2 (dp2a, exact block sums); f16 KV; f32 accumulation",
         "data": "synthetic (seeded random-init weights, N(0,1) f16 KV context, random prompt token)",
         "config": {"workload": f"qwen3-8b-shaped q4_0 decode, batch {B}, {CTX}-token context, {steps} greedy steps",
                    "hidden": cfg.hidden, "layers": cfg.n_layers, "heads": f"{cfg.n_heads}/{cfg.n_kv_heads}",
                    "head_dim": cfg.head_dim, "intermediate": cfg.intermediate, "vocab": cfg.vocab,
                    "batch": B, "context": CTX, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (%.2f GB of q4_0 weights streamed per step)" % (wbytes / 1e9)},
-        "roofline": {"bound": "hbm", "kernel": gu_kernel,
-                     "achieved": round(gu_gbs, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(gu_gbs / peak, 4), "traffic": gu_traffic, "peak_source": peak_src,
-                     **({"traffic_source": GU_TRAFFIC_SOURCE} if gu_traffic else {})},
+        "roofline": roof,
         "step_roofline": {"bytes_per_step": int(step_bytes), "achieved_gbs": round(step_gbs, 1),
                           "frac": round(step_gbs / peak, 4),
                           "roofline_tokens_s": round(B * peak * 1e9 / step_bytes, 1)},
-        "kernels": per_kernel,
+        "kernels": kernels,
         "clocks": clocks,
         "e2e": {"value": round(tok_total / e2e_s, 2), "unit": "tokens/s", "h2d_bytes_per_step": 4 * B,
                 "d2h_bytes_per_step": 4 * B},
@@ -354,6 +435,147 @@ def gpu_arm(args, rank, world, local_rank):
     }
     if phases:
         line["step_phases_us"] = phases
+    if not args.layers and not args.no_e32:
+        gm32 = gm.sibling(**e32_pool(cfg, E32_STEPS, 3))
+        try:
+            line["e32"] = e32_run(gm32, cfg, E32_STEPS, 3, s, local_rank, world)
+        finally:
+            gm32.close()
+    gm.close()
+    return line
+
+
+E32_STEPS = 128
+E32_FRESH = 128
+
+
+def e32_pool(cfg, steps, warmup):
+    lens0 = ql_inputs.batched_lengths(32, 128, 8192, seed=7)
+    cap = int(max(lens0.max(), E32_FRESH)) + warmup + steps + 2
+    maxb = (cap + 15) // 16
+    need = (sum((int(L) + warmup + steps + 2 + 15) // 16 for L in lens0)
+            + 32 * ((E32_FRESH + steps + 2 + 15) // 16) + 16)
+    return {"num_blocks": need, "max_batch": 32, "max_blocks_per_seq": maxb}
+
+
+def e32_run(gm, cfg, steps, warmup, s, local_rank, world):
+    """Batched decode: 32 sequences with initial context lengths uniform in [128, 8192], fragmented
+    block tables from the library's block allocator, `steps` greedy steps; every sequence finishes
+    at a random step and is replaced by a fresh 128-position context in newly allocated blocks.
+    The replacement work runs between graph replays and is excluded from the decode time
+    (reported separately). Each step is timed with CUDA events on the launching stream."""
+    import torch
+    import quantized_transformer_decode_ql_gb300 as ql
+    B = 32
+    lens0 = ql_inputs.batched_lengths(B, 128, 8192, seed=7)
+    finish = ql_inputs.sub_rng(8, B).integers(0, steps, size=B)
+    need, maxb = gm.num_blocks, gm.max_blocks_per_seq
+    pool = ql.BlockPool(need)
+    order = [pool.alloc() for _ in range(need)]
+    pool.free([order[i] for i in ql_inputs.fragmented_block_ids(need, seed=5)])
+    g = torch.Generator(device="cuda")
+    g.manual_seed(9)
+    bt_host = np.zeros((B, maxb), np.int32)
+    owned = [None] * B
+
+    def place(b, n_pos, n_total):
+        ids = [pool.alloc() for _ in range((n_total + 15) // 16)]
+        owned[b] = ids
+        bt_host[b, :] = 0
+        bt_host[b, :len(ids)] = ids
+        prefill_context(gm, cfg, ids, n_pos, g)
+
+    for b in range(B):
+        place(b, int(lens0[b]), int(lens0[b]) + warmup + steps + 2)
+    bt = torch.from_numpy(bt_host).cuda()
+    tokens = torch.from_numpy(ql_inputs.prompt_tokens(B, cfg.vocab, seed=1)).cuda()
+    positions = torch.from_numpy(lens0.astype(np.int32)).cuda()
+    sargs = gm.step_args(tokens, positions, bt, tokens)
+    torch.cuda.synchronize()
+    gm.ql_decode_graph_capture(sargs, s)
+    with torch.cuda.stream(s):
+        gm.ql_decode_graph_replay(B, warmup, s)
+    s.synchronize()
+    gm.ql_check_device_error()
+
+    clock = ClockSampler(local_rank)
+    time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    kv_tok = cfg.n_layers * 2 * cfg.n_kv_heads * cfg.head_dim * 2
+    live_len = positions.cpu().numpy().astype(np.int64) + 1
+    step_bytes = []
+    repl_s = 0.0
+    for i in range(steps):
+        step_bytes.append(gm.weight_bytes() + kv_tok * int(live_len.sum()) + B * (kv_tok + cfg.hidden * 4 + cfg.vocab * 4))
+        with torch.cuda.stream(s):
+            ev[i][0].record(s)
+            gm.ql_decode_graph_replay(B, 1, s)
+            ev[i][1].record(s)
+        live_len += 1
+        done = np.flatnonzero(finish == i)
+        if len(done):
+            t0 = time.perf_counter()
+            s.synchronize()
+            pos_h = positions.cpu().numpy()
+            for b in done:
+                pool.free(owned[b])
+                place(int(b), E32_FRESH, E32_FRESH + steps + 2)
+                pos_h[b] = E32_FRESH
+                live_len[b] = E32_FRESH + 1
+            bt.copy_(torch.from_numpy(bt_host))
+            positions.copy_(torch.from_numpy(pos_h))
+            torch.cuda.synchronize()
+            repl_s += time.perf_counter() - t0
+    s.synchronize()
+    clocks = clock.stop()
+    gm.ql_check_device_error()
+    ms = sum(a.elapsed_time(b) for a, b in ev)
+    ms = max_over_ranks(ms, world)
+    phases = launch_phases(gm, sargs, s, cfg)   # untimed, after the timed region
+    peak, peak_src = load_peaks()
+    value = sum_over_ranks(float(B * steps), world) / (ms / 1e3)
+    gbs = sum(step_bytes) / (ms / 1e3) / 1e9
+    return {
+        "value": round(value, 2), "unit": "tokens/s", "steps": steps, "warmup": warmup,
+        "ms_per_step": round(ms / steps, 4),
+        "workload": f"qwen3-8b-shaped q4_0 batched decode, 32 sequences, contexts uniform in [128, 8192], "
+                    f"{steps} greedy steps, finished sequences replaced by fresh {E32_FRESH}-position contexts",
+        "step_roofline": {"bytes_per_step_avg": int(np.mean(step_bytes)), "achieved_gbs": round(gbs, 1),
+                          "frac": round(gbs / peak, 4), "peak": peak, "peak_source": peak_src,
+                          "roofline_tokens_s": round(B * peak * 1e9 / float(np.mean(step_bytes)), 1)},
+        "replacement_s_excluded": round(repl_s, 3), "replacements": int((finish < steps).sum()),
+        "clocks": clocks, "gpu_launches": launches_per_step(cfg, B) * steps,
+        **({"step_phases_us": phases} if phases else {}),
+    }
+
+
+def gpu_arm_e32(args, rank, world, local_rank):
+    """The batched workload as its own bench line (``--config e32``)."""
+    import torch
+
+    from quantized_transformer_decode_ql_gb300 import build as qbuild
+    if rank == 0 or world == 1:
+        qbuild.build()
+    barrier(world)
+    from quantized_transformer_decode_ql_gb300.model import DeviceModel
+
+    torch.cuda.set_device(local_rank)
+    cfg = ql_inputs.QWEN3_8B
+    t_setup = time.time()
+    gm = DeviceModel.from_layer_fn(cfg, device_tensor_fn(cfg, seed=0), **e32_pool(cfg, args.steps, args.warmup))
+    setup_s = time.time() - t_setup
+    s = torch.cuda.Stream()
+    r = e32_run(gm, cfg, args.steps, args.warmup, s, local_rank, world)
+    gm.close()
+    line = {"metric": METRIC, "value": r.pop("value"), "unit": r.pop("unit"), "n_gpus": world,
+            "steps": r.pop("steps"), "warmup": r.pop("warmup"), "ms_per_step": r.pop("ms_per_step"),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "q4_0 weights, f16 act/KV, f32 accum",
+            "data": "synthetic (seeded random-init weights, N(0,1) f16 KV contexts, random tokens)",
+            "config": {"workload": r.pop("workload"), "batch": 32, "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2 (4.26 GB of weights + KV per step)"},
+            "setup_s": round(setup_s, 1)}
+    line.update(r)
     return line
 
 
@@ -381,14 +603,6 @@ def launches_per_step(cfg, B):
     per_layer = (gemv_passes(cfg.hidden, B) * 2 + gemv_passes(cfg.n_heads * cfg.head_dim, B)
                  + gemv_passes(cfg.intermediate, B) + 1)
     return 2 + per_layer * cfg.n_layers + gemv_passes(cfg.hidden, B)
-
-
-# DRAM bytes (read + write) of one launch of the batch-1 tile stream GEMV at the gate|up shape
-# (24576 x 4096), from one ncu capture of that kernel (plain epilogue; the SiLU*up launch that
-# the roofline times writes 72 KB less); reported only for that kernel and batch.
-GU_TRAFFIC_B1 = 57008640 + 227840
-GU_TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum, profiles/"
-                     "gemv_stream_q4_0_24576x4096_b1_ncu.md (same kernel, plain epilogue)")
 
 
 def ns_relative(raw, nstamps):
@@ -530,119 +744,6 @@ def step_phases(gm, sargs, s, cfg):
             out[n]["ring_wait_frac"] = round(float(wait / loop), 3)
     out["total_step_us"] = round((leave[rows - 1].max() - leave[0].min()) / 1e3, 1)
     return out
-
-
-def gpu_arm_e32(args, rank, world, local_rank):
-    """Batched decode: 32 sequences with initial context lengths uniform in [128, 8192], fragmented
-    block tables from the library's block allocator, K greedy steps; every sequence finishes at a
-    random step and is replaced by a fresh 128-position context in newly allocated blocks. The
-    replacement work runs between graph replays and is excluded from the decode time (reported
-    separately)."""
-    import torch
-
-    from quantized_transformer_decode_ql_gb300 import build as qbuild
-    if rank == 0 or world == 1:
-        qbuild.build()
-    barrier(world)
-    import quantized_transformer_decode_ql_gb300 as ql
-    from quantized_transformer_decode_ql_gb300.model import DeviceModel
-
-    torch.cuda.set_device(local_rank)
-    cfg = ql_inputs.QWEN3_8B
-    B, steps, warmup, fresh = 32, args.steps, args.warmup, 128
-    lens0 = ql_inputs.batched_lengths(B, 128, 8192, seed=7)
-    finish = ql_inputs.sub_rng(8, B).integers(0, steps, size=B)
-    cap = int(max(lens0.max(), fresh)) + warmup + steps + 2
-    maxb = (cap + 15) // 16
-    need = sum((int(L) + warmup + steps + 2 + 15) // 16 for L in lens0) + B * ((fresh + steps + 2 + 15) // 16) + 16
-    t_setup = time.time()
-    gm = DeviceModel.from_layer_fn(cfg, device_tensor_fn(cfg, seed=0), num_blocks=need, max_batch=B,
-                                   max_blocks_per_seq=maxb)
-    pool = ql.BlockPool(need)
-    order = [pool.alloc() for _ in range(need)]
-    pool.free([order[i] for i in ql_inputs.fragmented_block_ids(need, seed=5)])
-    g = torch.Generator(device="cuda")
-    g.manual_seed(4)
-    bt_host = np.zeros((B, maxb), np.int32)
-    owned = [None] * B
-
-    def place(b, n_pos, n_total):
-        ids = [pool.alloc() for _ in range((n_total + 15) // 16)]
-        owned[b] = ids
-        bt_host[b, :] = 0
-        bt_host[b, :len(ids)] = ids
-        nb = (n_pos + 15) // 16
-        idx = torch.tensor(ids[:nb], dtype=torch.long, device="cuda")
-        shape = (cfg.n_layers, nb, cfg.n_kv_heads, 16, cfg.head_dim)
-        gm.k_pool[:, idx] = torch.randn(shape, generator=g, device="cuda").half()
-        gm.v_pool[:, idx] = torch.randn(shape, generator=g, device="cuda").half()
-
-    for b in range(B):
-        place(b, int(lens0[b]), int(lens0[b]) + warmup + steps + 2)
-    bt = torch.from_numpy(bt_host).cuda()
-    tokens = torch.from_numpy(ql_inputs.prompt_tokens(B, cfg.vocab, seed=1)).cuda()
-    positions = torch.from_numpy(lens0.astype(np.int32)).cuda()
-    sargs = gm.step_args(tokens, positions, bt, tokens)
-    s = torch.cuda.Stream()
-    torch.cuda.synchronize()
-    gm.ql_decode_graph_capture(sargs, s)
-    setup_s = time.time() - t_setup
-    with torch.cuda.stream(s):
-        gm.ql_decode_graph_replay(B, warmup, s)
-    s.synchronize()
-    gm.ql_check_device_error()
-
-    clock = ClockSampler(local_rank)
-    time.sleep(0.3)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-    kv_tok = cfg.n_layers * 2 * cfg.n_kv_heads * cfg.head_dim * 2
-    live_len = positions.cpu().numpy().astype(np.int64) + 1
-    step_bytes = []
-    repl_s = 0.0
-    for i in range(steps):
-        step_bytes.append(gm.weight_bytes() + kv_tok * int(live_len.sum()) + B * (kv_tok + cfg.hidden * 4 + cfg.vocab * 4))
-        with torch.cuda.stream(s):
-            ev[i][0].record(s)
-            gm.ql_decode_graph_replay(B, 1, s)
-            ev[i][1].record(s)
-        live_len += 1
-        done = np.flatnonzero(finish == i)
-        if len(done):
-            t0 = time.perf_counter()
-            s.synchronize()
-            pos_h = positions.cpu().numpy()
-            for b in done:
-                pool.free(owned[b])
-                place(int(b), fresh, fresh + steps + 2)
-                pos_h[b] = fresh
-                live_len[b] = fresh + 1
-            bt.copy_(torch.from_numpy(bt_host))
-            positions.copy_(torch.from_numpy(pos_h))
-            torch.cuda.synchronize()
-            repl_s += time.perf_counter() - t0
-    s.synchronize()
-    clocks = clock.stop()
-    gm.ql_check_device_error()
-    ms = sum(a.elapsed_time(b) for a, b in ev)
-    phases = launch_phases(gm, sargs, s, cfg)   # untimed, after the timed region
-    peak, peak_src = load_peaks()
-    value = B * steps / (ms / 1e3)
-    gbs = sum(step_bytes) / (ms / 1e3) / 1e9
-    return {
-        "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world, "steps": steps,
-        "warmup": warmup, "ms_per_step": round(ms / steps, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "q4_0 weights, f16 act/KV, f32 accum",
-        "data": "synthetic (seeded random-init weights, N(0,1) f16 KV contexts, random tokens)",
-        "config": {"workload": f"qwen3-8b-shaped q4_0 batched decode, 32 sequences, contexts uniform in [128, 8192], "
-                               f"{steps} greedy steps, finished sequences replaced by fresh 128-position contexts",
-                   "batch": B, "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (4.26 GB of weights + KV per step)"},
-        "step_roofline": {"bytes_per_step_avg": int(np.mean(step_bytes)), "achieved_gbs": round(gbs, 1),
-                          "frac": round(gbs / peak, 4), "peak": peak, "peak_source": peak_src},
-        "replacement_s_excluded": round(repl_s, 3), "replacements": int((finish < steps).sum()),
-        "clocks": clocks, "gpu_launches": launches_per_step(cfg, B) * steps, "setup_s": round(setup_s, 1),
-        **({"step_phases_us": phases} if phases else {}),
-    }
 
 
 # ----------------------------------------------------------------------------- CPU oracle arm
@@ -871,6 +972,7 @@ def main():
     ap.add_argument("--impl", default="ql", choices=["ql", "reference"])
     ap.add_argument("--config", default="e1", choices=["e1", "e32"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e32", action="store_true", help="leave the batch-32 sub-result out of the default line")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling aid: run the 8B-shaped step with this many layers (default: all 36)")
     ap.add_argument("--step-kernel", default="auto", choices=["auto", "persistent", "launches"],

@@ -99,6 +99,20 @@ class DeviceModel:
         self._create()
         return self
 
+    def sibling(self, num_blocks: int, max_batch: int, max_blocks_per_seq: int) -> "DeviceModel":
+        """Another model handle over the same weight tensors, with its own KV pools, batch bound
+        and block-table width (for example a batched workload next to a batch-1 one). The
+        weights must outlive both handles."""
+        other = DeviceModel.__new__(DeviceModel)
+        other.cfg, other.device = self.cfg, self.device
+        other.num_blocks, other.max_batch, other.max_blocks_per_seq = num_blocks, max_batch, max_blocks_per_seq
+        other.embed, other.final_norm, other.lm_head, other.layers = self.embed, self.final_norm, self.lm_head, self.layers
+        shape = (self.cfg.n_layers, num_blocks, self.cfg.n_kv_heads, BLOCK, self.cfg.head_dim)
+        other.k_pool = torch.zeros(shape, dtype=torch.float16, device=self.device)
+        other.v_pool = torch.zeros(shape, dtype=torch.float16, device=self.device)
+        other._create()
+        return other
+
     def _create(self):
         cfg = self.cfg
         self._layer_descs = (LayerDesc * cfg.n_layers)()
