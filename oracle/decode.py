@@ -100,29 +100,40 @@ def _split_qkv(cfg, y: np.ndarray):
     return q, k, v
 
 
-def decode_step(model: Q4Model, cache: KVCache, tokens, positions) -> np.ndarray:
+def decode_step(model: Q4Model, cache: KVCache, tokens, positions, act=None) -> np.ndarray:
     """One decode step for every slot; returns logits ``[B, vocab]`` (f64).
 
     ``tokens[b]`` sits at position ``positions[b]``; cache positions ``0..positions[b]-1``
     must already hold that slot's context. The step writes K and V of position
-    ``positions[b]`` into the cache.
+    ``positions[b]`` into the cache. ``act``: see :func:`decode_hidden`.
     """
     tokens = np.asarray(tokens, dtype=np.int64)
-    hf = decode_hidden(model, cache, model.embed[tokens], positions)
-    return ops.gemv(model.dense(model.lm_head), hf)
+    act = _identity if act is None else act
+    hf = decode_hidden(model, cache, model.embed[tokens], positions, act=act)
+    return ops.gemv(model.dense(model.lm_head), act(hf))
 
 
-def decode_hidden(model: Q4Model, cache: KVCache, x, positions) -> np.ndarray:
+def _identity(v):
+    return v
+
+
+def decode_hidden(model: Q4Model, cache: KVCache, x, positions, act=None) -> np.ndarray:
     """Steps 2 and the final RMSNorm of 3 for embedded tokens ``x`` ``[B, hidden]``: the
-    normalised final hidden state ``[B, hidden]`` that the lm_head multiplies (f64)."""
+    normalised final hidden state ``[B, hidden]`` that the lm_head multiplies (f64).
+
+    ``act`` (default: none) is applied to the input vector of every GEMV of the layers, for a
+    GEMV that reads its activations in a quantised form (e.g. ``oracle.act8.absmax_dequant``,
+    the int8 absmax form of inferencelayer ``cuda_llm.rs``); the lm_head's input is left to the
+    caller."""
     cfg = model.cfg
+    act = _identity if act is None else act
     positions = np.asarray(positions, dtype=np.int64)
     x = np.array(x, dtype=np.float64)                               # [B, hidden]
     B = x.shape[0]
     scale = 1.0 / np.sqrt(cfg.head_dim)
     for li, L in enumerate(model.layers):
         hn = ops.rmsnorm(x, L["attn_norm"], cfg.eps)
-        y = ops.gemv(model.dense(L["wqkv"]), hn)
+        y = ops.gemv(model.dense(L["wqkv"]), act(hn))
         q, k, v = _split_qkv(cfg, y)
         o = np.empty((B, cfg.n_heads, cfg.head_dim))
         for b in range(B):
@@ -133,11 +144,11 @@ def decode_hidden(model: Q4Model, cache: KVCache, x, positions) -> np.ndarray:
             cache.v[b, li, :, p] = _f16(v[b])
             o[b] = ops.gqa_attention(qb, cache.k[b, li, :, : p + 1],
                                      cache.v[b, li, :, : p + 1], scale)
-        x = x + ops.gemv(model.dense(L["wo"]), o.reshape(B, -1))
+        x = x + ops.gemv(model.dense(L["wo"]), act(o.reshape(B, -1)))
         hn = ops.rmsnorm(x, L["ffn_norm"], cfg.eps)
-        gu = ops.gemv(model.dense(L["wgu"]), hn)
-        act = ops.swiglu(gu[:, : cfg.intermediate], gu[:, cfg.intermediate:])
-        x = x + ops.gemv(model.dense(L["wd"]), act)
+        gu = ops.gemv(model.dense(L["wgu"]), act(hn))
+        a = ops.swiglu(gu[:, : cfg.intermediate], gu[:, cfg.intermediate:])
+        x = x + ops.gemv(model.dense(L["wd"]), act(a))
     return ops.rmsnorm(x, model.final_norm, cfg.eps)
 
 
