@@ -130,6 +130,22 @@ int ql_q4_0_stream_pack(const void* d_scales, const void* d_quants, int64_t rows
 int ql_gemv_q4_0_stream(const void* d_stream, int64_t rows, int64_t cols, const void* d_x,
                         int64_t batch, void* d_y, int epilogue, void* d_workspace,
                         int64_t workspace_bytes, void* stream);
+/* Activation form of the batch 1-2 GEMV, for this process (ql_gemv_q4_0_stream and the decode
+ * step at batch 1-2; graphs keep the form they were captured with):
+ *   QL_GEMV_ACT_INT16 (default) 16-bit fixed point with one power-of-two scale per 32-element
+ *                     block (above); products and block sums exact (dp2a).
+ *   QL_GEMV_ACT_INT8  [IL] CudaQwen3::absmax + gemv: one scale per activation vector, read from
+ *                     xs = [max|x|, 1/max|x|]; codes q = round_half_even(x * (127 / max|x|)),
+ *                     the division and the product each one f32 operation; the weights are
+ *                     multiplied by q * max|x| / 127 with dp4a (products and block sums exact
+ *                     in 32 bits). Each output then differs from the exact product by at most
+ *                     sum_k |w_k| * max|x| / 254 plus f32 rounding: a coarser form (the
+ *                     decode step's logits tolerance is not met at the 8B width), selectable
+ *                     for speed. RMSNorm'd inputs take max|x w| times the norm scale as max|x|.
+ * The initial form is QL_GEMV_ACT_INT8 when the environment sets QL_GEMV_ACT=int8. Returns the
+ * previous form, or QL_EINVAL for an unknown one.                                          */
+enum { QL_GEMV_ACT_INT16 = 0, QL_GEMV_ACT_INT8 = 1 };
+int ql_set_gemv_activation_form(int form);
 /* Workspace bytes ql_gemv_q4_0_stream needs at batch 3-32 for this shape on the current
  * device (the split depends on its SM count); 0 on a bad shape.                           */
 int64_t ql_gemv_q4_0_stream_workspace_bytes(int64_t rows, int64_t cols, int silu);

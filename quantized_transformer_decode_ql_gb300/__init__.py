@@ -14,6 +14,7 @@ from ._lib import (QLError, QL_OK, QL_EINVAL, QL_ENOMEM, QL_ECUDA, QL_EPOOL, QL_
                    QL_EPI_ADD_RESIDUAL, QL_EPI_SILU_MUL, QL_STEP_AUTO, QL_STEP_LAUNCHES,
                    QL_STEP_PERSISTENT, QL_OPT_STEP_KERNEL, QL_OPT_BARRIER_TIMEOUT_NS,
                    QL_OPT_TEST_BARRIER_EXTRA, QL_OPT_STEP_TRACE, QL_BATCHED_MMA_SYNC, QL_BATCHED_TCGEN05,
+                   QL_GEMV_ACT_INT16, QL_GEMV_ACT_INT8,
                    QL_ATTN_MERGE_TICKET, QL_ATTN_MERGE_CLUSTER,
                    Q4Matrix, LayerDesc, ModelDesc,
                    StepArgs, SIGNATURES, LIB_PATH, lib, check, ptr, stream_ptr)
@@ -21,7 +22,7 @@ from ._lib import (QLError, QL_OK, QL_EINVAL, QL_ENOMEM, QL_ECUDA, QL_EPOOL, QL_
 __all__ = [
     "QLError", "lib", "ql_q4_0_pack", "ql_q4_0_unpack", "ql_q4_0_pack_device", "ql_gemv_q4_0",
     "ql_q4_0_stream_bytes", "ql_q4_0_stream_pack", "ql_gemv_q4_0_stream",
-    "ql_gemv_q4_0_stream_workspace_bytes", "ql_set_batched_gemv_form",
+    "ql_gemv_q4_0_stream_workspace_bytes", "ql_set_batched_gemv_form", "ql_set_gemv_activation_form",
     "ql_paged_attn_workspace_bytes", "ql_paged_attn_decode", "ql_paged_attn_decode_noalloc",
     "ql_set_attn_merge_form", "ql_paged_attn_merge_form",
     "ql_kv_q8_0_row_bytes", "ql_kv_q5_1_row_bytes", "ql_kv_quantize_q8_0", "ql_kv_dequantize_q8_0",
@@ -68,6 +69,14 @@ def ql_gemv_q4_0_stream_workspace_bytes(rows, cols, silu=0):
 def ql_set_batched_gemv_form(form):
     """Tensor-core form of the batch 3-32 GEMV for this process; returns the previous form."""
     rc = int(lib().ql_set_batched_gemv_form(form))
+    if rc < 0:
+        check(rc)
+    return rc
+
+
+def ql_set_gemv_activation_form(form):
+    """Activation form of the batch 1-2 GEMV for this process; returns the previous form."""
+    rc = int(lib().ql_set_gemv_activation_form(form))
     if rc < 0:
         check(rc)
     return rc

@@ -19,6 +19,7 @@ QL_EPI_NONE, QL_EPI_ADD_RESIDUAL, QL_EPI_SILU_MUL = 0, 1, 2
 QL_STEP_AUTO, QL_STEP_LAUNCHES, QL_STEP_PERSISTENT = 0, 1, 2
 QL_OPT_STEP_KERNEL, QL_OPT_BARRIER_TIMEOUT_NS, QL_OPT_TEST_BARRIER_EXTRA, QL_OPT_STEP_TRACE = 1, 2, 3, 4
 QL_BATCHED_MMA_SYNC, QL_BATCHED_TCGEN05 = 0, 1
+QL_GEMV_ACT_INT16, QL_GEMV_ACT_INT8 = 0, 1
 QL_ATTN_MERGE_TICKET, QL_ATTN_MERGE_CLUSTER = 0, 1
 
 
@@ -70,6 +71,7 @@ SIGNATURES = {
                                     c_int64, c_void_p]),
     "ql_gemv_q4_0_stream_workspace_bytes": (c_int64, [c_int64, c_int64, c_int]),
     "ql_set_batched_gemv_form": (c_int, [c_int]),
+    "ql_set_gemv_activation_form": (c_int, [c_int]),
     "ql_paged_attn_workspace_bytes": (c_size_t, [c_int64, c_int, c_int, c_int, c_int, c_int64]),
     "ql_paged_attn_decode": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int64,
                                      c_int, c_int, c_int, c_int, c_int64, c_int64, c_float,

@@ -2,6 +2,7 @@
 // itself is in ql_persist.cuh; head_dim 64 in ql_persist_hd64.cu).
 #include "ql_persist.cuh"
 
+#include <atomic>
 #include <cstdlib>
 #include <map>
 #include <mutex>
@@ -72,6 +73,22 @@ static int stream_gemv_warps() {
     return w;
 }
 
+// Activation form of the batch 1-2 GEMV (process-wide; graphs keep the form they were captured
+// with): 16-bit fixed point per 32-element block (default), or the int8 absmax form of the
+// pages ([IL] CudaQwen3::absmax) with QL_GEMV_ACT=int8 or ql_set_gemv_activation_form.
+static std::atomic<int> g_act_form{-1};
+static int act_form() {
+    int f = g_act_form.load();
+    if (f < 0) {
+        const char* e = std::getenv("QL_GEMV_ACT");
+        f = (e != nullptr && std::string(e) == "int8") ? QL_GEMV_ACT_INT8 : QL_GEMV_ACT_INT16;
+        int expect = -1;
+        g_act_form.compare_exchange_strong(expect, f);
+        f = g_act_form.load();
+    }
+    return f;
+}
+
 int stream_gemv_prepare() {
     static std::mutex mu;
     static std::set<int> done;
@@ -83,6 +100,8 @@ int stream_gemv_prepare() {
     if (e == cudaSuccess) e = persist::stream_gemv_one<2, 8>(false, nullptr, nullptr, 0, 0, nullptr, false);
     if (e == cudaSuccess) e = persist::stream_gemv_one<1, 16>(false, nullptr, nullptr, 0, 0, nullptr, false);
     if (e == cudaSuccess) e = persist::stream_gemv_one<2, 16>(false, nullptr, nullptr, 0, 0, nullptr, false);
+    if (e == cudaSuccess) e = persist::stream_gemv_one<1, 16, true>(false, nullptr, nullptr, 0, 0, nullptr, false);
+    if (e == cudaSuccess) e = persist::stream_gemv_one<2, 16, true>(false, nullptr, nullptr, 0, 0, nullptr, false);
     if (e != cudaSuccess) return cuda_error(e, "stream gemv: kernel attributes");
     done.insert(dev);
     return QL_OK;
@@ -138,7 +157,10 @@ int stream_gemv_launch(const StreamGemvArgs& a, cudaStream_t s, bool pdl) {
     int grid = num_sms() * (warps == 8 ? 2 : 1);
     if (a.grid > 0 && a.grid < grid) grid = a.grid;
     cudaError_t e;
-    if (warps == 8)
+    if (act_form() == QL_GEMV_ACT_INT8)   // the int8 absmax form (16 warps)
+        e = a.batch == 1 ? persist::stream_gemv_one<1, 16, true>(true, &p, &g, smem, num_sms(), s, pdl)
+                         : persist::stream_gemv_one<2, 16, true>(true, &p, &g, smem, num_sms(), s, pdl);
+    else if (warps == 8)
         e = a.batch == 1 ? persist::stream_gemv_one<1, 8>(true, &p, &g, smem, grid, s, pdl)
                          : persist::stream_gemv_one<2, 8>(true, &p, &g, smem, grid, s, pdl);
     else
@@ -184,6 +206,14 @@ ql::PMat stream_mat(const void* d_stream, int64_t rows, int64_t cols, int silu) 
 bool aligned(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) & (n - 1)) == 0; }
 
 }  // namespace
+
+extern "C" int ql_set_gemv_activation_form(int form) {
+    using namespace ql;
+    QL_REQUIRE(form == QL_GEMV_ACT_INT16 || form == QL_GEMV_ACT_INT8, "ql_set_gemv_activation_form: unknown form");
+    const int prev = act_form();
+    g_act_form.store(form);
+    return prev;
+}
 
 extern "C" int64_t ql_q4_0_stream_bytes(int64_t rows, int64_t cols, int silu) {
     if (!stream_shape_ok(rows, cols, silu)) return 0;

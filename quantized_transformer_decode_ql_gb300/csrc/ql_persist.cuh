@@ -111,6 +111,14 @@ __device__ __forceinline__ int dp2a_hi(uint32_t a, uint32_t b, int c) {
     return d;
 }
 
+// Four-way dot product of four signed bytes (a) with four unsigned bytes (b), accumulated
+// exactly in 32 bits.
+__device__ __forceinline__ int dp4a_su(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
 // ------------------------------------------------------------------------------ grid barrier
 __device__ __forceinline__ unsigned long long global_ns() {
     unsigned long long t;
@@ -501,6 +509,174 @@ __device__ __noinline__ void stage_x(int B, float eps, int nblk, int cstride, co
     }
 }
 
+// The int8 activation form ([IL] CudaQwen3::absmax: the GEMV reads its activation vector with
+// one scale, xs = [max|x|, 1/max|x|]): per column, m = max|x| over the whole vector (a CTA-wide
+// reduction; RMS: of |x w| times the RMSNorm scale, found with the mean square), codes
+// q = rint(x * (127 / m)) with the division and the product each one f32 operation (__fdiv_rn,
+// __fmul_rn, then the exact rounding of an FADD of 1.5 * 2^23). Per column and block j two
+// uint4: (x[0..3], x[16..19], x[4..7], x[20..23]) and (x[8..11], x[24..27], x[12..15], x[28..31])
+// as signed bytes (code word t's low and high nibbles' elements), and the block's pair
+// (-128 sum_e q[e], m / (127 * 16)).
+template <bool RMS, int W>
+__device__ __noinline__ void stage_x8(int B, float eps, int nblk, int cstride, const float* xf, const __half* x16,
+                                      const float* w, uint4* xs, int2* sxs, int sxstride) {
+    constexpr int kHeld = 3, kT = W * 32;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int cols = nblk * 32, nitems = B * nblk * 4;
+    const int rounds = (nitems + kT - 1) / kT;
+    auto where = [&](int item, int& b, int& j, int& t) -> size_t {
+        t = item & 3;
+        const int bj = item >> 2;
+        b = bj < nblk ? 0 : (bj < 2 * nblk ? 1 : bj / nblk);
+        j = bj - b * nblk;
+        return (size_t)b * cols + 32 * j + 4 * t;
+    };
+    auto load = [&](int item, float (&v)[8]) {
+        int b, j, t;
+        const size_t off = where(item, b, j, t);
+        if (RMS) {
+            const float4 a = __ldcg(reinterpret_cast<const float4*>(xf + off));
+            const float4 h = __ldcg(reinterpret_cast<const float4*>(xf + off + 16));
+            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+            v[4] = h.x; v[5] = h.y; v[6] = h.z; v[7] = h.w;
+        } else {
+            const uint2 a = __ldcg(reinterpret_cast<const uint2*>(x16 + off));
+            const uint2 h = __ldcg(reinterpret_cast<const uint2*>(x16 + off + 16));
+            const float2 f0 = __half22float2(as_h2(a.x)), f1 = __half22float2(as_h2(a.y));
+            const float2 f2 = __half22float2(as_h2(h.x)), f3 = __half22float2(as_h2(h.y));
+            v[0] = f0.x; v[1] = f0.y; v[2] = f1.x; v[3] = f1.y;
+            v[4] = f2.x; v[5] = f2.y; v[6] = f3.x; v[7] = f3.y;
+        }
+    };
+    auto load_w = [&](int item, float (&v)[8]) {
+        const int j = (item >> 2) % nblk, t = item & 3;
+        const float4 a = __ldg(reinterpret_cast<const float4*>(w + 32 * j + 4 * t));
+        const float4 h = __ldg(reinterpret_cast<const float4*>(w + 32 * j + 16 + 4 * t));
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = h.x; v[5] = h.y; v[6] = h.z; v[7] = h.w;
+    };
+    float hx[kHeld][8], hw[kHeld][8];
+#pragma unroll
+    for (int r = 0; r < kHeld; ++r)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) hx[r][i] = hw[r][i] = 0.f;
+#pragma unroll
+    for (int r = 0; r < kHeld; ++r) {
+        const int item = tid + r * kT;
+        if (item < nitems) {
+            load(item, hx[r]);
+            if (RMS) load_w(item, hw[r]);
+        }
+    }
+    // pass 1: per column the mean square (RMS) and the largest magnitude
+    float ss0 = 0.f, ss1 = 0.f, mx0 = 0.f, mx1 = 0.f;
+    auto account = [&](int item, const float (&v)[8], const float (&wv)[8]) {
+        float s2 = 0.f, m = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (RMS) s2 = fmaf(v[i], v[i], s2);
+            m = fmaxf(m, fabsf(RMS ? v[i] * wv[i] : v[i]));
+        }
+        if (item < nblk * 4) {
+            ss0 += s2;
+            mx0 = fmaxf(mx0, m);
+        } else {
+            ss1 += s2;
+            mx1 = fmaxf(mx1, m);
+        }
+    };
+#pragma unroll
+    for (int r = 0; r < kHeld; ++r)
+        if (tid + r * kT < nitems) account(tid + r * kT, hx[r], hw[r]);
+    for (int item = tid + kHeld * kT; item < nitems; item += kT) {
+        float v[8], wv[8];
+        load(item, v);
+        if (RMS) load_w(item, wv);
+        account(item, v, wv);
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        ss0 += __shfl_xor_sync(0xffffffffu, ss0, o);
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+        ss1 += __shfl_xor_sync(0xffffffffu, ss1, o);
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    }
+    __shared__ float4 wred[W];
+    if (lane == 0) wred[warp] = make_float4(ss0, ss1, mx0, mx1);
+    __syncthreads();
+    float a0 = 0.f, a1 = 0.f, m0 = 0.f, m1 = 0.f;
+#pragma unroll
+    for (int i = 0; i < W; ++i) {
+        const float4 v = wred[i];
+        a0 += v.x;
+        a1 += v.y;
+        m0 = fmaxf(m0, v.z);
+        m1 = fmaxf(m1, v.w);
+    }
+    const float rs0 = RMS ? rsqrtf(fmaf(a0, 1.0f / (float)cols, eps)) : 1.0f;
+    const float rs1 = RMS ? rsqrtf(fmaf(a1, 1.0f / (float)cols, eps)) : 1.0f;
+    if (RMS) {
+        m0 *= rs0;
+        m1 *= rs1;
+    }
+    const float sc0 = m0 > 0.f ? __fdiv_rn(127.0f, m0) : 0.f, sc1 = m1 > 0.f ? __fdiv_rn(127.0f, m1) : 0.f;
+    const int f0 = __float_as_int(__fdiv_rn(m0, 2032.0f)), f1 = __float_as_int(__fdiv_rn(m1, 2032.0f));
+    // pass 2: codes, the blocks' offset terms (4 consecutive items = the 4 lanes of a block)
+    uint2* xs2 = reinterpret_cast<uint2*>(xs);
+    auto emit = [&](int item, bool ok, const float (&v)[8], float sc, int fb) {
+        uint32_t u[8];
+        int sum = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float r = __fadd_rn(__fmul_rn(v[i], sc), 12582912.0f);   // 1.5 * 2^23 + rint(x sc)
+            int qv = (int)(__float_as_uint(r) - 0x4B400000u);
+            qv = qv > 127 ? 127 : (qv < -127 ? -127 : qv);
+            u[i] = (uint32_t)qv;
+            sum += qv;
+        }
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        if (ok) {
+            int b, j, t;
+            where(item, b, j, t);
+            const uint32_t lo = __byte_perm(__byte_perm(u[0], u[1], 0x0040), __byte_perm(u[2], u[3], 0x0040), 0x5410);
+            const uint32_t hi = __byte_perm(__byte_perm(u[4], u[5], 0x0040), __byte_perm(u[6], u[7], 0x0040), 0x5410);
+            xs2[(size_t)b * cstride * 2 + 4 * j + t] = make_uint2(lo, hi);
+            if (t == 0) sxs[b * sxstride + j] = make_int2(-128 * sum, fb);
+        }
+    };
+#pragma unroll
+    for (int r = 0; r < kHeld; ++r) {
+        if (r < rounds) {
+            const int item = tid + r * kT;
+            const bool first = item < nblk * 4;
+            const float rr = first ? rs0 : rs1;
+            float v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = RMS ? hx[r][i] * rr * hw[r][i] : hx[r][i];
+            emit(item, item < nitems, v, first ? sc0 : sc1, first ? f0 : f1);
+        }
+    }
+    for (int r = kHeld; r < rounds; ++r) {
+        const int item = tid + r * kT;
+        const bool ok = item < nitems;
+        const bool first = item < nblk * 4;
+        const float rr = first ? rs0 : rs1;
+        float v[8], wv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = wv[i] = 0.f;
+        if (ok) {
+            load(item, v);
+            if (RMS) load_w(item, wv);
+        }
+        if (RMS) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] *= rr * wv[i];
+        }
+        emit(item, ok, v, first ? sc0 : sc1, first ? f0 : f1);
+    }
+}
+
 // Epilogue of one finished 16-row tile. acc[b][0] / acc[b][1] are this lane's sums of rows
 // (lane & 7) and (lane & 7) + 8 of the tile over the blocks of its quarter (lane >> 3) of every
 // unit, for column b; the quarters are added here (lanes l, l ^ 8, l ^ 16, l ^ 24), then
@@ -564,7 +740,7 @@ __device__ __noinline__ void finish_tile(const PersistParams& p, const PMat& M, 
 // the f16 scale and the activation block's 2^-(s + 4) in f32. The two rows share every
 // activation load. (An MMA form wastes 7 of the 8 columns of an m16n8k16 tile at batch 1-2 and
 // measured slower; the f16 HFMA2 form of the same loop issued about twice the instructions.)
-template <int NB, int W>
+template <int NB, int W, bool I8 = false>
 __device__ __noinline__ void gemv_phase(const PersistParams& p, Hot h, const PMat* mats, int wp, int epi, bool rms,
                                         Ring& ring, const float* xf,
                                         const __half* x16, const float* norm_w, void* y, int ld,
@@ -579,10 +755,17 @@ __device__ __noinline__ void gemv_phase(const PersistParams& p, Hot h, const PMa
     int2* sxs = reinterpret_cast<int2*>(xs + (size_t)NB * cstride);
     float4* part = reinterpret_cast<float4*>(sxs + (size_t)NB * sxstride);   // [W][2][32]
 
-    if (rms)
-        stage_x<true, W>(h.B, h.eps, M.nblk, cstride, xf, x16, norm_w, xs, sxs, sxstride);
-    else
-        stage_x<false, W>(h.B, h.eps, M.nblk, cstride, xf, x16, norm_w, xs, sxs, sxstride);
+    if (I8) {
+        if (rms)
+            stage_x8<true, W>(h.B, h.eps, M.nblk, cstride, xf, x16, norm_w, xs, sxs, sxstride);
+        else
+            stage_x8<false, W>(h.B, h.eps, M.nblk, cstride, xf, x16, norm_w, xs, sxs, sxstride);
+    } else {
+        if (rms)
+            stage_x<true, W>(h.B, h.eps, M.nblk, cstride, xf, x16, norm_w, xs, sxs, sxstride);
+        else
+            stage_x<false, W>(h.B, h.eps, M.nblk, cstride, xf, x16, norm_w, xs, sxs, sxstride);
+    }
     __syncthreads();
     stamp(tr, 2);
 
@@ -628,20 +811,32 @@ __device__ __noinline__ void gemv_phase(const PersistParams& p, Hot h, const PMa
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
             const int2 ov = sxs[b * sxstride + j];
-            const float f = __int_as_float(ov.y);   // 2^-(s + 4) of this activation block
+            const float f = __int_as_float(ov.y);   // the activation block's scale / 16
             int lo0 = 0, hi0 = ov.x, lo1 = 0, hi1 = ov.x;
-            const uint4* xb = xs + (size_t)b * cstride + 4 * j;
+            if (I8) {   // int8 codes: one dp4a per nibble half of a code word
+                const uint4 XA = xs[(size_t)b * cstride + 2 * j], XB = xs[(size_t)b * cstride + 2 * j + 1];
+                const uint32_t xl[4] = {XA.x, XA.z, XB.x, XB.z}, xh[4] = {XA.y, XA.w, XB.y, XB.w};
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                const uint4 X = xb[t];
-                lo0 = dp2a_lo(X.x, l0[t], lo0);
-                lo1 = dp2a_lo(X.x, l1[t], lo1);
-                lo0 = dp2a_hi(X.y, l0[t], lo0);
-                lo1 = dp2a_hi(X.y, l1[t], lo1);
-                hi0 = dp2a_lo(X.z, h0[t], hi0);
-                hi1 = dp2a_lo(X.z, h1[t], hi1);
-                hi0 = dp2a_hi(X.w, h0[t], hi0);
-                hi1 = dp2a_hi(X.w, h1[t], hi1);
+                for (int t = 0; t < 4; ++t) {
+                    lo0 = dp4a_su(xl[t], l0[t], lo0);
+                    lo1 = dp4a_su(xl[t], l1[t], lo1);
+                    hi0 = dp4a_su(xh[t], h0[t], hi0);
+                    hi1 = dp4a_su(xh[t], h1[t], hi1);
+                }
+            } else {
+                const uint4* xb = xs + (size_t)b * cstride + 4 * j;
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const uint4 X = xb[t];
+                    lo0 = dp2a_lo(X.x, l0[t], lo0);
+                    lo1 = dp2a_lo(X.x, l1[t], lo1);
+                    lo0 = dp2a_hi(X.y, l0[t], lo0);
+                    lo1 = dp2a_hi(X.y, l1[t], lo1);
+                    hi0 = dp2a_lo(X.z, h0[t], hi0);
+                    hi1 = dp2a_lo(X.z, h1[t], hi1);
+                    hi0 = dp2a_hi(X.w, h0[t], hi0);
+                    hi1 = dp2a_hi(X.w, h1[t], hi1);
+                }
             }
             acc[b][0] = fmaf(d0 * f, (float)(lo0 * 16 + hi0), acc[b][0]);
             acc[b][1] = fmaf(d1 * f, (float)(lo1 * 16 + hi1), acc[b][1]);
@@ -1304,7 +1499,7 @@ struct StreamGemv {
     int prewait;                 // ring slots issued before the wait (the rest after staging)
 };
 
-template <int NB, int W>
+template <int NB, int W, bool I8>
 __global__ void __launch_bounds__(W * 32, 16 / W) gemv_stream_kernel(const __grid_constant__ PersistParams p,
                                                                       const __grid_constant__ StreamGemv g) {
     extern __shared__ __align__(16) unsigned char smem[];
@@ -1342,8 +1537,8 @@ __global__ void __launch_bounds__(W * 32, 16 / W) gemv_stream_kernel(const __gri
     pdl_wait();
     pdl_trigger();
     stamp(tr, 1);
-    gemv_phase<NB, W>(p, hot, &mat, 0, g.epi, g.rms != 0, r, g.xf, g.x16, g.norm_w, g.y, g.ld,
-                      smem + (size_t)W * kStages * kSlotBytes, kred, tr);
+    gemv_phase<NB, W, I8>(p, hot, &mat, 0, g.epi, g.rms != 0, r, g.xf, g.x16, g.norm_w, g.y, g.ld,
+                          smem + (size_t)W * kStages * kSlotBytes, kred, tr);
     const unsigned long long t0 = global_ns();
     while (r.consumed < r.issued) {   // only after a wait ran out: let copies land (bounded)
         const uint32_t mb = r.mbar + (r.consumed % kStages) * 8, parity = (r.consumed / kStages) & 1u;
@@ -1413,7 +1608,7 @@ cudaError_t launch_kernel_pdl(K kernel, int grid, int threads, size_t smem, cuda
     return ql::launch(kernel, dim3(grid), dim3(threads), smem, s, pdl, args...);
 }
 
-template <int NB, int W>
+template <int NB, int W, bool I8 = false>
 cudaError_t stream_gemv_one(bool launch, const PersistParams* p, const StreamGemv* g, size_t smem, int grid,
                             cudaStream_t s, bool pdl) {
     if (!launch) {
@@ -1421,13 +1616,13 @@ cudaError_t stream_gemv_one(bool launch, const PersistParams* p, const StreamGem
         cudaFuncAttributes fa = {};
         cudaError_t e = cudaGetDevice(&dev);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, gemv_stream_kernel<NB, W>);
+        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, gemv_stream_kernel<NB, W, I8>);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(gemv_stream_kernel<NB, W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            e = cudaFuncSetAttribute(gemv_stream_kernel<NB, W, I8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      optin - (int)fa.sharedSizeBytes);
         return e;
     }
-    return launch_kernel_pdl(gemv_stream_kernel<NB, W>, grid, W * 32, smem, s, pdl, *p, *g);
+    return launch_kernel_pdl(gemv_stream_kernel<NB, W, I8>, grid, W * 32, smem, s, pdl, *p, *g);
 }
 
 }  // namespace persist
