@@ -71,20 +71,44 @@ class Q4Model:
         return dequantize(*q4)
 
 
-class KVCache:
-    """Per slot, per layer: K and V ``[n_kv_heads, capacity, head_dim]`` holding f16 values."""
+KV_F16 = "f16"
+KV_Q8_Q5 = "q8_0/q5_1"
 
-    def __init__(self, cfg, batch: int, capacity: int):
+
+class KVCache:
+    """Per slot, per layer: K and V ``[n_kv_heads, capacity, head_dim]`` holding the values the
+    cache stores: f16 (``kv="f16"``), or (``kv="q8_0/q5_1"``, memra-engine ``qwen4exp_gpu.rs``,
+    the Q8Q5 quantised-cache store) each K row as the decoded q8_0 row and each V row as the
+    decoded q5_1 row of its f32 value (``oracle.kvq``)."""
+
+    def __init__(self, cfg, batch: int, capacity: int, kv: str = KV_F16):
+        if kv not in (KV_F16, KV_Q8_Q5):
+            raise ValueError("unknown KV format")
         self.cfg = cfg
+        self.kv = kv
         shape = (batch, cfg.n_layers, cfg.n_kv_heads, capacity, cfg.head_dim)
         self.k = np.zeros(shape, dtype=np.float64)
         self.v = np.zeros(shape, dtype=np.float64)
 
+    def stored(self, k_rows: np.ndarray, v_rows: np.ndarray):
+        """The values the cache keeps for rows ``[..., head_dim]`` of K and V."""
+        if self.kv == KV_F16:
+            return _f16(k_rows), _f16(v_rows)
+        from . import kvq
+        hd = self.cfg.head_dim
+        kr = np.asarray(k_rows, dtype=np.float64).astype(np.float32).reshape(-1, hd)
+        vr = np.asarray(v_rows, dtype=np.float64).astype(np.float32).reshape(-1, hd)
+        kd = kvq.dequantize_q8_0(kvq.quantize_q8_0(kr), hd).astype(np.float64)
+        vd = kvq.dequantize_q5_1(kvq.quantize_q5_1(vr), hd).astype(np.float64)
+        return kd.reshape(np.shape(k_rows)), vd.reshape(np.shape(v_rows))
+
     def preload(self, slot: int, k_ctx: np.ndarray, v_ctx: np.ndarray):
-        """Pre-filled context ``[n_layers, n_kv, n_pos, hd]`` (f16) at positions 0..n_pos-1."""
+        """Pre-filled context ``[n_layers, n_kv, n_pos, hd]`` at positions 0..n_pos-1 (the f16
+        cache keeps its values as f16; the quantised one quantises them)."""
         n = k_ctx.shape[2]
-        self.k[slot, :, :, :n] = np.asarray(k_ctx, dtype=np.float16).astype(np.float64)
-        self.v[slot, :, :, :n] = np.asarray(v_ctx, dtype=np.float16).astype(np.float64)
+        kd, vd = self.stored(k_ctx, v_ctx)
+        self.k[slot, :, :, :n] = kd
+        self.v[slot, :, :, :n] = vd
 
 
 def _f16(a: np.ndarray) -> np.ndarray:
@@ -140,8 +164,7 @@ def decode_hidden(model: Q4Model, cache: KVCache, x, positions, act=None) -> np.
             p = int(positions[b])
             qb = ops.rope(ops.rmsnorm(q[b], L["q_norm"], cfg.eps), p, cfg.rope_theta)
             kb = ops.rope(ops.rmsnorm(k[b], L["k_norm"], cfg.eps), p, cfg.rope_theta)
-            cache.k[b, li, :, p] = _f16(kb)
-            cache.v[b, li, :, p] = _f16(v[b])
+            cache.k[b, li, :, p], cache.v[b, li, :, p] = cache.stored(kb, v[b])
             o[b] = ops.gqa_attention(qb, cache.k[b, li, :, : p + 1],
                                      cache.v[b, li, :, : p + 1], scale)
         x = x + ops.gemv(model.dense(L["wo"]), act(o.reshape(B, -1)))
