@@ -248,6 +248,38 @@ int ql_paged_attn_decode_noalloc(const void* d_q, const void* d_k_pool, const vo
                                  int block_size, int64_t max_blocks_per_seq, int64_t num_blocks,
                                  float scale, void* d_out, void* stream);
 
+/* --------------------------------------------------------------- quantised KV pool
+ * [ME] the quantised-cache storage (Q8Q5 store; host_quant_q8_row / host_quant_q5_row): keys as
+ * q8_0 rows (f16 d = max|x| / 127, codes round(x / d) in [-127, 127]) and values as q5_1 rows
+ * (f16 d = (max - min) / 31, f16 m = min, codes round((x - min) / d) in [0, 31]), per 32-element
+ * block, every step one f32 operation (the rule of ql_kv_quantize_q8_0 / _q5_1 above).
+ * Layout: one record of ql_kvq_record_bytes(head_dim) = 29 * head_dim bytes per (physical
+ * block, kv head), a layer's pool [num_blocks][n_kv][record]. A record holds the block's 16 key
+ * rows and 16 value rows, each field in its own array, all starting on 16-byte boundaries:
+ *   key codes int8 [16][hd] at 0; value nibbles u8 [16][hd/2] at 16 hd (per 32-element block,
+ *   byte l = code l | code l+16 << 4); key scales f16 [16][hd/32] at 24 hd; value bit 4 u32
+ *   [16][hd/32] at 25 hd (bit l = code l's); value scales f16 [16][hd/32] at 27 hd; value minima
+ *   f16 [16][hd/32] at 28 hd.
+ * The page's q8_0 block is (key scale, 32 key codes), its q5_1 block (scale, minimum, bit-4
+ * word, 16 nibble bytes): the same bytes in another order. head_dim 64 or 128 (0 otherwise).  */
+int64_t ql_kvq_record_bytes(int head_dim);
+/* Quantise d_k / d_v (f32 [n][n_kv_heads][head_dim], device) into one layer's pool: row i of kv
+ * head g goes to slot d_slots[i] % 16 of the record of physical block d_slots[i] / 16
+ * (int64 [n], device). A slot outside the pool is skipped and recorded in the device error
+ * record, as is a non-finite value or an f16 overflow of a scale (the row is still written).
+ * d_pool 16-byte aligned. Asynchronous on stream.                                          */
+int ql_kvq_write(const float* d_k, const float* d_v, const int64_t* d_slots, int64_t n, int n_kv_heads,
+                 int head_dim, void* d_pool, int64_t num_blocks, void* stream);
+/* ql_paged_attn_decode over a quantised pool (d_pool: one layer, the layout above, 16-byte
+ * aligned): keys and values are decoded as f16(d * code) and f16(fma(d, code, m)) and enter
+ * the same split-K attention (ticket merge). Arguments, workspace and errors as for
+ * ql_paged_attn_decode.                                                                     */
+int ql_paged_attn_decode_kvq(const void* d_q, const void* d_pool, const int32_t* d_block_tables,
+                             const int32_t* d_context_lens, int64_t batch, int n_heads, int n_kv_heads,
+                             int head_dim, int block_size, int64_t max_blocks_per_seq, int64_t num_blocks,
+                             float scale, void* d_out, void* d_workspace, size_t workspace_bytes,
+                             void* stream);
+
 /* How the context splits of a (sequence, kv head) are merged, for this process (every
  * attention entry point and the decode step; graphs keep the form they were captured with).
  * Both forms take the same online-softmax merge over the splits in order, so their outputs
@@ -326,7 +358,15 @@ typedef struct {
     int block_size;             /* 16 */
     int64_t max_batch;          /* largest batch any step will use */
     int64_t max_blocks_per_seq; /* block-table row length; max context = this * block_size */
+    int kv_format;              /* QL_KV_F16 (k_pool / v_pool) or QL_KV_Q8_0_Q5_1 (kvq_pool) */
+    void* kvq_pool;             /* QL_KV_Q8_0_Q5_1: u8 [n_layers][num_blocks][n_kv][ql_kvq_record_bytes] */
 } ql_model_desc;
+
+/* KV cache formats of a model (ql_model_desc.kv_format). QL_KV_Q8_0_Q5_1: the quantised pool of
+ * ql_paged_attn_decode_kvq; the decode step quantises each appended K row as q8_0 and V row as
+ * q5_1 (ql_kvq_write's rule) and reads every record back through the quantised attention. The
+ * persistent step kernel takes only QL_KV_F16.                                            */
+enum { QL_KV_F16 = 0, QL_KV_Q8_0_Q5_1 = 1 };
 
 typedef struct ql_model ql_model;
 

@@ -14,7 +14,7 @@ from ._lib import (QLError, QL_OK, QL_EINVAL, QL_ENOMEM, QL_ECUDA, QL_EPOOL, QL_
                    QL_EPI_ADD_RESIDUAL, QL_EPI_SILU_MUL, QL_STEP_AUTO, QL_STEP_LAUNCHES,
                    QL_STEP_PERSISTENT, QL_OPT_STEP_KERNEL, QL_OPT_BARRIER_TIMEOUT_NS,
                    QL_OPT_TEST_BARRIER_EXTRA, QL_OPT_STEP_TRACE, QL_BATCHED_MMA_SYNC, QL_BATCHED_TCGEN05,
-                   QL_GEMV_ACT_INT16, QL_GEMV_ACT_INT8,
+                   QL_GEMV_ACT_INT16, QL_GEMV_ACT_INT8, QL_KV_F16, QL_KV_Q8_0_Q5_1,
                    QL_ATTN_MERGE_TICKET, QL_ATTN_MERGE_CLUSTER,
                    Q4Matrix, LayerDesc, ModelDesc,
                    StepArgs, SIGNATURES, LIB_PATH, lib, check, ptr, stream_ptr)
@@ -24,6 +24,7 @@ __all__ = [
     "ql_q4_0_stream_bytes", "ql_q4_0_stream_pack", "ql_gemv_q4_0_stream",
     "ql_gemv_q4_0_stream_workspace_bytes", "ql_set_batched_gemv_form", "ql_set_gemv_activation_form",
     "ql_paged_attn_workspace_bytes", "ql_paged_attn_decode", "ql_paged_attn_decode_noalloc",
+    "ql_kvq_record_bytes", "ql_kvq_write", "ql_paged_attn_decode_kvq",
     "ql_set_attn_merge_form", "ql_paged_attn_merge_form",
     "ql_kv_q8_0_row_bytes", "ql_kv_q5_1_row_bytes", "ql_kv_quantize_q8_0", "ql_kv_dequantize_q8_0",
     "ql_kv_quantize_q5_1", "ql_kv_dequantize_q5_1", "ql_kv_quantize_device", "ql_kv_dequantize_device",
@@ -174,6 +175,25 @@ def ql_paged_attn_decode(q, k_pool, v_pool, block_tables, context_lens, batch, n
                                      block_size, max_blocks_per_seq, num_blocks, scale, ptr(out),
                                      ptr(workspace), workspace.numel() * workspace.element_size(),
                                      stream_ptr(stream)))
+
+
+def ql_kvq_record_bytes(head_dim):
+    return int(lib().ql_kvq_record_bytes(head_dim))
+
+
+def ql_kvq_write(k, v, slots, n_kv_heads, head_dim, pool, num_blocks, stream=None):
+    """Quantise f32 rows ``k``, ``v`` [n, n_kv, hd] into one layer's pool at physical ``slots``
+    (int64 [n], block * 16 + offset)."""
+    check(lib().ql_kvq_write(ptr(k), ptr(v), ptr(slots), slots.numel(), n_kv_heads, head_dim, ptr(pool),
+                             num_blocks, stream_ptr(stream)))
+
+
+def ql_paged_attn_decode_kvq(q, pool, block_tables, context_lens, batch, n_heads, n_kv_heads, head_dim,
+                             block_size, max_blocks_per_seq, num_blocks, scale, out, workspace, stream=None):
+    check(lib().ql_paged_attn_decode_kvq(ptr(q), ptr(pool), ptr(block_tables), ptr(context_lens), batch, n_heads,
+                                         n_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks, scale,
+                                         ptr(out), ptr(workspace), workspace.numel() * workspace.element_size(),
+                                         stream_ptr(stream)))
 
 
 def ql_paged_attn_decode_noalloc(q, k_pool, v_pool, block_tables, context_lens, batch, n_heads,

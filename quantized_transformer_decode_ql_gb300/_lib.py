@@ -20,6 +20,7 @@ QL_STEP_AUTO, QL_STEP_LAUNCHES, QL_STEP_PERSISTENT = 0, 1, 2
 QL_OPT_STEP_KERNEL, QL_OPT_BARRIER_TIMEOUT_NS, QL_OPT_TEST_BARRIER_EXTRA, QL_OPT_STEP_TRACE = 1, 2, 3, 4
 QL_BATCHED_MMA_SYNC, QL_BATCHED_TCGEN05 = 0, 1
 QL_GEMV_ACT_INT16, QL_GEMV_ACT_INT8 = 0, 1
+QL_KV_F16, QL_KV_Q8_0_Q5_1 = 0, 1
 QL_ATTN_MERGE_TICKET, QL_ATTN_MERGE_CLUSTER = 0, 1
 
 
@@ -46,7 +47,7 @@ class ModelDesc(ctypes.Structure):
                 ("embed", c_void_p), ("final_norm", c_void_p), ("lm_head", Q4Matrix),
                 ("layers", POINTER(LayerDesc)), ("k_pool", c_void_p), ("v_pool", c_void_p),
                 ("num_blocks", c_int64), ("block_size", c_int), ("max_batch", c_int64),
-                ("max_blocks_per_seq", c_int64)]
+                ("max_blocks_per_seq", c_int64), ("kv_format", c_int), ("kvq_pool", c_void_p)]
 
 
 class StepArgs(ctypes.Structure):
@@ -72,6 +73,10 @@ SIGNATURES = {
     "ql_gemv_q4_0_stream_workspace_bytes": (c_int64, [c_int64, c_int64, c_int]),
     "ql_set_batched_gemv_form": (c_int, [c_int]),
     "ql_set_gemv_activation_form": (c_int, [c_int]),
+    "ql_kvq_record_bytes": (c_int64, [c_int]),
+    "ql_kvq_write": (c_int, [c_void_p, c_void_p, c_void_p, c_int64, c_int, c_int, c_void_p, c_int64, c_void_p]),
+    "ql_paged_attn_decode_kvq": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int, c_int, c_int, c_int,
+                                         c_int64, c_int64, c_float, c_void_p, c_void_p, c_size_t, c_void_p]),
     "ql_paged_attn_workspace_bytes": (c_size_t, [c_int64, c_int, c_int, c_int, c_int, c_int64]),
     "ql_paged_attn_decode": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int64,
                                      c_int, c_int, c_int, c_int, c_int64, c_int64, c_float,

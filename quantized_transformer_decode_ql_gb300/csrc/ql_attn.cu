@@ -34,6 +34,7 @@
 #include <set>
 
 #include "ql_internal.h"
+#include "ql_kvq_rec.cuh"
 
 namespace ql {
 namespace {
@@ -74,6 +75,9 @@ struct AParams {
     long long max_position;
     __half* kw;
     __half* vw;
+    // quantised pool (KQ kernels): one record per (block, kv head), keys q8_0 and values q5_1
+    // (ql_kvq_rec.cuh); read by the attention, written by the fused append
+    uint8_t* kvq;
     unsigned long long* trace;   // optional stamps of the CTAs with linear index < trace_ctas
     int trace_ctas;
 };
@@ -141,6 +145,31 @@ __device__ __forceinline__ void warp_norm_rope(const float* src, const RopeLane<
     }
 }
 
+// The same normalisation and rotation with the f32 results kept in registers: out[k] is
+// dimension lane + 32 k (the layout of the warp-level KV quantisers).
+template <int HD>
+__device__ __forceinline__ void warp_norm_rope_vals(const float* src, const RopeLane<HD>& rl, float eps, int lane,
+                                                    float (&out)[HD / 32]) {
+    constexpr int H2 = HD / 2, PER = RopeLane<HD>::PER;
+    float xa[PER], xb[PER];
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+        xa[k] = __ldcg(src + lane + 32 * k);
+        xb[k] = __ldcg(src + lane + 32 * k + H2);
+        ss += xa[k] * xa[k] + xb[k] * xb[k];
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float r = rsqrtf(fmaf(ss, 1.0f / (float)HD, eps));
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+        const float a = xa[k] * r * rl.wa[k], bb = xb[k] * r * rl.wb[k];
+        out[k] = a * rl.c[k] - bb * rl.s[k];
+        out[k + PER] = a * rl.s[k] + bb * rl.c[k];
+    }
+}
+
 __device__ __forceinline__ float2 h2f(uint32_t u) {
     __half2 h;
     *reinterpret_cast<uint32_t*>(&h) = u;
@@ -181,7 +210,10 @@ __device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t addr) {
 
 // CL: the splits of a (sequence, kv head) form one cluster (grid x = cluster x = nsplit) and are
 // merged through distributed shared memory; otherwise by the ticket.
-template <int HD, int G, int NW, bool CL>
+// KQ: the pool is quantised (keys q8_0, values q5_1, one record of 29 HD bytes per (block, kv
+// head), ql_kvq_rec.cuh): a warp stages its blocks' records (double-buffered) and decodes each
+// into one pair of f16 K / V tiles just before its MMAs; the fused append quantises the new rows.
+template <int HD, int G, int NW, bool CL, bool KQ = false>
 __global__ void __launch_bounds__(NW * 32) attn_split_kernel(AParams p, DevError* err) {
     constexpr int kAttnWarps = NW, kAttnThreads = NW * 32;
     constexpr int KSTEPS = HD / 16;           // k-steps of the Q.K^T MMA
@@ -189,6 +221,8 @@ __global__ void __launch_bounds__(NW * 32) attn_split_kernel(AParams p, DevError
     constexpr int PITCH = HD * 2 + 16;        // bytes per staged K/V row (padded: conflict-free ldmatrix)
     constexpr int TILE = kBS * PITCH;         // one staged 16-key K or V tile
     constexpr int CHUNKS = HD * 2 / 16;       // 16-byte chunks per K/V row
+    constexpr int REC = Kvq<HD>::BYTES;       // one quantised record (KQ)
+    constexpr int WBYTES = KQ ? 2 * REC + 2 * TILE : 4 * TILE;   // shared memory per warp
     extern __shared__ __align__(16) unsigned char asmem[];   // staged tiles, later the merge buffers
     __shared__ float wm[kAttnWarps][G], wl[kAttnWarps][G];
     __shared__ int last_flag;
@@ -234,7 +268,8 @@ __global__ void __launch_bounds__(NW * 32) attn_split_kernel(AParams p, DevError
     const int pos = L - 1, lblk = pos / kBS, kp = pos % kBS;
 
     const int32_t* bt = p.block_tables + (size_t)b * p.maxb;
-    unsigned char* wtiles = asmem + (size_t)warp * 4 * TILE;        // [buffer][K | V]
+    // f16: [buffer][K | V] tiles; KQ: [buffer] records, then one decoded K | V tile pair
+    unsigned char* wtiles = asmem + (size_t)warp * WBYTES;
     const uint32_t wtiles_s = static_cast<uint32_t>(__cvta_generic_to_shared(wtiles));
     const int nb_w = blk1 - blk0 > warp ? (blk1 - blk0 - warp + kAttnWarps - 1) / kAttnWarps : 0;
 
@@ -245,6 +280,13 @@ __global__ void __launch_bounds__(NW * 32) attn_split_kernel(AParams p, DevError
         bool ok = phys >= 0 && phys < p.num_blocks;
         if (!ok) {
             if (lane == 0) record_device_error(err, kErrAttnBlock, (long long)b * p.maxb + blk, phys);
+        } else if (KQ) {
+            const unsigned char* src = p.kvq + ((size_t)phys * p.n_kv + g) * REC;
+            const uint32_t dst = wtiles_s + (uint32_t)((i & 1) * REC);
+            const unsigned long long pol = l2_evict_first();
+            for (int c = lane; c < REC / 16; c += 32)
+                asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst + c * 16),
+                             "l"(src + c * 16), "l"(pol) : "memory");
         } else {
             const __half* ksrc = p.k_pool + ((size_t)phys * p.n_kv + g) * kBS * HD;
             const __half* vsrc = p.v_pool + ((size_t)phys * p.n_kv + g) * kBS * HD;
@@ -304,7 +346,23 @@ __global__ void __launch_bounds__(NW * 32) attn_split_kernel(AParams p, DevError
                 if (lane == 0) record_device_error(err, kErrRopeBlock, (long long)b * p.maxb + lblk, phys);
             } else {
                 const size_t off = (((size_t)phys * p.n_kv + g) * kBS + kp) * HD;
-                if (warp == 0) {
+                if (KQ) {
+                    // quantise the new rows into the record (keys q8_0 from the rotated f32 K,
+                    // values q5_1 from the f32 V); knew / vnew get them as the tiles decode them
+                    uint8_t* rec = p.kvq + ((size_t)phys * p.n_kv + g) * REC;
+                    float xr[HD / 32];
+                    bool ok;
+                    if (warp == 0) {
+                        warp_norm_rope_vals<HD>(src + (size_t)(p.n_heads + g) * HD, rk, p.eps, lane, xr);
+                        ok = kvq_put_k_row<HD>(xr, rec, kp, lane, knew);
+                    } else {
+                        const float* vs = src + (size_t)(p.n_heads + p.n_kv + g) * HD;
+#pragma unroll
+                        for (int k = 0; k < HD / 32; ++k) xr[k] = __ldcg(vs + lane + 32 * k);
+                        ok = kvq_put_v_row<HD>(xr, rec, kp, lane, vnew);
+                    }
+                    if (!ok && lane == 0) record_device_error(err, kErrKvOverflow, (long long)b * p.maxb + lblk, kp);
+                } else if (warp == 0) {
                     warp_norm_rope<HD>(src + (size_t)(p.n_heads + g) * HD, rk, p.eps, knew, lane);
                     __syncwarp();
                     for (int i = lane; i < HD / 8; i += 32)
@@ -347,9 +405,15 @@ __global__ void __launch_bounds__(NW * 32) attn_split_kernel(AParams p, DevError
         const bool vcur = vbuf[i & 1];
         const int blk = blk0 + warp + kAttnWarps * i;
         const int nt = min(kBS, L - blk * kBS);      // valid keys in this block
+        // the f16 tiles this block is read from: its staging buffer, or (KQ) the decoded pair
+        const int tbuf = KQ ? 2 * REC : (i & 1) * 2 * TILE;
+        if (KQ && vcur) {
+            kvq_decode_tile<HD>(wtiles + (size_t)(i & 1) * REC, wtiles + tbuf, wtiles + tbuf + TILE, PITCH, lane);
+            __syncwarp();
+        }
         if (vcur && fused && blk == lblk) {
             // the new row: staged (possibly) before it was appended, so patch it in
-            unsigned char* kt = wtiles + (size_t)(i & 1) * 2 * TILE;
+            unsigned char* kt = wtiles + tbuf;
             if (lane < CHUNKS)
                 *reinterpret_cast<uint4*>(kt + kp * PITCH + lane * 16) = reinterpret_cast<const uint4*>(knew)[lane];
             else if (lane < 2 * CHUNKS)
@@ -358,7 +422,7 @@ __global__ void __launch_bounds__(NW * 32) attn_split_kernel(AParams p, DevError
             __syncwarp();
         }
         if (vcur) {
-            unsigned char* vtile = wtiles + (size_t)(i & 1) * 2 * TILE + TILE;
+            unsigned char* vtile = wtiles + tbuf + TILE;
             if (nt < kBS) {
                 // keys past the context: their P is 0, but a stale V row must not be NaN/Inf
                 for (int c = lane; c < (kBS - nt) * CHUNKS; c += 32) {
@@ -367,7 +431,7 @@ __global__ void __launch_bounds__(NW * 32) attn_split_kernel(AParams p, DevError
                 }
                 __syncwarp();
             }
-            const uint32_t ks = wtiles_s + (uint32_t)((i & 1) * 2 * TILE), vs = ks + TILE;
+            const uint32_t ks = wtiles_s + (uint32_t)tbuf, vs = ks + TILE;
             // ---- S = Q K^T for the 16 keys (two 8-key tiles)
             float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
             const int lm = lane >> 3, lr = lane & 7;
@@ -635,9 +699,10 @@ Layout layout(int64_t batch, int n_heads, int n_kv, int head_dim, int64_t maxb, 
 
 // Dynamic shared memory of one CTA: the warps' double-buffered K/V tiles, reused afterwards for
 // the warp-merge state and the cluster form's split partial.
-template <int HD, int G, int NW>
+template <int HD, int G, int NW, bool KQ = false>
 constexpr size_t attn_smem() {
-    const size_t tiles = (size_t)NW * 4 * kBS * (HD * 2 + 16);
+    const size_t tile = (size_t)kBS * (HD * 2 + 16);
+    const size_t tiles = (size_t)NW * (KQ ? 2 * (size_t)Kvq<HD>::BYTES + 2 * tile : 4 * tile);
     const size_t merge = (size_t)NW * G * HD * 4 + (size_t)G * HD * 4 + 2 * G * 4;
     return tiles > merge ? tiles : merge;
 }
@@ -674,6 +739,12 @@ cudaError_t allow_attn_smem(ClusterFit& fit) {
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(attn_split_kernel<HD, G, 8, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)attn_smem<HD, G, 8>());
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(attn_split_kernel<HD, G, 4, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)attn_smem<HD, G, 4, true>());
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(attn_split_kernel<HD, G, 8, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)attn_smem<HD, G, 8, true>());
     auto* kcl = attn_split_kernel<HD, G, 8, true>;
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(kcl, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)attn_smem<HD, G, 8>());
@@ -739,6 +810,13 @@ cudaError_t launch_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size
 template <int HD, int G>
 cudaError_t launch_hg(const AParams& p, int batch, cudaStream_t s, bool pdl, DevError* err) {
     dim3 grid(p.nsplit, p.n_kv, batch);
+    if (p.kvq != nullptr) {   // quantised pool: the ticket merge
+        if (attn_warps(batch) == 8)
+            return launch(attn_split_kernel<HD, G, 8, false, true>, grid, dim3(8 * 32), attn_smem<HD, G, 8, true>(), s,
+                          pdl, p, err);
+        return launch(attn_split_kernel<HD, G, 4, false, true>, grid, dim3(4 * 32), attn_smem<HD, G, 4, true>(), s,
+                      pdl, p, err);
+    }
     if (use_cluster(HD, G, p.nsplit, p.n_kv, batch))
         return launch_cluster(attn_split_kernel<HD, G, 8, true>, grid, dim3(8 * 32), attn_smem<HD, G, 8>(), s, pdl,
                               (unsigned int)p.nsplit, p, err);
@@ -808,7 +886,7 @@ int attn_check_alignment(const void* q, const void* k_pool, const void* v_pool, 
 }
 
 int attn_launch(const AttnArgs& a, cudaStream_t s, bool pdl) {
-    QL_REQUIRE((a.q || a.qkv) && a.k_pool && a.v_pool && a.block_tables && a.out && a.workspace,
+    QL_REQUIRE((a.q || a.qkv) && ((a.k_pool && a.v_pool) || a.kvq) && a.block_tables && a.out && a.workspace,
                "attention: null pointer");
     QL_REQUIRE(!a.qkv || (a.q_norm && a.k_norm && a.cos_t && a.sin_t && a.positions && a.max_position > 0),
                "attention: the fused qk-norm/RoPE form needs norms, tables and positions");
@@ -825,7 +903,9 @@ int attn_launch(const AttnArgs& a, cudaStream_t s, bool pdl) {
     const Layout lo = layout(a.batch, a.n_heads, a.n_kv_heads, a.head_dim, a.max_blocks_per_seq, num_sms());
     if (a.workspace_bytes < lo.total)
         return set_error(QL_EINVAL, "attention: workspace too small (need " + std::to_string(lo.total) + " bytes)");
-    if (int rc = attn_check_alignment(a.q, a.k_pool, a.v_pool, a.out, "attention")) return rc;
+    const void* kpool = a.kvq ? static_cast<const void*>(a.kvq) : static_cast<const void*>(a.k_pool);
+    const void* vpool = a.kvq ? static_cast<const void*>(a.kvq) : static_cast<const void*>(a.v_pool);
+    if (int rc = attn_check_alignment(a.q, kpool, vpool, a.out, "attention")) return rc;
     if (!device_error_record()) return set_error(QL_ECUDA, "attention: no device error record");
     if (int rc = attn_prepare()) return rc;
     AParams p = {};
@@ -862,6 +942,7 @@ int attn_launch(const AttnArgs& a, cudaStream_t s, bool pdl) {
     p.max_position = a.max_position;
     p.kw = const_cast<__half*>(a.k_pool);
     p.vw = const_cast<__half*>(a.v_pool);
+    p.kvq = a.kvq;
     cudaError_t e = a.head_dim == 128 ? launch_h<128>(p, G, a.batch, s, pdl, device_error_record())
                                       : launch_h<64>(p, G, a.batch, s, pdl, device_error_record());
     if (e != cudaSuccess) return cuda_error(e, "attention launch");
@@ -903,6 +984,33 @@ extern "C" int ql_paged_attn_decode(const void* d_q, const void* d_k_pool, const
     a.workspace = d_workspace;
     a.workspace_bytes = workspace_bytes;
     if (batch < 1 || batch > 65535) return set_error(QL_EINVAL, "ql_paged_attn_decode: batch out of range");
+    return attn_launch(a, static_cast<cudaStream_t>(stream), true);
+}
+
+extern "C" int ql_paged_attn_decode_kvq(const void* d_q, const void* d_pool, const int32_t* d_block_tables,
+                                        const int32_t* d_context_lens, int64_t batch, int n_heads, int n_kv_heads,
+                                        int head_dim, int block_size, int64_t max_blocks_per_seq, int64_t num_blocks,
+                                        float scale, void* d_out, void* d_workspace, size_t workspace_bytes,
+                                        void* stream) {
+    using namespace ql;
+    QL_REQUIRE(d_context_lens && d_pool, "ql_paged_attn_decode_kvq: null pointer");
+    AttnArgs a = {};
+    a.q = static_cast<const __half*>(d_q);
+    a.kvq = static_cast<uint8_t*>(const_cast<void*>(d_pool));
+    a.block_tables = d_block_tables;
+    a.context_lens = d_context_lens;
+    a.batch = (int)batch;
+    a.n_heads = n_heads;
+    a.n_kv_heads = n_kv_heads;
+    a.head_dim = head_dim;
+    a.block_size = block_size;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.scale = scale;
+    a.out = static_cast<__half*>(d_out);
+    a.workspace = d_workspace;
+    a.workspace_bytes = workspace_bytes;
+    if (batch < 1 || batch > 65535) return set_error(QL_EINVAL, "ql_paged_attn_decode_kvq: batch out of range");
     return attn_launch(a, static_cast<cudaStream_t>(stream), true);
 }
 

@@ -183,6 +183,8 @@ struct AttnArgs {
     const float* sin_t;
     float eps;
     int64_t max_position;
+    uint8_t* kvq;                // quantised pool of the layer (keys q8_0, values q5_1) instead of
+                                 // k_pool / v_pool; the fused form appends to it
     unsigned long long* trace;   // optional [CTAs][8] globaltimer stamps (CTAs with a linear index
     int trace_ctas;              // below trace_ctas): 0 start, 1 past the wait, 2 q ready,
                                  // 3 blocks done, 4 partial written / ticket taken, 5 end

@@ -202,10 +202,14 @@ int run_step(ql_model* m, const ql_step_args* a, cudaStream_t s) {
     if (m->step_kernel == QL_STEP_PERSISTENT && B > m->persist_max_b)
         return set_error(QL_EINVAL, "decode step: the persistent step kernel takes batches up to " +
                                         std::to_string(m->persist_max_b) + " on this model");
+    if (m->step_kernel == QL_STEP_PERSISTENT && m->d.kv_format != QL_KV_F16)
+        return set_error(QL_EINVAL, "decode step: the persistent step kernel takes only the f16 KV format");
     if (m->step_kernel == QL_STEP_PERSISTENT) return run_persist(m, a, s);
     const bool pdl = true;
     const int hd = (int)d.head_dim, nh = (int)d.n_heads, nkv = (int)d.n_kv_heads;
     const size_t layer_pool = (size_t)d.num_blocks * nkv * d.block_size * hd;
+    const bool kvq = d.kv_format == QL_KV_Q8_0_Q5_1;
+    const size_t kvq_layer = (size_t)d.num_blocks * nkv * (size_t)ql_kvq_record_bytes(hd);
     int rc;
 
     // Each kernel asks L2 to fetch the weights of a GEMV that follows it, so that HBM keeps
@@ -278,8 +282,11 @@ int run_step(ql_model* m, const ql_step_args* a, cudaStream_t s) {
             at.sin_t = m->sin_t;
             at.eps = d.eps;
             at.max_position = d.max_blocks_per_seq * d.block_size;
-            at.k_pool = static_cast<__half*>(d.k_pool) + layer_pool * li;
-            at.v_pool = static_cast<__half*>(d.v_pool) + layer_pool * li;
+            if (kvq) at.kvq = static_cast<uint8_t*>(d.kvq_pool) + kvq_layer * li;
+            else {
+                at.k_pool = static_cast<__half*>(d.k_pool) + layer_pool * li;
+                at.v_pool = static_cast<__half*>(d.v_pool) + layer_pool * li;
+            }
             at.block_tables = a->block_tables;
             at.positions = a->positions;
             at.active = a->active;
@@ -341,8 +348,11 @@ int run_step(ql_model* m, const ql_step_args* a, cudaStream_t s) {
         at.sin_t = m->sin_t;
         at.eps = d.eps;
         at.max_position = d.max_blocks_per_seq * d.block_size;
-        at.k_pool = static_cast<__half*>(d.k_pool) + layer_pool * li;
-        at.v_pool = static_cast<__half*>(d.v_pool) + layer_pool * li;
+        if (kvq) at.kvq = static_cast<uint8_t*>(d.kvq_pool) + kvq_layer * li;
+        else {
+            at.k_pool = static_cast<__half*>(d.k_pool) + layer_pool * li;
+            at.v_pool = static_cast<__half*>(d.v_pool) + layer_pool * li;
+        }
         at.block_tables = a->block_tables;
         at.context_lens = nullptr;
         at.positions = a->positions;
@@ -569,7 +579,11 @@ extern "C" int ql_model_create(const ql_model_desc* desc, ql_model** out) {
     QL_REQUIRE((d.n_heads * d.head_dim) % 32 == 0, "ql_model_create: n_heads*head_dim must be a multiple of 32");
     QL_REQUIRE(d.vocab > 0 && d.embed && d.final_norm, "ql_model_create: need vocab, embed, final_norm");
     QL_REQUIRE(d.block_size == 16, "ql_model_create: block_size must be 16");
-    QL_REQUIRE(d.k_pool && d.v_pool && d.num_blocks > 0, "ql_model_create: need KV pools");
+    QL_REQUIRE(d.kv_format == QL_KV_F16 || d.kv_format == QL_KV_Q8_0_Q5_1, "ql_model_create: unknown kv_format");
+    QL_REQUIRE(d.num_blocks > 0 && (d.kv_format == QL_KV_F16 ? (d.k_pool && d.v_pool) : d.kvq_pool != nullptr),
+               "ql_model_create: need KV pools (k_pool and v_pool, or kvq_pool for the quantised format)");
+    QL_REQUIRE(d.kv_format == QL_KV_F16 || (reinterpret_cast<uintptr_t>(d.kvq_pool) & 15) == 0,
+               "ql_model_create: kvq_pool must be 16-byte aligned");
     QL_REQUIRE(d.max_batch >= 1 && d.max_batch <= 4096, "ql_model_create: max_batch out of range");
     QL_REQUIRE(d.max_blocks_per_seq >= 1, "ql_model_create: bad max_blocks_per_seq");
     QL_REQUIRE(d.eps > 0.f && d.rope_theta > 0.0, "ql_model_create: eps and rope_theta must be positive");
@@ -651,7 +665,7 @@ extern "C" int ql_model_set_option(ql_model* m, int option, int64_t value) {
         case QL_OPT_STEP_KERNEL:
             if (value != QL_STEP_AUTO && value != QL_STEP_LAUNCHES && value != QL_STEP_PERSISTENT)
                 return set_error(QL_EINVAL, "ql_model_set_option: unknown step kernel");
-            if (value == QL_STEP_PERSISTENT && m->persist_max_b < 1)
+            if (value == QL_STEP_PERSISTENT && (m->persist_max_b < 1 || m->d.kv_format != QL_KV_F16))
                 return set_error(QL_EINVAL, "ql_model_set_option: the persistent step kernel is not available for this model");
             m->step_kernel = (int)value;
             return QL_OK;

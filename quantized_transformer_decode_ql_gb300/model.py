@@ -11,7 +11,7 @@ import ctypes
 
 import torch
 
-from ._lib import (LayerDesc, ModelDesc, Q4Matrix, StepArgs, check, lib, ptr, stream_ptr)
+from ._lib import (LayerDesc, ModelDesc, Q4Matrix, QL_KV_F16, StepArgs, check, lib, ptr, stream_ptr)
 
 BLOCK = 16
 
@@ -50,9 +50,10 @@ class DeviceModel:
     """A dense Qwen3-style model resident on one GPU, plus its paged KV pools."""
 
     def __init__(self, cfg, weights: dict, num_blocks: int, max_batch: int,
-                 max_blocks_per_seq: int, device="cuda"):
+                 max_blocks_per_seq: int, device="cuda", kv_format: int = QL_KV_F16):
         self.cfg = cfg
         self.device = device
+        self.kv_format = kv_format
         self.num_blocks = num_blocks
         self.max_batch = max_batch
         self.max_blocks_per_seq = max_blocks_per_seq
@@ -68,17 +69,31 @@ class DeviceModel:
             self.layers.append(L)
         torch.cuda.synchronize()
         check(lib().ql_check_device_error(None))
-        shape = (cfg.n_layers, num_blocks, cfg.n_kv_heads, BLOCK, cfg.head_dim)
-        self.k_pool = torch.zeros(shape, dtype=torch.float16, device=device)
-        self.v_pool = torch.zeros(shape, dtype=torch.float16, device=device)
+        self._alloc_pools()
         self._create()
 
+    def _alloc_pools(self):
+        """KV pools: f16 K and V [n_layers, num_blocks, n_kv, 16, hd], or the quantised records
+        [n_layers, num_blocks, n_kv, ql_kvq_record_bytes(hd)] (u8)."""
+        cfg = self.cfg
+        if self.kv_format == QL_KV_F16:
+            shape = (cfg.n_layers, self.num_blocks, cfg.n_kv_heads, BLOCK, cfg.head_dim)
+            self.k_pool = torch.zeros(shape, dtype=torch.float16, device=self.device)
+            self.v_pool = torch.zeros(shape, dtype=torch.float16, device=self.device)
+            self.kvq_pool = None
+        else:
+            rec = int(lib().ql_kvq_record_bytes(cfg.head_dim))
+            self.k_pool = self.v_pool = None
+            self.kvq_pool = torch.zeros((cfg.n_layers, self.num_blocks, cfg.n_kv_heads, rec), dtype=torch.uint8,
+                                        device=self.device)
+
     @classmethod
-    def from_layer_fn(cls, cfg, tensor_fn, num_blocks, max_batch, max_blocks_per_seq, device="cuda"):
+    def from_layer_fn(cls, cfg, tensor_fn, num_blocks, max_batch, max_blocks_per_seq, device="cuda",
+                      kv_format: int = QL_KV_F16):
         """Build from ``tensor_fn(layer or None, name) -> f32 device tensor``, one tensor at a
         time (for models too large to hold as f32 anywhere)."""
         self = cls.__new__(cls)
-        self.cfg, self.device = cfg, device
+        self.cfg, self.device, self.kv_format = cfg, device, kv_format
         self.num_blocks, self.max_batch, self.max_blocks_per_seq = num_blocks, max_batch, max_blocks_per_seq
         self.embed = tensor_fn(None, "embed")
         self.final_norm = tensor_fn(None, "final_norm")
@@ -93,23 +108,21 @@ class DeviceModel:
             self.layers.append(L)
         torch.cuda.synchronize()
         check(lib().ql_check_device_error(None))
-        shape = (cfg.n_layers, num_blocks, cfg.n_kv_heads, BLOCK, cfg.head_dim)
-        self.k_pool = torch.zeros(shape, dtype=torch.float16, device=device)
-        self.v_pool = torch.zeros(shape, dtype=torch.float16, device=device)
+        self._alloc_pools()
         self._create()
         return self
 
-    def sibling(self, num_blocks: int, max_batch: int, max_blocks_per_seq: int) -> "DeviceModel":
-        """Another model handle over the same weight tensors, with its own KV pools, batch bound
-        and block-table width (for example a batched workload next to a batch-1 one). The
-        weights must outlive both handles."""
+    def sibling(self, num_blocks: int, max_batch: int, max_blocks_per_seq: int,
+                kv_format: int | None = None) -> "DeviceModel":
+        """Another model handle over the same weight tensors, with its own KV pools, batch bound,
+        block-table width and KV format (for example a batched workload next to a batch-1 one).
+        The weights must outlive both handles."""
         other = DeviceModel.__new__(DeviceModel)
         other.cfg, other.device = self.cfg, self.device
+        other.kv_format = self.kv_format if kv_format is None else kv_format
         other.num_blocks, other.max_batch, other.max_blocks_per_seq = num_blocks, max_batch, max_blocks_per_seq
         other.embed, other.final_norm, other.lm_head, other.layers = self.embed, self.final_norm, self.lm_head, self.layers
-        shape = (self.cfg.n_layers, num_blocks, self.cfg.n_kv_heads, BLOCK, self.cfg.head_dim)
-        other.k_pool = torch.zeros(shape, dtype=torch.float16, device=self.device)
-        other.v_pool = torch.zeros(shape, dtype=torch.float16, device=self.device)
+        other._alloc_pools()
         other._create()
         return other
 
@@ -129,6 +142,7 @@ class DeviceModel:
         d.k_pool, d.v_pool = ptr(self.k_pool), ptr(self.v_pool)
         d.num_blocks, d.block_size = self.num_blocks, BLOCK
         d.max_batch, d.max_blocks_per_seq = self.max_batch, self.max_blocks_per_seq
+        d.kv_format, d.kvq_pool = self.kv_format, ptr(self.kvq_pool)
         self._desc = d
         h = ctypes.c_void_p()
         check(lib().ql_model_create(ctypes.byref(d), ctypes.byref(h)))
@@ -170,9 +184,21 @@ class DeviceModel:
         check(lib().ql_check_device_error(self.handle))
 
     def write_context(self, slot_blocks, k_ctx, v_ctx):
-        """Place a pre-filled context ``[n_layers, n_kv, n_pos, hd]`` (f16) into the pools
-        through a slot's block list (a host-side copy that stands in for prefill)."""
+        """Place a pre-filled context ``[n_layers, n_kv, n_pos, hd]`` into the pools through a
+        slot's block list (stands in for prefill): f16 pools take the values as f16; the quantised
+        pool takes them quantised on the device (``ql_kvq_write``, per layer)."""
         n = k_ctx.shape[2]
+        if self.kv_format != QL_KV_F16:
+            cfg = self.cfg
+            pos = torch.arange(n, device=self.device)
+            blocks = torch.as_tensor(list(slot_blocks), dtype=torch.int64, device=self.device)
+            slots = (blocks[pos // BLOCK] * BLOCK + pos % BLOCK).contiguous()
+            for li in range(cfg.n_layers):
+                kl = torch.as_tensor(k_ctx[li], device=self.device).float().permute(1, 0, 2).contiguous()
+                vl = torch.as_tensor(v_ctx[li], device=self.device).float().permute(1, 0, 2).contiguous()
+                check(lib().ql_kvq_write(ptr(kl), ptr(vl), ptr(slots), n, cfg.n_kv_heads, cfg.head_dim,
+                                         ptr(self.kvq_pool[li]), self.num_blocks, stream_ptr(None)))
+            return
         kc = torch.as_tensor(k_ctx, dtype=torch.float16, device=self.device)
         vc = torch.as_tensor(v_ctx, dtype=torch.float16, device=self.device)
         for i, blk in enumerate(slot_blocks):

@@ -73,3 +73,40 @@ def test_decode_over_the_quantised_cache():
     rows = cq.k[0, :, :, :6].reshape(-1, cfg.head_dim).astype(np.float32)
     again = kvq.dequantize_q8_0(kvq.quantize_q8_0(rows), cfg.head_dim)
     assert np.array_equal(again.astype(np.float64), rows.astype(np.float64))
+
+
+def test_quantised_cache_amplifies_input_rounding():
+    """Why the GPU's quantised-cache decode is held to three times the step tolerance: the
+    codes are decided from the K and V rows, so a relative change of 1e-3 in those rows (the
+    rounding level of a GEMV with f16 activations) flips codes at rounding boundaries, and each
+    flip moves a value by a whole step. Measured here on the oracle alone (tiny model, batch 3,
+    20 teacher-forced steps): the f16 cache's logits move by well under the step tolerance
+    (2e-2 + 1e-2 |ref|), the quantised cache's by more than it, and by less than three times it."""
+    cfg = ql_inputs.TINY
+    w = ql_inputs.weights(cfg, seed=0)
+    m = decode.Q4Model(cfg, w)
+
+    class Perturbed(decode.KVCache):
+        def __init__(self, *a, **k):
+            super().__init__(*a, **k)
+            self.rng = np.random.default_rng(0)
+
+        def stored(self, k, v):
+            k = k * (1 + 1e-3 * self.rng.standard_normal(np.shape(k)))
+            v = v * (1 + 1e-3 * self.rng.standard_normal(np.shape(v)))
+            return super().stored(k, v)
+
+    worst = {}
+    for kv in (decode.KV_F16, decode.KV_Q8_Q5):
+        c0 = decode.KVCache(cfg, 3, 32, kv=kv)
+        c1 = Perturbed(cfg, 3, 32, kv=kv)
+        toks = ql_inputs.prompt_tokens(3, cfg.vocab, seed=1).astype(np.int64)
+        r = 0.0
+        for step in range(20):
+            a = decode.decode_step(m, c0, toks, [step] * 3)
+            b = decode.decode_step(m, c1, toks, [step] * 3)
+            r = max(r, float((np.abs(a - b) / (2e-2 + 1e-2 * np.abs(a))).max()))
+            toks = decode.greedy(a).astype(np.int64)
+        worst[kv] = r
+    assert worst[decode.KV_F16] < 0.25
+    assert 1.0 < worst[decode.KV_Q8_Q5] < 3.0
