@@ -217,7 +217,7 @@ def gemv_kinds(gm, cfg, B, s, g):
     return out
 
 
-def attn_alone(B, lo, hi, s, g, seed=6, iters=10):
+def attn_alone(B, lo, hi, s, g, seed=6, iters=10, kvq=False):
     """Paged GQA decode attention alone at the attention workload's shape (32/8 heads, head_dim
     128, 16-token blocks, randomly permuted block tables): B sequences with lengths uniform in
     [lo, hi]; L2 flushed (a 256 MB read) before every launch, the flush timed apart and taken out."""
@@ -233,8 +233,19 @@ def attn_alone(B, lo, hi, s, g, seed=6, iters=10):
     for b, n in enumerate(nblk):
         bt[b, :n] = perm[off:off + n]
         off += n
-    kp = torch.randn((num_blocks, nkv, 16, hd), generator=g, device="cuda").half()
-    vp = torch.randn((num_blocks, nkv, 16, hd), generator=g, device="cuda").half()
+    if kvq:   # records quantised on the device from N(0,1) rows, 65536 positions at a time
+        pool = torch.zeros((num_blocks, nkv, ql.ql_kvq_record_bytes(hd)), dtype=torch.uint8, device="cuda")
+        for p0 in range(0, num_blocks * 16, 65536):
+            n = min(65536, num_blocks * 16 - p0)
+            slots = torch.arange(p0, p0 + n, dtype=torch.int64, device="cuda")
+            k = torch.randn((n, nkv, hd), generator=g, device="cuda")
+            v = torch.randn((n, nkv, hd), generator=g, device="cuda")
+            ql.ql_kvq_write(k, v, slots, nkv, hd, pool, num_blocks)   # on the stream that made k, v
+        torch.cuda.synchronize()
+        del k, v
+    else:
+        kp = torch.randn((num_blocks, nkv, 16, hd), generator=g, device="cuda").half()
+        vp = torch.randn((num_blocks, nkv, 16, hd), generator=g, device="cuda").half()
     q = torch.randn((B, nh, hd), generator=g, device="cuda").half()
     o = torch.empty((B, nh * hd), dtype=torch.float16, device="cuda")
     cl = torch.from_numpy(lens).cuda()
@@ -244,7 +255,12 @@ def attn_alone(B, lo, hi, s, g, seed=6, iters=10):
     torch.cuda.synchronize()
 
     def run():
-        ql.ql_paged_attn_decode(q, kp, vp, bt, cl, B, nh, nkv, hd, 16, maxb, num_blocks, 1 / math.sqrt(hd), o, ws, s)
+        if kvq:
+            ql.ql_paged_attn_decode_kvq(q, pool, bt, cl, B, nh, nkv, hd, 16, maxb, num_blocks, 1 / math.sqrt(hd), o,
+                                        ws, s)
+        else:
+            ql.ql_paged_attn_decode(q, kp, vp, bt, cl, B, nh, nkv, hd, 16, maxb, num_blocks, 1 / math.sqrt(hd), o,
+                                    ws, s)
     with torch.cuda.stream(s):
         run()                       # first call outside capture (per-device set-up)
     s.synchronize()
@@ -258,21 +274,42 @@ def attn_alone(B, lo, hi, s, g, seed=6, iters=10):
         for _ in range(iters):
             flush_sum.copy_(flush.sum())
     us = (graph_ms(flush_then_run, s, 3) - graph_ms(flush_only, s, 3)) * 1e3 / iters
-    nbytes = sum(2 * int(L) * nkv * hd * 2 + 4 * ((int(L) + 15) // 16) for L in lens) + B * nh * hd * 4
+    per_pos = nkv * 29 * hd / 16 if kvq else 2 * nkv * hd * 2   # K and V bytes of one position
+    nbytes = int(sum(int(L) * per_pos + 4 * ((int(L) + 15) // 16) for L in lens) + B * nh * hd * 4)
     return {"batch": B, "lengths": f"uniform in [{lo}, {hi}] (seed {seed})", "sum_len": int(lens.sum()),
+            "kv": "q8_0 K / q5_1 V records" if kvq else "f16",
             "us_per_launch": round(us, 2), "bytes_per_launch": int(nbytes),
             "achieved_gbs": round(nbytes / (us * 1e-6) / 1e9, 1)}
 
 
 def prefill_context(gm, cfg, ids, n_pos, g):
-    """Synthetic pre-filled context (stands in for prefill): N(0,1) f16 K and V written straight
-    into a slot's blocks of every layer and kv head."""
+    """Synthetic pre-filled context (stands in for prefill): N(0,1) K and V written straight
+    into a slot's blocks of every layer and kv head: as f16 into an f16 pool, quantised on the
+    device (ql_kvq_write) into a quantised one."""
     import torch
+    import quantized_transformer_decode_ql_gb300 as ql
     nb = (n_pos + 15) // 16
     idx = torch.as_tensor(list(ids[:nb]), dtype=torch.long, device="cuda")
+    if gm.kv_format != ql.QL_KV_F16:
+        pos = torch.arange(n_pos, device="cuda")
+        slots = (idx[pos // 16] * 16 + pos % 16).contiguous()
+        for li in range(cfg.n_layers):
+            k = torch.randn((n_pos, cfg.n_kv_heads, cfg.head_dim), generator=g, device="cuda")
+            v = torch.randn((n_pos, cfg.n_kv_heads, cfg.head_dim), generator=g, device="cuda")
+            ql.ql_kvq_write(k, v, slots, cfg.n_kv_heads, cfg.head_dim, gm.kvq_pool[li], gm.num_blocks)
+        return
     shape = (cfg.n_layers, nb, cfg.n_kv_heads, 16, cfg.head_dim)
     gm.k_pool[:, idx] = torch.randn(shape, generator=g, device="cuda").half()
     gm.v_pool[:, idx] = torch.randn(shape, generator=g, device="cuda").half()
+
+
+def kv_bytes_per_token(gm, cfg):
+    """KV bytes one cached position costs over all layers: f16 K and V, or its share of the
+    quantised records (29 head_dim bytes per 16 positions and kv head)."""
+    import quantized_transformer_decode_ql_gb300 as ql
+    if gm.kv_format == ql.QL_KV_F16:
+        return cfg.n_layers * 2 * cfg.n_kv_heads * cfg.head_dim * 2
+    return cfg.n_layers * cfg.n_kv_heads * 29 * cfg.head_dim / 16
 
 
 def build_e1(cfg, steps, warmup):
@@ -389,6 +426,7 @@ def gpu_arm(args, rank, world, local_rank):
     kernels["paged_attention_e1"] = attn_alone(1, int(ctx_avg), int(ctx_avg), s, g)
     if not args.layers:
         kernels["paged_attention_a_b32"] = attn_alone(32, 512, 32768, s, g)
+        kernels["paged_attention_a_b32_kvq"] = attn_alone(32, 512, 32768, s, g, kvq=True)
     for k in kernels.values():
         for v in (k.values() if "qkv" in k else [k]):
             v["frac"] = round(v["achieved_gbs"] / peak, 4)
@@ -436,11 +474,13 @@ def gpu_arm(args, rank, world, local_rank):
     if phases:
         line["step_phases_us"] = phases
     if not args.layers and not args.no_e32:
-        gm32 = gm.sibling(**e32_pool(cfg, E32_STEPS, 3))
-        try:
-            line["e32"] = e32_run(gm32, cfg, E32_STEPS, 3, s, local_rank, world)
-        finally:
-            gm32.close()
+        for key, fmt in (("e32", ql.QL_KV_F16), ("e32_kvq", ql.QL_KV_Q8_0_Q5_1)):
+            gm32 = gm.sibling(**e32_pool(cfg, E32_STEPS, 3), kv_format=fmt)
+            try:
+                line[key] = e32_run(gm32, cfg, E32_STEPS, 3, s, local_rank, world)
+            finally:
+                gm32.close()
+                del gm32
     gm.close()
     return line
 
@@ -501,7 +541,7 @@ def e32_run(gm, cfg, steps, warmup, s, local_rank, world):
     clock = ClockSampler(local_rank)
     time.sleep(0.3)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-    kv_tok = cfg.n_layers * 2 * cfg.n_kv_heads * cfg.head_dim * 2
+    kv_tok = kv_bytes_per_token(gm, cfg)
     live_len = positions.cpu().numpy().astype(np.int64) + 1
     step_bytes = []
     repl_s = 0.0
@@ -539,7 +579,9 @@ def e32_run(gm, cfg, steps, warmup, s, local_rank, world):
         "value": round(value, 2), "unit": "tokens/s", "steps": steps, "warmup": warmup,
         "ms_per_step": round(ms / steps, 4),
         "workload": f"qwen3-8b-shaped q4_0 batched decode, 32 sequences, contexts uniform in [128, 8192], "
-                    f"{steps} greedy steps, finished sequences replaced by fresh {E32_FRESH}-position contexts",
+                    f"{steps} greedy steps, finished sequences replaced by fresh {E32_FRESH}-position contexts, "
+                    + ("f16 KV cache" if gm.kv_format == ql.QL_KV_F16 else "q8_0 K / q5_1 V cache"),
+        "kv_bytes_per_token": kv_tok,
         "step_roofline": {"bytes_per_step_avg": int(np.mean(step_bytes)), "achieved_gbs": round(gbs, 1),
                           "frac": round(gbs / peak, 4), "peak": peak, "peak_source": peak_src,
                           "roofline_tokens_s": round(B * peak * 1e9 / float(np.mean(step_bytes)), 1)},
@@ -562,7 +604,9 @@ def gpu_arm_e32(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     cfg = ql_inputs.QWEN3_8B
     t_setup = time.time()
-    gm = DeviceModel.from_layer_fn(cfg, device_tensor_fn(cfg, seed=0), **e32_pool(cfg, args.steps, args.warmup))
+    import quantized_transformer_decode_ql_gb300 as ql
+    gm = DeviceModel.from_layer_fn(cfg, device_tensor_fn(cfg, seed=0), **e32_pool(cfg, args.steps, args.warmup),
+                                   kv_format=ql.QL_KV_Q8_0_Q5_1 if args.kv == "q8q5" else ql.QL_KV_F16)
     setup_s = time.time() - t_setup
     s = torch.cuda.Stream()
     r = e32_run(gm, cfg, args.steps, args.warmup, s, local_rank, world)
@@ -972,7 +1016,8 @@ def main():
     ap.add_argument("--impl", default="ql", choices=["ql", "reference"])
     ap.add_argument("--config", default="e1", choices=["e1", "e32"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-e32", action="store_true", help="leave the batch-32 sub-result out of the default line")
+    ap.add_argument("--no-e32", action="store_true", help="leave the batch-32 sub-results out of the default line")
+    ap.add_argument("--kv", default="f16", choices=["f16", "q8q5"], help="--config e32: KV cache format")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling aid: run the 8B-shaped step with this many layers (default: all 36)")
     ap.add_argument("--step-kernel", default="auto", choices=["auto", "persistent", "launches"],
