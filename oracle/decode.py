@@ -21,10 +21,15 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import ops
+from . import moe, ops
 from .q4_0 import quantize, dequantize
 
 LAYER_MATRICES = ("wqkv", "wo", "wgu", "wd")
+MOE_MATRICES = ("wqkv", "wo", "w1", "w2")   # routed experts: w1 gate|up per expert, w2 down
+
+
+def layer_matrices(cfg):
+    return MOE_MATRICES if getattr(cfg, "num_experts", 0) else LAYER_MATRICES
 
 
 class Q4Model:
@@ -43,8 +48,10 @@ class Q4Model:
         for lw in w["layers"]:
             layer = {n: np.asarray(lw[n], dtype=np.float64)
                      for n in ("attn_norm", "ffn_norm", "q_norm", "k_norm")}
-            for n in LAYER_MATRICES:
+            for n in layer_matrices(cfg):
                 layer[n] = quantize(lw[n])
+            if getattr(cfg, "num_experts", 0):
+                layer["router"] = np.asarray(lw["router"], dtype=np.float64)
             self.layers.append(layer)
 
     @classmethod
@@ -61,8 +68,10 @@ class Q4Model:
         self.layers = []
         for lw in layers:
             layer = {n: np.asarray(lw[n], dtype=np.float64) for n in ("attn_norm", "ffn_norm", "q_norm", "k_norm")}
-            for n in LAYER_MATRICES:
+            for n in layer_matrices(cfg):
                 layer[n] = lw[n]
+            if getattr(cfg, "num_experts", 0):
+                layer["router"] = np.asarray(lw["router"], dtype=np.float64)
             self.layers.append(layer)
         return self
 
@@ -169,6 +178,10 @@ def decode_hidden(model: Q4Model, cache: KVCache, x, positions, act=None) -> np.
                                      cache.v[b, li, :, : p + 1], scale)
         x = x + ops.gemv(model.dense(L["wo"]), act(o.reshape(B, -1)))
         hn = ops.rmsnorm(x, L["ffn_norm"], cfg.eps)
+        if getattr(cfg, "num_experts", 0):
+            for b in range(B):
+                x[b] = x[b] + moe.moe_ffn(hn[b], L["router"], L["w1"], L["w2"], cfg)[0]
+            continue
         gu = ops.gemv(model.dense(L["wgu"]), act(hn))
         a = ops.swiglu(gu[:, : cfg.intermediate], gu[:, cfg.intermediate:])
         x = x + ops.gemv(model.dense(L["wd"]), act(a))
@@ -229,6 +242,10 @@ def forward_full(model: Q4Model, tokens, k_ctx=None, v_ctx=None) -> np.ndarray:
             o[:, h, :] = ops.softmax(s) @ V[g]
         x = x + o.reshape(T, -1) @ model.dense(L["wo"]).T
         hn = ops.rmsnorm(x, L["ffn_norm"], cfg.eps)
+        if getattr(cfg, "num_experts", 0):
+            # every position routes on its own normalised input
+            x = x + np.stack([moe.moe_ffn(hn[t], L["router"], L["w1"], L["w2"], cfg)[0] for t in range(T)])
+            continue
         gu = hn @ model.dense(L["wgu"]).T
         x = x + ops.swiglu(gu[:, : cfg.intermediate], gu[:, cfg.intermediate:]) \
             @ model.dense(L["wd"]).T

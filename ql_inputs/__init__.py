@@ -26,7 +26,8 @@ from dataclasses import dataclass, asdict
 import numpy as np
 
 __all__ = [
-    "Config", "TINY", "QWEN3_8B", "qwen3_8b_layers",
+    "Config", "TINY", "QWEN3_8B", "qwen3_8b_layers", "TINY_MOE", "QWEN3_30B_A3B", "qwen3_30b_a3b_layers",
+    "layer_tensor_names",
     "weights", "prompt_tokens", "kv_context", "fragmented_block_ids",
     "gemv_weight", "gemv_activations", "attention_case", "batched_lengths",
     "GEMV_SHAPES", "sub_rng", "device_tensor_fn",
@@ -45,6 +46,12 @@ class Config:
     vocab: int
     eps: float = 1e-6
     rope_theta: float = 1e6
+    # routed experts (inferencelayer cuda_llm.rs, Cfg: "MoE (Qwen3-30B-A3B): 0 => dense", no
+    # shared expert): num_experts 0 is a dense model
+    num_experts: int = 0
+    topk: int = 0
+    moe_inter: int = 0
+    norm_topk: bool = True
 
     @property
     def qkv_rows(self) -> int:
@@ -61,6 +68,23 @@ TINY = Config(hidden=256, n_layers=2, n_heads=4, n_kv_heads=2, head_dim=64,
 #: Qwen3-8B-shaped: hidden 4096, 36 layers, 32/8 heads, head_dim 128, SwiGLU 12288.
 QWEN3_8B = Config(hidden=4096, n_layers=36, n_heads=32, n_kv_heads=8, head_dim=128,
                   intermediate=12288, vocab=151936)
+
+
+#: tiny routed-expert model: the tiny dense shape with 8 experts of SwiGLU width 128, top-2.
+TINY_MOE = Config(hidden=256, n_layers=2, n_heads=4, n_kv_heads=2, head_dim=64, intermediate=0,
+                  vocab=1024, num_experts=8, topk=2, moe_inter=128)
+
+#: Qwen3-30B-A3B-shaped: hidden 2048, 48 layers, 32/4 heads, head_dim 128, 128 experts of SwiGLU
+#: width 768, top-8 with the selected weights renormalised, vocab 151936.
+QWEN3_30B_A3B = Config(hidden=2048, n_layers=48, n_heads=32, n_kv_heads=4, head_dim=128, intermediate=0,
+                       vocab=151936, num_experts=128, topk=8, moe_inter=768)
+
+
+def qwen3_30b_a3b_layers(n_layers: int) -> Config:
+    """The A3B shape with fewer layers (full width, experts and vocab) for oracle-sized parity."""
+    d = QWEN3_30B_A3B.as_dict()
+    d["n_layers"] = n_layers
+    return Config(**d)
 
 
 def qwen3_8b_layers(n_layers: int) -> Config:
@@ -90,6 +114,14 @@ def _normal(rng: np.random.Generator, shape, std: float, mean: float = 0.0) -> n
 
 
 _LAYER_TENSORS = ("attn_norm", "ffn_norm", "q_norm", "k_norm", "wqkv", "wo", "wgu", "wd")
+#: routed-expert layers: the router (f32 [E, hidden], not quantised), the experts' gate|up rows
+#: (expert e owns rows [e 2mi, e 2mi + mi) gate and the next mi up) and their down rows (expert e
+#: owns rows [e hidden, (e + 1) hidden))
+_MOE_TENSORS = ("attn_norm", "ffn_norm", "q_norm", "k_norm", "wqkv", "wo", "router", "w1", "w2")
+
+
+def layer_tensor_names(cfg: Config):
+    return _MOE_TENSORS if cfg.num_experts else _LAYER_TENSORS
 
 
 def _layer_shape(cfg: Config, name: str):
@@ -102,12 +134,15 @@ def _layer_shape(cfg: Config, name: str):
         "wo": (cfg.hidden, cfg.n_heads * cfg.head_dim),
         "wgu": (2 * cfg.intermediate, cfg.hidden),
         "wd": (cfg.hidden, cfg.intermediate),
+        "router": (cfg.num_experts, cfg.hidden),
+        "w1": (cfg.num_experts * 2 * cfg.moe_inter, cfg.hidden),
+        "w2": (cfg.num_experts * cfg.hidden, cfg.moe_inter),
     }[name]
 
 
 def layer_tensor(cfg: Config, seed: int, layer: int, name: str) -> np.ndarray:
     """One layer tensor, f32, drawn from its own stream (so any one can be regenerated)."""
-    k = _LAYER_TENSORS.index(name)
+    k = _LAYER_TENSORS.index(name) if name in _LAYER_TENSORS else 10 + _MOE_TENSORS.index(name)
     rng = sub_rng(seed, 1, layer, k)
     shape = _layer_shape(cfg, name)
     if name.endswith("norm"):
@@ -124,7 +159,7 @@ def weights(cfg: Config, seed: int = 0) -> dict:
         "layers": [],
     }
     for li in range(cfg.n_layers):
-        w["layers"].append({n: layer_tensor(cfg, seed, li, n) for n in _LAYER_TENSORS})
+        w["layers"].append({n: layer_tensor(cfg, seed, li, n) for n in layer_tensor_names(cfg)})
     return w
 
 
@@ -135,12 +170,10 @@ def device_tensor_fn(cfg: Config, seed: int):
     too large to draw on the host; the values differ from :func:`weights`."""
     import torch
 
-    names = ("attn_norm", "ffn_norm", "q_norm", "k_norm", "wqkv", "wo", "wgu", "wd")
-    shapes = {"attn_norm": (cfg.hidden,), "ffn_norm": (cfg.hidden,), "q_norm": (cfg.head_dim,),
-              "k_norm": (cfg.head_dim,), "wqkv": (cfg.qkv_rows, cfg.hidden),
-              "wo": (cfg.hidden, cfg.n_heads * cfg.head_dim), "wgu": (2 * cfg.intermediate, cfg.hidden),
-              "wd": (cfg.hidden, cfg.intermediate), "embed": (cfg.vocab, cfg.hidden),
-              "final_norm": (cfg.hidden,), "lm_head": (cfg.vocab, cfg.hidden)}
+    names = ("attn_norm", "ffn_norm", "q_norm", "k_norm", "wqkv", "wo", "wgu", "wd", "router", "w1", "w2")
+    shapes = {n: _layer_shape(cfg, n) for n in names}
+    shapes.update({"embed": (cfg.vocab, cfg.hidden), "final_norm": (cfg.hidden,),
+                   "lm_head": (cfg.vocab, cfg.hidden)})
 
     def fn(layer, name):
         key = (seed * 1000003 + (0 if layer is None else layer + 1) * 101
