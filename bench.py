@@ -154,9 +154,9 @@ device_tensor_fn = ql_inputs.device_tensor_fn
 # stream GEMV at the gate|up shape (24576 x 4096, plain epilogue), from one ncu capture. It is
 # reported only while the kernel's source files hash to the value recorded with it: any change
 # to the kernel makes it null until the counters are taken again.
-GU_TRAFFIC_BYTES = 57250048
+GU_TRAFFIC_BYTES = 57234432
 GU_TRAFFIC_SOURCES = ("ql_persist.cuh", "ql_persist.cu", "ql_internal.h")
-GU_TRAFFIC_SHA16 = "459407f49b84da0e"
+GU_TRAFFIC_SHA16 = "5cc0603626bc865c"
 
 
 def kernel_source_sha16(files) -> str:
@@ -473,6 +473,8 @@ def gpu_arm(args, rank, world, local_rank):
     }
     if phases:
         line["step_phases_us"] = phases
+    if not args.layers and not args.no_moe:
+        line["moe_a3b_b1"] = moe_run(min(steps, 64), 3, s, local_rank, world)
     if not args.layers and not args.no_e32:
         for key, fmt in (("e32", ql.QL_KV_F16), ("e32_kvq", ql.QL_KV_Q8_0_Q5_1)):
             gm32 = gm.sibling(**e32_pool(cfg, E32_STEPS, 3), kv_format=fmt)
@@ -483,6 +485,69 @@ def gpu_arm(args, rank, world, local_rank):
                 del gm32
     gm.close()
     return line
+
+
+def moe_run(steps, warmup, s, local_rank, world):
+    """The Qwen3-30B-A3B-shaped routed-expert model (48 layers, 128 experts of 768, top-8,
+    random-init, q4_0 on the device) at batch 1 over a 2048-token pre-filled context: `steps`
+    greedy steps timed as graph replays. Step bytes: the attention matrices, the f32 router and
+    the top-8 experts' rows of every layer, the lm_head, the KV read and written, the embedding
+    row and the logits."""
+    import torch
+    from quantized_transformer_decode_ql_gb300.model import DeviceModel
+    cfg = ql_inputs.QWEN3_30B_A3B
+    max_ctx = CTX + warmup + steps + 2
+    maxb = (max_ctx + 15) // 16
+    t0 = time.time()
+    gm = DeviceModel.from_layer_fn(cfg, device_tensor_fn(cfg, seed=0), num_blocks=maxb + 8, max_batch=1,
+                                   max_blocks_per_seq=maxb)
+    try:
+        bt = torch.from_numpy(ql_inputs.fragmented_block_ids(maxb + 8, seed=5)[:maxb]).cuda().reshape(1, maxb)
+        g = torch.Generator(device="cuda")
+        g.manual_seed(4)
+        prefill_context(gm, cfg, bt[0].tolist(), CTX, g)
+        first = torch.from_numpy(ql_inputs.prompt_tokens(1, cfg.vocab, seed=1)).cuda()
+        tokens = first.clone()
+        positions = torch.full((1,), CTX, dtype=torch.int32, device="cuda")
+        sargs = gm.step_args(tokens, positions, bt, tokens)
+        torch.cuda.synchronize()
+        gm.ql_decode_graph_capture(sargs, s)
+        setup_s = time.time() - t0
+        with torch.cuda.stream(s):
+            gm.ql_decode_graph_replay(1, warmup, s)
+            tokens.copy_(first)
+            positions.fill_(CTX)
+        s.synchronize()
+        gm.ql_check_device_error()
+        clock = ClockSampler(local_rank)
+        time.sleep(0.3)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record(s)
+            gm.ql_decode_graph_replay(1, steps, s)
+            e1.record(s)
+        s.synchronize()
+        clocks = clock.stop()
+        gm.ql_check_device_error()
+        ms = max_over_ranks(e0.elapsed_time(e1), world)
+        phases = launch_phases(gm, sargs, s, cfg)
+        peak, peak_src = load_peaks()
+        kv_tok = kv_bytes_per_token(gm, cfg)
+        ctx_avg = CTX + 1 + (steps - 1) / 2.0
+        step_bytes = gm.step_weight_bytes() + kv_tok * ctx_avg + kv_tok + cfg.hidden * 4 + cfg.vocab * 4
+        gbs = step_bytes * steps / (ms / 1e3) / 1e9
+        return {"value": round(sum_over_ranks(float(steps), world) / (ms / 1e3), 2), "unit": "tokens/s",
+                "steps": steps, "warmup": warmup, "ms_per_step": round(ms / steps, 4),
+                "workload": f"qwen3-30b-a3b-shaped routed-expert q4_0 decode (48 layers, 128 experts of 768, "
+                            f"top-8), batch 1, {CTX}-token context, {steps} greedy steps",
+                "weights_gb": round(gm.weight_bytes() / 1e9, 2),
+                "step_roofline": {"bytes_per_step": int(step_bytes), "achieved_gbs": round(gbs, 1),
+                                  "frac": round(gbs / peak, 4), "peak": peak, "peak_source": peak_src,
+                                  "roofline_tokens_s": round(peak * 1e9 / step_bytes, 1)},
+                "clocks": clocks, "gpu_launches": (3 + 7 * cfg.n_layers) * steps, "setup_s": round(setup_s, 1),
+                **({"step_phases_us": phases} if phases else {})}
+    finally:
+        gm.close()
 
 
 E32_STEPS = 128
@@ -1018,6 +1083,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e32", action="store_true", help="leave the batch-32 sub-results out of the default line")
     ap.add_argument("--kv", default="f16", choices=["f16", "q8q5"], help="--config e32: KV cache format")
+    ap.add_argument("--no-moe", action="store_true", help="leave the routed-expert sub-result out of the default line")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling aid: run the 8B-shaped step with this many layers (default: all 36)")
     ap.add_argument("--step-kernel", default="auto", choices=["auto", "persistent", "launches"],

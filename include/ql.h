@@ -340,8 +340,14 @@ typedef struct {
     const float* k_norm;    /* [head_dim] */
     ql_q4_0_matrix qkv;     /* [(n_heads + 2 n_kv) * head_dim, hidden], rows q | k | v */
     ql_q4_0_matrix o;       /* [hidden, n_heads * head_dim] */
-    ql_q4_0_matrix gate_up; /* [2 * intermediate, hidden], rows gate | up */
-    ql_q4_0_matrix down;    /* [hidden, intermediate] */
+    ql_q4_0_matrix gate_up; /* [2 * intermediate, hidden], rows gate | up (dense models) */
+    ql_q4_0_matrix down;    /* [hidden, intermediate] (dense models) */
+    /* routed experts (num_experts > 0; [IL] Cfg and the MoE weights as loaded): */
+    const float* router;             /* f32 [num_experts][hidden] */
+    ql_q4_0_matrix experts_gate_up;  /* [num_experts * 2 * moe_inter, hidden]: expert e owns rows
+                                        [e 2mi, e 2mi + mi) (gate) and the next mi (up)     */
+    ql_q4_0_matrix experts_down;     /* [num_experts * hidden, moe_inter]: expert e owns rows
+                                        [e hidden, (e + 1) hidden)                         */
 } ql_layer_desc;
 
 typedef struct {
@@ -360,6 +366,15 @@ typedef struct {
     int64_t max_blocks_per_seq; /* block-table row length; max context = this * block_size */
     int kv_format;              /* QL_KV_F16 (k_pool / v_pool) or QL_KV_Q8_0_Q5_1 (kvq_pool) */
     void* kvq_pool;             /* QL_KV_Q8_0_Q5_1: u8 [n_layers][num_blocks][n_kv][ql_kvq_record_bytes] */
+    /* Routed experts ([IL] Cfg: num_experts, topk, moe_inter, norm_topk; 0 experts = dense).
+     * Every layer's feed-forward block is then: router logits = router . rms(x) w_ffn (f32),
+     * the softmax over all experts, the topk largest (lowest index first on ties), their weights
+     * renormalised to sum 1 when norm_topk; per selected expert silu(gate) * up and its down
+     * rows; x += the weighted sum in slot order. Decode steps at batch 1 only (QL_EINVAL for a
+     * larger batch); intermediate, gate_up and down are then unused. moe_inter and hidden must
+     * be multiples of 128, num_experts <= 512, topk <= 64.                                    */
+    int64_t num_experts, topk, moe_inter;
+    int norm_topk;
 } ql_model_desc;
 
 /* KV cache formats of a model (ql_model_desc.kv_format). QL_KV_Q8_0_Q5_1: the quantised pool of

@@ -37,7 +37,8 @@ class Q4Matrix(ctypes.Structure):
 class LayerDesc(ctypes.Structure):
     _fields_ = [("attn_norm", c_void_p), ("ffn_norm", c_void_p), ("q_norm", c_void_p),
                 ("k_norm", c_void_p), ("qkv", Q4Matrix), ("o", Q4Matrix), ("gate_up", Q4Matrix),
-                ("down", Q4Matrix)]
+                ("down", Q4Matrix), ("router", c_void_p), ("experts_gate_up", Q4Matrix),
+                ("experts_down", Q4Matrix)]
 
 
 class ModelDesc(ctypes.Structure):
@@ -47,7 +48,8 @@ class ModelDesc(ctypes.Structure):
                 ("embed", c_void_p), ("final_norm", c_void_p), ("lm_head", Q4Matrix),
                 ("layers", POINTER(LayerDesc)), ("k_pool", c_void_p), ("v_pool", c_void_p),
                 ("num_blocks", c_int64), ("block_size", c_int), ("max_batch", c_int64),
-                ("max_blocks_per_seq", c_int64), ("kv_format", c_int), ("kvq_pool", c_void_p)]
+                ("max_blocks_per_seq", c_int64), ("kv_format", c_int), ("kvq_pool", c_void_p),
+                ("num_experts", c_int64), ("topk", c_int64), ("moe_inter", c_int64), ("norm_topk", c_int)]
 
 
 class StepArgs(ctypes.Structure):

@@ -47,6 +47,7 @@ enum DevErrWhere {
     kErrStepBarrier = 9,
     kErrKvNonFinite = 10,
     kErrKvOverflow = 11,
+    kErrMoeExpert = 12,
 };
 // The current device's record (allocated on first use, zero-filled).
 DevError* device_error_record();
@@ -227,6 +228,12 @@ struct PMat {
     int rows, nblk;     // nblk = cols / 32, a multiple of 4
     int silu;           // rows = [gate | up]; a tile is 8 gate rows + the matching 8 up rows
     int ntile;          // 16-row tiles
+    // Routed experts (stream GEMV only): a virtual matrix of nsel selected experts. Tile t of it
+    // is tile t % etiles of expert sel[t / etiles] of the stream (experts are consecutive runs
+    // of etiles tiles, nexp of them); rows and ntile count the virtual matrix. xsel: the
+    // activation column of tile t is t / etiles (nsel columns staged), else the batch column.
+    const int32_t* sel;
+    int etiles, nexp, nsel, xsel;
 };
 // Bytes of a matrix in the tile stream layout: ntile * (nblk / 4) units of 1152 B.
 size_t persist_stream_bytes(const PMat& m);
@@ -308,6 +315,21 @@ struct StreamGemvArgs {
     NextWeights next;     // batch 1-2: constants of a later kernel, prefetched into L2
     int grid;             // batch 1-2: CTAs (0: one per SM); fewer leave SMs to the kernel before
 };
+// Routed experts at batch 1 (ql_moe.cu): the router + top-k kernel and the combine kernel.
+struct MoeRouterArgs {
+    const float* x;        // [hidden] f32 residual stream (normalised inside with norm_w)
+    const float* norm_w;   // [hidden]
+    const float* router;   // [num_experts][hidden] f32
+    int hidden, num_experts, topk, norm_topk;
+    float eps;
+    float* logits;         // [num_experts] scratch
+    int* ticket;           // zero between launches (re-armed by the kernel)
+    int32_t* eidx;         // [topk] selected experts, by falling probability
+    float* ewt;            // [topk] their weights
+};
+int moe_router_launch(const MoeRouterArgs& a, cudaStream_t s, bool pdl);
+int moe_combine_launch(float* x, const float* y, const float* ewt, int hidden, int k, cudaStream_t s, bool pdl);
+
 int persist_trace_words();   // trace entries per CTA and row
 int stream_gemv_prepare();
 int stream_gemv_launch(const StreamGemvArgs& a, cudaStream_t s, bool pdl);

@@ -72,6 +72,14 @@ struct ql_model {
     float* ppacc = nullptr;
     int* ptickets = nullptr;
     unsigned int* psync = nullptr;
+    // routed experts (num_experts > 0): the router's logits and ticket, the selection, the
+    // selected experts' SiLU*up activations and down outputs
+    float* mlog = nullptr;       // [num_experts]
+    int* mticket = nullptr;
+    int32_t* meidx = nullptr;    // [topk]
+    float* mewt = nullptr;       // [topk]
+    __half* mact = nullptr;      // [topk][moe_inter]
+    float* medn = nullptr;       // [topk][hidden]
 };
 
 namespace ql {
@@ -202,8 +210,12 @@ int run_step(ql_model* m, const ql_step_args* a, cudaStream_t s) {
     if (m->step_kernel == QL_STEP_PERSISTENT && B > m->persist_max_b)
         return set_error(QL_EINVAL, "decode step: the persistent step kernel takes batches up to " +
                                         std::to_string(m->persist_max_b) + " on this model");
-    if (m->step_kernel == QL_STEP_PERSISTENT && m->d.kv_format != QL_KV_F16)
-        return set_error(QL_EINVAL, "decode step: the persistent step kernel takes only the f16 KV format");
+    if (m->step_kernel == QL_STEP_PERSISTENT && (m->d.kv_format != QL_KV_F16 || m->d.num_experts > 0))
+        return set_error(QL_EINVAL, "decode step: the persistent step kernel takes only dense models with f16 KV");
+    if (m->d.num_experts > 0 && B != 1)
+        return set_error(QL_EINVAL, "decode step: routed experts decode at batch 1");
+    if (m->d.num_experts > 0 && m->hmats.empty())
+        return set_error(QL_EINVAL, "decode step: routed experts need the tile stream copies (matrix widths multiples of 128)");
     if (m->step_kernel == QL_STEP_PERSISTENT) return run_persist(m, a, s);
     const bool pdl = true;
     const int hd = (int)d.head_dim, nh = (int)d.n_heads, nkv = (int)d.n_kv_heads;
@@ -313,6 +325,34 @@ int run_step(ql_model* m, const ql_step_args* a, cudaStream_t s) {
             if ((rc = sg(Ms[1], QL_EPI_ADD_RESIDUAL, false, nullptr, m->attn, nullptr, m->x, (int)d.hidden,
                          ffn_norm, o_grid)) != QL_OK)
                 return rc;
+            if (d.num_experts > 0) {
+                // routed experts: router + top-k, gate|up of the selected experts (RMSNorm'd x,
+                // SiLU*up), their down rows against each one's own activations, the combine
+                const int64_t K = d.topk, mi = d.moe_inter;
+                MoeRouterArgs ra = {};
+                ra.x = m->x;
+                ra.norm_w = L.ffn_norm;
+                ra.router = L.router;
+                ra.hidden = (int)d.hidden;
+                ra.num_experts = (int)d.num_experts;
+                ra.topk = (int)K;
+                ra.norm_topk = d.norm_topk;
+                ra.eps = d.eps;
+                ra.logits = m->mlog;
+                ra.ticket = m->mticket;
+                ra.eidx = m->meidx;
+                ra.ewt = m->mewt;
+                if ((rc = moe_router_launch(ra, s, pdl)) != QL_OK) return rc;
+                if ((rc = sg(Ms[2], QL_EPI_SILU_MUL, true, m->x, nullptr, L.ffn_norm, m->mact, (int)(K * mi),
+                             none)) != QL_OK)
+                    return rc;
+                if ((rc = sg(Ms[3], QL_EPI_NONE, false, nullptr, m->mact, nullptr, m->medn, (int)(K * d.hidden),
+                             none)) != QL_OK)
+                    return rc;
+                if ((rc = moe_combine_launch(m->x, m->medn, m->mewt, (int)d.hidden, (int)K, s, pdl)) != QL_OK)
+                    return rc;
+                continue;
+            }
             if ((rc = sg(Ms[2], QL_EPI_SILU_MUL, true, m->x, nullptr, L.ffn_norm, m->act, (int)d.intermediate,
                          none)) != QL_OK)
                 return rc;
@@ -469,12 +509,14 @@ int setup_persist(ql_model* m) {
     auto mat_ok = [&](const ql_q4_0_matrix& w) {
         return w.cols % 128 == 0 && w.rows < (1ll << 30) && al(w.quants, 16) && al(w.scales, 8);
     };
+    const bool moe = d.num_experts > 0;
     bool ok = d.vocab < (1ll << 30) && al(d.embed, 16) && al(d.final_norm, 16) && mat_ok(d.lm_head);
     for (const ql_layer_desc& L : m->layers)
-        ok = ok && mat_ok(L.qkv) && mat_ok(L.o) && mat_ok(L.gate_up) && mat_ok(L.down) && al(L.attn_norm, 16) &&
-             al(L.ffn_norm, 16);
+        ok = ok && mat_ok(L.qkv) && mat_ok(L.o) && al(L.attn_norm, 16) && al(L.ffn_norm, 16) &&
+             (moe ? (mat_ok(L.experts_gate_up) && mat_ok(L.experts_down) && al(L.router, 16))
+                  : (mat_ok(L.gate_up) && mat_ok(L.down)));
     if (!ok) return QL_OK;
-    const int64_t widths[3] = {d.hidden, d.intermediate, d.n_heads * d.head_dim};
+    const int64_t widths[3] = {d.hidden, moe ? d.moe_inter : d.intermediate, d.n_heads * d.head_dim};
     int64_t w = 0;
     for (int64_t v : widths) w = v > w ? v : w;
     m->max_nblk = (int)(w / 32);
@@ -484,26 +526,70 @@ int setup_persist(ql_model* m) {
         if (persist_prepare(maxb, m->max_nblk, (int)d.head_dim, G, (int)d.n_layers) == QL_OK) break;
     if (maxb < 1) return QL_OK;
     if (int rc0 = stream_gemv_prepare()) return rc0;
-    m->batched_ok = d.max_batch > kPersistMaxBatch && batched_gemv_shape_ok((int)(d.hidden / 32)) &&
+    m->batched_ok = !moe && d.max_batch > kPersistMaxBatch && batched_gemv_shape_ok((int)(d.hidden / 32)) &&
                     batched_gemv_shape_ok((int)(d.intermediate / 32)) &&
                     batched_gemv_shape_ok((int)(d.n_heads * d.head_dim / 32)) && batched_gemv_prepare() == QL_OK;
 
     std::vector<PLayer> hl(m->layers.size());
-    std::vector<PMat> all;
+    std::vector<PMat> all;     // the step's matrices: 4 per layer, then lm_head
+    std::vector<PMat> packs;   // what is re-laid, in stream order (routed experts: one per expert)
+    std::vector<size_t> where; // index into packs of each entry of all
+    auto add = [&](const PMat& pm) {
+        where.push_back(packs.size());
+        packs.push_back(pm);
+        all.push_back(pm);
+    };
+    const int64_t mi = d.moe_inter, E = d.num_experts, K = d.topk;
     for (size_t i = 0; i < hl.size(); ++i) {
         const ql_layer_desc& L = m->layers[i];
-        all.push_back(pmat(L.qkv, false));
-        all.push_back(pmat(L.o, false));
-        all.push_back(pmat(L.gate_up, true));
-        all.push_back(pmat(L.down, false));
+        add(pmat(L.qkv, false));
+        add(pmat(L.o, false));
+        if (moe) {
+            // gate|up: each expert's 2 mi rows re-laid as its own SiLU*up matrix (8 gate rows and
+            // the matching 8 up rows per tile), the experts back to back; the step reads a virtual
+            // matrix of the topk selected experts (PMat::sel)
+            const int nb1 = (int)(d.hidden / 32);
+            where.push_back(packs.size());
+            for (int64_t e = 0; e < E; ++e) {
+                ql_q4_0_matrix sub = L.experts_gate_up;
+                sub.rows = 2 * mi;
+                sub.quants = static_cast<const uint8_t*>(L.experts_gate_up.quants) + (size_t)e * 2 * mi * nb1 * 16;
+                sub.scales = static_cast<const __half*>(L.experts_gate_up.scales) + (size_t)e * 2 * mi * nb1;
+                packs.push_back(pmat(sub, true));
+            }
+            PMat v1 = pmat(L.experts_gate_up, true);
+            v1.rows = (int)(K * 2 * mi);
+            v1.ntile = (int)(K * (mi / 8));
+            v1.sel = m->meidx;
+            v1.etiles = (int)(mi / 8);
+            v1.nexp = (int)E;
+            v1.nsel = (int)K;
+            all.push_back(v1);
+            // down: the experts' rows in order are already one matrix; the step reads the topk
+            // selected experts' tiles, each against its own activation column
+            where.push_back(packs.size());
+            packs.push_back(pmat(L.experts_down, false));
+            PMat v2 = pmat(L.experts_down, false);
+            v2.rows = (int)(K * d.hidden);
+            v2.ntile = (int)(K * (d.hidden / 16));
+            v2.sel = m->meidx;
+            v2.etiles = (int)(d.hidden / 16);
+            v2.nexp = (int)E;
+            v2.nsel = (int)K;
+            v2.xsel = 1;
+            all.push_back(v2);
+        } else {
+            add(pmat(L.gate_up, true));
+            add(pmat(L.down, false));
+        }
         hl[i].attn_norm = L.attn_norm;
         hl[i].ffn_norm = L.ffn_norm;
         hl[i].q_norm = L.q_norm;
         hl[i].k_norm = L.k_norm;
     }
-    all.push_back(pmat(d.lm_head, false));
+    add(pmat(d.lm_head, false));
     size_t stream_bytes = 0;
-    for (const PMat& pm : all) stream_bytes += persist_stream_bytes(pm);
+    for (const PMat& pm : packs) stream_bytes += persist_stream_bytes(pm);
     int nsplit = num_sms();
     nsplit = nsplit > 256 ? 256 : nsplit;
     nsplit = nsplit > d.max_blocks_per_seq ? (int)d.max_blocks_per_seq : nsplit;
@@ -522,7 +608,8 @@ int setup_persist(ql_model* m) {
     A((void**)&m->xn, (size_t)d.max_batch * d.hidden * 2);
     if (rc != QL_OK) return rc;
     // the weights re-laid into the tile stream layout that the persistent kernel copies from
-    if ((rc = persist_pack_streams(all.data(), (int)all.size(), m->pstreams, nullptr)) != QL_OK) return rc;
+    if ((rc = persist_pack_streams(packs.data(), (int)packs.size(), m->pstreams, nullptr)) != QL_OK) return rc;
+    for (size_t i = 0; i < all.size(); ++i) all[i].stream = packs[where[i]].stream;
     for (size_t i = 0; i < hl.size(); ++i)
         for (int k = 0; k < 4; ++k) hl[i].m[k] = all[4 * i + k];
     m->plm = all.back();
@@ -575,7 +662,8 @@ extern "C" int ql_model_create(const ql_model_desc* desc, ql_model** out) {
     QL_REQUIRE(d.n_kv_heads > 0 && d.n_heads % d.n_kv_heads == 0, "ql_model_create: bad head counts");
     const int64_t G = d.n_heads / d.n_kv_heads;
     QL_REQUIRE(G == 1 || G == 2 || G == 4 || G == 8, "ql_model_create: GQA group must be 1, 2, 4 or 8");
-    QL_REQUIRE(d.intermediate > 0 && d.intermediate % 32 == 0, "ql_model_create: intermediate must be a multiple of 32");
+    QL_REQUIRE(d.num_experts > 0 || (d.intermediate > 0 && d.intermediate % 32 == 0),
+               "ql_model_create: intermediate must be a multiple of 32");
     QL_REQUIRE((d.n_heads * d.head_dim) % 32 == 0, "ql_model_create: n_heads*head_dim must be a multiple of 32");
     QL_REQUIRE(d.vocab > 0 && d.embed && d.final_norm, "ql_model_create: need vocab, embed, final_norm");
     QL_REQUIRE(d.block_size == 16, "ql_model_create: block_size must be 16");
@@ -589,12 +677,27 @@ extern "C" int ql_model_create(const ql_model_desc* desc, ql_model** out) {
     QL_REQUIRE(d.eps > 0.f && d.rope_theta > 0.0, "ql_model_create: eps and rope_theta must be positive");
     QL_REQUIRE(check_matrix(d.lm_head, d.vocab, d.hidden), "ql_model_create: lm_head must be [vocab, hidden]");
     const int64_t qkv_rows = (d.n_heads + 2 * d.n_kv_heads) * d.head_dim;
+    const bool moe = d.num_experts > 0;
+    if (moe) {
+        QL_REQUIRE(d.num_experts <= 512 && d.topk >= 1 && d.topk <= d.num_experts && d.topk <= 64,
+                   "ql_model_create: routed experts need 1 <= topk <= num_experts <= 512, topk <= 64");
+        QL_REQUIRE(d.moe_inter > 0 && d.moe_inter % 128 == 0 && d.hidden % 128 == 0,
+                   "ql_model_create: routed experts need moe_inter and hidden multiples of 128");
+    }
     for (int64_t i = 0; i < d.n_layers; ++i) {
         const ql_layer_desc& L = d.layers[i];
         const std::string li = " (layer " + std::to_string(i) + ")";
         QL_REQUIRE(L.attn_norm && L.ffn_norm && L.q_norm && L.k_norm, "ql_model_create: missing norm weights" + li);
         QL_REQUIRE(check_matrix(L.qkv, qkv_rows, d.hidden), "ql_model_create: qkv must be [(nh+2nkv)*hd, hidden]" + li);
         QL_REQUIRE(check_matrix(L.o, d.hidden, d.n_heads * d.head_dim), "ql_model_create: o must be [hidden, nh*hd]" + li);
+        if (moe) {
+            QL_REQUIRE(L.router, "ql_model_create: routed experts need the router weights" + li);
+            QL_REQUIRE(check_matrix(L.experts_gate_up, d.num_experts * 2 * d.moe_inter, d.hidden),
+                       "ql_model_create: experts_gate_up must be [num_experts*2*moe_inter, hidden]" + li);
+            QL_REQUIRE(check_matrix(L.experts_down, d.num_experts * d.hidden, d.moe_inter),
+                       "ql_model_create: experts_down must be [num_experts*hidden, moe_inter]" + li);
+            continue;
+        }
         QL_REQUIRE(check_matrix(L.gate_up, 2 * d.intermediate, d.hidden), "ql_model_create: gate_up must be [2*inter, hidden]" + li);
         QL_REQUIRE(check_matrix(L.down, d.hidden, d.intermediate), "ql_model_create: down must be [hidden, inter]" + li);
     }
@@ -617,7 +720,17 @@ extern "C" int ql_model_create(const ql_model_desc* desc, ql_model** out) {
     A((void**)&m->qkv, B * qkv_rows * 4);
     A((void**)&m->q16, B * d.n_heads * d.head_dim * 2);
     A((void**)&m->attn, B * d.n_heads * d.head_dim * 2);
-    A((void**)&m->act, B * d.intermediate * 2);
+    A((void**)&m->act, B * (d.intermediate > 0 ? d.intermediate : 1) * 2);
+    if (d.num_experts > 0) {
+        A((void**)&m->mlog, d.num_experts * 4);
+        A((void**)&m->mticket, 16);
+        A((void**)&m->meidx, d.topk * 4);
+        A((void**)&m->mewt, d.topk * 4);
+        A((void**)&m->mact, d.topk * d.moe_inter * 2);
+        A((void**)&m->medn, d.topk * d.hidden * 4);
+        if (rc == QL_OK && cudaMemset(m->mticket, 0, 16) != cudaSuccess) rc = set_error(QL_ECUDA, "ql_model_create: memset");
+        if (rc == QL_OK && cudaMemset(m->meidx, 0, d.topk * 4) != cudaSuccess) rc = set_error(QL_ECUDA, "ql_model_create: memset");
+    }
     A((void**)&m->logits, B * d.vocab * 4);
     A((void**)&m->keys, B * 8);
     A((void**)&m->cos_t, max_pos * (d.head_dim / 2) * 4);
@@ -665,7 +778,7 @@ extern "C" int ql_model_set_option(ql_model* m, int option, int64_t value) {
         case QL_OPT_STEP_KERNEL:
             if (value != QL_STEP_AUTO && value != QL_STEP_LAUNCHES && value != QL_STEP_PERSISTENT)
                 return set_error(QL_EINVAL, "ql_model_set_option: unknown step kernel");
-            if (value == QL_STEP_PERSISTENT && (m->persist_max_b < 1 || m->d.kv_format != QL_KV_F16))
+            if (value == QL_STEP_PERSISTENT && (m->persist_max_b < 1 || m->d.kv_format != QL_KV_F16 || m->d.num_experts > 0))
                 return set_error(QL_EINVAL, "ql_model_set_option: the persistent step kernel is not available for this model");
             m->step_kernel = (int)value;
             return QL_OK;

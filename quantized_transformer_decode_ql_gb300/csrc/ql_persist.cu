@@ -102,6 +102,7 @@ int stream_gemv_prepare() {
     if (e == cudaSuccess) e = persist::stream_gemv_one<2, 16>(false, nullptr, nullptr, 0, 0, nullptr, false);
     if (e == cudaSuccess) e = persist::stream_gemv_one<1, 16, true>(false, nullptr, nullptr, 0, 0, nullptr, false);
     if (e == cudaSuccess) e = persist::stream_gemv_one<2, 16, true>(false, nullptr, nullptr, 0, 0, nullptr, false);
+    if (e == cudaSuccess) e = persist::stream_gemv_one<1, 16, false, true>(false, nullptr, nullptr, 0, 0, nullptr, false);
     if (e != cudaSuccess) return cuda_error(e, "stream gemv: kernel attributes");
     done.insert(dev);
     return QL_OK;
@@ -112,6 +113,8 @@ int persist_trace_words() { return persist::kTraceWords; }
 int stream_gemv_launch(const StreamGemvArgs& a, cudaStream_t s, bool pdl) {
     QL_REQUIRE(a.M.stream && a.M.nblk > 0 && a.M.nblk % persist::kUnitBlocks == 0, "stream gemv: bad matrix");
     QL_REQUIRE(a.batch == 1 || a.batch == 2, "stream gemv: batch must be 1 or 2");
+    QL_REQUIRE(!a.M.sel || (a.batch == 1 && a.M.etiles > 0 && a.M.nsel > 0 && a.M.nsel <= 64 && a.M.nexp > 0),
+               "stream gemv: routed experts need batch 1 and a valid selection");
     QL_REQUIRE(a.rms ? (a.xf && a.norm_w) : a.x16 != nullptr, "stream gemv: null input");
     QL_REQUIRE(a.y && a.sync, "stream gemv: null output");
     QL_REQUIRE(a.epilogue != kEpiArgmax || a.keys, "stream gemv: argmax needs keys");
@@ -147,17 +150,22 @@ int stream_gemv_launch(const StreamGemvArgs& a, cudaStream_t s, bool pdl) {
         const int v = e ? std::atoi(e) : 1;
         return v < 0 ? 0 : (v > persist::kStages ? persist::kStages : v);
     }();
-    g.prewait = prewait;
+    // routed experts: which tiles to copy is known only once the predecessor (the router) is
+    // done, so nothing is issued before the wait
+    g.prewait = a.M.sel ? 0 : prewait;
     // one CTA of 16 warps per SM (measured faster in the step than two CTAs of 8 warps, which
     // would let a kernel's set-up overlap the previous kernel's tail); QL_STREAM_GEMV_WARPS=8
     // selects the two-CTA form for A/B measurements
     const int warps = stream_gemv_warps();
+    const int staged = a.M.xsel ? a.M.nsel : a.batch;   // activation columns staged
     const size_t smem = (size_t)warps * persist::kStages * persist::kSlotBytes +
-                        persist::gemv_region_bytes(a.batch, a.M.nblk, warps);
+                        persist::gemv_region_bytes(staged, a.M.nblk, warps);
     int grid = num_sms() * (warps == 8 ? 2 : 1);
     if (a.grid > 0 && a.grid < grid) grid = a.grid;
     cudaError_t e;
-    if (act_form() == QL_GEMV_ACT_INT8)   // the int8 absmax form (16 warps)
+    if (a.M.sel)   // routed experts (batch 1, 16 warps)
+        e = persist::stream_gemv_one<1, 16, false, true>(true, &p, &g, smem, num_sms(), s, pdl);
+    else if (act_form() == QL_GEMV_ACT_INT8)   // the int8 absmax form (16 warps)
         e = a.batch == 1 ? persist::stream_gemv_one<1, 16, true>(true, &p, &g, smem, num_sms(), s, pdl)
                          : persist::stream_gemv_one<2, 16, true>(true, &p, &g, smem, num_sms(), s, pdl);
     else if (warps == 8)

@@ -238,7 +238,8 @@ __device__ __forceinline__ int tile_row(const PMat& M, int tile, int r, bool& ok
 struct Ring {
     int wp, nmat;          // matrix of the next copy; nmat = end of the step
     int u, u_end;          // unit (within the warp's range of that matrix) and range end
-    const uint8_t* src;    // stream address of unit u
+    int ubase;             // the CTA's first unit in the matrix (routed experts)
+    const uint8_t* src;    // stream address of unit u (not used for routed experts)
     unsigned int issued, consumed;   // slots; ring slot = count % kStages
     uint32_t base;         // shared-memory address of this warp's ring
     uint32_t mbar;         // shared-memory address of this warp's kStages mbarriers
@@ -258,17 +259,30 @@ __device__ __forceinline__ void ring_seek(Ring& r, const PMat* mats, int warp) {
         if (u1 > u0) {
             r.u = u0;
             r.u_end = u1;
-            r.src = M.stream + ((size_t)t0 * nst + u0) * kUnitBytes;
+            r.ubase = t0 * nst;
+            // routed experts: the address depends on the selection, read when the copy is issued
+            r.src = M.sel ? nullptr : M.stream + ((size_t)t0 * nst + u0) * kUnitBytes;
             return;
         }
     }
 }
 
 // Copy the next slot's units (up to kSlotUnits, not past the warp's range end).
-template <int W>
+template <int W, bool SEL = false>
 __device__ __forceinline__ void ring_issue(Ring& r, const PMat* mats, int warp, int lane) {
     if (r.wp >= r.nmat || r.dead) return;
-    const int n = min(kSlotUnits, r.u_end - r.u);
+    int n = min(kSlotUnits, r.u_end - r.u);
+    if (SEL) {
+        const PMat& M = mats[r.wp];
+        // the selected expert's run of units; a copy stops at the expert's end. An id outside
+        // the experts (not one a router writes) reads expert 0 instead of leaving the stream.
+        const int per = M.etiles * (M.nblk / kUnitBlocks);
+        const int abs = r.ubase + r.u, j = abs / per, within = abs - j * per;
+        int e = M.sel[j];
+        if (e < 0 || e >= M.nexp) e = 0;
+        n = min(n, per - within);
+        r.src = M.stream + ((size_t)e * per + within) * kUnitBytes;
+    }
     if (lane == 0) {
         const unsigned int slot = r.issued % kStages;
         const uint32_t mb = r.mbar + slot * 8, dst = r.base + slot * kSlotBytes;
@@ -740,7 +754,7 @@ __device__ __noinline__ void finish_tile(const PersistParams& p, const PMat& M, 
 // the f16 scale and the activation block's 2^-(s + 4) in f32. The two rows share every
 // activation load. (An MMA form wastes 7 of the 8 columns of an m16n8k16 tile at batch 1-2 and
 // measured slower; the f16 HFMA2 form of the same loop issued about twice the instructions.)
-template <int NB, int W, bool I8 = false>
+template <int NB, int W, bool I8 = false, bool SEL = false>
 __device__ __noinline__ void gemv_phase(const PersistParams& p, Hot h, const PMat* mats, int wp, int epi, bool rms,
                                         Ring& ring, const float* xf,
                                         const __half* x16, const float* norm_w, void* y, int ld,
@@ -751,20 +765,22 @@ __device__ __noinline__ void gemv_phase(const PersistParams& p, Hot h, const PMa
     const PMat M = mats[wp];
     const int cstride = h.max_nblk * 4 + 4;   // uint4 units between staged columns (+64 B)
     const int sxstride = h.max_nblk + 4;      // block (offset, scale) pairs between staged columns
+    // staged activation columns: the batch, or (routed experts' down rows) one per expert slot
+    const int SB = (SEL && M.xsel) ? M.nsel : h.B;
     uint4* xs = reinterpret_cast<uint4*>(region);
-    int2* sxs = reinterpret_cast<int2*>(xs + (size_t)NB * cstride);
-    float4* part = reinterpret_cast<float4*>(sxs + (size_t)NB * sxstride);   // [W][2][32]
+    int2* sxs = reinterpret_cast<int2*>(xs + (size_t)SB * cstride);
+    float4* part = reinterpret_cast<float4*>(sxs + (size_t)SB * sxstride);   // [W][2][32]
 
     if (I8) {
         if (rms)
-            stage_x8<true, W>(h.B, h.eps, M.nblk, cstride, xf, x16, norm_w, xs, sxs, sxstride);
+            stage_x8<true, W>(SB, h.eps, M.nblk, cstride, xf, x16, norm_w, xs, sxs, sxstride);
         else
-            stage_x8<false, W>(h.B, h.eps, M.nblk, cstride, xf, x16, norm_w, xs, sxs, sxstride);
+            stage_x8<false, W>(SB, h.eps, M.nblk, cstride, xf, x16, norm_w, xs, sxs, sxstride);
     } else {
         if (rms)
-            stage_x<true, W>(h.B, h.eps, M.nblk, cstride, xf, x16, norm_w, xs, sxs, sxstride);
+            stage_x<true, W>(SB, h.eps, M.nblk, cstride, xf, x16, norm_w, xs, sxs, sxstride);
         else
-            stage_x<false, W>(h.B, h.eps, M.nblk, cstride, xf, x16, norm_w, xs, sxs, sxstride);
+            stage_x<false, W>(SB, h.eps, M.nblk, cstride, xf, x16, norm_w, xs, sxs, sxstride);
     }
     __syncthreads();
     stamp(tr, 2);
@@ -772,7 +788,7 @@ __device__ __noinline__ void gemv_phase(const PersistParams& p, Hot h, const PMa
     Ring r = ring;   // a register copy for the loop; written back at the end
     // slots not yet in flight (a kernel may issue fewer than kStages before it waits on its
     // predecessor, so that its activation loads do not queue behind a full ring)
-    for (unsigned int i = r.issued - r.consumed; i < (unsigned int)kStages; ++i) ring_issue<W>(r, mats, warp, lane);
+    for (unsigned int i = r.issued - r.consumed; i < (unsigned int)kStages; ++i) ring_issue<W, SEL>(r, mats, warp, lane);
     const int nst = M.nblk / kUnitBlocks;
     int T0, T1;
     cta_tiles(M.ntile, T0, T1);
@@ -791,6 +807,7 @@ __device__ __noinline__ void gemv_phase(const PersistParams& p, Hot h, const PMa
     const int q0 = u1 > u0 ? (nst == 32 ? u0 >> 5 : u0 / nst) : 0;   // 4096-column matrices: a shift
     int tile = T0 + q0, k = u1 > u0 ? u0 - q0 * nst : 0;
     const int first_tile = tile;
+    int xcol = (SEL && M.xsel) ? tile / M.etiles : 0;   // routed experts' down rows: the tile's slot
 
     // this lane's share of one unit (block group kk of the tile): block bq of rows rq, rq + 8
     auto unit = [&](const unsigned char* stg, int kk) {
@@ -810,11 +827,12 @@ __device__ __noinline__ void gemv_phase(const PersistParams& p, Hot h, const PMa
         }
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
-            const int2 ov = sxs[b * sxstride + j];
+            const int bc = (SEL && M.xsel) ? xcol : b;   // the staged column this tile multiplies
+            const int2 ov = sxs[bc * sxstride + j];
             const float f = __int_as_float(ov.y);   // the activation block's scale / 16
             int lo0 = 0, hi0 = ov.x, lo1 = 0, hi1 = ov.x;
             if (I8) {   // int8 codes: one dp4a per nibble half of a code word
-                const uint4 XA = xs[(size_t)b * cstride + 2 * j], XB = xs[(size_t)b * cstride + 2 * j + 1];
+                const uint4 XA = xs[(size_t)bc * cstride + 2 * j], XB = xs[(size_t)bc * cstride + 2 * j + 1];
                 const uint32_t xl[4] = {XA.x, XA.z, XB.x, XB.z}, xh[4] = {XA.y, XA.w, XB.y, XB.w};
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
@@ -824,7 +842,7 @@ __device__ __noinline__ void gemv_phase(const PersistParams& p, Hot h, const PMa
                     hi1 = dp4a_su(xh[t], h1[t], hi1);
                 }
             } else {
-                const uint4* xb = xs + (size_t)b * cstride + 4 * j;
+                const uint4* xb = xs + (size_t)bc * cstride + 4 * j;
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
                     const uint4 X = xb[t];
@@ -861,6 +879,7 @@ __device__ __noinline__ void gemv_phase(const PersistParams& p, Hot h, const PMa
             for (int b = 0; b < NB; ++b) acc[b][0] = acc[b][1] = 0.f;
             k = 0;
             ++tile;
+            if (SEL && M.xsel) xcol = tile / M.etiles;
         }
     };
     long long wait_cyc = 0;
@@ -884,7 +903,7 @@ __device__ __noinline__ void gemv_phase(const PersistParams& p, Hot h, const PMa
         }
         __syncwarp();
         ++r.consumed;
-        ring_issue<W>(r, mats, warp, lane);   // refill the slot just read
+        ring_issue<W, SEL>(r, mats, warp, lane);   // refill the slot just read
         u += n;
     }
     ring = r;
@@ -1499,7 +1518,7 @@ struct StreamGemv {
     int prewait;                 // ring slots issued before the wait (the rest after staging)
 };
 
-template <int NB, int W, bool I8>
+template <int NB, int W, bool I8, bool SEL = false>
 __global__ void __launch_bounds__(W * 32, 16 / W) gemv_stream_kernel(const __grid_constant__ PersistParams p,
                                                                       const __grid_constant__ StreamGemv g) {
     extern __shared__ __align__(16) unsigned char smem[];
@@ -1527,7 +1546,7 @@ __global__ void __launch_bounds__(W * 32, 16 / W) gemv_stream_kernel(const __gri
     r.mbar = static_cast<uint32_t>(__cvta_generic_to_shared(&mbar[warp * kStages]));
     ring_seek<W>(r, &mat, warp);
 #pragma unroll 1
-    for (int i = 0; i < g.prewait; ++i) ring_issue<W>(r, &mat, warp, lane);
+    for (int i = 0; i < g.prewait; ++i) ring_issue<W, SEL>(r, &mat, warp, lane);
     // constants of a later kernel of the step (its norm weights), into L2 off its critical path
     l2_prefetch_share(g.next.ptr[0], g.next.bytes[0]);
     l2_prefetch_share(g.next.ptr[1], g.next.bytes[1]);
@@ -1537,8 +1556,8 @@ __global__ void __launch_bounds__(W * 32, 16 / W) gemv_stream_kernel(const __gri
     pdl_wait();
     pdl_trigger();
     stamp(tr, 1);
-    gemv_phase<NB, W, I8>(p, hot, &mat, 0, g.epi, g.rms != 0, r, g.xf, g.x16, g.norm_w, g.y, g.ld,
-                          smem + (size_t)W * kStages * kSlotBytes, kred, tr);
+    gemv_phase<NB, W, I8, SEL>(p, hot, &mat, 0, g.epi, g.rms != 0, r, g.xf, g.x16, g.norm_w, g.y, g.ld,
+                               smem + (size_t)W * kStages * kSlotBytes, kred, tr);
     const unsigned long long t0 = global_ns();
     while (r.consumed < r.issued) {   // only after a wait ran out: let copies land (bounded)
         const uint32_t mb = r.mbar + (r.consumed % kStages) * 8, parity = (r.consumed / kStages) & 1u;
@@ -1608,21 +1627,21 @@ cudaError_t launch_kernel_pdl(K kernel, int grid, int threads, size_t smem, cuda
     return ql::launch(kernel, dim3(grid), dim3(threads), smem, s, pdl, args...);
 }
 
-template <int NB, int W, bool I8 = false>
+template <int NB, int W, bool I8 = false, bool SEL = false>
 cudaError_t stream_gemv_one(bool launch, const PersistParams* p, const StreamGemv* g, size_t smem, int grid,
                             cudaStream_t s, bool pdl) {
+    auto* k = gemv_stream_kernel<NB, W, I8, SEL>;
     if (!launch) {
         int dev = 0, optin = 0;
         cudaFuncAttributes fa = {};
         cudaError_t e = cudaGetDevice(&dev);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, gemv_stream_kernel<NB, W, I8>);
+        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, k);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(gemv_stream_kernel<NB, W, I8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     optin - (int)fa.sharedSizeBytes);
+            e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - (int)fa.sharedSizeBytes);
         return e;
     }
-    return launch_kernel_pdl(gemv_stream_kernel<NB, W, I8>, grid, W * 32, smem, s, pdl, *p, *g);
+    return launch_kernel_pdl(k, grid, W * 32, smem, s, pdl, *p, *g);
 }
 
 }  // namespace persist

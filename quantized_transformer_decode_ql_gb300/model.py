@@ -40,6 +40,15 @@ class Q4Tensor:
         return self.scales.numel() * 2 + self.quants.numel()
 
 
+def _moe(cfg) -> bool:
+    return getattr(cfg, "num_experts", 0) > 0
+
+
+def _matrices(cfg):
+    """The layer's q4_0 matrices: q|k|v, o and the dense gate|up, down, or the experts' w1, w2."""
+    return ("wqkv", "wo", "w1", "w2") if _moe(cfg) else ("wqkv", "wo", "wgu", "wd")
+
+
 def _dev(a, device="cuda") -> torch.Tensor:
     if isinstance(a, torch.Tensor):
         return a.to(device=device, dtype=torch.float32).contiguous()
@@ -64,8 +73,10 @@ class DeviceModel:
         self.layers = []
         for lw in weights["layers"]:
             L = {n: _dev(lw[n], device) for n in ("attn_norm", "ffn_norm", "q_norm", "k_norm")}
-            for n in ("wqkv", "wo", "wgu", "wd"):
+            for n in _matrices(cfg):
                 L[n] = Q4Tensor.pack(_dev(lw[n], device))
+            if _moe(cfg):
+                L["router"] = _dev(lw["router"], device)
             self.layers.append(L)
         torch.cuda.synchronize()
         check(lib().ql_check_device_error(None))
@@ -101,10 +112,12 @@ class DeviceModel:
         self.layers = []
         for li in range(cfg.n_layers):
             L = {n: tensor_fn(li, n) for n in ("attn_norm", "ffn_norm", "q_norm", "k_norm")}
-            for n in ("wqkv", "wo", "wgu", "wd"):
+            for n in _matrices(cfg):
                 w = tensor_fn(li, n)
                 L[n] = Q4Tensor.pack(w)
                 del w
+            if _moe(cfg):
+                L["router"] = tensor_fn(li, "router")
             self.layers.append(L)
         torch.cuda.synchronize()
         check(lib().ql_check_device_error(None))
@@ -129,10 +142,16 @@ class DeviceModel:
     def _create(self):
         cfg = self.cfg
         self._layer_descs = (LayerDesc * cfg.n_layers)()
+        empty = Q4Matrix(None, None, 0, 0)
         for i, L in enumerate(self.layers):
-            self._layer_descs[i] = LayerDesc(ptr(L["attn_norm"]), ptr(L["ffn_norm"]), ptr(L["q_norm"]),
-                                             ptr(L["k_norm"]), L["wqkv"].desc(), L["wo"].desc(),
-                                             L["wgu"].desc(), L["wd"].desc())
+            if _moe(cfg):
+                self._layer_descs[i] = LayerDesc(ptr(L["attn_norm"]), ptr(L["ffn_norm"]), ptr(L["q_norm"]),
+                                                 ptr(L["k_norm"]), L["wqkv"].desc(), L["wo"].desc(), empty, empty,
+                                                 ptr(L["router"]), L["w1"].desc(), L["w2"].desc())
+            else:
+                self._layer_descs[i] = LayerDesc(ptr(L["attn_norm"]), ptr(L["ffn_norm"]), ptr(L["q_norm"]),
+                                                 ptr(L["k_norm"]), L["wqkv"].desc(), L["wo"].desc(),
+                                                 L["wgu"].desc(), L["wd"].desc(), None, empty, empty)
         d = ModelDesc()
         d.hidden, d.n_layers, d.n_heads = cfg.hidden, cfg.n_layers, cfg.n_heads
         d.n_kv_heads, d.head_dim, d.intermediate, d.vocab = cfg.n_kv_heads, cfg.head_dim, cfg.intermediate, cfg.vocab
@@ -143,15 +162,32 @@ class DeviceModel:
         d.num_blocks, d.block_size = self.num_blocks, BLOCK
         d.max_batch, d.max_blocks_per_seq = self.max_batch, self.max_blocks_per_seq
         d.kv_format, d.kvq_pool = self.kv_format, ptr(self.kvq_pool)
+        d.num_experts, d.topk, d.moe_inter = cfg.num_experts, cfg.topk, cfg.moe_inter
+        d.norm_topk = 1 if cfg.norm_topk else 0
         self._desc = d
         h = ctypes.c_void_p()
         check(lib().ql_model_create(ctypes.byref(d), ctypes.byref(h)))
         self.handle = h.value
 
     def weight_bytes(self) -> int:
+        """Bytes of every q4_0 weight (and router) of the model."""
         n = self.lm_head.nbytes()
         for L in self.layers:
-            n += sum(L[k].nbytes() for k in ("wqkv", "wo", "wgu", "wd"))
+            n += sum(L[k].nbytes() for k in _matrices(self.cfg))
+            if _moe(self.cfg):
+                n += L["router"].numel() * 4
+        return n
+
+    def step_weight_bytes(self) -> int:
+        """Weight bytes one batch-1 decode step reads: every dense matrix, or for routed experts
+        the attention matrices, the router and topk experts' rows per layer."""
+        if not _moe(self.cfg):
+            return self.weight_bytes()
+        cfg = self.cfg
+        n = self.lm_head.nbytes()
+        for L in self.layers:
+            n += L["wqkv"].nbytes() + L["wo"].nbytes() + L["router"].numel() * 4
+            n += cfg.topk * (L["w1"].nbytes() + L["w2"].nbytes()) // cfg.num_experts
         return n
 
     @staticmethod
