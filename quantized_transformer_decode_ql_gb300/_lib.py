@@ -76,6 +76,7 @@ SIGNATURES = {
     "ql_set_batched_gemv_form": (c_int, [c_int]),
     "ql_set_gemv_activation_form": (c_int, [c_int]),
     "ql_kvq_record_bytes": (c_int64, [c_int]),
+    "ql_prefill_chunk": (c_int, [c_void_p, c_void_p, c_int64, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     "ql_kvq_write": (c_int, [c_void_p, c_void_p, c_void_p, c_int64, c_int, c_int, c_void_p, c_int64, c_void_p]),
     "ql_paged_attn_decode_kvq": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int, c_int, c_int, c_int,
                                          c_int64, c_int64, c_float, c_void_p, c_void_p, c_size_t, c_void_p]),

@@ -80,6 +80,11 @@ struct ql_model {
     float* mewt = nullptr;       // [topk]
     __half* mact = nullptr;      // [topk][moe_inter]
     float* medn = nullptr;       // [topk][hidden]
+    // chunked prefill: the chunk's per-token block tables (the sequence's row repeated),
+    // positions and context lengths
+    int32_t* pbt = nullptr;      // [max_batch][max_blocks_per_seq]
+    int32_t* ppos = nullptr;     // [max_batch]
+    int32_t* plen = nullptr;     // [max_batch]
 };
 
 namespace ql {
@@ -121,6 +126,31 @@ __global__ void finalize_kernel(unsigned long long* keys, const int32_t* active,
             out_tokens[(size_t)b * out_stride + pos + 1] = tok;
         positions[b] = pos + 1;
     }
+}
+
+// Chunked prefill: token t of the chunk sits at position p0 + t (p0 = *position) and attends
+// to positions 0 .. p0 + t; every token uses the sequence's block table row.
+__global__ void prefill_setup_kernel(const int32_t* position, const int32_t* block_table, int maxb, int T,
+                                     int32_t* bt, int32_t* pos, int32_t* len) {
+    pdl_wait();
+    pdl_trigger();
+    const int p0 = *position;
+    for (int i = threadIdx.x; i < T * maxb; i += blockDim.x) bt[i] = block_table[i % maxb];
+    for (int t = threadIdx.x; t < T; t += blockDim.x) {
+        pos[t] = p0 + t;
+        len[t] = p0 + t + 1;
+    }
+}
+
+// The chunk's last token's greedy next token (its argmax key), the position advanced by T.
+__global__ void prefill_finish_kernel(unsigned long long* keys, int32_t* position, int32_t* next_token, int T) {
+    pdl_wait();
+    pdl_trigger();
+    if (threadIdx.x != 0) return;
+    const unsigned long long k = keys[0];
+    keys[0] = 0ull;
+    if (next_token) *next_token = (int)(0xFFFFFFFFu - (uint32_t)(k & 0xFFFFFFFFull));
+    *position += T;
 }
 
 bool check_matrix(const ql_q4_0_matrix& m, int64_t rows, int64_t cols) {
@@ -489,6 +519,107 @@ int run_step(ql_model* m, const ql_step_args* a, cudaStream_t s) {
     return QL_OK;
 }
 
+// A chunk of T prompt tokens of one sequence through every layer together: the step's GEMVs at
+// batch T (stream form at T <= 2, the split-K tensor-core form at 3..32), qk-norm + RoPE +
+// append for all T positions, then causal attention of each token over the cache (its own
+// context length), and logits of the last token only.
+int run_prefill(ql_model* m, const int32_t* tokens, int T, int32_t* position, const int32_t* block_table,
+                float* logits, int32_t* next_token, cudaStream_t s) {
+    const ql_model_desc& d = m->d;
+    const bool pdl = true;
+    const int hd = (int)d.head_dim, nh = (int)d.n_heads, nkv = (int)d.n_kv_heads;
+    const size_t layer_pool = (size_t)d.num_blocks * nkv * d.block_size * hd;
+    const int maxb = (int)d.max_blocks_per_seq;
+    int rc;
+    cudaError_t e = launch(prefill_setup_kernel, dim3(1), dim3(256), 0, s, pdl, position, block_table, maxb, T, m->pbt,
+                           m->ppos, m->plen);
+    if (e != cudaSuccess) return cuda_error(e, "prefill setup launch");
+    const NextWeights none = {{nullptr, nullptr}, {0, 0}};
+    e = launch(embed_kernel, dim3(T), dim3(256), 0, s, pdl, d.embed, tokens, (const int32_t*)nullptr, m->x,
+               (int)d.hidden, (int)d.vocab, device_error_record(), none);
+    if (e != cudaSuccess) return cuda_error(e, "embed launch");
+    auto sg = [&](const PMat& M, int epi, bool rms, const float* xf, const __half* x16, const float* nw, void* y,
+                  int ld, int batch) {
+        StreamGemvArgs ga = {};
+        ga.next = none;
+        ga.M = M;
+        ga.batch = batch;
+        ga.epilogue = epi;
+        ga.rms = rms ? 1 : 0;
+        ga.xf = xf;
+        ga.x16 = x16;
+        ga.norm_w = nw;
+        ga.eps = d.eps;
+        ga.y = y;
+        ga.ld = ld;
+        ga.keys = m->keys;
+        ga.active = nullptr;
+        ga.sync = m->ssync;
+        ga.xn = m->xn;
+        ga.workspace = m->bws;
+        ga.workspace_bytes = m->bws_bytes;
+        return batch <= kPersistMaxBatch ? stream_gemv_launch(ga, s, pdl) : batched_gemv_launch(ga, s, pdl);
+    };
+    const int qkv_ld = (int)((d.n_heads + 2 * d.n_kv_heads) * d.head_dim);
+    for (int li = 0; li < d.n_layers; ++li) {
+        const ql_layer_desc& L = m->layers[li];
+        const PMat* Ms = &m->hmats[4 * li];
+        if ((rc = sg(Ms[0], QL_EPI_NONE, true, m->x, nullptr, L.attn_norm, m->qkv, qkv_ld, T)) != QL_OK) return rc;
+        RopeArgs ra = {};
+        ra.qkv = m->qkv;
+        ra.q_norm = L.q_norm;
+        ra.k_norm = L.k_norm;
+        ra.cos_t = m->cos_t;
+        ra.sin_t = m->sin_t;
+        ra.positions = m->ppos;
+        ra.eps = d.eps;
+        ra.batch = T;
+        ra.n_heads = nh;
+        ra.n_kv_heads = nkv;
+        ra.head_dim = hd;
+        ra.q_out = m->q16;
+        ra.k_pool = static_cast<__half*>(d.k_pool) + layer_pool * li;
+        ra.v_pool = static_cast<__half*>(d.v_pool) + layer_pool * li;
+        ra.block_tables = m->pbt;
+        ra.max_blocks_per_seq = maxb;
+        ra.block_size = d.block_size;
+        ra.num_blocks = d.num_blocks;
+        ra.max_position = d.max_blocks_per_seq * d.block_size;
+        if ((rc = rope_launch(ra, s, pdl)) != QL_OK) return rc;
+        AttnArgs at = {};
+        at.q = m->q16;
+        at.k_pool = ra.k_pool;
+        at.v_pool = ra.v_pool;
+        at.block_tables = m->pbt;
+        at.context_lens = m->plen;
+        at.batch = T;
+        at.n_heads = nh;
+        at.n_kv_heads = nkv;
+        at.head_dim = hd;
+        at.block_size = d.block_size;
+        at.max_blocks_per_seq = maxb;
+        at.num_blocks = d.num_blocks;
+        at.scale = 1.0f / sqrtf((float)hd);
+        at.out = m->attn;
+        at.workspace = m->attn_ws;
+        at.workspace_bytes = m->attn_ws_bytes;
+        if ((rc = attn_launch(at, s, pdl)) != QL_OK) return rc;
+        if ((rc = sg(Ms[1], QL_EPI_ADD_RESIDUAL, false, nullptr, m->attn, nullptr, m->x, (int)d.hidden, T)) != QL_OK)
+            return rc;
+        if ((rc = sg(Ms[2], QL_EPI_SILU_MUL, true, m->x, nullptr, L.ffn_norm, m->act, (int)d.intermediate, T)) != QL_OK)
+            return rc;
+        if ((rc = sg(Ms[3], QL_EPI_ADD_RESIDUAL, false, nullptr, m->act, nullptr, m->x, (int)d.hidden, T)) != QL_OK)
+            return rc;
+    }
+    // the last token's logits and greedy next token
+    if ((rc = sg(m->hmats.back(), kEpiArgmax, true, m->x + (size_t)(T - 1) * d.hidden, nullptr, d.final_norm,
+                 logits ? logits : m->logits, (int)d.vocab, 1)) != QL_OK)
+        return rc;
+    e = launch(prefill_finish_kernel, dim3(1), dim3(32), 0, s, pdl, m->keys, position, next_token, T);
+    if (e != cudaSuccess) return cuda_error(e, "prefill finish launch");
+    return QL_OK;
+}
+
 PMat pmat(const ql_q4_0_matrix& w, bool silu) {
     PMat p = {};
     p.stream = nullptr;
@@ -721,6 +852,9 @@ extern "C" int ql_model_create(const ql_model_desc* desc, ql_model** out) {
     A((void**)&m->q16, B * d.n_heads * d.head_dim * 2);
     A((void**)&m->attn, B * d.n_heads * d.head_dim * 2);
     A((void**)&m->act, B * (d.intermediate > 0 ? d.intermediate : 1) * 2);
+    A((void**)&m->pbt, B * d.max_blocks_per_seq * 4);
+    A((void**)&m->ppos, B * 4);
+    A((void**)&m->plen, B * 4);
     if (d.num_experts > 0) {
         A((void**)&m->mlog, d.num_experts * 4);
         A((void**)&m->mticket, 16);
@@ -805,6 +939,23 @@ extern "C" int ql_decode_step(ql_model* m, const ql_step_args* args, void* strea
     int rc = check_step_args(m, args);
     if (rc != QL_OK) return rc;
     return run_step(m, args, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int ql_prefill_chunk(ql_model* m, const int32_t* d_tokens, int64_t n_tokens, int32_t* d_position,
+                                const int32_t* d_block_table, float* d_logits, int32_t* d_next_token, void* stream) {
+    if (!m || !d_tokens || !d_position || !d_block_table) return set_error(QL_EINVAL, "ql_prefill_chunk: null pointer");
+    const ql_model_desc& d = m->d;
+    if (d.num_experts > 0 || d.kv_format != QL_KV_F16)
+        return set_error(QL_EINVAL, "ql_prefill_chunk: dense models with the f16 KV cache only");
+    if (n_tokens < 1 || n_tokens > 32 || n_tokens > d.max_batch)
+        return set_error(QL_EINVAL, "ql_prefill_chunk: n_tokens must be in [1, min(32, max_batch)]");
+    if (m->hmats.empty() || (n_tokens > kPersistMaxBatch && !m->batched_ok))
+        return set_error(QL_EINVAL, "ql_prefill_chunk: needs the tile stream copies (and the batched GEMV above 2 tokens)");
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev != m->device) return set_error(QL_EINVAL, "ql_prefill_chunk: current device differs from the model's");
+    return run_prefill(m, d_tokens, (int)n_tokens, d_position, d_block_table, d_logits, d_next_token,
+                       static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int ql_decode_graph_capture(ql_model* m, const ql_step_args* args, void* stream) {

@@ -216,6 +216,13 @@ class DeviceModel:
     def ql_decode_graph_replay(self, batch: int, n_steps: int, stream=None):
         check(lib().ql_decode_graph_replay(self.handle, batch, n_steps, stream_ptr(stream)))
 
+    def ql_prefill_chunk(self, tokens, position, block_table, logits=None, next_token=None, stream=None):
+        """Run the prompt tokens ``tokens`` (int32 [T] device, T <= 32) of one sequence as one
+        chunk at ``position`` (int32 [1] device, advanced by T) through the sequence's
+        ``block_table`` (int32 [max_blocks_per_seq] device)."""
+        check(lib().ql_prefill_chunk(self.handle, ptr(tokens), tokens.numel(), ptr(position), ptr(block_table),
+                                     ptr(logits), ptr(next_token), stream_ptr(stream)))
+
     def ql_check_device_error(self):
         check(lib().ql_check_device_error(self.handle))
 
