@@ -473,6 +473,8 @@ def gpu_arm(args, rank, world, local_rank):
     }
     if phases:
         line["step_phases_us"] = phases
+    if not args.layers:
+        line["prefill_8b"] = prefill_run(gm, cfg, s)
     if not args.layers and not args.no_moe:
         line["moe_a3b_b1"] = moe_run(min(steps, 64), 3, s, local_rank, world)
     if not args.layers and not args.no_e32:
@@ -548,6 +550,45 @@ def moe_run(steps, warmup, s, local_rank, world):
                 **({"step_phases_us": phases} if phases else {})}
     finally:
         gm.close()
+
+
+def prefill_run(gm, cfg, s, n_prompt=2048, chunk=32):
+    """Chunked prefill of one n_prompt-token prompt on the 8B shape (a sibling handle with batch
+    bound 32 over the same weights): n_prompt / chunk calls of ql_prefill_chunk timed with CUDA
+    events on the launching stream, against the weights streamed once per chunk."""
+    import torch
+    maxb = (n_prompt + 15) // 16 + 1
+    gp = gm.sibling(num_blocks=maxb + 8, max_batch=chunk, max_blocks_per_seq=maxb)
+    try:
+        bt = torch.from_numpy(ql_inputs.fragmented_block_ids(maxb + 8, seed=5)[:maxb].copy()).cuda()
+        prompt = torch.from_numpy(ql_inputs.prompt_tokens(n_prompt, cfg.vocab, seed=1)).cuda()
+        position = torch.zeros(1, dtype=torch.int32, device="cuda")
+        nxt = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+        def run():
+            for c0 in range(0, n_prompt, chunk):
+                gp.ql_prefill_chunk(prompt[c0:c0 + chunk], position, bt, next_token=nxt, stream=s)
+        with torch.cuda.stream(s):
+            run()                       # warm-up pass over the whole prompt
+            position.zero_()
+        s.synchronize()
+        gp.ql_check_device_error()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record(s)
+            run()
+            e1.record(s)
+        s.synchronize()
+        gp.ql_check_device_error()
+        ms = e0.elapsed_time(e1)
+        n_chunks = -(-n_prompt // chunk)
+        wbytes = gp.weight_bytes()
+        return {"value": round(n_prompt / (ms / 1e3), 1), "unit": "prompt tokens/s", "prompt": n_prompt,
+                "chunk": chunk, "ms": round(ms, 3), "ms_per_chunk": round(ms / n_chunks, 4),
+                "workload": f"qwen3-8b-shaped q4_0 prefill of one {n_prompt}-token prompt in chunks of {chunk}",
+                "weights_gbs": round(wbytes * n_chunks / (ms / 1e3) / 1e9, 1)}
+    finally:
+        gp.close()
 
 
 E32_STEPS = 128
