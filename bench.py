@@ -1042,7 +1042,7 @@ def micro_gemv_stream(shapes, batches, iters):
             y = torch.empty((B, rows), dtype=torch.float32, device="cuda")
             ws = None
             if B > 2:
-                ws = torch.empty(ql.ql_gemv_q4_0_stream_workspace_bytes(rows, cols, 0), dtype=torch.uint8,
+                ws = torch.zeros(ql.ql_gemv_q4_0_stream_workspace_bytes(rows, cols, 0), dtype=torch.uint8,
                                  device="cuda")
 
             def run(n):

@@ -122,11 +122,15 @@ int ql_q4_0_stream_pack(const void* d_scales, const void* d_quants, int64_t rows
  * exactly, and each block is scaled by its f16 scale and 2^-s and accumulated in f32. Batch 3-32 (needs cols in 128..896 or a multiple of 1024): the
  * tensor-core form (A = (q - 8) d rounded once to f16, f16 x, f32 products and sums), split
  * over K in windows of 1024 columns so that every weight byte is streamed once; each window's
- * f32 partial sums go to d_workspace and a second kernel adds them in window order
- * (deterministic) and applies the epilogue. d_workspace (device, 256-byte aligned, at least
- * ql_gemv_q4_0_stream_workspace_bytes) is caller-owned scratch; calls that run concurrently
- * need separate workspaces. It may be NULL at batch 1-2. One CTA per SM; its waits for the bulk copies are
- * bounded (2 s, then the device error record says so). QL_EINVAL for other batches.       */
+ * f32 partial sums go to d_workspace and are added in window order (deterministic) before the
+ * epilogue: by a second kernel or (tcgen05 form, selectable) inside the kernel by the CTA that
+ * finishes a row block's last window (an atomic ticket per row block). d_workspace
+ * (device, 256-byte aligned, at least ql_gemv_q4_0_stream_workspace_bytes) is caller-owned
+ * scratch, ZERO-FILLED before its first use; every call leaves it valid for the next call of
+ * any shape (the tickets re-armed), unless the device error record reports a failed wait, after
+ * which it must be zero-filled again. Calls that run concurrently need separate workspaces.
+ * It may be NULL at batch 1-2. One CTA per SM; its waits are bounded (2 s, then the device error
+ * record says so). QL_EINVAL for other batches.                                             */
 int ql_gemv_q4_0_stream(const void* d_stream, int64_t rows, int64_t cols, const void* d_x,
                         int64_t batch, void* d_y, int epilogue, void* d_workspace,
                         int64_t workspace_bytes, void* stream);
@@ -152,10 +156,15 @@ int64_t ql_gemv_q4_0_stream_workspace_bytes(int64_t rows, int64_t cols, int silu
 /* Tensor-core form of the batch 3-32 GEMV, for this process (ql_gemv_q4_0_stream and the
  * decode step; graphs keep the form they were captured with):
  *   QL_BATCHED_MMA_SYNC  (default) warps issue mma.sync m16n8k16 on the dequantised weights;
- *   QL_BATCHED_TCGEN05   16 warps write (q - 8) d into tensor memory (tcgen05.st) and one warp
- *                        issues tcgen05.mma (kind::f16, M 128, N 32, K 16) against the staged
- *                        activations; same partial sums, same merge. Parity-tested; slower on
- *                        the decode step so far (its expansion and copy pipeline is latency-bound).
+ *   QL_BATCHED_TCGEN05   a producer lane streams the codes into a 16-stage shared-memory ring
+ *                        (tensor-map copies), 16 warps write (q - 8) d into tensor memory
+ *                        (tcgen05.st), one lane issues tcgen05.mma (kind::f16, M 128, N 32,
+ *                        K 16) against the staged activations into double-buffered f32
+ *                        accumulators, 4 warps drain them as partial sums, and the second
+ *                        kernel adds the K windows (QL_TC_KERNEL_MERGE=1 in the environment: the
+ *                        CTA finishing a row block's last window does, by ticket). Same results
+ *                        as the mma.sync form up to f32 summation order; slower on the decode
+ *                        step at batch 32 (the MMA issue rate at N = 32 is the limit).
  * The initial form is QL_BATCHED_TCGEN05 when the environment sets QL_BATCHED_TC=1. Returns
  * the previous form, or QL_EINVAL for an unknown one.                                     */
 enum { QL_BATCHED_MMA_SYNC = 0, QL_BATCHED_TCGEN05 = 1 };

@@ -21,6 +21,8 @@
 // ring of bulk copies (TMA) as the batch-1 kernel.
 #include "ql_persist.cuh"
 
+#include <cuda.h>   // CUtensorMap and its enums (the encoder is taken from the driver at run time)
+
 #include <atomic>
 #include <cstdlib>
 #include <mutex>
@@ -60,6 +62,10 @@ struct BParams {
     unsigned long long timeout_ns;
     float* part;           // [nwin][ntile * 16][kMaxCols] f32 partial sums of the K windows
     int ngr;               // row groups (grid = nwin * ngr)
+    int* tickets;          // tcgen05 form: [ngr][maxrb] window counts per row block, zero between calls
+    int maxrb;             // row blocks (8 tiles) of the largest row group
+    int kernel_merge;      // tcgen05 form: 1 = merge the K windows in the kernel (tickets), 0 = merge_kernel
+    CUtensorMap tmap;      // tcgen05 form: the stream as [tile][unit][144 x 8 bytes], boxes of 8 tiles x 1 unit
     unsigned long long* trace;   // optional [grid][8] globaltimer stamps: 0 start, 1 past the wait,
                                  // 2 staged, 3 units done, 4 partials written, 5 end
 };
@@ -505,32 +511,59 @@ __global__ void __launch_bounds__(kNormT) rms_norm_kernel(const float* x, int co
 }
 
 // ------------------------------------------------------------------ tcgen05 form
-// The same split over K, with the products on the 5th-generation tensor cores: per row block of
-// 8 tiles (128 rows, the MMA's M) and unit of the window, 16 dequantisation warps write the
-// block's (q - 8) d into tensor memory (one thread per row: its 16-byte code runs expand, with
-// LOP3 / HSUB2 / HMUL2, to the f16 values of the A operand, `tcgen05.st`), and one control warp
-// issues `tcgen05.mma` (kind::f16, M = 128, N = 32 batch columns, K = 16) against the window's
-// activations staged once in shared memory (the B operand, K-major core matrices), accumulating
-// in f32 in tensor memory. The K order inside a 32-bit code word is the same permutation on both
-// operands (the staged pairs of stage_window), so the sums are exact dot products. The codes
-// stream in by bulk copies (one per tile per row block, 2 row blocks in flight); the
-// accumulators of a row block are read back (`tcgen05.ld`) by 4 warps and written as the
-// window's partial sums for merge_kernel. Every wait is bounded.
+// The same split over K, with the products on the 5th-generation tensor cores and every stage
+// of the work in its own warps, joined by mbarriers:
+//  * a producer lane streams the codes into a ring of kS shared-memory stages, one stage = one
+//    unit (128 columns) of every tile of a row block (8 tiles = 128 rows, the MMA's M): one
+//    tensor-map copy of 8 tiles x 1 unit (single-tile copies for a row group's last, partial
+//    row block), completing on the stage's mbarrier;
+//  * 16 dequantisation warps in 4 groups (one warp per tensor-memory lane quarter each: the
+//    warp of quarter q handles rows 32q..32q+31, tiles 2q and 2q+1 of the row block) take
+//    groups of kPair units in turn: each thread expands its row's codes into (q - 8) d in f16
+//    (LOP3 / HSUB2 / HMUL2, the K order of the staged activations) and stores them into one of
+//    kA rotating A slots of tensor memory (`tcgen05.st`);
+//  * one lane issues `tcgen05.mma` (kind::f16, M = 128, N = 32 batch columns, K = 16, A in
+//    tensor memory, B = the window's activations staged once in shared memory as K-major core
+//    matrices) into one of two f32 accumulators, and commits each group of units and each
+//    finished row block to mbarriers;
+//  * 4 epilogue warps read a finished row block's accumulator (`tcgen05.ld`) and write it as the
+//    window's partial sums; merge_kernel adds the windows in window order, or (selectable) the
+//    CTA that takes a row block's last ticket does (results do not depend on which CTA merges).
+// Measured on GB300: one M128 N32 K16 MMA occupies the tensor core ~28 ns whatever N up to 64,
+// ~35 ns while other warps store into tensor memory, so at N = 32 the products alone take about
+// as long as streaming the weights; with the waits, fences and commits around each group the
+// form runs behind the mma.sync form on the batch-32 step.
+// Every wait is bounded; after a timeout the CTA records the error, stops, lets its copies in
+// flight land and frees its tensor memory.
 namespace tc {
 constexpr int kDW = 16;                        // dequantisation warps, 4 per tensor-memory lane quarter
-constexpr int kCtl = kDW;                      // the control warp (allocation, MMA issue)
-constexpr int kThreads = (kDW + 1) * 32;
+constexpr int kMmaWarp = kDW;                  // tensor-memory allocation; lane 0 issues the MMAs
+constexpr int kProdWarp = kDW + 1;             // lane 0 issues the bulk copies
+constexpr int kEpiWarp0 = kDW + 2;             // 4 epilogue warps (quarter = warp & 3)
+constexpr int kWarps = kDW + 6, kThreads = kWarps * 32;
 constexpr int kRB = 8;                         // tiles per row block: 128 rows
+constexpr int kStageBytes = kRB * kUnitBytes;  // one unit of each tile of a row block
+constexpr int kS = 16;                         // shared-memory stages
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kACol = 64;                 // A slots: kASlots x 64 columns from here; D: 2 x 32 below
-constexpr int kASlots = 7;                     // unit g of the CTA (row block x window units) uses slot g % 7
-constexpr size_t kCodesBytes = (size_t)kRB * kWinUnits * kUnitBytes;   // one row block's codes
+constexpr int kAcc = 1;                        // accumulators per set (32 columns each)
+constexpr uint32_t kDCols = 32u * kAcc;        // one set
+constexpr uint32_t kACol = 2 * kDCols;         // A slots after the two sets
+constexpr int kPair = 2;                       // units of a row block per A slot (one MMA group)
+constexpr int kA = (int)((kTmemCols - kACol) / (64 * kPair));   // A slots of kPair x 64 columns
 constexpr size_t kBBytes = (size_t)kWinUnits * kUnitBlocks * 4 * 4 * 128;   // window x 32 columns, f16
-constexpr size_t kSmem = 2 * kCodesBytes + kBBytes;
+constexpr size_t kSmem = (size_t)kS * kStageBytes + kBBytes;
 // MMA instruction descriptor: D f32, A and B f16, both K-major, N = 32, M = 128
 constexpr uint32_t kIdesc = (1u << 4) | ((32u >> 3) << 17) | ((128u >> 4) << 24);
-enum { kFull = 0, kFree = 2, kAFull = 4, kAFree = 4 + kASlots, kDFull = 4 + 2 * kASlots, kDFree = kDFull + 2,
-       kDone = kDFree + 2, kBars = kDone + 1 };
+constexpr int kGroups = kDW / 4;                // dequantisation groups (one warp per lane quarter each)
+// Barriers. A waiter on phase k of an mbarrier must know that phase k - 1 has completed (a parity
+// test cannot tell phase k - 1 from k + 1), so every barrier has one waiter role that takes its
+// phases in order: the producer SFree, the group of a slot's stages SFull (stage s and s + kS
+// always fall to the same group), the MMA lane AFull and DFree, the epilogue DFull, and each
+// group its own AFreeG, which the MMA lane commits in that group's order of unit groups.
+enum { kSFull = 0, kSFree = kS, kAFull = 2 * kS, kAFreeG = 2 * kS + kA, kDFull = 2 * kS + kA + kGroups,
+       kDFree = kDFull + 2, kDone = kDFree + 2, kBars = kDone + 1 };
+static_assert(kS % (2 * kGroups) == 0, "a slot's stages must fall to one group");
+constexpr int kEpiBarrier = 1;                 // named barrier of the 4 epilogue warps
 
 __device__ __forceinline__ uint32_t su32(const void* q) { return static_cast<uint32_t>(__cvta_generic_to_shared(q)); }
 
@@ -555,8 +588,28 @@ __device__ __forceinline__ bool tc_wait(uint32_t mb, uint32_t parity, const BPar
     return false;
 }
 
+// tc_wait by every lane of a warp, with one answer for the warp (its collective tcgen05
+// instructions that follow need every lane or none): false if any lane's wait failed.
+__device__ __forceinline__ bool warp_wait(uint32_t mb, uint32_t parity, const BParams& p, int* abort_flag, int where) {
+    const bool ok = tc_wait(mb, parity, p, abort_flag, where);
+    return __all_sync(0xffffffffu, ok);
+}
+
 __device__ __forceinline__ void arrive(uint32_t mb) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(mb) : "memory");
+}
+
+// 16 consecutive 32-bit columns of this warp's 32 tensor-memory lanes, waited for.
+__device__ __forceinline__ void tmem_ld16(uint32_t addr, uint32_t (&v)[16]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+                   "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+                 : "r"(addr) : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void epi_sync() {
+    asm volatile("bar.sync %0, %1;" ::"n"(kEpiBarrier), "n"(4 * 32) : "memory");
 }
 
 // Stage window w of every column as the B operand: chunk kc = 4 j + t (8 f16: the pairs of
@@ -606,23 +659,109 @@ __device__ void stage_b(const BParams& p, const Geo& G, unsigned char* bsm, int 
     }
 }
 
-// Bulk copy of tile i of row block rb (its units of the window, contiguous) into the row
-// block's codes buffer; one lane. A tile past the row group only arrives.
-__device__ __forceinline__ void issue_tile(const BParams& p, const Geo& G, unsigned char* codes, uint32_t bar, int rb,
-                                           int i) {
-    const int tl = rb * kRB + i, b = rb & 1;
-    const uint32_t mb = bar + (kFull + b) * 8;
-    if (tl >= G.T1 - G.T0) {
-        arrive(mb);
+// Bulk copies of stage s (row block s / kwu, unit s % kwu of the window: that unit of each of
+// the row block's tiles) into its shared-memory slot; one lane. Tiles past the row group are
+// not copied (their rows are never written out).
+__device__ __forceinline__ void issue_stage(const BParams& p, const Geo& G, unsigned char* ring, uint32_t bar, int rb,
+                                            int kk, int slot, unsigned long long pol) {
+    const int T = G.T1 - G.T0;
+    const int nt = T - rb * kRB < kRB ? T - rb * kRB : kRB;
+    const uint32_t mb = bar + (kSFull + slot) * 8;
+    // the slot's previous contents were read through the generic proxy; the copy below writes it
+    // through the async proxy
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mb), "r"((uint32_t)(nt * kUnitBytes))
+                 : "memory");
+    if (nt == kRB) {   // a whole row block: one tensor copy of 8 tiles x 1 unit
+        asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+                     " [%0], [%1, {%2, %3, %4}], [%5], %6;"
+                     ::"r"(su32(ring + (size_t)slot * kStageBytes)), "l"(reinterpret_cast<uint64_t>(&p.tmap)), "r"(0),
+                       "r"(G.w * G.kwu + kk), "r"(G.T0 + rb * kRB), "r"(mb), "l"(pol) : "memory");
         return;
     }
-    const uint32_t bytes = (uint32_t)(G.kwu * kUnitBytes);
-    const uint8_t* src = p.M.stream + ((size_t)(G.T0 + tl) * G.nst + (size_t)G.w * G.kwu) * kUnitBytes;
-    const uint32_t dst = su32(codes + (size_t)b * kCodesBytes + (size_t)i * G.kwu * kUnitBytes);
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mb), "r"(bytes) : "memory");
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
-                 ::"r"(dst), "l"(src), "r"(bytes), "r"(mb), "l"(l2_evict_first()) : "memory");
+    for (int i = 0; i < nt; ++i) {
+        const uint8_t* src = p.M.stream + ((size_t)(G.T0 + rb * kRB + i) * G.nst + (size_t)G.w * G.kwu + kk) * kUnitBytes;
+        const uint32_t dst = su32(ring + (size_t)slot * kStageBytes + (size_t)i * kUnitBytes);
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+                     ::"r"(dst), "l"(src), "r"((uint32_t)kUnitBytes), "r"(mb), "l"(pol) : "memory");
+    }
+}
+
+// The merge of row block rb (tiles T0 + 8 rb ..) by the 4 epilogue warps: every output's window
+// partials added in window order, then the epilogue. A window's partials of a row block are
+// one contiguous run of 128 rows x 32 columns (f32); thread e reads float4 e + 128 j of it (row
+// e / 8 + 16 j, i.e. tile j, row e / 8 of the tile; columns 4 (e % 8) ..), so that each warp
+// load is 512 contiguous bytes. SiLU*up: the threads holding a gate row (row of the tile < 8)
+// also read its up row 8 further; the others idle. Every epilogue thread runs the whole
+// function, so that the argmax reduction can shuffle over full warps.
+template <bool SILU>
+__device__ __noinline__ void merge_rb(const BParams& p, const Geo& G, int rb, int e) {
+    const bool resid = p.epi == QL_EPI_ADD_RESIDUAL, amax = p.epi == kEpiArgmax;
+    const int T = G.T1 - G.T0, ntl = T - rb * kRB < kRB ? T - rb * kRB : kRB;
+    const int rit = e >> 3, c4 = e & 7;                 // row of the tile, column group
+    const int lim = SILU ? (p.M.rows >> 1) : p.M.rows;
+    const size_t wstride = (size_t)p.M.ntile * 16 * (kMaxCols / 4);   // float4 per window
+    const float4* base = reinterpret_cast<const float4*>(p.part) + (size_t)(G.T0 + rb * kRB) * 16 * (kMaxCols / 4) + e;
+    float* yf = static_cast<float*>(p.y);
+    constexpr int kJ = 4;                               // tiles per round
+    for (int j0 = 0; j0 < kRB; j0 += kJ) {
+        float4 sg[kJ], su[kJ];
+#pragma unroll
+        for (int j = 0; j < kJ; ++j) sg[j] = su[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        const bool lanes = !SILU || rit < 8;
+        for (int w = 0; w < G.nwin; ++w) {
+            float4 vg[kJ], vu[kJ];
+#pragma unroll
+            for (int j = 0; j < kJ; ++j) {
+                if (lanes && j0 + j < ntl) {
+                    const float4* q = base + (size_t)w * wstride + (size_t)(j0 + j) * 128;
+                    vg[j] = __ldcg(q);
+                    if (SILU) vu[j] = __ldcg(q + 64);   // row + 8 of the tile
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kJ; ++j) {
+                if (lanes && j0 + j < ntl) {
+                    sg[j].x += vg[j].x; sg[j].y += vg[j].y; sg[j].z += vg[j].z; sg[j].w += vg[j].w;
+                    if (SILU) { su[j].x += vu[j].x; su[j].y += vu[j].y; su[j].z += vu[j].z; su[j].w += vu[j].w; }
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kJ; ++j) {
+            const int tile = G.T0 + rb * kRB + j0 + j;
+            const int row = SILU ? tile * 8 + rit : tile * 16 + rit;
+            const bool valid = lanes && j0 + j < ntl && row < lim;
+            const float sv[4] = {sg[j].x, sg[j].y, sg[j].z, sg[j].w};
+            const float uv[4] = {su[j].x, su[j].y, su[j].z, su[j].w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int c = 4 * c4 + k;
+                if (valid && c < p.B) {
+                    if (SILU) {
+                        static_cast<__half*>(p.y)[(size_t)c * p.ld + row] = __float2half_rn(persist::silu(sv[k]) * uv[k]);
+                    } else if (resid) {
+                        float* yp = yf + (size_t)c * p.ld + row;
+                        *yp = __ldcg(yp) + sv[k];
+                    } else {
+                        yf[(size_t)c * p.ld + row] = sv[k];
+                    }
+                }
+                if (!SILU && amax) {
+                    // per column: the largest key over the lanes holding it (lanes e % 8 equal),
+                    // then one atomic per warp and column
+                    unsigned long long key = valid && c < p.B ? persist::argmax_key(sv[k], row) : 0ull;
+#pragma unroll
+                    for (int o = 8; o < 32; o <<= 1) {
+                        const unsigned long long ok = __shfl_xor_sync(0xffffffffu, key, o);
+                        key = ok > key ? ok : key;
+                    }
+                    const bool act = c < p.B && (p.active == nullptr || p.active[c] != 0);
+                    if (act && key != 0ull && (threadIdx.x & 31) < 8) atomicMax(p.keys + c, key);
+                }
+            }
+        }
+    }
 }
 
 __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_constant__ BParams p) {
@@ -630,32 +769,39 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
     __shared__ __align__(8) unsigned long long bars[kBars];
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
-    __shared__ int last_issued[2];   // per codes buffer: the last row block copied into it (-1: none)
+    __shared__ int merge_flag, epi_stop;
+    __shared__ int issued_stages;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const Geo G = geometry(p);
-    const int T = G.T1 - G.T0, nrb = (T + kRB - 1) / kRB, kwu = G.kwu;
-    unsigned char* codes = smem;
-    unsigned char* bsm = smem + 2 * kCodesBytes;
+    const int T = G.T1 - G.T0, nrb = (T + kRB - 1) / kRB, kwu = G.kwu, nstage = nrb * kwu;
+    // units per A-slot group: kPair, or 1 when kwu is odd (then group g is stage g, and stages s and
+    // s + kS still fall to the same dequantisation group)
+    const int ps = (kwu % kPair) == 0 ? kPair : 1;
+    const int npr = kwu / ps, npair = nrb * npr;
+    unsigned char* ring = smem;
+    unsigned char* bsm = smem + (size_t)kS * kStageBytes;
     const uint32_t bar = su32(bars);
     unsigned long long* tr = p.trace ? p.trace + (size_t)blockIdx.x * persist::kTraceWords : nullptr;
     persist::stamp(tr, 0);
     if (tid == 0) {
-        for (int b = 0; b < 2; ++b) {
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar + (kFull + b) * 8), "r"(kRB) : "memory");
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar + (kFree + b) * 8), "r"(kDW) : "memory");
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar + (kDFull + b) * 8) : "memory");
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 4;" ::"r"(bar + (kDFree + b) * 8) : "memory");
-            last_issued[b] = -1;
+        for (int i = 0; i < kS; ++i) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar + (kSFull + i) * 8) : "memory");
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 4;" ::"r"(bar + (kSFree + i) * 8) : "memory");
         }
-        for (int a = 0; a < kASlots; ++a) {
+        for (int a = 0; a < kA; ++a)
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 4;" ::"r"(bar + (kAFull + a) * 8) : "memory");
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar + (kAFree + a) * 8) : "memory");
+        for (int j = 0; j < kGroups; ++j)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar + (kAFreeG + j) * 8) : "memory");
+        for (int d = 0; d < 2; ++d) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar + (kDFull + d) * 8) : "memory");
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 4;" ::"r"(bar + (kDFree + d) * 8) : "memory");
         }
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar + kDone * 8) : "memory");
         abort_flag = 0;
+        issued_stages = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == kCtl) {
+    if (warp == kMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&tmem_base)),
                      "r"(kTmemCols) : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
@@ -666,11 +812,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
     const uint32_t tb = tmem_base;
     int* abt = &abort_flag;
 
-    // the first two row blocks' codes before the wait (the weights do not depend on the predecessor)
-    if (warp < kRB && lane == 0) {
-        for (int rb = 0; rb < 2 && rb < nrb; ++rb) {
-            issue_tile(p, G, codes, bar, rb, warp);
-            last_issued[rb] = rb;
+    // the first stages' codes before the wait (the weights do not depend on the predecessor);
+    // (prb, pkk) is the row block and unit of stage `issued`
+    int issued = 0, prb = 0, pkk = 0;
+    unsigned long long pol = 0;
+    if (warp == kProdWarp && lane == 0) {
+        pol = l2_evict_first();
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap)) : "memory");
+        for (; issued < kS && issued < nstage; ++issued) {
+            issue_stage(p, G, ring, bar, prb, pkk, issued, pol);
+            if (++pkk == kwu) { pkk = 0; ++prb; }
         }
     }
     pdl_wait();
@@ -682,79 +833,51 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
     persist::stamp(tr, 2);
 
     if (warp < kDW) {
-        const int q = warp & 3, sub = warp >> 2;
-        const int nks = sub < kwu ? (kwu - sub + 3) / 4 : 0;   // units of the window this warp expands
-        const int tr_ = 2 * q + (lane >> 4), rit = lane & 15;   // this thread's row: tile, row in tile
+        // ------------------------------------------------ dequantisation: stages j, j + 4, ...
+        const int q = warp & 3, j = warp >> 2;
+        const int trb = 2 * q + (lane >> 4), rit = lane & 15;   // this thread's row: tile of the block, row
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
         const __half2 off_lo = as_h2(0x64086408u), off_hi = as_h2(0x64806480u);   // 1032, 1152
-        auto epilogue = [&](int rb) {
-            const int d = rb & 1;
-            if (!tc_wait(bar + (kDFull + d) * 8, (uint32_t)(rb >> 1) & 1u, p, abt, 1000 + rb)) return false;
+        // group j takes the pairs j, j + 4, ...; pair g is units 2 pp, 2 pp + 1 (those < kwu) of row
+        // block rb = g / npr, and uses A slot g % kA
+        uint32_t nfree = 0;   // waits on this group's AFreeG so far
+        for (int g = j; g < npair; g += kGroups) {
+            const int rb = g / npr, pp = g - rb * npr, a = g % kA;
+            const int nu = ps;
+            // the slot's previous group of units (g - kA) has been multiplied; the fence orders this
+            // warp's tensor-memory stores below after the MMAs' reads that the wait has seen end
+            if (g >= kA && !warp_wait(bar + (kAFreeG + j) * 8, nfree++ & 1u, p, abt, 2000 + g)) break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            uint32_t v[32];
-            asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-                         "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-                         : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-                           "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
-                           "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]),
-                           "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]),
-                           "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
-                         : "r"(tb + lane_base + 32u * (uint32_t)d) : "memory");
-            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-            __syncwarp();
-            if (lane == 0) arrive(bar + (kDFree + d) * 8);
-            const int tl = rb * kRB + tr_;
-            if (tl < T) {
-                float4* dst = reinterpret_cast<float4*>(p.part + (((size_t)G.w * p.M.ntile + G.T0 + tl) * 16 + rit) * kMaxCols);
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    dst[c] = make_float4(__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
-                                         __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3]));
-            }
-            return true;
-        };
-        bool ok = true;
-        for (int rb = 0; rb < nrb && ok; ++rb) {
-            const int b = rb & 1;
-            // refill the other buffer with row block rb + 1 once every warp is done with rb - 1
-            if (warp < kRB && rb >= 1 && rb + 1 < nrb) {
-                if (lane == 0) {
-                    ok = tc_wait(bar + (kFree + ((rb + 1) & 1)) * 8, (uint32_t)((rb - 1) >> 1) & 1u, p, abt, 2000 + rb);
-                    if (ok) {
-                        issue_tile(p, G, codes, bar, rb + 1, warp);
-                        last_issued[(rb + 1) & 1] = rb + 1;
-                    }
-                }
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) break;
-            }
-            if (!tc_wait(bar + (kFull + b) * 8, (uint32_t)(rb >> 1) & 1u, p, abt, 3000 + rb)) {
-                ok = false;
-                break;
-            }
-            const unsigned char* cb = codes + (size_t)b * kCodesBytes;
-            for (int k2 = 0; k2 < nks; ++k2) {
-                const int kk = sub + 4 * k2, g = rb * kwu + kk, slot = g % kASlots, use = g / kASlots;
-                if (use > 0 && !tc_wait(bar + (kAFree + slot) * 8, (uint32_t)(use - 1) & 1u, p, abt, 4000 + rb)) {
+            const bool warp_rows = rb * kRB + 2 * q < T;       // the warp's first tile exists
+            const bool mine = rb * kRB + trb < T;              // this thread's tile exists
+            bool ok = true;
+            for (int u = 0; u < nu; ++u) {
+                const int st = rb * kwu + ps * pp + u, slot = st % kS;
+                if (!warp_wait(bar + (kSFull + slot) * 8, (uint32_t)(st / kS) & 1u, p, abt, 1000 + st)) {
                     ok = false;
                     break;
                 }
-                const int tl = rb * kRB + tr_;
-                const unsigned char* unit = cb + ((size_t)tr_ * kwu + kk) * kUnitBytes;
-                const uint32_t ta = tb + lane_base + kACol + 64u * (uint32_t)slot;
+                uint4 cw[4] = {};
+                uint2 sc = make_uint2(0u, 0u);
+                if (mine) {
+                    const unsigned char* unit = ring + (size_t)slot * kStageBytes + (size_t)trb * kUnitBytes;
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {   // blocks 2 half, 2 half + 1: 32 columns
-                    uint32_t v[32];
-                    if (tl < T) {
-                        const uint2 sc = *reinterpret_cast<const uint2*>(unit + 1024 + rit * 8);
+                    for (int qb = 0; qb < 4; ++qb) cw[qb] = *reinterpret_cast<const uint4*>(unit + (qb * 16 + rit) * 16);
+                    sc = *reinterpret_cast<const uint2*>(unit + 1024 + rit * 8);
+                }
+                __syncwarp();
+                if (lane == 0) arrive(bar + (kSFree + slot) * 8);   // the stage's codes are in registers
+                if (warp_rows) {
+                    const uint32_t ta = tb + lane_base + kACol + (uint32_t)(64 * kPair) * (uint32_t)a + 64u * (uint32_t)u;
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {   // blocks 2 half, 2 half + 1: 32 columns
+                        uint32_t v[32];
                         const uint32_t sw = half ? sc.y : sc.x;
 #pragma unroll
                         for (int e = 0; e < 2; ++e) {
-                            const int qb = 2 * half + e;
-                            const uint4 cw = *reinterpret_cast<const uint4*>(unit + (qb * 16 + rit) * 16);
+                            const uint4 c4 = cw[2 * half + e];
                             const __half2 d2 = e ? __high2half2(as_h2(sw)) : __low2half2(as_h2(sw));
-                            const uint32_t ws[4] = {cw.x, cw.y, cw.z, cw.w};
+                            const uint32_t ws[4] = {c4.x, c4.y, c4.z, c4.w};
 #pragma unroll
                             for (int t = 0; t < 4; ++t) {
                                 const uint32_t w = ws[t], w8 = w >> 8;
@@ -764,80 +887,152 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
                                 v[(e * 4 + t) * 4 + 3] = as_u32(__hmul2(__hsub2(as_h2((w8 & 0x00F000F0u) | 0x64006400u), off_hi), d2));
                             }
                         }
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = 0u;
+                        asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+                                     "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+                                     ::"r"(ta + 32u * (uint32_t)half), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]),
+                                       "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]),
+                                       "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+                                       "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]),
+                                       "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31]) : "memory");
                     }
-                    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
-                                 "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
-                                 ::"r"(ta + 32u * (uint32_t)half), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]),
-                                   "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]),
-                                   "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
-                                   "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]),
-                                   "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31]) : "memory");
                 }
-                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-                asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-                __syncwarp();
-                if (lane == 0) arrive(bar + (kAFull + slot) * 8);
             }
             if (!ok) break;
+            if (warp_rows) asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             __syncwarp();
-            if (lane == 0) arrive(bar + (kFree + b) * 8);   // this warp is done with the buffer
-            if (sub == 3 && rb >= 1) ok = epilogue(rb - 1);
+            if (lane == 0) arrive(bar + (kAFull + a) * 8);
         }
-        if (ok && sub == 3 && nrb > 0) epilogue(nrb - 1);
-    } else if (lane == 0) {
-        // the control warp's single issuing thread
-        const uint32_t bbase = su32(bsm);
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------ MMA issue (one lane)
+        if (lane == 0) {
+            // B descriptors: K-major core matrices, 512 bytes between the K halves of a step, 128
+            // between 8-column groups; step ks of unit kk starts (16 kk + 2 ks) x 512 bytes in
+            const uint32_t bbase = su32(bsm);
+            const unsigned long long desc0 = (unsigned long long)((bbase & 0x3FFFFu) >> 4) |
+                                             ((unsigned long long)(512u >> 4) << 16) |
+                                             ((unsigned long long)(128u >> 4) << 32) | (1ull << 46);
+            int rb = 0, pp = 0, a = 0;
+            uint32_t aph = 0;   // phase parity of the A slots' current round
+            for (int g = 0; g < npair; ++g) {
+                const int d = rb & 1, kk0 = ps * pp;
+                const int nu = ps;
+                if (pp == 0 && rb >= 2 &&
+                    !tc_wait(bar + (kDFree + d) * 8, (uint32_t)((rb >> 1) - 1) & 1u, p, abt, 3000 + rb))
+                    break;
+                if (!tc_wait(bar + (kAFull + a) * 8, aph, p, abt, 4000 + g)) break;
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const uint32_t dbase = tb + kDCols * (uint32_t)d, abase = tb + kACol + (uint32_t)(64 * kPair) * (uint32_t)a;
+                for (int u = 0; u < nu; ++u) {
+                    const unsigned long long dk = desc0 + (unsigned long long)((kk0 + u) * 16 * 32);
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t acc = (kk0 + u > 0 || ks >= kAcc) ? 1u : 0u;   // each accumulator's first MMA overwrites
+                        asm volatile("{\n .reg .pred pa;\n setp.ne.u32 pa, %4, 0;\n"
+                                     " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pa;\n}"
+                                     ::"r"(dbase + 32u * (uint32_t)(ks % kAcc)), "r"(abase + 64u * (uint32_t)u + 8u * (uint32_t)ks),
+                                       "l"(dk + (unsigned long long)(ks * 2 * 32)), "r"(kIdesc), "r"(acc) : "memory");
+                    }
+                }
+                if (g + kA < npair)   // the group that takes this slot next may write it
+                    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                                 ::"r"(bar + (kAFreeG + (g + kA) % kGroups) * 8) : "memory");
+                if (kk0 + nu == kwu)
+                    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                                 ::"r"(bar + (kDFull + d) * 8) : "memory");
+                if (++pp == npr) { pp = 0; ++rb; }
+                if (++a == kA) { a = 0; aph ^= 1u; }
+            }
+            // every MMA issued has completed before the tensor memory is released
+            asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                         ::"r"(bar + kDone * 8) : "memory");
+            tc_wait(bar + kDone * 8, 0u, p, nullptr, 7000);
+        }
+        __syncwarp();
+    } else if (warp == kProdWarp) {
+        // ------------------------------------------------ bulk copies (one lane)
+        if (lane == 0) {
+            for (; issued < nstage; ++issued) {
+                const int slot = issued % kS;
+                if (!tc_wait(bar + (kSFree + slot) * 8, (uint32_t)(issued / kS - 1) & 1u, p, abt, 5000 + issued)) break;
+                issue_stage(p, G, ring, bar, prb, pkk, slot, pol);
+                if (++pkk == kwu) { pkk = 0; ++prb; }
+            }
+            issued_stages = issued;
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ epilogue: drain, partials, ticket merge
+        const int q = warp & 3, e = q * 32 + lane;
+        const int trb = 2 * q + (lane >> 4), rit = lane & 15;
+        const uint32_t lane_base = (uint32_t)(32 * q) << 16;
         for (int rb = 0; rb < nrb; ++rb) {
             const int d = rb & 1;
-            if (rb >= 2 && !tc_wait(bar + (kDFree + d) * 8, (uint32_t)((rb - 2) >> 1) & 1u, p, abt, 5000 + rb)) break;
-            bool ok = true;
-            for (int kk = 0; kk < kwu && ok; ++kk) {
-                const int g = rb * kwu + kk, s = g % kASlots, use = g / kASlots;
-                if (!tc_wait(bar + (kAFull + s) * 8, (uint32_t)use & 1u, p, abt, 6000 + rb)) {
-                    ok = false;
-                    break;
-                }
+            // a failed wait sets the abort flag before the barrier below: every epilogue warp then
+            // sees it through epi_stop and leaves together (the named barriers need all four)
+            if (warp_wait(bar + (kDFull + d) * 8, (uint32_t)(rb >> 1) & 1u, p, abt, 6000 + rb)) {
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const int tl = rb * kRB + trb;
+                float4* dst =
+                    reinterpret_cast<float4*>(p.part + (((size_t)G.w * p.M.ntile + G.T0 + tl) * 16 + rit) * kMaxCols);
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t baddr = bbase + (uint32_t)(kk * 16 + ks * 2) * 512u;
-                    const unsigned long long desc = (unsigned long long)((baddr & 0x3FFFFu) >> 4) |
-                                                    ((unsigned long long)(512u >> 4) << 16) |
-                                                    ((unsigned long long)(128u >> 4) << 32) | (1ull << 46);
-                    const uint32_t acc = (kk | ks) ? 1u : 0u;
-                    asm volatile("{\n .reg .pred pa;\n setp.ne.u32 pa, %4, 0;\n"
-                                 " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pa;\n}"
-                                 ::"r"(tb + 32u * (uint32_t)d), "r"(tb + kACol + 64u * (uint32_t)s + 8u * (uint32_t)ks),
-                                   "l"(desc), "r"(kIdesc), "r"(acc) : "memory");
+                for (int h = 0; h < 2; ++h) {   // 16 batch columns at a time
+                    float f[16];
+#pragma unroll
+                    for (int ac = 0; ac < kAcc; ++ac) {   // the set's accumulators, summed in order
+                        uint32_t v[16];
+                        tmem_ld16(tb + lane_base + kDCols * (uint32_t)d + 32u * (uint32_t)ac + 16u * (uint32_t)h, v);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) f[i] = ac == 0 ? __uint_as_float(v[i]) : f[i] + __uint_as_float(v[i]);
+                    }
+                    if (tl < T) {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) dst[4 * h + c] = make_float4(f[4 * c], f[4 * c + 1], f[4 * c + 2], f[4 * c + 3]);
+                    }
                 }
-                asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-                             ::"r"(bar + (kAFree + s) * 8) : "memory");
+                asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) arrive(bar + (kDFree + d) * 8);
+                __threadfence();   // this thread's partial stores visible at gpu scope before the ticket
             }
-            if (!ok) break;
-            asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-                         ::"r"(bar + (kDFull + d) * 8) : "memory");
+            epi_sync();   // every epilogue thread's fenced partial stores before thread 0's ticket below
+            if (e == 0) {
+                const int stop = *reinterpret_cast<volatile int*>(abt);
+                epi_stop = stop;
+                int last = 1;   // one window: this CTA has the whole sum
+                if (!p.kernel_merge && G.nwin > 1) last = 0;   // merge_kernel adds the windows
+                else if (!stop && G.nwin > 1) {
+                    int t;
+                    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
+                                 : "=r"(t) : "l"(p.tickets + (size_t)G.rg * p.maxrb + rb) : "memory");
+                    last = t == G.nwin - 1;
+                }
+                merge_flag = last;
+            }
+            epi_sync();
+            if (epi_stop) break;
+            if (merge_flag) {
+                if (p.epi == QL_EPI_SILU_MUL) merge_rb<true>(p, G, rb, e);
+                else merge_rb<false>(p, G, rb, e);
+                if (e == 0 && G.nwin > 1) p.tickets[(size_t)G.rg * p.maxrb + rb] = 0;   // re-armed for the next call
+            }
+            epi_sync();   // merge_flag and epi_stop are read by every epilogue thread before they change
         }
-        // every MMA issued has completed before the tensor memory is released
-        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-                     ::"r"(bar + kDone * 8) : "memory");
-        tc_wait(bar + kDone * 8, 0u, p, nullptr, 7000);
     }
     persist::stamp(tr, 3);
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
     persist::stamp(tr, 4);
-    if (warp == kCtl) {
+    if (warp == kMmaWarp) {
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tb), "r"(kTmemCols) : "memory");
     }
-    // copies still in flight (only after an abort): let them land before the CTA leaves (bounded)
-    if (tid == 0) {
-        for (int b = 0; b < 2; ++b)
-            if (last_issued[b] >= 0)
-                tc_wait(bar + (kFull + b) * 8, (uint32_t)(last_issued[b] >> 1) & 1u, p, nullptr, 8000);
+    // copies still in flight (only after an abort): the last use of each slot lands before the
+    // CTA leaves (bounded)
+    if (warp == kProdWarp && lane == 0) {
+        const int n = issued_stages;
+        for (int s = n - kS < 0 ? 0 : n - kS; s < n; ++s)
+            tc_wait(bar + (kSFull + s % kS) * 8, (uint32_t)(s / kS) & 1u, p, nullptr, 8000 + s);
     }
     persist::stamp(tr, 5);
     if (tr != nullptr && tid == 0) tr[6] = tr[7] = 0ull;
@@ -877,12 +1072,60 @@ static void batched_split(int nblk, int ntile, int sms, int& nwin, int& ngr) {
     if (ngr < 1) ngr = 1;
 }
 
-// Workspace: the windows' partial sums.
+// Workspace: a fixed region of row-block tickets (tcgen05 form; zero between calls, whatever
+// the shape, so that calls of different shapes can take turns on one workspace), then the
+// windows' partial sums.
+constexpr size_t kTicketInts = 65536;
+struct BatchedLayout {
+    int nwin, ngr, maxrb;
+    size_t part_off, total;
+};
+static BatchedLayout batched_layout(int ntile, int nblk) {
+    BatchedLayout L = {};
+    batched_split(nblk, ntile, num_sms(), L.nwin, L.ngr);
+    const int max_tiles = (ntile + L.ngr - 1) / L.ngr;
+    L.maxrb = (max_tiles + batched::tc::kRB - 1) / batched::tc::kRB;
+    L.part_off = kTicketInts * sizeof(int);
+    L.total = L.part_off + (size_t)L.nwin * ntile * 16 * batched::kMaxCols * sizeof(float);
+    if ((size_t)L.ngr * L.maxrb > kTicketInts) L.total = 0;   // more row blocks than tickets
+    return L;
+}
+
 size_t batched_gemv_workspace_bytes(int rows, int nblk, int silu) {
     const int ntile = silu ? (rows / 2 + 7) / 8 : (rows + 15) / 16;
-    int nwin, ngr;
-    batched_split(nblk, ntile, num_sms(), nwin, ngr);
-    return (size_t)nwin * ntile * 16 * batched::kMaxCols * sizeof(float);
+    return batched_layout(ntile, nblk).total;
+}
+
+// cuTensorMapEncodeTiled from the driver (no link-time dependency on libcuda).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+static EncodeTiledFn encode_tiled() {
+    static const EncodeTiledFn fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            f = nullptr;
+        return reinterpret_cast<EncodeTiledFn>(f);
+    }();
+    return fn;
+}
+
+// The stream of M as a 3-D tensor for the tcgen05 form's stage copies: [tile][unit][144 x 8 bytes]
+// (a unit is 1152 bytes), boxes of one unit of 8 consecutive tiles.
+static int stream_tensor_map(const PMat& M, CUtensorMap* map) {
+    const EncodeTiledFn enc = encode_tiled();
+    if (enc == nullptr) return set_error(QL_ECUDA, "batched gemv: cuTensorMapEncodeTiled is not available");
+    const int nst = M.nblk / batched::kUnitBlocks;
+    const cuuint64_t dims[3] = {(cuuint64_t)(batched::kUnitBytes / 8), (cuuint64_t)nst, (cuuint64_t)M.ntile};
+    const cuuint64_t strides[2] = {(cuuint64_t)batched::kUnitBytes, (cuuint64_t)nst * batched::kUnitBytes};
+    const cuuint32_t box[3] = {(cuuint32_t)(batched::kUnitBytes / 8), 1u, (cuuint32_t)batched::tc::kRB};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, const_cast<uint8_t*>(M.stream), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? QL_OK : set_error(QL_ECUDA, "batched gemv: tensor map encoding failed (" + std::to_string((int)r) + ")");
 }
 
 // The tensor-core form of batch 3-32 (process-wide): mma.sync by default (measured faster on the
@@ -934,15 +1177,15 @@ int batched_gemv_launch(const StreamGemvArgs& a, cudaStream_t s, bool pdl) {
     QL_REQUIRE(a.batch >= 1 && a.batch <= batched::kMaxCols, "batched gemv: batch must be in [1, 32]");
     QL_REQUIRE(a.rms ? (a.xf && a.norm_w && a.xn) : a.x16 != nullptr, "batched gemv: null input");
     QL_REQUIRE(a.y && a.sync && a.workspace, "batched gemv: null output or workspace");
-    QL_REQUIRE(a.workspace_bytes >= batched_gemv_workspace_bytes(a.M.rows, a.M.nblk, a.M.silu),
-               "batched gemv: workspace too small");
+    const size_t need = batched_gemv_workspace_bytes(a.M.rows, a.M.nblk, a.M.silu);
+    QL_REQUIRE(need > 0 && a.workspace_bytes >= need, "batched gemv: workspace too small");
     QL_REQUIRE(a.epilogue != kEpiArgmax || a.keys, "batched gemv: argmax needs keys");
     QL_REQUIRE((a.epilogue == QL_EPI_SILU_MUL) == (a.M.silu != 0), "batched gemv: SiLU*up needs a matrix packed for it");
     DevError* err = device_error_record();
     if (!err) return set_error(QL_ECUDA, "batched gemv: no device error record");
     if (int rc = batched_gemv_prepare()) return rc;
-    int nwin, ngr;
-    batched_split(a.M.nblk, a.M.ntile, num_sms(), nwin, ngr);
+    const BatchedLayout L = batched_layout(a.M.ntile, a.M.nblk);
+    const int nwin = L.nwin, ngr = L.ngr;
     batched::BParams p = {};
     p.M = a.M;
     p.B = a.batch;
@@ -955,8 +1198,10 @@ int batched_gemv_launch(const StreamGemvArgs& a, cudaStream_t s, bool pdl) {
     p.sync = a.sync;
     p.err = err;
     p.timeout_ns = 2000000000ull;
-    p.part = static_cast<float*>(a.workspace);
+    p.part = reinterpret_cast<float*>(static_cast<char*>(a.workspace) + L.part_off);
     p.ngr = ngr;
+    p.tickets = static_cast<int*>(a.workspace);
+    p.maxrb = L.maxrb;
     p.trace = a.trace;
     if (a.rms) {   // the RMSNorm'd activations of every column, once, for all CTAs
         const cudaError_t e0 = ql::launch(batched::rms_norm_kernel, dim3(a.batch), dim3(batched::kNormT), 0, s, pdl,
@@ -965,14 +1210,27 @@ int batched_gemv_launch(const StreamGemvArgs& a, cudaStream_t s, bool pdl) {
     }
     const int nt = (a.batch + 7) / 8, grid = nwin * ngr;
     cudaError_t e;
-    if (use_tc())
+    if (use_tc()) {
+        // the K windows merged by merge_kernel (default: measured faster on the batch-32 step than
+        // the in-kernel ticket merge, whose merging CTA becomes the launch's tail);
+        // QL_TC_KERNEL_MERGE=1 merges them inside the kernel
+        static const int env_km = [] {
+            const char* ev = std::getenv("QL_TC_KERNEL_MERGE");
+            return ev != nullptr && std::atoi(ev) != 0 ? 1 : 0;
+        }();
+        p.kernel_merge = env_km;
+        if (int rc = stream_tensor_map(a.M, &p.tmap)) return rc;
         e = ql::launch(batched::tc::gemv_tc_kernel, dim3(grid), dim3(batched::tc::kThreads), batched::tc::kSmem, s,
                        pdl, p);
-    else
-        e = nt == 1   ? batched::run<1>(true, &p, grid, s, pdl)
-            : nt == 2 ? batched::run<2>(true, &p, grid, s, pdl)
-            : nt == 3 ? batched::run<3>(true, &p, grid, s, pdl)
-                      : batched::run<4>(true, &p, grid, s, pdl);
+        if (e != cudaSuccess) return cuda_error(e, "batched gemv launch");
+        if (env_km || nwin == 1) return QL_OK;
+        e = ql::launch(batched::merge_kernel, dim3(2 * num_sms()), dim3(batched::kMergeT), 0, s, pdl, p);
+        return e == cudaSuccess ? QL_OK : cuda_error(e, "batched gemv merge launch");
+    }
+    e = nt == 1   ? batched::run<1>(true, &p, grid, s, pdl)
+        : nt == 2 ? batched::run<2>(true, &p, grid, s, pdl)
+        : nt == 3 ? batched::run<3>(true, &p, grid, s, pdl)
+                  : batched::run<4>(true, &p, grid, s, pdl);
     if (e != cudaSuccess) return cuda_error(e, "batched gemv launch");
     // the windows added up and the epilogue, over every SM
     e = ql::launch(batched::merge_kernel, dim3(2 * num_sms()), dim3(batched::kMergeT), 0, s, pdl, p);

@@ -752,6 +752,8 @@ int setup_persist(ql_model* m) {
         }
         A(&m->bws, m->bws_bytes);
         if (rc != QL_OK) return rc;
+        // the tcgen05 form's row-block tickets start at zero (each call leaves them zero)
+        if (cudaMemset(m->bws, 0, m->bws_bytes) != cudaSuccess) return set_error(QL_ECUDA, "ql_model_create: memset");
     }
     cudaError_t e = cudaMemcpy(m->players, hl.data(), hl.size() * sizeof(PLayer), cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemset(m->ptickets, 0, (size_t)maxb * d.n_kv_heads * 4);

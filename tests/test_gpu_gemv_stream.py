@@ -102,9 +102,9 @@ def run(w, x, epilogue, residual=None):
     else:
         y = torch.full((B, rows), float("nan"), dtype=torch.float32, device="cuda")
     ws = None
-    if B > 2:   # scratch: its contents do not matter
-        ws = torch.full((ql.ql_gemv_q4_0_stream_workspace_bytes(rows, cols, silu),), 0x7F, dtype=torch.uint8,
-                        device="cuda")
+    if B > 2:   # scratch, zero-filled before its first use (the calls keep it valid)
+        ws = torch.zeros((ql.ql_gemv_q4_0_stream_workspace_bytes(rows, cols, silu),), dtype=torch.uint8,
+                         device="cuda")
     y0 = y.clone()
     ql.ql_gemv_q4_0_stream(buf, rows, cols, dev(x), B, y, epilogue, ws)
     torch.cuda.synchronize()
