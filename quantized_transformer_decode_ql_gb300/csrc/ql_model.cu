@@ -27,6 +27,7 @@
 #include <map>
 #include <vector>
 
+#include "ql_chunk_attn.h"
 #include "ql_internal.h"
 
 struct ql_model {
@@ -85,6 +86,8 @@ struct ql_model {
     int32_t* pbt = nullptr;      // [max_batch][max_blocks_per_seq]
     int32_t* ppos = nullptr;     // [max_batch]
     int32_t* plen = nullptr;     // [max_batch]
+    void* cws = nullptr;         // prefill chunk attention: the splits' partials
+    size_t cws_bytes = 0;
 };
 
 namespace ql {
@@ -586,24 +589,24 @@ int run_prefill(ql_model* m, const int32_t* tokens, int T, int32_t* position, co
         ra.num_blocks = d.num_blocks;
         ra.max_position = d.max_blocks_per_seq * d.block_size;
         if ((rc = rope_launch(ra, s, pdl)) != QL_OK) return rc;
-        AttnArgs at = {};
-        at.q = m->q16;
-        at.k_pool = ra.k_pool;
-        at.v_pool = ra.v_pool;
-        at.block_tables = m->pbt;
-        at.context_lens = m->plen;
-        at.batch = T;
-        at.n_heads = nh;
-        at.n_kv_heads = nkv;
-        at.head_dim = hd;
-        at.block_size = d.block_size;
-        at.max_blocks_per_seq = maxb;
-        at.num_blocks = d.num_blocks;
-        at.scale = 1.0f / sqrtf((float)hd);
-        at.out = m->attn;
-        at.workspace = m->attn_ws;
-        at.workspace_bytes = m->attn_ws_bytes;
-        if ((rc = attn_launch(at, s, pdl)) != QL_OK) return rc;
+        // the chunk's T tokens against the cache in one pass (each K/V block read once)
+        ChunkAttnArgs ca = {};
+        ca.q = m->q16;
+        ca.k_pool = ra.k_pool;
+        ca.v_pool = ra.v_pool;
+        ca.block_table = m->pbt;   // row 0: the sequence's table
+        ca.position = m->ppos;     // [0] = the chunk's first position
+        ca.T = T;
+        ca.n_heads = nh;
+        ca.n_kv_heads = nkv;
+        ca.head_dim = hd;
+        ca.max_blocks_per_seq = maxb;
+        ca.num_blocks = (int)d.num_blocks;
+        ca.scale = 1.0f / sqrtf((float)hd);
+        ca.out = m->attn;
+        ca.workspace = m->cws;
+        ca.workspace_bytes = m->cws_bytes;
+        if ((rc = chunk_attn_launch(ca, s, pdl)) != QL_OK) return rc;
         if ((rc = sg(Ms[1], QL_EPI_ADD_RESIDUAL, false, nullptr, m->attn, nullptr, m->x, (int)d.hidden, T)) != QL_OK)
             return rc;
         if ((rc = sg(Ms[2], QL_EPI_SILU_MUL, true, m->x, nullptr, L.ffn_norm, m->act, (int)d.intermediate, T)) != QL_OK)
@@ -878,6 +881,14 @@ extern "C" int ql_model_create(const ql_model_desc* desc, ql_model** out) {
         if (need > m->attn_ws_bytes) m->attn_ws_bytes = need;
     }
     A(&m->attn_ws, m->attn_ws_bytes);
+    {   // prefill chunks of up to min(32, max_batch) tokens
+        const int tmax = (int)(B < 32 ? B : 32);
+        for (int t = 1; t <= tmax; ++t) {
+            const size_t need = chunk_attn_workspace_bytes(t, (int)d.n_heads, (int)d.n_kv_heads, (int)d.head_dim);
+            if (need > m->cws_bytes) m->cws_bytes = need;
+        }
+        A(&m->cws, m->cws_bytes);
+    }
     if (rc == QL_OK) {
         std::vector<float> hc(max_pos * (d.head_dim / 2)), hs(hc.size());
         rc = ql_rope_tables(hc.data(), hs.data(), max_pos, (int)d.head_dim, d.rope_theta);
