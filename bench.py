@@ -734,6 +734,38 @@ def gpu_arm_e32(args, rank, world, local_rank):
     return line
 
 
+def gpu_arm_prefill(args, rank, world, local_rank):
+    """The chunked prefill workload as its own line (``--config prefill``): one 2048-token prompt
+    in 32-token chunks on the 8B shape, timed as in the default line's prefill_8b key."""
+    import torch
+
+    from quantized_transformer_decode_ql_gb300 import build as qbuild
+    if rank == 0 or world == 1:
+        qbuild.build()
+    barrier(world)
+    from quantized_transformer_decode_ql_gb300.model import DeviceModel
+
+    torch.cuda.set_device(local_rank)
+    cfg = ql_inputs.QWEN3_8B
+    gm = DeviceModel.from_layer_fn(cfg, device_tensor_fn(cfg, seed=0), num_blocks=16, max_batch=1,
+                                   max_blocks_per_seq=4)
+    s = torch.cuda.Stream()
+    clock = ClockSampler(local_rank)
+    r = prefill_run(gm, cfg, s)
+    clocks = clock.stop()
+    gm.close()
+    value = sum_over_ranks(r.pop("value"), world)
+    line = {"metric": "prefill prompt tokens/s at 1 GB300 (q4_0 weights, chunks of 32)", "value": value,
+            "unit": r.pop("unit"), "n_gpus": world, "steps": 2048 // 32, "warmup": 2048 // 32,
+            "ms_per_step": r["ms_per_chunk"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "q4_0 weights, f16 act/KV, f32 accum", "data": "synthetic (seeded random-init weights, random prompt)",
+            "config": {"workload": r.pop("workload"), "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2 (4.6 GB of weights streamed per chunk)"},
+            "clocks": clocks}
+    line.update(r)
+    return line
+
+
 STEP_KERNELS = {"auto": 0, "launches": 1, "persistent": 2}
 
 
@@ -1125,7 +1157,7 @@ def main():
     ap.add_argument("--steps", type=int, default=256)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ql", choices=["ql", "reference"])
-    ap.add_argument("--config", default="e1", choices=["e1", "e32"])
+    ap.add_argument("--config", default="e1", choices=["e1", "e32", "prefill"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e32", action="store_true", help="leave the batch-32 sub-results out of the default line")
     ap.add_argument("--kv", default="f16", choices=["f16", "q8q5"], help="--config e32: KV cache format")
@@ -1173,6 +1205,11 @@ def main():
     assert args.warmup >= 3, "at least 3 warm-up steps"
     if args.config == "e32":
         line = gpu_arm_e32(args, rank, world, local_rank)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        return
+    if args.config == "prefill":
+        line = gpu_arm_prefill(args, rank, world, local_rank)
         if rank == 0:
             print(json.dumps(line), flush=True)
         return
