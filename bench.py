@@ -401,8 +401,9 @@ def gpu_arm(args, rank, world, local_rank):
     ctx_avg = CTX + 1 + (steps - 1) / 2.0
     step_bytes = wbytes + B * (kv_tok * ctx_avg + kv_tok + cfg.hidden * 4 + cfg.vocab * 4)
 
-    # ---- end to end through the public API with host buffers: per step, H2D of the step's
-    # token ids from pinned memory, one graph replay, D2H of the next tokens, host sync
+    # ---- end to end through the C ABI with host buffers: per step one ql_decode_graph_step_host
+    # call (H2D of the step's token ids from pinned memory, one graph replay, D2H of the next
+    # tokens, stream sync)
     h_tok = torch.empty((B,), dtype=torch.int32, pin_memory=True)
     h_out = torch.empty((B,), dtype=torch.int32, pin_memory=True)
     h_tok.copy_(first.cpu())
@@ -411,11 +412,7 @@ def gpu_arm(args, rank, world, local_rank):
     s.synchronize()
     t0 = time.perf_counter()
     for _ in range(steps):
-        with torch.cuda.stream(s):
-            tokens.copy_(h_tok, non_blocking=True)
-            gm.ql_decode_graph_replay(B, 1, s)
-            h_out.copy_(tokens, non_blocking=True)
-        s.synchronize()
+        gm.ql_decode_graph_step_host(B, h_tok, h_out, s)
         h_tok.copy_(h_out)
     e2e_s = time.perf_counter() - t0
     e2e_s = max_over_ranks(e2e_s, world)
@@ -469,7 +466,7 @@ def gpu_arm(args, rank, world, local_rank):
         "kernels": kernels,
         "clocks": clocks,
         "e2e": {"value": round(tok_total / e2e_s, 2), "unit": "tokens/s", "h2d_bytes_per_step": 4 * B,
-                "d2h_bytes_per_step": 4 * B},
+                "d2h_bytes_per_step": 4 * B, "api": "ql_decode_graph_step_host (host token buffers)"},
         "gpu_launches": kernels_per_step * steps,
         "setup_s": round(setup_s, 1),
         "tokens_head": toks[0, CTX + 1: CTX + 9].tolist(),

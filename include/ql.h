@@ -486,6 +486,14 @@ int ql_decode_graph_capture(ql_model* m, const ql_step_args* args, void* stream)
 /* Replay the graph of this batch n_steps times back to back ([IL] run_graph).
  * QL_ESTATE if no graph of that batch was captured.                                    */
 int ql_decode_graph_replay(ql_model* m, int64_t batch, int n_steps, void* stream);
+/* One decode step from host buffers: copies h_tokens (int32 [batch], host; pinned memory keeps
+ * the copy asynchronous) into the tokens buffer the graph of this batch was captured with,
+ * replays the graph once, copies its next_tokens buffer into h_next_tokens (int32 [batch],
+ * host) and waits for the stream, so that h_next_tokens holds the step's greedy tokens on
+ * return. The other step buffers (positions, tables, logits) stay on the device and advance as
+ * with ql_decode_graph_replay. QL_ESTATE if no graph of that batch was captured.           */
+int ql_decode_graph_step_host(ql_model* m, int64_t batch, const int32_t* h_tokens, int32_t* h_next_tokens,
+                              void* stream);
 /* Chunked prefill of one sequence. [IL] runs a prompt as sequential decode (its module doc);
  * here a chunk of n_tokens prompt tokens (d_tokens int32 [n_tokens], device) at positions
  * *d_position .. *d_position + n_tokens - 1 goes through every layer together: the GEMVs take

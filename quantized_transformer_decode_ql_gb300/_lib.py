@@ -111,6 +111,7 @@ SIGNATURES = {
     "ql_decode_step": (c_int, [c_void_p, POINTER(StepArgs), c_void_p]),
     "ql_decode_graph_capture": (c_int, [c_void_p, POINTER(StepArgs), c_void_p]),
     "ql_decode_graph_replay": (c_int, [c_void_p, c_int64, c_int, c_void_p]),
+    "ql_decode_graph_step_host": (c_int, [c_void_p, c_int64, c_void_p, c_void_p, c_void_p]),
     "ql_check_device_error": (c_int, [c_void_p]),
     "ql_block_pool_create": (c_int, [c_int64, POINTER(c_void_p)]),
     "ql_block_pool_destroy": (c_int, [c_void_p]),

@@ -48,6 +48,7 @@ struct ql_model {
     size_t attn_ws_bytes = 0;
     std::vector<void*> owned;
     std::map<int64_t, cudaGraphExec_t> graphs;
+    std::map<int64_t, ql_step_args> graph_args;   // the device buffers each graph was captured with
     // L2 prefetch of the following GEMV's weights by every kernel (A/B switch QL_NEXT_PREFETCH=1).
     // Off by default: measured slower (kernels that issue megabytes of prefetch stall).
     bool next_prefetch = false;
@@ -992,6 +993,24 @@ extern "C" int ql_decode_graph_capture(ql_model* m, const ql_step_args* args, vo
     auto it = m->graphs.find(args->batch);
     if (it != m->graphs.end()) cudaGraphExecDestroy(it->second);
     m->graphs[args->batch] = ex;
+    m->graph_args[args->batch] = *args;
+    return QL_OK;
+}
+
+extern "C" int ql_decode_graph_step_host(ql_model* m, int64_t batch, const int32_t* h_tokens, int32_t* h_next_tokens,
+                                         void* stream) {
+    if (!m) return set_error(QL_EINVAL, "ql_decode_graph_step_host: null model");
+    if (!h_tokens || !h_next_tokens) return set_error(QL_EINVAL, "ql_decode_graph_step_host: null host buffer");
+    auto it = m->graphs.find(batch);
+    if (it == m->graphs.end())
+        return set_error(QL_ESTATE, "ql_decode_graph_step_host: no graph captured for batch " + std::to_string(batch));
+    const ql_step_args& a = m->graph_args[batch];
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t bytes = (size_t)batch * sizeof(int32_t);
+    QL_TRY_CUDA(cudaMemcpyAsync(const_cast<int32_t*>(a.tokens), h_tokens, bytes, cudaMemcpyHostToDevice, s));
+    QL_TRY_CUDA(cudaGraphLaunch(it->second, s));
+    QL_TRY_CUDA(cudaMemcpyAsync(h_next_tokens, a.next_tokens, bytes, cudaMemcpyDeviceToHost, s));
+    QL_TRY_CUDA(cudaStreamSynchronize(s));
     return QL_OK;
 }
 

@@ -216,6 +216,13 @@ class DeviceModel:
     def ql_decode_graph_replay(self, batch: int, n_steps: int, stream=None):
         check(lib().ql_decode_graph_replay(self.handle, batch, n_steps, stream_ptr(stream)))
 
+    def ql_decode_graph_step_host(self, batch: int, h_tokens, h_next_tokens, stream=None):
+        """One replayed step from host buffers (int32 CPU tensors, pinned for asynchronous
+        copies): h_tokens in, the step's greedy tokens out in h_next_tokens on return."""
+        assert h_tokens.device.type == "cpu" and h_next_tokens.device.type == "cpu"
+        check(lib().ql_decode_graph_step_host(self.handle, batch, h_tokens.data_ptr(), h_next_tokens.data_ptr(),
+                                              stream_ptr(stream)))
+
     def ql_prefill_chunk(self, tokens, position, block_table, logits=None, next_token=None, stream=None):
         """Run the prompt tokens ``tokens`` (int32 [T] device, T <= 32) of one sequence as one
         chunk at ``position`` (int32 [1] device, advanced by T) through the sequence's

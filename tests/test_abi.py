@@ -136,6 +136,7 @@ def test_argument_validation_without_gpu(ql):
                                 None) == ql.QL_EINVAL
     assert L.ql_model_create(None, None) == ql.QL_EINVAL
     assert L.ql_decode_graph_replay(None, 1, 1, None) == ql.QL_EINVAL
+    assert L.ql_decode_graph_step_host(None, 1, None, None, None) == ql.QL_EINVAL
     assert L.ql_model_set_option(None, ql.QL_OPT_STEP_KERNEL, ql.QL_STEP_AUTO) == ql.QL_EINVAL
     assert L.ql_model_persistent_max_batch(None) == 0
     assert L.ql_q4_0_stream_pack(None, None, 16, 128, 0, None, None) == ql.QL_EINVAL

@@ -124,6 +124,39 @@ def test_graph_replay_equals_eager(tiny, B):
     assert np.all(runs[0][0][:, 1:13] >= 0)
 
 
+def test_graph_step_from_host_buffers(tiny):
+    """ql_decode_graph_step_host (token ids in from pinned host memory, next tokens back) gives
+    the same tokens, step for step, as replays of the same graph on device buffers."""
+    gm, _ = tiny
+    B = 2
+    start = ql_inputs.prompt_tokens(B, CFG.vocab, seed=11).astype(np.int32)
+    seqs = []
+    for mode in ("device", "host"):
+        tokens = dev(start)
+        positions = torch.zeros(B, dtype=torch.int32, device="cuda")
+        bt = dev(slot_tables(B, 4, seed=23))
+        args = gm.step_args(tokens, positions, bt, tokens)
+        s = torch.cuda.Stream()
+        gm.ql_decode_graph_capture(args, s)
+        got = []
+        if mode == "device":
+            for _ in range(10):
+                gm.ql_decode_graph_replay(B, 1, s)
+                s.synchronize()
+                got.append(tokens.cpu().numpy().copy())
+        else:
+            h_in = torch.from_numpy(start.copy()).pin_memory()
+            h_out = torch.zeros(B, dtype=torch.int32).pin_memory()
+            for _ in range(10):
+                gm.ql_decode_graph_step_host(B, h_in, h_out, s)
+                got.append(h_out.numpy().copy())
+                h_in.copy_(h_out)
+        seqs.append(np.stack(got))
+        assert np.all(positions.cpu().numpy() == 10)
+    assert np.array_equal(seqs[0], seqs[1])
+    gm.ql_check_device_error()
+
+
 def test_identical_slots_equal_batch_one(tiny):
     """Identical slots give bit-identical logits within a batch (the step treats the batch
     columns independently); across batch sizes and step kernels the f32 sums are taken in
