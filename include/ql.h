@@ -233,6 +233,22 @@ int ql_paged_attn_decode(const void* d_q, const void* d_k_pool, const void* d_v_
                          float scale, void* d_out, void* d_workspace,
                          size_t workspace_bytes, void* stream);
 
+/* Causal attention of a prefill chunk ([IL] prefill as sequential decode: token t of the chunk,
+ * at position *d_position + t, attends keys 0 .. *d_position + t): d_q f16 [n_tokens][n_heads]
+ * [head_dim] (normalised and rotated), the sequence's K/V rows for positions 0 ..
+ * *d_position + n_tokens - 1 already in d_k_pool / d_v_pool (layout as ql_paged_attn_decode),
+ * d_block_table int32 [max_blocks_per_seq] of the sequence, d_position int32 [1] (device). Each
+ * K/V block is read once for all the chunk's tokens (the chunk's tokens x query heads of a kv head
+ * are the MMA rows); the block table's splits are merged by a second kernel. d_out f16
+ * [n_tokens][n_heads * head_dim]. d_workspace: ql_paged_attn_chunk_workspace_bytes, contents
+ * need not be initialised. Tolerance as ql_paged_attn_decode. Block ids out of range are
+ * recorded in the device error record and their keys skipped. 1 <= n_tokens <= 256.       */
+size_t ql_paged_attn_chunk_workspace_bytes(int64_t n_tokens, int n_heads, int n_kv_heads, int head_dim);
+int ql_paged_attn_chunk(const void* d_q, const void* d_k_pool, const void* d_v_pool, const int32_t* d_block_table,
+                        const int32_t* d_position, int64_t n_tokens, int n_heads, int n_kv_heads, int head_dim,
+                        int block_size, int64_t max_blocks_per_seq, int64_t num_blocks, float scale, void* d_out,
+                        void* d_workspace, size_t workspace_bytes, void* stream);
+
 /* The same attention without a caller-supplied workspace, for callers that cannot allocate
  * device memory: for example a plugin inside a host application whose own pool owns all
  * device memory, or a latency-critical loop that cannot afford cudaMalloc/cudaFree (they can

@@ -24,6 +24,7 @@ __all__ = [
     "ql_q4_0_stream_bytes", "ql_q4_0_stream_pack", "ql_gemv_q4_0_stream",
     "ql_gemv_q4_0_stream_workspace_bytes", "ql_set_batched_gemv_form", "ql_set_gemv_activation_form",
     "ql_paged_attn_workspace_bytes", "ql_paged_attn_decode", "ql_paged_attn_decode_noalloc",
+    "ql_paged_attn_chunk_workspace_bytes", "ql_paged_attn_chunk",
     "ql_kvq_record_bytes", "ql_kvq_write", "ql_paged_attn_decode_kvq",
     "ql_set_attn_merge_form", "ql_paged_attn_merge_form",
     "ql_kv_q8_0_row_bytes", "ql_kv_q5_1_row_bytes", "ql_kv_quantize_q8_0", "ql_kv_dequantize_q8_0",
@@ -160,6 +161,20 @@ def ql_gemv_q4_0_stream(w_stream, rows, cols, x, batch, y, epilogue=QL_EPI_NONE,
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     check(lib().ql_gemv_q4_0_stream(ptr(w_stream), rows, cols, ptr(x), batch, ptr(y), epilogue,
                                     ptr(workspace), nbytes, stream_ptr(stream)))
+
+
+def ql_paged_attn_chunk_workspace_bytes(n_tokens, n_heads, n_kv_heads, head_dim):
+    return int(lib().ql_paged_attn_chunk_workspace_bytes(n_tokens, n_heads, n_kv_heads, head_dim))
+
+
+def ql_paged_attn_chunk(q, k_pool, v_pool, block_table, position, n_tokens, n_heads, n_kv_heads, head_dim,
+                        block_size, max_blocks_per_seq, num_blocks, scale, out, workspace, stream=None):
+    """Causal attention of a prefill chunk: ``q`` f16 [n_tokens][n_heads][head_dim] at positions
+    ``position[0] + t`` (int32 [1] device) over the sequence's ``block_table``."""
+    check(lib().ql_paged_attn_chunk(ptr(q), ptr(k_pool), ptr(v_pool), ptr(block_table), ptr(position), n_tokens,
+                                    n_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks,
+                                    scale, ptr(out), ptr(workspace), workspace.numel() * workspace.element_size(),
+                                    stream_ptr(stream)))
 
 
 def ql_paged_attn_workspace_bytes(batch, n_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq):

@@ -81,6 +81,10 @@ SIGNATURES = {
     "ql_paged_attn_decode_kvq": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int, c_int, c_int, c_int,
                                          c_int64, c_int64, c_float, c_void_p, c_void_p, c_size_t, c_void_p]),
     "ql_paged_attn_workspace_bytes": (c_size_t, [c_int64, c_int, c_int, c_int, c_int, c_int64]),
+    "ql_paged_attn_chunk_workspace_bytes": (c_size_t, [c_int64, c_int, c_int, c_int]),
+    "ql_paged_attn_chunk": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int, c_int,
+                                    c_int, c_int, c_int64, c_int64, c_float, c_void_p, c_void_p, c_size_t,
+                                    c_void_p]),
     "ql_paged_attn_decode": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int64,
                                      c_int, c_int, c_int, c_int, c_int64, c_int64, c_float,
                                      c_void_p, c_void_p, c_size_t, c_void_p]),

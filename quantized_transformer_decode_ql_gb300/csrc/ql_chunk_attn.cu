@@ -370,3 +370,41 @@ int chunk_attn_launch(const ChunkAttnArgs& a, cudaStream_t st, bool pdl) {
 }
 
 }  // namespace ql
+
+extern "C" size_t ql_paged_attn_chunk_workspace_bytes(int64_t n_tokens, int n_heads, int n_kv_heads, int head_dim) {
+    if (n_tokens < 1 || n_tokens > 256 || (head_dim != 64 && head_dim != 128)) return 0;
+    return ql::chunk_attn_workspace_bytes((int)n_tokens, n_heads, n_kv_heads, head_dim);
+}
+
+extern "C" int ql_paged_attn_chunk(const void* d_q, const void* d_k_pool, const void* d_v_pool,
+                                   const int32_t* d_block_table, const int32_t* d_position, int64_t n_tokens,
+                                   int n_heads, int n_kv_heads, int head_dim, int block_size,
+                                   int64_t max_blocks_per_seq, int64_t num_blocks, float scale, void* d_out,
+                                   void* d_workspace, size_t workspace_bytes, void* stream) {
+    using namespace ql;
+    QL_REQUIRE(block_size == 16, "ql_paged_attn_chunk: block_size must be 16");
+    QL_REQUIRE(max_blocks_per_seq >= 1 && max_blocks_per_seq < (1ll << 26) && num_blocks >= 1 &&
+                   num_blocks < (1ll << 31),
+               "ql_paged_attn_chunk: bad table or pool size");
+    QL_REQUIRE(n_tokens >= 1 && n_tokens <= 256, "ql_paged_attn_chunk: 1..256 tokens");
+    QL_REQUIRE((reinterpret_cast<uintptr_t>(d_k_pool) & 15) == 0 && (reinterpret_cast<uintptr_t>(d_v_pool) & 15) == 0 &&
+                   (reinterpret_cast<uintptr_t>(d_q) & 3) == 0 && (reinterpret_cast<uintptr_t>(d_out) & 3) == 0,
+               "ql_paged_attn_chunk: K/V pools must be 16-byte aligned, q and the output 4-byte aligned");
+    ChunkAttnArgs a = {};
+    a.q = static_cast<const __half*>(d_q);
+    a.k_pool = static_cast<const __half*>(d_k_pool);
+    a.v_pool = static_cast<const __half*>(d_v_pool);
+    a.block_table = d_block_table;
+    a.position = d_position;
+    a.T = (int)n_tokens;
+    a.n_heads = n_heads;
+    a.n_kv_heads = n_kv_heads;
+    a.head_dim = head_dim;
+    a.max_blocks_per_seq = (int)max_blocks_per_seq;
+    a.num_blocks = (int)num_blocks;
+    a.scale = scale;
+    a.out = static_cast<__half*>(d_out);
+    a.workspace = d_workspace;
+    a.workspace_bytes = workspace_bytes;
+    return chunk_attn_launch(a, static_cast<cudaStream_t>(stream), false);
+}
