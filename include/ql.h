@@ -420,7 +420,7 @@ int ql_model_destroy(ql_model* m);
  * step as ONE cooperative kernel, one CTA per SM, that streams every layer's weights through
  * shared-memory rings and separates the phases with grid-wide barriers in device memory;
  * batches up to ql_model_persistent_max_batch() (at most 2). QL_STEP_AUTO (the default):
- * QL_STEP_LAUNCHES, the faster of the two on GB300 (2.12 vs 3.09 ms per batch-1 step of the
+ * QL_STEP_LAUNCHES, the faster of the two on GB300 (1.55 vs 2.89 ms per batch-1 step of the
  * 8B-shaped model). Both compute the same step ([IL] CudaQwen3::step); their sums differ only
  * in rounding order.                                                                     */
 enum { QL_STEP_AUTO = 0, QL_STEP_LAUNCHES = 1, QL_STEP_PERSISTENT = 2 };
