@@ -474,7 +474,7 @@ def gpu_arm(args, rank, world, local_rank):
     }
     if phases:
         line["step_phases_us"] = phases
-    if not args.layers:
+    if not args.layers and not args.no_prefill:
         line["prefill_8b"] = prefill_run(gm, cfg, s)
     if not args.layers and not args.no_moe:
         line["moe_a3b_b1"] = moe_run(min(steps, 64), 3, s, local_rank, world)
@@ -1159,6 +1159,7 @@ def main():
     ap.add_argument("--no-e32", action="store_true", help="leave the batch-32 sub-results out of the default line")
     ap.add_argument("--kv", default="f16", choices=["f16", "q8q5"], help="--config e32: KV cache format")
     ap.add_argument("--no-moe", action="store_true", help="leave the routed-expert sub-result out of the default line")
+    ap.add_argument("--no-prefill", action="store_true", help="leave the prefill sub-result out of the default line")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling aid: run the 8B-shaped step with this many layers (default: all 36)")
     ap.add_argument("--step-kernel", default="auto", choices=["auto", "persistent", "launches"],
