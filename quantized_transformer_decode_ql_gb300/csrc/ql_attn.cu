@@ -245,8 +245,17 @@ __global__ void __launch_bounds__(NW * 32) attn_split_kernel(AParams p, DevError
         pdl_wait();
         pdl_trigger();
     }
-    if (p.active && p.active[b] == 0) return;
+    // The CTA's first loads, in flight together (one round trip instead of a chain of three):
+    // the slot's activity, its length, and the block-table entries of this warp's first two
+    // blocks (a split's first block, s * spb, does not depend on the length; entries are read
+    // only inside the table's row).
+    const int32_t* bt = p.block_tables + (size_t)b * p.maxb;
+    const int e0 = s * p.spb + warp;
+    const int act = p.active ? p.active[b] : 1;
     const int L = p.context_lens ? p.context_lens[b] : p.positions[b] + 1;
+    const int pre0 = e0 < p.maxb ? bt[e0] : -1;
+    const int pre1 = e0 + kAttnWarps < p.maxb ? bt[e0 + kAttnWarps] : -1;
+    if (act == 0) return;
     if (L <= 0) return;   // idle slot
     if (L > p.maxb * kBS) {
         if (s == 0 && threadIdx.x == 0) record_device_error(err, kErrAttnLength, b, L);
@@ -267,16 +276,16 @@ __global__ void __launch_bounds__(NW * 32) attn_split_kernel(AParams p, DevError
     const int blk1 = min(nblocks, blk0 + p.spb);
     const int pos = L - 1, lblk = pos / kBS, kp = pos % kBS;
 
-    const int32_t* bt = p.block_tables + (size_t)b * p.maxb;
     // f16: [buffer][K | V] tiles; KQ: [buffer] records, then one decoded K | V tile pair
     unsigned char* wtiles = asmem + (size_t)warp * WBYTES;
     const uint32_t wtiles_s = static_cast<uint32_t>(__cvta_generic_to_shared(wtiles));
     const int nb_w = blk1 - blk0 > warp ? (blk1 - blk0 - warp + kAttnWarps - 1) / kAttnWarps : 0;
 
-    // stage block i of this warp into buffer (i & 1) with 16-byte asynchronous copies
+    // stage block i of this warp into buffer (i & 1) with 16-byte asynchronous copies (blocks 0
+    // and 1: their table entries were loaded with the length)
     auto stage = [&](int i) -> bool {
         const int blk = blk0 + warp + kAttnWarps * i;
-        const int phys = bt[blk];
+        const int phys = i == 0 ? pre0 : (i == 1 ? pre1 : bt[blk]);
         bool ok = phys >= 0 && phys < p.num_blocks;
         if (!ok) {
             if (lane == 0) record_device_error(err, kErrAttnBlock, (long long)b * p.maxb + blk, phys);
