@@ -168,3 +168,98 @@ def test_a3b_width_step_matches_oracle():
         gm.ql_check_device_error()
     finally:
         gm.close()
+
+
+def _run_steps(cfg, w, n_steps):
+    """GPU logits and greedy tokens of n_steps teacher-forced decode steps (the oracle's greedy
+    tokens fed back), with the oracle's logits, for the weights w."""
+    from quantized_transformer_decode_ql_gb300.model import DeviceModel
+    gm = DeviceModel(cfg, w, num_blocks=16, max_batch=1, max_blocks_per_seq=4)
+    try:
+        om = decode.Q4Model(cfg, w)
+        cache = decode.KVCache(cfg, 1, 64)
+        bt = dev(ql_inputs.fragmented_block_ids(16, seed=5)[:4].reshape(1, 4).copy())
+        tokens = torch.zeros(1, dtype=torch.int32, device="cuda")
+        positions = torch.zeros(1, dtype=torch.int32, device="cuda")
+        nxt = torch.zeros(1, dtype=torch.int32, device="cuda")
+        logits = torch.zeros((1, cfg.vocab), dtype=torch.float32, device="cuda")
+        args = gm.step_args(tokens, positions, bt, nxt, logits=logits)
+        tok = int(ql_inputs.prompt_tokens(1, cfg.vocab, seed=1)[0])
+        out = []
+        for step in range(n_steps):
+            gaps = []
+            orig = moe.moe_ffn
+
+            def spy(hn, router, w1, w2, c):
+                lg = np.sort(np.asarray(router) @ np.asarray(hn))[::-1]
+                gaps.append(lg[c.topk - 1] - lg[c.topk])
+                return orig(hn, router, w1, w2, c)
+            moe.moe_ffn = spy
+            try:
+                want = decode.decode_step(om, cache, [tok], [step])[0]
+            finally:
+                moe.moe_ffn = orig
+            tokens.fill_(tok)
+            gm.ql_decode_step(args)
+            torch.cuda.synchronize()
+            out.append((host(logits)[0].astype(np.float64), int(nxt.item()), want, gaps))
+            tok = int(decode.greedy(want))
+        gm.ql_check_device_error()
+        return out
+    finally:
+        gm.close()
+
+
+def _reversed_experts(cfg, w):
+    """The same model with its experts in reverse order: exact router ties then break toward the
+    other end of the original order."""
+    import copy
+    r = copy.deepcopy(w)
+    E, inter, hid = cfg.num_experts, cfg.moe_inter, cfg.hidden
+    for L in r["layers"]:
+        L["router"] = L["router"][::-1].copy()
+        L["w1"] = L["w1"].reshape(E, 2 * inter, hid)[::-1].reshape(E * 2 * inter, hid).copy()
+        L["w2"] = L["w2"].reshape(E, hid, inter)[::-1].reshape(E * hid, inter).copy()
+    return r
+
+
+@pytest.mark.parametrize("form", ["zero_router", "three_equal_rows"])
+def test_router_ties_take_the_lowest_index(form):
+    """Exact ties between router logits ([IL] CudaQwen3::step's top-k; the reading in oracle.moe:
+    the lower expert index first among equal values). An all-zero router makes every logit 0;
+    equal router rows for experts 0, 1 and 2 make those three logits equal (bit for bit on the
+    GPU too: each is the same dot product in the same order). The GPU must pick what the oracle
+    picks: its logits within the step tolerance at every step. A near-tie that is not exact is
+    still excluded (gap > 1e-4 unless exactly 0). Non-vacuity: the oracle of the same model with
+    its experts reversed (ties then resolved toward the other end) differs from the oracle by
+    more than the tolerance at some step."""
+    import copy
+    lib()
+    cfg = ql_inputs.TINY_MOE
+    w = copy.deepcopy(ql_inputs.weights(cfg, seed=0))
+    for L in w["layers"]:
+        if form == "zero_router":
+            L["router"] = np.zeros_like(L["router"])
+        else:
+            r = L["router"].copy()
+            r[1] = r[0]
+            r[2] = r[0]
+            L["router"] = r
+    steps = 8
+    res = _run_steps(cfg, w, steps)
+    for step, (got, nxt, want, gaps) in enumerate(res):
+        assert all(g == 0.0 or g > 1e-4 for g in gaps), f"step {step}: a near-tie that is not exact: {gaps}"
+        ok = decode.logits_close(got, want)
+        assert ok.all(), f"step {step}: max err {np.abs(got - want).max():.3e}"
+        if decode.greedy_must_agree(want):
+            assert nxt == int(decode.greedy(want)), f"step {step}"
+    # non-vacuity: resolving the ties the other way changes the result beyond the tolerance
+    om_r = decode.Q4Model(cfg, _reversed_experts(cfg, w))
+    cache_r = decode.KVCache(cfg, 1, 64)
+    tok = int(ql_inputs.prompt_tokens(1, cfg.vocab, seed=1)[0])
+    differs = False
+    for step in range(steps):
+        want_r = decode.decode_step(om_r, cache_r, [tok], [step])[0]
+        differs |= not decode.logits_close(want_r, res[step][2]).all()
+        tok = int(decode.greedy(res[step][2]))
+    assert differs, "reversing the experts left every step within the tolerance: the test would not see a wrong tie-break"
