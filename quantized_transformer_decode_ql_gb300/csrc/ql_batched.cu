@@ -66,6 +66,16 @@ struct BParams {
     int maxrb;             // row blocks (8 tiles) of the largest row group
     int kernel_merge;      // tcgen05 form: 1 = merge the K windows in the kernel (tickets), 0 = merge_kernel
     CUtensorMap tmap;      // tcgen05 form: the stream as [tile][unit][144 x 8 bytes], boxes of 8 tiles x 1 unit
+    // RMSNorm folded into the merges (mma.sync form, decode step): a consumer GEMV stages x16 =
+    // f16(x w) of its un-normalised input, and its merge multiplies the window sums of column c by
+    // rsqrt(sum_i x_c[i]^2 / cols + eps), from ssq_in ([cols / 32][kMaxCols] sums over 32-row
+    // chunks). A producer (residual epilogue) writes, besides the new x, xn_out = f16(x w_next)
+    // ([B][rows]) and those chunk sums of the new x into ssq_out.
+    const float* ssq_in;
+    float* ssq_out;
+    const float* w_next;
+    __half* xn_out;
+    float eps;
     unsigned long long* trace;   // optional [grid][8] globaltimer stamps: 0 start, 1 past the wait,
                                  // 2 staged, 3 units done, 4 partials written, 5 end
 };
@@ -208,7 +218,26 @@ __device__ __forceinline__ void write_partial(const BParams& p, const Geo& G, in
 constexpr int kMergeWin = 8, kMergeT = 256;
 __global__ void __launch_bounds__(kMergeT) merge_kernel(const __grid_constant__ BParams p) {
     __shared__ unsigned long long kred[kMaxCols];
+    __shared__ float nred[kMergeT / kMaxCols][kMaxCols];
+    __shared__ float nf[kMaxCols];   // the RMSNorm factor per column (consumer form)
     if (threadIdx.x < kMaxCols) kred[threadIdx.x] = 0ull;
+    if (p.ssq_in != nullptr) {
+        // before the wait: the producer's merge that wrote the sums ran two launches back. Per
+        // column, chunk slices summed in a fixed order (thread = column + 32 slice), then the slices
+        static_assert(kMergeT % kMaxCols == 0, "merge threads: whole column sets");
+        constexpr int kSl = kMergeT / kMaxCols;
+        const int c = threadIdx.x % kMaxCols, sl = threadIdx.x / kMaxCols, nch = p.M.nblk;
+        float a = 0.f;
+        for (int j = sl; j < nch; j += kSl) a += __ldcg(p.ssq_in + (size_t)j * kMaxCols + c);
+        nred[sl][c] = a;
+        __syncthreads();
+        if (threadIdx.x < kMaxCols) {
+            float t = 0.f;
+#pragma unroll
+            for (int q = 0; q < kSl; ++q) t += nred[q][threadIdx.x];
+            nf[threadIdx.x] = rsqrtf(fmaf(t, 1.0f / (float)(nch * 32), p.eps));
+        }
+    }
     pdl_wait();
     pdl_trigger();
     __syncthreads();
@@ -259,6 +288,40 @@ __global__ void __launch_bounds__(kMergeT) merge_kernel(const __grid_constant__ 
                     t[4] += v[k][1].x; t[5] += v[k][1].y; t[6] += v[k][1].z; t[7] += v[k][1].w;
                 }
             }
+        }
+        if (p.ssq_in != nullptr) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float f = nf[8 * c8 + k];
+                s[k] *= f;
+                su[k] *= f;
+            }
+        }
+        if (resid && p.ssq_out != nullptr) {
+            // the new x, f16(x w_next) for the next GEMV, and the 32-row chunk sums of x^2 (the
+            // warp's 32 lanes hold 32 consecutive rows of one column group: a fixed shuffle tree)
+            float sq[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int c = 8 * c8 + k;
+                float v = 0.f;
+                if (c < p.B) {
+                    v = res[k] + s[k];
+                    yf[(size_t)c * p.ld + row] = v;
+                    p.xn_out[(size_t)c * p.M.rows + row] = __float2half_rn(v * __ldg(p.w_next + row));
+                }
+                sq[k] = v * v;
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+#pragma unroll
+                for (int o = 16; o; o >>= 1) sq[k] += __shfl_xor_sync(0xffffffffu, sq[k], o);
+            if ((threadIdx.x & 31) == 0) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    if (8 * c8 + k < p.B) p.ssq_out[(size_t)(row >> 5) * kMaxCols + 8 * c8 + k] = sq[k];
+            }
+            continue;
         }
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
@@ -1203,7 +1266,26 @@ int batched_gemv_launch(const StreamGemvArgs& a, cudaStream_t s, bool pdl) {
     p.tickets = static_cast<int*>(a.workspace);
     p.maxrb = L.maxrb;
     p.trace = a.trace;
-    if (a.rms) {   // the RMSNorm'd activations of every column, once, for all CTAs
+    // the RMSNorm folded into the merges (merge_kernel runs in the mma.sync form only); the
+    // producer's rows must come in whole warps of 32 (its chunk sums are warp reductions)
+    static const bool fold_off = [] {   // QL_BATCHED_NORM_FOLD=0: rms_norm_kernel (A/B measurements)
+        const char* e = std::getenv("QL_BATCHED_NORM_FOLD");
+        return e != nullptr && std::atoi(e) == 0;
+    }();
+    const bool fold = !use_tc() && !fold_off;
+    const bool consume = a.rms && a.ssq_in != nullptr && fold;
+    const bool produce = a.ssq_out != nullptr && a.w_next != nullptr && a.xn != nullptr &&
+                         a.epilogue == QL_EPI_ADD_RESIDUAL && fold && a.M.rows % 32 == 0 && !a.M.silu;
+    if (consume) {
+        p.ssq_in = a.ssq_in;
+        p.eps = a.eps;
+    }
+    if (produce) {
+        p.ssq_out = a.ssq_out;
+        p.w_next = a.w_next;
+        p.xn_out = a.xn;
+    }
+    if (a.rms && !consume) {   // the RMSNorm'd activations of every column, once, for all CTAs
         const cudaError_t e0 = ql::launch(batched::rms_norm_kernel, dim3(a.batch), dim3(batched::kNormT), 0, s, pdl,
                                           a.xf, a.M.nblk * 32, a.eps, a.norm_w, a.xn);
         if (e0 != cudaSuccess) return cuda_error(e0, "rms norm launch");

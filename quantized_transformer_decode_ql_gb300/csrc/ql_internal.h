@@ -314,6 +314,13 @@ struct StreamGemvArgs {
     unsigned long long* trace;   // batch 1-2, optional: [grid][8] globaltimer stamps per CTA
     NextWeights next;     // batch 1-2: constants of a later kernel, prefetched into L2
     int grid;             // batch 1-2: CTAs (0: one per SM); fewer leave SMs to the kernel before
+    // batch 3-32, the RMSNorm folded into the merges (mma.sync form): a residual-epilogue GEMV
+    // given ssq_out and w_next also writes xn = f16(x w_next) and the 32-row chunk sums of x^2 of
+    // the new x; an RMSNorm'd GEMV given ssq_in stages xn as it is (no rms_norm_kernel) and its
+    // merge applies the norm factor from those sums
+    const float* ssq_in;
+    float* ssq_out;
+    const float* w_next;
 };
 // Routed experts at batch 1 (ql_moe.cu): the router + top-k kernel and the combine kernel.
 struct MoeRouterArgs {

@@ -63,6 +63,7 @@ struct ql_model {
     size_t persist_stream_bytes = 0;
     std::vector<ql::PMat> hmats;            // host copies: 4 per layer, then lm_head
     unsigned int* ssync = nullptr;          // abort flag of the stand-alone stream GEMVs
+    float* ssq = nullptr;                   // batch 3-32: 32-row chunk sums of x^2 ([hidden / 32][32])
     __half* xn = nullptr;                   // [max_batch][hidden] RMSNorm'd input of a batched GEMV
     void* bws = nullptr;                    // batched GEMV partial sums
     size_t bws_bytes = 0;
@@ -283,10 +284,16 @@ int run_step(ql_model* m, const ql_step_args* a, cudaStream_t s) {
     const bool streamed = !m->hmats.empty() && (B <= kPersistMaxBatch || (m->batched_ok && B <= 32));
     int gemv_k = 0;   // GEMV launches so far (their trace rows)
     auto sg = [&](const PMat& M, int epi, bool rms, const float* xf, const __half* x16, const float* nw, void* y,
-                  int ld, NextWeights next, int grid = 0) {
+                  int ld, NextWeights next, int grid = 0, const float* ssq_in = nullptr,
+                  const float* w_next = nullptr) {
         StreamGemvArgs ga = {};
         ga.next = next;
         ga.grid = grid;
+        // batch 3-32: the RMSNorm folded into the merges (a residual GEMV given the next norm's
+        // weight produces its input; an RMSNorm'd GEMV given the sums consumes it)
+        ga.ssq_in = ssq_in;
+        ga.w_next = w_next;
+        ga.ssq_out = w_next ? m->ssq : nullptr;
         if (m->trace) ga.trace = m->trace + (size_t)gemv_k * num_sms() * persist_trace_words();
         ++gemv_k;
         ga.M = M;
@@ -318,7 +325,11 @@ int run_step(ql_model* m, const ql_step_args* a, cudaStream_t s) {
             const float* next_norm = li + 1 < d.n_layers ? m->layers[li + 1].attn_norm : d.final_norm;
             const NextWeights next_attn_norm = {{next_norm, nullptr}, {(size_t)d.hidden * 4, 0}};
             const NextWeights none = {{nullptr, nullptr}, {0, 0}};
-            if ((rc = sg(Ms[0], QL_EPI_NONE, true, m->x, nullptr, L.attn_norm, m->qkv, qkv_ld, qk_norms)) != QL_OK)
+            // batch 3-32: from layer 1 on, the previous down GEMV's merge has written this GEMV's
+            // input (f16 x w) and the sums of squares of x (the RMSNorm folded into the merges)
+            const bool fold = B > kPersistMaxBatch;
+            if ((rc = sg(Ms[0], QL_EPI_NONE, true, m->x, nullptr, L.attn_norm, m->qkv, qkv_ld, qk_norms, 0,
+                         fold && li > 0 ? m->ssq : nullptr)) != QL_OK)
                 return rc;
             AttnArgs at = {};
             at.qkv = m->qkv;
@@ -357,7 +368,7 @@ int run_step(ql_model* m, const ql_step_args* a, cudaStream_t s) {
             // freed early, while the CTA with the most tiles keeps the same count
             const int o_grid = o_gemv_grid(num_sms(), B * nkv, (int)Ms[1].ntile);
             if ((rc = sg(Ms[1], QL_EPI_ADD_RESIDUAL, false, nullptr, m->attn, nullptr, m->x, (int)d.hidden,
-                         ffn_norm, o_grid)) != QL_OK)
+                         ffn_norm, o_grid, nullptr, fold && d.num_experts == 0 ? L.ffn_norm : nullptr)) != QL_OK)
                 return rc;
             if (d.num_experts > 0) {
                 // routed experts: router + top-k, gate|up of the selected experts (RMSNorm'd x,
@@ -388,10 +399,10 @@ int run_step(ql_model* m, const ql_step_args* a, cudaStream_t s) {
                 continue;
             }
             if ((rc = sg(Ms[2], QL_EPI_SILU_MUL, true, m->x, nullptr, L.ffn_norm, m->act, (int)d.intermediate,
-                         none)) != QL_OK)
+                         none, 0, fold ? m->ssq : nullptr)) != QL_OK)
                 return rc;
             if ((rc = sg(Ms[3], QL_EPI_ADD_RESIDUAL, false, nullptr, m->act, nullptr, m->x, (int)d.hidden,
-                         next_attn_norm)) != QL_OK)
+                         next_attn_norm, 0, nullptr, fold ? next_norm : nullptr)) != QL_OK)
                 return rc;
             continue;
         }
@@ -492,8 +503,11 @@ int run_step(ql_model* m, const ql_step_args* a, cudaStream_t s) {
 
     if (streamed) {
         const NextWeights first_norm = {{m->layers[0].attn_norm, nullptr}, {(size_t)d.hidden * 4, 0}};
+        // batch 3-32: the last down GEMV's merge wrote f16(x final_norm) and the sums of squares
+        const bool fold_lm = B > kPersistMaxBatch && d.num_experts == 0;
         if ((rc = sg(m->hmats.back(), kEpiArgmax, true, m->x, nullptr, d.final_norm,
-                     a->logits ? a->logits : m->logits, (int)d.vocab, first_norm)) != QL_OK)
+                     a->logits ? a->logits : m->logits, (int)d.vocab, first_norm, 0,
+                     fold_lm ? m->ssq : nullptr)) != QL_OK)
             return rc;
         e = launch(finalize_kernel, dim3(1), dim3(64), 0, s, pdl, m->keys, a->active, a->positions,
                    a->next_tokens, a->out_tokens, (long long)a->out_stride, (float*)nullptr, B);
@@ -741,6 +755,7 @@ int setup_persist(ql_model* m) {
     A((void**)&m->psync, 16);
     A((void**)&m->ssync, 16);
     A((void**)&m->xn, (size_t)d.max_batch * d.hidden * 2);
+    A((void**)&m->ssq, (size_t)(d.hidden / 32 + 1) * 32 * sizeof(float));
     if (rc != QL_OK) return rc;
     // the weights re-laid into the tile stream layout that the persistent kernel copies from
     if ((rc = persist_pack_streams(packs.data(), (int)packs.size(), m->pstreams, nullptr)) != QL_OK) return rc;
