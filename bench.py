@@ -156,9 +156,9 @@ device_tensor_fn = ql_inputs.device_tensor_fn
 # stream GEMV at the gate|up shape (24576 x 4096, plain epilogue), from one ncu capture. It is
 # reported only while the kernel's source files hash to the value recorded with it: any change
 # to the kernel makes it null until the counters are taken again.
-GU_TRAFFIC_BYTES = 57234432
+GU_TRAFFIC_BYTES = 57192192
 GU_TRAFFIC_SOURCES = ("ql_persist.cuh", "ql_persist.cu", "ql_internal.h")
-GU_TRAFFIC_SHA16 = "5cc0603626bc865c"
+GU_TRAFFIC_SHA16 = "96f7f477bb83a1db"
 
 
 def kernel_source_sha16(files) -> str:
