@@ -34,7 +34,7 @@ N_POS = 256
 def _model(max_batch):
     """A full-depth model whose every slot holds the same N_POS-position context."""
     from quantized_transformer_decode_ql_gb300.model import DeviceModel
-    maxb = (N_POS + 8 + 15) // 16
+    maxb = (N_POS + 40 + 15) // 16   # room for 40 more positions (a 32-token chunk)
     nb = max_batch * maxb
     gm = DeviceModel.from_layer_fn(CFG, ql_inputs.device_tensor_fn(CFG, seed=0), num_blocks=nb,
                                    max_batch=max_batch, max_blocks_per_seq=maxb)
@@ -110,5 +110,66 @@ def test_full_depth_two_identical_slots_equal_batch_one():
         assert int(t1[0]) == _argmax_first(l1[0])
         if decode.greedy_must_agree(l1[0].astype(np.float64)):
             assert int(t2[0]) == int(t1[0])
+    finally:
+        gm.close()
+
+
+def test_full_depth_prefill_chunk_equals_sequential_decode():
+    """[IL] runs a prompt as sequential decode (its module doc): one 32-token prefill chunk (the
+    batch-32 split-K GEMVs, the chunk attention) must give the last token's logits of 32
+    teacher-forced decode steps (the batch-1 stream GEMVs, the split attention) at the full
+    depth. Both are held to the step tolerance tol(w) = 2e-2 + 1e-2 |w| against the exact result,
+    so two GPU paths are compared at twice it (|a - b| <= |a - exact| + |exact - b|): logits and
+    the appended K/V rows within 2 tol(w), the greedy tokens equal where the top-2 margin
+    exceeds 2 tol(top)."""
+    lib()
+    gm, bt = _model(32)
+    try:
+        T = 32
+        toks = ql_inputs.prompt_tokens(T, CFG.vocab, seed=2).astype(np.int32)
+        row = bt[0].copy()
+        # 32 decode steps of slot 0, one token each (teacher-forced)
+        tokens = torch.zeros(1, dtype=torch.int32, device="cuda")
+        positions = torch.full((1,), N_POS, dtype=torch.int32, device="cuda")
+        nxt = torch.zeros(1, dtype=torch.int32, device="cuda")
+        logits = torch.zeros((1, CFG.vocab), dtype=torch.float32, device="cuda")
+        args = gm.step_args(tokens, positions, dev(row.reshape(1, -1)), nxt, logits=logits)
+        for t in range(T):
+            tokens.fill_(int(toks[t]))
+            gm.ql_decode_step(args)
+        torch.cuda.synchronize()
+        gm.ql_check_device_error()
+        assert int(positions.item()) == N_POS + T
+        want = logits.cpu().numpy()[0].astype(np.float64)
+        nblk_new = (N_POS + T + 15) // 16
+        idx = torch.as_tensor(row[N_POS // 16:nblk_new], dtype=torch.long, device="cuda")
+        k_dec = gm.k_pool[:, idx].float().cpu().numpy()
+        v_dec = gm.v_pool[:, idx].float().cpu().numpy()
+        # the same 32 tokens as one prefill chunk from the same position
+        position = torch.full((1,), N_POS, dtype=torch.int32, device="cuda")
+        plog = torch.zeros(CFG.vocab, dtype=torch.float32, device="cuda")
+        pnxt = torch.zeros(1, dtype=torch.int32, device="cuda")
+        gm.ql_prefill_chunk(dev(toks), position, dev(row), logits=plog, next_token=pnxt)
+        torch.cuda.synchronize()
+        gm.ql_check_device_error()
+        assert int(position.item()) == N_POS + T
+        got = plog.cpu().numpy().astype(np.float64)
+        two_tol = 2 * (2e-2 + 1e-2 * np.abs(want))
+        assert (np.abs(got - want) <= two_tol).all(), f"max err {np.abs(got - want).max():.3e}"
+        top = _argmax_first(want)
+        margin = want[top] - np.delete(want, top).max()
+        if margin > 2 * (2e-2 + 1e-2 * abs(want[top])):
+            assert int(pnxt.item()) == top
+        k_pre = gm.k_pool[:, idx].float().cpu().numpy()
+        v_pre = gm.v_pool[:, idx].float().cpu().numpy()
+        lo = N_POS % 16   # the new rows: positions N_POS .. N_POS + T - 1 of these blocks
+        sel = np.zeros((len(idx), 16), bool)
+        for p in range(N_POS, N_POS + T):
+            sel[p // 16 - N_POS // 16, p % 16] = True
+        assert lo == 0
+        for name, a, b in (("K", k_pre, k_dec), ("V", v_pre, v_dec)):
+            d = np.abs(a - b)[:, sel.nonzero()[0], :, sel.nonzero()[1], :]
+            w = np.abs(b)[:, sel.nonzero()[0], :, sel.nonzero()[1], :]
+            assert (d <= 2 * (2e-2 + 1e-2 * w)).all(), f"{name} rows: max err {d.max():.3e}"
     finally:
         gm.close()
