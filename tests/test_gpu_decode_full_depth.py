@@ -1,6 +1,7 @@
 """The full Qwen3-8B shape in the benchmark's decode configurations: 36 layers, the full
 151,936-row vocabulary, batch 1 (the tile stream GEMVs) and batch 32 (the split-K tensor-core
-GEMVs with the RMSNorm folded into their merges).
+GEMVs with the RMSNorm folded into their merges), with the f16 and the q8_0 / q5_1 KV cache;
+and the full Qwen3-30B-A3B routed-expert shape (48 layers) at batch 1.
 
 The f64 oracle cannot hold 36 layers of these weights, so the element-by-element comparison
 with it is made at two layers of the same width (test_gpu_decode_full.py). At the full depth the
@@ -31,18 +32,32 @@ CFG = ql_inputs.QWEN3_8B
 N_POS = 256
 
 
-def _model(max_batch):
-    """A full-depth model whose every slot holds the same N_POS-position context."""
+def _model(max_batch, cfg=CFG, quantised_cache=False):
+    """A full-depth model whose every slot holds the same N_POS-position context (f16 pool, or
+    the q8_0 / q5_1 records written by ql_kvq_write)."""
+    import quantized_transformer_decode_ql_gb300 as ql
     from quantized_transformer_decode_ql_gb300.model import DeviceModel
+    kvf = ql.QL_KV_Q8_0_Q5_1 if quantised_cache else ql.QL_KV_F16
     maxb = (N_POS + 40 + 15) // 16   # room for 40 more positions (a 32-token chunk)
     nb = max_batch * maxb
-    gm = DeviceModel.from_layer_fn(CFG, ql_inputs.device_tensor_fn(CFG, seed=0), num_blocks=nb,
-                                   max_batch=max_batch, max_blocks_per_seq=maxb)
+    gm = DeviceModel.from_layer_fn(cfg, ql_inputs.device_tensor_fn(cfg, seed=0), num_blocks=nb,
+                                   max_batch=max_batch, max_blocks_per_seq=maxb, kv_format=kvf)
     bt = ql_inputs.fragmented_block_ids(nb, seed=5).reshape(max_batch, maxb).copy()
     g = torch.Generator(device="cuda")
     g.manual_seed(4)
     nblk = (N_POS + 15) // 16
-    shape = (CFG.n_layers, nblk, CFG.n_kv_heads, 16, CFG.head_dim)
+    if quantised_cache:
+        k = torch.randn((cfg.n_layers, N_POS, cfg.n_kv_heads, cfg.head_dim), generator=g, device="cuda")
+        v = torch.randn((cfg.n_layers, N_POS, cfg.n_kv_heads, cfg.head_dim), generator=g, device="cuda")
+        pos = torch.arange(N_POS, device="cuda")
+        for b in range(max_batch):
+            idx = torch.as_tensor(bt[b, :nblk], dtype=torch.long, device="cuda")
+            slots = (idx[pos // 16] * 16 + pos % 16).contiguous()
+            for li in range(cfg.n_layers):
+                ql.ql_kvq_write(k[li].contiguous(), v[li].contiguous(), slots, cfg.n_kv_heads, cfg.head_dim,
+                                gm.kvq_pool[li], gm.num_blocks)
+        return gm, bt
+    shape = (cfg.n_layers, nblk, cfg.n_kv_heads, 16, cfg.head_dim)
     k = torch.randn(shape, generator=g, device="cuda").half()
     v = torch.randn(shape, generator=g, device="cuda").half()
     for b in range(max_batch):
@@ -55,10 +70,11 @@ def _model(max_batch):
 def _step(gm, bt, B, token, graph=False):
     """One decode step of B slots (the first B rows of bt), all with `token` at position N_POS;
     returns (logits [B, vocab], next tokens [B])."""
+    vocab = gm.cfg.vocab
     tokens = torch.full((B,), token, dtype=torch.int32, device="cuda")
     positions = torch.full((B,), N_POS, dtype=torch.int32, device="cuda")
     nxt = torch.zeros(B, dtype=torch.int32, device="cuda")
-    logits = torch.zeros((B, CFG.vocab), dtype=torch.float32, device="cuda")
+    logits = torch.zeros((B, vocab), dtype=torch.float32, device="cuda")
     args = gm.step_args(tokens, positions, dev(bt[:B].copy()), nxt, logits=logits)
     if graph:
         s = torch.cuda.Stream()
@@ -79,12 +95,16 @@ def _argmax_first(row):
     return int(np.flatnonzero(row == row.max())[0])
 
 
-@pytest.mark.parametrize("B", [1, 32])
-def test_full_depth_graph_equals_eager_and_identical_slots_agree(B):
+@pytest.mark.parametrize("case", ["b1", "b32", "b32_quantised_cache", "moe_b1"])
+def test_full_depth_graph_equals_eager_and_identical_slots_agree(case):
+    """Also the follow-on rows at full size: the q8_0 / q5_1 cache at batch 32, and the
+    Qwen3-30B-A3B-shaped routed-expert model (48 layers, 128 experts, top-8) at batch 1."""
     lib()
-    gm, bt = _model(B)
+    B = 32 if case.startswith("b32") else 1
+    cfg = ql_inputs.QWEN3_30B_A3B if case == "moe_b1" else CFG
+    gm, bt = _model(B, cfg, quantised_cache=case == "b32_quantised_cache")
     try:
-        token = int(ql_inputs.prompt_tokens(1, CFG.vocab, seed=1)[0])
+        token = int(ql_inputs.prompt_tokens(1, cfg.vocab, seed=1)[0])
         le, te = _step(gm, bt, B, token)
         lg, tg = _step(gm, bt, B, token, graph=True)
         assert np.isfinite(le).all()
