@@ -403,17 +403,21 @@ def gpu_arm(args, rank, world, local_rank):
 
     # ---- end to end through the C ABI with host buffers: per step one ql_decode_graph_step_host
     # call (H2D of the step's token ids from pinned memory, one graph replay, D2H of the next
-    # tokens, stream sync)
-    h_tok = torch.empty((B,), dtype=torch.int32, pin_memory=True)
-    h_out = torch.empty((B,), dtype=torch.int32, pin_memory=True)
-    h_tok.copy_(first.cpu())
+    # tokens, stream sync), made as a C caller makes it (arguments bound once). A greedy loop
+    # passes one pinned buffer as input and output: the step's tokens become the next input.
+    import quantized_transformer_decode_ql_gb300._lib as qlib
+    h_buf = torch.empty((B,), dtype=torch.int32, pin_memory=True)
+    h_buf.copy_(first.cpu())
     with torch.cuda.stream(s):
         positions.fill_(CTX)
     s.synchronize()
+    step_host = qlib.lib().ql_decode_graph_step_host
+    call = (gm.handle, B, h_buf.data_ptr(), h_buf.data_ptr(), s.cuda_stream)
     t0 = time.perf_counter()
     for _ in range(steps):
-        gm.ql_decode_graph_step_host(B, h_tok, h_out, s)
-        h_tok.copy_(h_out)
+        rc = step_host(*call)
+        if rc != qlib.QL_OK:
+            qlib.check(rc)
     e2e_s = time.perf_counter() - t0
     e2e_s = max_over_ranks(e2e_s, world)
 

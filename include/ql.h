@@ -506,8 +506,10 @@ int ql_decode_graph_replay(ql_model* m, int64_t batch, int n_steps, void* stream
  * the copy asynchronous) into the tokens buffer the graph of this batch was captured with,
  * replays the graph once, copies its next_tokens buffer into h_next_tokens (int32 [batch],
  * host) and waits for the stream, so that h_next_tokens holds the step's greedy tokens on
- * return. The other step buffers (positions, tables, logits) stay on the device and advance as
- * with ql_decode_graph_replay. QL_ESTATE if no graph of that batch was captured.           */
+ * return. h_tokens and h_next_tokens may be the same buffer (a greedy loop feeding each step's
+ * tokens to the next): the copies are ordered on the stream. The other step buffers
+ * (positions, tables, logits) stay on the device and advance as with ql_decode_graph_replay.
+ * QL_ESTATE if no graph of that batch was captured.                                        */
 int ql_decode_graph_step_host(ql_model* m, int64_t batch, const int32_t* h_tokens, int32_t* h_next_tokens,
                               void* stream);
 /* Chunked prefill of one sequence. [IL] runs a prompt as sequential decode (its module doc);
