@@ -126,12 +126,13 @@ def test_graph_replay_equals_eager(tiny, B):
 
 def test_graph_step_from_host_buffers(tiny):
     """ql_decode_graph_step_host (token ids in from pinned host memory, next tokens back) gives
-    the same tokens, step for step, as replays of the same graph on device buffers."""
+    the same tokens, step for step, as replays of the same graph on device buffers, also with
+    one host buffer as both input and output."""
     gm, _ = tiny
     B = 2
     start = ql_inputs.prompt_tokens(B, CFG.vocab, seed=11).astype(np.int32)
     seqs = []
-    for mode in ("device", "host"):
+    for mode in ("device", "host", "host_in_place"):
         tokens = dev(start)
         positions = torch.zeros(B, dtype=torch.int32, device="cuda")
         bt = dev(slot_tables(B, 4, seed=23))
@@ -144,16 +145,22 @@ def test_graph_step_from_host_buffers(tiny):
                 gm.ql_decode_graph_replay(B, 1, s)
                 s.synchronize()
                 got.append(tokens.cpu().numpy().copy())
-        else:
+        elif mode == "host":
             h_in = torch.from_numpy(start.copy()).pin_memory()
             h_out = torch.zeros(B, dtype=torch.int32).pin_memory()
             for _ in range(10):
                 gm.ql_decode_graph_step_host(B, h_in, h_out, s)
                 got.append(h_out.numpy().copy())
                 h_in.copy_(h_out)
+        else:   # one buffer in and out: each step's tokens are the next input
+            h_buf = torch.from_numpy(start.copy()).pin_memory()
+            for _ in range(10):
+                gm.ql_decode_graph_step_host(B, h_buf, h_buf, s)
+                got.append(h_buf.numpy().copy())
         seqs.append(np.stack(got))
         assert np.all(positions.cpu().numpy() == 10)
     assert np.array_equal(seqs[0], seqs[1])
+    assert np.array_equal(seqs[0], seqs[2])
     gm.ql_check_device_error()
 
 
