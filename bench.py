@@ -793,15 +793,17 @@ def launches_per_step(cfg, B):
     return 2 + per_layer * cfg.n_layers + gemv_passes(cfg.hidden, B)
 
 
-def ns_relative(raw, nstamps):
+def ns_relative(raw, nstamps, base=None):
     """The trace as float64 with its first `nstamps` words (globaltimer ns, ~1.8e18) taken
-    relative to the earliest stamp, in int64 first: float64 cannot hold the absolute values to
-    better than 256 ns. Unwritten (zero) stamps stay zero, written ones are >= 1."""
+    relative to the earliest stamp (or to `base`), in int64 first: float64 cannot hold the
+    absolute values to better than 256 ns. Unwritten (zero) stamps stay zero, written ones are
+    >= 1."""
     import numpy as np
     out = raw.astype(np.float64)
     ts = raw[..., :nstamps]
     if (ts > 0).any():
-        base = ts[ts > 0].min() - 1
+        if base is None:
+            base = ts[ts > 0].min() - 1
         out[..., :nstamps] = np.where(ts > 0, ts - base, 0).astype(np.float64)
     return out
 
@@ -821,22 +823,33 @@ def launch_phases(gm, sargs, s, cfg):
     rows = 4 * cfg.n_layers + 1
     B = int(sargs.batch) if hasattr(sargs, "batch") else 1
     buf = torch.zeros((rows + cfg.n_layers) * grid * 8, dtype=torch.int64, device="cuda")
+    # batch 3-32: the merge launch after each split-K GEMV, [rows][grid CTAs][4]
+    mbuf = torch.zeros(rows * grid * 4, dtype=torch.int64, device="cuda") if B > 2 else None
     gm.ql_model_set_option(ql.QL_OPT_STEP_TRACE, buf.data_ptr())
+    if mbuf is not None:
+        gm.ql_model_set_option(ql.QL_OPT_MERGE_TRACE, mbuf.data_ptr())
     try:   # a graph captured with the trace on, replayed as the timed graph is (2 steps: one warm)
         gm.ql_decode_graph_capture(sargs, s)
         with torch.cuda.stream(s):
             gm.ql_decode_graph_replay(B, 1, s)
         s.synchronize()
         buf.zero_()
+        if mbuf is not None:
+            mbuf.zero_()
         with torch.cuda.stream(s):
             gm.ql_decode_graph_replay(B, 1, s)
         s.synchronize()
     finally:
         gm.ql_model_set_option(ql.QL_OPT_STEP_TRACE, 0)
+        gm.ql_model_set_option(ql.QL_OPT_MERGE_TRACE, 0)
         gm.ql_decode_graph_capture(sargs, s)
     gm.ql_check_device_error()
-    ta = ns_relative(buf.cpu().numpy().reshape(rows + cfg.n_layers, grid, 8), 6)
+    raw = buf.cpu().numpy().reshape(rows + cfg.n_layers, grid, 8)
+    stamped = raw[..., :6][raw[..., :6] > 0]
+    base = stamped.min() - 1 if stamped.size else None
+    ta = ns_relative(raw, 6, base)
     t, tat = ta[:rows], ta[rows:]
+    tm = ns_relative(mbuf.cpu().numpy().reshape(rows, grid, 4), 4, base) if mbuf is not None else None
     if not (t[:, 0, 0] > 0).all():
         return None   # another GEMV form ran (not traced)
     kinds = [k for _ in range(cfg.n_layers) for k in ("qkv", "o", "gate_up", "down")] + ["lm_head"]
@@ -877,6 +890,31 @@ def launch_phases(gm, sargs, s, cfg):
                     "last_end": r[:, 5].max() - qkv_end, "o_past_wait": o[:, 1].max() - qkv_end})
     if att:
         out["attention"] = {k: round(float(np.nanmean([a[k] for a in att])) / 1e3, 3) for k in att[0]}
+    # the merges (batch 3-32), from their GEMV's last CTA end: first CTA start, first and last
+    # CTA past the wait, last CTA done with its outputs, last CTA end, and the next launch's
+    # first CTA past its wait (attention after q|k|v, else the next GEMV)
+    if tm is not None and (tm[:, :, 0] > 0).any():
+        mg = {}
+        for k in range(rows):
+            m = tm[k][tm[k][:, 0] > 0]
+            if len(m) == 0:
+                continue
+            g_end = t[k][t[k][:, 0] > 0][:, 5].max()
+            kind = kinds[k]
+            if kind == "qkv":
+                a = tat[k // 4]
+                a = a[a[:, 5] > 0]
+                nxt = a[:, 1].min() if len(a) else float("nan")
+            elif k + 1 < rows:
+                nxt = t[k + 1][t[k + 1][:, 0] > 0][:, 1].min()
+            else:
+                nxt = float("nan")
+            mg.setdefault(kind, []).append({
+                "first_start": m[:, 0].min() - g_end, "first_past_wait": m[:, 1].min() - g_end,
+                "last_past_wait": m[:, 1].max() - g_end, "last_done": m[:, 2].max() - g_end,
+                "last_end": m[:, 3].max() - g_end, "next_past_wait": nxt - g_end})
+        out["merge"] = {n: {key: round(float(np.nanmean([d[key] for d in lst])) / 1e3, 3) for key in lst[0]}
+                        for n, lst in mg.items()}
     out["total_step_us"] = round((t[rows - 1][:, 5].max() - t[0][t[0][:, 0] > 0][:, 0].min()) / 1e3, 1)
     return out
 

@@ -455,9 +455,16 @@ enum { QL_STEP_AUTO = 0, QL_STEP_LAUNCHES = 1, QL_STEP_PERSISTENT = 2 };
  *                              predecessor done, 2 q ready, 3 blocks done, 4 split ticket
  *                              taken, 5 end, 6 = 1 for the CTA that merged the splits. A
  *                              profiling aid
+ *   QL_OPT_MERGE_TRACE         device address of a uint64 buffer of at least
+ *                              (4 n_layers + 1) * num_SMs * 4 entries, or 0 (default, off):
+ *                              at batch 3-32 the merge launch that adds up the K windows of
+ *                              GEMV launch k (numbered as for QL_OPT_STEP_TRACE) fills row k,
+ *                              per CTA (num_SMs CTAs): 0 start, 1 past its wait on the GEMV,
+ *                              2 the CTA's outputs written, 3 end. Other batch sizes leave it
+ *                              untouched. A profiling aid
  * Applies to steps issued (or graphs captured) afterwards. QL_EINVAL for anything else.  */
 enum { QL_OPT_STEP_KERNEL = 1, QL_OPT_BARRIER_TIMEOUT_NS = 2, QL_OPT_TEST_BARRIER_EXTRA = 3,
-       QL_OPT_STEP_TRACE = 4 };
+       QL_OPT_STEP_TRACE = 4, QL_OPT_MERGE_TRACE = 5 };
 int ql_model_set_option(ql_model* m, int option, int64_t value);
 /* When the persistent kernel is available, ql_model_create also keeps a copy of every q4_0
  * matrix re-laid as a tile stream (16 rows x 4 blocks of codes and their scales contiguous,

@@ -13,7 +13,7 @@ from ._lib import (QLError, QL_OK, QL_EINVAL, QL_ENOMEM, QL_ECUDA, QL_EPOOL, QL_
                    QL_EDEVICE, QL_ESTATE, QL_DTYPE_F32, QL_DTYPE_F16, QL_EPI_NONE,
                    QL_EPI_ADD_RESIDUAL, QL_EPI_SILU_MUL, QL_STEP_AUTO, QL_STEP_LAUNCHES,
                    QL_STEP_PERSISTENT, QL_OPT_STEP_KERNEL, QL_OPT_BARRIER_TIMEOUT_NS,
-                   QL_OPT_TEST_BARRIER_EXTRA, QL_OPT_STEP_TRACE, QL_BATCHED_MMA_SYNC, QL_BATCHED_TCGEN05,
+                   QL_OPT_TEST_BARRIER_EXTRA, QL_OPT_STEP_TRACE, QL_OPT_MERGE_TRACE, QL_BATCHED_MMA_SYNC, QL_BATCHED_TCGEN05,
                    QL_GEMV_ACT_INT16, QL_GEMV_ACT_INT8, QL_KV_F16, QL_KV_Q8_0_Q5_1,
                    QL_ATTN_MERGE_TICKET, QL_ATTN_MERGE_CLUSTER,
                    Q4Matrix, LayerDesc, ModelDesc,

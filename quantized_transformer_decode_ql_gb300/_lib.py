@@ -18,6 +18,7 @@ QL_DTYPE_F32, QL_DTYPE_F16 = 0, 1
 QL_EPI_NONE, QL_EPI_ADD_RESIDUAL, QL_EPI_SILU_MUL = 0, 1, 2
 QL_STEP_AUTO, QL_STEP_LAUNCHES, QL_STEP_PERSISTENT = 0, 1, 2
 QL_OPT_STEP_KERNEL, QL_OPT_BARRIER_TIMEOUT_NS, QL_OPT_TEST_BARRIER_EXTRA, QL_OPT_STEP_TRACE = 1, 2, 3, 4
+QL_OPT_MERGE_TRACE = 5
 QL_BATCHED_MMA_SYNC, QL_BATCHED_TCGEN05 = 0, 1
 QL_GEMV_ACT_INT16, QL_GEMV_ACT_INT8 = 0, 1
 QL_KV_F16, QL_KV_Q8_0_Q5_1 = 0, 1

@@ -19,6 +19,7 @@
 // in window order (deterministic) and applies the epilogue (a merge left to one CTA per row
 // group made that CTA the launch's long tail). The weights arrive through the same per-warp
 // ring of bulk copies (TMA) as the batch-1 kernel.
+#include "ql_batched.h"
 #include "ql_persist.cuh"
 
 #include <cuda.h>   // CUtensorMap and its enums (the encoder is taken from the driver at run time)
@@ -60,7 +61,9 @@ struct BParams {
     unsigned int* sync;    // [4]: [2] is the abort flag of the bounded waits
     DevError* err;
     unsigned long long timeout_ns;
-    float* part;           // [nwin][ntile * 16][kMaxCols] f32 partial sums of the K windows
+    float* part;           // [nwin][kMaxCols][ntile * 16] f32 partial sums of the K windows (per
+                           // window and batch column, the rows in order: warp loads of 32
+                           // consecutive rows of a column are one 128-byte line)
     int ngr;               // row groups (grid = nwin * ngr)
     int* tickets;          // tcgen05 form: [ngr][maxrb] window counts per row block, zero between calls
     int maxrb;             // row blocks (8 tiles) of the largest row group
@@ -78,6 +81,8 @@ struct BParams {
     float eps;
     unsigned long long* trace;   // optional [grid][8] globaltimer stamps: 0 start, 1 past the wait,
                                  // 2 staged, 3 units done, 4 partials written, 5 end
+    unsigned long long* mtrace;  // merge_kernel's, optional [grid][kMergeTraceWords]: 0 start, 1 past
+                                 // the wait, 2 items done, 3 end
 };
 
 // This CTA's K window and row group: CTA c = (window c % nwin, row group c / nwin).
@@ -191,35 +196,40 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r
 }
 
 // Write this lane's fragment of a tile's partial sums for the CTA's window (rows g, g + 8 of
-// the tile; columns 8 nt + 2t, +1).
+// the tile; columns 8 nt + 2t, +1). Each store instruction writes 8 consecutive rows of 4
+// columns: four 32-byte sectors.
 template <int NT>
 __device__ __forceinline__ void write_partial(const BParams& p, const Geo& G, int tile, const float (&acc)[NT][4],
                                               int lane) {
     const int g = lane >> 2, t = lane & 3;
-    float* base = p.part + ((size_t)G.w * p.M.ntile + tile) * 16 * kMaxCols;
+    const int R = p.M.ntile * 16;   // (32 R is far below 2^31 for every supported shape)
+    float* base = p.part + (size_t)G.w * kMaxCols * R + tile * 16 + g;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         const int c = nt * 8 + 2 * t;
         if (c < p.B) {
-            base[g * kMaxCols + c] = acc[nt][0];
-            base[(g + 8) * kMaxCols + c] = acc[nt][2];
+            base[c * R] = acc[nt][0];
+            base[c * R + 8] = acc[nt][2];
         }
         if (c + 1 < p.B) {
-            base[g * kMaxCols + c + 1] = acc[nt][1];
-            base[(g + 8) * kMaxCols + c + 1] = acc[nt][3];
+            base[(c + 1) * R] = acc[nt][1];
+            base[(c + 1) * R + 8] = acc[nt][3];
         }
     }
 }
 
 // The result: every output's window partials summed in window order, then the epilogue. An
-// item is one output row and 8 columns (one 32-byte sector of a partial row per window);
-// consecutive threads take consecutive rows, so the stores to y [column][row] coalesce. The
-// loads of up to kMergeWin windows are in flight together. Grid-stride over the whole matrix.
+// item is one output row and 8 columns; consecutive threads take consecutive rows, so that
+// both the partial loads (per window and column, a warp reads 32 consecutive rows: one line)
+// and the stores to y [column][row] coalesce. The loads of up to kMergeWin windows are in
+// flight together. Grid-stride over the whole matrix.
 constexpr int kMergeWin = 8, kMergeT = 256;
 __global__ void __launch_bounds__(kMergeT) merge_kernel(const __grid_constant__ BParams p) {
     __shared__ unsigned long long kred[kMaxCols];
     __shared__ float nred[kMergeT / kMaxCols][kMaxCols];
     __shared__ float nf[kMaxCols];   // the RMSNorm factor per column (consumer form)
+    unsigned long long* mt = p.mtrace ? p.mtrace + (size_t)blockIdx.x * kMergeTraceWords : nullptr;
+    persist::stamp(mt, 0);
     if (threadIdx.x < kMaxCols) kred[threadIdx.x] = 0ull;
     if (p.ssq_in != nullptr) {
         // before the wait: the producer's merge that wrote the sums ran two launches back. Per
@@ -240,14 +250,14 @@ __global__ void __launch_bounds__(kMergeT) merge_kernel(const __grid_constant__ 
     }
     pdl_wait();
     pdl_trigger();
+    persist::stamp(mt, 1);
     __syncthreads();
     const int nst = p.M.nblk / kUnitBlocks, kwu = nst < kWinUnits ? nst : kWinUnits, nwin = nst / kwu;
     const bool silu = p.epi == QL_EPI_SILU_MUL, resid = p.epi == QL_EPI_ADD_RESIDUAL;
     const int rpt = silu ? 8 : 16;                         // output rows per tile
     const int nrows = p.M.ntile * rpt, c8n = (p.B + 7) >> 3;
     const int lim = silu ? (p.M.rows >> 1) : p.M.rows;
-    const size_t wstride = (size_t)p.M.ntile * 16 * (kMaxCols / 4);   // float4 per window
-    const float4* part = reinterpret_cast<const float4*>(p.part);
+    const size_t R = (size_t)p.M.ntile * 16;           // partial rows per window and column
     float* yf = static_cast<float*>(p.y);
     const long long nitems = (long long)nrows * c8n;
     for (long long i = blockIdx.x * (long long)kMergeT + threadIdx.x; i < nitems; i += (long long)gridDim.x * kMergeT) {
@@ -257,7 +267,9 @@ __global__ void __launch_bounds__(kMergeT) merge_kernel(const __grid_constant__ 
         const int tile = silu ? lr >> 3 : lr >> 4, r = lr - tile * rpt;
         const int row = tile * rpt + r;
         if (row >= lim) continue;
-        const float4* q = part + ((size_t)tile * 16 + r) * (kMaxCols / 4) + 2 * c8;
+        const int nc = p.B - 8 * c8 < 8 ? p.B - 8 * c8 : 8;   // columns of this group in the batch
+        // the partial row of column 8 c8 in window 0 (SiLU*up: the gate row; the up row is 8 further)
+        const float* q = p.part + (size_t)8 * c8 * R + (size_t)tile * 16 + r;
         float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         float su[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         float res[8];   // the residual, loaded with the first windows
@@ -268,15 +280,15 @@ __global__ void __launch_bounds__(kMergeT) merge_kernel(const __grid_constant__ 
         // SiLU*up reads two rows per window: half as many windows per round
         const int wpr = silu ? kMergeWin / 2 : kMergeWin;
         for (int w0 = 0; w0 < nwin; w0 += wpr) {
-            float4 v[kMergeWin][2];
+            float v[kMergeWin][8];
 #pragma unroll
             for (int k = 0; k < kMergeWin; ++k) {
                 const int wk = silu ? w0 + (k >> 1) : w0 + k;
                 if ((silu ? (k >> 1) : k) < wpr && wk < nwin) {
                     // SiLU*up: odd k is the up row (8 rows further in the tile)
-                    const float4* qw = q + (size_t)wk * wstride + (silu && (k & 1) ? 8 * (kMaxCols / 4) : 0);
-                    v[k][0] = __ldcg(qw);
-                    v[k][1] = __ldcg(qw + 1);
+                    const float* qw = q + (size_t)wk * kMaxCols * R + (silu && (k & 1) ? 8 : 0);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) v[k][j] = j < nc ? __ldcg(qw + (size_t)j * R) : 0.f;
                 }
             }
 #pragma unroll
@@ -284,8 +296,8 @@ __global__ void __launch_bounds__(kMergeT) merge_kernel(const __grid_constant__ 
                 const int wk = silu ? w0 + (k >> 1) : w0 + k;
                 if ((silu ? (k >> 1) : k) < wpr && wk < nwin) {
                     float* t = silu && (k & 1) ? su : s;
-                    t[0] += v[k][0].x; t[1] += v[k][0].y; t[2] += v[k][0].z; t[3] += v[k][0].w;
-                    t[4] += v[k][1].x; t[5] += v[k][1].y; t[6] += v[k][1].z; t[7] += v[k][1].w;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) t[j] += v[k][j];
                 }
             }
         }
@@ -337,6 +349,10 @@ __global__ void __launch_bounds__(kMergeT) merge_kernel(const __grid_constant__ 
             }
         }
     }
+    if (mt != nullptr) {   // (the condition is the same for every thread of the CTA)
+        __syncthreads();
+        persist::stamp(mt, 2);
+    }
     if (p.epi == kEpiArgmax) {
         __syncthreads();
         if (threadIdx.x < p.B) {
@@ -344,6 +360,7 @@ __global__ void __launch_bounds__(kMergeT) merge_kernel(const __grid_constant__ 
             if (kred[threadIdx.x] && act) atomicMax(p.keys + threadIdx.x, kred[threadIdx.x]);
         }
     }
+    persist::stamp(mt, 3);
 }
 
 template <int NT>
@@ -751,20 +768,19 @@ __device__ __forceinline__ void issue_stage(const BParams& p, const Geo& G, unsi
 }
 
 // The merge of row block rb (tiles T0 + 8 rb ..) by the 4 epilogue warps: every output's window
-// partials added in window order, then the epilogue. A window's partials of a row block are
-// one contiguous run of 128 rows x 32 columns (f32); thread e reads float4 e + 128 j of it (row
-// e / 8 + 16 j, i.e. tile j, row e / 8 of the tile; columns 4 (e % 8) ..), so that each warp
-// load is 512 contiguous bytes. SiLU*up: the threads holding a gate row (row of the tile < 8)
-// also read its up row 8 further; the others idle. Every epilogue thread runs the whole
-// function, so that the argmax reduction can shuffle over full warps.
+// partials added in window order, then the epilogue. Thread e takes row e % 16 of each tile
+// and columns 4 (e / 16) ..; per window and column a half warp reads 16 consecutive rows (64
+// contiguous bytes). SiLU*up: the threads holding a gate row (row of the tile < 8) also read its
+// up row 8 further; the others idle. Every epilogue thread runs the whole function, so that the
+// argmax reduction can shuffle over full warps.
 template <bool SILU>
 __device__ __noinline__ void merge_rb(const BParams& p, const Geo& G, int rb, int e) {
     const bool resid = p.epi == QL_EPI_ADD_RESIDUAL, amax = p.epi == kEpiArgmax;
     const int T = G.T1 - G.T0, ntl = T - rb * kRB < kRB ? T - rb * kRB : kRB;
-    const int rit = e >> 3, c4 = e & 7;                 // row of the tile, column group
+    const int rit = e & 15, c4 = e >> 4;                // row of the tile, column group
     const int lim = SILU ? (p.M.rows >> 1) : p.M.rows;
-    const size_t wstride = (size_t)p.M.ntile * 16 * (kMaxCols / 4);   // float4 per window
-    const float4* base = reinterpret_cast<const float4*>(p.part) + (size_t)(G.T0 + rb * kRB) * 16 * (kMaxCols / 4) + e;
+    const size_t R = (size_t)p.M.ntile * 16;           // partial rows per window and column
+    const float* base = p.part + (size_t)4 * c4 * R + (size_t)(G.T0 + rb * kRB) * 16 + rit;
     float* yf = static_cast<float*>(p.y);
     constexpr int kJ = 4;                               // tiles per round
     for (int j0 = 0; j0 < kRB; j0 += kJ) {
@@ -777,9 +793,10 @@ __device__ __noinline__ void merge_rb(const BParams& p, const Geo& G, int rb, in
 #pragma unroll
             for (int j = 0; j < kJ; ++j) {
                 if (lanes && j0 + j < ntl) {
-                    const float4* q = base + (size_t)w * wstride + (size_t)(j0 + j) * 128;
-                    vg[j] = __ldcg(q);
-                    if (SILU) vu[j] = __ldcg(q + 64);   // row + 8 of the tile
+                    const float* q = base + (size_t)w * kMaxCols * R + (size_t)(j0 + j) * 16;
+                    vg[j] = make_float4(__ldcg(q), __ldcg(q + R), __ldcg(q + 2 * R), __ldcg(q + 3 * R));
+                    if (SILU)   // row + 8 of the tile
+                        vu[j] = make_float4(__ldcg(q + 8), __ldcg(q + R + 8), __ldcg(q + 2 * R + 8), __ldcg(q + 3 * R + 8));
                 }
             }
 #pragma unroll
@@ -811,16 +828,16 @@ __device__ __noinline__ void merge_rb(const BParams& p, const Geo& G, int rb, in
                     }
                 }
                 if (!SILU && amax) {
-                    // per column: the largest key over the lanes holding it (lanes e % 8 equal),
-                    // then one atomic per warp and column
+                    // per column: the largest key over the lanes holding it (a half warp, e / 16
+                    // equal), then one atomic per half warp and column
                     unsigned long long key = valid && c < p.B ? persist::argmax_key(sv[k], row) : 0ull;
 #pragma unroll
-                    for (int o = 8; o < 32; o <<= 1) {
+                    for (int o = 1; o < 16; o <<= 1) {
                         const unsigned long long ok = __shfl_xor_sync(0xffffffffu, key, o);
                         key = ok > key ? ok : key;
                     }
                     const bool act = c < p.B && (p.active == nullptr || p.active[c] != 0);
-                    if (act && key != 0ull && (threadIdx.x & 31) < 8) atomicMax(p.keys + c, key);
+                    if (act && key != 0ull && (threadIdx.x & 15) == 0) atomicMax(p.keys + c, key);
                 }
             }
         }
@@ -1036,8 +1053,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
             if (warp_wait(bar + (kDFull + d) * 8, (uint32_t)(rb >> 1) & 1u, p, abt, 6000 + rb)) {
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 const int tl = rb * kRB + trb;
-                float4* dst =
-                    reinterpret_cast<float4*>(p.part + (((size_t)G.w * p.M.ntile + G.T0 + tl) * 16 + rit) * kMaxCols);
+                const size_t R = (size_t)p.M.ntile * 16;   // partial rows per window and column
+                float* dst = p.part + (size_t)G.w * kMaxCols * R + (size_t)(G.T0 + tl) * 16 + rit;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {   // 16 batch columns at a time
                     float f[16];
@@ -1048,9 +1065,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
 #pragma unroll
                         for (int i = 0; i < 16; ++i) f[i] = ac == 0 ? __uint_as_float(v[i]) : f[i] + __uint_as_float(v[i]);
                     }
-                    if (tl < T) {
+                    if (tl < T) {   // per column, a half warp stores 16 consecutive rows
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) dst[4 * h + c] = make_float4(f[4 * c], f[4 * c + 1], f[4 * c + 2], f[4 * c + 3]);
+                        for (int c = 0; c < 16; ++c) dst[(size_t)(16 * h + c) * R] = f[c];
                     }
                 }
                 asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -1235,6 +1252,10 @@ int batched_gemv_prepare() {
 }
 
 int batched_gemv_launch(const StreamGemvArgs& a, cudaStream_t s, bool pdl) {
+    return batched_gemv_launch_traced(a, nullptr, s, pdl);
+}
+
+int batched_gemv_launch_traced(const StreamGemvArgs& a, unsigned long long* merge_trace, cudaStream_t s, bool pdl) {
     QL_REQUIRE(a.M.stream && batched_gemv_shape_ok(a.M.nblk),
                "batched gemv: cols must be 128, 256, ..., 896 or a multiple of 1024");
     QL_REQUIRE(a.batch >= 1 && a.batch <= batched::kMaxCols, "batched gemv: batch must be in [1, 32]");
@@ -1266,6 +1287,7 @@ int batched_gemv_launch(const StreamGemvArgs& a, cudaStream_t s, bool pdl) {
     p.tickets = static_cast<int*>(a.workspace);
     p.maxrb = L.maxrb;
     p.trace = a.trace;
+    p.mtrace = merge_trace;
     // the RMSNorm folded into the merges (merge_kernel runs in the mma.sync form only); the
     // producer's rows must come in whole warps of 32 (its chunk sums are warp reductions)
     static const bool fold_off = [] {   // QL_BATCHED_NORM_FOLD=0: rms_norm_kernel (A/B measurements)
@@ -1306,7 +1328,7 @@ int batched_gemv_launch(const StreamGemvArgs& a, cudaStream_t s, bool pdl) {
                        pdl, p);
         if (e != cudaSuccess) return cuda_error(e, "batched gemv launch");
         if (env_km || nwin == 1) return QL_OK;
-        e = ql::launch(batched::merge_kernel, dim3(2 * num_sms()), dim3(batched::kMergeT), 0, s, pdl, p);
+        e = ql::launch(batched::merge_kernel, dim3(num_sms()), dim3(batched::kMergeT), 0, s, pdl, p);
         return e == cudaSuccess ? QL_OK : cuda_error(e, "batched gemv merge launch");
     }
     e = nt == 1   ? batched::run<1>(true, &p, grid, s, pdl)
@@ -1314,8 +1336,10 @@ int batched_gemv_launch(const StreamGemvArgs& a, cudaStream_t s, bool pdl) {
         : nt == 3 ? batched::run<3>(true, &p, grid, s, pdl)
                   : batched::run<4>(true, &p, grid, s, pdl);
     if (e != cudaSuccess) return cuda_error(e, "batched gemv launch");
-    // the windows added up and the epilogue, over every SM
-    e = ql::launch(batched::merge_kernel, dim3(2 * num_sms()), dim3(batched::kMergeT), 0, s, pdl, p);
+    // the windows added up and the epilogue, one CTA per SM: in the step's graph a grid of two
+    // per SM ran as two waves (the second wave's CTAs passed their wait only when the first
+    // wave's were done), so a larger grid only lengthens the merge
+    e = ql::launch(batched::merge_kernel, dim3(num_sms()), dim3(batched::kMergeT), 0, s, pdl, p);
     if (e != cudaSuccess) return cuda_error(e, "batched gemv merge launch");
     return QL_OK;
 }

@@ -27,6 +27,7 @@
 #include <map>
 #include <vector>
 
+#include "ql_batched.h"
 #include "ql_chunk_attn.h"
 #include "ql_internal.h"
 
@@ -58,6 +59,7 @@ struct ql_model {
     unsigned long long barrier_timeout_ns = 2000000000ull;
     unsigned int barrier_extra = 0;
     unsigned long long* trace = nullptr;    // caller-owned, see QL_OPT_STEP_TRACE
+    unsigned long long* mtrace = nullptr;   // caller-owned, see QL_OPT_MERGE_TRACE
     ql::PLayer* players = nullptr;          // device [n_layers]
     uint8_t* pstreams = nullptr;            // all matrices in the tile stream layout
     size_t persist_stream_bytes = 0;
@@ -295,6 +297,8 @@ int run_step(ql_model* m, const ql_step_args* a, cudaStream_t s) {
         ga.w_next = w_next;
         ga.ssq_out = w_next ? m->ssq : nullptr;
         if (m->trace) ga.trace = m->trace + (size_t)gemv_k * num_sms() * persist_trace_words();
+        unsigned long long* mt =
+            m->mtrace ? m->mtrace + (size_t)gemv_k * num_sms() * kMergeTraceWords : nullptr;
         ++gemv_k;
         ga.M = M;
         ga.batch = B;
@@ -312,7 +316,7 @@ int run_step(ql_model* m, const ql_step_args* a, cudaStream_t s) {
         ga.xn = m->xn;
         ga.workspace = m->bws;
         ga.workspace_bytes = m->bws_bytes;
-        return B <= kPersistMaxBatch ? stream_gemv_launch(ga, s, pdl) : batched_gemv_launch(ga, s, pdl);
+        return B <= kPersistMaxBatch ? stream_gemv_launch(ga, s, pdl) : batched_gemv_launch_traced(ga, mt, s, pdl);
     };
     for (int li = 0; li < d.n_layers; ++li) {
         const ql_layer_desc& L = m->layers[li];
@@ -956,6 +960,10 @@ extern "C" int ql_model_set_option(ql_model* m, int option, int64_t value) {
         case QL_OPT_STEP_TRACE:
             if ((value & 7) != 0) return set_error(QL_EINVAL, "ql_model_set_option: trace buffer must be 8-byte aligned");
             m->trace = reinterpret_cast<unsigned long long*>(static_cast<uintptr_t>(value));
+            return QL_OK;
+        case QL_OPT_MERGE_TRACE:
+            if ((value & 7) != 0) return set_error(QL_EINVAL, "ql_model_set_option: trace buffer must be 8-byte aligned");
+            m->mtrace = reinterpret_cast<unsigned long long*>(static_cast<uintptr_t>(value));
             return QL_OK;
         default:
             return set_error(QL_EINVAL, "ql_model_set_option: unknown option");

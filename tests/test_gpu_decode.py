@@ -357,23 +357,29 @@ def test_launch_trace_stamps(tiny, B):
     """QL_OPT_STEP_TRACE on the one-launch-per-phase step: every GEMV launch row has its CTAs'
     stamps in order (start <= past the wait <= staged <= units done <= end), each GEMV starts
     no earlier than the previous one started, and each layer's attention row is stamped in
-    order for the CTAs that took part; turning the option off leaves the buffer untouched."""
+    order for the CTAs that took part. QL_OPT_MERGE_TRACE: at batch 3 every GEMV's merge row
+    is stamped in order (start <= past the wait <= outputs written <= end), and no merge CTA
+    passes its wait before the GEMV's last CTA has ended; at batch 1 (no merges) it stays
+    untouched. Turning the options off leaves both buffers untouched."""
     ql = lib()
     gm, _ = tiny
     set_mode(gm, "launches")
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     L = CFG.n_layers
     buf = torch.zeros((5 * L + 1) * sms * 8, dtype=torch.int64, device="cuda")
+    mbuf = torch.zeros((4 * L + 1) * sms * 4, dtype=torch.int64, device="cuda")
     tokens = torch.zeros(B, dtype=torch.int32, device="cuda")
     positions = torch.full((B,), 3, dtype=torch.int32, device="cuda")
     bt = dev(slot_tables(B, 4, seed=11))
     args = gm.step_args(tokens, positions, bt, torch.zeros(B, dtype=torch.int32, device="cuda"))
     gm.ql_model_set_option(ql.QL_OPT_STEP_TRACE, buf.data_ptr())
+    gm.ql_model_set_option(ql.QL_OPT_MERGE_TRACE, mbuf.data_ptr())
     try:
         gm.ql_decode_step(args)
         torch.cuda.synchronize()
     finally:
         gm.ql_model_set_option(ql.QL_OPT_STEP_TRACE, 0)
+        gm.ql_model_set_option(ql.QL_OPT_MERGE_TRACE, 0)
     gm.ql_check_device_error()
     t = buf.cpu().numpy().reshape(5 * L + 1, sms, 8)
     starts = []
@@ -390,7 +396,18 @@ def test_launch_trace_stamps(tiny, B):
         assert len(r) > 0, f"attention of layer {l} not stamped"
         for a, b in ((0, 1), (1, 2), (2, 3), (3, 4), (4, 5)):
             assert (r[:, a] <= r[:, b]).all()
-    before = buf.clone()
+    m = mbuf.cpu().numpy().reshape(4 * L + 1, sms, 4)
+    if B <= 2:
+        assert not m.any(), "the batch 1-2 step has no merge launches"
+    else:
+        for k in range(4 * L + 1):
+            r = m[k][m[k][:, 0] > 0]
+            assert len(r) == sms, f"merge of GEMV launch {k}: {len(r)} CTAs stamped"
+            for a, b in ((0, 1), (1, 2), (2, 3)):
+                assert (r[:, a] <= r[:, b]).all(), f"merge {k}: stamp {a} after {b}"
+            g_end = t[k][t[k][:, 0] > 0][:, 5].max()
+            assert r[:, 1].min() >= g_end, f"merge {k} passed its wait before GEMV {k} ended"
+    before, mbefore = buf.clone(), mbuf.clone()
     gm.ql_decode_step(args)
     torch.cuda.synchronize()
-    assert torch.equal(buf, before)
+    assert torch.equal(buf, before) and torch.equal(mbuf, mbefore)
