@@ -219,14 +219,21 @@ __device__ __forceinline__ void write_partial(const BParams& p, const Geo& G, in
 }
 
 // The result: every output's window partials summed in window order, then the epilogue. An
-// item is one output row and 8 columns; consecutive threads take consecutive rows, so that
+// item is one output row and CG columns; consecutive threads take consecutive rows, so that
 // both the partial loads (per window and column, a warp reads 32 consecutive rows: one line)
-// and the stores to y [column][row] coalesce. The loads of up to kMergeWin windows are in
-// flight together. Grid-stride over the whole matrix.
-constexpr int kMergeWin = 8, kMergeT = 256;
-__global__ void __launch_bounds__(kMergeT) merge_kernel(const __grid_constant__ BParams p) {
+// and the stores to y [column][row] coalesce. The loads of up to 64 / CG windows (SiLU*up: half
+// as many, two rows each) are in flight together: CG = 4 when a matrix has more than 8 K
+// windows, so that the down projection's 12 windows take one round. One CTA of 512 threads per
+// SM; the items go out warp by warp over the CTAs first (the 32 items of a warp are 32
+// consecutive rows), so that a small matrix still spreads over every SM, and at batch 32 the
+// gate|up merge is one round.
+constexpr int kMergeT = 512;
+template <int CG>
+__global__ void __launch_bounds__(kMergeT, 1) merge_kernel(const __grid_constant__ BParams p) {
+    constexpr int kWin = 64 / CG;        // windows per round of loads
+    constexpr int kSl = 8;               // RMSNorm factor: chunk slices per column (threads < 256)
     __shared__ unsigned long long kred[kMaxCols];
-    __shared__ float nred[kMergeT / kMaxCols][kMaxCols];
+    __shared__ float nred[kSl][kMaxCols];
     __shared__ float nf[kMaxCols];   // the RMSNorm factor per column (consumer form)
     unsigned long long* mt = p.mtrace ? p.mtrace + (size_t)blockIdx.x * kMergeTraceWords : nullptr;
     persist::stamp(mt, 0);
@@ -234,18 +241,18 @@ __global__ void __launch_bounds__(kMergeT) merge_kernel(const __grid_constant__ 
     if (p.ssq_in != nullptr) {
         // before the wait: the producer's merge that wrote the sums ran two launches back. Per
         // column, chunk slices summed in a fixed order (thread = column + 32 slice), then the slices
-        static_assert(kMergeT % kMaxCols == 0, "merge threads: whole column sets");
-        constexpr int kSl = kMergeT / kMaxCols;
-        const int c = threadIdx.x % kMaxCols, sl = threadIdx.x / kMaxCols, nch = p.M.nblk;
-        float a = 0.f;
-        for (int j = sl; j < nch; j += kSl) a += __ldcg(p.ssq_in + (size_t)j * kMaxCols + c);
-        nred[sl][c] = a;
+        if (threadIdx.x < kSl * kMaxCols) {
+            const int c = threadIdx.x % kMaxCols, sl = threadIdx.x / kMaxCols, nch = p.M.nblk;
+            float a = 0.f;
+            for (int j = sl; j < nch; j += kSl) a += __ldcg(p.ssq_in + (size_t)j * kMaxCols + c);
+            nred[sl][c] = a;
+        }
         __syncthreads();
         if (threadIdx.x < kMaxCols) {
             float t = 0.f;
 #pragma unroll
             for (int q = 0; q < kSl; ++q) t += nred[q][threadIdx.x];
-            nf[threadIdx.x] = rsqrtf(fmaf(t, 1.0f / (float)(nch * 32), p.eps));
+            nf[threadIdx.x] = rsqrtf(fmaf(t, 1.0f / (float)(p.M.nblk * 32), p.eps));
         }
     }
     pdl_wait();
@@ -255,56 +262,61 @@ __global__ void __launch_bounds__(kMergeT) merge_kernel(const __grid_constant__ 
     const int nst = p.M.nblk / kUnitBlocks, kwu = nst < kWinUnits ? nst : kWinUnits, nwin = nst / kwu;
     const bool silu = p.epi == QL_EPI_SILU_MUL, resid = p.epi == QL_EPI_ADD_RESIDUAL;
     const int rpt = silu ? 8 : 16;                         // output rows per tile
-    const int nrows = p.M.ntile * rpt, c8n = (p.B + 7) >> 3;
+    const int nrows = p.M.ntile * rpt, ncg = (p.B + CG - 1) / CG;
     const int lim = silu ? (p.M.rows >> 1) : p.M.rows;
     const size_t R = (size_t)p.M.ntile * 16;           // partial rows per window and column
     float* yf = static_cast<float*>(p.y);
-    const long long nitems = (long long)nrows * c8n;
-    for (long long i = blockIdx.x * (long long)kMergeT + threadIdx.x; i < nitems; i += (long long)gridDim.x * kMergeT) {
-        // (no divisions: at most 4 column groups, 8 or 16 rows per tile)
-        const int c8 = i < nrows ? 0 : i < 2ll * nrows ? 1 : i < 3ll * nrows ? 2 : 3;
-        const int lr = (int)(i - (long long)c8 * nrows);
+    const long long nitems = (long long)nrows * ncg;
+    const long long i0 = ((long long)(threadIdx.x >> 5) * gridDim.x + blockIdx.x) * 32 + (threadIdx.x & 31);
+    for (long long i = i0; i < nitems; i += (long long)gridDim.x * kMergeT) {
+        int cg = 0;   // (no division: at most 8 column groups)
+        long long li = i;
+        while (li >= nrows) {
+            li -= nrows;
+            ++cg;
+        }
+        const int lr = (int)li;
         const int tile = silu ? lr >> 3 : lr >> 4, r = lr - tile * rpt;
         const int row = tile * rpt + r;
         if (row >= lim) continue;
-        const int nc = p.B - 8 * c8 < 8 ? p.B - 8 * c8 : 8;   // columns of this group in the batch
-        // the partial row of column 8 c8 in window 0 (SiLU*up: the gate row; the up row is 8 further)
-        const float* q = p.part + (size_t)8 * c8 * R + (size_t)tile * 16 + r;
-        float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        float su[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        float res[8];   // the residual, loaded with the first windows
+        const int c0 = CG * cg;
+        const int nc = p.B - c0 < CG ? p.B - c0 : CG;   // columns of this group in the batch
+        // the partial row of column c0 in window 0 (SiLU*up: the gate row; the up row is 8 further)
+        const float* q = p.part + (size_t)c0 * R + (size_t)tile * 16 + r;
+        float s[CG], su[CG], res[CG];   // res: the residual, loaded with the first windows
+#pragma unroll
+        for (int k = 0; k < CG; ++k) s[k] = su[k] = 0.f;
         if (resid) {
 #pragma unroll
-            for (int k = 0; k < 8; ++k) res[k] = 8 * c8 + k < p.B ? __ldcg(yf + (size_t)(8 * c8 + k) * p.ld + row) : 0.f;
+            for (int k = 0; k < CG; ++k) res[k] = k < nc ? __ldcg(yf + (size_t)(c0 + k) * p.ld + row) : 0.f;
         }
-        // SiLU*up reads two rows per window: half as many windows per round
-        const int wpr = silu ? kMergeWin / 2 : kMergeWin;
+        const int wpr = silu ? kWin / 2 : kWin;
         for (int w0 = 0; w0 < nwin; w0 += wpr) {
-            float v[kMergeWin][8];
+            float v[kWin][CG];
 #pragma unroll
-            for (int k = 0; k < kMergeWin; ++k) {
+            for (int k = 0; k < kWin; ++k) {
                 const int wk = silu ? w0 + (k >> 1) : w0 + k;
                 if ((silu ? (k >> 1) : k) < wpr && wk < nwin) {
                     // SiLU*up: odd k is the up row (8 rows further in the tile)
                     const float* qw = q + (size_t)wk * kMaxCols * R + (silu && (k & 1) ? 8 : 0);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) v[k][j] = j < nc ? __ldcg(qw + (size_t)j * R) : 0.f;
+                    for (int j = 0; j < CG; ++j) v[k][j] = j < nc ? __ldcg(qw + (size_t)j * R) : 0.f;
                 }
             }
 #pragma unroll
-            for (int k = 0; k < kMergeWin; ++k) {
+            for (int k = 0; k < kWin; ++k) {
                 const int wk = silu ? w0 + (k >> 1) : w0 + k;
                 if ((silu ? (k >> 1) : k) < wpr && wk < nwin) {
                     float* t = silu && (k & 1) ? su : s;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) t[j] += v[k][j];
+                    for (int j = 0; j < CG; ++j) t[j] += v[k][j];
                 }
             }
         }
         if (p.ssq_in != nullptr) {
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const float f = nf[8 * c8 + k];
+            for (int k = 0; k < CG; ++k) {
+                const float f = k < nc ? nf[c0 + k] : 0.f;
                 s[k] *= f;
                 su[k] *= f;
             }
@@ -312,33 +324,34 @@ __global__ void __launch_bounds__(kMergeT) merge_kernel(const __grid_constant__ 
         if (resid && p.ssq_out != nullptr) {
             // the new x, f16(x w_next) for the next GEMV, and the 32-row chunk sums of x^2 (the
             // warp's 32 lanes hold 32 consecutive rows of one column group: a fixed shuffle tree)
-            float sq[8];
+            float sq[CG];
+            const float wn = __ldg(p.w_next + row);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int c = 8 * c8 + k;
+            for (int k = 0; k < CG; ++k) {
+                const int c = c0 + k;
                 float v = 0.f;
-                if (c < p.B) {
+                if (k < nc) {
                     v = res[k] + s[k];
                     yf[(size_t)c * p.ld + row] = v;
-                    p.xn_out[(size_t)c * p.M.rows + row] = __float2half_rn(v * __ldg(p.w_next + row));
+                    p.xn_out[(size_t)c * p.M.rows + row] = __float2half_rn(v * wn);
                 }
                 sq[k] = v * v;
             }
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
+            for (int k = 0; k < CG; ++k)
 #pragma unroll
                 for (int o = 16; o; o >>= 1) sq[k] += __shfl_xor_sync(0xffffffffu, sq[k], o);
             if ((threadIdx.x & 31) == 0) {
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    if (8 * c8 + k < p.B) p.ssq_out[(size_t)(row >> 5) * kMaxCols + 8 * c8 + k] = sq[k];
+                for (int k = 0; k < CG; ++k)
+                    if (k < nc) p.ssq_out[(size_t)(row >> 5) * kMaxCols + c0 + k] = sq[k];
             }
             continue;
         }
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int c = 8 * c8 + k;
-            if (c >= p.B) break;
+        for (int k = 0; k < CG; ++k) {
+            const int c = c0 + k;
+            if (k >= nc) break;
             if (silu) {
                 static_cast<__half*>(p.y)[(size_t)c * p.ld + row] = __float2half_rn(persist::silu(s[k]) * su[k]);
             } else if (resid) {
@@ -361,6 +374,12 @@ __global__ void __launch_bounds__(kMergeT) merge_kernel(const __grid_constant__ 
         }
     }
     persist::stamp(mt, 3);
+}
+
+// the merge's launch: 4-column items above 8 K windows (see merge_kernel)
+static cudaError_t launch_merge(const BParams& p, int nwin, cudaStream_t s, bool pdl) {
+    if (nwin > 8) return ql::launch(merge_kernel<4>, dim3(num_sms()), dim3(kMergeT), 0, s, pdl, p);
+    return ql::launch(merge_kernel<8>, dim3(num_sms()), dim3(kMergeT), 0, s, pdl, p);
 }
 
 template <int NT>
@@ -1328,7 +1347,7 @@ int batched_gemv_launch_traced(const StreamGemvArgs& a, unsigned long long* merg
                        pdl, p);
         if (e != cudaSuccess) return cuda_error(e, "batched gemv launch");
         if (env_km || nwin == 1) return QL_OK;
-        e = ql::launch(batched::merge_kernel, dim3(num_sms()), dim3(batched::kMergeT), 0, s, pdl, p);
+        e = batched::launch_merge(p, nwin, s, pdl);
         return e == cudaSuccess ? QL_OK : cuda_error(e, "batched gemv merge launch");
     }
     e = nt == 1   ? batched::run<1>(true, &p, grid, s, pdl)
@@ -1339,7 +1358,7 @@ int batched_gemv_launch_traced(const StreamGemvArgs& a, unsigned long long* merg
     // the windows added up and the epilogue, one CTA per SM: in the step's graph a grid of two
     // per SM ran as two waves (the second wave's CTAs passed their wait only when the first
     // wave's were done), so a larger grid only lengthens the merge
-    e = ql::launch(batched::merge_kernel, dim3(num_sms()), dim3(batched::kMergeT), 0, s, pdl, p);
+    e = batched::launch_merge(p, nwin, s, pdl);
     if (e != cudaSuccess) return cuda_error(e, "batched gemv merge launch");
     return QL_OK;
 }
