@@ -410,12 +410,16 @@ __global__ void __launch_bounds__(kT, 1) gemv_batched_kernel(const __grid_consta
     r.dead = 0;
     r.base = static_cast<uint32_t>(__cvta_generic_to_shared(smem)) + (uint32_t)(warp * kStages * kSlotBytes);
     r.mbar = static_cast<uint32_t>(__cvta_generic_to_shared(&mbar[warp * kStages]));
-#pragma unroll 1
-    for (int i = 0; i < kStages; ++i) bring_issue(r, M, G, lane);
+    // one ring slot before the wait, the rest once the window's activation loads are out: in the
+    // step a CTA often starts only as the merge before it ends, and staging loads queued behind
+    // both slots' copies (E32 6382 vs 6325 tokens/s with both slots first, 6280 with none)
+    bring_issue(r, M, G, lane);
     pdl_wait();
     pdl_trigger();
     persist::stamp(tr, 1);
     stage_window(p, G, G.w, xs);
+#pragma unroll 1
+    for (int i = 1; i < kStages; ++i) bring_issue(r, M, G, lane);
     __syncthreads();
     persist::stamp(tr, 2);
 
