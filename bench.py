@@ -45,6 +45,15 @@ def load_peaks():
         return 6800.0, "fallback"
 
 
+def load_peaks_tflops():
+    """The measured dense bf16 burst peak (TFLOP/s), or None."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except Exception:
+        return None
+
+
 # ----------------------------------------------------------------------------- distributed
 def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
@@ -1134,6 +1143,58 @@ def micro_gemv_stream(shapes, batches, iters):
     return out
 
 
+def micro_gemm(shapes, tokens, iters):
+    """The prompt-chunk q4_0 GEMM (tcgen05) alone: T tokens x the tile stream copy, plain
+    epilogue; rotates weight copies totalling > 3x L2. Reports us per call, the weight bytes'
+    rate and TFLOP/s (2 T rows cols flops) against the measured bf16 peak."""
+    import torch
+    from quantized_transformer_decode_ql_gb300 import build as qbuild
+    qbuild.build()
+    import quantized_transformer_decode_ql_gb300 as ql
+    from quantized_transformer_decode_ql_gb300.model import Q4Tensor
+    peak, src = load_peaks()
+    tf_peak = load_peaks_tflops()
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    s = torch.cuda.Stream()
+    g = torch.Generator(device="cuda")
+    g.manual_seed(2)
+    out = []
+    for rows, cols in shapes:
+        one = rows * cols * 18 // 32
+        copies = max(1, min(64, -(-3 * l2 // one)))
+        Ws = []
+        for c in range(copies):
+            w = torch.randn((rows, cols), generator=g, device="cuda").mul_(0.02)
+            W = Q4Tensor.pack(w)
+            del w
+            buf = torch.empty(ql.ql_q4_0_stream_bytes(rows, cols, 0), dtype=torch.uint8, device="cuda")
+            ql.ql_q4_0_stream_pack(W.scales, W.quants, rows, cols, 0, buf)
+            del W
+            Ws.append(buf)
+        torch.cuda.synchronize()
+        for T in tokens:
+            x = torch.randn((T, cols), generator=g, device="cuda").half()
+            y = torch.empty((T, rows), dtype=torch.float32, device="cuda")
+
+            def run(n):
+                for i in range(n):
+                    ql.ql_gemm_q4_0_stream(Ws[i % copies], rows, cols, x, T, y, ql.QL_EPI_NONE, s)
+            n = max(iters, copies)
+            with torch.cuda.stream(s):
+                run(1)
+            s.synchronize()
+            us = graph_ms(lambda: run(n), s, 3) * 1e3 / n
+            tflops = 2.0 * T * rows * cols / (us * 1e-6) / 1e12
+            gbs = one / (us * 1e-6) / 1e9
+            out.append({"kernel": "ql_gemm_q4_0_stream", "rows": rows, "cols": cols, "tokens": T,
+                        "us": round(us, 2), "TFLOP/s": round(tflops, 1),
+                        "tflops_frac_of_bf16": round(tflops / tf_peak, 4) if tf_peak else None,
+                        "weight_GB/s": round(gbs, 1), "copies": copies})
+            print(json.dumps(out[-1]), flush=True)
+        del Ws
+    return out
+
+
 def micro_attn(batches, iters, ctx=0):
     """Paged GQA decode attention alone: 32/8 heads, hd 128, lengths uniform in [512, 32768]
     (ctx > 0: every sequence ctx tokens long)."""
@@ -1206,7 +1267,7 @@ def main():
                     help="profiling aid: run the 8B-shaped step with this many layers (default: all 36)")
     ap.add_argument("--step-kernel", default="auto", choices=["auto", "persistent", "launches"],
                     help="decode step implementation (auto: persistent when the batch allows it)")
-    ap.add_argument("--micro", choices=["gemv", "gemv_stream", "attn"], help="time one kernel family alone")
+    ap.add_argument("--micro", choices=["gemv", "gemv_stream", "gemm", "attn"], help="time one kernel family alone")
     ap.add_argument("--shape", default=None, help="micro gemv: ROWSxCOLS (default: all shapes)")
     ap.add_argument("--batch", default=None, help="micro: comma-separated batch sizes")
     ap.add_argument("--iters", type=int, default=50)
@@ -1221,6 +1282,11 @@ def main():
         shapes = [tuple(int(v) for v in args.shape.split("x"))] if args.shape else ql_inputs.GEMV_SHAPES
         batches = [int(b) for b in args.batch.split(",")] if args.batch else [1, 2, 8, 32]
         micro_gemv_stream(shapes, batches, args.iters)
+        return
+    if args.micro == "gemm":
+        shapes = [tuple(int(v) for v in args.shape.split("x"))] if args.shape else ql_inputs.GEMV_SHAPES
+        tokens = [int(b) for b in args.batch.split(",")] if args.batch else [128, 256]
+        micro_gemm(shapes, tokens, args.iters)
         return
     if args.micro == "attn":
         batches = [int(b) for b in args.batch.split(",")] if args.batch else [1, 2, 4, 8, 16, 32, 64]

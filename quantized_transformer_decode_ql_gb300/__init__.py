@@ -22,7 +22,7 @@ from ._lib import (QLError, QL_OK, QL_EINVAL, QL_ENOMEM, QL_ECUDA, QL_EPOOL, QL_
 __all__ = [
     "QLError", "lib", "ql_q4_0_pack", "ql_q4_0_unpack", "ql_q4_0_pack_device", "ql_gemv_q4_0",
     "ql_q4_0_stream_bytes", "ql_q4_0_stream_pack", "ql_gemv_q4_0_stream",
-    "ql_gemv_q4_0_stream_workspace_bytes", "ql_set_batched_gemv_form", "ql_set_gemv_activation_form",
+    "ql_gemv_q4_0_stream_workspace_bytes", "ql_gemm_q4_0_stream", "ql_set_batched_gemv_form", "ql_set_gemv_activation_form",
     "ql_paged_attn_workspace_bytes", "ql_paged_attn_decode", "ql_paged_attn_decode_noalloc",
     "ql_paged_attn_chunk_workspace_bytes", "ql_paged_attn_chunk",
     "ql_kvq_record_bytes", "ql_kvq_write", "ql_paged_attn_decode_kvq",
@@ -161,6 +161,12 @@ def ql_gemv_q4_0_stream(w_stream, rows, cols, x, batch, y, epilogue=QL_EPI_NONE,
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     check(lib().ql_gemv_q4_0_stream(ptr(w_stream), rows, cols, ptr(x), batch, ptr(y), epilogue,
                                     ptr(workspace), nbytes, stream_ptr(stream)))
+
+
+def ql_gemm_q4_0_stream(w_stream, rows, cols, x, n_tokens, y, epilogue=QL_EPI_NONE, stream=None):
+    """The prompt-chunk GEMM over the tile stream copy: ``x`` f16 [n_tokens, cols]."""
+    check(lib().ql_gemm_q4_0_stream(ptr(w_stream), rows, cols, ptr(x), n_tokens, ptr(y), epilogue,
+                                    stream_ptr(stream)))
 
 
 def ql_paged_attn_chunk_workspace_bytes(n_tokens, n_heads, n_kv_heads, head_dim):

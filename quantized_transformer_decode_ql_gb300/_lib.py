@@ -74,6 +74,7 @@ SIGNATURES = {
     "ql_gemv_q4_0_stream": (c_int, [c_void_p, c_int64, c_int64, c_void_p, c_int64, c_void_p, c_int, c_void_p,
                                     c_int64, c_void_p]),
     "ql_gemv_q4_0_stream_workspace_bytes": (c_int64, [c_int64, c_int64, c_int]),
+    "ql_gemm_q4_0_stream": (c_int, [c_void_p, c_int64, c_int64, c_void_p, c_int64, c_void_p, c_int, c_void_p]),
     "ql_set_batched_gemv_form": (c_int, [c_int]),
     "ql_set_gemv_activation_form": (c_int, [c_int]),
     "ql_kvq_record_bytes": (c_int64, [c_int]),

@@ -1,5 +1,8 @@
-// The batch 3-32 GEMV's profiling entry point (ql_batched.cu).
+// Internal entry points of the batch 3-32 GEMV's profiling form (ql_batched.cu) and of the q4_0
+// GEMM for prompt chunks (ql_gemm.cu).
 #pragma once
+
+#include <cuda.h>   // CUtensorMap
 
 #include "ql_internal.h"
 
@@ -11,5 +14,27 @@ namespace ql {
 int batched_gemv_launch_traced(const StreamGemvArgs& a, unsigned long long* merge_trace, cudaStream_t s, bool pdl);
 
 constexpr int kMergeTraceWords = 4;   // merge trace entries per CTA
+
+// Tensor maps (the driver's encoder, QL_ECUDA if it is unavailable or refuses the layout):
+// the tile stream of M as [tile][unit][144 x 8 B] with boxes of 8 tiles x 1 unit; and a
+// row-major f16 matrix [outer][inner] (16-byte aligned base, inner % 8 == 0) with boxes of
+// box_outer rows x box_inner elements, reads past the matrix returning zero.
+int q4_stream_tensor_map(const PMat& M, CUtensorMap* map);
+int f16_rows_tensor_map(const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer,
+                        CUtensorMap* map);
+
+// The prompt GEMM (ql_gemm.cu): y[t][r] = sum_k W[r][k] x16[t][k] for t < T over the tile stream
+// copy of W (M.stream), with the epilogue QL_EPI_NONE (f32 y), QL_EPI_ADD_RESIDUAL (f32 y +=) or
+// QL_EPI_SILU_MUL (f16 y [T][rows / 2] = SiLU(gate) * up, M packed for it); ld is y's row pitch
+// in elements. x16: f16 [T][K], 16-byte aligned.
+struct GemmArgs {
+    PMat M;
+    int T;
+    const __half* x16;
+    void* y;
+    int ld;
+    int epi;
+};
+int gemm_tc_launch(const GemmArgs& a, cudaStream_t s, bool pdl);
 
 }  // namespace ql
