@@ -1234,7 +1234,7 @@ static int stream_tensor_map(const PMat& M, CUtensorMap* map) {
 int q4_stream_tensor_map(const PMat& M, CUtensorMap* map) { return stream_tensor_map(M, map); }
 
 int f16_rows_tensor_map(const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer,
-                        CUtensorMap* map) {
+                        CUtensorMap* map, bool swizzle128) {
     const EncodeTiledFn enc = encode_tiled();
     if (enc == nullptr) return set_error(QL_ECUDA, "tensor map: cuTensorMapEncodeTiled is not available");
     const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
@@ -1242,8 +1242,8 @@ int f16_rows_tensor_map(const void* base, uint64_t inner, uint64_t outer, uint32
     const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t estr[2] = {1u, 1u};
     const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? QL_OK : set_error(QL_ECUDA, "tensor map: f16 rows encoding failed (" + std::to_string((int)r) + ")");
 }
 

@@ -18,10 +18,11 @@ constexpr int kMergeTraceWords = 4;   // merge trace entries per CTA
 // Tensor maps (the driver's encoder, QL_ECUDA if it is unavailable or refuses the layout):
 // the tile stream of M as [tile][unit][144 x 8 B] with boxes of 8 tiles x 1 unit; and a
 // row-major f16 matrix [outer][inner] (16-byte aligned base, inner % 8 == 0) with boxes of
-// box_outer rows x box_inner elements, reads past the matrix returning zero.
+// box_outer rows x box_inner elements, reads past the matrix returning zero; swizzle128: the
+// box lands with the 128-byte swizzle (box_inner * 2 == 128, a 1024-byte aligned destination).
 int q4_stream_tensor_map(const PMat& M, CUtensorMap* map);
 int f16_rows_tensor_map(const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer,
-                        CUtensorMap* map);
+                        CUtensorMap* map, bool swizzle128);
 
 // The prompt GEMM (ql_gemm.cu): y[t][r] = sum_k W[r][k] x16[t][k] for t < T over the tile stream
 // copy of W (M.stream), with the epilogue QL_EPI_NONE (f32 y), QL_EPI_ADD_RESIDUAL (f32 y +=) or

@@ -8,23 +8,29 @@
 // no f16 copy of the weights exists: (q - 8) d is formed in registers and stored into tensor
 // memory as the MMA's A operand.
 //
-// One CTA per (block of 128 weight rows = 8 tiles, tile of 128 tokens); K streams in units of
-// 128 columns (one 1152-byte unit of each tile):
-//  * warp 5, lane 0: per unit, one tensor-map copy of the row block's 8 tiles x 1 unit of codes
-//    and scales (tiles past the matrix read as zero) and 16 tensor-map copies of the tokens'
-//    activations (8 f16 of K x 128 tokens each: K-major core matrices, tokens past the chunk
-//    read as zero) into a ring of kS stages, completing on the stage's mbarrier. The weight
-//    copies of the first stages go out before the wait on the previous kernel;
-//  * warps 0-3 (warp q serves tensor-memory lanes 32q..32q+31, i.e. rows 32q.. of the block):
-//    each thread expands its row's 128 codes of the unit into (q - 8) d in f16, in K order
-//    (two consecutive K per 32-bit column), and stores them into one of kA A slots of tensor
-//    memory; after the last unit they run the epilogue;
-//  * warp 4 allocates the tensor memory; its lane 0 issues tcgen05.mma (kind::f16, M 128, N 128,
-//    K 16, A in tensor memory, B in shared memory) into one f32 accumulator of 128 columns and
-//    commits each unit's MMAs to the barriers that free the unit's stage and A slot;
-//  * epilogue: tcgen05.ld of the accumulator (a thread holds its row's 128 tokens), then the
-//    stores: f32, added to the residual, or SiLU(gate) * up in f16 (the gate row's thread takes
-//    the up row from the lane 8 above).
+// One CTA per (block of 128 weight rows = 8 tiles, tile of NT tokens: 256 when the chunk has
+// more than 128, else 128); K streams in units of 128 columns (one 1152-byte unit of each tile):
+//  * warp 17, lane 0: per unit, one tensor-map copy of the row block's 8 tiles x 1 unit of codes
+//    and scales (tiles past the matrix read as zero) into a ring of kSW stages. The first kSW
+//    go out before the wait on the previous kernel (the weights do not depend on it);
+//  * warp 18, lane 0: per half unit, one tensor-map copy of the tokens' activations (64 f16 of
+//    K x NT tokens: each token's 128 bytes one row, with the 128-byte swizzle, i.e. the K-major
+//    layout the MMA reads with a SWIZZLE_128B descriptor; tokens past the chunk read as zero)
+//    into a ring of kSB stages;
+//  * warps 0-15 (warp w serves tensor-memory lanes 32 (w % 4).., i.e. rows 32 (w % 4).. of the
+//    block, and the unit's block w / 4): each thread expands its row's 32 codes of that block
+//    into (q - 8) d in f16, in K order (two consecutive K per 32-bit column), frees the code
+//    stage, and stores the values into one of kA A slots of tensor memory; after the last unit
+//    these warps run the epilogue;
+//  * warp 16 allocates the tensor memory; its lane 0 issues tcgen05.mma (kind::f16, M 128,
+//    N NT, K 16, A in tensor memory, B in shared memory) into one f32 accumulator of NT columns
+//    and commits each half unit's MMAs to the barrier that frees its activation stage, and each
+//    unit's to the one that frees its A slot;
+//  * epilogue: tcgen05.ld of the accumulator (warp w: its lanes' rows, tokens NT / 4 (w / 4)..),
+//    then the stores: f32, added to the residual, or SiLU(gate) * up in f16 (the gate row's
+//    thread takes the up row from the lane 8 above).
+// The codes (from HBM) and the activations (from L2) have rings of their own, so that the
+// codes can run up to kSW units ahead.
 // Every barrier has one waiter role, which takes its phases in order. Every wait is bounded: an
 // expiry records a device error and stops the CTA, whose copies in flight land (bounded) and
 // whose tensor memory is freed before it leaves.
@@ -44,27 +50,30 @@ using persist::as_u32;
 
 constexpr int kUnitBytes = persist::kUnitBytes;   // 16 rows x 128 columns: codes, then scales
 constexpr int kRB = 8;                             // tiles per row block: the MMA's M of 128 rows
-constexpr int kN = 128;                            // tokens per CTA: the MMA's N
-constexpr int kS = 4;                              // ring stages
+constexpr int kSW = 8;                             // code stages (one unit of the row block each)
+constexpr int kSB = 4;                             // activation stages (half a unit: 64 K)
 constexpr int kA = 4;                              // A slots of tensor memory, one unit (64 columns) each
 constexpr int kCodeBytes = kRB * kUnitBytes;       // 9216
-constexpr int kChunkBytes = kN * 16;               // 8 f16 of K for 128 tokens
-constexpr int kBBytes = 16 * kChunkBytes;          // the unit's 128 K for 128 tokens
-constexpr int kStage = kCodeBytes + kBBytes;       // a multiple of 128
-constexpr size_t kSmem = (size_t)kS * kStage;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kACol = kN;                     // the A slots after the accumulator's columns
-// instruction descriptor: D f32, A and B f16, both K-major, N = 128, M = 128
-constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kN >> 3) << 17) | ((128u >> 4) << 24);
-constexpr int kMmaWarp = 4, kProdWarp = 5, kThreads = 6 * 32;
-enum { kFull = 0, kEmpty = kS, kAFull = 2 * kS, kAFree = 2 * kS + kA, kDFull = 2 * kS + 2 * kA, kDone = kDFull + 1,
-       kBars = kDone + 1 };
-static_assert(kStage % 128 == 0 && kCodeBytes % 128 == 0, "stage regions 128-byte aligned");
-static_assert(kACol + kA * 64 <= kTmemCols, "tensor memory: accumulator + A slots");
+constexpr int kDW = 16;                            // dequantisation (and epilogue) warps
+constexpr int kMmaWarp = kDW, kWProdWarp = kDW + 1, kBProdWarp = kDW + 2, kThreads = (kDW + 3) * 32;
+enum { kWFull = 0, kWEmpty = kSW, kBFull = 2 * kSW, kBEmpty = 2 * kSW + kSB, kAFull = 2 * kSW + 2 * kSB,
+       kAFree = kAFull + kA, kDFull = kAFree + kA, kDone = kDFull + 1, kBars = kDone + 1 };
+
+template <int NT>
+struct Cfg {
+    static constexpr int kBStage = NT * 128;               // half a unit (64 K) for NT tokens
+    static constexpr size_t kSmem = (size_t)kSW * kCodeBytes + (size_t)kSB * kBStage;
+    static constexpr uint32_t kACol = NT;                  // the A slots after the accumulator's columns
+    // instruction descriptor: D f32, A and B f16, both K-major, N = NT, M = 128
+    static constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(NT >> 3) << 17) | ((128u >> 4) << 24);
+    static_assert(NT + kA * 64 <= (int)kTmemCols, "tensor memory: accumulator + A slots");
+    static_assert((kSW * kCodeBytes) % 1024 == 0, "activation stages 1024-byte aligned");
+};
 
 struct Params {
     CUtensorMap tw;       // weights: [tile][unit][144 x 8 B], boxes of 8 tiles x 1 unit
-    CUtensorMap tx;       // activations: [T][K] f16, boxes of 128 tokens x 8
+    CUtensorMap tx;       // activations: [T][K] f16, boxes of NT tokens x 64, 128-byte swizzle
     int T, rows, nst, silu, epi, ld;
     void* y;
     DevError* err;
@@ -91,7 +100,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t mb, uint32_t parity, const Par
     return false;
 }
 
-// wait_bar by every lane, one answer for the warp (its collective tcgen05 instructions need
+// wait_bar by every lane, one answer for the warp (its collective instructions that follow need
 // every lane or none)
 __device__ __forceinline__ bool warp_wait(uint32_t mb, uint32_t parity, const Params& p, int* abort_flag, int where) {
     const bool ok = wait_bar(mb, parity, p, abort_flag, where);
@@ -100,6 +109,10 @@ __device__ __forceinline__ bool warp_wait(uint32_t mb, uint32_t parity, const Pa
 
 __device__ __forceinline__ void arrive(uint32_t mb) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(mb) : "memory");
+}
+
+__device__ __forceinline__ void expect_tx(uint32_t mb, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mb), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void commit(uint32_t mb) {
@@ -113,28 +126,35 @@ __device__ __forceinline__ uint32_t deq2(uint32_t w, __half2 d2) {
     return as_u32(__hmul2(__hsub2(as_h2((w & 0x000F000Fu) | 0x64006400u), off), d2));
 }
 
+template <int NT>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ Params p) {
+    using C = Cfg<NT>;
     extern __shared__ __align__(1024) unsigned char smem[];
     __shared__ __align__(8) unsigned long long bars[kBars];
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
-    __shared__ int issued_units;
+    __shared__ int issued_w, issued_b;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int rb = blockIdx.x, n0 = blockIdx.y * kN, nst = p.nst;
+    const int rb = blockIdx.x, n0 = blockIdx.y * NT, nst = p.nst;
     const uint32_t bar = su32(bars);
+    unsigned char* bsm = smem + (size_t)kSW * kCodeBytes;   // the activation stages
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kS; ++s) {
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar + (kFull + s) * 8) : "memory");
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar + (kEmpty + s) * 8) : "memory");
+        for (int s = 0; s < kSW; ++s) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar + (kWFull + s) * 8) : "memory");
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar + (kWEmpty + s) * 8), "r"(kDW) : "memory");
+        }
+        for (int s = 0; s < kSB; ++s) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar + (kBFull + s) * 8) : "memory");
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar + (kBEmpty + s) * 8) : "memory");
         }
         for (int a = 0; a < kA; ++a) {
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 4;" ::"r"(bar + (kAFull + a) * 8) : "memory");
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar + (kAFull + a) * 8), "r"(kDW) : "memory");
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar + (kAFree + a) * 8) : "memory");
         }
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar + kDFull * 8) : "memory");
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar + kDone * 8) : "memory");
         abort_flag = 0;
-        issued_units = 0;
+        issued_w = issued_b = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == kMmaWarp) {
@@ -148,149 +168,148 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     const uint32_t tb = tmem_base;
     int* abt = &abort_flag;
 
-    // the weight copy of unit u into stage u % kS, and the activation copies (16 chunks of 8 K)
-    auto copy_w = [&](int u, unsigned long long pol) {
-        const int s = u % kS;
+    const int prew = nst < kSW ? nst : kSW;
+    unsigned long long pol = 0;
+    auto copy_w = [&](int u) {   // the codes of unit u into stage u % kSW
+        const int s = u % kSW;
+        expect_tx(bar + (kWFull + s) * 8, (uint32_t)kCodeBytes);
         asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
                      " [%0], [%1, {%2, %3, %4}], [%5], %6;"
-                     ::"r"(su32(smem + (size_t)s * kStage)), "l"(reinterpret_cast<uint64_t>(&p.tw)), "r"(0), "r"(u),
-                       "r"(rb * kRB), "r"(bar + (kFull + s) * 8), "l"(pol) : "memory");
+                     ::"r"(su32(smem + (size_t)s * kCodeBytes)), "l"(reinterpret_cast<uint64_t>(&p.tw)), "r"(0),
+                       "r"(u), "r"(rb * kRB), "r"(bar + (kWFull + s) * 8), "l"(pol) : "memory");
     };
-    auto copy_x = [&](int u) {
-        const int s = u % kS;
-        const uint32_t dst = su32(smem + (size_t)s * kStage + kCodeBytes);
-        for (int c = 0; c < 16; ++c)
-            asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-                         " [%0], [%1, {%2, %3}], [%4];"
-                         ::"r"(dst + (uint32_t)(c * kChunkBytes)), "l"(reinterpret_cast<uint64_t>(&p.tx)),
-                           "r"(128 * u + 8 * c), "r"(n0), "r"(bar + (kFull + s) * 8) : "memory");
-    };
-    const int pre = nst < kS ? nst : kS;
-    unsigned long long pol = 0;
-    if (warp == kProdWarp && lane == 0) {
+    if (warp == kWProdWarp && lane == 0) {
         pol = l2_evict_first();
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tw)) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tx)) : "memory");
-        // the weights do not depend on the previous kernel: the first stages' codes go out now
-        for (int u = 0; u < pre; ++u) {
-            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar + (kFull + u) * 8),
-                         "r"((uint32_t)kStage) : "memory");
-            copy_w(u, pol);
-        }
+        for (int u = 0; u < prew; ++u) copy_w(u);   // before the wait
     }
+    if (warp == kBProdWarp && lane == 0)
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tx)) : "memory");
     pdl_wait();
     pdl_trigger();
 
-    if (warp == kProdWarp) {
-        // ------------------------------------------------ copies (one lane)
+    if (warp == kWProdWarp) {
+        // ------------------------------------------------ code copies (one lane)
         if (lane == 0) {
-            int u = 0;
-            for (; u < pre; ++u) copy_x(u);
+            int u = prew;
             for (; u < nst; ++u) {
-                const int s = u % kS;
-                if (!wait_bar(bar + (kEmpty + s) * 8, (uint32_t)(u / kS - 1) & 1u, p, abt, 100 + u)) break;
-                // the stage's codes were read through the generic proxy; the copies write it
-                // through the async proxy
+                const int s = u % kSW;
+                if (!wait_bar(bar + (kWEmpty + s) * 8, (uint32_t)(u / kSW - 1) & 1u, p, abt, 100 + u)) break;
+                // the stage was read through the generic proxy; the copy writes it through the
+                // async proxy
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar + (kFull + s) * 8),
-                             "r"((uint32_t)kStage) : "memory");
-                copy_w(u, pol);
-                copy_x(u);
+                copy_w(u);
             }
-            issued_units = u;
+            issued_w = u;
+        }
+        __syncwarp();
+    } else if (warp == kBProdWarp) {
+        // ------------------------------------------------ activation copies (one lane)
+        if (lane == 0) {
+            const int nh = 2 * nst;
+            int h = 0;
+            for (; h < nh; ++h) {
+                const int s = h % kSB;
+                if (h >= kSB && !wait_bar(bar + (kBEmpty + s) * 8, (uint32_t)(h / kSB - 1) & 1u, p, abt, 200 + h)) break;
+                expect_tx(bar + (kBFull + s) * 8, (uint32_t)C::kBStage);
+                asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                             " [%0], [%1, {%2, %3}], [%4];"
+                             ::"r"(su32(bsm + (size_t)s * C::kBStage)), "l"(reinterpret_cast<uint64_t>(&p.tx)),
+                               "r"(64 * h), "r"(n0), "r"(bar + (kBFull + s) * 8) : "memory");
+            }
+            issued_b = h;
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------ MMA issue (one lane)
         if (lane == 0) {
-            const uint32_t sb = su32(smem);
+            const uint32_t b0 = su32(bsm);
             for (int u = 0; u < nst; ++u) {
-                const int s = u % kS, a = u % kA;
-                if (!wait_bar(bar + (kAFull + a) * 8, (uint32_t)(u / kA) & 1u, p, abt, 200 + u)) break;
-                if (!wait_bar(bar + (kFull + s) * 8, (uint32_t)(u / kS) & 1u, p, abt, 300 + u)) break;
+                const int a = u % kA;
+                if (!wait_bar(bar + (kAFull + a) * 8, (uint32_t)(u / kA) & 1u, p, abt, 300 + u)) break;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                // B: K-major core matrices, 2048 bytes between the K halves of a step (a chunk of 8
-                // K for 128 tokens), 128 bytes between 8-token groups; step ks starts 2 chunks in
-                const uint32_t b0 = sb + (uint32_t)(s * kStage + kCodeBytes);
+                bool ok = true;
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int h = 2 * u + hh, s = h % kSB;
+                    if (!wait_bar(bar + (kBFull + s) * 8, (uint32_t)(h / kSB) & 1u, p, abt, 400 + h)) {
+                        ok = false;
+                        break;
+                    }
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    // B: K-major with the 128-byte swizzle: a token's 64 K in one 128-byte row,
+                    // 1024 bytes between 8-token groups; step ks starts 32 bytes (16 K) in
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t baddr = b0 + (uint32_t)(ks * 2 * kChunkBytes);
-                    const unsigned long long bdesc = (unsigned long long)((baddr & 0x3FFFFu) >> 4) |
-                                                     ((unsigned long long)(kChunkBytes >> 4) << 16) |
-                                                     ((unsigned long long)(128u >> 4) << 32) | (1ull << 46);
-                    const uint32_t acc = (u > 0 || ks > 0) ? 1u : 0u;   // the first MMA overwrites
-                    asm volatile("{\n .reg .pred pa;\n setp.ne.u32 pa, %4, 0;\n"
-                                 " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pa;\n}"
-                                 ::"r"(tb), "r"(tb + kACol + 64u * (uint32_t)a + 8u * (uint32_t)ks), "l"(bdesc),
-                                   "r"(kIdesc), "r"(acc) : "memory");
+                    for (int ks = 0; ks < 4; ++ks) {
+                        const uint32_t baddr = b0 + (uint32_t)(s * C::kBStage + ks * 32);
+                        const unsigned long long bdesc = (unsigned long long)((baddr & 0x3FFFFu) >> 4) |
+                                                         (1ull << 16) | ((unsigned long long)(1024u >> 4) << 32) |
+                                                         (1ull << 46) | (2ull << 61);
+                        const uint32_t acc = (u > 0 || hh > 0 || ks > 0) ? 1u : 0u;   // the first MMA overwrites
+                        asm volatile("{\n .reg .pred pa;\n setp.ne.u32 pa, %4, 0;\n"
+                                     " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pa;\n}"
+                                     ::"r"(tb), "r"(tb + C::kACol + 64u * (uint32_t)a + 32u * (uint32_t)hh + 8u * (uint32_t)ks),
+                                       "l"(bdesc), "r"(C::kIdesc), "r"(acc) : "memory");
+                    }
+                    commit(bar + (kBEmpty + s) * 8);
                 }
-                commit(bar + (kEmpty + s) * 8);   // the stage (codes already read, activations read now)
+                if (!ok) break;
                 commit(bar + (kAFree + a) * 8);
                 if (u == nst - 1) commit(bar + kDFull * 8);
             }
             // every MMA issued has completed before the tensor memory is released
             commit(bar + kDone * 8);
-            wait_bar(bar + kDone * 8, 0u, p, nullptr, 400);
+            wait_bar(bar + kDone * 8, 0u, p, nullptr, 500);
         }
         __syncwarp();
     } else {
         // ------------------------------------------------ dequantisation, then the epilogue
-        const int q = warp, r = 32 * q + lane;          // this thread's row of the block
+        const int q = warp & 3, blk = warp >> 2;        // lane quarter; block of the unit (32 K)
+        const int r = 32 * q + lane;                    // this thread's row of the block
         const int tl = r >> 4, rit = r & 15;            // its tile of the block, row of the tile
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
         bool ok = true;
         for (int u = 0; u < nst && ok; ++u) {
-            const int s = u % kS, a = u % kA;
-            if (u >= kA && !warp_wait(bar + (kAFree + a) * 8, (uint32_t)(u / kA - 1) & 1u, p, abt, 500 + u)) {
+            const int s = u % kSW, a = u % kA;
+            if (u >= kA && !warp_wait(bar + (kAFree + a) * 8, (uint32_t)(u / kA - 1) & 1u, p, abt, 600 + u)) {
                 ok = false;
                 break;
             }
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            if (!warp_wait(bar + (kFull + s) * 8, (uint32_t)(u / kS) & 1u, p, abt, 600 + u)) {
+            if (!warp_wait(bar + (kWFull + s) * 8, (uint32_t)(u / kSW) & 1u, p, abt, 700 + u)) {
                 ok = false;
                 break;
             }
-            const unsigned char* unit = smem + (size_t)s * kStage + (size_t)tl * kUnitBytes;
-            uint4 cw[4];
-#pragma unroll
-            for (int b = 0; b < 4; ++b) cw[b] = *reinterpret_cast<const uint4*>(unit + (b * 16 + rit) * 16);
+            const unsigned char* unit = smem + (size_t)s * kCodeBytes + (size_t)tl * kUnitBytes;
+            const uint4 c4 = *reinterpret_cast<const uint4*>(unit + (blk * 16 + rit) * 16);
             const uint2 sc = *reinterpret_cast<const uint2*>(unit + 1024 + rit * 8);
+            __syncwarp();
+            if (lane == 0) arrive(bar + (kWEmpty + s) * 8);   // the codes are in registers
+            const uint32_t sw = (blk & 2) ? sc.y : sc.x;
+            const __half2 d2 = (blk & 1) ? __high2half2(as_h2(sw)) : __low2half2(as_h2(sw));
+            const uint32_t ws[4] = {c4.x, c4.y, c4.z, c4.w};
+            uint32_t v[16];
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {   // blocks 2 half, 2 half + 1: 64 K, 32 columns
-                uint32_t v[32];
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const uint4 c4 = cw[2 * half + e];
-                    const uint32_t sw = half ? sc.y : sc.x;
-                    const __half2 d2 = e ? __high2half2(as_h2(sw)) : __low2half2(as_h2(sw));
-                    const uint32_t ws[4] = {c4.x, c4.y, c4.z, c4.w};
-#pragma unroll
-                    for (int w = 0; w < 4; ++w) {
-                        // byte j of a block holds codes j (low nibble) and j + 16 (high): the pairs
-                        // (4w, 4w + 1), (4w + 2, 4w + 3) and the same + 16, as columns 2w, 2w + 1,
-                        // 8 + 2w, 9 + 2w of the block
-                        const uint32_t r01 = __byte_perm(ws[w], 0u, 0x4140u), r23 = __byte_perm(ws[w], 0u, 0x4342u);
-                        v[16 * e + 2 * w] = deq2(r01, d2);
-                        v[16 * e + 2 * w + 1] = deq2(r23, d2);
-                        v[16 * e + 8 + 2 * w] = deq2(r01 >> 4, d2);
-                        v[16 * e + 9 + 2 * w] = deq2(r23 >> 4, d2);
-                    }
-                }
-                asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
-                             "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
-                             ::"r"(tb + lane_base + kACol + 64u * (uint32_t)a + 32u * (uint32_t)half), "r"(v[0]),
-                               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
-                               "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),
-                               "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]),
-                               "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]),
-                               "r"(v[30]), "r"(v[31]) : "memory");
+            for (int w = 0; w < 4; ++w) {
+                // byte j of a block holds codes j (low nibble) and j + 16 (high): the pairs
+                // (4w, 4w + 1), (4w + 2, 4w + 3) and the same + 16, as columns 2w, 2w + 1,
+                // 8 + 2w, 9 + 2w of the block
+                const uint32_t r01 = __byte_perm(ws[w], 0u, 0x4140u), r23 = __byte_perm(ws[w], 0u, 0x4342u);
+                v[2 * w] = deq2(r01, d2);
+                v[2 * w + 1] = deq2(r23, d2);
+                v[8 + 2 * w] = deq2(r01 >> 4, d2);
+                v[9 + 2 * w] = deq2(r23 >> 4, d2);
             }
+            asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+                         "%13,%14,%15,%16};"
+                         ::"r"(tb + lane_base + C::kACol + 64u * (uint32_t)a + 16u * (uint32_t)blk), "r"(v[0]),
+                           "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+                           "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]) : "memory");
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             __syncwarp();
             if (lane == 0) arrive(bar + (kAFull + a) * 8);
         }
-        if (ok && warp_wait(bar + kDFull * 8, 0u, p, abt, 700)) {
+        if (ok && warp_wait(bar + kDFull * 8, 0u, p, abt, 800)) {
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             const int tile = rb * kRB + tl;
             const bool silu = p.silu != 0;
@@ -299,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             float* yf = static_cast<float*>(p.y);
             __half* yh = static_cast<__half*>(p.y);
 #pragma unroll 1
-            for (int c = 0; c < kN / 32; ++c) {   // 32 tokens at a time
+            for (int c = blk * (NT / 128); c < (blk + 1) * (NT / 128); ++c) {   // this warp's NT / 4 tokens
                 uint32_t v[32];
                 asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
                              "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
@@ -332,16 +351,32 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     }
     // copies still in flight (only after an abort): the last use of each stage lands before the
     // CTA leaves (bounded)
-    if (warp == kProdWarp && lane == 0) {
-        const int n = issued_units > pre ? issued_units : pre;
-        for (int u = n - kS < 0 ? 0 : n - kS; u < n; ++u)
-            wait_bar(bar + (kFull + u % kS) * 8, (uint32_t)(u / kS) & 1u, p, nullptr, 800 + u);
+    if (warp == kWProdWarp && lane == 0) {
+        const int n = issued_w > prew ? issued_w : prew;
+        for (int u = n - kSW < 0 ? 0 : n - kSW; u < n; ++u)
+            wait_bar(bar + (kWFull + u % kSW) * 8, (uint32_t)(u / kSW) & 1u, p, nullptr, 900 + u);
+    }
+    if (warp == kBProdWarp && lane == 0) {
+        const int n = issued_b;
+        for (int h = n - kSB < 0 ? 0 : n - kSB; h < n; ++h)
+            wait_bar(bar + (kBFull + h % kSB) * 8, (uint32_t)(h / kSB) & 1u, p, nullptr, 1000 + h);
     }
 }
 
 }  // namespace gemm
 
 namespace {
+
+template <int NT>
+cudaError_t gemm_attr(int optin) {
+    cudaFuncAttributes fa = {};
+    cudaError_t e = cudaFuncGetAttributes(&fa, gemm::gemm_tc_kernel<NT>);
+    if (e == cudaSuccess && gemm::Cfg<NT>::kSmem + fa.sharedSizeBytes > (size_t)optin) e = cudaErrorInvalidConfiguration;
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gemm::gemm_tc_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)gemm::Cfg<NT>::kSmem);
+    return e;
+}
 
 int gemm_prepare() {
     static std::mutex mu;
@@ -351,12 +386,9 @@ int gemm_prepare() {
     std::lock_guard<std::mutex> lk(mu);
     if (done.count(dev)) return QL_OK;
     int optin = 0;
-    cudaFuncAttributes fa = {};
     cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, gemm::gemm_tc_kernel);
-    if (e == cudaSuccess && gemm::kSmem + fa.sharedSizeBytes > (size_t)optin) e = cudaErrorInvalidConfiguration;
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(gemm::gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gemm::kSmem);
+    if (e == cudaSuccess) e = gemm_attr<128>(optin);
+    if (e == cudaSuccess) e = gemm_attr<256>(optin);
     if (e != cudaSuccess) return cuda_error(e, "gemm: kernel attributes");
     done.insert(dev);
     return QL_OK;
@@ -378,7 +410,8 @@ int gemm_tc_launch(const GemmArgs& a, cudaStream_t s, bool pdl) {
     gemm::Params p = {};
     if (int rc = q4_stream_tensor_map(M, &p.tw)) return rc;
     const uint64_t K = (uint64_t)M.nblk * 32;
-    if (int rc = f16_rows_tensor_map(a.x16, K, (uint64_t)a.T, 8, gemm::kN, &p.tx)) return rc;
+    const int nt = a.T > 128 ? 256 : 128;   // tokens per CTA: every weight byte read once per nt tokens
+    if (int rc = f16_rows_tensor_map(a.x16, K, (uint64_t)a.T, 64, (uint32_t)nt, &p.tx, true)) return rc;
     p.T = a.T;
     p.rows = M.rows;
     p.nst = M.nblk / 4;
@@ -388,8 +421,11 @@ int gemm_tc_launch(const GemmArgs& a, cudaStream_t s, bool pdl) {
     p.y = a.y;
     p.err = err;
     p.timeout_ns = 2000000000ull;
-    const dim3 grid((unsigned)((M.ntile + gemm::kRB - 1) / gemm::kRB), (unsigned)((a.T + gemm::kN - 1) / gemm::kN));
-    const cudaError_t e = ql::launch(gemm::gemm_tc_kernel, grid, dim3(gemm::kThreads), gemm::kSmem, s, pdl, p);
+    const dim3 grid((unsigned)((M.ntile + gemm::kRB - 1) / gemm::kRB), (unsigned)((a.T + nt - 1) / nt));
+    const cudaError_t e = nt == 256 ? ql::launch(gemm::gemm_tc_kernel<256>, grid, dim3(gemm::kThreads),
+                                                 gemm::Cfg<256>::kSmem, s, pdl, p)
+                                    : ql::launch(gemm::gemm_tc_kernel<128>, grid, dim3(gemm::kThreads),
+                                                 gemm::Cfg<128>::kSmem, s, pdl, p);
     return e == cudaSuccess ? QL_OK : cuda_error(e, "gemm launch");
 }
 
