@@ -489,6 +489,7 @@ def gpu_arm(args, rank, world, local_rank):
         line["step_phases_us"] = phases
     if not args.layers and not args.no_prefill:
         line["prefill_8b"] = prefill_run(gm, cfg, s)
+        line["prefill_8b_chunk32"] = prefill_run(gm, cfg, s, chunk=32)
     if not args.layers and not args.no_moe:
         line["moe_a3b_b1"] = moe_run(min(steps, 64), 3, s, local_rank, world)
     if not args.layers and not args.no_e32:
@@ -566,10 +567,14 @@ def moe_run(steps, warmup, s, local_rank, world):
         gm.close()
 
 
-def prefill_run(gm, cfg, s, n_prompt=2048, chunk=32):
+PREFILL_CHUNK = 256
+
+
+def prefill_run(gm, cfg, s, n_prompt=2048, chunk=PREFILL_CHUNK):
     """Chunked prefill of one n_prompt-token prompt on the 8B shape (a sibling handle with batch
-    bound 32 over the same weights): n_prompt / chunk calls of ql_prefill_chunk timed with CUDA
-    events on the launching stream, against the weights streamed once per chunk."""
+    bound `chunk` over the same weights): n_prompt / chunk calls of ql_prefill_chunk timed with
+    CUDA events on the launching stream, against the weights streamed once per chunk (above 32
+    tokens the chunk's projections are the tcgen05 GEMM, below the batched GEMVs)."""
     import torch
     maxb = (n_prompt + 15) // 16 + 1
     gp = gm.sibling(num_blocks=maxb + 8, max_batch=chunk, max_blocks_per_seq=maxb)
@@ -746,7 +751,7 @@ def gpu_arm_e32(args, rank, world, local_rank):
 
 def gpu_arm_prefill(args, rank, world, local_rank):
     """The chunked prefill workload as its own line (``--config prefill``): one 2048-token prompt
-    in 32-token chunks on the 8B shape, timed as in the default line's prefill_8b key."""
+    in chunks of --chunk tokens on the 8B shape, timed as in the default line's prefill_8b key."""
     import torch
 
     from quantized_transformer_decode_ql_gb300 import build as qbuild
@@ -761,12 +766,13 @@ def gpu_arm_prefill(args, rank, world, local_rank):
                                    max_blocks_per_seq=4)
     s = torch.cuda.Stream()
     clock = ClockSampler(local_rank)
-    r = prefill_run(gm, cfg, s)
+    chunk = args.chunk
+    r = prefill_run(gm, cfg, s, chunk=chunk)
     clocks = clock.stop()
     gm.close()
     value = sum_over_ranks(r.pop("value"), world)
-    line = {"metric": "prefill prompt tokens/s at 1 GB300 (q4_0 weights, chunks of 32)", "value": value,
-            "unit": r.pop("unit"), "n_gpus": world, "steps": 2048 // 32, "warmup": 2048 // 32,
+    line = {"metric": f"prefill prompt tokens/s at 1 GB300 (q4_0 weights, chunks of {chunk})", "value": value,
+            "unit": r.pop("unit"), "n_gpus": world, "steps": -(-2048 // chunk), "warmup": -(-2048 // chunk),
             "ms_per_step": r["ms_per_chunk"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "q4_0 weights, f16 act/KV, f32 accum", "data": "synthetic (seeded random-init weights, random prompt)",
             "config": {"workload": r.pop("workload"), "parallelism": f"replicas x{world}",
@@ -1263,6 +1269,7 @@ def main():
     ap.add_argument("--kv", default="f16", choices=["f16", "q8q5"], help="--config e32: KV cache format")
     ap.add_argument("--no-moe", action="store_true", help="leave the routed-expert sub-result out of the default line")
     ap.add_argument("--no-prefill", action="store_true", help="leave the prefill sub-result out of the default line")
+    ap.add_argument("--chunk", type=int, default=256, help="--config prefill: prompt tokens per chunk (1-256)")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling aid: run the 8B-shaped step with this many layers (default: all 36)")
     ap.add_argument("--step-kernel", default="auto", choices=["auto", "persistent", "launches"],

@@ -535,12 +535,13 @@ int ql_decode_graph_step_host(ql_model* m, int64_t batch, const int32_t* h_token
  * here a chunk of n_tokens prompt tokens (d_tokens int32 [n_tokens], device) at positions
  * *d_position .. *d_position + n_tokens - 1 goes through every layer together: the GEMVs take
  * the chunk as their batch (every weight byte streamed once per chunk; the split-K tensor-core
- * form from 3 tokens), qk-norm + RoPE append all its K/V rows to the sequence's blocks, then
+ * form from 3 tokens; above 32 tokens the tcgen05 GEMM of ql_gemm_q4_0_stream, once per 256
+ * tokens), qk-norm + RoPE append all its K/V rows to the sequence's blocks, then
  * each token attends causally to positions 0 .. its own. The result equals n_tokens decode
  * steps of those tokens (teacher-forced) up to rounding. d_block_table: int32
  * [max_blocks_per_seq] of the sequence (blocks for every position of the chunk assigned);
  * d_position: int32 [1], advanced by n_tokens; d_logits: f32 [vocab] of the chunk's last token,
- * or NULL; d_next_token: int32 [1], its greedy argmax, or NULL. 1 <= n_tokens <= min(32,
+ * or NULL; d_next_token: int32 [1], its greedy argmax, or NULL. 1 <= n_tokens <= min(256,
  * max_batch); dense models with the f16 KV format. Asynchronous on stream; not for capture. */
 int ql_prefill_chunk(ql_model* m, const int32_t* d_tokens, int64_t n_tokens, int32_t* d_position,
                      const int32_t* d_block_table, float* d_logits, int32_t* d_next_token, void* stream);

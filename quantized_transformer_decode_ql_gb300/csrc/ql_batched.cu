@@ -1233,6 +1233,11 @@ static int stream_tensor_map(const PMat& M, CUtensorMap* map) {
 
 int q4_stream_tensor_map(const PMat& M, CUtensorMap* map) { return stream_tensor_map(M, map); }
 
+int rms_norm_launch(const float* x, int cols, float eps, const float* w, __half* xn, int T, cudaStream_t s, bool pdl) {
+    const cudaError_t e = ql::launch(batched::rms_norm_kernel, dim3(T), dim3(batched::kNormT), 0, s, pdl, x, cols, eps, w, xn);
+    return e == cudaSuccess ? QL_OK : cuda_error(e, "rms norm launch");
+}
+
 int f16_rows_tensor_map(const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer,
                         CUtensorMap* map, bool swizzle128) {
     const EncodeTiledFn enc = encode_tiled();

@@ -15,6 +15,11 @@ int batched_gemv_launch_traced(const StreamGemvArgs& a, unsigned long long* merg
 
 constexpr int kMergeTraceWords = 4;   // merge trace entries per CTA
 
+// Prompt chunks (ql_prefill_chunk): up to kPrefillGemvMax tokens through the decode step's GEMVs,
+// above it through the GEMM; at most kPrefillMax tokens per chunk.
+constexpr int kPrefillGemvMax = 32;
+constexpr int kPrefillMax = 256;
+
 // Tensor maps (the driver's encoder, QL_ECUDA if it is unavailable or refuses the layout):
 // the tile stream of M as [tile][unit][144 x 8 B] with boxes of 8 tiles x 1 unit; and a
 // row-major f16 matrix [outer][inner] (16-byte aligned base, inner % 8 == 0) with boxes of
@@ -37,5 +42,8 @@ struct GemmArgs {
     int epi;
 };
 int gemm_tc_launch(const GemmArgs& a, cudaStream_t s, bool pdl);
+
+// RMSNorm of T columns: xn[t] = f16(x[t] / rms(x[t]) * w), x f32 [T][cols] (ql_batched.cu).
+int rms_norm_launch(const float* x, int cols, float eps, const float* w, __half* xn, int T, cudaStream_t s, bool pdl);
 
 }  // namespace ql

@@ -542,9 +542,10 @@ int run_step(ql_model* m, const ql_step_args* a, cudaStream_t s) {
 }
 
 // A chunk of T prompt tokens of one sequence through every layer together: the step's GEMVs at
-// batch T (stream form at T <= 2, the split-K tensor-core form at 3..32), qk-norm + RoPE +
-// append for all T positions, then causal attention of each token over the cache (its own
-// context length), and logits of the last token only.
+// batch T (stream form at T <= 2, the split-K tensor-core form at 3..32) or, above 32 tokens,
+// the tcgen05 GEMM (ql_gemm.cu) after an RMSNorm launch, qk-norm + RoPE + append for all T
+// positions, then causal attention of each token over the cache (its own context length), and
+// logits of the last token only.
 int run_prefill(ql_model* m, const int32_t* tokens, int T, int32_t* position, const int32_t* block_table,
                 float* logits, int32_t* next_token, cudaStream_t s) {
     const ql_model_desc& d = m->d;
@@ -580,6 +581,21 @@ int run_prefill(ql_model* m, const int32_t* tokens, int T, int32_t* position, co
         ga.xn = m->xn;
         ga.workspace = m->bws;
         ga.workspace_bytes = m->bws_bytes;
+        if (batch > kPrefillGemvMax) {   // a GEMM: the normalised input once, then the tcgen05 kernel
+            const __half* xin = x16;
+            if (rms) {
+                if (int rc0 = rms_norm_launch(xf, M.nblk * 32, d.eps, nw, m->xn, batch, s, pdl)) return rc0;
+                xin = m->xn;
+            }
+            GemmArgs g = {};
+            g.M = M;
+            g.T = batch;
+            g.x16 = xin;
+            g.y = y;
+            g.ld = ld;
+            g.epi = epi;
+            return gemm_tc_launch(g, s, pdl);
+        }
         return batch <= kPersistMaxBatch ? stream_gemv_launch(ga, s, pdl) : batched_gemv_launch(ga, s, pdl);
     };
     const int qkv_ld = (int)((d.n_heads + 2 * d.n_kv_heads) * d.head_dim);
@@ -901,8 +917,8 @@ extern "C" int ql_model_create(const ql_model_desc* desc, ql_model** out) {
         if (need > m->attn_ws_bytes) m->attn_ws_bytes = need;
     }
     A(&m->attn_ws, m->attn_ws_bytes);
-    {   // prefill chunks of up to min(32, max_batch) tokens
-        const int tmax = (int)(B < 32 ? B : 32);
+    {   // prefill chunks of up to min(256, max_batch) tokens
+        const int tmax = (int)(B < kPrefillMax ? B : kPrefillMax);
         for (int t = 1; t <= tmax; ++t) {
             const size_t need = chunk_attn_workspace_bytes(t, (int)d.n_heads, (int)d.n_kv_heads, (int)d.head_dim);
             if (need > m->cws_bytes) m->cws_bytes = need;
@@ -984,9 +1000,9 @@ extern "C" int ql_prefill_chunk(ql_model* m, const int32_t* d_tokens, int64_t n_
     const ql_model_desc& d = m->d;
     if (d.num_experts > 0 || d.kv_format != QL_KV_F16)
         return set_error(QL_EINVAL, "ql_prefill_chunk: dense models with the f16 KV cache only");
-    if (n_tokens < 1 || n_tokens > 32 || n_tokens > d.max_batch)
-        return set_error(QL_EINVAL, "ql_prefill_chunk: n_tokens must be in [1, min(32, max_batch)]");
-    if (m->hmats.empty() || (n_tokens > kPersistMaxBatch && !m->batched_ok))
+    if (n_tokens < 1 || n_tokens > kPrefillMax || n_tokens > d.max_batch)
+        return set_error(QL_EINVAL, "ql_prefill_chunk: n_tokens must be in [1, min(256, max_batch)]");
+    if (m->hmats.empty() || (n_tokens > kPersistMaxBatch && n_tokens <= kPrefillGemvMax && !m->batched_ok))
         return set_error(QL_EINVAL, "ql_prefill_chunk: needs the tile stream copies (and the batched GEMV above 2 tokens)");
     int dev = 0;
     cudaGetDevice(&dev);
