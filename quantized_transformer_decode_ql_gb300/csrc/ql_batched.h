@@ -33,6 +33,8 @@ int f16_rows_tensor_map(const void* base, uint64_t inner, uint64_t outer, uint32
 // copy of W (M.stream), with the epilogue QL_EPI_NONE (f32 y), QL_EPI_ADD_RESIDUAL (f32 y +=) or
 // QL_EPI_SILU_MUL (f16 y [T][rows / 2] = SiLU(gate) * up, M packed for it); ld is y's row pitch
 // in elements. x16: f16 [T][K], 16-byte aligned.
+// part (optional, part_bytes): scratch for splitting K over CTAs when the matrix has few row
+// blocks (then a second kernel adds the parts in order); null: no split.
 struct GemmArgs {
     PMat M;
     int T;
@@ -40,6 +42,8 @@ struct GemmArgs {
     void* y;
     int ld;
     int epi;
+    float* part;
+    size_t part_bytes;
 };
 int gemm_tc_launch(const GemmArgs& a, cudaStream_t s, bool pdl);
 

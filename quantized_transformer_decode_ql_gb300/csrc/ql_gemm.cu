@@ -30,7 +30,9 @@
 //    then the stores: f32, added to the residual, or SiLU(gate) * up in f16 (the gate row's
 //    thread takes the up row from the lane 8 above).
 // The codes (from HBM) and the activations (from L2) have rings of their own, so that the
-// codes can run up to kSW units ahead.
+// codes can run up to kSW units ahead. A matrix with few row blocks is split over K as well
+// (blockIdx.z takes a run of units): each CTA then stores its raw f32 sums, and gemm_merge_kernel
+// adds the K parts in order and applies the epilogue.
 // Every barrier has one waiter role, which takes its phases in order. Every wait is bounded: an
 // expiry records a device error and stops the CTA, whose copies in flight land (bounded) and
 // whose tensor memory is freed before it leaves.
@@ -78,6 +80,9 @@ struct Params {
     void* y;
     DevError* err;
     unsigned long long timeout_ns;
+    int kparts, upp;      // K parts (blockIdx.z) and units per part
+    float* part;          // kparts > 1: [kparts][T][ntile * 16] raw f32 sums (the stream's row order)
+    int R;                // ntile * 16
 };
 
 __device__ __forceinline__ uint32_t su32(const void* q) { return static_cast<uint32_t>(__cvta_generic_to_shared(q)); }
@@ -135,7 +140,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     __shared__ int abort_flag;
     __shared__ int issued_w, issued_b;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int rb = blockIdx.x, n0 = blockIdx.y * NT, nst = p.nst;
+    const int rb = blockIdx.x, n0 = blockIdx.y * NT, kp = blockIdx.z;
+    const int u0 = kp * p.upp;                         // this CTA's first unit (of the matrix's K)
+    const int nst = p.nst - u0 < p.upp ? p.nst - u0 : p.upp;   // its units
     const uint32_t bar = su32(bars);
     unsigned char* bsm = smem + (size_t)kSW * kCodeBytes;   // the activation stages
     if (threadIdx.x == 0) {
@@ -176,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
                      " [%0], [%1, {%2, %3, %4}], [%5], %6;"
                      ::"r"(su32(smem + (size_t)s * kCodeBytes)), "l"(reinterpret_cast<uint64_t>(&p.tw)), "r"(0),
-                       "r"(u), "r"(rb * kRB), "r"(bar + (kWFull + s) * 8), "l"(pol) : "memory");
+                       "r"(u0 + u), "r"(rb * kRB), "r"(bar + (kWFull + s) * 8), "l"(pol) : "memory");
     };
     if (warp == kWProdWarp && lane == 0) {
         pol = l2_evict_first();
@@ -215,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
                              " [%0], [%1, {%2, %3}], [%4];"
                              ::"r"(su32(bsm + (size_t)s * C::kBStage)), "l"(reinterpret_cast<uint64_t>(&p.tx)),
-                               "r"(64 * h), "r"(n0), "r"(bar + (kBFull + s) * 8) : "memory");
+                               "r"(64 * (2 * u0 + h)), "r"(n0), "r"(bar + (kBFull + s) * 8) : "memory");
             }
             issued_b = h;
         }
@@ -312,11 +319,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         if (ok && warp_wait(bar + kDFull * 8, 0u, p, abt, 800)) {
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             const int tile = rb * kRB + tl;
-            const bool silu = p.silu != 0;
+            const bool silu = p.silu != 0, split = p.kparts > 1;
             const int orow = silu ? tile * 8 + rit : tile * 16 + rit;   // output row
-            const bool row_ok = silu ? (rit < 8 && orow < (p.rows >> 1)) : orow < p.rows;
+            const bool row_ok = split ? tile * 16 < p.R : silu ? (rit < 8 && orow < (p.rows >> 1)) : orow < p.rows;
             float* yf = static_cast<float*>(p.y);
             __half* yh = static_cast<__half*>(p.y);
+            float* pf = split ? p.part + (size_t)kp * p.T * p.R + tile * 16 + rit : nullptr;
 #pragma unroll 1
             for (int c = blk * (NT / 128); c < (blk + 1) * (NT / 128); ++c) {   // this warp's NT / 4 tokens
                 uint32_t v[32];
@@ -335,6 +343,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     const float val = __uint_as_float(v[j]);
                     const float up = __shfl_down_sync(0xffffffffu, val, 8);   // the up row of a gate row
                     if (!row_ok || t >= p.T) continue;
+                    if (split) {   // the raw sum; the merge applies the epilogue
+                        pf[(size_t)t * p.R] = val;
+                        continue;
+                    }
                     const size_t o = (size_t)t * p.ld + orow;
                     if (silu) yh[o] = __float2half_rn(persist::silu(val) * up);
                     else if (p.epi == QL_EPI_ADD_RESIDUAL) yf[o] = yf[o] + val;
@@ -360,6 +372,32 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         const int n = issued_b;
         for (int h = n - kSB < 0 ? 0 : n - kSB; h < n; ++h)
             wait_bar(bar + (kBFull + h % kSB) * 8, (uint32_t)(h / kSB) & 1u, p, nullptr, 1000 + h);
+    }
+}
+
+// The K parts of a split GEMM added in part order (deterministic), then the epilogue: one item
+// per output (token, row); consecutive threads take consecutive rows.
+__global__ void __launch_bounds__(256) gemm_merge_kernel(const __grid_constant__ Params p) {
+    pdl_wait();
+    pdl_trigger();
+    const bool silu = p.silu != 0;
+    const int orows = silu ? p.rows >> 1 : p.rows;
+    const long long n = (long long)p.T * orows;
+    const size_t pstride = (size_t)p.T * p.R;
+    for (long long i = blockIdx.x * 256ll + threadIdx.x; i < n; i += (long long)gridDim.x * 256) {
+        const int t = (int)(i / orows), j = (int)(i - (long long)t * orows);
+        // the stream's row of output j (SiLU*up: tile j / 8 holds the gate row, then the up row)
+        const int r = silu ? (j >> 3) * 16 + (j & 7) : j;
+        const float* q = p.part + (size_t)t * p.R + r;
+        float g = 0.f, u = 0.f;
+        for (int k = 0; k < p.kparts; ++k) {
+            g += __ldcg(q + k * pstride);
+            if (silu) u += __ldcg(q + k * pstride + 8);
+        }
+        const size_t o = (size_t)t * p.ld + j;
+        if (silu) static_cast<__half*>(p.y)[o] = __float2half_rn(persist::silu(g) * u);
+        else if (p.epi == QL_EPI_ADD_RESIDUAL) static_cast<float*>(p.y)[o] += g;
+        else static_cast<float*>(p.y)[o] = g;
     }
 }
 
@@ -421,12 +459,32 @@ int gemm_tc_launch(const GemmArgs& a, cudaStream_t s, bool pdl) {
     p.y = a.y;
     p.err = err;
     p.timeout_ns = 2000000000ull;
-    const dim3 grid((unsigned)((M.ntile + gemm::kRB - 1) / gemm::kRB), (unsigned)((a.T + nt - 1) / nt));
-    const cudaError_t e = nt == 256 ? ql::launch(gemm::gemm_tc_kernel<256>, grid, dim3(gemm::kThreads),
-                                                 gemm::Cfg<256>::kSmem, s, pdl, p)
-                                    : ql::launch(gemm::gemm_tc_kernel<128>, grid, dim3(gemm::kThreads),
-                                                 gemm::Cfg<128>::kSmem, s, pdl, p);
-    return e == cudaSuccess ? QL_OK : cuda_error(e, "gemm launch");
+    p.R = M.ntile * 16;
+    // K parts: enough CTAs for the SMs when the matrix has few row blocks, at least 4 units each,
+    // as many as the workspace holds
+    const int nrb = (M.ntile + gemm::kRB - 1) / gemm::kRB, ntok = (a.T + nt - 1) / nt;
+    int kparts = 1;
+    if (a.part != nullptr) {
+        kparts = num_sms() / (nrb * ntok);
+        if (kparts > p.nst / 4) kparts = p.nst / 4;
+        while (kparts > 1 && (size_t)kparts * a.T * p.R * sizeof(float) > a.part_bytes) --kparts;
+        if (kparts < 1) kparts = 1;
+    }
+    p.upp = (p.nst + kparts - 1) / kparts;
+    kparts = (p.nst + p.upp - 1) / p.upp;   // (no empty part)
+    p.kparts = kparts;
+    p.part = kparts > 1 ? a.part : nullptr;
+    const dim3 grid((unsigned)nrb, (unsigned)ntok, (unsigned)kparts);
+    cudaError_t e = nt == 256 ? ql::launch(gemm::gemm_tc_kernel<256>, grid, dim3(gemm::kThreads),
+                                           gemm::Cfg<256>::kSmem, s, pdl, p)
+                              : ql::launch(gemm::gemm_tc_kernel<128>, grid, dim3(gemm::kThreads),
+                                           gemm::Cfg<128>::kSmem, s, pdl, p);
+    if (e != cudaSuccess) return cuda_error(e, "gemm launch");
+    if (kparts > 1) {
+        e = ql::launch(gemm::gemm_merge_kernel, dim3(2 * num_sms()), dim3(256), 0, s, pdl, p);
+        if (e != cudaSuccess) return cuda_error(e, "gemm merge launch");
+    }
+    return QL_OK;
 }
 
 }  // namespace ql

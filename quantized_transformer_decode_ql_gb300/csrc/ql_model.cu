@@ -92,6 +92,8 @@ struct ql_model {
     int32_t* plen = nullptr;     // [max_batch]
     void* cws = nullptr;         // prefill chunk attention: the splits' partials
     size_t cws_bytes = 0;
+    void* gws = nullptr;         // prefill GEMM: the K parts' sums of matrices with few row blocks
+    size_t gws_bytes = 0;
 };
 
 namespace ql {
@@ -594,6 +596,8 @@ int run_prefill(ql_model* m, const int32_t* tokens, int T, int32_t* position, co
             g.y = y;
             g.ld = ld;
             g.epi = epi;
+            g.part = static_cast<float*>(m->gws);
+            g.part_bytes = m->gws_bytes;
             return gemm_tc_launch(g, s, pdl);
         }
         return batch <= kPersistMaxBatch ? stream_gemv_launch(ga, s, pdl) : batched_gemv_launch(ga, s, pdl);
@@ -784,6 +788,15 @@ int setup_persist(ql_model* m) {
         for (int k = 0; k < 4; ++k) hl[i].m[k] = all[4 * i + k];
     m->plm = all.back();
     m->hmats = all;
+    if (d.max_batch > kPrefillGemvMax) {   // the prompt GEMM's K parts (up to 4, the lm_head excluded)
+        const int64_t tmax = d.max_batch < kPrefillMax ? d.max_batch : kPrefillMax;
+        size_t rmax = 0;
+        for (size_t i = 0; i + 1 < all.size(); ++i)
+            if (!all[i].silu && (size_t)all[i].ntile * 16 > rmax) rmax = (size_t)all[i].ntile * 16;
+        m->gws_bytes = 4 * (size_t)tmax * rmax * sizeof(float);
+        A(&m->gws, m->gws_bytes);
+        if (rc != QL_OK) return rc;
+    }
     if (m->batched_ok) {
         for (const PMat& pm : all) {
             const size_t need = batched_gemv_workspace_bytes(pm.rows, pm.nblk, pm.silu);
