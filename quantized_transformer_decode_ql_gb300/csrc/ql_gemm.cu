@@ -52,8 +52,8 @@ using persist::as_u32;
 
 constexpr int kUnitBytes = persist::kUnitBytes;   // 16 rows x 128 columns: codes, then scales
 constexpr int kRB = 8;                             // tiles per row block: the MMA's M of 128 rows
-constexpr int kSW = 8;                             // code stages (one unit of the row block each)
-constexpr int kSB = 4;                             // activation stages (half a unit: 64 K)
+constexpr int kSW = 3;                             // code stages (one unit of the row block each)
+constexpr int kSB = 6;                             // activation stages (half a unit: 64 K)
 constexpr int kA = 4;                              // A slots of tensor memory, one unit (64 columns) each
 constexpr int kCodeBytes = kRB * kUnitBytes;       // 9216
 constexpr uint32_t kTmemCols = 512;
@@ -375,29 +375,46 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     }
 }
 
-// The K parts of a split GEMM added in part order (deterministic), then the epilogue: one item
-// per output (token, row); consecutive threads take consecutive rows.
+// The K parts of a split GEMM added in part order (deterministic), then the epilogue. Grid
+// (output rows / 1024, tokens): a thread takes 4 consecutive output rows of one token (4
+// consecutive rows of the stream, SiLU*up: of a tile's gate rows, the up rows 8 further), and
+// the loads of all its parts are in flight together.
+constexpr int kMaxParts = 4;
 __global__ void __launch_bounds__(256) gemm_merge_kernel(const __grid_constant__ Params p) {
     pdl_wait();
     pdl_trigger();
     const bool silu = p.silu != 0;
     const int orows = silu ? p.rows >> 1 : p.rows;
-    const long long n = (long long)p.T * orows;
-    const size_t pstride = (size_t)p.T * p.R;
-    for (long long i = blockIdx.x * 256ll + threadIdx.x; i < n; i += (long long)gridDim.x * 256) {
-        const int t = (int)(i / orows), j = (int)(i - (long long)t * orows);
-        // the stream's row of output j (SiLU*up: tile j / 8 holds the gate row, then the up row)
-        const int r = silu ? (j >> 3) * 16 + (j & 7) : j;
-        const float* q = p.part + (size_t)t * p.R + r;
-        float g = 0.f, u = 0.f;
-        for (int k = 0; k < p.kparts; ++k) {
-            g += __ldcg(q + k * pstride);
-            if (silu) u += __ldcg(q + k * pstride + 8);
+    const int t = blockIdx.y, j0 = (blockIdx.x * 256 + threadIdx.x) * 4;
+    if (j0 >= orows) return;
+    const int r0 = silu ? (j0 >> 3) * 16 + (j0 & 7) : j0;
+    const float* q = p.part + (size_t)t * p.R + r0;
+    const size_t ps = (size_t)p.T * p.R;
+    float4 g[kMaxParts], u[kMaxParts];
+#pragma unroll
+    for (int k = 0; k < kMaxParts; ++k) {
+        g[k] = u[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (k < p.kparts) {
+            g[k] = __ldcg(reinterpret_cast<const float4*>(q + k * ps));
+            if (silu) u[k] = __ldcg(reinterpret_cast<const float4*>(q + k * ps + 8));
         }
-        const size_t o = (size_t)t * p.ld + j;
-        if (silu) static_cast<__half*>(p.y)[o] = __float2half_rn(persist::silu(g) * u);
-        else if (p.epi == QL_EPI_ADD_RESIDUAL) static_cast<float*>(p.y)[o] += g;
-        else static_cast<float*>(p.y)[o] = g;
+    }
+    float4 sg = g[0], su = u[0];
+#pragma unroll
+    for (int k = 1; k < kMaxParts; ++k) {
+        if (k < p.kparts) {
+            sg.x += g[k].x; sg.y += g[k].y; sg.z += g[k].z; sg.w += g[k].w;
+            su.x += u[k].x; su.y += u[k].y; su.z += u[k].z; su.w += u[k].w;
+        }
+    }
+    const float gv[4] = {sg.x, sg.y, sg.z, sg.w}, uv[4] = {su.x, su.y, su.z, su.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if (j0 + i >= orows) break;
+        const size_t o = (size_t)t * p.ld + j0 + i;
+        if (silu) static_cast<__half*>(p.y)[o] = __float2half_rn(persist::silu(gv[i]) * uv[i]);
+        else if (p.epi == QL_EPI_ADD_RESIDUAL) static_cast<float*>(p.y)[o] += gv[i];
+        else static_cast<float*>(p.y)[o] = gv[i];
     }
 }
 
@@ -466,6 +483,7 @@ int gemm_tc_launch(const GemmArgs& a, cudaStream_t s, bool pdl) {
     int kparts = 1;
     if (a.part != nullptr) {
         kparts = num_sms() / (nrb * ntok);
+        if (kparts > gemm::kMaxParts) kparts = gemm::kMaxParts;
         if (kparts > p.nst / 4) kparts = p.nst / 4;
         while (kparts > 1 && (size_t)kparts * a.T * p.R * sizeof(float) > a.part_bytes) --kparts;
         if (kparts < 1) kparts = 1;
@@ -481,7 +499,9 @@ int gemm_tc_launch(const GemmArgs& a, cudaStream_t s, bool pdl) {
                                            gemm::Cfg<128>::kSmem, s, pdl, p);
     if (e != cudaSuccess) return cuda_error(e, "gemm launch");
     if (kparts > 1) {
-        e = ql::launch(gemm::gemm_merge_kernel, dim3(2 * num_sms()), dim3(256), 0, s, pdl, p);
+        const int orows = M.silu ? M.rows / 2 : M.rows;
+        e = ql::launch(gemm::gemm_merge_kernel, dim3((unsigned)((orows + 1023) / 1024), (unsigned)a.T), dim3(256), 0, s,
+                       pdl, p);
         if (e != cudaSuccess) return cuda_error(e, "gemm merge launch");
     }
     return QL_OK;
