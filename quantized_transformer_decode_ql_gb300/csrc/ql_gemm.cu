@@ -9,7 +9,8 @@
 // memory as the MMA's A operand.
 //
 // One CTA per (block of 128 weight rows = 8 tiles, tile of NT tokens: 256 when the chunk has
-// more than 128, else 128); K streams in units of 128 columns (one 1152-byte unit of each tile):
+// more than 128 tokens, 128 when it has more than 32, else 32); K streams in units of 128
+// columns (one 1152-byte unit of each tile):
 //  * warp 17, lane 0: per unit, one tensor-map copy of the row block's 8 tiles x 1 unit of codes
 //    and scales (tiles past the matrix read as zero) into a ring of kSW stages. The first kSW
 //    go out before the wait on the previous kernel (the weights do not depend on it);
@@ -326,7 +327,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             __half* yh = static_cast<__half*>(p.y);
             float* pf = split ? p.part + (size_t)kp * p.T * p.R + tile * 16 + rit : nullptr;
 #pragma unroll 1
-            for (int c = blk * (NT / 128); c < (blk + 1) * (NT / 128); ++c) {   // this warp's NT / 4 tokens
+            // 32-column loads of the accumulator: NT / 128 per warp (NT = 32: the first warp of a
+            // lane quarter takes the only one)
+            constexpr int kLoads = NT / 32, kPerWarp = kLoads >= 4 ? kLoads / 4 : 1;
+            for (int c = blk * kPerWarp; c < (blk + 1) * kPerWarp && c < kLoads; ++c) {
                 uint32_t v[32];
                 asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
                              "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
@@ -442,6 +446,7 @@ int gemm_prepare() {
     if (done.count(dev)) return QL_OK;
     int optin = 0;
     cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e == cudaSuccess) e = gemm_attr<32>(optin);
     if (e == cudaSuccess) e = gemm_attr<128>(optin);
     if (e == cudaSuccess) e = gemm_attr<256>(optin);
     if (e != cudaSuccess) return cuda_error(e, "gemm: kernel attributes");
@@ -465,7 +470,7 @@ int gemm_tc_launch(const GemmArgs& a, cudaStream_t s, bool pdl) {
     gemm::Params p = {};
     if (int rc = q4_stream_tensor_map(M, &p.tw)) return rc;
     const uint64_t K = (uint64_t)M.nblk * 32;
-    const int nt = a.T > 128 ? 256 : 128;   // tokens per CTA: every weight byte read once per nt tokens
+    const int nt = a.T > 128 ? 256 : a.T > 32 ? 128 : 32;   // tokens per CTA: the weights read once per nt tokens
     if (int rc = f16_rows_tensor_map(a.x16, K, (uint64_t)a.T, 64, (uint32_t)nt, &p.tx, true)) return rc;
     p.T = a.T;
     p.rows = M.rows;
@@ -493,10 +498,12 @@ int gemm_tc_launch(const GemmArgs& a, cudaStream_t s, bool pdl) {
     p.kparts = kparts;
     p.part = kparts > 1 ? a.part : nullptr;
     const dim3 grid((unsigned)nrb, (unsigned)ntok, (unsigned)kparts);
-    cudaError_t e = nt == 256 ? ql::launch(gemm::gemm_tc_kernel<256>, grid, dim3(gemm::kThreads),
-                                           gemm::Cfg<256>::kSmem, s, pdl, p)
-                              : ql::launch(gemm::gemm_tc_kernel<128>, grid, dim3(gemm::kThreads),
-                                           gemm::Cfg<128>::kSmem, s, pdl, p);
+    cudaError_t e = nt == 256  ? ql::launch(gemm::gemm_tc_kernel<256>, grid, dim3(gemm::kThreads),
+                                            gemm::Cfg<256>::kSmem, s, pdl, p)
+                    : nt == 128 ? ql::launch(gemm::gemm_tc_kernel<128>, grid, dim3(gemm::kThreads),
+                                             gemm::Cfg<128>::kSmem, s, pdl, p)
+                                : ql::launch(gemm::gemm_tc_kernel<32>, grid, dim3(gemm::kThreads),
+                                             gemm::Cfg<32>::kSmem, s, pdl, p);
     if (e != cudaSuccess) return cuda_error(e, "gemm launch");
     if (kparts > 1) {
         const int orows = M.silu ? M.rows / 2 : M.rows;
