@@ -230,6 +230,37 @@ def gemv_kinds(gm, cfg, B, s, g):
     return out
 
 
+def gemm_gate_up_alone(gm, s, g, T=256):
+    """The prompt GEMM (tcgen05) on the 8B gate|up matrices for a T-token chunk, SiLU*up epilogue
+    as in prefill, over 8 layers' matrices in turn (> 3x L2); CUDA-event time per launch over 3
+    graph replays; TFLOP/s against the measured dense bf16 peak (the tensor roofline)."""
+    import torch
+    import quantized_transformer_decode_ql_gb300 as ql
+    mats = [L["wgu"] for L in gm.layers][:8]
+    W = mats[0]
+    bufs = []
+    for Wl in mats:
+        buf = torch.empty(ql.ql_q4_0_stream_bytes(Wl.rows, Wl.cols, 1), dtype=torch.uint8, device="cuda")
+        ql.ql_q4_0_stream_pack(Wl.scales, Wl.quants, Wl.rows, Wl.cols, 1, buf, s)
+        bufs.append(buf)
+    x = torch.randn((T, W.cols), generator=g, device="cuda").half()
+    y = torch.empty((T, W.rows // 2), dtype=torch.float16, device="cuda")
+    s.synchronize()
+
+    def run():
+        for buf in bufs:
+            ql.ql_gemm_q4_0_stream(buf, W.rows, W.cols, x, T, y, ql.QL_EPI_SILU_MUL, s)
+    us = graph_ms(run, s, 3) * 1e3 / len(bufs)
+    flops = 2.0 * T * W.rows * W.cols
+    tf = flops / (us * 1e-6) / 1e12
+    peak = load_peaks_tflops()
+    del bufs
+    return {"rows": W.rows, "cols": W.cols, "tokens": T, "epilogue": "silu", "us_per_launch": round(us, 3),
+            "bound": "tensor", "flops_per_launch": flops, "achieved_tflops": round(tf, 1),
+            "peak_tflops": peak, "peak_source": "measured bf16 burst (the f16 kind's rate)",
+            "frac": round(tf / peak, 4) if peak else None, "matrices_rotated": len(mats)}
+
+
 def attn_alone(B, lo, hi, s, g, seed=6, iters=10, kvq=False):
     """Paged GQA decode attention alone at the attention workload's shape (32/8 heads, head_dim
     128, 16-token blocks, randomly permuted block tables): B sequences with lengths uniform in
@@ -444,6 +475,8 @@ def gpu_arm(args, rank, world, local_rank):
     for k in kernels.values():
         for v in (k.values() if "qkv" in k else [k]):
             v["frac"] = round(v["achieved_gbs"] / peak, 4)
+    if not args.layers and streamed:
+        kernels["gemm_prefill_gate_up_t256"] = gemm_gate_up_alone(gm, s, g)
 
     tok_total = sum_over_ranks(float(B * steps), world)
     value = tok_total / (ms_max / 1e3)
