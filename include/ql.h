@@ -139,11 +139,13 @@ int ql_gemv_q4_0_stream(const void* d_stream, int64_t rows, int64_t cols, const 
  * epilogue(W x_t) for n_tokens tokens at once, from the tile stream copy (d_stream, as for
  * ql_gemv_q4_0_stream). d_x: f16 [n_tokens][cols], 16-byte aligned; epilogue and d_y as for
  * ql_gemv_q4_0_stream with n_tokens in place of batch. On the tcgen05 tensor cores: one CTA per
- * 128 rows x 128 tokens, the weights expanded into tensor memory as (q - 8) d rounded once to
- * f16, f16 activations, f32 products and sums (each output one accumulator, K in order: the
- * result does not depend on the launch). Every weight byte is read once per 128 tokens. No
- * workspace; waits are bounded (2 s, then the device error record says so). cols % 128 == 0
- * (even rows with SiLU*up), 1 <= n_tokens <= 2^20. Asynchronous on stream.                */
+ * 128 rows x NT tokens (NT = 256 above 128 tokens, 128 above 32, else 32), the weights expanded
+ * into tensor memory as (q - 8) d rounded once to f16, f16 activations, f32 products and sums
+ * (each output one tensor-core accumulator over K: the result does not depend on the call).
+ * Every weight byte is read once per NT tokens. No workspace (no split over K, which the
+ * chunked prefill uses with a workspace of its own); waits are bounded (2 s, then the device
+ * error record says so). cols % 128 == 0 (even rows with SiLU*up), 1 <= n_tokens <= 2^20.
+ * Asynchronous on stream.                                                                  */
 int ql_gemm_q4_0_stream(const void* d_stream, int64_t rows, int64_t cols, const void* d_x, int64_t n_tokens,
                         void* d_y, int epilogue, void* stream);
 /* Activation form of the batch 1-2 GEMV, for this process (ql_gemv_q4_0_stream and the decode
