@@ -242,7 +242,8 @@ __global__ void __launch_bounds__(kCT) chunk_attn_kernel(CParams p, DevError* er
 // out[row] = sum_s acc_s 2^(m_s - M) / sum_s l_s 2^(m_s - M), M = max_s m_s, over the active
 // splits in order; one warp per (token, head) row. Lane s reads split s's max and sum (one round
 // of loads for up to 32 splits), the warp reduces them; then lane = 4 output dims, the splits'
-// accumulators loaded 4 at a time and added in split order.
+// accumulators loaded 8 at a time (the first 8 together with the max and sum) and added in split
+// order.
 template <int HD>
 __global__ void __launch_bounds__(256) chunk_merge_kernel(CParams p) {
     pdl_wait();
@@ -253,10 +254,20 @@ __global__ void __launch_bounds__(256) chunk_merge_kernel(CParams p) {
     const int NR = p.T * p.n_heads;
     const int lane = threadIdx.x & 31;
     for (int row = blockIdx.x * 8 + (threadIdx.x >> 5); row < NR; row += gridDim.x * 8) {
+        // the first 32 splits' (m, l) are loaded once (a chunk rarely has more splits), together
+        // with the first round of partial sums, which do not depend on the maximum
+        constexpr int kRound = 8;   // partial sums whose loads are in flight together
+        const float m0 = lane < n_active ? __ldcg(p.pm + (size_t)lane * NR + row) : -INFINITY;
+        const float l0 = lane < n_active ? __ldcg(p.pl + (size_t)lane * NR + row) : 0.f;
+        float4 a[kRound];
+#pragma unroll
+        for (int u = 0; u < kRound; ++u)
+            if (u < n_active && lane < HD / 4)
+                a[u] = __ldcg(reinterpret_cast<const float4*>(p.pacc + ((size_t)u * NR + row) * HD) + lane);
         float M = -INFINITY;
         for (int s0 = 0; s0 < n_active; s0 += 32) {   // max over the splits
             const int s = s0 + lane;
-            const float ms = s < n_active ? __ldcg(p.pm + (size_t)s * NR + row) : -INFINITY;
+            const float ms = s0 == 0 ? m0 : s < n_active ? __ldcg(p.pm + (size_t)s * NR + row) : -INFINITY;
             float m = ms;
 #pragma unroll
             for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -268,23 +279,23 @@ __global__ void __launch_bounds__(256) chunk_merge_kernel(CParams p) {
             const int ns = n_active - s0 < 32 ? n_active - s0 : 32;
             // lane s: split s0 + s's weight 2^(m - M) and weighted sum
             const int sl = s0 + lane;
-            const float ms = lane < ns ? __ldcg(p.pm + (size_t)sl * NR + row) : -INFINITY;
-            const float ls = lane < ns ? __ldcg(p.pl + (size_t)sl * NR + row) : 0.f;
+            const float ms = s0 == 0 ? m0 : lane < ns ? __ldcg(p.pm + (size_t)sl * NR + row) : -INFINITY;
+            const float ls = s0 == 0 ? l0 : lane < ns ? __ldcg(p.pl + (size_t)sl * NR + row) : 0.f;
             const float f = ms == -INFINITY ? 0.f : exp2f(ms - M);
             // the splits' sums in split order (lane 0 adds them after a gather)
             float lw = ls * f;
             for (int k = 0; k < ns; ++k) Ls += __shfl_sync(0xffffffffu, lw, k);
-            for (int k0 = 0; k0 < ns; k0 += 4) {
-                float4 a[4];
-                float fk[4];
+            for (int k0 = 0; k0 < ns; k0 += kRound) {
+                float fk[kRound];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
+                for (int u = 0; u < kRound; ++u) {
                     fk[u] = __shfl_sync(0xffffffffu, f, (k0 + u) & 31);
-                    if (k0 + u < ns && lane < HD / 4)
+                    // the first round's loads went out with the (m, l) above
+                    if ((s0 > 0 || k0 > 0) && k0 + u < ns && lane < HD / 4)
                         a[u] = __ldcg(reinterpret_cast<const float4*>(p.pacc + ((size_t)(s0 + k0 + u) * NR + row) * HD) + lane);
                 }
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
+                for (int u = 0; u < kRound; ++u) {
                     if (k0 + u < ns && lane < HD / 4) {
                         A.x = fmaf(a[u].x, fk[u], A.x);
                         A.y = fmaf(a[u].y, fk[u], A.y);
