@@ -14,10 +14,10 @@
 //  * warp 17, lane 0: per unit, one tensor-map copy of the row block's 8 tiles x 1 unit of codes
 //    and scales (tiles past the matrix read as zero) into a ring of kSW stages. The first kSW
 //    go out before the wait on the previous kernel (the weights do not depend on it);
-//  * warp 18, lane 0: per half unit, one tensor-map copy of the tokens' activations (64 f16 of
-//    K x NT tokens: each token's 128 bytes one row, with the 128-byte swizzle, i.e. the K-major
+//  * warp 18, lane 0: per unit, two tensor-map copies of the tokens' activations (64 f16 of K x
+//    NT tokens each: each token's 128 bytes one row, with the 128-byte swizzle, i.e. the K-major
 //    layout the MMA reads with a SWIZZLE_128B descriptor; tokens past the chunk read as zero)
-//    into a ring of kSB stages;
+//    into a ring of kSB stages (kSW and kSB by NT, as many as the shared memory holds);
 //  * warps 0-15 (warp w serves tensor-memory lanes 32 (w % 4).., i.e. rows 32 (w % 4).. of the
 //    block, and the unit's block w / 4): each thread expands its row's 32 codes of that block
 //    into (q - 8) d in f16, in K order (two consecutive K per 32-bit column), frees the code
@@ -25,8 +25,7 @@
 //    these warps run the epilogue;
 //  * warp 16 allocates the tensor memory; its lane 0 issues tcgen05.mma (kind::f16, M 128,
 //    N NT, K 16, A in tensor memory, B in shared memory) into one f32 accumulator of NT columns
-//    and commits each half unit's MMAs to the barrier that frees its activation stage, and each
-//    unit's to the one that frees its A slot;
+//    and commits each unit's MMAs to the barriers that free its activation stage and A slot;
 //  * epilogue: tcgen05.ld of the accumulator (warp w: its lanes' rows, tokens NT / 4 (w / 4)..),
 //    then the stores: f32, added to the residual, or SiLU(gate) * up in f16 (the gate row's
 //    thread takes the up row from the lane 8 above).
@@ -53,19 +52,21 @@ using persist::as_u32;
 
 constexpr int kUnitBytes = persist::kUnitBytes;   // 16 rows x 128 columns: codes, then scales
 constexpr int kRB = 8;                             // tiles per row block: the MMA's M of 128 rows
-constexpr int kSW = 3;                             // code stages (one unit of the row block each)
-constexpr int kSB = 6;                             // activation stages (half a unit: 64 K)
 constexpr int kA = 4;                              // A slots of tensor memory, one unit (64 columns) each
 constexpr int kCodeBytes = kRB * kUnitBytes;       // 9216
 constexpr uint32_t kTmemCols = 512;
 constexpr int kDW = 16;                            // dequantisation (and epilogue) warps
 constexpr int kMmaWarp = kDW, kWProdWarp = kDW + 1, kBProdWarp = kDW + 2, kThreads = (kDW + 3) * 32;
-enum { kWFull = 0, kWEmpty = kSW, kBFull = 2 * kSW, kBEmpty = 2 * kSW + kSB, kAFull = 2 * kSW + 2 * kSB,
-       kAFree = kAFull + kA, kDFull = kAFree + kA, kDone = kDFull + 1, kBars = kDone + 1 };
 
 template <int NT>
 struct Cfg {
-    static constexpr int kBStage = NT * 128;               // half a unit (64 K) for NT tokens
+    static constexpr int kSW = NT == 32 ? 4 : 3;                    // code stages (one unit each)
+    static constexpr int kSB = NT == 256 ? 3 : NT == 128 ? 6 : 16;  // activation stages (one unit each)
+    static constexpr int kWFull = 0, kWEmpty = kSW, kBFull = 2 * kSW, kBEmpty = 2 * kSW + kSB,
+                         kAFull = 2 * kSW + 2 * kSB, kAFree = kAFull + kA, kDFull = kAFree + kA, kDone = kDFull + 1,
+                         kBars = kDone + 1;
+    static constexpr int kBHalf = NT * 128;                // 64 K for NT tokens: one 128-byte-swizzled box
+    static constexpr int kBStage = 2 * kBHalf;             // a unit (128 K) for NT tokens
     static constexpr size_t kSmem = (size_t)kSW * kCodeBytes + (size_t)kSB * kBStage;
     static constexpr uint32_t kACol = NT;                  // the A slots after the accumulator's columns
     // instruction descriptor: D f32, A and B f16, both K-major, N = NT, M = 128
@@ -135,6 +136,9 @@ __device__ __forceinline__ uint32_t deq2(uint32_t w, __half2 d2) {
 template <int NT>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ Params p) {
     using C = Cfg<NT>;
+    constexpr int kSW = C::kSW, kSB = C::kSB;
+    constexpr int kWFull = C::kWFull, kWEmpty = C::kWEmpty, kBFull = C::kBFull, kBEmpty = C::kBEmpty,
+                  kAFull = C::kAFull, kAFree = C::kAFree, kDFull = C::kDFull, kDone = C::kDone, kBars = C::kBars;
     extern __shared__ __align__(1024) unsigned char smem[];
     __shared__ __align__(8) unsigned long long bars[kBars];
     __shared__ uint32_t tmem_base;
@@ -214,18 +218,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     } else if (warp == kBProdWarp) {
         // ------------------------------------------------ activation copies (one lane)
         if (lane == 0) {
-            const int nh = 2 * nst;
-            int h = 0;
-            for (; h < nh; ++h) {
-                const int s = h % kSB;
-                if (h >= kSB && !wait_bar(bar + (kBEmpty + s) * 8, (uint32_t)(h / kSB - 1) & 1u, p, abt, 200 + h)) break;
+            int u = 0;
+            for (; u < nst; ++u) {
+                const int s = u % kSB;
+                if (u >= kSB && !wait_bar(bar + (kBEmpty + s) * 8, (uint32_t)(u / kSB - 1) & 1u, p, abt, 200 + u)) break;
                 expect_tx(bar + (kBFull + s) * 8, (uint32_t)C::kBStage);
-                asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-                             " [%0], [%1, {%2, %3}], [%4];"
-                             ::"r"(su32(bsm + (size_t)s * C::kBStage)), "l"(reinterpret_cast<uint64_t>(&p.tx)),
-                               "r"(64 * (2 * u0 + h)), "r"(n0), "r"(bar + (kBFull + s) * 8) : "memory");
+                for (int hh = 0; hh < 2; ++hh)   // the unit's two 64-K halves
+                    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                                 " [%0], [%1, {%2, %3}], [%4];"
+                                 ::"r"(su32(bsm + (size_t)s * C::kBStage + (size_t)hh * C::kBHalf)),
+                                   "l"(reinterpret_cast<uint64_t>(&p.tx)), "r"(128 * (u0 + u) + 64 * hh), "r"(n0),
+                                   "r"(bar + (kBFull + s) * 8) : "memory");
             }
-            issued_b = h;
+            issued_b = u;
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
@@ -234,33 +239,27 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             const uint32_t b0 = su32(bsm);
             for (int u = 0; u < nst; ++u) {
                 const int a = u % kA;
+                const int s = u % kSB;
+                // one wait for the A slot, one for the unit's activations, one fence, 8 MMAs: a
+                // tcgen05 wait and fence cost the issuing lane as much as several MMAs
                 if (!wait_bar(bar + (kAFull + a) * 8, (uint32_t)(u / kA) & 1u, p, abt, 300 + u)) break;
+                if (!wait_bar(bar + (kBFull + s) * 8, (uint32_t)(u / kSB) & 1u, p, abt, 400 + u)) break;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                bool ok = true;
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int h = 2 * u + hh, s = h % kSB;
-                    if (!wait_bar(bar + (kBFull + s) * 8, (uint32_t)(h / kSB) & 1u, p, abt, 400 + h)) {
-                        ok = false;
-                        break;
-                    }
-                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                    // B: K-major with the 128-byte swizzle: a token's 64 K in one 128-byte row,
-                    // 1024 bytes between 8-token groups; step ks starts 32 bytes (16 K) in
+                // B: K-major with the 128-byte swizzle: a token's 64 K in one 128-byte row, 1024
+                // bytes between 8-token groups; step ks starts 32 bytes (16 K) into its half
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {
-                        const uint32_t baddr = b0 + (uint32_t)(s * C::kBStage + ks * 32);
-                        const unsigned long long bdesc = (unsigned long long)((baddr & 0x3FFFFu) >> 4) |
-                                                         (1ull << 16) | ((unsigned long long)(1024u >> 4) << 32) |
-                                                         (1ull << 46) | (2ull << 61);
-                        const uint32_t acc = (u > 0 || hh > 0 || ks > 0) ? 1u : 0u;   // the first MMA overwrites
-                        asm volatile("{\n .reg .pred pa;\n setp.ne.u32 pa, %4, 0;\n"
-                                     " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pa;\n}"
-                                     ::"r"(tb), "r"(tb + C::kACol + 64u * (uint32_t)a + 32u * (uint32_t)hh + 8u * (uint32_t)ks),
-                                       "l"(bdesc), "r"(C::kIdesc), "r"(acc) : "memory");
-                    }
-                    commit(bar + (kBEmpty + s) * 8);
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t baddr = b0 + (uint32_t)(s * C::kBStage + (ks >> 2) * C::kBHalf + (ks & 3) * 32);
+                    const unsigned long long bdesc = (unsigned long long)((baddr & 0x3FFFFu) >> 4) |
+                                                     (1ull << 16) | ((unsigned long long)(1024u >> 4) << 32) |
+                                                     (1ull << 46) | (2ull << 61);
+                    const uint32_t acc = (u > 0 || ks > 0) ? 1u : 0u;   // the first MMA overwrites
+                    asm volatile("{\n .reg .pred pa;\n setp.ne.u32 pa, %4, 0;\n"
+                                 " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pa;\n}"
+                                 ::"r"(tb), "r"(tb + C::kACol + 64u * (uint32_t)a + 8u * (uint32_t)ks),
+                                   "l"(bdesc), "r"(C::kIdesc), "r"(acc) : "memory");
                 }
-                if (!ok) break;
+                commit(bar + (kBEmpty + s) * 8);
                 commit(bar + (kAFree + a) * 8);
                 if (u == nst - 1) commit(bar + kDFull * 8);
             }
@@ -374,8 +373,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     }
     if (warp == kBProdWarp && lane == 0) {
         const int n = issued_b;
-        for (int h = n - kSB < 0 ? 0 : n - kSB; h < n; ++h)
-            wait_bar(bar + (kBFull + h % kSB) * 8, (uint32_t)(h / kSB) & 1u, p, nullptr, 1000 + h);
+        for (int u = n - kSB < 0 ? 0 : n - kSB; u < n; ++u)
+            wait_bar(bar + (kBFull + u % kSB) * 8, (uint32_t)(u / kSB) & 1u, p, nullptr, 1000 + u);
     }
 }
 
