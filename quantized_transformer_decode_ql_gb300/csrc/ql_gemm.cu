@@ -52,7 +52,6 @@ using persist::as_u32;
 
 constexpr int kUnitBytes = persist::kUnitBytes;   // 16 rows x 128 columns: codes, then scales
 constexpr int kRB = 8;                             // tiles per row block: the MMA's M of 128 rows
-constexpr int kA = 4;                              // A slots of tensor memory, one unit (64 columns) each
 constexpr int kCodeBytes = kRB * kUnitBytes;       // 9216
 constexpr uint32_t kTmemCols = 512;
 constexpr int kDW = 16;                            // dequantisation (and epilogue) warps
@@ -61,10 +60,13 @@ constexpr int kMmaWarp = kDW, kWProdWarp = kDW + 1, kBProdWarp = kDW + 2, kThrea
 template <int NT>
 struct Cfg {
     static constexpr int kSW = NT == 32 ? 4 : 3;                    // code stages (one unit each)
-    static constexpr int kSB = NT == 256 ? 3 : NT == 128 ? 6 : 16;  // activation stages (one unit each)
-    static constexpr int kWFull = 0, kWEmpty = kSW, kBFull = 2 * kSW, kBEmpty = 2 * kSW + kSB,
-                         kAFull = 2 * kSW + 2 * kSB, kAFree = kAFull + kA, kDFull = kAFree + kA, kDone = kDFull + 1,
-                         kBars = kDone + 1;
+    // units in flight between the dequantisation and the MMAs: unit u's activations (stage
+    // u % kSB) and its expanded weights (A slot u % kSB of tensor memory, 64 columns) are freed
+    // together by one commit, so the stages and the slots are one ring
+    static constexpr int kSB = NT == 256 ? 3 : NT == 128 ? 6 : 7;
+    static constexpr int kA = kSB;
+    static constexpr int kWFull = 0, kWEmpty = kSW, kBFull = 2 * kSW, kAFull = 2 * kSW + kSB,
+                         kFree = 2 * kSW + 2 * kSB, kDFull = kFree + kSB, kDone = kDFull + 1, kBars = kDone + 1;
     static constexpr int kBHalf = NT * 128;                // 64 K for NT tokens: one 128-byte-swizzled box
     static constexpr int kBStage = 2 * kBHalf;             // a unit (128 K) for NT tokens
     static constexpr size_t kSmem = (size_t)kSW * kCodeBytes + (size_t)kSB * kBStage;
@@ -136,9 +138,9 @@ __device__ __forceinline__ uint32_t deq2(uint32_t w, __half2 d2) {
 template <int NT>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ Params p) {
     using C = Cfg<NT>;
-    constexpr int kSW = C::kSW, kSB = C::kSB;
-    constexpr int kWFull = C::kWFull, kWEmpty = C::kWEmpty, kBFull = C::kBFull, kBEmpty = C::kBEmpty,
-                  kAFull = C::kAFull, kAFree = C::kAFree, kDFull = C::kDFull, kDone = C::kDone, kBars = C::kBars;
+    constexpr int kSW = C::kSW, kSB = C::kSB, kA = C::kA;
+    constexpr int kWFull = C::kWFull, kWEmpty = C::kWEmpty, kBFull = C::kBFull, kAFull = C::kAFull,
+                  kFree = C::kFree, kDFull = C::kDFull, kDone = C::kDone, kBars = C::kBars;
     extern __shared__ __align__(1024) unsigned char smem[];
     __shared__ __align__(8) unsigned long long bars[kBars];
     __shared__ uint32_t tmem_base;
@@ -157,11 +159,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         }
         for (int s = 0; s < kSB; ++s) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar + (kBFull + s) * 8) : "memory");
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar + (kBEmpty + s) * 8) : "memory");
-        }
-        for (int a = 0; a < kA; ++a) {
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar + (kAFull + a) * 8), "r"(kDW) : "memory");
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar + (kAFree + a) * 8) : "memory");
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar + (kAFull + s) * 8), "r"(kDW) : "memory");
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar + (kFree + s) * 8) : "memory");
         }
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar + kDFull * 8) : "memory");
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar + kDone * 8) : "memory");
@@ -221,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             int u = 0;
             for (; u < nst; ++u) {
                 const int s = u % kSB;
-                if (u >= kSB && !wait_bar(bar + (kBEmpty + s) * 8, (uint32_t)(u / kSB - 1) & 1u, p, abt, 200 + u)) break;
+                if (u >= kSB && !wait_bar(bar + (kFree + s) * 8, (uint32_t)(u / kSB - 1) & 1u, p, abt, 200 + u)) break;
                 expect_tx(bar + (kBFull + s) * 8, (uint32_t)C::kBStage);
                 for (int hh = 0; hh < 2; ++hh)   // the unit's two 64-K halves
                     asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
@@ -259,8 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                                  ::"r"(tb), "r"(tb + C::kACol + 64u * (uint32_t)a + 8u * (uint32_t)ks),
                                    "l"(bdesc), "r"(C::kIdesc), "r"(acc) : "memory");
                 }
-                commit(bar + (kBEmpty + s) * 8);
-                commit(bar + (kAFree + a) * 8);
+                commit(bar + (kFree + s) * 8);   // the stage and the A slot (a == s)
                 if (u == nst - 1) commit(bar + kDFull * 8);
             }
             // every MMA issued has completed before the tensor memory is released
@@ -277,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         bool ok = true;
         for (int u = 0; u < nst && ok; ++u) {
             const int s = u % kSW, a = u % kA;
-            if (u >= kA && !warp_wait(bar + (kAFree + a) * 8, (uint32_t)(u / kA - 1) & 1u, p, abt, 600 + u)) {
+            if (u >= kA && !warp_wait(bar + (kFree + a) * 8, (uint32_t)(u / kA - 1) & 1u, p, abt, 600 + u)) {
                 ok = false;
                 break;
             }
