@@ -65,8 +65,10 @@ struct Cfg {
     // together by one commit, so the stages and the slots are one ring
     static constexpr int kSB = NT == 256 ? 3 : NT == 128 ? 6 : 7;
     static constexpr int kA = kSB;
-    static constexpr int kWFull = 0, kWEmpty = kSW, kBFull = 2 * kSW, kAFull = 2 * kSW + kSB,
-                         kFree = 2 * kSW + 2 * kSB, kDFull = kFree + kSB, kDone = kDFull + 1, kBars = kDone + 1;
+    // kReady[s]: unit u's activations landed (the copies' bytes and the producer's arrival) and
+    // its A slot stored (one arrival per dequantisation warp): the MMA lane's one wait per unit
+    static constexpr int kWFull = 0, kWEmpty = kSW, kReady = 2 * kSW, kFree = 2 * kSW + kSB,
+                         kDFull = kFree + kSB, kDone = kDFull + 1, kBars = kDone + 1;
     static constexpr int kBHalf = NT * 128;                // 64 K for NT tokens: one 128-byte-swizzled box
     static constexpr int kBStage = 2 * kBHalf;             // a unit (128 K) for NT tokens
     static constexpr size_t kSmem = (size_t)kSW * kCodeBytes + (size_t)kSB * kBStage;
@@ -139,8 +141,8 @@ template <int NT>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ Params p) {
     using C = Cfg<NT>;
     constexpr int kSW = C::kSW, kSB = C::kSB, kA = C::kA;
-    constexpr int kWFull = C::kWFull, kWEmpty = C::kWEmpty, kBFull = C::kBFull, kAFull = C::kAFull,
-                  kFree = C::kFree, kDFull = C::kDFull, kDone = C::kDone, kBars = C::kBars;
+    constexpr int kWFull = C::kWFull, kWEmpty = C::kWEmpty, kReady = C::kReady, kFree = C::kFree,
+                  kDFull = C::kDFull, kDone = C::kDone, kBars = C::kBars;
     extern __shared__ __align__(1024) unsigned char smem[];
     __shared__ __align__(8) unsigned long long bars[kBars];
     __shared__ uint32_t tmem_base;
@@ -158,8 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar + (kWEmpty + s) * 8), "r"(kDW) : "memory");
         }
         for (int s = 0; s < kSB; ++s) {
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar + (kBFull + s) * 8) : "memory");
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar + (kAFull + s) * 8), "r"(kDW) : "memory");
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar + (kReady + s) * 8), "r"(kDW + 1) : "memory");
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar + (kFree + s) * 8) : "memory");
         }
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar + kDFull * 8) : "memory");
@@ -221,13 +222,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             for (; u < nst; ++u) {
                 const int s = u % kSB;
                 if (u >= kSB && !wait_bar(bar + (kFree + s) * 8, (uint32_t)(u / kSB - 1) & 1u, p, abt, 200 + u)) break;
-                expect_tx(bar + (kBFull + s) * 8, (uint32_t)C::kBStage);
+                expect_tx(bar + (kReady + s) * 8, (uint32_t)C::kBStage);
                 for (int hh = 0; hh < 2; ++hh)   // the unit's two 64-K halves
                     asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
                                  " [%0], [%1, {%2, %3}], [%4];"
                                  ::"r"(su32(bsm + (size_t)s * C::kBStage + (size_t)hh * C::kBHalf)),
                                    "l"(reinterpret_cast<uint64_t>(&p.tx)), "r"(128 * (u0 + u) + 64 * hh), "r"(n0),
-                                   "r"(bar + (kBFull + s) * 8) : "memory");
+                                   "r"(bar + (kReady + s) * 8) : "memory");
             }
             issued_b = u;
         }
@@ -239,10 +240,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             for (int u = 0; u < nst; ++u) {
                 const int a = u % kA;
                 const int s = u % kSB;
-                // one wait for the A slot, one for the unit's activations, one fence, 8 MMAs: a
-                // tcgen05 wait and fence cost the issuing lane as much as several MMAs
-                if (!wait_bar(bar + (kAFull + a) * 8, (uint32_t)(u / kA) & 1u, p, abt, 300 + u)) break;
-                if (!wait_bar(bar + (kBFull + s) * 8, (uint32_t)(u / kSB) & 1u, p, abt, 400 + u)) break;
+                // one wait (the A slot and the activations), one fence, 8 MMAs, one commit: a
+                // tcgen05 wait, fence or commit costs the issuing lane as much as several MMAs
+                if (!wait_bar(bar + (kReady + s) * 8, (uint32_t)(u / kSB) & 1u, p, abt, 300 + u)) break;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 // B: K-major with the 128-byte swizzle: a token's 64 K in one 128-byte row, 1024
                 // bytes between 8-token groups; step ks starts 32 bytes (16 K) into its half
@@ -312,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             __syncwarp();
-            if (lane == 0) arrive(bar + (kAFull + a) * 8);
+            if (lane == 0) arrive(bar + (kReady + a) * 8);
         }
         if (ok && warp_wait(bar + kDFull * 8, 0u, p, abt, 800)) {
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -323,10 +323,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             float* yf = static_cast<float*>(p.y);
             __half* yh = static_cast<__half*>(p.y);
             float* pf = split ? p.part + (size_t)kp * p.T * p.R + tile * 16 + rit : nullptr;
-#pragma unroll 1
             // 32-column loads of the accumulator: NT / 128 per warp (NT = 32: the first warp of a
             // lane quarter takes the only one)
             constexpr int kLoads = NT / 32, kPerWarp = kLoads >= 4 ? kLoads / 4 : 1;
+#pragma unroll 1
             for (int c = blk * kPerWarp; c < (blk + 1) * kPerWarp && c < kLoads; ++c) {
                 uint32_t v[32];
                 asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
@@ -372,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     if (warp == kBProdWarp && lane == 0) {
         const int n = issued_b;
         for (int u = n - kSB < 0 ? 0 : n - kSB; u < n; ++u)
-            wait_bar(bar + (kBFull + u % kSB) * 8, (uint32_t)(u / kSB) & 1u, p, nullptr, 1000 + u);
+            wait_bar(bar + (kReady + u % kSB) * 8, (uint32_t)(u / kSB) & 1u, p, nullptr, 1000 + u);
     }
 }
 
