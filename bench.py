@@ -830,12 +830,15 @@ def gemv_passes(cols, batch):
 def launches_per_step(cfg, B):
     """Kernel launches of one step in the one-launch-per-phase form. Batch 1-2: embed, per layer
     qkv / attention / o / gate_up / down GEMVs over the tile stream layout, lm_head, finalize.
-    Batch 3-32: each GEMV is the split-K kernel plus its merge kernel, and the two RMSNorm'd
-    GEMVs of a layer (and lm_head) get a statistics kernel first. Above 32: row-major passes."""
+    Batch 3-32 (the mma.sync form): each GEMV is the split-K kernel plus its merge kernel; the
+    RMSNorm is folded into the merges, so only layer 0's q|k|v GEMV gets an RMSNorm kernel first
+    (every RMSNorm'd GEMV does with QL_BATCHED_NORM_FOLD=0). Above 32: row-major passes."""
     if B <= 2:
         return 3 + 5 * cfg.n_layers
     if B <= 32:
-        return 5 + 11 * cfg.n_layers
+        if os.environ.get("QL_BATCHED_NORM_FOLD", "1").strip() == "0":
+            return 5 + 11 * cfg.n_layers   # an RMSNorm before q|k|v and gate|up, and before lm_head
+        return 5 + 9 * cfg.n_layers
     per_layer = (gemv_passes(cfg.hidden, B) * 2 + gemv_passes(cfg.n_heads * cfg.head_dim, B)
                  + gemv_passes(cfg.intermediate, B) + 1)
     return 2 + per_layer * cfg.n_layers + gemv_passes(cfg.hidden, B)

@@ -25,13 +25,20 @@ def test_trace_stamps_keep_nanoseconds():
     assert (out[..., 6] == 11).all()                  # other words untouched
 
 
-def test_launches_per_step():
+def test_launches_per_step(monkeypatch):
+    monkeypatch.delenv("QL_BATCHED_NORM_FOLD", raising=False)
     cfg = ql_inputs.QWEN3_8B
     L = cfg.n_layers
     # batch 1-2: embed, per layer q|k|v, attention, o, gate|up, down, then lm_head, finalize
     assert bench.launches_per_step(cfg, 1) == 3 + 5 * L
     assert bench.launches_per_step(cfg, 2) == 3 + 5 * L
-    # batch 3-32: every GEMV plus its merge, an RMSNorm before q|k|v, gate|up and lm_head
-    assert bench.launches_per_step(cfg, 32) == 5 + 11 * L
+    # batch 3-32: every GEMV plus its merge and the attention (9 per layer); embed, layer 0's
+    # RMSNorm, lm_head and its merge, finalize. The ncu launch list of the batch-32 step has,
+    # per 36-layer step, 144 + 1 GEMVs, as many merges, 36 attentions and 1 RMSNorm.
+    assert bench.launches_per_step(cfg, 32) == 5 + 9 * L
+    assert 5 + 9 * 36 == 1 + 1 + 36 * (4 + 4 + 1) + 2 + 1
     small = dataclasses.replace(cfg, n_layers=2)
     assert bench.launches_per_step(small, 1) == 13
+    # with the fold switched off every RMSNorm'd GEMV (q|k|v, gate|up, lm_head) gets its kernel
+    monkeypatch.setenv("QL_BATCHED_NORM_FOLD", "0")
+    assert bench.launches_per_step(cfg, 32) == 5 + 11 * L
